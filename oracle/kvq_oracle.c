@@ -1,0 +1,295 @@
+/*
+ * kvq_oracle.c -- plain, slow CPU oracle for the paged quantized KV-cache
+ * write/read path.  TEST INFRASTRUCTURE ONLY: the library under
+ * paged_quantized_kv_gb300/ never links, loads or calls this file; only the
+ * tests, the smoke check and the benchmark's CPU-baseline leg do.
+ *
+ * It restates, step by step and without blocking, fusion or reordering, the
+ * operations described on these pages:
+ *   [nvfp4-cu]  vLLM csrc/libtorch_stable/nvfp4_kv_cache_kernels.cu
+ *               (commit 7ce4c8e): "swizzle_scale_offset" comment block,
+ *               "reshape_and_cache_nvfp4_kernel" and
+ *               "reshape_and_cache_nvfp4_dispatch".
+ *   [pr25931]   vLLM PR #25931 "Add gather_indexer_k_quant_cache kernel".
+ *   [pr26456]   vLLM PR #26456 "[Deepseek-V3.2][Kernel] Integrate cuda
+ *               indexer k cache gather" (k_scale viewed as float32).
+ *
+ * The per-group quantiser (cvt_warp_fp16_to_fp4) is named but not shown on
+ * the pages; its rule is taken as: amax over the 16 values,
+ * sf = e4m3_rn_satfinite((amax / 6) * g) with g = 1 / k_scale, every element
+ * e2m1_rn_satfinite(x * (g / float(sf))) or 0 when sf == 0, two elements per
+ * byte with the even element in the low nibble.  Every division is an IEEE
+ * fp32 division, every product one fp32 rounding, no fused multiply-add
+ * (build with -ffp-contract=off, no -ffast-math).
+ *
+ * Format tables are built from the bit-level definitions of the two formats
+ * (OCP 8-bit e4m3 "fn" variant: bias 7, no infinities, 0x7F/0xFF NaN, max
+ * 448; e2m1: bias 1, no inf/NaN, max 6) and every encoding is a search over
+ * the table with round-to-nearest, ties to the even code, saturating to the
+ * largest finite magnitude.
+ *
+ * Parity pins for every function live in tests/test_oracle_*.py.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+#define KVQO_OK 0
+#define KVQO_ERR_ARG (-1)
+#define KVQO_ERR_NONFINITE (-2)
+#define KVQO_ERR_BOUNDS (-3)
+
+#define KVQO_LAYOUT_HND 0
+#define KVQO_LAYOUT_NHD 1
+#define KVQO_F_SWIZZLE_K_SCALE 1u
+
+/* ------------------------------------------------------------------------ */
+/* Format tables                                                            */
+/* ------------------------------------------------------------------------ */
+
+/* Non-negative finite e4m3 codes 0x00..0x7E and e2m1 codes 0..7. */
+static double e4m3_val[127];
+static double e2m1_val[8];
+static int tables_ready = 0;
+
+static void build_tables(void) {
+  if (tables_ready) return;
+  for (int c = 0; c < 127; ++c) {
+    int e = (c >> 3) & 0xF, m = c & 7;
+    /* subnormal: m/8 * 2^(1-7); normal: (1 + m/8) * 2^(e-7) */
+    e4m3_val[c] = (e == 0) ? ldexp((double)m / 8.0, 1 - 7)
+                           : ldexp(1.0 + (double)m / 8.0, e - 7);
+  }
+  for (int c = 0; c < 8; ++c) {
+    int e = (c >> 1) & 3, m = c & 1;
+    /* subnormal: m/2 * 2^(1-1); normal: (1 + m/2) * 2^(e-1) */
+    e2m1_val[c] = (e == 0) ? ldexp((double)m / 2.0, 1 - 1)
+                           : ldexp(1.0 + (double)m / 2.0, e - 1);
+  }
+  tables_ready = 1;
+}
+
+/* Round |v| to the nearest table entry, ties to the even code, saturating
+ * at the top entry.  vals[] is strictly increasing, vals[0] == 0. */
+static int encode_magnitude(double a, const double* vals, int n) {
+  if (a >= vals[n - 1]) return n - 1;
+  int c = 0;
+  while (!(vals[c] <= a && a < vals[c + 1])) ++c;
+  double mid = 0.5 * (vals[c] + vals[c + 1]); /* exact in double */
+  if (a < mid) return c;
+  if (a > mid) return c + 1;
+  return (c % 2 == 0) ? c : c + 1;
+}
+
+double kvqo_e4m3_decode(uint8_t code) {
+  build_tables();
+  int mag = code & 0x7F;
+  if (mag == 0x7F) return NAN;
+  double v = e4m3_val[mag];
+  return (code & 0x80) ? -v : v;
+}
+
+double kvqo_e2m1_decode(uint8_t nibble) {
+  build_tables();
+  double v = e2m1_val[nibble & 7];
+  return (nibble & 8) ? -v : v;
+}
+
+/* e4m3 round-to-nearest-even, satfinite; the sign of v (including -0) is
+ * kept.  Non-finite input returns 0x7F (NaN code). */
+uint8_t kvqo_e4m3_encode(float v) {
+  build_tables();
+  if (!isfinite(v)) return 0x7F;
+  int mag = encode_magnitude(fabs((double)v), e4m3_val, 127);
+  return (uint8_t)((signbit(v) ? 0x80 : 0x00) | mag);
+}
+
+/* e2m1 round-to-nearest-even, satfinite; the sign of v (including -0) is
+ * kept in bit 3.  Non-finite input returns 0xF. */
+uint8_t kvqo_e2m1_encode(float v) {
+  build_tables();
+  if (!isfinite(v)) return 0xF;
+  int mag = encode_magnitude(fabs((double)v), e2m1_val, 8);
+  return (uint8_t)((signbit(v) ? 0x8 : 0x0) | mag);
+}
+
+/* bf16 bits -> fp32 (exact). */
+static float bf16_to_float(uint16_t b) {
+  uint32_t u = (uint32_t)b << 16;
+  float f;
+  memcpy(&f, &u, sizeof f);
+  return f;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Scale-tile swizzle ([nvfp4-cu] "swizzle_scale_offset" comment):          */
+/* the [T, S] tile viewed as [T/4, 4, 4, S/4], permuted (0, 2, 3, 1) and    */
+/* read back as [T, S].  Returns row * S + col of the swizzled position.    */
+/* ------------------------------------------------------------------------ */
+int kvqo_swizzle(int t, int s, int S) {
+  int q = S / 4;
+  int row = (t / 4) * 4 + s / q;
+  int col = (s % q) * 4 + t % 4;
+  return row * S + col;
+}
+
+/* ------------------------------------------------------------------------ */
+/* One 16-element group ([nvfp4-cu] kernel: load group, quantise, pack).     */
+/* x: 16 bf16 bit patterns.  g: global scale (1 / k_scale).                  */
+/* data8: 8 output bytes.  *sf: e4m3 scale code.                             */
+/* ------------------------------------------------------------------------ */
+int kvqo_quantize_group(const uint16_t* x, float g, uint8_t* data8,
+                        uint8_t* sf_out) {
+  float xs[16];
+  for (int i = 0; i < 16; ++i) {
+    xs[i] = bf16_to_float(x[i]);
+    if (!isfinite(xs[i])) return KVQO_ERR_NONFINITE;
+  }
+  float amax = 0.0f;
+  for (int i = 0; i < 16; ++i) {
+    float a = fabsf(xs[i]);
+    if (a > amax) amax = a;
+  }
+  float sfv = (amax / 6.0f) * g; /* two IEEE fp32 roundings */
+  uint8_t sf = kvqo_e4m3_encode(sfv);
+  uint8_t q[16];
+  if (sf == 0) {
+    for (int i = 0; i < 16; ++i) q[i] = 0;
+  } else {
+    float r = g / (float)kvqo_e4m3_decode(sf); /* IEEE fp32 division */
+    for (int i = 0; i < 16; ++i) q[i] = kvqo_e2m1_encode(xs[i] * r);
+  }
+  for (int k = 0; k < 8; ++k)
+    data8[k] = (uint8_t)(q[2 * k] | (q[2 * k + 1] << 4));
+  *sf_out = sf;
+  return KVQO_OK;
+}
+
+/* ------------------------------------------------------------------------ */
+/* NVFP4 paged store ([nvfp4-cu] kernel and dispatch).                      */
+/*                                                                          */
+/* key/value: bf16 bits [num_tokens, H, D], row stride key_stride0 /        */
+/*   value_stride0 elements, heads and elements contiguous.                 */
+/* key_cache/value_cache: base of the K side and of the V side of page 0    */
+/*   (kv_cache[:, 0] and kv_cache[:, 1]); pages are page_stride bytes apart. */
+/*   Inside one side: data region [H, B, D/2] (HND) or [B, H, D/2] (NHD),    */
+/*   then the scale region at +H*B*D/2, [H, B, S] or [B, H, S].              */
+/* slot_mapping: int64 per token; slot < 0 skips the token.                 */
+/* k_scale/v_scale: the per-tensor scales; g = 1/k_scale, 1/v_scale.         */
+/* flags & KVQO_F_SWIZZLE_K_SCALE: K scales also swizzled (default linear). */
+/* Bytes of the cache that no token owns are left as they were.             */
+/* ------------------------------------------------------------------------ */
+int kvqo_store_nvfp4(const uint16_t* key, int64_t key_stride0,
+                     const uint16_t* value, int64_t value_stride0,
+                     int32_t num_tokens, int32_t num_heads, int32_t head_size,
+                     uint8_t* key_cache, uint8_t* value_cache,
+                     int64_t page_stride, int32_t block_size,
+                     int64_t num_blocks, int32_t layout,
+                     const int64_t* slot_mapping, float k_scale, float v_scale,
+                     uint32_t flags) {
+  if (num_tokens < 0 || num_heads <= 0 || head_size <= 0 || block_size <= 0)
+    return KVQO_ERR_ARG;
+  if (head_size % 64 != 0 || block_size % 4 != 0) return KVQO_ERR_ARG;
+  if (layout != KVQO_LAYOUT_HND && layout != KVQO_LAYOUT_NHD)
+    return KVQO_ERR_ARG;
+
+  const int64_t H = num_heads, D = head_size, B = block_size;
+  const int64_t data_dim = D / 2, S = D / 16;
+  const int64_t groups_per_head = D / 16;
+
+  /* Inner strides of one side ([nvfp4-cu] dispatch, layout detection). */
+  int64_t dhs, dts, shs, sts;
+  if (layout == KVQO_LAYOUT_HND) {
+    dhs = B * data_dim; dts = data_dim;
+    shs = B * S;        sts = S;
+  } else {
+    dhs = data_dim;     dts = H * data_dim;
+    shs = S;            sts = H * S;
+  }
+  const int64_t data_per_side = H * B * data_dim;
+
+  /* S2: global scale per side. */
+  const float g_side[2] = {1.0f / k_scale, 1.0f / v_scale};
+
+  for (int64_t t = 0; t < num_tokens; ++t) {
+    /* S1: slot decode, skip rule. */
+    const int64_t slot = slot_mapping[t];
+    if (slot < 0) continue;
+    const int64_t blk = slot / B;
+    const int64_t off = slot % B;
+    if (blk >= num_blocks) return KVQO_ERR_BOUNDS;
+
+    for (int side = 0; side < 2; ++side) {
+      const uint16_t* src = (side == 0) ? key + t * key_stride0
+                                        : value + t * value_stride0;
+      uint8_t* side_base = (side == 0) ? key_cache : value_cache;
+      uint8_t* data_page = side_base + blk * page_stride;
+      uint8_t* scale_page = data_page + data_per_side;
+      const float g = g_side[side];
+      const int swizzle = (side == 1) || (flags & KVQO_F_SWIZZLE_K_SCALE);
+
+      for (int64_t h = 0; h < H; ++h) {
+        for (int64_t j = 0; j < groups_per_head; ++j) {
+          /* S3..S5 */
+          uint8_t packed[8], sf;
+          int rc = kvqo_quantize_group(src + h * D + 16 * j, g, packed, &sf);
+          if (rc != KVQO_OK) return rc;
+          /* S6: 8 data bytes of group j. */
+          uint8_t* dst = data_page + h * dhs + off * dts + 8 * j;
+          for (int k = 0; k < 8; ++k) dst[k] = packed[k];
+          /* S7: scale byte, linear or swizzled inside the head's tile. */
+          uint8_t* sdst;
+          if (!swizzle) {
+            sdst = scale_page + h * shs + off * sts + j;
+          } else {
+            int pos = kvqo_swizzle((int)off, (int)j, (int)S);
+            int64_t row = pos / S, col = pos % S;
+            sdst = scale_page + h * shs + row * sts + col;
+          }
+          *sdst = sf;
+        }
+      }
+    }
+  }
+  return KVQO_OK;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Indexer-K gather ([pr25931] cp_gather_indexer_k_quant_cache; [pr26456]   */
+/* scale bytes viewed as float32 by the consumer).                          */
+/*                                                                          */
+/* cache: blocks block_stride bytes apart; block = [B*D fp8 K | B*4 scale]. */
+/* block_table: int32 [num_seqs, bt_stride]; cu_seq_lens: int32 [num_seqs+1]*/
+/* Sequence b's token p (0 <= p < len_b) is output row cu[b] + p:           */
+/*   k_fp8[row, 0:D]      = K bytes of (block_table[b, p/B], p%B)            */
+/*   k_scale[4*row, +4]   = the 4 scale bytes of that token (raw copy).      */
+/* Rows at or beyond total_tokens are not written.                          */
+/* ------------------------------------------------------------------------ */
+int kvqo_gather_indexer_k(const uint8_t* cache, int64_t block_stride,
+                          int64_t num_blocks, int32_t block_size,
+                          int32_t head_dim, const int32_t* block_table,
+                          int64_t bt_stride, int32_t max_blocks_per_seq,
+                          const int32_t* cu_seq_lens, int32_t num_seqs,
+                          int64_t total_tokens, uint8_t* k_fp8,
+                          uint8_t* k_scale) {
+  if (num_seqs < 0 || block_size <= 0 || head_dim <= 0 || total_tokens < 0)
+    return KVQO_ERR_ARG;
+  const int64_t B = block_size, D = head_dim;
+  for (int32_t b = 0; b < num_seqs; ++b) {
+    const int64_t start = cu_seq_lens[b];
+    const int64_t len = (int64_t)cu_seq_lens[b + 1] - start;
+    for (int64_t p = 0; p < len; ++p) {
+      const int64_t row = start + p;
+      if (row < 0 || row >= total_tokens) return KVQO_ERR_BOUNDS;
+      if (p / B >= max_blocks_per_seq) return KVQO_ERR_BOUNDS;
+      const int64_t blk = block_table[b * bt_stride + p / B];
+      const int64_t off = p % B;
+      if (blk < 0 || blk >= num_blocks) return KVQO_ERR_BOUNDS;
+      const uint8_t* block = cache + blk * block_stride;
+      for (int64_t d = 0; d < D; ++d) k_fp8[row * D + d] = block[off * D + d];
+      for (int k = 0; k < 4; ++k)
+        k_scale[row * 4 + k] = block[B * D + off * 4 + k];
+    }
+  }
+  return KVQO_OK;
+}

@@ -1,0 +1,339 @@
+"""Seeded synthetic workloads for the NVFP4 KV store and the indexer-K gather.
+
+This module only draws inputs (numpy ``default_rng``); it holds none of the
+quantisation or gather arithmetic, so the CUDA path and the CPU oracle can
+both consume its arrays.  Every array is produced on the host as exact
+bytes; callers copy them to the device.
+
+Named workloads (seed = workload index unless given):
+
+0. ``tiny`` -- store: 24 tokens, 2 KV heads, head_size 64, block_size 16,
+   8-block cache, bf16 N(0,1) with one x20 outlier per (side, head),
+   k_scale = v_scale = 1, 24 distinct random slots in [0, 128) with 3 set
+   to -1.  Gather: sequences of 5 and 37 tokens, block_size 64, head_dim 128,
+   4-block cache, random non-NaN e4m3 K bytes, scales U[1e-3, 1], block table
+   a random permutation of the 4 blocks as [2, 2].
+1. ``decode`` -- store: 256 tokens (one per request), 8 heads, head_size 128,
+   block_size 16, N(0,1), per-tensor scale amax/(448*6), 65536-block cache,
+   256 random distinct slots.
+2. ``prefill`` -- store: 16 requests x 1024 tokens, 8 heads, head_size 128,
+   block_size 16, N(0,1) with 0.1% of values x50, per-tensor scales, each
+   request's tokens in contiguous runs over 64 randomly chosen blocks of a
+   65536-block cache; K and V are the two halves of a [T, 2, H, D] buffer
+   (row stride 2*H*D).
+3. ``prefill_gather`` -- gather: 16 sequences with lengths U[1000, 8192],
+   block_size 64, head_dim 128, 4096-block cache, log-uniform scales in
+   [1e-4, 1], block table [16, 128] from a random permutation of the blocks.
+4. ``long`` -- (a) store: 256 requests x 512 tokens, 4 heads, head_size 256,
+   block_size 32, N(0,1), per-tensor scales, each request on 16 blocks of a
+   4096-block cache in random order; (b) gather: 256 sequences x 512 tokens,
+   block_size 64, head_dim 128, 8192-block cache, block table [256, 8].
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+
+import numpy as np
+import torch
+
+LAYOUT_HND = 0
+LAYOUT_NHD = 1
+
+
+def bf16_bits(x: np.ndarray) -> np.ndarray:
+    """fp32 -> bf16 (round to nearest even, torch's CPU cast) as uint16."""
+    t = torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32))
+    return t.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+def bf16_values(bits: np.ndarray) -> np.ndarray:
+    """uint16 bf16 bit patterns -> exact fp32 values."""
+    return (bits.astype(np.uint32) << 16).view(np.float32)
+
+
+@dataclass
+class StoreWorkload:
+    """Inputs of one NVFP4 paged store.
+
+    ``src`` is the flat bf16 (uint16 bits) backing buffer; key token t, head
+    h, element d sits at ``key_offset + t*key_stride0 + h*D + d`` and value
+    likewise.  The cache is ``num_blocks`` pages of ``page_stride`` bytes;
+    the K side of a page starts at byte 0 of the page and the V side at
+    ``value_side_offset``."""
+    name: str
+    num_tokens: int
+    num_heads: int
+    head_size: int
+    block_size: int
+    num_blocks: int
+    src: np.ndarray
+    key_offset: int
+    key_stride0: int
+    value_offset: int
+    value_stride0: int
+    slot_mapping: np.ndarray
+    k_scale: np.float32
+    v_scale: np.float32
+    layout: int = LAYOUT_HND
+    flags: int = 0
+    page_stride: int = 0
+    extra: dict = field(default_factory=dict)
+
+    def __post_init__(self):
+        if self.page_stride == 0:
+            self.page_stride = 2 * self.side_bytes
+
+    @property
+    def scale_dim(self) -> int:
+        return self.head_size // 16
+
+    @property
+    def side_bytes(self) -> int:
+        H, B, D = self.num_heads, self.block_size, self.head_size
+        return H * B * (D // 2 + D // 16)
+
+    @property
+    def value_side_offset(self) -> int:
+        return self.side_bytes
+
+    @property
+    def cache_bytes(self) -> int:
+        return self.num_blocks * self.page_stride
+
+    @property
+    def stored_tokens(self) -> int:
+        return int((self.slot_mapping[: self.num_tokens] >= 0).sum())
+
+    def algorithmic_bytes(self) -> int:
+        """bf16 K and V read + int64 slot read + NVFP4 data and scales
+        written, for the tokens that are stored (a skipped token reads only
+        its slot)."""
+        H, D = self.num_heads, self.head_size
+        n = self.stored_tokens
+        return (n * 2 * H * D * 2 + self.num_tokens * 8
+                + n * 2 * H * (D // 2 + D // 16))
+
+    def key_array(self) -> np.ndarray:
+        """[T, H, D] view of the key bits (strided)."""
+        return _view(self.src, self.key_offset, self.key_stride0,
+                     self.num_tokens, self.num_heads, self.head_size)
+
+    def value_array(self) -> np.ndarray:
+        return _view(self.src, self.value_offset, self.value_stride0,
+                     self.num_tokens, self.num_heads, self.head_size)
+
+
+def _view(src, offset, stride0, T, H, D):
+    if T == 0:
+        return np.zeros((0, H, D), dtype=np.uint16)
+    it = src.itemsize
+    return np.lib.stride_tricks.as_strided(
+        src[offset:], shape=(T, H, D), strides=(stride0 * it, D * it, it),
+        writeable=False)
+
+
+@dataclass
+class GatherWorkload:
+    """Inputs of one indexer-K gather.
+
+    ``cache`` holds ``num_blocks`` blocks of ``block_stride`` bytes; block =
+    [block_size*head_dim fp8 K | block_size*4 fp32 scale bytes]."""
+    name: str
+    block_size: int
+    head_dim: int
+    num_blocks: int
+    cache: np.ndarray
+    block_table: np.ndarray
+    cu_seq_lens: np.ndarray
+    block_stride: int = 0
+    extra: dict = field(default_factory=dict)
+
+    def __post_init__(self):
+        if self.block_stride == 0:
+            self.block_stride = self.block_size * (self.head_dim + 4)
+
+    @property
+    def num_seqs(self) -> int:
+        return int(self.cu_seq_lens.size - 1)
+
+    @property
+    def total_tokens(self) -> int:
+        return int(self.cu_seq_lens[-1])
+
+    def algorithmic_bytes(self) -> int:
+        """K row and scale read and written per token, plus the block-table
+        entries and cu_seq_lens read."""
+        B = self.block_size
+        lens = np.diff(self.cu_seq_lens.astype(np.int64))
+        table_entries = int(((lens + B - 1) // B).sum())
+        return (self.total_tokens * 2 * (self.head_dim + 4)
+                + 4 * table_entries + 4 * self.cu_seq_lens.size)
+
+
+# --- generators ---------------------------------------------------------------
+
+def random_e4m3_bytes(rng, n: int) -> np.ndarray:
+    """n bytes uniform over the 254 non-NaN e4m3 codes (all but 0x7F, 0xFF)."""
+    v = rng.integers(0, 254, size=n, dtype=np.int32)
+    v = np.where(v >= 0x7F, v + 1, v)
+    return v.astype(np.uint8)
+
+
+def _normal_f32(rng, shape, outlier_p=0.0, outlier_mult=1.0):
+    x = rng.standard_normal(size=shape, dtype=np.float32)
+    if outlier_p > 0:
+        mask = rng.random(size=shape) < outlier_p
+        x = np.where(mask, x * np.float32(outlier_mult), x)
+    return x
+
+
+def per_tensor_scale(bits: np.ndarray) -> np.float32:
+    """Checkpoint scale recipe of the decode/prefill workloads:
+    amax(|x|) / (448 * 6) in fp32."""
+    if bits.size == 0:
+        return np.float32(1.0)
+    amax = np.abs(bf16_values(bits)).max()
+    return np.float32(amax) / np.float32(448.0 * 6.0)
+
+
+def make_store(name: str, seed: int, num_tokens: int, num_heads: int,
+               head_size: int, block_size: int, num_blocks: int,
+               slots: str = "random", skip: int = 0, row_mult: int = 1,
+               outlier_p: float = 0.0, outlier_mult: float = 1.0,
+               outlier_per_head: float = 0.0, scales: str = "per_tensor",
+               request_len: int = 0, layout: int = LAYOUT_HND,
+               flags: int = 0) -> StoreWorkload:
+    """Generic store workload.
+
+    slots: "random" (distinct random slots over the whole cache),
+    "runs" (requests of ``request_len`` tokens, each on randomly chosen
+    distinct blocks filled in order), or "dense" (token t -> slot t).
+    skip: number of tokens whose slot is set to -1.
+    row_mult: K and V are halves of a [T, row_mult, H, D] buffer when 2."""
+    rng = np.random.default_rng(seed)
+    T, H, D, B = num_tokens, num_heads, head_size, block_size
+    if row_mult == 2:
+        x = _normal_f32(rng, (T, 2, H, D), outlier_p, outlier_mult)
+        if outlier_per_head:
+            for side in range(2):
+                for h in range(H):
+                    t = rng.integers(0, max(T, 1))
+                    d = rng.integers(0, D)
+                    if T:
+                        x[t, side, h, d] *= np.float32(outlier_per_head)
+        src = bf16_bits(x.reshape(-1))
+        key_offset, value_offset, stride0 = 0, H * D, 2 * H * D
+    else:
+        kx = _normal_f32(rng, (T, H, D), outlier_p, outlier_mult)
+        vx = _normal_f32(rng, (T, H, D), outlier_p, outlier_mult)
+        if outlier_per_head and T:
+            for arr in (kx, vx):
+                for h in range(H):
+                    t = rng.integers(0, T)
+                    d = rng.integers(0, D)
+                    arr[t, h, d] *= np.float32(outlier_per_head)
+        src = bf16_bits(np.concatenate([kx.reshape(-1), vx.reshape(-1)]))
+        key_offset, value_offset, stride0 = 0, T * H * D, H * D
+
+    capacity = num_blocks * B
+    if slots == "random":
+        sm = rng.choice(capacity, size=T, replace=False).astype(np.int64)
+    elif slots == "dense":
+        sm = np.arange(T, dtype=np.int64)
+    elif slots == "runs":
+        assert request_len > 0 and T % request_len == 0
+        n_req = T // request_len
+        bpr = (request_len + B - 1) // B
+        blocks = rng.permutation(num_blocks)[: n_req * bpr].reshape(n_req, bpr)
+        k = np.arange(request_len)
+        sm = (blocks[:, k // B] * B + (k % B)[None, :]).reshape(-1)
+        sm = sm.astype(np.int64)
+    else:
+        raise ValueError(slots)
+    if skip:
+        sm[rng.choice(T, size=skip, replace=False)] = -1
+
+    wl = StoreWorkload(name=name, num_tokens=T, num_heads=H, head_size=D,
+                       block_size=B, num_blocks=num_blocks, src=src,
+                       key_offset=key_offset, key_stride0=stride0,
+                       value_offset=value_offset, value_stride0=stride0,
+                       slot_mapping=sm, k_scale=np.float32(1.0),
+                       v_scale=np.float32(1.0), layout=layout, flags=flags)
+    if scales == "per_tensor":
+        wl.k_scale = per_tensor_scale(np.asarray(wl.key_array()))
+        wl.v_scale = per_tensor_scale(np.asarray(wl.value_array()))
+    elif scales == "one":
+        pass
+    else:
+        wl.k_scale, wl.v_scale = np.float32(scales[0]), np.float32(scales[1])
+    return wl
+
+
+def make_gather(name: str, seed: int, seq_lens, block_size: int,
+                head_dim: int, num_blocks: int, max_blocks: int = 0,
+                scales: str = "log", block_stride: int = 0) -> GatherWorkload:
+    """Generic gather workload: random non-NaN e4m3 K bytes, fp32 scales
+    ("uniform": U[1e-3, 1]; "log": 10^U(-4, 0)), block table rows filled
+    from one random permutation of the cache's blocks."""
+    rng = np.random.default_rng(seed)
+    B, D = block_size, head_dim
+    stride = block_stride or B * (D + 4)
+    lens = np.asarray(seq_lens, dtype=np.int64)
+    n = lens.size
+    need = (lens + B - 1) // B
+    mb = max_blocks or max(int(need.max()) if n else 1, 1)
+    cache = np.zeros((num_blocks, stride), dtype=np.uint8)
+    cache[:, : B * D] = random_e4m3_bytes(rng, num_blocks * B * D).reshape(
+        num_blocks, B * D)
+    if scales == "uniform":
+        sc = rng.uniform(1e-3, 1.0, size=(num_blocks, B)).astype(np.float32)
+    else:
+        sc = (10.0 ** rng.uniform(-4.0, 0.0, size=(num_blocks, B))).astype(
+            np.float32)
+    cache[:, B * D: B * D + 4 * B] = sc.view(np.uint8).reshape(num_blocks,
+                                                               4 * B)
+    perm = rng.permutation(num_blocks).astype(np.int32)
+    assert n * mb <= num_blocks
+    block_table = perm[: n * mb].reshape(n, mb).copy()
+    cu = np.zeros(n + 1, dtype=np.int32)
+    cu[1:] = np.cumsum(lens)
+    return GatherWorkload(name=name, block_size=B, head_dim=D,
+                          num_blocks=num_blocks, cache=cache.reshape(-1),
+                          block_table=block_table, cu_seq_lens=cu,
+                          block_stride=stride)
+
+
+# --- the five named workloads --------------------------------------------------
+
+def store_workload(index: int, seed: int | None = None) -> StoreWorkload:
+    s = index if seed is None else seed
+    if index == 0:
+        return make_store("tiny_store", s, 24, 2, 64, 16, 8, slots="random",
+                          skip=3, outlier_per_head=20.0, scales="one")
+    if index == 1:
+        return make_store("decode_store", s, 256, 8, 128, 16, 65536,
+                          slots="random")
+    if index == 2:
+        return make_store("prefill_store", s, 16384, 8, 128, 16, 65536,
+                          slots="runs", request_len=1024, row_mult=2,
+                          outlier_p=1e-3, outlier_mult=50.0)
+    if index == 4:
+        return make_store("long_store", s, 131072, 4, 256, 32, 4096,
+                          slots="runs", request_len=512)
+    raise ValueError(f"workload {index} has no store part")
+
+
+def gather_workload(index: int, seed: int | None = None) -> GatherWorkload:
+    s = index if seed is None else seed
+    if index == 0:
+        return make_gather("tiny_gather", s, [5, 37], 64, 128, 4,
+                           max_blocks=2, scales="uniform")
+    if index == 3:
+        lens = np.random.default_rng([s, 1]).integers(1000, 8192, size=16,
+                                                       endpoint=True)
+        return make_gather("prefill_gather", s, lens, 64, 128, 4096,
+                           max_blocks=128)
+    if index == 4:
+        return make_gather("long_gather", s, [512] * 256, 64, 128, 8192,
+                           max_blocks=8)
+    raise ValueError(f"workload {index} has no gather part")

@@ -1,0 +1,81 @@
+"""The oracle's pins are sensitive: each plausible mistake planted in a copy
+of the oracle source (a dropped term, a wrong sign, index, operand order or
+tie rule) must make at least one pin fail.  Runs on the CPU only; the
+mutants are compiled into a temporary directory and never replace the real
+oracle."""
+import pytest
+
+import oracle
+from tests import test_oracle_formats as F
+from tests import test_oracle_gather as G
+from tests import test_oracle_store as S
+
+ALL_CHECKS = F.CHECKS + S.CHECKS + G.CHECKS
+
+# (id, original text, planted mistake) -- every original occurs exactly once
+MUTANTS = [
+    ("scale_divides_by_g", "float sfv = (amax / 6.0f) * g;",
+     "float sfv = (amax / 6.0f) / g;"),
+    ("scale_drops_six", "float sfv = (amax / 6.0f) * g;",
+     "float sfv = (amax / 4.0f) * g;"),
+    ("ties_away_from_even", "return (c % 2 == 0) ? c : c + 1;",
+     "return c + 1;"),
+    ("ties_toward_zero", "return (c % 2 == 0) ? c : c + 1;", "return c;"),
+    ("nibbles_swapped",
+     "data8[k] = (uint8_t)(q[2 * k] | (q[2 * k + 1] << 4));",
+     "data8[k] = (uint8_t)(q[2 * k + 1] | (q[2 * k] << 4));"),
+    ("signed_amax", "float a = fabsf(xs[i]);", "float a = xs[i];"),
+    ("ratio_without_g", "float r = g / (float)kvqo_e4m3_decode(sf);",
+     "float r = 1.0f / (float)kvqo_e4m3_decode(sf);"),
+    ("e4m3_subnormal_exponent", "ldexp((double)m / 8.0, 1 - 7)",
+     "ldexp((double)m / 8.0, -7)"),
+    ("e4m3_bias", "ldexp(1.0 + (double)m / 8.0, e - 7)",
+     "ldexp(1.0 + (double)m / 8.0, e - 8)"),
+    ("e2m1_drops_sign",
+     "return (uint8_t)((signbit(v) ? 0x8 : 0x0) | mag);",
+     "return (uint8_t)(mag);"),
+    ("saturates_one_code_low", "if (a >= vals[n - 1]) return n - 1;",
+     "if (a >= vals[n - 1]) return n - 2;"),
+    ("sf_zero_branch_missing", "if (sf == 0) {", "if (sf == 0xFF) {"),
+    ("swizzle_row", "int row = (t / 4) * 4 + s / q;",
+     "int row = (t / 4) * 4 + s % 4;"),
+    ("swizzle_col", "int col = (s % q) * 4 + t % 4;",
+     "int col = (s % q) * 4 + (t + 1) % 4;"),
+    ("swizzles_k_not_v",
+     "const int swizzle = (side == 1) || (flags & KVQO_F_SWIZZLE_K_SCALE);",
+     "const int swizzle = (side == 0) || (flags & KVQO_F_SWIZZLE_K_SCALE);"),
+    ("nhd_as_hnd", "dhs = data_dim;     dts = H * data_dim;",
+     "dhs = B * data_dim; dts = data_dim;"),
+    ("scale_region_offset",
+     "uint8_t* scale_page = data_page + data_per_side;",
+     "uint8_t* scale_page = data_page + data_per_side / 2;"),
+    ("v_uses_k_scale",
+     "const float g_side[2] = {1.0f / k_scale, 1.0f / v_scale};",
+     "const float g_side[2] = {1.0f / k_scale, 1.0f / k_scale};"),
+    ("skip_rule_includes_zero", "if (slot < 0) continue;",
+     "if (slot <= 0) continue;"),
+    ("gather_offset", "const int64_t off = p % B;\n      if (blk < 0",
+     "const int64_t off = (p + 1) % B;\n      if (blk < 0"),
+    ("gather_scale_byte_order", "k_scale[row * 4 + k] = block[B * D + off * 4 + k];",
+     "k_scale[row * 4 + k] = block[B * D + off * 4 + (3 - k)];"),
+    ("gather_row_bytes", "k_fp8[row * D + d] = block[off * D + d];",
+     "k_fp8[row * D + d] = block[off * D + (d ^ 1)];"),
+]
+
+
+@pytest.mark.parametrize("mid,orig,mutant", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_pins_catch_planted_mistake(tmp_path, mid, orig, mutant):
+    src = open(oracle.SOURCE).read()
+    assert src.count(orig) == 1, mid
+    path = tmp_path / f"kvq_oracle_{mid}.c"
+    path.write_text(src.replace(orig, mutant))
+    so = oracle.compile_oracle(str(path), str(tmp_path / f"lib_{mid}.so"))
+    o = oracle.Oracle(so)
+    caught = None
+    for check in ALL_CHECKS:
+        try:
+            check(o)
+        except (AssertionError, ValueError):
+            caught = check.__name__
+            break
+    assert caught is not None, f"no pin caught mutant {mid}"
