@@ -1,0 +1,542 @@
+"""Benchmark of the paged quantized KV-cache hot path on GB300.
+
+One step = the long-context mix: an NVFP4 paged store of 131072 tokens
+(256 requests x 512, 4 KV heads, head_size 256, block_size 32, bf16 N(0,1))
+followed by an indexer-K gather of 256 sequences x 512 tokens (block_size
+64, head_dim 128, 8192-block cache).  Inputs are seeded synthetic arrays
+copied to HBM before timing; L2 is flushed (256 MiB write) before every
+step, outside the timed events.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line (rank 0).  ``--impl reference`` times the CPU oracle on
+the host cores on a bounded sample of the same workload.  Under torchrun
+each rank runs its own replica (different seeds, no data exchange): weak
+scaling, the slowest rank's time counts.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = ("HBM GB/s (% of GB300 peak) and tokens/s for NVFP4 KV store and "
+          "indexer-K gather")
+WORKLOAD = ("long-context mix: NVFP4 store 131072 tokens (256 req x 512), "
+            "4 KV heads, head_size 256, block_size 32, 4096-block cache + "
+            "indexer-K gather 256 seqs x 512 tokens, block_size 64, "
+            "head_dim 128, 8192-block cache")
+FALLBACK_HBM_GBS = 6800.0
+FLUSH_BYTES = 256 << 20
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--cpu-sample-tokens", type=int, default=65536)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--clock-window-s", type=float, default=1.5)
+    return ap.parse_args()
+
+
+# --- distributed plumbing (host side only) ------------------------------------
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")),
+            int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(value: float, world: int, device=None) -> float:
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def rank_seed(base: int, rank: int) -> int:
+    """Each replica draws its own requests."""
+    return base + 1000 * rank
+
+
+# --- workload -------------------------------------------------------------------
+
+def make_workload(rank: int):
+    from paged_quantized_kv_gb300 import workloads as W
+    st = W.store_workload(4, seed=rank_seed(4, rank))
+    ga = W.gather_workload(4, seed=rank_seed(4, rank))
+    return st, ga
+
+
+def measured_hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_sha(fname: str) -> str:
+    path = os.path.join(ROOT, "paged_quantized_kv_gb300", "csrc", fname)
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def profiled_traffic(profile_md: str, src_file: str):
+    """DRAM bytes per launch from a committed ncu summary, or None if the
+    summary is absent or was taken on a different kernel source."""
+    path = os.path.join(ROOT, "profiles", profile_md)
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    m_sha = re.search(r"source_sha256_16:\s*([0-9a-f]+)", text)
+    m_b = re.search(r"dram_bytes_per_full_launch:\s*([0-9]+)", text)
+    if not (m_sha and m_b) or m_sha.group(1) != kernel_sha(src_file):
+        return None
+    return int(m_b.group(1))
+
+
+# --- clocks ---------------------------------------------------------------------
+
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,"
+             "clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+             "clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,"
+             "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.out = tempfile.NamedTemporaryFile("w+", suffix=".csv",
+                                               delete=False)
+        self.proc = None
+        self.dev = device_index
+
+    def start(self):
+        import torch
+        sel = []
+        try:
+            uuid = str(torch.cuda.get_device_properties(self.dev).uuid)
+            sel = ["-i", uuid if uuid.startswith("GPU-") else "GPU-" + uuid]
+        except Exception:
+            sel = []
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "50", *sel],
+                stdout=self.out, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.out.flush()
+        self.out.seek(0)
+        rows = [r.split(",") for r in self.out.read().splitlines()
+                if r.strip()]
+        os.unlink(self.out.name)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                 "sw_power_cap"]
+        for r in rows:
+            r = [x.strip() for x in r]
+            if len(r) < 9:
+                continue
+            try:
+                sm.append(float(r[1]))
+                smax.append(float(r[2]))
+            except ValueError:
+                continue
+            for name, flag in zip(names, r[5:9]):
+                if flag.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# --- our arm ----------------------------------------------------------------------
+
+def run_ours(args):
+    import torch
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+
+    import __graft_entry__
+    __graft_entry__.build()
+    from paged_quantized_kv_gb300 import kvq
+
+    st, ga = make_workload(rank)
+    T, H, D = st.num_tokens, st.num_heads, st.head_size
+
+    # ---- device-resident inputs and outputs -------------------------------
+    src = torch.from_numpy(st.src.view(np.int16)).to(dev).view(torch.bfloat16)
+    key = src.as_strided((T, H, D), (st.key_stride0, D, 1), st.key_offset)
+    value = src.as_strided((T, H, D), (st.value_stride0, D, 1),
+                           st.value_offset)
+    slots = torch.from_numpy(st.slot_mapping).to(dev)
+    ks = torch.tensor([float(st.k_scale)], dtype=torch.float32, device=dev)
+    vs = torch.tensor([float(st.v_scale)], dtype=torch.float32, device=dev)
+    kv, kc, vc = kvq.alloc_nvfp4_cache(st.num_blocks, st.block_size, H, D,
+                                       device=dev, fill=0xAA)
+    gcache = torch.from_numpy(ga.cache).to(dev).view(ga.num_blocks, -1)
+    bt = torch.from_numpy(ga.block_table).to(dev)
+    cu = torch.from_numpy(ga.cu_seq_lens).to(dev)
+    n = ga.total_tokens
+    k_fp8 = torch.empty((n, ga.head_dim), dtype=torch.uint8, device=dev)
+    k_scale = torch.empty((n, 4), dtype=torch.uint8, device=dev)
+    dev_err = torch.zeros(1, dtype=torch.int32, device=dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    sh = stream.cuda_stream
+
+    def store():
+        kvq.kvq_store_nvfp4(key, value, kc, vc, slots, ks, vs,
+                            dev_error=dev_err, stream=sh)
+
+    def gather():
+        kvq.kvq_gather_indexer_k(gcache, k_fp8, k_scale, bt, cu,
+                                 block_size=ga.block_size, dev_error=dev_err,
+                                 stream=sh)
+
+    for i in range(max(args.warmup, 3)):
+        flush.fill_(i & 0xFF)
+        store()
+        gather()
+    torch.cuda.synchronize(dev)
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)]
+          for _ in range(K)]
+    sampler = ClockSampler(dev.index)
+    sampler.start()
+    time.sleep(0.2)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    t0 = time.perf_counter()
+    for i in range(K):
+        flush.fill_(i & 0xFF)
+        ev[i][0].record(stream)
+        store()
+        ev[i][1].record(stream)
+        gather()
+        ev[i][2].record(stream)
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        torch.distributed.barrier()
+    wall = time.perf_counter() - t0
+    # keep the same steps running so the clock sampler sees the load
+    t1 = time.perf_counter()
+    j = 0
+    while time.perf_counter() - t1 < args.clock_window_s:
+        flush.fill_(j & 0xFF)
+        store()
+        gather()
+        j += 1
+        if j % 50 == 0:
+            torch.cuda.synchronize(dev)
+    torch.cuda.synchronize(dev)
+    clocks = sampler.stop()
+
+    store_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(K)]
+    gather_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(K)]
+    step_ms = [ev[i][0].elapsed_time(ev[i][2]) for i in range(K)]
+    assert int(dev_err.item()) == 0, "device error flag raised"
+
+    st_bytes = st.algorithmic_bytes()
+    ga_bytes = ga.algorithmic_bytes()
+    mean_step = statistics.fmean(step_ms)
+    mean_store = statistics.fmean(store_ms)
+    mean_gather = statistics.fmean(gather_ms)
+    step_s = max_over_ranks(mean_step / 1e3, world, dev)
+    total_bytes = sum_over_ranks(float(st_bytes + ga_bytes), world, dev)
+    total_tokens = sum_over_ranks(float(T + n), world, dev)
+    peak, peak_kind = measured_hbm_peak()
+    store_gbs = st_bytes / (mean_store / 1e3) / 1e9
+    gather_gbs = ga_bytes / (mean_gather / 1e3) / 1e9
+    traffic = profiled_traffic("store_nvfp4_long.md", "store_nvfp4.cu")
+
+    e2e = run_e2e(args, st, ga, dev, kvq)
+
+    line = {
+        "metric": METRIC,
+        "value": round(total_bytes / step_s / 1e9, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": max(args.warmup, 3),
+        "ms_per_step": round(step_s * 1e3, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic",
+        "config": {
+            "workload": WORKLOAD,
+            "store": {"tokens": T, "num_heads": H, "head_size": D,
+                      "block_size": st.block_size,
+                      "num_blocks": st.num_blocks, "layout": "HND",
+                      "io": "bf16 in, e2m1 data + e4m3 scales out"},
+            "gather": {"seqs": ga.num_seqs, "tokens": n,
+                       "block_size": ga.block_size,
+                       "head_dim": ga.head_dim,
+                       "num_blocks": ga.num_blocks, "io": "u8 copy"},
+            "l2": "flushed before every step (256 MiB write) outside the "
+                  "timed events; store inputs alone exceed L2",
+            "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
+            "timing": "CUDA events per kernel on the launch stream, mean "
+                      "over the timed steps; max over ranks",
+        },
+        "tokens_per_s": round(total_tokens / step_s, 1),
+        "kernels": {
+            "store_nvfp4": {
+                "ms": round(mean_store, 5),
+                "GB_s": round(store_gbs, 1),
+                "frac_of_peak": round(store_gbs / peak, 4),
+                "tokens_per_s": round(T / (mean_store / 1e3), 1),
+                "algorithmic_bytes": st_bytes},
+            "gather_indexer_k": {
+                "ms": round(mean_gather, 5),
+                "GB_s": round(gather_gbs, 1),
+                "frac_of_peak": round(gather_gbs / peak, 4),
+                "tokens_per_s": round(n / (mean_gather / 1e3), 1),
+                "algorithmic_bytes": ga_bytes},
+        },
+        "roofline": {
+            "bound": "hbm",
+            "kernel": "store_nvfp4",
+            "achieved": round(store_gbs, 1),
+            "peak": peak,
+            "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
+                           if peak_kind == "measured" else "fallback 6.8 TB/s",
+            "unit": "GB/s",
+            "frac": round(store_gbs / peak, 4),
+            "traffic": traffic,
+        },
+        "wall_s_timed_region": round(wall, 4),
+        "e2e": e2e,
+        "gpu_launches": 2 * K,
+        "clocks": clocks,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(st, ga, args.cpu_sample_tokens)
+    if world > 1:
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def run_e2e(args, st, ga, dev, kvq):
+    """Same step through the public binding with pinned HOST buffers: H2D of
+    the step's inputs, both calls, D2H of the gathered rows and of the
+    written cache pages, all inside the timed region."""
+    import torch
+    T, H, D = st.num_tokens, st.num_heads, st.head_size
+    h_src = torch.from_numpy(st.src.view(np.int16)).pin_memory()
+    h_slots = torch.from_numpy(st.slot_mapping).pin_memory()
+    h_scales = torch.tensor([float(st.k_scale), float(st.v_scale)],
+                            dtype=torch.float32).pin_memory()
+    h_bt = torch.from_numpy(ga.block_table).pin_memory()
+    h_cu = torch.from_numpy(ga.cu_seq_lens).pin_memory()
+    n = ga.total_tokens
+    h_k = torch.empty((n, ga.head_dim), dtype=torch.uint8).pin_memory()
+    h_s = torch.empty((n, 4), dtype=torch.uint8).pin_memory()
+    kv, kc, vc = kvq.alloc_nvfp4_cache(st.num_blocks, st.block_size, H, D,
+                                       device=dev, fill=0xAA)
+    h_cache = torch.empty(kv.shape, dtype=torch.uint8).pin_memory()
+    d_src = torch.empty(h_src.shape, dtype=torch.int16, device=dev)
+    d_slots = torch.empty_like(h_slots, device=dev)
+    d_scales = torch.empty(2, dtype=torch.float32, device=dev)
+    d_bt = torch.empty_like(h_bt, device=dev)
+    d_cu = torch.empty_like(h_cu, device=dev)
+    gcache = torch.from_numpy(ga.cache).to(dev).view(ga.num_blocks, -1)
+    k_fp8 = torch.empty((n, ga.head_dim), dtype=torch.uint8, device=dev)
+    k_scale = torch.empty((n, 4), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        d_src.copy_(h_src, non_blocking=True)
+        d_slots.copy_(h_slots, non_blocking=True)
+        d_scales.copy_(h_scales, non_blocking=True)
+        d_bt.copy_(h_bt, non_blocking=True)
+        d_cu.copy_(h_cu, non_blocking=True)
+        src = d_src.view(torch.bfloat16)
+        key = src.as_strided((T, H, D), (st.key_stride0, D, 1), st.key_offset)
+        value = src.as_strided((T, H, D), (st.value_stride0, D, 1),
+                               st.value_offset)
+        kvq.kvq_store_nvfp4(key, value, kc, vc, d_slots, d_scales[0:1],
+                            d_scales[1:2])
+        kvq.kvq_gather_indexer_k(gcache, k_fp8, k_scale, d_bt, d_cu,
+                                 block_size=ga.block_size)
+        h_k.copy_(k_fp8, non_blocking=True)
+        h_s.copy_(k_scale, non_blocking=True)
+        h_cache.copy_(kv, non_blocking=True)
+
+    for _ in range(2):
+        step()
+    torch.cuda.synchronize(dev)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    E = max(args.e2e_steps, 1)
+    e0.record(stream)
+    for _ in range(E):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = e0.elapsed_time(e1) / E
+    h2d = (h_src.numel() * 2 + h_slots.numel() * 8 + 8 + h_bt.numel() * 4
+           + h_cu.numel() * 4)
+    d2h = h_k.numel() + h_s.numel() + h_cache.numel()
+    byts = st.algorithmic_bytes() + ga.algorithmic_bytes()
+    return {"value": round(byts / (ms / 1e3) / 1e9, 2), "unit": "GB/s",
+            "ms_per_step": round(ms, 4), "h2d_bytes_per_step": int(h2d),
+            "d2h_bytes_per_step": int(d2h), "steps": E}
+
+
+# --- CPU oracle legs ----------------------------------------------------------------
+
+def oracle_sample(st, ga, sample_tokens):
+    """A bounded slice of the workload: the first requests of the store and
+    the first sequences of the gather, same shapes and distributions."""
+    from paged_quantized_kv_gb300 import workloads as W
+    T = min(sample_tokens, st.num_tokens)
+    sub = W.StoreWorkload(
+        name="sample", num_tokens=T, num_heads=st.num_heads,
+        head_size=st.head_size, block_size=st.block_size,
+        num_blocks=st.num_blocks, src=st.src, key_offset=st.key_offset,
+        key_stride0=st.key_stride0, value_offset=st.value_offset,
+        value_stride0=st.value_stride0, slot_mapping=st.slot_mapping[:T],
+        k_scale=st.k_scale, v_scale=st.v_scale, layout=st.layout,
+        flags=st.flags)
+    n_seq = max(1, (ga.num_seqs * T) // st.num_tokens)
+    cu = ga.cu_seq_lens[: n_seq + 1].copy()
+    gsub = W.GatherWorkload(
+        name="sample", block_size=ga.block_size, head_dim=ga.head_dim,
+        num_blocks=ga.num_blocks, cache=ga.cache,
+        block_table=ga.block_table[:n_seq], cu_seq_lens=cu,
+        block_stride=ga.block_stride)
+    return sub, gsub
+
+
+def oracle_step(o, sub, gsub, cache, k, s):
+    o.store_nvfp4(sub.src, sub.key_stride0, sub.src, sub.value_stride0,
+                  sub.num_tokens, sub.num_heads, sub.head_size, cache, 0,
+                  sub.value_side_offset, sub.page_stride, sub.block_size,
+                  sub.num_blocks, sub.layout, sub.slot_mapping, sub.k_scale,
+                  sub.v_scale, sub.flags, key_base=sub.key_offset,
+                  value_base=sub.value_offset)
+    o.gather_indexer_k(gsub.cache, gsub.block_stride, gsub.num_blocks,
+                       gsub.block_size, gsub.head_dim, gsub.block_table,
+                       gsub.cu_seq_lens, gsub.total_tokens, k, s)
+
+
+def cpu_baseline(st, ga, sample_tokens):
+    import oracle
+    o = oracle.get()
+    sub, gsub = oracle_sample(st, ga, sample_tokens)
+    cache = np.full(sub.cache_bytes, 0xAA, dtype=np.uint8)
+    k = np.empty(gsub.total_tokens * gsub.head_dim, dtype=np.uint8)
+    s = np.empty(gsub.total_tokens * 4, dtype=np.uint8)
+    t = time.perf_counter()
+    oracle_step(o, sub, gsub, cache, k, s)
+    dt = time.perf_counter() - t
+    byts = sub.algorithmic_bytes() + gsub.algorithmic_bytes()
+    return {"value": round(byts / dt / 1e9, 4), "unit": "GB/s", "cores": 1,
+            "kind": "oracle",
+            "seconds": round(dt, 3),
+            "sample": f"first {sub.num_tokens} store tokens "
+                      f"({sub.num_tokens // 512} requests) and first "
+                      f"{gsub.num_seqs} gather sequences of the same "
+                      f"workload, single-threaded plain C oracle"}
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return  # the reference arm runs on rank 0 only
+    import oracle
+    st, ga = make_workload(0)
+    o = oracle.get()
+    sub, gsub = oracle_sample(st, ga, 4096)
+    cache = np.full(sub.cache_bytes, 0xAA, dtype=np.uint8)
+    k = np.empty(gsub.total_tokens * gsub.head_dim, dtype=np.uint8)
+    s = np.empty(gsub.total_tokens * 4, dtype=np.uint8)
+    for _ in range(max(args.warmup, 3)):
+        oracle_step(o, sub, gsub, cache, k, s)
+    t = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_step(o, sub, gsub, cache, k, s)
+    dt = (time.perf_counter() - t) / max(args.steps, 1)
+    byts = sub.algorithmic_bytes() + gsub.algorithmic_bytes()
+    val = round(byts / dt / 1e9, 4)
+    sample = (f"per step: first {sub.num_tokens} store tokens and first "
+              f"{gsub.num_seqs} gather sequences of the workload")
+    print(json.dumps({
+        "impl": "reference",
+        "metric": METRIC, "value": val, "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": max(args.warmup, 3),
+        "ms_per_step": round(dt * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD, "sample": sample},
+        "cpu_baseline": {"value": val, "unit": "GB/s", "cores": 1,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": val, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

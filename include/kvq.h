@@ -1,0 +1,180 @@
+/*
+ * kvq.h -- C ABI of libkvq: GB300 (sm_103a) kernels for the write and read
+ * hot path of a paged quantized KV cache.
+ *
+ * Two operations:
+ *
+ *   kvq_store_nvfp4       bf16 K/V -> NVFP4, scattered into paged cache pages
+ *                         (vLLM csrc/libtorch_stable/nvfp4_kv_cache_kernels.cu,
+ *                         commit 7ce4c8e: reshape_and_cache_nvfp4_kernel and
+ *                         reshape_and_cache_nvfp4_dispatch).
+ *   kvq_gather_indexer_k  fp8 indexer-K rows and per-token fp32 scales
+ *                         gathered out of a paged cache (vLLM PR #25931 "Add
+ *                         gather_indexer_k_quant_cache kernel"; PR #26456
+ *                         "[Deepseek-V3.2][Kernel] Integrate cuda indexer k
+ *                         cache gather").
+ *
+ * Conventions shared by every entry point:
+ *   - Every buffer pointer is DEVICE memory owned by the caller, on the
+ *     calling thread's current CUDA device.  The library never allocates,
+ *     frees or synchronises.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy
+ *     default stream).  A KVQ_OK return means the work was enqueued.
+ *   - Arguments are validated on the host without touching device memory;
+ *     a failed check returns an error code and launches nothing.  Nothing
+ *     throws across this boundary and no kernel traps.
+ *   - `dev_error` (nullable, device int32): kernels OR KVQ_DEVERR_* bits into
+ *     it when they meet an out-of-range slot, block id or sequence position;
+ *     the offending token is skipped, never written out of bounds.  The
+ *     caller zeroes it beforehand and reads it after synchronising.
+ */
+#ifndef KVQ_H
+#define KVQ_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  KVQ_OK = 0,
+  KVQ_ERR_NULL = -1,    /* a required pointer is NULL */
+  KVQ_ERR_SHAPE = -2,   /* a size is negative, zero where it cannot be, or
+                           breaks a divisibility rule */
+  KVQ_ERR_ALIGN = -3,   /* a pointer or stride breaks the 16-byte rule */
+  KVQ_ERR_DTYPE = -4,   /* unsupported input element type */
+  KVQ_ERR_LAYOUT = -5,  /* layout is neither HND nor NHD */
+  KVQ_ERR_CUDA = -6,    /* the CUDA runtime reported an error at launch */
+  KVQ_ERR_ARG = -7      /* unknown flag bits or inconsistent arguments */
+} kvq_status;
+
+/* Physical layout of one side (K or V) of a cache page. */
+enum {
+  KVQ_LAYOUT_HND = 0, /* data [H][B][D/2], scales [H][B][S]: per-head tiles */
+  KVQ_LAYOUT_NHD = 1  /* data [B][H][D/2], scales [B][H][S] */
+};
+
+/* Input element types. */
+enum { KVQ_DTYPE_BF16 = 0 };
+
+/* kvq_store_nvfp4 flags. */
+enum {
+  /* Also write K scales in the swizzled tile order (by default K scales are
+     linear and only V scales are swizzled, as the page's kernel does). */
+  KVQ_F_SWIZZLE_K_SCALE = 1u << 0
+};
+
+/* Bits OR-ed into *dev_error by the kernels. */
+enum {
+  KVQ_DEVERR_SLOT = 1 << 0,  /* slot >= num_blocks * block_size */
+  KVQ_DEVERR_BLOCK = 1 << 1, /* block-table entry outside [0, num_blocks) */
+  KVQ_DEVERR_SEQ = 1 << 2    /* position beyond max_blocks_per_seq * B, or an
+                                output row that no sequence covers, or
+                                cu_seq_lens[num_seqs] != total_tokens */
+};
+
+/*
+ * kvq_store_nvfp4 -- quantise bf16 K and V to NVFP4 and scatter them into
+ * paged cache pages by slot.  (vLLM nvfp4_kv_cache_kernels.cu, commit
+ * 7ce4c8e: reshape_and_cache_nvfp4_kernel, reshape_and_cache_nvfp4_dispatch.)
+ *
+ * For token t with s = slot_mapping[t] >= 0 (s < 0: the token is skipped and
+ * nothing of it is written), blk = s / block_size, off = s % block_size, for
+ * each side (K with g = 1/k_scale[0], V with g = 1/v_scale[0]), head h and
+ * 16-element group j of the head:
+ *   amax = max |x_i|;  sf = e4m3_rn_satfinite((amax / 6) * g)
+ *   q_i  = sf == 0 ? 0 : e2m1_rn_satfinite(x_i * (g / float(sf)))
+ * (fp32 IEEE divisions and products, no fused multiply-add), packed two codes
+ * per byte, element 2k in the low nibble of byte k.
+ *
+ * Page layout (side = key_cache or value_cache, i.e. kv_cache[:, 0] and
+ * kv_cache[:, 1]; page p of a side starts at side + p * page_stride):
+ *   [data: H*B*D/2 bytes | scales: H*B*S bytes], S = head_size / 16,
+ *   HND: data (h, off) row at h*B*D/2 + off*D/2, scale tile of head h at
+ *        D/2*H*B + h*B*S;  NHD: data row at off*H*D/2 + h*D/2, scale tile
+ *        of head h at D/2*H*B + h*S with rows H*S apart.
+ *   The 8 data bytes of group j sit at +8*j of the row.  Inside the head's
+ *   [B, S] scale tile, K scales are linear (row off, column j) unless
+ *   KVQ_F_SWIZZLE_K_SCALE; V scales are swizzled: row (off/4)*4 + j/(S/4),
+ *   column (j % (S/4))*4 + off % 4.
+ *   Bytes that no stored token owns are left unchanged.
+ *
+ * key, value      bf16 [num_tokens, num_heads, head_size]; heads and
+ *                 elements contiguous, rows key_stride0 / value_stride0
+ *                 ELEMENTS apart (>= 0, multiple of 8); 16-byte aligned.
+ * dtype           KVQ_DTYPE_BF16.
+ * key_cache, value_cache  page 0 of the K side and of the V side;
+ *                 16-byte aligned; page_stride multiple of 16 and
+ *                 >= H*B*(D/2 + S).
+ * block_size      multiple of 4;  head_size multiple of 64;
+ * num_blocks      pages in the cache (bounds check for slots).
+ * slot_mapping    int64 [num_tokens]; distinct non-negative slots
+ *                 (duplicates race; the result is then unspecified).
+ * k_scale, v_scale  device fp32 scalars, finite and > 0.
+ * flags           0 or KVQ_F_SWIZZLE_K_SCALE.
+ * dev_error       nullable device int32 (KVQ_DEVERR_SLOT).
+ * stream          cudaStream_t.
+ * num_tokens == 0 returns KVQ_OK without launching.
+ */
+kvq_status kvq_store_nvfp4(const void* key, int64_t key_stride0,
+                           const void* value, int64_t value_stride0,
+                           int32_t dtype, int32_t num_tokens,
+                           int32_t num_heads, int32_t head_size,
+                           uint8_t* key_cache, uint8_t* value_cache,
+                           int64_t page_stride, int32_t block_size,
+                           int64_t num_blocks, int32_t layout,
+                           const int64_t* slot_mapping, const float* k_scale,
+                           const float* v_scale, uint32_t flags,
+                           int32_t* dev_error, void* stream);
+
+/*
+ * kvq_gather_indexer_k -- gather fp8 indexer-K rows and their fp32 scales out
+ * of a paged cache into contiguous outputs.  (vLLM PR #25931
+ * cp_gather_indexer_k_quant_cache(kv_cache, k_fp8, k_scale, block_table,
+ * cu_seq_lens); PR #26456: k_scale is a byte buffer the consumer views as
+ * float32.)
+ *
+ * Block layout: [block_size*head_dim fp8 K | block_size * 4 scale bytes],
+ * blocks block_stride bytes apart.  For sequence b (0 <= b < num_seqs) and
+ * position p in [0, cu_seq_lens[b+1] - cu_seq_lens[b]), output row
+ * i = cu_seq_lens[b] + p receives, from blk = block_table[b *
+ * block_table_stride + p / block_size], off = p % block_size:
+ *   k_fp8[i*head_dim .. +head_dim) = K bytes of (blk, off)
+ *   k_scale[4*i .. +4)             = the 4 scale bytes of (blk, off)
+ * Rows are written for i < total_tokens only; scale bytes are copied raw.
+ *
+ * kv_cache        16-byte aligned; block_stride multiple of 16 and
+ *                 >= block_size * (head_dim + 4).
+ * head_dim        multiple of 16.   block_size > 0.
+ * block_table     int32, rows block_table_stride entries apart, first
+ *                 max_blocks_per_seq entries of each row used.
+ * cu_seq_lens     int32 [num_seqs + 1], non-decreasing, cu_seq_lens[0] == 0.
+ * total_tokens    cu_seq_lens[num_seqs], as known on the host (the kernel
+ *                 flags KVQ_DEVERR_SEQ if the two disagree).
+ * k_fp8           [total_tokens, head_dim] bytes, 16-byte aligned.
+ * k_scale         [total_tokens * 4] bytes, 4-byte aligned.
+ * dev_error       nullable device int32 (KVQ_DEVERR_BLOCK | KVQ_DEVERR_SEQ).
+ * total_tokens == 0 returns KVQ_OK without launching.
+ */
+kvq_status kvq_gather_indexer_k(const uint8_t* kv_cache, int64_t block_stride,
+                                int64_t num_blocks, int32_t block_size,
+                                int32_t head_dim, const int32_t* block_table,
+                                int64_t block_table_stride,
+                                int32_t max_blocks_per_seq,
+                                const int32_t* cu_seq_lens, int32_t num_seqs,
+                                int64_t total_tokens, uint8_t* k_fp8,
+                                uint8_t* k_scale, int32_t* dev_error,
+                                void* stream);
+
+/* Static text for a status code. */
+const char* kvq_status_string(kvq_status status);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int32_t kvq_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVQ_H */

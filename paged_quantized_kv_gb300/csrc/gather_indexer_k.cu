@@ -1,0 +1,159 @@
+// gather_indexer_k.cu -- paged fp8 indexer-K + fp32 scale gather, sm_103a.
+//
+// Operation: vLLM PR #25931 "Add gather_indexer_k_quant_cache kernel"
+// (cp_gather_indexer_k_quant_cache(kv_cache, k_fp8, k_scale, block_table,
+// cu_seq_lens)) and PR #26456 (k_scale handed on as raw bytes viewed as
+// float32).  Output row i = cu_seq_lens[b] + p takes the K row and the scale
+// of token p of sequence b from block block_table[b, p / B], offset p % B.
+// The first published version of this op launched too few blocks for long
+// sequences; here every output row belongs to exactly one warp unit, so the
+// grid covers total_tokens by construction.
+//
+// GB300 design: a pure copy, HBM-bound (2 x (D + 4) bytes per row).  One warp
+// owns 32 consecutive output rows: lane l resolves row r0 + l (binary search
+// in cu_seq_lens, one block-table read), then the warp moves the 32 rows as
+// 16-byte vectors -- every load of a unit is issued before its stores, so a
+// warp has 32 x D bytes in flight -- and each lane copies its row's 4 scale
+// bytes.  Destination rows are contiguous, so every store is a full sector.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "kvq_internal.h"
+#include "kvq.h"
+
+namespace kvq {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+
+__device__ __forceinline__ uint4 ld_nc_16(const void* p) {
+  uint4 v;
+  asm volatile(
+      "ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+      : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+      : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ void st_16(void* p, const uint4& v) {
+  asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p),
+               "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+               : "memory");
+}
+
+// Largest b in [0, n] with cu[b] <= r (cu[0] == 0 <= r).
+__device__ __forceinline__ int find_seq(const int32_t* cu, int n, int64_t r) {
+  int lo = 0, hi = n;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (static_cast<int64_t>(__ldg(cu + mid)) <= r)
+      lo = mid;
+    else
+      hi = mid - 1;
+  }
+  return lo;
+}
+
+// CPR = 16-byte chunks per K row (head_dim / 16); 0 = runtime value.
+template <int CPR>
+__global__ void __launch_bounds__(kThreads)
+gather_indexer_k_kernel(const GatherParams p) {
+  const int lane = threadIdx.x & 31;
+  const int64_t unit =
+      static_cast<int64_t>(blockIdx.x) * kWarps + (threadIdx.x >> 5);
+  const int64_t r0 = unit * 32;
+  if (r0 >= p.total) return;  // whole warp leaves together
+
+  if (unit == 0 && lane == 0 && p.dev_error != nullptr &&
+      static_cast<int64_t>(__ldg(p.cu + p.num_seqs)) != p.total)
+    atomicOr(p.dev_error, KVQ_DEVERR_SEQ);
+
+  // ---- resolve this lane's row ----------------------------------------
+  const int64_t r = r0 + lane;
+  const uint8_t* src_row = nullptr;
+  const uint8_t* src_scale = nullptr;
+  if (r < p.total) {
+    const int b = find_seq(p.cu, p.num_seqs, r);
+    int err = 0;
+    if (b >= p.num_seqs) {
+      err = KVQ_DEVERR_SEQ;  // no sequence covers this row
+    } else {
+      const int64_t pos64 = r - __ldg(p.cu + b);
+      const int32_t pos = static_cast<int32_t>(pos64);
+      const int32_t kb = pos / p.B;
+      const int32_t off = pos - kb * p.B;
+      if (pos64 < 0 || pos64 >= (int64_t{1} << 31) || kb >= p.max_blocks) {
+        err = KVQ_DEVERR_SEQ;
+      } else {
+        const int64_t blk = __ldg(p.block_table + b * p.bt_stride + kb);
+        if (blk < 0 || blk >= p.num_blocks) {
+          err = KVQ_DEVERR_BLOCK;
+        } else {
+          const uint8_t* base = p.cache + blk * p.block_stride;
+          src_row = base + static_cast<int64_t>(off) * p.D;
+          src_scale = base + static_cast<int64_t>(p.B) * p.D + off * 4;
+        }
+      }
+    }
+    if (err != 0 && p.dev_error != nullptr) atomicOr(p.dev_error, err);
+  }
+
+  // ---- copy the 32 K rows as 16-byte vectors ---------------------------
+  const int cpr = CPR > 0 ? CPR : (p.D >> 4);
+  const unsigned long long my_src =
+      reinterpret_cast<unsigned long long>(src_row);
+  if constexpr (CPR > 0) {
+    // all CPR loads of this lane first, then the stores
+    uint4 v[CPR];
+    const uint8_t* s[CPR];
+#pragma unroll
+    for (int i = 0; i < CPR; ++i) {
+      const int c = i * 32 + lane;
+      const int row = c / CPR;
+      s[i] = reinterpret_cast<const uint8_t*>(
+          __shfl_sync(0xFFFFFFFFu, my_src, row));
+      if (s[i] != nullptr) v[i] = ld_nc_16(s[i] + (c % CPR) * 16);
+    }
+#pragma unroll
+    for (int i = 0; i < CPR; ++i) {
+      const int c = i * 32 + lane;
+      const int row = c / CPR;
+      if (s[i] != nullptr)
+        st_16(p.k_fp8 + (r0 + row) * p.D + (c % CPR) * 16, v[i]);
+    }
+  } else {
+    for (int c = lane; c < 32 * cpr; c += 32) {
+      const int row = c / cpr;
+      const uint8_t* s = reinterpret_cast<const uint8_t*>(
+          __shfl_sync(0xFFFFFFFFu, my_src, row));
+      if (s != nullptr) {
+        const uint4 v = ld_nc_16(s + (c % cpr) * 16);
+        st_16(p.k_fp8 + (r0 + row) * p.D + (c % cpr) * 16, v);
+      }
+    }
+  }
+
+  // ---- the row's 4 scale bytes -----------------------------------------
+  if (src_scale != nullptr) {
+    const uint32_t sc = __ldg(reinterpret_cast<const uint32_t*>(src_scale));
+    *reinterpret_cast<uint32_t*>(p.k_scale + r * 4) = sc;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_gather_indexer_k(const GatherParams& p,
+                                    cudaStream_t stream) {
+  const int64_t units = (p.total + 31) / 32;
+  const int64_t grid = (units + kWarps - 1) / kWarps;
+  if (p.D == 128)
+    gather_indexer_k_kernel<8>
+        <<<static_cast<unsigned>(grid), kThreads, 0, stream>>>(p);
+  else
+    gather_indexer_k_kernel<0>
+        <<<static_cast<unsigned>(grid), kThreads, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace kvq

@@ -1,0 +1,62 @@
+// kvq_internal.h -- launch parameters and device helpers shared by the
+// libkvq translation units (not part of the public ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace kvq {
+
+// ---------------------------------------------------------------------------
+// NVFP4 store
+// ---------------------------------------------------------------------------
+struct StoreParams {
+  const uint16_t* src[2];  // key, value (bf16 bit patterns)
+  int64_t src_stride[2];   // row stride in elements
+  uint8_t* side[2];        // page 0 of the K side / V side
+  const int64_t* slots;
+  const float* scale[2];   // device k_scale / v_scale
+  int32_t* dev_error;      // nullable
+  int64_t page_stride;     // bytes
+  int64_t num_slots;       // num_blocks * block_size
+  int64_t data_per_side;   // H * B * D/2: offset of the scale region
+  int64_t dhs, dts;        // data head / token strides (bytes)
+  int64_t shs, sts;        // scale head / token strides (bytes)
+  int32_t num_tokens;
+  int32_t H, D, S, B;
+  int32_t b_shift;         // log2(B) when B is a power of two, else -1
+  int32_t cpt;             // 16-byte input chunks per token, both sides
+  int32_t tpp;             // tokens per pass (cpt <= 256: 256 / cpt)
+  int32_t slices_log2;     // passes per token = 1 << slices_log2
+  int32_t num_passes;
+  uint32_t swizzle_sides;  // bit s set: side s's scales are swizzled
+};
+
+cudaError_t launch_store_nvfp4(const StoreParams& p, cudaStream_t stream);
+
+// ---------------------------------------------------------------------------
+// Indexer-K gather
+// ---------------------------------------------------------------------------
+struct GatherParams {
+  const uint8_t* cache;
+  int64_t block_stride;
+  int64_t num_blocks;
+  const int32_t* block_table;
+  int64_t bt_stride;
+  const int32_t* cu;
+  uint8_t* k_fp8;
+  uint8_t* k_scale;
+  int32_t* dev_error;
+  int64_t total;
+  int32_t B, D;
+  int32_t max_blocks;
+  int32_t num_seqs;
+};
+
+cudaError_t launch_gather_indexer_k(const GatherParams& p,
+                                    cudaStream_t stream);
+
+// Streaming-multiprocessor count of the current device (cached per device).
+int sm_count();
+
+}  // namespace kvq
