@@ -337,3 +337,47 @@ def gather_workload(index: int, seed: int | None = None) -> GatherWorkload:
         return make_gather("long_gather", s, [512] * 256, 64, 128, 8192,
                            max_blocks=8)
     raise ValueError(f"workload {index} has no gather part")
+
+
+# --- sharding across ranks (data parallel, no exchange) ----------------------------
+
+def shard_range(n: int, rank: int, world: int):
+    """Contiguous [lo, hi) share of n units for one rank."""
+    lo = (n * rank) // world
+    hi = (n * (rank + 1)) // world
+    return lo, hi
+
+
+def shard_store(wl: StoreWorkload, rank: int, world: int,
+                unit_tokens: int = 1) -> StoreWorkload:
+    """The rank's share of a store: a contiguous range of units of
+    ``unit_tokens`` tokens (whole requests), same cache and scales."""
+    n_units = wl.num_tokens // unit_tokens
+    lo, hi = shard_range(n_units, rank, world)
+    t0, t1 = lo * unit_tokens, hi * unit_tokens
+    return StoreWorkload(
+        name=f"{wl.name}[{rank}/{world}]", num_tokens=t1 - t0,
+        num_heads=wl.num_heads, head_size=wl.head_size,
+        block_size=wl.block_size, num_blocks=wl.num_blocks, src=wl.src,
+        key_offset=wl.key_offset + t0 * wl.key_stride0,
+        key_stride0=wl.key_stride0,
+        value_offset=wl.value_offset + t0 * wl.value_stride0,
+        value_stride0=wl.value_stride0,
+        slot_mapping=wl.slot_mapping[t0:t1].copy(), k_scale=wl.k_scale,
+        v_scale=wl.v_scale, layout=wl.layout, flags=wl.flags,
+        page_stride=wl.page_stride)
+
+
+def shard_gather(wl: GatherWorkload, rank: int, world: int):
+    """The rank's share of a gather: a contiguous range of sequences, with
+    cu_seq_lens rebased to 0.  Returns (sub-workload, first output row)."""
+    lo, hi = shard_range(wl.num_seqs, rank, world)
+    cu = wl.cu_seq_lens[lo: hi + 1].astype(np.int64)
+    first = int(cu[0])
+    sub = GatherWorkload(
+        name=f"{wl.name}[{rank}/{world}]", block_size=wl.block_size,
+        head_dim=wl.head_dim, num_blocks=wl.num_blocks, cache=wl.cache,
+        block_table=wl.block_table[lo:hi].copy(),
+        cu_seq_lens=(cu - first).astype(np.int32),
+        block_stride=wl.block_stride)
+    return sub, first

@@ -42,10 +42,15 @@ def gpu_store(wl, sentinel=0xAA, slot_mapping=None):
     return kv.cpu().numpy().reshape(-1), int(err.item())
 
 
-def gpu_gather(wl, total=None, sentinel=0xCD, block_table=None):
+def gpu_gather(wl, total=None, sentinel=0xCD, block_table=None,
+               bt_cols=None):
+    """bt_cols: hand the kernel only the first bt_cols columns of the block
+    table (a view whose row stride is wider than its used part)."""
     total = wl.total_tokens if total is None else total
     cache = to_dev(wl.cache).view(wl.num_blocks, wl.block_stride)
     bt = to_dev(wl.block_table if block_table is None else block_table)
+    if bt_cols is not None:
+        bt = bt[:, :bt_cols]
     cu = to_dev(wl.cu_seq_lens)
     k = torch.full((max(total, 1), wl.head_dim), sentinel, dtype=torch.uint8,
                    device="cuda")[:total]
