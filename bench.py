@@ -53,6 +53,9 @@ def parse_args():
     ap.add_argument("--cpu-sample-tokens", type=int, default=65536)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--clock-window-s", type=float, default=1.5)
+    ap.add_argument("--kernel-only", choices=["store", "gather"],
+                    help="launch only this kernel (each launch after an L2 "
+                         "flush) and print its mean time; used for ncu")
     return ap.parse_args()
 
 
@@ -530,9 +533,69 @@ def run_reference(args):
     }), flush=True)
 
 
+def run_kernel_only(args):
+    """One kernel of the long-context mix, warmup + steps launches, each
+    after a 256 MiB L2 flush; prints the mean CUDA-event time."""
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    from paged_quantized_kv_gb300 import kvq
+    dev = torch.device("cuda", 0)
+    st, ga = make_workload(0)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    if args.kernel_only == "store":
+        T, H, D = st.num_tokens, st.num_heads, st.head_size
+        src = torch.from_numpy(st.src.view(np.int16)).to(dev).view(
+            torch.bfloat16)
+        key = src.as_strided((T, H, D), (st.key_stride0, D, 1),
+                             st.key_offset)
+        value = src.as_strided((T, H, D), (st.value_stride0, D, 1),
+                               st.value_offset)
+        slots = torch.from_numpy(st.slot_mapping).to(dev)
+        ks = torch.tensor([float(st.k_scale)], device=dev)
+        vs = torch.tensor([float(st.v_scale)], device=dev)
+        kv, kc, vc = kvq.alloc_nvfp4_cache(st.num_blocks, st.block_size, H,
+                                           D, device=dev, fill=0xAA)
+
+        def launch():
+            kvq.kvq_store_nvfp4(key, value, kc, vc, slots, ks, vs)
+        byts = st.algorithmic_bytes()
+    else:
+        gcache = torch.from_numpy(ga.cache).to(dev).view(ga.num_blocks, -1)
+        bt = torch.from_numpy(ga.block_table).to(dev)
+        cu = torch.from_numpy(ga.cu_seq_lens).to(dev)
+        n = ga.total_tokens
+        k_fp8 = torch.empty((n, ga.head_dim), dtype=torch.uint8, device=dev)
+        k_scale = torch.empty((n, 4), dtype=torch.uint8, device=dev)
+
+        def launch():
+            kvq.kvq_gather_indexer_k(gcache, k_fp8, k_scale, bt, cu,
+                                     block_size=ga.block_size)
+        byts = ga.algorithmic_bytes()
+    for i in range(args.warmup):
+        flush.fill_(i & 0xFF)
+        launch()
+    ms = []
+    for i in range(args.steps):
+        flush.fill_(i & 0xFF)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        launch()
+        e1.record()
+        torch.cuda.synchronize()
+        ms.append(e0.elapsed_time(e1))
+    mean = statistics.fmean(ms)
+    print(json.dumps({"kernel": args.kernel_only, "ms": round(mean, 5),
+                      "GB_s": round(byts / (mean / 1e3) / 1e9, 1),
+                      "launches": args.warmup + args.steps}), flush=True)
+
+
 def main():
     args = parse_args()
-    if args.impl == "reference":
+    if args.kernel_only:
+        run_kernel_only(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)
