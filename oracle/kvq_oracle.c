@@ -96,19 +96,20 @@ double kvqo_e2m1_decode(uint8_t nibble) {
 }
 
 /* e4m3 round-to-nearest-even, satfinite; the sign of v (including -0) is
- * kept.  Non-finite input returns 0x7F (NaN code). */
+ * kept.  Saturation covers infinities (+-inf -> +-448); NaN returns 0x7F. */
 uint8_t kvqo_e4m3_encode(float v) {
   build_tables();
-  if (!isfinite(v)) return 0x7F;
+  if (isnan(v)) return 0x7F;
   int mag = encode_magnitude(fabs((double)v), e4m3_val, 127);
   return (uint8_t)((signbit(v) ? 0x80 : 0x00) | mag);
 }
 
 /* e2m1 round-to-nearest-even, satfinite; the sign of v (including -0) is
- * kept in bit 3.  Non-finite input returns 0xF. */
+ * kept in bit 3.  Saturation covers infinities (+-inf -> +-6); e2m1 has no
+ * NaN, so NaN input returns 0xF. */
 uint8_t kvqo_e2m1_encode(float v) {
   build_tables();
-  if (!isfinite(v)) return 0xF;
+  if (isnan(v)) return 0xF;
   int mag = encode_magnitude(fabs((double)v), e2m1_val, 8);
   return (uint8_t)((signbit(v) ? 0x8 : 0x0) | mag);
 }

@@ -71,8 +71,8 @@ kvq_status kvq_store_nvfp4(const void* key, int64_t key_stride0,
   const int64_t side_bytes = H * B * (D / 2 + S);
   if (page_stride < side_bytes) return KVQ_ERR_SHAPE;
   if (key_stride0 < 0 || value_stride0 < 0) return KVQ_ERR_SHAPE;
-  const int64_t cpt = 2 * H * D / 8;  // 16-byte chunks per token
-  if (cpt > (int64_t{1} << 20)) return KVQ_ERR_SHAPE;
+  const int64_t gpt = 2 * H * D / 16;  // 16-element groups per token
+  if (gpt > (int64_t{1} << 20)) return KVQ_ERR_SHAPE;
   if (num_tokens == 0) return KVQ_OK;
 
   if (key == nullptr || value == nullptr || key_cache == nullptr ||
@@ -117,14 +117,14 @@ kvq_status kvq_store_nvfp4(const void* key, int64_t key_stride0,
   p.S = static_cast<int32_t>(S);
   p.B = block_size;
   p.b_shift = ilog2_exact(B);
-  p.cpt = static_cast<int32_t>(cpt);
-  if (cpt <= 256) {
-    p.tpp = static_cast<int32_t>(256 / cpt);
+  p.gpt = static_cast<int32_t>(gpt);
+  if (gpt <= 256) {
+    p.tpp = static_cast<int32_t>(256 / gpt);
     p.slices_log2 = 0;
   } else {
     p.tpp = 1;
     int sl = 0;
-    while ((int64_t{256} << sl) < cpt) ++sl;
+    while ((int64_t{256} << sl) < gpt) ++sl;
     p.slices_log2 = sl;
   }
   const int64_t passes =

@@ -25,8 +25,8 @@ struct StoreParams {
   int32_t num_tokens;
   int32_t H, D, S, B;
   int32_t b_shift;         // log2(B) when B is a power of two, else -1
-  int32_t cpt;             // 16-byte input chunks per token, both sides
-  int32_t tpp;             // tokens per pass (cpt <= 256: 256 / cpt)
+  int32_t gpt;             // 16-element groups per token, both sides
+  int32_t tpp;             // tokens per pass (gpt <= 256: 256 / gpt)
   int32_t slices_log2;     // passes per token = 1 << slices_log2
   int32_t num_passes;
   uint32_t swizzle_sides;  // bit s set: side s's scales are swizzled

@@ -9,23 +9,28 @@
 // [block_size, S] tile.
 //
 // GB300 design (this file's own, not the page's one-CTA-per-token loop):
-//   * HBM-bound: ~2 B read per element, 0.5625 B written.  The grid is
-//     persistent (a multiple of the SM count x resident CTAs); every thread
-//     owns one fixed 16-byte chunk "role" (side, head, group half) of a token
-//     and walks tokens with a grid stride, issuing UNROLL independent 16-byte
-//     streaming loads before using any of them, so each SM keeps tens of KB
-//     of reads in flight.
-//   * A 16-element group is two adjacent lanes (8 bf16 = one 16-byte load
-//     each); amax is a packed unsigned max on the sign-cleared bf16 bits
-//     (non-negative bf16 order == integer order) plus one xor-1 shuffle.
+//   * HBM-bound at ~2.6 B per element, so the budget is instructions per
+//     byte: the grid is persistent (SMs x resident CTAs) and every thread
+//     owns one fixed 16-element group "role" (side, head, group) of a token,
+//     computes all role addresses once and walks tokens with a grid stride,
+//     issuing kUnroll independent loads (one 256-bit load per group when the
+//     rows are 32-byte aligned) before using any of them.
+//   * amax: sign bits cleared, a tree of max.bf16x2, one final max.
+//   * amax / 6 in three instructions that equal the IEEE quotient for every
+//     finite bf16 amax: q0 = amax * RN(1/6), the exact residual
+//     r = fma(-q0, 6, amax), q = fma(r, RN(1/6), q0) -- the quotient
+//     correction step of P. Markstein, "Computation of elementary functions
+//     on the IBM RISC System/6000 processor", IBM J. Res. Dev. 34(1), 1990;
+//     checked exhaustively over all 32640 finite non-negative bf16 values by
+//     tests/test_div6.py.
 //   * g = 1/k_scale and g / float(sf) are IEEE divisions; the second one is
-//     taken from a 2 x 256-entry shared-memory table filled once per CTA with
-//     __fdiv_rn (exactly the per-group IEEE quotient, since sf has only 256
-//     codes), so the hot loop holds one division (amax / 6).
-//   * e4m3 and e2m1 codes come from the sm_100-family cvt instructions
-//     (cvt.rn.satfinite.{e4m3x2,e2m1x2}.f32), round-to-nearest-even.
-//   * Each lane stores its 4 packed bytes (a warp writes whole 32-byte
-//     sectors of a head row); the even lane of a pair stores the scale byte.
+//     read from a 2 x 256 shared-memory table filled once per CTA with
+//     __fdiv_rn (exactly the per-group quotient, since sf has 256 codes).
+//   * x * r as packed mul.rn.f32x2 (two IEEE products per instruction), codes
+//     from cvt.rn.satfinite.e2m1x2.f32 / cvt.rn.satfinite.e4m3x2.f32; the
+//     sf == 0 case is a select.
+//   * Each thread stores its group's 8 data bytes (a warp writes whole
+//     sectors of head rows) and its scale byte.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -37,20 +42,41 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kUnroll = 4;
+constexpr uint32_t kInv6Bits = 0x3E2AAAABu;  // RN(1/6) in fp32
 
-__device__ __forceinline__ uint4 ld_stream_16(const void* p) {
-  uint4 v;
-  asm volatile(
-      "ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
-      : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-      : "l"(p));
-  return v;
+// 16 bf16 of one group into w[0..7] (element 2k in the low half of w[k]).
+template <bool kVec32>
+__device__ __forceinline__ void load_group(const uint16_t* p,
+                                           uint32_t (&w)[8]) {
+  if constexpr (kVec32) {
+    asm volatile(
+        "ld.global.nc.L1::no_allocate.v8.u32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+        : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]), "=r"(w[4]),
+          "=r"(w[5]), "=r"(w[6]), "=r"(w[7])
+        : "l"(p));
+  } else {
+    asm volatile(
+        "ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+        : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
+        : "l"(p));
+    asm volatile(
+        "ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+        : "=r"(w[4]), "=r"(w[5]), "=r"(w[6]), "=r"(w[7])
+        : "l"(p + 8));
+  }
 }
 
 __device__ __forceinline__ int64_t ld_nc_s64(const int64_t* p) {
   int64_t v;
   asm volatile("ld.global.nc.s64 %0, [%1];" : "=l"(v) : "l"(p));
   return v;
+}
+
+__device__ __forceinline__ uint32_t bf16x2_max(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
 }
 
 // e4m3 code -> fp32 (exact: every e4m3 value is an f16 value).
@@ -72,31 +98,44 @@ __device__ __forceinline__ uint32_t float_to_e4m3(float v) {
   uint16_t pair;
   asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(pair) : "f"(0.0f),
       "f"(v));
-  return pair & 0xFFu;  // second operand lands in the low byte
+  return pair & 0xFFu;  // the second operand lands in the low byte
 }
 
-// Eight fp32 -> eight e2m1 codes, element 2k in the low nibble of byte k.
-__device__ __forceinline__ uint32_t pack_e2m1x8(const float (&y)[8]) {
+// Four packed bf16 pairs times r (IEEE fp32 products, two per mul.f32x2)
+// -> four bytes of e2m1 codes, element 2k in the low nibble of byte k.
+__device__ __forceinline__ uint32_t quant4(uint32_t w0, uint32_t w1,
+                                           uint32_t w2, uint32_t w3,
+                                           uint64_t rr) {
   uint32_t out;
-  asm("{ .reg .b8 b0, b1, b2, b3;\n"
-      "  cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n"
-      "  cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n"
-      "  cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n"
-      "  cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n"
+  asm("{ .reg .b32 l0, h0, l1, h1, l2, h2, l3, h3;\n"
+      "  .reg .b64 x0, x1, x2, x3;\n"
+      "  .reg .b8 b0, b1, b2, b3;\n"
+      "  shl.b32 l0, %1, 16;  and.b32 h0, %1, 0xFFFF0000;\n"
+      "  shl.b32 l1, %2, 16;  and.b32 h1, %2, 0xFFFF0000;\n"
+      "  shl.b32 l2, %3, 16;  and.b32 h2, %3, 0xFFFF0000;\n"
+      "  shl.b32 l3, %4, 16;  and.b32 h3, %4, 0xFFFF0000;\n"
+      "  mov.b64 x0, {l0, h0};  mov.b64 x1, {l1, h1};\n"
+      "  mov.b64 x2, {l2, h2};  mov.b64 x3, {l3, h3};\n"
+      "  mul.rn.f32x2 x0, x0, %5;  mul.rn.f32x2 x1, x1, %5;\n"
+      "  mul.rn.f32x2 x2, x2, %5;  mul.rn.f32x2 x3, x3, %5;\n"
+      "  mov.b64 {l0, h0}, x0;  mov.b64 {l1, h1}, x1;\n"
+      "  mov.b64 {l2, h2}, x2;  mov.b64 {l3, h3}, x3;\n"
+      "  cvt.rn.satfinite.e2m1x2.f32 b0, h0, l0;\n"
+      "  cvt.rn.satfinite.e2m1x2.f32 b1, h1, l1;\n"
+      "  cvt.rn.satfinite.e2m1x2.f32 b2, h2, l2;\n"
+      "  cvt.rn.satfinite.e2m1x2.f32 b3, h3, l3;\n"
       "  mov.b32 %0, {b0, b1, b2, b3}; }"
       : "=r"(out)
-      : "f"(y[0]), "f"(y[1]), "f"(y[2]), "f"(y[3]), "f"(y[4]), "f"(y[5]),
-        "f"(y[6]), "f"(y[7]));
+      : "r"(w0), "r"(w1), "r"(w2), "r"(w3), "l"(rr));
   return out;
 }
 
-__device__ __forceinline__ float bf16_lo(uint32_t w) {
-  return __uint_as_float(w << 16);
-}
-__device__ __forceinline__ float bf16_hi(uint32_t w) {
-  return __uint_as_float(w & 0xFFFF0000u);
+__device__ __forceinline__ void st_v2(uint8_t* p, uint32_t a, uint32_t b) {
+  asm volatile("st.global.v2.u32 [%0], {%1, %2};" ::"l"(p), "r"(a), "r"(b)
+               : "memory");
 }
 
+template <bool kVec32>
 __global__ void __launch_bounds__(kThreads)
 store_nvfp4_kernel(const StoreParams p) {
   __shared__ float s_ratio[2][256];  // g_side / float(e4m3 code)
@@ -116,87 +155,81 @@ store_nvfp4_kernel(const StoreParams p) {
 
   // ---- this thread's fixed role inside a token ---------------------------
   const int slices = 1 << p.slices_log2;
-  int chunk, tok_sub;
+  int grp_in_tok, tok_sub;
   if (slices == 1) {
-    tok_sub = tid / p.cpt;
-    chunk = tid - tok_sub * p.cpt;
+    tok_sub = tid / p.gpt;
+    grp_in_tok = tid - tok_sub * p.gpt;
   } else {
     tok_sub = 0;
-    chunk = (static_cast<int>(blockIdx.x) & (slices - 1)) * kThreads + tid;
+    grp_in_tok = (static_cast<int>(blockIdx.x) & (slices - 1)) * kThreads + tid;
   }
-  const bool role_ok = (tok_sub < p.tpp) && (chunk < p.cpt);
-  const int cps = p.cpt >> 1;          // chunks per side
-  const int side = chunk >= cps ? 1 : 0;
-  const int e = chunk - side * cps;
-  const int cph = p.D >> 3;            // chunks per head
-  const int head = e / cph;
-  const int ch = e - head * cph;
-  const int grp = ch >> 1;
-  const int half = ch & 1;
+  if (tok_sub >= p.tpp || grp_in_tok >= p.gpt) return;  // idle role
+  const int gps = p.gpt >> 1;  // groups per side
+  const int side = grp_in_tok >= gps ? 1 : 0;
+  const int e = grp_in_tok - side * gps;
+  const int head = e / p.S;  // S = groups per head
+  const int j = e - head * p.S;
   const int q = p.S >> 2;
   const bool swz = (p.swizzle_sides >> side) & 1u;
 
-  const uint16_t* src_base = p.src[side] + head * p.D + ch * 8;
+  const uint16_t* const src_role = p.src[side] + head * p.D + j * 16;
   const int64_t src_stride = p.src_stride[side];
-  uint8_t* const data_base = p.side[side] + head * p.dhs + grp * 8 + half * 4;
-  uint8_t* const scale_base =
+  uint8_t* const data_role = p.side[side] + head * p.dhs + j * 8;
+  uint8_t* const scale_role =
       p.side[side] + p.data_per_side + head * p.shs +
-      (swz ? (grp / q) * p.sts + (grp % q) * 4 : static_cast<int64_t>(grp));
-  const float* ratio = s_ratio[side];
+      (swz ? (j / q) * p.sts + (j % q) * 4 : static_cast<int64_t>(j));
+  const float* const ratio = s_ratio[side];
   const float g = __fdiv_rn(1.0f, __ldg(p.scale[side]));
+  const float inv6 = __uint_as_float(kInv6Bits);
 
-  const int grid = gridDim.x;
-  for (int p0 = blockIdx.x; p0 < p.num_passes; p0 += kUnroll * grid) {
-    uint4 raw[kUnroll];
+  const int64_t T = p.num_tokens;
+  const int64_t tstep =
+      static_cast<int64_t>(gridDim.x >> p.slices_log2) * p.tpp;
+  for (int64_t t0 = static_cast<int64_t>(blockIdx.x >> p.slices_log2) *
+                        p.tpp + tok_sub;
+       t0 < T; t0 += kUnroll * tstep) {
+    uint32_t w[kUnroll][8];
     int64_t slot[kUnroll];
-    bool act[kUnroll];
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
-      const int pass = p0 + u * grid;
-      const int t = (pass >> p.slices_log2) * p.tpp + tok_sub;
-      act[u] = role_ok && pass < p.num_passes && t < p.num_tokens;
-      raw[u] = make_uint4(0u, 0u, 0u, 0u);
+      const int64_t t = t0 + u * tstep;
       slot[u] = -1;
-      if (act[u]) {
+      if (t < T) {
         slot[u] = ld_nc_s64(p.slots + t);
-        raw[u] = ld_stream_16(src_base + static_cast<int64_t>(t) * src_stride);
+        load_group<kVec32>(src_role + t * src_stride, w[u]);
       }
     }
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
-      // group amax over the lane pair (all lanes take part in the shuffle)
-      const uint32_t m01 = __vmaxu2(raw[u].x & 0x7FFF7FFFu,
-                                    raw[u].y & 0x7FFF7FFFu);
-      const uint32_t m23 = __vmaxu2(raw[u].z & 0x7FFF7FFFu,
-                                    raw[u].w & 0x7FFF7FFFu);
-      const uint32_t m = __vmaxu2(m01, m23);
-      uint32_t a = max(m & 0xFFFFu, m >> 16);
-      a = max(a, __shfl_xor_sync(0xFFFFFFFFu, a, 1));
-
-      if (!act[u] || slot[u] < 0) continue;
+      if (slot[u] < 0) continue;  // skipped token, or past the end
       if (slot[u] >= p.num_slots) {
-        if (p.dev_error != nullptr && half == 0)
-          atomicOr(p.dev_error, KVQ_DEVERR_SLOT);
+        if (p.dev_error != nullptr) atomicOr(p.dev_error, KVQ_DEVERR_SLOT);
         continue;
       }
-      const float amax = __uint_as_float(a << 16);
-      const float sfv = __fmul_rn(__fdiv_rn(amax, 6.0f), g);
-      const uint32_t sf = float_to_e4m3(sfv);
+      // amax of the 16 magnitudes
+      const uint32_t m =
+          bf16x2_max(bf16x2_max(bf16x2_max(w[u][0] & 0x7FFF7FFFu,
+                                           w[u][1] & 0x7FFF7FFFu),
+                                bf16x2_max(w[u][2] & 0x7FFF7FFFu,
+                                           w[u][3] & 0x7FFF7FFFu)),
+                     bf16x2_max(bf16x2_max(w[u][4] & 0x7FFF7FFFu,
+                                           w[u][5] & 0x7FFF7FFFu),
+                                bf16x2_max(w[u][6] & 0x7FFF7FFFu,
+                                           w[u][7] & 0x7FFF7FFFu)));
+      const float amax = __uint_as_float(bf16x2_max(m, m >> 16) << 16);
+      // IEEE amax / 6 (see the header comment), then * g
+      const float q0 = __fmul_rn(amax, inv6);
+      const float res = __fmaf_rn(-q0, 6.0f, amax);
+      const float d6 = __fmaf_rn(res, inv6, q0);
+      const uint32_t sf = float_to_e4m3(__fmul_rn(d6, g));
+      const float r = ratio[sf];
+      const uint64_t rr = (static_cast<uint64_t>(__float_as_uint(r)) << 32) |
+                          __float_as_uint(r);
+      uint32_t lo = quant4(w[u][0], w[u][1], w[u][2], w[u][3], rr);
+      uint32_t hi = quant4(w[u][4], w[u][5], w[u][6], w[u][7], rr);
+      lo = sf != 0u ? lo : 0u;
+      hi = sf != 0u ? hi : 0u;
 
-      uint32_t packed = 0u;
-      if (sf != 0u) {
-        const float r = ratio[sf];
-        float y[8];
-        y[0] = __fmul_rn(bf16_lo(raw[u].x), r);
-        y[1] = __fmul_rn(bf16_hi(raw[u].x), r);
-        y[2] = __fmul_rn(bf16_lo(raw[u].y), r);
-        y[3] = __fmul_rn(bf16_hi(raw[u].y), r);
-        y[4] = __fmul_rn(bf16_lo(raw[u].z), r);
-        y[5] = __fmul_rn(bf16_hi(raw[u].z), r);
-        y[6] = __fmul_rn(bf16_lo(raw[u].w), r);
-        y[7] = __fmul_rn(bf16_hi(raw[u].w), r);
-        packed = pack_e2m1x8(y);
-      }
       int64_t blk, off;
       if (p.b_shift >= 0) {
         blk = slot[u] >> p.b_shift;
@@ -206,19 +239,16 @@ store_nvfp4_kernel(const StoreParams p) {
         off = slot[u] - blk * p.B;
       }
       const int64_t page = blk * p.page_stride;
-      *reinterpret_cast<uint32_t*>(data_base + page + off * p.dts) = packed;
-      if (half == 0) {
-        const int64_t soff = swz ? (off & ~int64_t{3}) * p.sts + (off & 3)
-                                 : off * p.sts;
-        scale_base[page + soff] = static_cast<uint8_t>(sf);
-      }
+      st_v2(data_role + page + off * p.dts, lo, hi);
+      const int64_t soff =
+          swz ? (off & ~int64_t{3}) * p.sts + (off & 3) : off * p.sts;
+      scale_role[page + soff] = static_cast<uint8_t>(sf);
     }
   }
 }
 
-}  // namespace
-
-cudaError_t launch_store_nvfp4(const StoreParams& p, cudaStream_t stream) {
+template <bool kVec32>
+cudaError_t launch(const StoreParams& p, cudaStream_t stream) {
   static int ctas_per_sm[64] = {0};
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
@@ -226,7 +256,7 @@ cudaError_t launch_store_nvfp4(const StoreParams& p, cudaStream_t stream) {
   int& occ = ctas_per_sm[dev & 63];
   if (occ == 0) {
     err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-        &occ, store_nvfp4_kernel, kThreads, 0);
+        &occ, store_nvfp4_kernel<kVec32>, kThreads, 0);
     if (err != cudaSuccess) return err;
     if (occ < 1) occ = 1;
   }
@@ -235,8 +265,20 @@ cudaError_t launch_store_nvfp4(const StoreParams& p, cudaStream_t stream) {
   if (grid > p.num_passes) grid = p.num_passes;
   grid = (grid / slices) * slices;  // every CTA keeps one slice of a token
   if (grid < slices) grid = slices;
-  store_nvfp4_kernel<<<static_cast<unsigned>(grid), kThreads, 0, stream>>>(p);
+  store_nvfp4_kernel<kVec32>
+      <<<static_cast<unsigned>(grid), kThreads, 0, stream>>>(p);
   return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_store_nvfp4(const StoreParams& p, cudaStream_t stream) {
+  // 256-bit loads need every group start 32-byte aligned
+  const bool vec32 =
+      (reinterpret_cast<uintptr_t>(p.src[0]) % 32 == 0) &&
+      (reinterpret_cast<uintptr_t>(p.src[1]) % 32 == 0) &&
+      (p.src_stride[0] % 16 == 0) && (p.src_stride[1] % 16 == 0);
+  return vec32 ? launch<true>(p, stream) : launch<false>(p, stream);
 }
 
 }  // namespace kvq

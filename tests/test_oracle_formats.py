@@ -68,6 +68,10 @@ def check_e4m3_encode(o):
         assert o.e4m3_encode(v) == 0x7E
         assert o.e4m3_encode(-v) == 0xFE
     assert o.e4m3_encode(-0.0) == 0x80
+    # satfinite covers infinities; NaN stays NaN
+    assert o.e4m3_encode(float("inf")) == 0x7E
+    assert o.e4m3_encode(float("-inf")) == 0xFE
+    assert o.e4m3_encode(float("nan")) & 0x7F == 0x7F
     # every finite code round-trips
     for c in list(range(0x7F)) + list(range(0x80, 0xFF)):
         assert o.e4m3_encode(o.e4m3_decode(c)) == c
@@ -111,6 +115,8 @@ def check_e2m1_encode(o):
     rng = np.random.default_rng(12)
     for p in e2m1_sweep(rng):
         assert o.e2m1_encode(p) == e2m1_closed_form(p), float(p)
+    assert o.e2m1_encode(float("inf")) == 0x7
+    assert o.e2m1_encode(float("-inf")) == 0xF
 
 
 def check_swizzle_golden(o):

@@ -148,6 +148,21 @@ def test_e4m3_boundaries(orc):
     _probe_store(orc, groups, 1.0)
 
 
+@pytest.mark.parametrize("scale", [1.0, 0.37, 2.0 ** -20])
+def test_every_bf16_amax(orc, scale):
+    """One group per finite non-negative bf16 amax (32640 groups): covers the
+    kernel's division-free amax / 6 on every value it can see, and with
+    k_scale = 2^-20 the overflow of (amax/6)*g to +inf (saturates to 448)."""
+    bits = np.arange(0, 0x7F80, dtype=np.uint32)
+    a = (bits << 16).view(np.float32)
+    groups = np.zeros((a.size, 16), np.float32)
+    groups[:, 0] = a
+    groups[:, 5] = -a * np.float32(0.375)
+    groups[:, 11] = a * np.float32(0.5)
+    groups[:, 14] = -a
+    _probe_store(orc, groups, scale)
+
+
 def _probe_store(orc, groups, scale):
     """Store each 16-value group as one head of one token (H=1, D=16*...)."""
     n = groups.shape[0]
