@@ -9,12 +9,18 @@
 // sequences; here every output row belongs to exactly one warp unit, so the
 // grid covers total_tokens by construction.
 //
-// GB300 design: a pure copy, HBM-bound (2 x (D + 4) bytes per row).  One warp
-// owns 32 consecutive output rows: lane l resolves row r0 + l (binary search
-// in cu_seq_lens, one block-table read), then the warp moves the 32 rows as
-// 16-byte vectors -- every load of a unit is issued before its stores, so a
-// warp has 32 x D bytes in flight -- and each lane copies its row's 4 scale
-// bytes.  Destination rows are contiguous, so every store is a full sector.
+// GB300 design: a pure copy, HBM-bound (2 x (D + 4) bytes per row), whose
+// time is dominated by the dependent-load chain before the first row load
+// (cu_seq_lens -> block_table -> K rows), since the whole grid fits in one
+// wave.  Each CTA first stages cu_seq_lens in shared memory with one
+// coalesced load (when it fits in 48 KB; otherwise the search reads global
+// memory), so the per-row binary search costs one DRAM latency instead of
+// one per search level.  One warp owns 32 consecutive output rows: lane l
+// resolves row r0 + l (search, one block-table read, bounds checks), then the
+// warp moves the 32 rows as 16-byte vectors -- every load of a unit issued
+// before its stores, 32 x D bytes in flight per warp -- and each lane copies
+// its row's 4 scale bytes.  Destination rows are contiguous, so every store
+// is a full sector.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -42,12 +48,15 @@ __device__ __forceinline__ void st_16(void* p, const uint4& v) {
                : "memory");
 }
 
-// Largest b in [0, n] with cu[b] <= r (cu[0] == 0 <= r).
+// Largest b in [0, n] with cu[b] <= r (cu[0] == 0 <= r); cu in shared
+// memory (kShared) or global memory.
+template <bool kShared>
 __device__ __forceinline__ int find_seq(const int32_t* cu, int n, int64_t r) {
   int lo = 0, hi = n;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
-    if (static_cast<int64_t>(__ldg(cu + mid)) <= r)
+    const int32_t v = kShared ? cu[mid] : __ldg(cu + mid);
+    if (static_cast<int64_t>(v) <= r)
       lo = mid;
     else
       hi = mid - 1;
@@ -55,10 +64,22 @@ __device__ __forceinline__ int find_seq(const int32_t* cu, int n, int64_t r) {
   return lo;
 }
 
+// cu_seq_lens entries staged in shared memory at most (48 KB, no opt-in).
+constexpr int kMaxSharedCu = 12288;
+
 // CPR = 16-byte chunks per K row (head_dim / 16); 0 = runtime value.
-template <int CPR>
+// kSharedCu: cu_seq_lens is staged in dynamic shared memory.
+template <int CPR, bool kSharedCu>
 __global__ void __launch_bounds__(kThreads)
 gather_indexer_k_kernel(const GatherParams p) {
+  extern __shared__ int32_t s_cu[];
+  const int32_t* cu = p.cu;
+  if constexpr (kSharedCu) {
+    for (int i = threadIdx.x; i <= p.num_seqs; i += kThreads)
+      s_cu[i] = __ldg(p.cu + i);
+    __syncthreads();
+    cu = s_cu;
+  }
   const int lane = threadIdx.x & 31;
   const int64_t unit =
       static_cast<int64_t>(blockIdx.x) * kWarps + (threadIdx.x >> 5);
@@ -66,7 +87,7 @@ gather_indexer_k_kernel(const GatherParams p) {
   if (r0 >= p.total) return;  // whole warp leaves together
 
   if (unit == 0 && lane == 0 && p.dev_error != nullptr &&
-      static_cast<int64_t>(__ldg(p.cu + p.num_seqs)) != p.total)
+      static_cast<int64_t>(cu[p.num_seqs]) != p.total)
     atomicOr(p.dev_error, KVQ_DEVERR_SEQ);
 
   // ---- resolve this lane's row ----------------------------------------
@@ -74,12 +95,12 @@ gather_indexer_k_kernel(const GatherParams p) {
   const uint8_t* src_row = nullptr;
   const uint8_t* src_scale = nullptr;
   if (r < p.total) {
-    const int b = find_seq(p.cu, p.num_seqs, r);
+    const int b = find_seq<kSharedCu>(cu, p.num_seqs, r);
     int err = 0;
     if (b >= p.num_seqs) {
       err = KVQ_DEVERR_SEQ;  // no sequence covers this row
     } else {
-      const int64_t pos64 = r - __ldg(p.cu + b);
+      const int64_t pos64 = r - cu[b];
       const int32_t pos = static_cast<int32_t>(pos64);
       const int32_t kb = pos / p.B;
       const int32_t off = pos - kb * p.B;
@@ -141,18 +162,26 @@ gather_indexer_k_kernel(const GatherParams p) {
   }
 }
 
+template <int CPR>
+void launch_cpr(const GatherParams& p, unsigned grid, cudaStream_t stream) {
+  if (p.num_seqs + 1 <= kMaxSharedCu) {
+    const size_t smem = static_cast<size_t>(p.num_seqs + 1) * sizeof(int32_t);
+    gather_indexer_k_kernel<CPR, true><<<grid, kThreads, smem, stream>>>(p);
+  } else {
+    gather_indexer_k_kernel<CPR, false><<<grid, kThreads, 0, stream>>>(p);
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_gather_indexer_k(const GatherParams& p,
                                     cudaStream_t stream) {
   const int64_t units = (p.total + 31) / 32;
-  const int64_t grid = (units + kWarps - 1) / kWarps;
+  const unsigned grid = static_cast<unsigned>((units + kWarps - 1) / kWarps);
   if (p.D == 128)
-    gather_indexer_k_kernel<8>
-        <<<static_cast<unsigned>(grid), kThreads, 0, stream>>>(p);
+    launch_cpr<8>(p, grid, stream);
   else
-    gather_indexer_k_kernel<0>
-        <<<static_cast<unsigned>(grid), kThreads, 0, stream>>>(p);
+    launch_cpr<0>(p, grid, stream);
   return cudaGetLastError();
 }
 

@@ -41,6 +41,9 @@ CASES = [
     ("d256_wide_table", [90, 17], 16, 256, 30, 12),  # kernel sees 6 cols
     ("single_token", [1], 64, 128, 2, 0),
     ("many_short", [3] * 200, 4, 16, 400, 0),
+    # more sequences than fit in the kernel's shared-memory copy of
+    # cu_seq_lens: the search reads global memory instead
+    ("many_seqs_global_cu", [1, 2, 0, 3] * 3300, 16, 16, 13300, 0),
 ]
 
 
