@@ -43,15 +43,21 @@ def _stale() -> bool:
     return any(os.path.getmtime(d) > t for d in _inputs())
 
 
-def build(force: bool = False, ptxas_verbose: bool = False) -> str:
-    if not force and not _stale():
+def build(force: bool = False, ptxas_verbose: bool = False,
+          defines: dict | None = None, out: str | None = None) -> str:
+    """Build libkvq.so (or ``out``) if stale; ``defines`` are passed to nvcc
+    as -DNAME=VALUE (tuning knobs of the kernels; defaults otherwise)."""
+    lib = out or LIB
+    if not force and not defines and out is None and not _stale():
         return LIB
-    os.makedirs(BUILD, exist_ok=True)
+    bdir = BUILD if out is None else out + ".build"
+    os.makedirs(bdir, exist_ok=True)
     nvcc = _nvcc()
     extra = ["-Xptxas", "-v"] if ptxas_verbose else []
+    extra += [f"-D{k}={v}" for k, v in (defines or {}).items()]
 
     def compile_one(src):
-        obj = os.path.join(BUILD, src.replace(".cu", ".o"))
+        obj = os.path.join(bdir, src.replace(".cu", ".o"))
         cmd = [nvcc, *ARCH, *NVCC_FLAGS, *extra, "-c",
                os.path.join(CSRC, src), "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
@@ -64,14 +70,14 @@ def build(force: bool = False, ptxas_verbose: bool = False) -> str:
     if ptxas_verbose:
         for _, log in results:
             sys.stderr.write(log)
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib + f".tmp{os.getpid()}"
     cmd = [nvcc, *ARCH, "-shared", "-cudart", "static",
            *[o for o, _ in results], "-o", tmp]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":

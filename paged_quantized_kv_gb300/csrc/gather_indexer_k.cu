@@ -30,8 +30,17 @@
 namespace kvq {
 namespace {
 
-constexpr int kThreads = 256;
+#ifndef KVQ_GATHER_THREADS
+#define KVQ_GATHER_THREADS 256
+#endif
+constexpr int kThreads = KVQ_GATHER_THREADS;
 constexpr int kWarps = kThreads / 32;
+
+__device__ __forceinline__ uint32_t ld_nc_u32(const void* p) {
+  uint32_t v;
+  asm volatile("ld.global.nc.u32 %0, [%1];" : "=r"(v) : "l"(p));
+  return v;
+}
 
 __device__ __forceinline__ uint4 ld_nc_16(const void* p) {
   uint4 v;
@@ -120,6 +129,10 @@ gather_indexer_k_kernel(const GatherParams p) {
     if (err != 0 && p.dev_error != nullptr) atomicOr(p.dev_error, err);
   }
 
+  // the scale load goes out first, alongside the row loads below
+  uint32_t scale_bits = 0;
+  if (src_scale != nullptr) scale_bits = ld_nc_u32(src_scale);
+
   // ---- copy the 32 K rows as 16-byte vectors ---------------------------
   const int cpr = CPR > 0 ? CPR : (p.D >> 4);
   const unsigned long long my_src =
@@ -156,10 +169,8 @@ gather_indexer_k_kernel(const GatherParams p) {
   }
 
   // ---- the row's 4 scale bytes -----------------------------------------
-  if (src_scale != nullptr) {
-    const uint32_t sc = __ldg(reinterpret_cast<const uint32_t*>(src_scale));
-    *reinterpret_cast<uint32_t*>(p.k_scale + r * 4) = sc;
-  }
+  if (src_scale != nullptr)
+    *reinterpret_cast<uint32_t*>(p.k_scale + r * 4) = scale_bits;
 }
 
 template <int CPR>

@@ -40,8 +40,14 @@
 namespace kvq {
 namespace {
 
+#ifndef KVQ_STORE_UNROLL
+#define KVQ_STORE_UNROLL 4
+#endif
+#ifndef KVQ_STORE_MIN_BLOCKS
+#define KVQ_STORE_MIN_BLOCKS 1
+#endif
 constexpr int kThreads = 256;
-constexpr int kUnroll = 4;
+constexpr int kUnroll = KVQ_STORE_UNROLL;
 constexpr uint32_t kInv6Bits = 0x3E2AAAABu;  // RN(1/6) in fp32
 
 // 16 bf16 of one group into w[0..7] (element 2k in the low half of w[k]).
@@ -136,7 +142,7 @@ __device__ __forceinline__ void st_v2(uint8_t* p, uint32_t a, uint32_t b) {
 }
 
 template <bool kVec32>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, KVQ_STORE_MIN_BLOCKS)
 store_nvfp4_kernel(const StoreParams p) {
   __shared__ float s_ratio[2][256];  // g_side / float(e4m3 code)
 
