@@ -12,10 +12,11 @@
 // GB300 design: a pure copy, HBM-bound (2 x (D + 4) bytes per row), whose
 // time is dominated by the dependent-load chain before the first row load
 // (cu_seq_lens -> block_table -> K rows), since the whole grid fits in one
-// wave.  Each CTA first stages cu_seq_lens in shared memory with one
-// coalesced load (when it fits in 48 KB; otherwise the search reads global
-// memory), so the per-row binary search costs one DRAM latency instead of
-// one per search level.  One warp owns 32 consecutive output rows: lane l
+// wave.  Each CTA first stages cu_seq_lens -- and, when it is contiguous
+// and fits, the used block table -- in shared memory with one batch of
+// coalesced loads (48 KB at most; otherwise the reads go to global memory),
+// so the per-row binary search and the block lookup cost one memory round
+// trip together instead of one per search level plus one.  One warp owns 32 consecutive output rows: lane l
 // resolves row r0 + l (search, one block-table read, bounds checks), then the
 // warp moves the 32 rows as 16-byte vectors -- every load of a unit issued
 // before its stores, 32 x D bytes in flight per warp -- and each lane copies
@@ -73,21 +74,58 @@ __device__ __forceinline__ int find_seq(const int32_t* cu, int n, int64_t r) {
   return lo;
 }
 
-// cu_seq_lens entries staged in shared memory at most (48 KB, no opt-in).
-constexpr int kMaxSharedCu = 12288;
+// int32 metadata entries staged in shared memory at most (48 KB, no opt-in).
+constexpr int kMaxSharedInts = 12288;
+constexpr int kStageBatch = 16;
+
+// Where the kernel reads its metadata from.
+enum MetaMode {
+  kMetaGlobal = 0,       // cu_seq_lens and block_table from global memory
+  kMetaSharedCu = 1,     // cu_seq_lens staged in shared memory
+  kMetaSharedCuBt = 2    // cu_seq_lens and the (contiguous) block table
+};
+
+// Copy int32 ranges a[0, na) and b[0, nb) into dst[0, na + nb): every load
+// of a batch is issued before its stores, so both ranges arrive in about
+// one memory round trip.
+__device__ __forceinline__ void stage_meta(int32_t* dst, const int32_t* a,
+                                           int na, const int32_t* b,
+                                           int nb) {
+  const int total = na + nb;
+  for (int base = threadIdx.x; base < total; base += kThreads * kStageBatch) {
+    int32_t v[kStageBatch];
+#pragma unroll
+    for (int k = 0; k < kStageBatch; ++k) {
+      const int i = base + k * kThreads;
+      v[k] = 0;
+      if (i < na)
+        v[k] = __ldg(a + i);
+      else if (i < total)
+        v[k] = __ldg(b + (i - na));
+    }
+#pragma unroll
+    for (int k = 0; k < kStageBatch; ++k) {
+      const int i = base + k * kThreads;
+      if (i < total) dst[i] = v[k];
+    }
+  }
+}
 
 // CPR = 16-byte chunks per K row (head_dim / 16); 0 = runtime value.
-// kSharedCu: cu_seq_lens is staged in dynamic shared memory.
-template <int CPR, bool kSharedCu>
+template <int CPR, int kMode>
 __global__ void __launch_bounds__(kThreads)
 gather_indexer_k_kernel(const GatherParams p) {
-  extern __shared__ int32_t s_cu[];
+  extern __shared__ int32_t s_meta[];
   const int32_t* cu = p.cu;
-  if constexpr (kSharedCu) {
-    for (int i = threadIdx.x; i <= p.num_seqs; i += kThreads)
-      s_cu[i] = __ldg(p.cu + i);
+  const int32_t* s_bt = nullptr;
+  if constexpr (kMode != kMetaGlobal) {
+    const int ncu = p.num_seqs + 1;
+    const int nbt =
+        kMode == kMetaSharedCuBt ? p.num_seqs * p.max_blocks : 0;
+    stage_meta(s_meta, p.cu, ncu, p.block_table, nbt);
     __syncthreads();
-    cu = s_cu;
+    cu = s_meta;
+    s_bt = s_meta + ncu;
   }
   const int lane = threadIdx.x & 31;
   const int64_t unit =
@@ -104,7 +142,7 @@ gather_indexer_k_kernel(const GatherParams p) {
   const uint8_t* src_row = nullptr;
   const uint8_t* src_scale = nullptr;
   if (r < p.total) {
-    const int b = find_seq<kSharedCu>(cu, p.num_seqs, r);
+    const int b = find_seq<kMode != kMetaGlobal>(cu, p.num_seqs, r);
     int err = 0;
     if (b >= p.num_seqs) {
       err = KVQ_DEVERR_SEQ;  // no sequence covers this row
@@ -116,7 +154,10 @@ gather_indexer_k_kernel(const GatherParams p) {
       if (pos64 < 0 || pos64 >= (int64_t{1} << 31) || kb >= p.max_blocks) {
         err = KVQ_DEVERR_SEQ;
       } else {
-        const int64_t blk = __ldg(p.block_table + b * p.bt_stride + kb);
+        const int64_t blk =
+            kMode == kMetaSharedCuBt
+                ? s_bt[b * p.max_blocks + kb]
+                : __ldg(p.block_table + b * p.bt_stride + kb);
         if (blk < 0 || blk >= p.num_blocks) {
           err = KVQ_DEVERR_BLOCK;
         } else {
@@ -175,11 +216,19 @@ gather_indexer_k_kernel(const GatherParams p) {
 
 template <int CPR>
 void launch_cpr(const GatherParams& p, unsigned grid, cudaStream_t stream) {
-  if (p.num_seqs + 1 <= kMaxSharedCu) {
-    const size_t smem = static_cast<size_t>(p.num_seqs + 1) * sizeof(int32_t);
-    gather_indexer_k_kernel<CPR, true><<<grid, kThreads, smem, stream>>>(p);
+  const int64_t ncu = static_cast<int64_t>(p.num_seqs) + 1;
+  const int64_t nbt = static_cast<int64_t>(p.num_seqs) * p.max_blocks;
+  if (p.bt_stride == p.max_blocks && ncu + nbt <= kMaxSharedInts) {
+    const size_t smem = static_cast<size_t>(ncu + nbt) * sizeof(int32_t);
+    gather_indexer_k_kernel<CPR, kMetaSharedCuBt>
+        <<<grid, kThreads, smem, stream>>>(p);
+  } else if (ncu <= kMaxSharedInts) {
+    const size_t smem = static_cast<size_t>(ncu) * sizeof(int32_t);
+    gather_indexer_k_kernel<CPR, kMetaSharedCu>
+        <<<grid, kThreads, smem, stream>>>(p);
   } else {
-    gather_indexer_k_kernel<CPR, false><<<grid, kThreads, 0, stream>>>(p);
+    gather_indexer_k_kernel<CPR, kMetaGlobal>
+        <<<grid, kThreads, 0, stream>>>(p);
   }
 }
 
