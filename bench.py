@@ -198,7 +198,8 @@ class ClockSampler:
 
 # --- our arm ----------------------------------------------------------------------
 
-GATHER_SETS = 4  # gather buffer sets rotated so no launch finds its data in L2
+GATHER_SETS = 8  # gather buffer sets rotated so no launch finds its data in
+# L2 (8 x 35 MB > the 129 MB L2, even in the gather-only loop)
 
 
 def run_ours(args):
@@ -241,26 +242,40 @@ def run_ours(args):
     stream = torch.cuda.current_stream(dev)
     sh = stream.cuda_stream
 
-    def store():
-        kvq.kvq_store_nvfp4(key, value, kc, vc, slots, ks, vs,
+    def store(flags):
+        kvq.kvq_store_nvfp4(key, value, kc, vc, slots, ks, vs, flags=flags,
                             dev_error=dev_err, stream=sh)
 
-    def gather(i):
+    def gather(i, flags):
         g = gsets[i % GATHER_SETS]
         kvq.kvq_gather_indexer_k(g["cache"], g["k"], g["s"], g["bt"], g["cu"],
-                                 block_size=ga.block_size, dev_error=dev_err,
-                                 stream=sh)
+                                 block_size=ga.block_size, flags=flags,
+                                 dev_error=dev_err, stream=sh)
+
+    def step(i, flags):
+        store(flags)
+        gather(i, flags)
+
+    def span_ms(fn, count):
+        """Mean time per call of `count` back-to-back calls (two events)."""
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(count):
+            fn(i)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        return e0.elapsed_time(e1) / count
 
     W = max(args.warmup, 3)
+    PDL = kvq.KVQ_F_PDL
     for i in range(W):
-        store()
-        gather(i)
+        step(i, PDL)
+        step(i, 0)
     torch.cuda.synchronize(dev)
 
     # ---- timed region: K steps back to back -------------------------------
     K = args.steps
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)]
-          for _ in range(K)]
     sampler = ClockSampler(dev.index)
     sampler.start()
     time.sleep(0.2)
@@ -268,39 +283,35 @@ def run_ours(args):
         torch.distributed.barrier()
     torch.cuda.synchronize(dev)
     t0 = time.perf_counter()
-    for i in range(K):
-        ev[i][0].record(stream)
-        store()
-        ev[i][1].record(stream)
-        gather(W + i)
-        ev[i][2].record(stream)
-    torch.cuda.synchronize(dev)
+    step_ms = span_ms(lambda i: step(i, PDL), K)
     if world > 1:
         torch.distributed.barrier()
     wall = time.perf_counter() - t0
+    # per-kernel averages: each kernel alone, back to back (inputs larger
+    # than L2: the store streams 689 MB per call; the gather rotates over
+    # GATHER_SETS buffer sets)
+    store_ms = span_ms(lambda i: store(PDL), K)
+    gather_ms = span_ms(lambda i: gather(i, PDL), K)
+    plain = {"step_ms": span_ms(lambda i: step(i, 0), K),
+             "store_ms": span_ms(lambda i: store(0), K),
+             "gather_ms": span_ms(lambda i: gather(i, 0), K)}
     # keep the same steps running so the clock sampler sees the load
     t1 = time.perf_counter()
     j = 0
     while time.perf_counter() - t1 < args.clock_window_s:
-        store()
-        gather(j)
+        step(j, PDL)
         j += 1
         if j % 50 == 0:
             torch.cuda.synchronize(dev)
     torch.cuda.synchronize(dev)
     clocks = sampler.stop()
     assert int(dev_err.item()) == 0, "device error flag raised"
-
-    region_ms = ev[0][0].elapsed_time(ev[K - 1][2])
-    store_ms = statistics.fmean(ev[i][0].elapsed_time(ev[i][1])
-                                for i in range(K))
-    gather_ms = statistics.fmean(ev[i][1].elapsed_time(ev[i][2])
-                                 for i in range(K))
-    cold = single_launch_cold(store, lambda: gather(0), dev)
+    region_ms = step_ms * K
+    cold = single_launch_cold(lambda: store(0), lambda: gather(0, 0), dev)
 
     st_bytes = st.algorithmic_bytes()
     ga_bytes = ga.algorithmic_bytes()
-    step_s = max_over_ranks(region_ms / K / 1e3, world, dev)
+    step_s = max_over_ranks(step_ms / 1e3, world, dev)
     total_bytes = sum_over_ranks(float(st_bytes + ga_bytes), world, dev)
     total_tokens = sum_over_ranks(float(T + n), world, dev)
     peak, peak_kind = measured_hbm_peak()
@@ -335,12 +346,15 @@ def run_ours(args):
                        "num_blocks": ga.num_blocks, "io": "u8 copy"},
             "l2": "inputs larger than L2: each step streams the store's "
                   "537 MB of bf16 K/V and 151 MB of pages; the gather "
-                  f"rotates over {GATHER_SETS} buffer sets (35 MB each), so "
-                  "every launch's data was evicted by the intervening store",
+                  f"rotates over {GATHER_SETS} buffer sets (35 MB each, "
+                  f"{GATHER_SETS * 35} MB in all), so no launch finds its "
+                  "data in L2",
             "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
-            "timing": "K steps back to back on one stream; CUDA events "
-                      "before the store, between the kernels and after the "
-                      "gather; ms_per_step = event span / K; max over ranks",
+            "timing": "K steps (store + gather, launched with the "
+                      "KVQ_F_PDL flag) back to back on one stream between "
+                      "two CUDA events; ms_per_step = span / K, max over "
+                      "ranks.  Per-kernel times: K launches of that kernel "
+                      "alone, back to back, same way",
         },
         "tokens_per_s": round(total_tokens / step_s, 1),
         "kernels": {
@@ -357,6 +371,7 @@ def run_ours(args):
                 "tokens_per_s": round(n / (gather_ms / 1e3), 1),
                 "algorithmic_bytes": ga_bytes},
         },
+        "without_pdl": {k: round(v, 5) for k, v in plain.items()},
         "single_launch_after_l2_write_flush": {
             "note": "each kernel alone after writing a 256 MiB buffer "
                     "(L2 left dirty), events around the launch; includes "
@@ -378,6 +393,8 @@ def run_ours(args):
         "wall_s_timed_region": round(wall, 4),
         "e2e": e2e,
         "gpu_launches": 2 * K,
+        "gpu_launches_note": "in the timed step region; the per-kernel and "
+                             "no-PDL loops after it launch 6K more",
         "clocks": clocks,
     }
     if rank == 0 and not args.no_cpu_baseline:

@@ -58,11 +58,21 @@ enum {
 /* Input element types. */
 enum { KVQ_DTYPE_BF16 = 0 };
 
-/* kvq_store_nvfp4 flags. */
+/* Flags. */
 enum {
-  /* Also write K scales in the swizzled tile order (by default K scales are
-     linear and only V scales are swizzled, as the page's kernel does). */
-  KVQ_F_SWIZZLE_K_SCALE = 1u << 0
+  /* kvq_store_nvfp4 only: also write K scales in the swizzled tile order (by
+     default K scales are linear and only V scales are swizzled, as the
+     page's kernel does). */
+  KVQ_F_SWIZZLE_K_SCALE = 1u << 0,
+  /* Both calls: launch with programmatic dependent launch.  The kernel may
+     become resident while the previous kernel on the stream is finishing;
+     it waits (griddepcontrol.wait, in hardware) for that kernel to complete
+     and its writes to be visible before it touches any memory, so the
+     result is the same as a plain launch -- only the launch latency between
+     the two kernels is hidden.  Each kernel also allows the next
+     PDL-launched kernel to do the same.  Useful when these calls run back
+     to back with other kernels on one stream. */
+  KVQ_F_PDL = 1u << 1
 };
 
 /* Bits OR-ed into *dev_error by the kernels. */
@@ -112,7 +122,7 @@ enum {
  * slot_mapping    int64 [num_tokens]; distinct non-negative slots
  *                 (duplicates race; the result is then unspecified).
  * k_scale, v_scale  device fp32 scalars, finite and > 0.
- * flags           0 or KVQ_F_SWIZZLE_K_SCALE.
+ * flags           KVQ_F_SWIZZLE_K_SCALE | KVQ_F_PDL, or 0.
  * dev_error       nullable device int32 (KVQ_DEVERR_SLOT).
  * stream          cudaStream_t.
  * num_tokens == 0 returns KVQ_OK without launching.
@@ -154,6 +164,7 @@ kvq_status kvq_store_nvfp4(const void* key, int64_t key_stride0,
  *                 flags KVQ_DEVERR_SEQ if the two disagree).
  * k_fp8           [total_tokens, head_dim] bytes, 16-byte aligned.
  * k_scale         [total_tokens * 4] bytes, 4-byte aligned.
+ * flags           KVQ_F_PDL or 0.
  * dev_error       nullable device int32 (KVQ_DEVERR_BLOCK | KVQ_DEVERR_SEQ).
  * total_tokens == 0 returns KVQ_OK without launching.
  */
@@ -164,8 +175,8 @@ kvq_status kvq_gather_indexer_k(const uint8_t* kv_cache, int64_t block_stride,
                                 int32_t max_blocks_per_seq,
                                 const int32_t* cu_seq_lens, int32_t num_seqs,
                                 int64_t total_tokens, uint8_t* k_fp8,
-                                uint8_t* k_scale, int32_t* dev_error,
-                                void* stream);
+                                uint8_t* k_scale, uint32_t flags,
+                                int32_t* dev_error, void* stream);
 
 /* Static text for a status code. */
 const char* kvq_status_string(kvq_status status);

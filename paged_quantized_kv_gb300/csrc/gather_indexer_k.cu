@@ -116,6 +116,7 @@ template <int CPR, int kMode>
 __global__ void __launch_bounds__(kThreads)
 gather_indexer_k_kernel(const GatherParams p) {
   extern __shared__ int32_t s_meta[];
+  pdl_prologue();
   const int32_t* cu = p.cu;
   const int32_t* s_bt = nullptr;
   if constexpr (kMode != kMetaGlobal) {
@@ -215,21 +216,22 @@ gather_indexer_k_kernel(const GatherParams p) {
 }
 
 template <int CPR>
-void launch_cpr(const GatherParams& p, unsigned grid, cudaStream_t stream) {
+cudaError_t launch_cpr(const GatherParams& p, unsigned grid,
+                       cudaStream_t stream) {
   const int64_t ncu = static_cast<int64_t>(p.num_seqs) + 1;
   const int64_t nbt = static_cast<int64_t>(p.num_seqs) * p.max_blocks;
   if (p.bt_stride == p.max_blocks && ncu + nbt <= kMaxSharedInts) {
     const size_t smem = static_cast<size_t>(ncu + nbt) * sizeof(int32_t);
-    gather_indexer_k_kernel<CPR, kMetaSharedCuBt>
-        <<<grid, kThreads, smem, stream>>>(p);
-  } else if (ncu <= kMaxSharedInts) {
-    const size_t smem = static_cast<size_t>(ncu) * sizeof(int32_t);
-    gather_indexer_k_kernel<CPR, kMetaSharedCu>
-        <<<grid, kThreads, smem, stream>>>(p);
-  } else {
-    gather_indexer_k_kernel<CPR, kMetaGlobal>
-        <<<grid, kThreads, 0, stream>>>(p);
+    return launch_kernel(gather_indexer_k_kernel<CPR, kMetaSharedCuBt>, grid,
+                         kThreads, smem, stream, p.pdl, p);
   }
+  if (ncu <= kMaxSharedInts) {
+    const size_t smem = static_cast<size_t>(ncu) * sizeof(int32_t);
+    return launch_kernel(gather_indexer_k_kernel<CPR, kMetaSharedCu>, grid,
+                         kThreads, smem, stream, p.pdl, p);
+  }
+  return launch_kernel(gather_indexer_k_kernel<CPR, kMetaGlobal>, grid,
+                       kThreads, 0, stream, p.pdl, p);
 }
 
 }  // namespace
@@ -238,11 +240,8 @@ cudaError_t launch_gather_indexer_k(const GatherParams& p,
                                     cudaStream_t stream) {
   const int64_t units = (p.total + 31) / 32;
   const unsigned grid = static_cast<unsigned>((units + kWarps - 1) / kWarps);
-  if (p.D == 128)
-    launch_cpr<8>(p, grid, stream);
-  else
-    launch_cpr<0>(p, grid, stream);
-  return cudaGetLastError();
+  return p.D == 128 ? launch_cpr<8>(p, grid, stream)
+                    : launch_cpr<0>(p, grid, stream);
 }
 
 }  // namespace kvq

@@ -58,7 +58,8 @@ kvq_status kvq_store_nvfp4(const void* key, int64_t key_stride0,
   if (dtype != KVQ_DTYPE_BF16) return KVQ_ERR_DTYPE;
   if (layout != KVQ_LAYOUT_HND && layout != KVQ_LAYOUT_NHD)
     return KVQ_ERR_LAYOUT;
-  if ((flags & ~static_cast<uint32_t>(KVQ_F_SWIZZLE_K_SCALE)) != 0u)
+  if ((flags & ~static_cast<uint32_t>(KVQ_F_SWIZZLE_K_SCALE | KVQ_F_PDL)) !=
+      0u)
     return KVQ_ERR_ARG;
   if (num_tokens < 0 || num_heads <= 0 || head_size <= 0 || block_size <= 0 ||
       num_blocks < 0)
@@ -132,6 +133,7 @@ kvq_status kvq_store_nvfp4(const void* key, int64_t key_stride0,
   if (passes >= (int64_t{1} << 31)) return KVQ_ERR_SHAPE;
   p.num_passes = static_cast<int32_t>(passes);
   p.swizzle_sides = 2u | ((flags & KVQ_F_SWIZZLE_K_SCALE) ? 1u : 0u);
+  p.pdl = (flags & KVQ_F_PDL) != 0u;
 
   const cudaError_t err =
       launch_store_nvfp4(p, static_cast<cudaStream_t>(stream));
@@ -145,9 +147,10 @@ kvq_status kvq_gather_indexer_k(const uint8_t* kv_cache, int64_t block_stride,
                                 int32_t max_blocks_per_seq,
                                 const int32_t* cu_seq_lens, int32_t num_seqs,
                                 int64_t total_tokens, uint8_t* k_fp8,
-                                uint8_t* k_scale, int32_t* dev_error,
-                                void* stream) {
+                                uint8_t* k_scale, uint32_t flags,
+                                int32_t* dev_error, void* stream) {
   using namespace kvq;
+  if ((flags & ~static_cast<uint32_t>(KVQ_F_PDL)) != 0u) return KVQ_ERR_ARG;
   if (block_size <= 0 || head_dim <= 0 || num_seqs < 0 || total_tokens < 0 ||
       num_blocks < 0 || max_blocks_per_seq < 0 ||
       block_table_stride < max_blocks_per_seq)
@@ -181,6 +184,7 @@ kvq_status kvq_gather_indexer_k(const uint8_t* kv_cache, int64_t block_stride,
   p.D = head_dim;
   p.max_blocks = max_blocks_per_seq;
   p.num_seqs = num_seqs;
+  p.pdl = (flags & KVQ_F_PDL) != 0u;
   const cudaError_t err =
       launch_gather_indexer_k(p, static_cast<cudaStream_t>(stream));
   return err == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;

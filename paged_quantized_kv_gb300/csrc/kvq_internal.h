@@ -30,6 +30,7 @@ struct StoreParams {
   int32_t slices_log2;     // passes per token = 1 << slices_log2
   int32_t num_passes;
   uint32_t swizzle_sides;  // bit s set: side s's scales are swizzled
+  bool pdl;                // launch with programmatic dependent launch
 };
 
 cudaError_t launch_store_nvfp4(const StoreParams& p, cudaStream_t stream);
@@ -51,6 +52,7 @@ struct GatherParams {
   int32_t B, D;
   int32_t max_blocks;
   int32_t num_seqs;
+  bool pdl;                // launch with programmatic dependent launch
 };
 
 cudaError_t launch_gather_indexer_k(const GatherParams& p,
@@ -58,5 +60,33 @@ cudaError_t launch_gather_indexer_k(const GatherParams& p,
 
 // Streaming-multiprocessor count of the current device (cached per device).
 int sm_count();
+
+// Launch `kernel<<<grid, block, smem, stream>>>(params)`, with programmatic
+// dependent launch when `pdl` is set.
+template <typename Params>
+cudaError_t launch_kernel(void (*kernel)(Params), unsigned grid,
+                          unsigned block, size_t smem, cudaStream_t stream,
+                          bool pdl, const Params& params) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(block);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, params);
+}
+
+// First thing every kernel does: wait until the grid it depends on (when
+// launched with programmatic dependent launch) has completed and its writes
+// are visible -- a no-op otherwise -- then let a dependent grid start its
+// own launch.
+__device__ __forceinline__ void pdl_prologue() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
 
 }  // namespace kvq

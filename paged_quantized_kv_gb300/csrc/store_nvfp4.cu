@@ -146,6 +146,7 @@ __global__ void __launch_bounds__(kThreads, KVQ_STORE_MIN_BLOCKS)
 store_nvfp4_kernel(const StoreParams p) {
   __shared__ float s_ratio[2][256];  // g_side / float(e4m3 code)
 
+  pdl_prologue();
   const int tid = threadIdx.x;
   {
     const float g0 = __fdiv_rn(1.0f, __ldg(p.scale[0]));
@@ -271,9 +272,9 @@ cudaError_t launch(const StoreParams& p, cudaStream_t stream) {
   if (grid > p.num_passes) grid = p.num_passes;
   grid = (grid / slices) * slices;  // every CTA keeps one slice of a token
   if (grid < slices) grid = slices;
-  store_nvfp4_kernel<kVec32>
-      <<<static_cast<unsigned>(grid), kThreads, 0, stream>>>(p);
-  return cudaGetLastError();
+  return launch_kernel(store_nvfp4_kernel<kVec32>,
+                       static_cast<unsigned>(grid), kThreads, 0, stream,
+                       p.pdl, p);
 }
 
 }  // namespace

@@ -42,6 +42,7 @@ KVQ_LAYOUT_HND = 0
 KVQ_LAYOUT_NHD = 1
 KVQ_DTYPE_BF16 = 0
 KVQ_F_SWIZZLE_K_SCALE = 1
+KVQ_F_PDL = 2
 KVQ_DEVERR_SLOT = 1
 KVQ_DEVERR_BLOCK = 2
 KVQ_DEVERR_SEQ = 4
@@ -76,7 +77,7 @@ def lib() -> ctypes.CDLL:
         L.kvq_store_nvfp4.restype = c.c_int
         L.kvq_gather_indexer_k.argtypes = [
             P, c.c_int64, c.c_int64, c.c_int32, c.c_int32, P, c.c_int64,
-            c.c_int32, P, c.c_int32, c.c_int64, P, P, P, P]
+            c.c_int32, P, c.c_int32, c.c_int64, P, P, c.c_uint32, P, P]
         L.kvq_gather_indexer_k.restype = c.c_int
         L.kvq_status_string.argtypes = [c.c_int]
         L.kvq_status_string.restype = c.c_char_p
@@ -144,6 +145,7 @@ def kvq_store_nvfp4(key: torch.Tensor, value: torch.Tensor,
 def kvq_gather_indexer_k(kv_cache: torch.Tensor, k_fp8: torch.Tensor,
                          k_scale: torch.Tensor, block_table: torch.Tensor,
                          cu_seq_lens: torch.Tensor, block_size: int | None = None,
+                         flags: int = 0,
                          dev_error: torch.Tensor | None = None,
                          stream: int | None = None) -> None:
     """Indexer-K gather (see ``include/kvq.h``).
@@ -172,7 +174,7 @@ def kvq_gather_indexer_k(kv_cache: torch.Tensor, k_fp8: torch.Tensor,
         int(block_size), int(head_dim), block_table.data_ptr(),
         block_table.stride(0), block_table.size(1), cu_seq_lens.data_ptr(),
         cu_seq_lens.numel() - 1, int(total), k_fp8.data_ptr(),
-        k_scale.data_ptr(), _ptr(dev_error),
+        k_scale.data_ptr(), int(flags), _ptr(dev_error),
         _stream_of(kv_cache) if stream is None else stream)
     _check("kvq_gather_indexer_k", st)
 

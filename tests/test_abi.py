@@ -36,10 +36,8 @@ def header_functions():
 
 def test_exports_match_header(lib):
     declared = header_functions()
-    assert declared == {"kvq_store_nvfp4", "kvq_gather_indexer_k",
-                        "kvq_status_string", "kvq_version"} | (
-        declared - {"kvq_store_nvfp4", "kvq_gather_indexer_k",
-                    "kvq_status_string", "kvq_version"})
+    assert {"kvq_store_nvfp4", "kvq_gather_indexer_k", "kvq_status_string",
+            "kvq_version"} <= declared
     out = subprocess.run(["nm", "-D", "--defined-only", kvq.LIB_PATH],
                          capture_output=True, text=True, check=True).stdout
     exported = set(re.findall(r"\sT\s(kvq_\w+)$", out, flags=re.M))
@@ -73,7 +71,7 @@ def store(lib, **kw):
 @pytest.mark.parametrize("kw,code", [
     (dict(dtype=1), kvq.KVQ_ERR_DTYPE),
     (dict(layout=2), kvq.KVQ_ERR_LAYOUT),
-    (dict(flags=2), kvq.KVQ_ERR_ARG),
+    (dict(flags=4), kvq.KVQ_ERR_ARG),
     (dict(head_size=96), kvq.KVQ_ERR_SHAPE),
     (dict(head_size=0), kvq.KVQ_ERR_SHAPE),
     (dict(block_size=6), kvq.KVQ_ERR_SHAPE),
@@ -101,7 +99,7 @@ def gather(lib, **kw):
     args = dict(kv_cache=A, block_stride=64 * 132, num_blocks=8,
                 block_size=64, head_dim=128, block_table=A,
                 block_table_stride=4, max_blocks_per_seq=4, cu_seq_lens=A,
-                num_seqs=2, total_tokens=100, k_fp8=A, k_scale=A,
+                num_seqs=2, total_tokens=100, k_fp8=A, k_scale=A, flags=0,
                 dev_error=None, stream=None)
     args.update(kw)
     return lib.kvq_gather_indexer_k(*args.values())
@@ -116,6 +114,8 @@ def gather(lib, **kw):
     (dict(total_tokens=-5), kvq.KVQ_ERR_SHAPE),
     (dict(total_tokens=1 << 31), kvq.KVQ_ERR_SHAPE),
     (dict(num_seqs=0), kvq.KVQ_ERR_ARG),
+    (dict(flags=1), kvq.KVQ_ERR_ARG),
+    (dict(flags=4), kvq.KVQ_ERR_ARG),
     (dict(k_fp8=None), kvq.KVQ_ERR_NULL),
     (dict(cu_seq_lens=None), kvq.KVQ_ERR_NULL),
     (dict(k_fp8=A + 4), kvq.KVQ_ERR_ALIGN),

@@ -1,0 +1,82 @@
+"""Calls launched with KVQ_F_PDL (programmatic dependent launch) give the
+same bytes as the oracle, including when they run back to back with the
+other call and with themselves on one stream: each kernel waits for the
+previous kernel's completion before it touches memory, so a chain of
+stores into the same pages ends with the last store's bytes."""
+import numpy as np
+import pytest
+import torch
+
+from paged_quantized_kv_gb300 import kvq
+from paged_quantized_kv_gb300 import workloads as W
+from tests.gpu_helpers import assert_bytes_equal, store_inputs, to_dev
+from tests.test_oracle_gather import run_gather
+from tests.test_oracle_store import run_store
+
+pytestmark = pytest.mark.gpu
+PDL = kvq.KVQ_F_PDL
+
+
+def _gather_args(g):
+    cache = to_dev(g.cache).view(g.num_blocks, g.block_stride)
+    n = g.total_tokens
+    k = torch.full((n, g.head_dim), 0xCD, dtype=torch.uint8, device="cuda")
+    s = torch.full((n, 4), 0xCD, dtype=torch.uint8, device="cuda")
+    return cache, k, s, to_dev(g.block_table), to_dev(g.cu_seq_lens)
+
+
+@pytest.mark.parametrize("index", [0, 4])
+def test_store_then_gather_pdl(orc, index):
+    st = W.store_workload(index)
+    ga = W.gather_workload(index)
+    key, value, slots, ks, vs = store_inputs(st)
+    kv, kc, vc = kvq.alloc_nvfp4_cache(st.num_blocks, st.block_size,
+                                       st.num_heads, st.head_size, fill=0xAA)
+    cache, k, s, bt, cu = _gather_args(ga)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    for _ in range(3):  # back to back, each depending on nothing but order
+        kvq.kvq_store_nvfp4(key, value, kc, vc, slots, ks, vs, flags=PDL,
+                            dev_error=err)
+        kvq.kvq_gather_indexer_k(cache, k, s, bt, cu,
+                                 block_size=ga.block_size, flags=PDL,
+                                 dev_error=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert_bytes_equal(kv.cpu().numpy().reshape(-1), run_store(orc, st),
+                       st.name)
+    wk, ws = run_gather(orc, ga)
+    assert_bytes_equal(k.cpu().numpy().reshape(-1), wk, ga.name + " k")
+    assert_bytes_equal(s.cpu().numpy().reshape(-1), ws, ga.name + " s")
+
+
+def test_chain_of_dependent_stores(orc):
+    """Alternate two inputs into the same slots 9 times with PDL; the pages
+    must hold exactly the last store's result."""
+    a = W.make_store("a", 40, 4096, 4, 256, 32, 128, slots="runs",
+                     request_len=512)
+    b = W.make_store("b", 41, 4096, 4, 256, 32, 128, slots="runs",
+                     request_len=512)
+    b.slot_mapping = a.slot_mapping.copy()
+    ins = [store_inputs(a), store_inputs(b)]
+    kv, kc, vc = kvq.alloc_nvfp4_cache(a.num_blocks, a.block_size,
+                                       a.num_heads, a.head_size, fill=0xAA)
+    for i in range(9):
+        key, value, slots, ks, vs = ins[i % 2]
+        kvq.kvq_store_nvfp4(key, value, kc, vc, slots, ks, vs, flags=PDL)
+    torch.cuda.synchronize()
+    assert_bytes_equal(kv.cpu().numpy().reshape(-1), run_store(orc, a), "a")
+
+
+def test_pdl_after_foreign_kernel(orc):
+    """A PDL launch right after an ordinary torch kernel that writes the
+    store's input sees the finished input."""
+    st = W.store_workload(0)
+    key, value, slots, ks, vs = store_inputs(st)
+    kv, kc, vc = kvq.alloc_nvfp4_cache(st.num_blocks, st.block_size,
+                                       st.num_heads, st.head_size, fill=0xAA)
+    k2 = torch.zeros_like(key)
+    k2.copy_(key)  # torch kernel writing the input just before the launch
+    kvq.kvq_store_nvfp4(k2, value, kc, vc, slots, ks, vs, flags=PDL)
+    torch.cuda.synchronize()
+    assert_bytes_equal(kv.cpu().numpy().reshape(-1), run_store(orc, st),
+                       st.name)
