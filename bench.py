@@ -254,7 +254,7 @@ def run_ours(args):
 
     def step(i, flags):
         store(flags)
-        gather(i, flags)
+        gather(i, flags | (kvq.KVQ_F_PDL_EARLY_META if flags else 0))
 
     def span_ms(fn, count):
         """Mean time per call of `count` back-to-back calls (two events)."""
@@ -291,7 +291,7 @@ def run_ours(args):
     # than L2: the store streams 689 MB per call; the gather rotates over
     # GATHER_SETS buffer sets)
     store_ms = span_ms(lambda i: store(PDL), K)
-    gather_ms = span_ms(lambda i: gather(i, PDL), K)
+    gather_ms = span_ms(lambda i: gather(i, kvq.KVQ_F_PDL_EARLY_META), K)
     plain = {"step_ms": span_ms(lambda i: step(i, 0), K),
              "store_ms": span_ms(lambda i: store(0), K),
              "gather_ms": span_ms(lambda i: gather(i, 0), K)}
@@ -350,11 +350,12 @@ def run_ours(args):
                   f"{GATHER_SETS * 35} MB in all), so no launch finds its "
                   "data in L2",
             "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
-            "timing": "K steps (store + gather, launched with the "
-                      "KVQ_F_PDL flag) back to back on one stream between "
-                      "two CUDA events; ms_per_step = span / K, max over "
-                      "ranks.  Per-kernel times: K launches of that kernel "
-                      "alone, back to back, same way",
+            "timing": "K steps (store with KVQ_F_PDL, gather with "
+                      "KVQ_F_PDL_EARLY_META: its metadata is not written by "
+                      "the kernel before it) back to back on one stream "
+                      "between two CUDA events; ms_per_step = span / K, max "
+                      "over ranks.  Per-kernel times: K launches of that "
+                      "kernel alone, back to back, same flags",
         },
         "tokens_per_s": round(total_tokens / step_s, 1),
         "kernels": {

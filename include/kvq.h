@@ -72,16 +72,25 @@ enum {
      the two kernels is hidden.  Each kernel also allows the next
      PDL-launched kernel to do the same.  Useful when these calls run back
      to back with other kernels on one stream. */
-  KVQ_F_PDL = 1u << 1
+  KVQ_F_PDL = 1u << 1,
+  /* kvq_gather_indexer_k only; implies KVQ_F_PDL.  The caller promises that
+     block_table and cu_seq_lens are not written by the kernel that runs
+     just before this call on the stream (they are ready before it starts),
+     so the kernel stages and resolves them while that kernel finishes and
+     waits only before it reads the cache or writes anything. */
+  KVQ_F_PDL_EARLY_META = 1u << 2
 };
 
 /* Bits OR-ed into *dev_error by the kernels. */
 enum {
   KVQ_DEVERR_SLOT = 1 << 0,  /* slot >= num_blocks * block_size */
   KVQ_DEVERR_BLOCK = 1 << 1, /* block-table entry outside [0, num_blocks) */
-  KVQ_DEVERR_SEQ = 1 << 2    /* position beyond max_blocks_per_seq * B, or an
+  KVQ_DEVERR_SEQ = 1 << 2,   /* position beyond max_blocks_per_seq * B, or an
                                 output row that no sequence covers, or
                                 cu_seq_lens[num_seqs] != total_tokens */
+  KVQ_DEVERR_TIMEOUT = 1 << 3 /* a bounded wait for an asynchronous copy
+                                 gave up; the affected rows were not
+                                 written */
 };
 
 /*
@@ -164,8 +173,9 @@ kvq_status kvq_store_nvfp4(const void* key, int64_t key_stride0,
  *                 flags KVQ_DEVERR_SEQ if the two disagree).
  * k_fp8           [total_tokens, head_dim] bytes, 16-byte aligned.
  * k_scale         [total_tokens * 4] bytes, 4-byte aligned.
- * flags           KVQ_F_PDL or 0.
- * dev_error       nullable device int32 (KVQ_DEVERR_BLOCK | KVQ_DEVERR_SEQ).
+ * flags           KVQ_F_PDL, KVQ_F_PDL_EARLY_META, or 0.
+ * dev_error       nullable device int32 (KVQ_DEVERR_BLOCK | KVQ_DEVERR_SEQ |
+ *                 KVQ_DEVERR_TIMEOUT).
  * total_tokens == 0 returns KVQ_OK without launching.
  */
 kvq_status kvq_gather_indexer_k(const uint8_t* kv_cache, int64_t block_stride,

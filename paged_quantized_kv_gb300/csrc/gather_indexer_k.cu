@@ -10,18 +10,25 @@
 // grid covers total_tokens by construction.
 //
 // GB300 design: a pure copy, HBM-bound (2 x (D + 4) bytes per row), whose
-// time is dominated by the dependent-load chain before the first row load
-// (cu_seq_lens -> block_table -> K rows), since the whole grid fits in one
-// wave.  Each CTA first stages cu_seq_lens -- and, when it is contiguous
-// and fits, the used block table -- in shared memory with one batch of
-// coalesced loads (48 KB at most; otherwise the reads go to global memory),
-// so the per-row binary search and the block lookup cost one memory round
-// trip together instead of one per search level plus one.  One warp owns 32 consecutive output rows: lane l
-// resolves row r0 + l (search, one block-table read, bounds checks), then the
-// warp moves the 32 rows as 16-byte vectors -- every load of a unit issued
-// before its stores, 32 x D bytes in flight per warp -- and each lane copies
-// its row's 4 scale bytes.  Destination rows are contiguous, so every store
-// is a full sector.
+// time at tens of MB is dominated by the fixed launch cost and by the
+// dependent-load chain before the first row load (cu_seq_lens ->
+// block_table -> K rows), since the whole grid fits in one wave.
+//   * Each CTA stages cu_seq_lens -- and, when it is contiguous and fits,
+//     the used block table -- in shared memory: the 16-byte-aligned body of
+//     each range with one TMA bulk copy (cp.async.bulk, completion counted
+//     on an mbarrier, waited on with a bounded poll), the few unaligned
+//     head/tail entries with plain loads.  Row resolution (binary search,
+//     block lookup) then costs one memory round trip and few instructions.
+//     Ranges beyond 48 KB fall back to global reads.
+//   * With KVQ_F_PDL the kernel waits for its predecessor (griddepcontrol)
+//     before touching memory; with KVQ_F_PDL_EARLY_META it stages and
+//     resolves the metadata first and waits only before the cache reads and
+//     any write, overlapping that round trip with the predecessor's tail.
+//   * One warp owns 32 consecutive output rows: lane l resolves row r0 + l,
+//     then the warp moves the 32 rows as 16-byte vectors -- all loads of the
+//     unit issued before its stores, 32 x D bytes in flight per warp -- and
+//     each lane copies its row's 4 scale bytes.  Destination rows are
+//     contiguous, so every store is a full sector.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -36,12 +43,8 @@ namespace {
 #endif
 constexpr int kThreads = KVQ_GATHER_THREADS;
 constexpr int kWarps = kThreads / 32;
-
-__device__ __forceinline__ uint32_t ld_nc_u32(const void* p) {
-  uint32_t v;
-  asm volatile("ld.global.nc.u32 %0, [%1];" : "=r"(v) : "l"(p));
-  return v;
-}
+constexpr size_t kMaxMetaSmem = 48 * 1024;  // no opt-in needed
+constexpr uint32_t kMaxPolls = 1u << 22;     // bounded mbarrier wait
 
 __device__ __forceinline__ uint4 ld_nc_16(const void* p) {
   uint4 v;
@@ -52,10 +55,37 @@ __device__ __forceinline__ uint4 ld_nc_16(const void* p) {
   return v;
 }
 
+__device__ __forceinline__ uint32_t ld_nc_u32(const void* p) {
+  uint32_t v;
+  asm volatile("ld.global.nc.u32 %0, [%1];" : "=r"(v) : "l"(p));
+  return v;
+}
+
 __device__ __forceinline__ void st_16(void* p, const uint4& v) {
   asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p),
                "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
                : "memory");
+}
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// Bounded wait for phase `parity` of the mbarrier at `bar`; false on
+// timeout.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+  for (uint32_t i = 0; i < kMaxPolls; ++i) {
+    uint32_t done;
+    asm volatile(
+        "{ .reg .pred p;\n"
+        "  mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        "  selp.u32 %0, 1, 0, p; }"
+        : "=r"(done)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    if (done) return true;
+  }
+  return false;
 }
 
 // Largest b in [0, n] with cu[b] <= r (cu[0] == 0 <= r); cu in shared
@@ -74,77 +104,132 @@ __device__ __forceinline__ int find_seq(const int32_t* cu, int n, int64_t r) {
   return lo;
 }
 
-// int32 metadata entries staged in shared memory at most (48 KB, no opt-in).
-constexpr int kMaxSharedInts = 12288;
-constexpr int kStageBatch = 16;
-
 // Where the kernel reads its metadata from.
 enum MetaMode {
-  kMetaGlobal = 0,       // cu_seq_lens and block_table from global memory
-  kMetaSharedCu = 1,     // cu_seq_lens staged in shared memory
-  kMetaSharedCuBt = 2    // cu_seq_lens and the (contiguous) block table
+  kMetaGlobal = 0,     // cu_seq_lens and block_table from global memory
+  kMetaSharedCu = 1,   // cu_seq_lens staged in shared memory
+  kMetaSharedCuBt = 2  // cu_seq_lens and the (contiguous) block table
 };
 
-// Copy int32 ranges a[0, na) and b[0, nb) into dst[0, na + nb): every load
-// of a batch is issued before its stores, so both ranges arrive in about
-// one memory round trip.
-__device__ __forceinline__ void stage_meta(int32_t* dst, const int32_t* a,
-                                           int na, const int32_t* b,
-                                           int nb) {
-  const int total = na + nb;
-  for (int base = threadIdx.x; base < total; base += kThreads * kStageBatch) {
-    int32_t v[kStageBatch];
-#pragma unroll
-    for (int k = 0; k < kStageBatch; ++k) {
-      const int i = base + k * kThreads;
-      v[k] = 0;
-      if (i < na)
-        v[k] = __ldg(a + i);
-      else if (i < total)
-        v[k] = __ldg(b + (i - na));
-    }
-#pragma unroll
-    for (int k = 0; k < kStageBatch; ++k) {
-      const int i = base + k * kThreads;
-      if (i < total) dst[i] = v[k];
-    }
+// Shared-memory image of an int32 range: it starts at base + (src % 16) so
+// that every 16-byte-aligned source address maps to a 16-byte-aligned
+// shared address; the range needs at most 16 + 4 * n bytes, rounded to 16.
+__host__ __device__ constexpr size_t region_bytes(int64_t n) {
+  return (16 + 4 * static_cast<size_t>(n) + 15) & ~size_t{15};
+}
+
+struct RangeSplit {
+  int head;  // entries before the first 16-byte boundary
+  int body;  // entries in whole 16-byte chunks
+};
+
+__device__ __forceinline__ RangeSplit split_range(const int32_t* src, int n) {
+  const int mis = static_cast<int>(reinterpret_cast<uintptr_t>(src) & 15);
+  int head = ((16 - mis) & 15) >> 2;
+  if (head > n) head = n;
+  const int body = ((n - head) >> 2) << 2;
+  return {head, body};
+}
+
+// Stage cu_seq_lens (and the block table) into shared memory.  Thread 0
+// arms the mbarrier and issues the bulk copies of the aligned bodies; warp
+// 1 copies the unaligned heads and tails.  Returns false if the bulk copy
+// did not complete within the poll budget.
+__device__ __forceinline__ bool stage_meta(uint8_t* smem, uint64_t* bar,
+                                           const int32_t* cu, int ncu,
+                                           const int32_t* bt, int nbt,
+                                           int32_t** s_cu, int32_t** s_bt) {
+  const int tid = threadIdx.x;
+  int32_t* dcu = reinterpret_cast<int32_t*>(
+      smem + (reinterpret_cast<uintptr_t>(cu) & 15));
+  uint8_t* bt_base = smem + region_bytes(ncu);
+  int32_t* dbt = reinterpret_cast<int32_t*>(
+      bt_base + (reinterpret_cast<uintptr_t>(bt) & 15));
+  *s_cu = dcu;
+  *s_bt = dbt;
+  const RangeSplit rc = split_range(cu, ncu);
+  const RangeSplit rb =
+      nbt > 0 ? split_range(bt, nbt) : RangeSplit{0, 0};
+  const uint32_t bytes = 4u * static_cast<uint32_t>(rc.body + rb.body);
+  const uint32_t b = smem_addr(bar);
+
+  if (tid == 0) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(b)
+                 : "memory");
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
+  __syncthreads();
+  if (tid == 0 && bytes > 0) {
+    asm volatile(
+        "mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;"
+        ::"r"(b), "r"(bytes)
+        : "memory");
+    if (rc.body > 0)
+      asm volatile(
+          "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes"
+          " [%0], [%1], %2, [%3];" ::"r"(smem_addr(dcu + rc.head)),
+          "l"(cu + rc.head), "r"(4u * rc.body), "r"(b)
+          : "memory");
+    if (rb.body > 0)
+      asm volatile(
+          "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes"
+          " [%0], [%1], %2, [%3];" ::"r"(smem_addr(dbt + rb.head)),
+          "l"(bt + rb.head), "r"(4u * rb.body), "r"(b)
+          : "memory");
+  }
+  // unaligned heads and tails: at most 3 + 3 entries per range
+  if (tid >= 32 && tid < 32 + 12) {
+    const int k = tid - 32;
+    const int32_t* src = k < 6 ? cu : bt;
+    int32_t* dst = k < 6 ? dcu : dbt;
+    const int n = k < 6 ? ncu : nbt;
+    const RangeSplit r = k < 6 ? rc : rb;
+    const int j = k % 6;
+    const int i = j < 3 ? j : r.head + r.body + (j - 3);
+    if ((j < 3 && i < r.head) || (j >= 3 && i < n)) dst[i] = __ldg(src + i);
+  }
+  bool ok = true;
+  if (bytes > 0) {
+    ok = mbar_wait(b, 0);
+    if (!ok) mbar_wait(b, 0);  // give a copy still in flight a second term
+  }
+  __syncthreads();
+  return ok;
 }
 
 // CPR = 16-byte chunks per K row (head_dim / 16); 0 = runtime value.
-template <int CPR, int kMode>
+template <int CPR, int kMode, bool kEarlyMeta>
 __global__ void __launch_bounds__(kThreads)
 gather_indexer_k_kernel(const GatherParams p) {
-  extern __shared__ int32_t s_meta[];
-  pdl_prologue();
+  extern __shared__ __align__(16) uint8_t s_raw[];
+  __shared__ __align__(8) uint64_t s_bar;
+
+  if constexpr (!kEarlyMeta) pdl_prologue();
   const int32_t* cu = p.cu;
-  const int32_t* s_bt = nullptr;
+  int32_t* s_cu = nullptr;
+  int32_t* s_bt = nullptr;
+  bool staged = true;
   if constexpr (kMode != kMetaGlobal) {
-    const int ncu = p.num_seqs + 1;
-    const int nbt =
-        kMode == kMetaSharedCuBt ? p.num_seqs * p.max_blocks : 0;
-    stage_meta(s_meta, p.cu, ncu, p.block_table, nbt);
-    __syncthreads();
-    cu = s_meta;
-    s_bt = s_meta + ncu;
+    staged = stage_meta(s_raw, &s_bar, p.cu, p.num_seqs + 1, p.block_table,
+                        kMode == kMetaSharedCuBt ? p.num_seqs * p.max_blocks
+                                                 : 0,
+                        &s_cu, &s_bt);
+    cu = s_cu;
   }
   const int lane = threadIdx.x & 31;
   const int64_t unit =
       static_cast<int64_t>(blockIdx.x) * kWarps + (threadIdx.x >> 5);
   const int64_t r0 = unit * 32;
-  if (r0 >= p.total) return;  // whole warp leaves together
 
-  if (unit == 0 && lane == 0 && p.dev_error != nullptr &&
-      static_cast<int64_t>(cu[p.num_seqs]) != p.total)
-    atomicOr(p.dev_error, KVQ_DEVERR_SEQ);
-
-  // ---- resolve this lane's row ----------------------------------------
+  // ---- resolve this lane's row (metadata only) ---------------------------
   const int64_t r = r0 + lane;
   const uint8_t* src_row = nullptr;
   const uint8_t* src_scale = nullptr;
-  if (r < p.total) {
+  int err = 0;
+  if (!staged) {
+    err = KVQ_DEVERR_TIMEOUT;
+  } else if (r < p.total) {
     const int b = find_seq<kMode != kMetaGlobal>(cu, p.num_seqs, r);
-    int err = 0;
     if (b >= p.num_seqs) {
       err = KVQ_DEVERR_SEQ;  // no sequence covers this row
     } else {
@@ -168,8 +253,17 @@ gather_indexer_k_kernel(const GatherParams p) {
         }
       }
     }
-    if (err != 0 && p.dev_error != nullptr) atomicOr(p.dev_error, err);
   }
+  const bool total_mismatch = unit == 0 && lane == 0 && staged &&
+                              static_cast<int64_t>(cu[p.num_seqs]) != p.total;
+
+  // ---- from here on: cache reads and writes ------------------------------
+  if constexpr (kEarlyMeta) pdl_prologue();
+  if (p.dev_error != nullptr) {
+    if (err != 0) atomicOr(p.dev_error, err);
+    if (total_mismatch) atomicOr(p.dev_error, KVQ_DEVERR_SEQ);
+  }
+  if (r0 >= p.total || !staged) return;  // whole warp leaves together
 
   // the scale load goes out first, alongside the row loads below
   uint32_t scale_bits = 0;
@@ -215,23 +309,29 @@ gather_indexer_k_kernel(const GatherParams p) {
     *reinterpret_cast<uint32_t*>(p.k_scale + r * 4) = scale_bits;
 }
 
+template <int CPR, bool kEarlyMeta>
+cudaError_t launch_mode(const GatherParams& p, unsigned grid,
+                        cudaStream_t stream) {
+  const int64_t ncu = static_cast<int64_t>(p.num_seqs) + 1;
+  const int64_t nbt = static_cast<int64_t>(p.num_seqs) * p.max_blocks;
+  const size_t both = region_bytes(ncu) + region_bytes(nbt);
+  if (p.bt_stride == p.max_blocks && both <= kMaxMetaSmem)
+    return launch_kernel(
+        gather_indexer_k_kernel<CPR, kMetaSharedCuBt, kEarlyMeta>, grid,
+        kThreads, both, stream, p.pdl, p);
+  if (region_bytes(ncu) <= kMaxMetaSmem)
+    return launch_kernel(
+        gather_indexer_k_kernel<CPR, kMetaSharedCu, kEarlyMeta>, grid,
+        kThreads, region_bytes(ncu), stream, p.pdl, p);
+  return launch_kernel(gather_indexer_k_kernel<CPR, kMetaGlobal, kEarlyMeta>,
+                       grid, kThreads, 0, stream, p.pdl, p);
+}
+
 template <int CPR>
 cudaError_t launch_cpr(const GatherParams& p, unsigned grid,
                        cudaStream_t stream) {
-  const int64_t ncu = static_cast<int64_t>(p.num_seqs) + 1;
-  const int64_t nbt = static_cast<int64_t>(p.num_seqs) * p.max_blocks;
-  if (p.bt_stride == p.max_blocks && ncu + nbt <= kMaxSharedInts) {
-    const size_t smem = static_cast<size_t>(ncu + nbt) * sizeof(int32_t);
-    return launch_kernel(gather_indexer_k_kernel<CPR, kMetaSharedCuBt>, grid,
-                         kThreads, smem, stream, p.pdl, p);
-  }
-  if (ncu <= kMaxSharedInts) {
-    const size_t smem = static_cast<size_t>(ncu) * sizeof(int32_t);
-    return launch_kernel(gather_indexer_k_kernel<CPR, kMetaSharedCu>, grid,
-                         kThreads, smem, stream, p.pdl, p);
-  }
-  return launch_kernel(gather_indexer_k_kernel<CPR, kMetaGlobal>, grid,
-                       kThreads, 0, stream, p.pdl, p);
+  return p.early_meta ? launch_mode<CPR, true>(p, grid, stream)
+                      : launch_mode<CPR, false>(p, grid, stream);
 }
 
 }  // namespace

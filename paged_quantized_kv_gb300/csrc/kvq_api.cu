@@ -150,7 +150,9 @@ kvq_status kvq_gather_indexer_k(const uint8_t* kv_cache, int64_t block_stride,
                                 uint8_t* k_scale, uint32_t flags,
                                 int32_t* dev_error, void* stream) {
   using namespace kvq;
-  if ((flags & ~static_cast<uint32_t>(KVQ_F_PDL)) != 0u) return KVQ_ERR_ARG;
+  if ((flags & ~static_cast<uint32_t>(KVQ_F_PDL | KVQ_F_PDL_EARLY_META)) !=
+      0u)
+    return KVQ_ERR_ARG;
   if (block_size <= 0 || head_dim <= 0 || num_seqs < 0 || total_tokens < 0 ||
       num_blocks < 0 || max_blocks_per_seq < 0 ||
       block_table_stride < max_blocks_per_seq)
@@ -184,7 +186,8 @@ kvq_status kvq_gather_indexer_k(const uint8_t* kv_cache, int64_t block_stride,
   p.D = head_dim;
   p.max_blocks = max_blocks_per_seq;
   p.num_seqs = num_seqs;
-  p.pdl = (flags & KVQ_F_PDL) != 0u;
+  p.early_meta = (flags & KVQ_F_PDL_EARLY_META) != 0u;
+  p.pdl = p.early_meta || (flags & KVQ_F_PDL) != 0u;
   const cudaError_t err =
       launch_gather_indexer_k(p, static_cast<cudaStream_t>(stream));
   return err == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;

@@ -53,6 +53,7 @@ struct GatherParams {
   int32_t max_blocks;
   int32_t num_seqs;
   bool pdl;                // launch with programmatic dependent launch
+  bool early_meta;         // read metadata before waiting on the predecessor
 };
 
 cudaError_t launch_gather_indexer_k(const GatherParams& p,

@@ -43,9 +43,11 @@ KVQ_LAYOUT_NHD = 1
 KVQ_DTYPE_BF16 = 0
 KVQ_F_SWIZZLE_K_SCALE = 1
 KVQ_F_PDL = 2
+KVQ_F_PDL_EARLY_META = 4
 KVQ_DEVERR_SLOT = 1
 KVQ_DEVERR_BLOCK = 2
 KVQ_DEVERR_SEQ = 4
+KVQ_DEVERR_TIMEOUT = 8
 
 _lock = threading.Lock()
 _lib = None

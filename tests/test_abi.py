@@ -115,7 +115,7 @@ def gather(lib, **kw):
     (dict(total_tokens=1 << 31), kvq.KVQ_ERR_SHAPE),
     (dict(num_seqs=0), kvq.KVQ_ERR_ARG),
     (dict(flags=1), kvq.KVQ_ERR_ARG),
-    (dict(flags=4), kvq.KVQ_ERR_ARG),
+    (dict(flags=8), kvq.KVQ_ERR_ARG),
     (dict(k_fp8=None), kvq.KVQ_ERR_NULL),
     (dict(cu_seq_lens=None), kvq.KVQ_ERR_NULL),
     (dict(k_fp8=A + 4), kvq.KVQ_ERR_ALIGN),

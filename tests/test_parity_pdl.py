@@ -80,3 +80,51 @@ def test_pdl_after_foreign_kernel(orc):
     torch.cuda.synchronize()
     assert_bytes_equal(kv.cpu().numpy().reshape(-1), run_store(orc, st),
                        st.name)
+
+
+EARLY = kvq.KVQ_F_PDL_EARLY_META
+
+
+@pytest.mark.parametrize("index", [0, 3, 4])
+def test_gather_early_meta(orc, index):
+    ga = W.gather_workload(index)
+    cache, k, s, bt, cu = _gather_args(ga)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    for _ in range(3):
+        kvq.kvq_gather_indexer_k(cache, k, s, bt, cu,
+                                 block_size=ga.block_size, flags=EARLY,
+                                 dev_error=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    wk, ws = run_gather(orc, ga)
+    assert_bytes_equal(k.cpu().numpy().reshape(-1), wk, ga.name + " k")
+    assert_bytes_equal(s.cpu().numpy().reshape(-1), ws, ga.name + " s")
+
+
+def test_early_meta_gather_reads_bytes_the_store_just_wrote(orc):
+    """The gather's cache is the very buffer the preceding PDL store
+    writes: the early-metadata gather may start while the store runs, but
+    must read the cache only after the store has finished."""
+    st = W.make_store("src", 42, 4096, 4, 256, 32, 128, slots="runs",
+                      request_len=512)
+    key, value, slots, ks, vs = store_inputs(st)
+    kv, kc, vc = kvq.alloc_nvfp4_cache(st.num_blocks, st.block_size,
+                                       st.num_heads, st.head_size, fill=0xAA)
+    B, D = 64, 128
+    stride = B * (D + 4)
+    nb = st.cache_bytes // stride
+    g = W.make_gather("over_store", 43, [500, 700, 300, 1], B, D, nb)
+    g_cache = kv.view(-1)[: nb * stride].view(nb, stride)
+    n = g.total_tokens
+    k = torch.full((n, D), 0xCD, dtype=torch.uint8, device="cuda")
+    s = torch.full((n, 4), 0xCD, dtype=torch.uint8, device="cuda")
+    bt, cu = to_dev(g.block_table), to_dev(g.cu_seq_lens)
+    kvq.kvq_store_nvfp4(key, value, kc, vc, slots, ks, vs, flags=PDL)
+    kvq.kvq_gather_indexer_k(g_cache, k, s, bt, cu, block_size=B,
+                             flags=EARLY)
+    torch.cuda.synchronize()
+    stored = run_store(orc, st)
+    g.cache = stored[: nb * stride].copy()
+    wk, ws = run_gather(orc, g)
+    assert_bytes_equal(k.cpu().numpy().reshape(-1), wk, "k over store")
+    assert_bytes_equal(s.cpu().numpy().reshape(-1), ws, "s over store")
