@@ -55,8 +55,8 @@ enum {
   KVQ_LAYOUT_NHD = 1  /* data [B][H][D/2], scales [B][H][S] */
 };
 
-/* Input element types. */
-enum { KVQ_DTYPE_BF16 = 0 };
+/* Input element types (the page's dispatch takes both half types). */
+enum { KVQ_DTYPE_BF16 = 0, KVQ_DTYPE_FP16 = 1 };
 
 /* Flags. */
 enum {
@@ -119,10 +119,11 @@ enum {
  *   column (j % (S/4))*4 + off % 4.
  *   Bytes that no stored token owns are left unchanged.
  *
- * key, value      bf16 [num_tokens, num_heads, head_size]; heads and
+ * key, value      bf16 or fp16 [num_tokens, num_heads, head_size]; heads and
  *                 elements contiguous, rows key_stride0 / value_stride0
  *                 ELEMENTS apart (>= 0, multiple of 8); 16-byte aligned.
- * dtype           KVQ_DTYPE_BF16.
+ * dtype           KVQ_DTYPE_BF16 or KVQ_DTYPE_FP16 (both widen to fp32
+ *                 exactly; the arithmetic is the same).
  * key_cache, value_cache  page 0 of the K side and of the V side;
  *                 16-byte aligned; page_stride multiple of 16 and
  *                 >= H*B*(D/2 + S).

@@ -37,6 +37,8 @@ _LIB = os.path.join(_HERE, "libkvq_oracle.so")
 
 LAYOUT_HND = 0
 LAYOUT_NHD = 1
+DTYPE_BF16 = 0
+DTYPE_F16 = 1
 F_SWIZZLE_K_SCALE = 1
 
 OK = 0
@@ -87,9 +89,13 @@ class Oracle:
         lib.kvqo_swizzle.restype = c.c_int
         lib.kvqo_quantize_group.argtypes = [P, c.c_float, P, P]
         lib.kvqo_quantize_group.restype = c.c_int
+        lib.kvqo_quantize_group_t.argtypes = [P, c.c_int, c.c_float, P, P]
+        lib.kvqo_quantize_group_t.restype = c.c_int
+        lib.kvqo_f16_decode.argtypes = [c.c_uint16]
+        lib.kvqo_f16_decode.restype = c.c_double
         lib.kvqo_store_nvfp4.argtypes = [
             P, c.c_int64, P, c.c_int64, c.c_int32, c.c_int32, c.c_int32,
-            P, P, c.c_int64, c.c_int32, c.c_int64, c.c_int32, P,
+            c.c_int32, P, P, c.c_int64, c.c_int32, c.c_int64, c.c_int32, P,
             c.c_float, c.c_float, c.c_uint32]
         lib.kvqo_store_nvfp4.restype = c.c_int
         lib.kvqo_gather_indexer_k.argtypes = [
@@ -120,16 +126,23 @@ class Oracle:
         """Swizzled offset of (token-in-page t, scale s) in a [B, S] tile."""
         return self.lib.kvqo_swizzle(int(t), int(s), int(S))
 
-    def quantize_group(self, x_bf16_bits: np.ndarray, g: float):
-        """Quantise 16 bf16 values (uint16 bit patterns) with global scale g.
+    def f16_decode(self, bits: int) -> float:
+        """Value of an IEEE binary16 bit pattern."""
+        return self.lib.kvqo_f16_decode(int(bits) & 0xFFFF)
+
+    def quantize_group(self, x_bits: np.ndarray, g: float,
+                       dtype: int = DTYPE_BF16):
+        """Quantise 16 bf16 (or fp16) values, given as uint16 bit patterns,
+        with global scale g.
 
         Returns (data: uint8[8], sf: int).  Raises on non-finite input."""
-        x = np.ascontiguousarray(x_bf16_bits, dtype=np.uint16)
+        x = np.ascontiguousarray(x_bits, dtype=np.uint16)
         assert x.shape == (16,)
         data = np.zeros(8, dtype=np.uint8)
         sf = np.zeros(1, dtype=np.uint8)
-        rc = self.lib.kvqo_quantize_group(_ptr(x), float(np.float32(g)),
-                                          _ptr(data), _ptr(sf))
+        rc = self.lib.kvqo_quantize_group_t(_ptr(x), int(dtype),
+                                            float(np.float32(g)),
+                                            _ptr(data), _ptr(sf))
         if rc != OK:
             raise ValueError(f"kvqo_quantize_group failed: {rc}")
         return data, int(sf[0])
@@ -142,10 +155,12 @@ class Oracle:
                     page_stride: int, block_size: int, num_blocks: int,
                     layout: int, slot_mapping: np.ndarray,
                     k_scale: float, v_scale: float, flags: int = 0,
-                    key_base: int = 0, value_base: int = 0) -> None:
+                    key_base: int = 0, value_base: int = 0,
+                    dtype: int = DTYPE_BF16) -> None:
         """NVFP4 paged store into ``kv_cache`` (uint8, modified in place).
 
-        ``key_bits``/``value_bits`` are uint16 bf16 bit patterns; key token
+        ``key_bits``/``value_bits`` are uint16 bf16 (or fp16, ``dtype``) bit
+        patterns; key token
         t, head h, element d is ``key_bits[key_base + t*stride0 + h*D + d]``
         (value likewise).  ``key_offset``/``value_offset`` are the byte
         offsets of the K side and the V side of page 0 inside ``kv_cache``."""
@@ -156,7 +171,7 @@ class Oracle:
         rc = self.lib.kvqo_store_nvfp4(
             _ptr(key_bits, 2 * key_base), int(key_stride0),
             _ptr(value_bits, 2 * value_base), int(value_stride0),
-            int(num_tokens), int(num_heads), int(head_size), _ptr(kv_cache, key_offset),
+            int(dtype), int(num_tokens), int(num_heads), int(head_size), _ptr(kv_cache, key_offset),
             _ptr(kv_cache, value_offset), int(page_stride), int(block_size),
             int(num_blocks), int(layout), _ptr(slots),
             float(np.float32(k_scale)), float(np.float32(v_scale)),

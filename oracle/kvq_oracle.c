@@ -41,6 +41,8 @@
 
 #define KVQO_LAYOUT_HND 0
 #define KVQO_LAYOUT_NHD 1
+#define KVQO_DTYPE_BF16 0
+#define KVQO_DTYPE_F16 1
 #define KVQO_F_SWIZZLE_K_SCALE 1u
 
 /* ------------------------------------------------------------------------ */
@@ -122,6 +124,26 @@ static float bf16_to_float(uint16_t b) {
   return f;
 }
 
+/* IEEE binary16 bits -> fp32 (exact): 1 sign, 5 exponent (bias 15),
+ * 10 mantissa; subnormals m * 2^-24; exponent 31 is inf / NaN. */
+static float f16_to_float(uint16_t h) {
+  int sign = (h >> 15) & 1, e = (h >> 10) & 0x1F, m = h & 0x3FF;
+  double v;
+  if (e == 0)
+    v = ldexp((double)m, -24);
+  else if (e == 31)
+    v = (m == 0) ? INFINITY : NAN;
+  else
+    v = ldexp(1.0 + (double)m / 1024.0, e - 15);
+  return (float)(sign ? -v : v);
+}
+
+double kvqo_f16_decode(uint16_t h) { return (double)f16_to_float(h); }
+
+static float element_to_float(uint16_t x, int dtype) {
+  return dtype == KVQO_DTYPE_F16 ? f16_to_float(x) : bf16_to_float(x);
+}
+
 /* ------------------------------------------------------------------------ */
 /* Scale-tile swizzle ([nvfp4-cu] "swizzle_scale_offset" comment):          */
 /* the [T, S] tile viewed as [T/4, 4, 4, S/4], permuted (0, 2, 3, 1) and    */
@@ -136,14 +158,14 @@ int kvqo_swizzle(int t, int s, int S) {
 
 /* ------------------------------------------------------------------------ */
 /* One 16-element group ([nvfp4-cu] kernel: load group, quantise, pack).     */
-/* x: 16 bf16 bit patterns.  g: global scale (1 / k_scale).                  */
+/* x: 16 bf16 (or fp16, dtype) bit patterns.  g: global scale (1/k_scale).  */
 /* data8: 8 output bytes.  *sf: e4m3 scale code.                             */
 /* ------------------------------------------------------------------------ */
-int kvqo_quantize_group(const uint16_t* x, float g, uint8_t* data8,
-                        uint8_t* sf_out) {
+int kvqo_quantize_group_t(const uint16_t* x, int dtype, float g,
+                          uint8_t* data8, uint8_t* sf_out) {
   float xs[16];
   for (int i = 0; i < 16; ++i) {
-    xs[i] = bf16_to_float(x[i]);
+    xs[i] = element_to_float(x[i], dtype);
     if (!isfinite(xs[i])) return KVQO_ERR_NONFINITE;
   }
   float amax = 0.0f;
@@ -166,10 +188,16 @@ int kvqo_quantize_group(const uint16_t* x, float g, uint8_t* data8,
   return KVQO_OK;
 }
 
+int kvqo_quantize_group(const uint16_t* x, float g, uint8_t* data8,
+                        uint8_t* sf_out) {
+  return kvqo_quantize_group_t(x, KVQO_DTYPE_BF16, g, data8, sf_out);
+}
+
 /* ------------------------------------------------------------------------ */
 /* NVFP4 paged store ([nvfp4-cu] kernel and dispatch).                      */
 /*                                                                          */
-/* key/value: bf16 bits [num_tokens, H, D], row stride key_stride0 /        */
+/* key/value: bf16 (dtype 0) or fp16 (dtype 1) bits [num_tokens, H, D],    */
+/*   row stride key_stride0 /                                               */
 /*   value_stride0 elements, heads and elements contiguous.                 */
 /* key_cache/value_cache: base of the K side and of the V side of page 0    */
 /*   (kv_cache[:, 0] and kv_cache[:, 1]); pages are page_stride bytes apart. */
@@ -182,7 +210,8 @@ int kvqo_quantize_group(const uint16_t* x, float g, uint8_t* data8,
 /* ------------------------------------------------------------------------ */
 int kvqo_store_nvfp4(const uint16_t* key, int64_t key_stride0,
                      const uint16_t* value, int64_t value_stride0,
-                     int32_t num_tokens, int32_t num_heads, int32_t head_size,
+                     int32_t dtype, int32_t num_tokens, int32_t num_heads,
+                     int32_t head_size,
                      uint8_t* key_cache, uint8_t* value_cache,
                      int64_t page_stride, int32_t block_size,
                      int64_t num_blocks, int32_t layout,
@@ -193,6 +222,7 @@ int kvqo_store_nvfp4(const uint16_t* key, int64_t key_stride0,
   if (head_size % 64 != 0 || block_size % 4 != 0) return KVQO_ERR_ARG;
   if (layout != KVQO_LAYOUT_HND && layout != KVQO_LAYOUT_NHD)
     return KVQO_ERR_ARG;
+  if (dtype != KVQO_DTYPE_BF16 && dtype != KVQO_DTYPE_F16) return KVQO_ERR_ARG;
 
   const int64_t H = num_heads, D = head_size, B = block_size;
   const int64_t data_dim = D / 2, S = D / 16;
@@ -233,7 +263,8 @@ int kvqo_store_nvfp4(const uint16_t* key, int64_t key_stride0,
         for (int64_t j = 0; j < groups_per_head; ++j) {
           /* S3..S5 */
           uint8_t packed[8], sf;
-          int rc = kvqo_quantize_group(src + h * D + 16 * j, g, packed, &sf);
+          int rc = kvqo_quantize_group_t(src + h * D + 16 * j, dtype, g,
+                                         packed, &sf);
           if (rc != KVQO_OK) return rc;
           /* S6: 8 data bytes of group j. */
           uint8_t* dst = data_page + h * dhs + off * dts + 8 * j;

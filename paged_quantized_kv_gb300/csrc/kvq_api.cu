@@ -55,7 +55,7 @@ kvq_status kvq_store_nvfp4(const void* key, int64_t key_stride0,
                            const float* v_scale, uint32_t flags,
                            int32_t* dev_error, void* stream) {
   using namespace kvq;
-  if (dtype != KVQ_DTYPE_BF16) return KVQ_ERR_DTYPE;
+  if (dtype != KVQ_DTYPE_BF16 && dtype != KVQ_DTYPE_FP16) return KVQ_ERR_DTYPE;
   if (layout != KVQ_LAYOUT_HND && layout != KVQ_LAYOUT_NHD)
     return KVQ_ERR_LAYOUT;
   if ((flags & ~static_cast<uint32_t>(KVQ_F_SWIZZLE_K_SCALE | KVQ_F_PDL)) !=
@@ -134,6 +134,7 @@ kvq_status kvq_store_nvfp4(const void* key, int64_t key_stride0,
   p.num_passes = static_cast<int32_t>(passes);
   p.swizzle_sides = 2u | ((flags & KVQ_F_SWIZZLE_K_SCALE) ? 1u : 0u);
   p.pdl = (flags & KVQ_F_PDL) != 0u;
+  p.f16 = dtype == KVQ_DTYPE_FP16;
 
   const cudaError_t err =
       launch_store_nvfp4(p, static_cast<cudaStream_t>(stream));

@@ -11,7 +11,7 @@ namespace kvq {
 // NVFP4 store
 // ---------------------------------------------------------------------------
 struct StoreParams {
-  const uint16_t* src[2];  // key, value (bf16 bit patterns)
+  const uint16_t* src[2];  // key, value (bf16 or fp16 bit patterns)
   int64_t src_stride[2];   // row stride in elements
   uint8_t* side[2];        // page 0 of the K side / V side
   const int64_t* slots;
@@ -31,6 +31,7 @@ struct StoreParams {
   int32_t num_passes;
   uint32_t swizzle_sides;  // bit s set: side s's scales are swizzled
   bool pdl;                // launch with programmatic dependent launch
+  bool f16;                // inputs are IEEE fp16 (else bf16)
 };
 
 cudaError_t launch_store_nvfp4(const StoreParams& p, cudaStream_t stream);

@@ -15,14 +15,16 @@
 //     computes all role addresses once and walks tokens with a grid stride,
 //     issuing kUnroll independent loads (one 256-bit load per group when the
 //     rows are 32-byte aligned) before using any of them.
-//   * amax: sign bits cleared, a tree of max.bf16x2, one final max.
+//   * Inputs are bf16 or IEEE fp16 (a template parameter); both widen to
+//     fp32 exactly.  amax: sign bits cleared, a tree of max.bf16x2 /
+//     max.f16x2, one final max.
 //   * amax / 6 in three instructions that equal the IEEE quotient for every
 //     finite bf16 amax: q0 = amax * RN(1/6), the exact residual
 //     r = fma(-q0, 6, amax), q = fma(r, RN(1/6), q0) -- the quotient
 //     correction step of P. Markstein, "Computation of elementary functions
 //     on the IBM RISC System/6000 processor", IBM J. Res. Dev. 34(1), 1990;
-//     checked exhaustively over all 32640 finite non-negative bf16 values by
-//     tests/test_div6.py.
+//     checked exhaustively over every finite non-negative bf16 and fp16
+//     value by tests/test_div6.py.
 //   * g = 1/k_scale and g / float(sf) are IEEE divisions; the second one is
 //     read from a 2 x 256 shared-memory table filled once per CTA with
 //     __fdiv_rn (exactly the per-group quotient, since sf has 256 codes).
@@ -79,10 +81,32 @@ __device__ __forceinline__ int64_t ld_nc_s64(const int64_t* p) {
   return v;
 }
 
-__device__ __forceinline__ uint32_t bf16x2_max(uint32_t a, uint32_t b) {
+// Packed max of two pairs of non-negative half-precision values (bf16 or
+// IEEE fp16 bit patterns).
+template <bool kF16>
+__device__ __forceinline__ uint32_t half2_max(uint32_t a, uint32_t b) {
   uint32_t d;
-  asm("max.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  if constexpr (kF16)
+    asm("max.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  else
+    asm("max.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
   return d;
+}
+
+// Low half of a packed pair -> fp32 (exact for both types).
+template <bool kF16>
+__device__ __forceinline__ float half_lo_to_float(uint32_t w) {
+  if constexpr (kF16) {
+    float f;
+    asm("{ .reg .f16 lo, hi;\n"
+        "  mov.b32 {lo, hi}, %1;\n"
+        "  cvt.f32.f16 %0, lo; }"
+        : "=f"(f)
+        : "r"(w));
+    return f;
+  } else {
+    return __uint_as_float(w << 16);
+  }
 }
 
 // e4m3 code -> fp32 (exact: every e4m3 value is an f16 value).
@@ -107,32 +131,60 @@ __device__ __forceinline__ uint32_t float_to_e4m3(float v) {
   return pair & 0xFFu;  // the second operand lands in the low byte
 }
 
-// Four packed bf16 pairs times r (IEEE fp32 products, two per mul.f32x2)
-// -> four bytes of e2m1 codes, element 2k in the low nibble of byte k.
+// Four packed pairs (bf16, or fp16 with kF16) times r (IEEE fp32 products,
+// two per mul.f32x2) -> four bytes of e2m1 codes, element 2k in the low
+// nibble of byte k.  Both element types widen to fp32 exactly.
+template <bool kF16>
 __device__ __forceinline__ uint32_t quant4(uint32_t w0, uint32_t w1,
                                            uint32_t w2, uint32_t w3,
                                            uint64_t rr) {
   uint32_t out;
-  asm("{ .reg .b32 l0, h0, l1, h1, l2, h2, l3, h3;\n"
-      "  .reg .b64 x0, x1, x2, x3;\n"
-      "  .reg .b8 b0, b1, b2, b3;\n"
-      "  shl.b32 l0, %1, 16;  and.b32 h0, %1, 0xFFFF0000;\n"
-      "  shl.b32 l1, %2, 16;  and.b32 h1, %2, 0xFFFF0000;\n"
-      "  shl.b32 l2, %3, 16;  and.b32 h2, %3, 0xFFFF0000;\n"
-      "  shl.b32 l3, %4, 16;  and.b32 h3, %4, 0xFFFF0000;\n"
-      "  mov.b64 x0, {l0, h0};  mov.b64 x1, {l1, h1};\n"
-      "  mov.b64 x2, {l2, h2};  mov.b64 x3, {l3, h3};\n"
-      "  mul.rn.f32x2 x0, x0, %5;  mul.rn.f32x2 x1, x1, %5;\n"
-      "  mul.rn.f32x2 x2, x2, %5;  mul.rn.f32x2 x3, x3, %5;\n"
-      "  mov.b64 {l0, h0}, x0;  mov.b64 {l1, h1}, x1;\n"
-      "  mov.b64 {l2, h2}, x2;  mov.b64 {l3, h3}, x3;\n"
-      "  cvt.rn.satfinite.e2m1x2.f32 b0, h0, l0;\n"
-      "  cvt.rn.satfinite.e2m1x2.f32 b1, h1, l1;\n"
-      "  cvt.rn.satfinite.e2m1x2.f32 b2, h2, l2;\n"
-      "  cvt.rn.satfinite.e2m1x2.f32 b3, h3, l3;\n"
-      "  mov.b32 %0, {b0, b1, b2, b3}; }"
-      : "=r"(out)
-      : "r"(w0), "r"(w1), "r"(w2), "r"(w3), "l"(rr));
+  if constexpr (kF16) {
+    asm("{ .reg .b32 l0, h0, l1, h1, l2, h2, l3, h3;\n"
+        "  .reg .f16 a0, b0_, a1, b1_, a2, b2_, a3, b3_;\n"
+        "  .reg .b64 x0, x1, x2, x3;\n"
+        "  .reg .b8 b0, b1, b2, b3;\n"
+        "  mov.b32 {a0, b0_}, %1;  mov.b32 {a1, b1_}, %2;\n"
+        "  mov.b32 {a2, b2_}, %3;  mov.b32 {a3, b3_}, %4;\n"
+        "  cvt.f32.f16 l0, a0;  cvt.f32.f16 h0, b0_;\n"
+        "  cvt.f32.f16 l1, a1;  cvt.f32.f16 h1, b1_;\n"
+        "  cvt.f32.f16 l2, a2;  cvt.f32.f16 h2, b2_;\n"
+        "  cvt.f32.f16 l3, a3;  cvt.f32.f16 h3, b3_;\n"
+        "  mov.b64 x0, {l0, h0};  mov.b64 x1, {l1, h1};\n"
+        "  mov.b64 x2, {l2, h2};  mov.b64 x3, {l3, h3};\n"
+        "  mul.rn.f32x2 x0, x0, %5;  mul.rn.f32x2 x1, x1, %5;\n"
+        "  mul.rn.f32x2 x2, x2, %5;  mul.rn.f32x2 x3, x3, %5;\n"
+        "  mov.b64 {l0, h0}, x0;  mov.b64 {l1, h1}, x1;\n"
+        "  mov.b64 {l2, h2}, x2;  mov.b64 {l3, h3}, x3;\n"
+        "  cvt.rn.satfinite.e2m1x2.f32 b0, h0, l0;\n"
+        "  cvt.rn.satfinite.e2m1x2.f32 b1, h1, l1;\n"
+        "  cvt.rn.satfinite.e2m1x2.f32 b2, h2, l2;\n"
+        "  cvt.rn.satfinite.e2m1x2.f32 b3, h3, l3;\n"
+        "  mov.b32 %0, {b0, b1, b2, b3}; }"
+        : "=r"(out)
+        : "r"(w0), "r"(w1), "r"(w2), "r"(w3), "l"(rr));
+  } else {
+    asm("{ .reg .b32 l0, h0, l1, h1, l2, h2, l3, h3;\n"
+        "  .reg .b64 x0, x1, x2, x3;\n"
+        "  .reg .b8 b0, b1, b2, b3;\n"
+        "  shl.b32 l0, %1, 16;  and.b32 h0, %1, 0xFFFF0000;\n"
+        "  shl.b32 l1, %2, 16;  and.b32 h1, %2, 0xFFFF0000;\n"
+        "  shl.b32 l2, %3, 16;  and.b32 h2, %3, 0xFFFF0000;\n"
+        "  shl.b32 l3, %4, 16;  and.b32 h3, %4, 0xFFFF0000;\n"
+        "  mov.b64 x0, {l0, h0};  mov.b64 x1, {l1, h1};\n"
+        "  mov.b64 x2, {l2, h2};  mov.b64 x3, {l3, h3};\n"
+        "  mul.rn.f32x2 x0, x0, %5;  mul.rn.f32x2 x1, x1, %5;\n"
+        "  mul.rn.f32x2 x2, x2, %5;  mul.rn.f32x2 x3, x3, %5;\n"
+        "  mov.b64 {l0, h0}, x0;  mov.b64 {l1, h1}, x1;\n"
+        "  mov.b64 {l2, h2}, x2;  mov.b64 {l3, h3}, x3;\n"
+        "  cvt.rn.satfinite.e2m1x2.f32 b0, h0, l0;\n"
+        "  cvt.rn.satfinite.e2m1x2.f32 b1, h1, l1;\n"
+        "  cvt.rn.satfinite.e2m1x2.f32 b2, h2, l2;\n"
+        "  cvt.rn.satfinite.e2m1x2.f32 b3, h3, l3;\n"
+        "  mov.b32 %0, {b0, b1, b2, b3}; }"
+        : "=r"(out)
+        : "r"(w0), "r"(w1), "r"(w2), "r"(w3), "l"(rr));
+  }
   return out;
 }
 
@@ -141,7 +193,7 @@ __device__ __forceinline__ void st_v2(uint8_t* p, uint32_t a, uint32_t b) {
                : "memory");
 }
 
-template <bool kVec32>
+template <bool kVec32, bool kF16>
 __global__ void __launch_bounds__(kThreads, KVQ_STORE_MIN_BLOCKS)
 store_nvfp4_kernel(const StoreParams p) {
   __shared__ float s_ratio[2][256];  // g_side / float(e4m3 code)
@@ -214,16 +266,16 @@ store_nvfp4_kernel(const StoreParams p) {
         continue;
       }
       // amax of the 16 magnitudes
-      const uint32_t m =
-          bf16x2_max(bf16x2_max(bf16x2_max(w[u][0] & 0x7FFF7FFFu,
-                                           w[u][1] & 0x7FFF7FFFu),
-                                bf16x2_max(w[u][2] & 0x7FFF7FFFu,
-                                           w[u][3] & 0x7FFF7FFFu)),
-                     bf16x2_max(bf16x2_max(w[u][4] & 0x7FFF7FFFu,
-                                           w[u][5] & 0x7FFF7FFFu),
-                                bf16x2_max(w[u][6] & 0x7FFF7FFFu,
-                                           w[u][7] & 0x7FFF7FFFu)));
-      const float amax = __uint_as_float(bf16x2_max(m, m >> 16) << 16);
+      const uint32_t m = half2_max<kF16>(
+          half2_max<kF16>(half2_max<kF16>(w[u][0] & 0x7FFF7FFFu,
+                                          w[u][1] & 0x7FFF7FFFu),
+                          half2_max<kF16>(w[u][2] & 0x7FFF7FFFu,
+                                          w[u][3] & 0x7FFF7FFFu)),
+          half2_max<kF16>(half2_max<kF16>(w[u][4] & 0x7FFF7FFFu,
+                                          w[u][5] & 0x7FFF7FFFu),
+                          half2_max<kF16>(w[u][6] & 0x7FFF7FFFu,
+                                          w[u][7] & 0x7FFF7FFFu)));
+      const float amax = half_lo_to_float<kF16>(half2_max<kF16>(m, m >> 16));
       // IEEE amax / 6 (see the header comment), then * g
       const float q0 = __fmul_rn(amax, inv6);
       const float res = __fmaf_rn(-q0, 6.0f, amax);
@@ -232,8 +284,8 @@ store_nvfp4_kernel(const StoreParams p) {
       const float r = ratio[sf];
       const uint64_t rr = (static_cast<uint64_t>(__float_as_uint(r)) << 32) |
                           __float_as_uint(r);
-      uint32_t lo = quant4(w[u][0], w[u][1], w[u][2], w[u][3], rr);
-      uint32_t hi = quant4(w[u][4], w[u][5], w[u][6], w[u][7], rr);
+      uint32_t lo = quant4<kF16>(w[u][0], w[u][1], w[u][2], w[u][3], rr);
+      uint32_t hi = quant4<kF16>(w[u][4], w[u][5], w[u][6], w[u][7], rr);
       lo = sf != 0u ? lo : 0u;
       hi = sf != 0u ? hi : 0u;
 
@@ -254,7 +306,7 @@ store_nvfp4_kernel(const StoreParams p) {
   }
 }
 
-template <bool kVec32>
+template <bool kVec32, bool kF16>
 cudaError_t launch(const StoreParams& p, cudaStream_t stream) {
   static int ctas_per_sm[64] = {0};
   int dev = 0;
@@ -263,7 +315,7 @@ cudaError_t launch(const StoreParams& p, cudaStream_t stream) {
   int& occ = ctas_per_sm[dev & 63];
   if (occ == 0) {
     err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-        &occ, store_nvfp4_kernel<kVec32>, kThreads, 0);
+        &occ, store_nvfp4_kernel<kVec32, kF16>, kThreads, 0);
     if (err != cudaSuccess) return err;
     if (occ < 1) occ = 1;
   }
@@ -272,7 +324,7 @@ cudaError_t launch(const StoreParams& p, cudaStream_t stream) {
   if (grid > p.num_passes) grid = p.num_passes;
   grid = (grid / slices) * slices;  // every CTA keeps one slice of a token
   if (grid < slices) grid = slices;
-  return launch_kernel(store_nvfp4_kernel<kVec32>,
+  return launch_kernel(store_nvfp4_kernel<kVec32, kF16>,
                        static_cast<unsigned>(grid), kThreads, 0, stream,
                        p.pdl, p);
 }
@@ -285,7 +337,9 @@ cudaError_t launch_store_nvfp4(const StoreParams& p, cudaStream_t stream) {
       (reinterpret_cast<uintptr_t>(p.src[0]) % 32 == 0) &&
       (reinterpret_cast<uintptr_t>(p.src[1]) % 32 == 0) &&
       (p.src_stride[0] % 16 == 0) && (p.src_stride[1] % 16 == 0);
-  return vec32 ? launch<true>(p, stream) : launch<false>(p, stream);
+  if (p.f16)
+    return vec32 ? launch<true, true>(p, stream) : launch<false, true>(p, stream);
+  return vec32 ? launch<true, false>(p, stream) : launch<false, false>(p, stream);
 }
 
 }  // namespace kvq

@@ -41,6 +41,7 @@ KVQ_ERR_ARG = -7
 KVQ_LAYOUT_HND = 0
 KVQ_LAYOUT_NHD = 1
 KVQ_DTYPE_BF16 = 0
+KVQ_DTYPE_FP16 = 1
 KVQ_F_SWIZZLE_K_SCALE = 1
 KVQ_F_PDL = 2
 KVQ_F_PDL_EARLY_META = 4
@@ -118,11 +119,12 @@ def kvq_store_nvfp4(key: torch.Tensor, value: torch.Tensor,
                     stream: int | None = None) -> None:
     """NVFP4 paged store (see ``include/kvq.h``).
 
-    key, value: bf16 [T, H, D], last two dims contiguous.  key_cache,
+    key, value: bf16 or fp16 [T, H, D], last two dims contiguous.  key_cache,
     value_cache: uint8 [num_blocks, block_size, H, D/2 + D/16] views whose
     stride(0) is the page stride and whose stride(2) > stride(1) marks HND.
     slot_mapping: int64 [T].  k_scale, v_scale: fp32 device scalars."""
-    if key.dtype != torch.bfloat16 or value.dtype != torch.bfloat16:
+    dtypes = {torch.bfloat16: KVQ_DTYPE_BF16, torch.float16: KVQ_DTYPE_FP16}
+    if key.dtype not in dtypes or value.dtype != key.dtype:
         raise KvqError("kvq_store_nvfp4", KVQ_ERR_DTYPE)
     T, H, D = key.shape
     if (key.stride(2) != 1 or key.stride(1) != D or value.stride(2) != 1
@@ -136,7 +138,7 @@ def kvq_store_nvfp4(key: torch.Tensor, value: torch.Tensor,
               else KVQ_LAYOUT_NHD)
     st = lib().kvq_store_nvfp4(
         key.data_ptr(), key.stride(0), value.data_ptr(), value.stride(0),
-        KVQ_DTYPE_BF16, T, H, D, key_cache.data_ptr(),
+        dtypes[key.dtype], T, H, D, key_cache.data_ptr(),
         value_cache.data_ptr(), key_cache.stride(0), key_cache.size(1),
         key_cache.size(0), layout, slot_mapping.data_ptr(),
         k_scale.data_ptr(), v_scale.data_ptr(), int(flags),

@@ -38,6 +38,8 @@ import torch
 
 LAYOUT_HND = 0
 LAYOUT_NHD = 1
+DTYPE_BF16 = 0
+DTYPE_F16 = 1
 
 
 def bf16_bits(x: np.ndarray) -> np.ndarray:
@@ -49,6 +51,24 @@ def bf16_bits(x: np.ndarray) -> np.ndarray:
 def bf16_values(bits: np.ndarray) -> np.ndarray:
     """uint16 bf16 bit patterns -> exact fp32 values."""
     return (bits.astype(np.uint32) << 16).view(np.float32)
+
+
+def f16_bits(x: np.ndarray) -> np.ndarray:
+    """fp32 -> IEEE fp16 (round to nearest even, numpy's cast) as uint16."""
+    return np.ascontiguousarray(x, dtype=np.float32).astype(
+        np.float16).view(np.uint16)
+
+
+def element_bits(x: np.ndarray, dtype: int) -> np.ndarray:
+    return f16_bits(x) if dtype == DTYPE_F16 else bf16_bits(x)
+
+
+def element_values(bits: np.ndarray, dtype: int) -> np.ndarray:
+    """uint16 bit patterns of the given element type -> fp32 values."""
+    if dtype == DTYPE_F16:
+        return np.asarray(bits, dtype=np.uint16).view(np.float16).astype(
+            np.float32)
+    return bf16_values(np.asarray(bits))
 
 
 @dataclass
@@ -77,6 +97,7 @@ class StoreWorkload:
     layout: int = LAYOUT_HND
     flags: int = 0
     page_stride: int = 0
+    dtype: int = DTYPE_BF16
     extra: dict = field(default_factory=dict)
 
     def __post_init__(self):
@@ -187,12 +208,12 @@ def _normal_f32(rng, shape, outlier_p=0.0, outlier_mult=1.0):
     return x
 
 
-def per_tensor_scale(bits: np.ndarray) -> np.float32:
+def per_tensor_scale(bits: np.ndarray, dtype: int = DTYPE_BF16) -> np.float32:
     """Checkpoint scale recipe of the decode/prefill workloads:
     amax(|x|) / (448 * 6) in fp32."""
     if bits.size == 0:
         return np.float32(1.0)
-    amax = np.abs(bf16_values(bits)).max()
+    amax = np.abs(element_values(bits, dtype)).max()
     return np.float32(amax) / np.float32(448.0 * 6.0)
 
 
@@ -202,14 +223,15 @@ def make_store(name: str, seed: int, num_tokens: int, num_heads: int,
                outlier_p: float = 0.0, outlier_mult: float = 1.0,
                outlier_per_head: float = 0.0, scales: str = "per_tensor",
                request_len: int = 0, layout: int = LAYOUT_HND,
-               flags: int = 0) -> StoreWorkload:
+               flags: int = 0, dtype: int = DTYPE_BF16) -> StoreWorkload:
     """Generic store workload.
 
     slots: "random" (distinct random slots over the whole cache),
     "runs" (requests of ``request_len`` tokens, each on randomly chosen
     distinct blocks filled in order), or "dense" (token t -> slot t).
     skip: number of tokens whose slot is set to -1.
-    row_mult: K and V are halves of a [T, row_mult, H, D] buffer when 2."""
+    row_mult: K and V are halves of a [T, row_mult, H, D] buffer when 2.
+    dtype: element type of K and V (bf16 or fp16 bit patterns)."""
     rng = np.random.default_rng(seed)
     T, H, D, B = num_tokens, num_heads, head_size, block_size
     if row_mult == 2:
@@ -221,7 +243,7 @@ def make_store(name: str, seed: int, num_tokens: int, num_heads: int,
                     d = rng.integers(0, D)
                     if T:
                         x[t, side, h, d] *= np.float32(outlier_per_head)
-        src = bf16_bits(x.reshape(-1))
+        src = element_bits(x.reshape(-1), dtype)
         key_offset, value_offset, stride0 = 0, H * D, 2 * H * D
     else:
         kx = _normal_f32(rng, (T, H, D), outlier_p, outlier_mult)
@@ -232,7 +254,8 @@ def make_store(name: str, seed: int, num_tokens: int, num_heads: int,
                     t = rng.integers(0, T)
                     d = rng.integers(0, D)
                     arr[t, h, d] *= np.float32(outlier_per_head)
-        src = bf16_bits(np.concatenate([kx.reshape(-1), vx.reshape(-1)]))
+        src = element_bits(np.concatenate([kx.reshape(-1), vx.reshape(-1)]),
+                           dtype)
         key_offset, value_offset, stride0 = 0, T * H * D, H * D
 
     capacity = num_blocks * B
@@ -258,10 +281,11 @@ def make_store(name: str, seed: int, num_tokens: int, num_heads: int,
                        key_offset=key_offset, key_stride0=stride0,
                        value_offset=value_offset, value_stride0=stride0,
                        slot_mapping=sm, k_scale=np.float32(1.0),
-                       v_scale=np.float32(1.0), layout=layout, flags=flags)
+                       v_scale=np.float32(1.0), layout=layout, flags=flags,
+                       dtype=dtype)
     if scales == "per_tensor":
-        wl.k_scale = per_tensor_scale(np.asarray(wl.key_array()))
-        wl.v_scale = per_tensor_scale(np.asarray(wl.value_array()))
+        wl.k_scale = per_tensor_scale(np.asarray(wl.key_array()), dtype)
+        wl.v_scale = per_tensor_scale(np.asarray(wl.value_array()), dtype)
     elif scales == "one":
         pass
     else:
@@ -365,7 +389,7 @@ def shard_store(wl: StoreWorkload, rank: int, world: int,
         value_stride0=wl.value_stride0,
         slot_mapping=wl.slot_mapping[t0:t1].copy(), k_scale=wl.k_scale,
         v_scale=wl.v_scale, layout=wl.layout, flags=wl.flags,
-        page_stride=wl.page_stride)
+        page_stride=wl.page_stride, dtype=wl.dtype)
 
 
 def shard_gather(wl: GatherWorkload, rank: int, world: int):

@@ -11,8 +11,8 @@ def to_dev(a: np.ndarray) -> torch.Tensor:
 
 
 def store_inputs(wl, device="cuda"):
-    src = torch.from_numpy(wl.src.view(np.int16)).to(device).view(
-        torch.bfloat16)
+    tdt = torch.float16 if wl.dtype == 1 else torch.bfloat16
+    src = torch.from_numpy(wl.src.view(np.int16)).to(device).view(tdt)
     T, H, D = wl.num_tokens, wl.num_heads, wl.head_size
     key = src.as_strided((T, H, D), (wl.key_stride0, D, 1), wl.key_offset)
     value = src.as_strided((T, H, D), (wl.value_stride0, D, 1),

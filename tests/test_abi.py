@@ -69,7 +69,7 @@ def store(lib, **kw):
 
 
 @pytest.mark.parametrize("kw,code", [
-    (dict(dtype=1), kvq.KVQ_ERR_DTYPE),
+    (dict(dtype=2), kvq.KVQ_ERR_DTYPE),
     (dict(layout=2), kvq.KVQ_ERR_LAYOUT),
     (dict(flags=4), kvq.KVQ_ERR_ARG),
     (dict(head_size=96), kvq.KVQ_ERR_SHAPE),

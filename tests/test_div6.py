@@ -2,8 +2,9 @@
 q0 = amax * RN(1/6), r = fma(-q0, 6, amax), q = fma(r, RN(1/6), q0)
 (Markstein's quotient correction with an exact FMA residual).  This test
 checks, in exact rational arithmetic, that the sequence equals the IEEE
-fp32 quotient for every finite non-negative bf16 value -- the only values
-amax can take -- and that the residual is always exact.  CPU only."""
+fp32 quotient for every finite non-negative bf16 and fp16 value -- the only
+values amax can take -- and that the residual is always exact.  CPU
+only."""
 from fractions import Fraction as F
 
 import numpy as np
@@ -27,9 +28,7 @@ def test_inv6_constant():
     assert INV6 == np.float32(1.0) / np.float32(6.0)
 
 
-def test_fma_corrected_division_by_six_is_exact_for_all_bf16():
-    bits = np.arange(0, 0x7F80, dtype=np.uint32)  # finite, non-negative
-    a = (bits << 16).view(np.float32)
+def _check_all(a):
     ieee = a / np.float32(6.0)
     q0 = a * INV6  # fp32 products, correctly rounded
     c = F(float(INV6))
@@ -40,3 +39,13 @@ def test_fma_corrected_division_by_six_is_exact_for_all_bf16():
         assert F(float(r)) == res, a[i]          # fma residual is exact
         q1 = rn32(F(float(r)) * c + q)            # one rounding, as fma
         assert q1 == ieee[i], (a[i], q1, ieee[i])
+
+
+def test_fma_corrected_division_by_six_is_exact_for_all_bf16():
+    bits = np.arange(0, 0x7F80, dtype=np.uint32)  # finite, non-negative
+    _check_all((bits << 16).view(np.float32))
+
+
+def test_fma_corrected_division_by_six_is_exact_for_all_fp16():
+    bits = np.arange(0, 0x7C00, dtype=np.uint32).astype(np.uint16)
+    _check_all(bits.view(np.float16).astype(np.float32))

@@ -119,6 +119,18 @@ def check_e2m1_encode(o):
     assert o.e2m1_encode(float("-inf")) == 0xF
 
 
+def check_f16_decode(o):
+    """IEEE binary16 decode against numpy's float16 (an independent
+    library) on all 65536 bit patterns."""
+    codes = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    ref = codes.view(np.float16).astype(np.float64)
+    got = np.array([o.f16_decode(c) for c in range(65536)])
+    nan = np.isnan(ref)
+    assert (np.isnan(got) == nan).all()
+    assert (got[~nan] == ref[~nan]).all()
+    assert (np.signbit(got[~nan]) == np.signbit(ref[~nan])).all()
+
+
 def check_swizzle_golden(o):
     from tests.golden_io import swizzle_points
     for t, s, S, off in swizzle_points():
@@ -149,7 +161,8 @@ def check_swizzle_permute(o):
 
 
 CHECKS = [check_e4m3_decode, check_e4m3_encode, check_e2m1_decode,
-          check_e2m1_encode, check_swizzle_golden, check_swizzle_permute]
+          check_e2m1_encode, check_f16_decode, check_swizzle_golden,
+          check_swizzle_permute]
 
 
 @pytest.mark.parametrize("check", CHECKS, ids=lambda f: f.__name__)

@@ -58,6 +58,10 @@ MUTANTS = [
      "const int64_t off = (p + 1) % B;\n      if (blk < 0"),
     ("gather_scale_byte_order", "k_scale[row * 4 + k] = block[B * D + off * 4 + k];",
      "k_scale[row * 4 + k] = block[B * D + off * 4 + (3 - k)];"),
+    ("f16_exponent_bias", "ldexp(1.0 + (double)m / 1024.0, e - 15)",
+     "ldexp(1.0 + (double)m / 1024.0, e - 14)"),
+    ("f16_subnormal_scale", "v = ldexp((double)m, -24);",
+     "v = ldexp((double)m, -23);"),
     ("gather_row_bytes", "k_fp8[row * D + d] = block[off * D + d];",
      "k_fp8[row * D + d] = block[off * D + (d ^ 1)];"),
 ]

@@ -16,7 +16,7 @@ import numpy as np
 import pytest
 
 from paged_quantized_kv_gb300 import workloads as W
-from tests.golden_io import as_bf16_bits, nvfp4_groups
+from tests.golden_io import as_bits, nvfp4_groups
 
 E2M1 = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
 
@@ -35,15 +35,15 @@ def unpack(data8):
 
 
 def check_golden_groups(o):
-    for name, g, xs, sf, data in nvfp4_groups():
-        got_data, got_sf = o.quantize_group(as_bf16_bits(xs), g)
+    for name, g, xs, sf, data, dtype in nvfp4_groups():
+        got_data, got_sf = o.quantize_group(as_bits(xs, dtype), g, dtype)
         assert got_sf == sf, (name, hex(got_sf), hex(sf))
         assert bytes(got_data) == data, (name, bytes(got_data).hex(),
                                          data.hex())
 
 
-def _groups(rng, n):
-    """Random bf16 groups from several value distributions."""
+def _groups(rng, n, dtype=W.DTYPE_BF16):
+    """Random bf16 (or fp16) groups from several value distributions."""
     kinds = [
         lambda: rng.standard_normal(16),
         lambda: rng.standard_normal(16) * np.where(rng.random(16) < .1, 50, 1),
@@ -53,7 +53,9 @@ def _groups(rng, n):
     ]
     for i in range(n):
         x = kinds[i % len(kinds)]().astype(np.float32)
-        yield W.bf16_bits(x)
+        if dtype == W.DTYPE_F16:
+            x = np.clip(x, -60000, 60000)
+        yield W.element_bits(x, dtype)
 
 
 def check_error_bound(o):
@@ -61,11 +63,13 @@ def check_error_bound(o):
     e4m3_min_normal = 2.0 ** -6
     checked = 0
     vals = np.array([o.e4m3_decode(c) for c in range(127)])
-    for g in (1.0, 0.37, 13.0, 580.0, 2.0 ** -5):
+    cases = [(g, W.DTYPE_BF16) for g in (1.0, 0.37, 13.0, 580.0, 2.0 ** -5)]
+    cases += [(g, W.DTYPE_F16) for g in (1.0, 41.0)]
+    for g, dtype in cases:
         g32 = float(np.float32(g))
-        for bits in _groups(rng, 300):
-            x = W.bf16_values(bits).astype(np.float64)
-            data, sf = o.quantize_group(bits, g32)
+        for bits in _groups(rng, 300, dtype):
+            x = W.element_values(bits, dtype).astype(np.float64)
+            data, sf = o.quantize_group(bits, g32, dtype)
             s = o.e4m3_decode(sf)
             amax = np.abs(x).max()
             target = amax * g32 / 6.0  # exact-arithmetic scale
@@ -144,7 +148,7 @@ def expected_cache(o, wl, sentinel=0xAA):
             for h in range(wl.num_heads):
                 for j in range(wl.head_size // 16):
                     d8, sf = o.quantize_group(src[t, h, 16 * j:16 * j + 16],
-                                              g[side])
+                                              g[side], wl.dtype)
                     data_row(blk, h, off)[8 * j: 8 * j + 8] = d8
                     tile = scale_tile(blk, h)
                     if swz:
@@ -161,7 +165,7 @@ def run_store(o, wl, sentinel=0xAA):
                   wl.value_side_offset, wl.page_stride, wl.block_size,
                   wl.num_blocks, wl.layout, wl.slot_mapping, wl.k_scale,
                   wl.v_scale, wl.flags, key_base=wl.key_offset,
-                  value_base=wl.value_offset)
+                  value_base=wl.value_offset, dtype=wl.dtype)
     return cache
 
 
@@ -176,6 +180,9 @@ SMALL_CASES = [
     dict(name="nhd_swzk_stride", seed=4, num_tokens=9, num_heads=2,
          head_size=64, block_size=8, num_blocks=3, row_mult=2,
          layout=W.LAYOUT_NHD, flags=1),
+    dict(name="fp16_hnd", seed=5, num_tokens=11, num_heads=2, head_size=128,
+         block_size=8, num_blocks=4, skip=1, dtype=W.DTYPE_F16,
+         scales=(0.02, 3.0)),
 ]
 
 

@@ -32,6 +32,29 @@ def test_named_workload(orc, index):
     _compare(orc, W.store_workload(index))
 
 
+FP16_CASES = [
+    dict(name="fp16_decode_shape", seed=50, num_tokens=256, num_heads=8,
+         head_size=128, block_size=16, num_blocks=4096),
+    dict(name="fp16_prefill_shape", seed=51, num_tokens=4096, num_heads=8,
+         head_size=128, block_size=16, num_blocks=1024, slots="runs",
+         request_len=1024, row_mult=2, outlier_p=1e-3, outlier_mult=50.0),
+    dict(name="fp16_long_shape_nhd", seed=52, num_tokens=8192, num_heads=4,
+         head_size=256, block_size=32, num_blocks=512, slots="runs",
+         request_len=512, layout=W.LAYOUT_NHD),
+    dict(name="fp16_ragged_odd_heads", seed=53, num_tokens=37, num_heads=3,
+         head_size=64, block_size=16, num_blocks=9, skip=5, flags=1),
+    dict(name="fp16_tiny_scale", seed=54, num_tokens=16, num_heads=2,
+         head_size=64, block_size=8, num_blocks=4, scales=(1e-4, 3e-5)),
+]
+
+
+@pytest.mark.parametrize("case", FP16_CASES, ids=lambda c: c["name"])
+def test_fp16_input(orc, case):
+    c = dict(case)
+    _compare(orc, W.make_store(c.pop("name"), c.pop("seed"),
+                               dtype=W.DTYPE_F16, **c))
+
+
 EDGE_CASES = SMALL_CASES + [
     dict(name="one_token", seed=10, num_tokens=1, num_heads=1, head_size=64,
          block_size=4, num_blocks=3),
@@ -163,19 +186,33 @@ def test_every_bf16_amax(orc, scale):
     _probe_store(orc, groups, scale)
 
 
-def _probe_store(orc, groups, scale):
+@pytest.mark.parametrize("scale", [1.0, 2.0 ** -20])
+def test_every_fp16_amax(orc, scale):
+    """One group per finite non-negative fp16 amax (31744 groups), fp16
+    inputs (subnormals included)."""
+    bits = np.arange(0, 0x7C00, dtype=np.uint32).astype(np.uint16)
+    a = bits.view(np.float16).astype(np.float32)
+    groups = np.zeros((a.size, 16), np.float32)
+    groups[:, 0] = a
+    groups[:, 5] = -a * np.float32(0.375)
+    groups[:, 11] = a * np.float32(0.5)
+    groups[:, 14] = -a
+    _probe_store(orc, groups, scale, dtype=W.DTYPE_F16)
+
+
+def _probe_store(orc, groups, scale, dtype=W.DTYPE_BF16):
     """Store each 16-value group as one head of one token (H=1, D=16*...)."""
     n = groups.shape[0]
     per_tok = 4                          # head_size 64 = 4 groups
     T = -(-n // per_tok)
     x = np.zeros((T * per_tok, 16), np.float32)
     x[:n] = groups
-    bits = W.bf16_bits(x.reshape(-1))
+    bits = W.element_bits(x.reshape(-1), dtype)
     src = np.concatenate([bits, bits[::-1].copy()])
     wl = W.StoreWorkload(
         name="probe", num_tokens=T, num_heads=1, head_size=64, block_size=4,
         num_blocks=-(-T // 4), src=src, key_offset=0, key_stride0=64,
         value_offset=T * 64, value_stride0=64,
         slot_mapping=np.arange(T, dtype=np.int64),
-        k_scale=np.float32(scale), v_scale=np.float32(scale))
+        k_scale=np.float32(scale), v_scale=np.float32(scale), dtype=dtype)
     _compare(orc, wl)
