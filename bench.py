@@ -295,6 +295,21 @@ def run_ours(args):
     plain = {"step_ms": span_ms(lambda i: step(i, 0), K),
              "store_ms": span_ms(lambda i: store(0), K),
              "gather_ms": span_ms(lambda i: gather(i, 0), K)}
+    # the store's other input type and cache layout, same shape
+    key16 = key.to(torch.float16)
+    value16 = value.to(torch.float16)
+    kv_n, kc_n, vc_n = kvq.alloc_nvfp4_cache(
+        st.num_blocks, st.block_size, H, D, layout=kvq.KVQ_LAYOUT_NHD,
+        device=dev, fill=0xAA)
+    variants_ms = {
+        "store_fp16_hnd": span_ms(lambda i: kvq.kvq_store_nvfp4(
+            key16, value16, kc, vc, slots, ks, vs, flags=PDL,
+            dev_error=dev_err, stream=sh), K),
+        "store_bf16_nhd": span_ms(lambda i: kvq.kvq_store_nvfp4(
+            key, value, kc_n, vc_n, slots, ks, vs, flags=PDL,
+            dev_error=dev_err, stream=sh), K),
+    }
+    del key16, value16, kv_n, kc_n, vc_n
     # keep the same steps running so the clock sampler sees the load
     t1 = time.perf_counter()
     j = 0
@@ -373,6 +388,11 @@ def run_ours(args):
                 "algorithmic_bytes": ga_bytes},
         },
         "without_pdl": {k: round(v, 5) for k, v in plain.items()},
+        "store_variants": {
+            k: {"ms": round(v, 5),
+                "GB_s": round(st_bytes / v / 1e6, 1),
+                "frac_of_peak": round(st_bytes / v / 1e6 / peak, 4)}
+            for k, v in variants_ms.items()},
         "single_launch_after_l2_write_flush": {
             "note": "each kernel alone after writing a 256 MiB buffer "
                     "(L2 left dirty), events around the launch; includes "
