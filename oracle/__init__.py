@@ -14,6 +14,9 @@ passage each function restates:
   ``reshape_and_cache_nvfp4_dispatch``.
 * vLLM PR #25931 "Add gather_indexer_k_quant_cache kernel" and PR #26456
   "[Deepseek-V3.2][Kernel] Integrate cuda indexer k cache gather".
+* The NVFP4 paged load (the read side of the store) follows the same page
+  layout and swizzle; its dequantisation rule is the plain inverse of the
+  store's (the pages state none).
 
 Parity status: every function here is pinned by ``tests/test_oracle_*.py``
 (format tables against closed forms and torch's float8 cast, hand-worked
@@ -102,6 +105,13 @@ class Oracle:
             P, c.c_int64, c.c_int64, c.c_int32, c.c_int32, P, c.c_int64,
             c.c_int32, P, c.c_int32, c.c_int64, P, P]
         lib.kvqo_gather_indexer_k.restype = c.c_int
+        lib.kvqo_float_to_bf16.argtypes = [c.c_float]
+        lib.kvqo_float_to_bf16.restype = c.c_uint16
+        lib.kvqo_load_nvfp4.argtypes = [
+            P, P, c.c_int64, c.c_int32, c.c_int64, c.c_int32, c.c_int32,
+            c.c_int32, P, c.c_int64, c.c_int32, P, c.c_int32, c.c_int64,
+            c.c_float, c.c_float, c.c_uint32, P, P, c.c_int64]
+        lib.kvqo_load_nvfp4.restype = c.c_int
         self.lib = lib
         self.path = lib_path
 
@@ -147,7 +157,11 @@ class Oracle:
             raise ValueError(f"kvqo_quantize_group failed: {rc}")
         return data, int(sf[0])
 
-    # --- the two operations -------------------------------------------------
+    def float_to_bf16(self, v: float) -> int:
+        """fp32 -> bf16 bits, round to nearest even."""
+        return int(self.lib.kvqo_float_to_bf16(float(np.float32(v))))
+
+    # --- the operations -----------------------------------------------------
     def store_nvfp4(self, key_bits: np.ndarray, key_stride0: int,
                     value_bits: np.ndarray, value_stride0: int,
                     num_tokens: int, num_heads: int, head_size: int,
@@ -201,6 +215,30 @@ class Oracle:
         if rc != OK:
             raise ValueError(f"kvqo_gather_indexer_k failed: {rc}")
 
+    def load_nvfp4(self, kv_cache: np.ndarray, key_offset: int,
+                   value_offset: int, page_stride: int, block_size: int,
+                   num_blocks: int, layout: int, num_heads: int,
+                   head_size: int, block_table: np.ndarray,
+                   cu_seq_lens: np.ndarray, total_tokens: int,
+                   k_scale: float, v_scale: float, flags: int = 0):
+        """NVFP4 paged load: returns (key, value) bf16 bit arrays
+        [total_tokens, H, D] (uint16), rows of sequences in cu_seq_lens order;
+        rows no sequence covers stay 0."""
+        bt = np.ascontiguousarray(block_table, dtype=np.int32)
+        cu = np.ascontiguousarray(cu_seq_lens, dtype=np.int32)
+        H, D = num_heads, head_size
+        k = np.zeros((max(total_tokens, 1), H, D), dtype=np.uint16)
+        v = np.zeros((max(total_tokens, 1), H, D), dtype=np.uint16)
+        rc = self.lib.kvqo_load_nvfp4(
+            _ptr(kv_cache, key_offset), _ptr(kv_cache, value_offset),
+            int(page_stride), int(block_size), int(num_blocks), int(layout),
+            int(H), int(D), _ptr(bt), int(bt.shape[1]), int(bt.shape[1]),
+            _ptr(cu), int(cu.size - 1), int(total_tokens),
+            float(np.float32(k_scale)), float(np.float32(v_scale)), int(flags),
+            _ptr(k), _ptr(v), H * D)
+        if rc != OK:
+            raise ValueError(f"kvqo_load_nvfp4 failed: {rc}")
+        return k[:total_tokens], v[:total_tokens]
 
 _default = None
 _lock = threading.Lock()
@@ -213,3 +251,4 @@ def get() -> Oracle:
         if _default is None:
             _default = Oracle(build())
         return _default
+

@@ -325,3 +325,94 @@ int kvqo_gather_indexer_k(const uint8_t* cache, int64_t block_stride,
   }
   return KVQO_OK;
 }
+
+/* ------------------------------------------------------------------------ */
+/* NVFP4 paged load -- the read side of the store ([nvfp4-cu] page layout   */
+/* and swizzle; the pages give no dequantisation rule, so this is the plain */
+/* inverse of the store's: x' = e2m1(q) * (float(sf) * k_scale), the scale  */
+/* product and the element product each one fp32 rounding, then rounded to  */
+/* bf16, nearest-even).                                                     */
+/*                                                                          */
+/* Sequence b's token p (0 <= p < cu[b+1]-cu[b]) is output row cu[b] + p,   */
+/* read from page block_table[b*bt_stride + p/B], offset p%B.  key_out /     */
+/* value_out: bf16 bits [total, H, D] with row stride out_stride0 elements. */
+/* ------------------------------------------------------------------------ */
+
+/* fp32 -> bf16 bits, round to nearest even (NaN -> quiet NaN). */
+static uint16_t float_to_bf16(float f) {
+  uint32_t u;
+  memcpy(&u, &f, sizeof u);
+  if ((u & 0x7FFFFFFFu) > 0x7F800000u) return (uint16_t)((u >> 16) | 0x40);
+  uint32_t lsb = (u >> 16) & 1u;
+  return (uint16_t)((u + 0x7FFFu + lsb) >> 16);
+}
+
+uint16_t kvqo_float_to_bf16(float f) { return float_to_bf16(f); }
+
+int kvqo_load_nvfp4(const uint8_t* key_cache, const uint8_t* value_cache,
+                    int64_t page_stride, int32_t block_size,
+                    int64_t num_blocks, int32_t layout, int32_t num_heads,
+                    int32_t head_size, const int32_t* block_table,
+                    int64_t bt_stride, int32_t max_blocks_per_seq,
+                    const int32_t* cu_seq_lens, int32_t num_seqs,
+                    int64_t total_tokens, float k_scale, float v_scale,
+                    uint32_t flags, uint16_t* key_out, uint16_t* value_out,
+                    int64_t out_stride0) {
+  if (num_heads <= 0 || head_size <= 0 || block_size <= 0 || num_seqs < 0)
+    return KVQO_ERR_ARG;
+  if (head_size % 64 != 0 || block_size % 4 != 0) return KVQO_ERR_ARG;
+  if (layout != KVQO_LAYOUT_HND && layout != KVQO_LAYOUT_NHD)
+    return KVQO_ERR_ARG;
+  const int64_t H = num_heads, D = head_size, B = block_size;
+  const int64_t data_dim = D / 2, S = D / 16;
+  int64_t dhs, dts, shs, sts;
+  if (layout == KVQO_LAYOUT_HND) {
+    dhs = B * data_dim; dts = data_dim;
+    shs = B * S;        sts = S;
+  } else {
+    dhs = data_dim;     dts = H * data_dim;
+    shs = S;            sts = H * S;
+  }
+  const int64_t data_per_side = H * B * data_dim;
+  const float side_scale[2] = {k_scale, v_scale};
+
+  for (int32_t b = 0; b < num_seqs; ++b) {
+    const int64_t start = cu_seq_lens[b];
+    const int64_t len = (int64_t)cu_seq_lens[b + 1] - start;
+    for (int64_t p = 0; p < len; ++p) {
+      const int64_t row = start + p;
+      if (row < 0 || row >= total_tokens) return KVQO_ERR_BOUNDS;
+      if (p / B >= max_blocks_per_seq) return KVQO_ERR_BOUNDS;
+      const int64_t blk = block_table[b * bt_stride + p / B];
+      const int64_t off = p % B;
+      if (blk < 0 || blk >= num_blocks) return KVQO_ERR_BOUNDS;
+      for (int side = 0; side < 2; ++side) {
+        const uint8_t* page =
+            (side == 0 ? key_cache : value_cache) + blk * page_stride;
+        const uint8_t* scale_page = page + data_per_side;
+        uint16_t* out = (side == 0 ? key_out : value_out) + row * out_stride0;
+        const int swizzle = (side == 1) || (flags & KVQO_F_SWIZZLE_K_SCALE);
+        for (int64_t h = 0; h < H; ++h) {
+          for (int64_t j = 0; j < S; ++j) {
+            const uint8_t* sptr;
+            if (!swizzle) {
+              sptr = scale_page + h * shs + off * sts + j;
+            } else {
+              int pos = kvqo_swizzle((int)off, (int)j, (int)S);
+              sptr = scale_page + h * shs + (pos / S) * sts + pos % S;
+            }
+            const float c = (float)kvqo_e4m3_decode(*sptr) * side_scale[side];
+            const uint8_t* dptr = page + h * dhs + off * dts + 8 * j;
+            for (int k = 0; k < 16; ++k) {
+              const uint8_t byte = dptr[k / 2];
+              const uint8_t nib = (k % 2 == 0) ? (byte & 0xF) : (byte >> 4);
+              const float v = (float)kvqo_e2m1_decode(nib) * c;
+              out[h * D + 16 * j + k] = float_to_bf16(v);
+            }
+          }
+        }
+      }
+    }
+  }
+  return KVQO_OK;
+}

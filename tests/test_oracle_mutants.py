@@ -8,11 +8,13 @@ import pytest
 import oracle
 from tests import test_oracle_formats as F
 from tests import test_oracle_gather as G
+from tests import test_oracle_load as L
 from tests import test_oracle_store as S
 
-ALL_CHECKS = F.CHECKS + S.CHECKS + G.CHECKS
+ALL_CHECKS = F.CHECKS + S.CHECKS + G.CHECKS + L.CHECKS
 
-# (id, original text, planted mistake) -- every original occurs exactly once
+# (id, original text, planted mistake[, occurrence]) -- the mistake is
+# planted at the given occurrence of the original (default: the only one)
 MUTANTS = [
     ("scale_divides_by_g", "float sfv = (amax / 6.0f) * g;",
      "float sfv = (amax / 6.0f) / g;"),
@@ -43,9 +45,16 @@ MUTANTS = [
      "int col = (s % q) * 4 + (t + 1) % 4;"),
     ("swizzles_k_not_v",
      "const int swizzle = (side == 1) || (flags & KVQO_F_SWIZZLE_K_SCALE);",
-     "const int swizzle = (side == 0) || (flags & KVQO_F_SWIZZLE_K_SCALE);"),
+     "const int swizzle = (side == 0) || (flags & KVQO_F_SWIZZLE_K_SCALE);",
+     0),
+    ("load_swizzles_k_not_v",
+     "const int swizzle = (side == 1) || (flags & KVQO_F_SWIZZLE_K_SCALE);",
+     "const int swizzle = (side == 0) || (flags & KVQO_F_SWIZZLE_K_SCALE);",
+     1),
     ("nhd_as_hnd", "dhs = data_dim;     dts = H * data_dim;",
-     "dhs = B * data_dim; dts = data_dim;"),
+     "dhs = B * data_dim; dts = data_dim;", 0),
+    ("load_nhd_as_hnd", "dhs = data_dim;     dts = H * data_dim;",
+     "dhs = B * data_dim; dts = data_dim;", 1),
     ("scale_region_offset",
      "uint8_t* scale_page = data_page + data_per_side;",
      "uint8_t* scale_page = data_page + data_per_side / 2;"),
@@ -55,24 +64,53 @@ MUTANTS = [
     ("skip_rule_includes_zero", "if (slot < 0) continue;",
      "if (slot <= 0) continue;"),
     ("gather_offset", "const int64_t off = p % B;\n      if (blk < 0",
-     "const int64_t off = (p + 1) % B;\n      if (blk < 0"),
+     "const int64_t off = (p + 1) % B;\n      if (blk < 0", 0),
     ("gather_scale_byte_order", "k_scale[row * 4 + k] = block[B * D + off * 4 + k];",
      "k_scale[row * 4 + k] = block[B * D + off * 4 + (3 - k)];"),
     ("f16_exponent_bias", "ldexp(1.0 + (double)m / 1024.0, e - 15)",
      "ldexp(1.0 + (double)m / 1024.0, e - 14)"),
     ("f16_subnormal_scale", "v = ldexp((double)m, -24);",
      "v = ldexp((double)m, -23);"),
+    ("load_unswizzle_transposed",
+     "sptr = scale_page + h * shs + (pos / S) * sts + pos % S;",
+     "sptr = scale_page + h * shs + (pos % S) * sts + pos / S;"),
+    ("load_k_uses_v_scale",
+     "const float side_scale[2] = {k_scale, v_scale};",
+     "const float side_scale[2] = {v_scale, v_scale};"),
+    ("load_nibble_order",
+     "(k % 2 == 0) ? (byte & 0xF) : (byte >> 4)",
+     "(k % 2 == 0) ? (byte >> 4) : (byte & 0xF)"),
+    ("bf16_cast_truncates",
+     "return (uint16_t)((u + 0x7FFFu + lsb) >> 16);",
+     "return (uint16_t)(u >> 16);"),
+    ("load_divides_by_scale",
+     "const float c = (float)kvqo_e4m3_decode(*sptr) * side_scale[side];",
+     "const float c = (float)kvqo_e4m3_decode(*sptr) / side_scale[side];"),
+    ("load_block_offset", "const int64_t off = p % B;\n      if (blk < 0",
+     "const int64_t off = (p + 1) % B;\n      if (blk < 0", 1),
     ("gather_row_bytes", "k_fp8[row * D + d] = block[off * D + d];",
      "k_fp8[row * D + d] = block[off * D + (d ^ 1)];"),
 ]
 
 
-@pytest.mark.parametrize("mid,orig,mutant", MUTANTS, ids=[m[0] for m in MUTANTS])
-def test_pins_catch_planted_mistake(tmp_path, mid, orig, mutant):
+def _plant(src, orig, mutant, occurrence):
+    parts = src.split(orig)
+    if occurrence is None:
+        assert len(parts) == 2, "ambiguous original"
+        occurrence = 0
+    assert len(parts) > occurrence + 1, "occurrence not found"
+    head = orig.join(parts[: occurrence + 1])
+    tail = orig.join(parts[occurrence + 1:])
+    return head + mutant + tail
+
+
+@pytest.mark.parametrize("mutant", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_pins_catch_planted_mistake(tmp_path, mutant):
+    mid, orig, planted = mutant[:3]
+    occurrence = mutant[3] if len(mutant) > 3 else None
     src = open(oracle.SOURCE).read()
-    assert src.count(orig) == 1, mid
     path = tmp_path / f"kvq_oracle_{mid}.c"
-    path.write_text(src.replace(orig, mutant))
+    path.write_text(_plant(src, orig, planted, occurrence))
     so = oracle.compile_oracle(str(path), str(tmp_path / f"lib_{mid}.so"))
     o = oracle.Oracle(so)
     caught = None
