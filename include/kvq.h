@@ -8,6 +8,8 @@
  *                         (vLLM csrc/libtorch_stable/nvfp4_kv_cache_kernels.cu,
  *                         commit 7ce4c8e: reshape_and_cache_nvfp4_kernel and
  *                         reshape_and_cache_nvfp4_dispatch).
+ *   kvq_load_nvfp4        the read side of the store: NVFP4 pages named by a
+ *                         block table -> bf16 K/V rows.
  *   kvq_gather_indexer_k  fp8 indexer-K rows and per-token fp32 scales
  *                         gathered out of a paged cache (vLLM PR #25931 "Add
  *                         gather_indexer_k_quant_cache kernel"; PR #26456
@@ -73,11 +75,12 @@ enum {
      PDL-launched kernel to do the same.  Useful when these calls run back
      to back with other kernels on one stream. */
   KVQ_F_PDL = 1u << 1,
-  /* kvq_gather_indexer_k only; implies KVQ_F_PDL.  The caller promises that
+  /* kvq_gather_indexer_k and kvq_load_nvfp4; implies KVQ_F_PDL.  The caller
+     promises that
      block_table and cu_seq_lens are not written by the kernel that runs
      just before this call on the stream (they are ready before it starts),
-     so the kernel stages and resolves them while that kernel finishes and
-     waits only before it reads the cache or writes anything. */
+     so the kernel stages them while that kernel finishes and waits only
+     before it reads the cache or the scales, or writes anything. */
   KVQ_F_PDL_EARLY_META = 1u << 2
 };
 
@@ -188,6 +191,50 @@ kvq_status kvq_gather_indexer_k(const uint8_t* kv_cache, int64_t block_stride,
                                 int64_t total_tokens, uint8_t* k_fp8,
                                 uint8_t* k_scale, uint32_t flags,
                                 int32_t* dev_error, void* stream);
+
+/*
+ * kvq_load_nvfp4 -- the read side of kvq_store_nvfp4: gather the tokens a
+ * block table names out of NVFP4 pages and dequantise them to bf16 rows.
+ * (Page layout, strides and scale swizzle: vLLM nvfp4_kv_cache_kernels.cu,
+ * commit 7ce4c8e, as for the store.  The pages state no dequantisation
+ * rule; this is the plain inverse of the store's.)
+ *
+ * For sequence b and position p in [0, cu_seq_lens[b+1] - cu_seq_lens[b]),
+ * output row i = cu_seq_lens[b] + p reads page blk = block_table[b *
+ * block_table_stride + p / block_size], offset off = p % block_size; for
+ * each side, head h and group j, with s = float(scale byte) (linear or
+ * swizzled position as the store wrote it) and c = s * k_scale[0] (or
+ * v_scale[0]) in fp32:
+ *   out[i, h, 16j + k] = bf16_rn(e2m1(q_k) * c)   (fp32 product, then
+ *                                                   round to nearest even)
+ *
+ * key_cache, value_cache, page_stride, block_size, num_blocks, layout,
+ * num_heads, head_size   as for kvq_store_nvfp4.
+ * block_table, block_table_stride, max_blocks_per_seq, cu_seq_lens,
+ * num_seqs, total_tokens   as for kvq_gather_indexer_k.
+ * k_scale, v_scale  device fp32 scalars (the store's).
+ * out_dtype       KVQ_DTYPE_BF16.
+ * key_out, value_out  [total_tokens, num_heads, head_size] rows,
+ *                 out_stride0 elements apart (>= H*D, multiple of 8);
+ *                 16-byte aligned.
+ * flags           KVQ_F_SWIZZLE_K_SCALE (the pages were stored with it),
+ *                 KVQ_F_PDL, KVQ_F_PDL_EARLY_META, or 0.
+ * dev_error       nullable (KVQ_DEVERR_BLOCK | KVQ_DEVERR_SEQ |
+ *                 KVQ_DEVERR_TIMEOUT); rows it names are left unwritten.
+ * total_tokens == 0 returns KVQ_OK without launching.
+ */
+kvq_status kvq_load_nvfp4(const uint8_t* key_cache, const uint8_t* value_cache,
+                          int64_t page_stride, int32_t block_size,
+                          int64_t num_blocks, int32_t layout,
+                          int32_t num_heads, int32_t head_size,
+                          const int32_t* block_table,
+                          int64_t block_table_stride,
+                          int32_t max_blocks_per_seq,
+                          const int32_t* cu_seq_lens, int32_t num_seqs,
+                          int64_t total_tokens, const float* k_scale,
+                          const float* v_scale, int32_t out_dtype,
+                          void* key_out, void* value_out, int64_t out_stride0,
+                          uint32_t flags, int32_t* dev_error, void* stream);
 
 /* Static text for a status code. */
 const char* kvq_status_string(kvq_status status);

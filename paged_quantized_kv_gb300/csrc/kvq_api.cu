@@ -194,6 +194,107 @@ kvq_status kvq_gather_indexer_k(const uint8_t* kv_cache, int64_t block_stride,
   return err == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
 }
 
+kvq_status kvq_load_nvfp4(const uint8_t* key_cache, const uint8_t* value_cache,
+                          int64_t page_stride, int32_t block_size,
+                          int64_t num_blocks, int32_t layout,
+                          int32_t num_heads, int32_t head_size,
+                          const int32_t* block_table,
+                          int64_t block_table_stride,
+                          int32_t max_blocks_per_seq,
+                          const int32_t* cu_seq_lens, int32_t num_seqs,
+                          int64_t total_tokens, const float* k_scale,
+                          const float* v_scale, int32_t out_dtype,
+                          void* key_out, void* value_out, int64_t out_stride0,
+                          uint32_t flags, int32_t* dev_error, void* stream) {
+  using namespace kvq;
+  if (out_dtype != KVQ_DTYPE_BF16) return KVQ_ERR_DTYPE;
+  if (layout != KVQ_LAYOUT_HND && layout != KVQ_LAYOUT_NHD)
+    return KVQ_ERR_LAYOUT;
+  if ((flags & ~static_cast<uint32_t>(KVQ_F_SWIZZLE_K_SCALE | KVQ_F_PDL |
+                                      KVQ_F_PDL_EARLY_META)) != 0u)
+    return KVQ_ERR_ARG;
+  if (num_heads <= 0 || head_size <= 0 || block_size <= 0 ||
+      num_blocks < 0 || num_seqs < 0 || total_tokens < 0 ||
+      max_blocks_per_seq < 0 || block_table_stride < max_blocks_per_seq)
+    return KVQ_ERR_SHAPE;
+  if (head_size % 64 != 0 || block_size % 4 != 0) return KVQ_ERR_SHAPE;
+  const int64_t H = num_heads, D = head_size, B = block_size;
+  const int64_t S = D / 16;
+  if (page_stride < H * B * (D / 2 + S)) return KVQ_ERR_SHAPE;
+  if (out_stride0 < H * D) return KVQ_ERR_SHAPE;
+  const int64_t gpt = 2 * H * S;
+  if (gpt > (int64_t{1} << 20) || total_tokens >= (int64_t{1} << 31))
+    return KVQ_ERR_SHAPE;
+  if (total_tokens == 0) return KVQ_OK;
+  if (num_seqs == 0) return KVQ_ERR_ARG;
+  if (key_cache == nullptr || value_cache == nullptr ||
+      block_table == nullptr || cu_seq_lens == nullptr ||
+      k_scale == nullptr || v_scale == nullptr || key_out == nullptr ||
+      value_out == nullptr)
+    return KVQ_ERR_NULL;
+  if (!aligned(key_cache, 16) || !aligned(value_cache, 16) ||
+      page_stride % 16 != 0 || !aligned(key_out, 16) ||
+      !aligned(value_out, 16) || out_stride0 % 8 != 0 ||
+      !aligned(block_table, 4) || !aligned(cu_seq_lens, 4) ||
+      !aligned(k_scale, 4) || !aligned(v_scale, 4))
+    return KVQ_ERR_ALIGN;
+
+  LoadParams p{};
+  p.side[0] = key_cache;
+  p.side[1] = value_cache;
+  p.out[0] = static_cast<uint16_t*>(key_out);
+  p.out[1] = static_cast<uint16_t*>(value_out);
+  p.scale[0] = k_scale;
+  p.scale[1] = v_scale;
+  p.block_table = block_table;
+  p.cu = cu_seq_lens;
+  p.dev_error = dev_error;
+  p.bt_stride = block_table_stride;
+  p.page_stride = page_stride;
+  p.num_blocks = num_blocks;
+  p.data_per_side = H * B * (D / 2);
+  if (layout == KVQ_LAYOUT_HND) {
+    p.dhs = B * (D / 2);
+    p.dts = D / 2;
+    p.shs = B * S;
+    p.sts = S;
+  } else {
+    p.dhs = D / 2;
+    p.dts = H * (D / 2);
+    p.shs = S;
+    p.sts = H * S;
+  }
+  p.out_stride0 = out_stride0;
+  p.total = total_tokens;
+  p.H = num_heads;
+  p.D = head_size;
+  p.S = static_cast<int32_t>(S);
+  p.B = block_size;
+  p.b_shift = ilog2_exact(B);
+  p.gpt = static_cast<int32_t>(gpt);
+  if (gpt <= 256) {
+    p.tpp = static_cast<int32_t>(256 / gpt);
+    p.slices_log2 = 0;
+  } else {
+    p.tpp = 1;
+    int sl = 0;
+    while ((int64_t{256} << sl) < gpt) ++sl;
+    p.slices_log2 = sl;
+  }
+  const int64_t passes =
+      ((total_tokens + p.tpp - 1) / p.tpp) << p.slices_log2;
+  if (passes >= (int64_t{1} << 31)) return KVQ_ERR_SHAPE;
+  p.num_passes = static_cast<int32_t>(passes);
+  p.num_seqs = num_seqs;
+  p.max_blocks = max_blocks_per_seq;
+  p.swizzle_sides = 2u | ((flags & KVQ_F_SWIZZLE_K_SCALE) ? 1u : 0u);
+  p.early_meta = (flags & KVQ_F_PDL_EARLY_META) != 0u;
+  p.pdl = p.early_meta || (flags & KVQ_F_PDL) != 0u;
+  const cudaError_t err =
+      launch_load_nvfp4(p, static_cast<cudaStream_t>(stream));
+  return err == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
+}
+
 const char* kvq_status_string(kvq_status status) {
   switch (status) {
     case KVQ_OK: return "ok";

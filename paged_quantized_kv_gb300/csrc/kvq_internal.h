@@ -60,6 +60,33 @@ struct GatherParams {
 cudaError_t launch_gather_indexer_k(const GatherParams& p,
                                     cudaStream_t stream);
 
+// ---------------------------------------------------------------------------
+// NVFP4 paged load (dequantise pages back to bf16 rows)
+// ---------------------------------------------------------------------------
+struct LoadParams {
+  const uint8_t* side[2];  // page 0 of the K side / V side
+  uint16_t* out[2];        // bf16 key / value rows
+  const float* scale[2];   // device k_scale / v_scale
+  const int32_t* block_table;
+  const int32_t* cu;
+  int32_t* dev_error;      // nullable
+  int64_t bt_stride;
+  int64_t page_stride;
+  int64_t num_blocks;
+  int64_t data_per_side;
+  int64_t dhs, dts, shs, sts;
+  int64_t out_stride0;     // elements
+  int64_t total;
+  int32_t H, D, S, B;
+  int32_t b_shift;
+  int32_t gpt, tpp, slices_log2, num_passes;
+  int32_t num_seqs, max_blocks;
+  uint32_t swizzle_sides;
+  bool pdl, early_meta;
+};
+
+cudaError_t launch_load_nvfp4(const LoadParams& p, cudaStream_t stream);
+
 // Streaming-multiprocessor count of the current device (cached per device).
 int sm_count();
 

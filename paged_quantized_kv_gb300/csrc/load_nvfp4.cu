@@ -1,0 +1,304 @@
+// load_nvfp4.cu -- NVFP4 paged cache -> bf16 rows (the read side of the
+// store), sm_103a.
+//
+// Operation: the pages written by reshape_and_cache_nvfp4 (vLLM
+// csrc/libtorch_stable/nvfp4_kv_cache_kernels.cu, commit 7ce4c8e: page
+// layout [K_data | K_scale | V_data | V_scale], HND/NHD strides, V scales
+// swizzled inside each head's [block_size, S] tile) are read back for the
+// tokens a block table names and dequantised.  The pages state no
+// dequantisation rule; this takes the plain inverse of the store's:
+// x' = bf16_rn(e2m1(q) * (float(sf) * k_scale)) -- the scale product and
+// the element product are each one fp32 rounding, then round-to-nearest-even
+// to bf16.  Output row cu_seq_lens[b] + p is token p of sequence b, read
+// from page block_table[b, p / B], offset p % B.
+//
+// GB300 design: HBM-bound, 0.5625 B read and 2 B written per element.
+//   * Persistent grid; every thread owns one fixed 16-element group role
+//     (side, head, group) and walks output rows with a grid stride, kUnroll
+//     rows in flight (8 data bytes + 1 scale byte each) before any of them
+//     is used.
+//   * cu_seq_lens and the block table are staged in shared memory once per
+//     CTA (TMA bulk copies, shared with the indexer gather); each row is
+//     resolved with a binary search in shared memory, in lockstep across the
+//     lanes that share the row.
+//   * e2m1 -> f16x2 with cvt.rn.f16x2.e2m1x2 (exact), widened to fp32,
+//     times the group's fp32 scale with mul.rn.f32x2, packed to bf16x2 with
+//     cvt.rn.bf16x2.f32; each thread writes its group's 32 bytes with one
+//     256-bit store when the rows are 32-byte aligned.
+//   * KVQ_F_PDL / KVQ_F_PDL_EARLY_META as for the gather (the scales and the
+//     cache are read only after the wait).
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "kvq_device.cuh"
+#include "kvq_internal.h"
+#include "kvq.h"
+
+namespace kvq {
+namespace {
+
+using namespace kvq::dev;
+
+constexpr int kThreads = 256;
+constexpr int kUnroll = 4;
+
+__device__ __forceinline__ void ld_nc_8(const void* p, uint32_t& a,
+                                        uint32_t& b) {
+  asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0, %1}, [%2];"
+               : "=r"(a), "=r"(b)
+               : "l"(p));
+}
+
+__device__ __forceinline__ uint32_t ld_nc_u8(const void* p) {
+  uint32_t v;
+  asm volatile("ld.global.nc.u8 %0, [%1];" : "=r"(v) : "l"(p));
+  return v;
+}
+
+// e4m3 code -> fp32 (exact: every e4m3 value is an f16 value).
+__device__ __forceinline__ float e4m3_value(uint32_t code) {
+  uint32_t h2;
+  uint16_t in = static_cast<uint16_t>(code & 0xFFu);
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(in));
+  float f;
+  asm("{ .reg .f16 lo, hi;\n"
+      "  mov.b32 {lo, hi}, %1;\n"
+      "  cvt.f32.f16 %0, lo; }"
+      : "=f"(f)
+      : "r"(h2));
+  return f;
+}
+
+// Four bytes of e2m1 pairs (element 2k in the low nibble of byte k) times c
+// -> four bf16x2 words, element 2k in the low half of word k.
+__device__ __forceinline__ void dequant4(uint32_t bytes, uint64_t cc,
+                                         uint32_t (&out)[4]) {
+  asm("{ .reg .b8 q0, q1, q2, q3;\n"
+      "  .reg .b32 h0, h1, h2, h3;\n"
+      "  .reg .f16 a0, b0, a1, b1, a2, b2, a3, b3;\n"
+      "  .reg .f32 l0, u0, l1, u1, l2, u2, l3, u3;\n"
+      "  .reg .b64 x0, x1, x2, x3;\n"
+      "  mov.b32 {q0, q1, q2, q3}, %4;\n"
+      "  cvt.rn.f16x2.e2m1x2 h0, q0;  cvt.rn.f16x2.e2m1x2 h1, q1;\n"
+      "  cvt.rn.f16x2.e2m1x2 h2, q2;  cvt.rn.f16x2.e2m1x2 h3, q3;\n"
+      "  mov.b32 {a0, b0}, h0;  mov.b32 {a1, b1}, h1;\n"
+      "  mov.b32 {a2, b2}, h2;  mov.b32 {a3, b3}, h3;\n"
+      "  cvt.f32.f16 l0, a0;  cvt.f32.f16 u0, b0;\n"
+      "  cvt.f32.f16 l1, a1;  cvt.f32.f16 u1, b1;\n"
+      "  cvt.f32.f16 l2, a2;  cvt.f32.f16 u2, b2;\n"
+      "  cvt.f32.f16 l3, a3;  cvt.f32.f16 u3, b3;\n"
+      "  mov.b64 x0, {l0, u0};  mov.b64 x1, {l1, u1};\n"
+      "  mov.b64 x2, {l2, u2};  mov.b64 x3, {l3, u3};\n"
+      "  mul.rn.f32x2 x0, x0, %5;  mul.rn.f32x2 x1, x1, %5;\n"
+      "  mul.rn.f32x2 x2, x2, %5;  mul.rn.f32x2 x3, x3, %5;\n"
+      "  mov.b64 {l0, u0}, x0;  mov.b64 {l1, u1}, x1;\n"
+      "  mov.b64 {l2, u2}, x2;  mov.b64 {l3, u3}, x3;\n"
+      "  cvt.rn.bf16x2.f32 %0, u0, l0;  cvt.rn.bf16x2.f32 %1, u1, l1;\n"
+      "  cvt.rn.bf16x2.f32 %2, u2, l2;  cvt.rn.bf16x2.f32 %3, u3, l3; }"
+      : "=r"(out[0]), "=r"(out[1]), "=r"(out[2]), "=r"(out[3])
+      : "r"(bytes), "l"(cc));
+}
+
+template <bool kVec32>
+__device__ __forceinline__ void store_group(uint16_t* p,
+                                            const uint32_t (&w)[8]) {
+  if constexpr (kVec32) {
+    asm volatile(
+        "st.global.v8.u32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p),
+        "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]),
+        "r"(w[6]), "r"(w[7])
+        : "memory");
+  } else {
+    asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p),
+                 "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3])
+                 : "memory");
+    asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p + 8),
+                 "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+                 : "memory");
+  }
+}
+
+template <int kMode, bool kEarlyMeta, bool kVec32>
+__global__ void __launch_bounds__(kThreads)
+load_nvfp4_kernel(const LoadParams p) {
+  extern __shared__ __align__(16) uint8_t s_raw[];
+  __shared__ __align__(8) uint64_t s_bar;
+
+  if constexpr (!kEarlyMeta) pdl_prologue();
+  const int32_t* cu = p.cu;
+  int32_t* s_cu = nullptr;
+  int32_t* s_bt = nullptr;
+  bool staged = true;
+  if constexpr (kMode != kMetaGlobal) {
+    staged = stage_meta(s_raw, &s_bar, p.cu, p.num_seqs + 1, p.block_table,
+                        kMode == kMetaSharedCuBt ? p.num_seqs * p.max_blocks
+                                                 : 0,
+                        &s_cu, &s_bt);
+    cu = s_cu;
+  }
+  if constexpr (kEarlyMeta) pdl_prologue();
+  if (!staged) {
+    if (threadIdx.x == 0 && p.dev_error != nullptr)
+      atomicOr(p.dev_error, KVQ_DEVERR_TIMEOUT);
+    return;
+  }
+  if (blockIdx.x == 0 && threadIdx.x == 0 && p.dev_error != nullptr &&
+      static_cast<int64_t>(cu[p.num_seqs]) != p.total)
+    atomicOr(p.dev_error, KVQ_DEVERR_SEQ);
+
+  // ---- this thread's fixed role inside a row ------------------------------
+  const int tid = threadIdx.x;
+  const int slices = 1 << p.slices_log2;
+  int grp_in_tok, tok_sub;
+  if (slices == 1) {
+    tok_sub = tid / p.gpt;
+    grp_in_tok = tid - tok_sub * p.gpt;
+  } else {
+    tok_sub = 0;
+    grp_in_tok = (static_cast<int>(blockIdx.x) & (slices - 1)) * kThreads + tid;
+  }
+  if (tok_sub >= p.tpp || grp_in_tok >= p.gpt) return;  // idle role
+  const int gps = p.gpt >> 1;  // groups per side
+  const int side = grp_in_tok >= gps ? 1 : 0;
+  const int e = grp_in_tok - side * gps;
+  const int head = e / p.S;
+  const int j = e - head * p.S;
+  const int q = p.S >> 2;
+  const bool swz = (p.swizzle_sides >> side) & 1u;
+
+  const uint8_t* const data_role = p.side[side] + head * p.dhs + j * 8;
+  const uint8_t* const scale_role =
+      p.side[side] + p.data_per_side + head * p.shs +
+      (swz ? (j / q) * p.sts + (j % q) * 4 : static_cast<int64_t>(j));
+  uint16_t* const out_role = p.out[side] + head * p.D + j * 16;
+  const float kscale = __ldg(p.scale[side]);
+
+  const int64_t T = p.total;
+  const int64_t tstep =
+      static_cast<int64_t>(gridDim.x >> p.slices_log2) * p.tpp;
+  for (int64_t t0 = static_cast<int64_t>(blockIdx.x >> p.slices_log2) *
+                        p.tpp + tok_sub;
+       t0 < T; t0 += kUnroll * tstep) {
+    uint32_t d0[kUnroll], d1[kUnroll], sfb[kUnroll];
+    bool ok[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int64_t row = t0 + u * tstep;
+      ok[u] = false;
+      d0[u] = d1[u] = sfb[u] = 0u;
+      if (row >= T) continue;
+      const int b = find_seq<kMode != kMetaGlobal>(cu, p.num_seqs, row);
+      int err = 0;
+      if (b >= p.num_seqs) {
+        err = KVQ_DEVERR_SEQ;
+      } else {
+        const int64_t pos = row - cu[b];
+        int64_t kb, off;
+        if (p.b_shift >= 0) {
+          kb = pos >> p.b_shift;
+          off = pos & (p.B - 1);
+        } else {
+          kb = pos / p.B;
+          off = pos - kb * p.B;
+        }
+        if (pos < 0 || kb >= p.max_blocks) {
+          err = KVQ_DEVERR_SEQ;
+        } else {
+          const int64_t blk =
+              kMode == kMetaSharedCuBt
+                  ? s_bt[b * p.max_blocks + kb]
+                  : __ldg(p.block_table + b * p.bt_stride + kb);
+          if (blk < 0 || blk >= p.num_blocks) {
+            err = KVQ_DEVERR_BLOCK;
+          } else {
+            const int64_t page = blk * p.page_stride;
+            ld_nc_8(data_role + page + off * p.dts, d0[u], d1[u]);
+            const int64_t soff =
+                swz ? (off & ~int64_t{3}) * p.sts + (off & 3) : off * p.sts;
+            sfb[u] = ld_nc_u8(scale_role + page + soff);
+            ok[u] = true;
+          }
+        }
+      }
+      if (err != 0 && p.dev_error != nullptr && j == 0)
+        atomicOr(p.dev_error, err);
+    }
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      if (!ok[u]) continue;
+      const float c = __fmul_rn(e4m3_value(sfb[u]), kscale);
+      const uint64_t cc = (static_cast<uint64_t>(__float_as_uint(c)) << 32) |
+                          __float_as_uint(c);
+      uint32_t w[8];
+      uint32_t lo[4], hi[4];
+      dequant4(d0[u], cc, lo);
+      dequant4(d1[u], cc, hi);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        w[k] = lo[k];
+        w[4 + k] = hi[k];
+      }
+      store_group<kVec32>(out_role + (t0 + u * tstep) * p.out_stride0, w);
+    }
+  }
+}
+
+template <int kMode, bool kEarlyMeta, bool kVec32>
+cudaError_t launch_variant(const LoadParams& p, size_t smem,
+                           cudaStream_t stream) {
+  static int ctas_per_sm[64] = {0};  // register-limited, per device
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  int& occ_regs = ctas_per_sm[dev & 63];
+  if (occ_regs == 0) {
+    err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+        &occ_regs, load_nvfp4_kernel<kMode, kEarlyMeta, kVec32>, kThreads,
+        0);
+    if (err != cudaSuccess) return err;
+    if (occ_regs < 1) occ_regs = 1;
+  }
+  // shared-memory limit for this launch's metadata (228 KB per SM, 1 KB
+  // reserved per CTA)
+  int occ = occ_regs;
+  const int by_smem = static_cast<int>((228 * 1024) / (smem + 1024 + 64));
+  if (by_smem < occ) occ = by_smem < 1 ? 1 : by_smem;
+  const int slices = 1 << p.slices_log2;
+  int64_t grid = static_cast<int64_t>(sm_count()) * occ;
+  if (grid > p.num_passes) grid = p.num_passes;
+  grid = (grid / slices) * slices;
+  if (grid < slices) grid = slices;
+  return launch_kernel(load_nvfp4_kernel<kMode, kEarlyMeta, kVec32>,
+                       static_cast<unsigned>(grid), kThreads, smem, stream,
+                       p.pdl, p);
+}
+
+template <bool kEarlyMeta, bool kVec32>
+cudaError_t launch_mode(const LoadParams& p, cudaStream_t stream) {
+  const int64_t ncu = static_cast<int64_t>(p.num_seqs) + 1;
+  const int64_t nbt = static_cast<int64_t>(p.num_seqs) * p.max_blocks;
+  const size_t both = region_bytes(ncu) + region_bytes(nbt);
+  if (p.bt_stride == p.max_blocks && both <= kMaxMetaSmem)
+    return launch_variant<kMetaSharedCuBt, kEarlyMeta, kVec32>(p, both,
+                                                               stream);
+  if (region_bytes(ncu) <= kMaxMetaSmem)
+    return launch_variant<kMetaSharedCu, kEarlyMeta, kVec32>(
+        p, region_bytes(ncu), stream);
+  return launch_variant<kMetaGlobal, kEarlyMeta, kVec32>(p, 0, stream);
+}
+
+}  // namespace
+
+cudaError_t launch_load_nvfp4(const LoadParams& p, cudaStream_t stream) {
+  // 256-bit stores need every group start 32-byte aligned
+  const bool vec32 = (reinterpret_cast<uintptr_t>(p.out[0]) % 32 == 0) &&
+                     (reinterpret_cast<uintptr_t>(p.out[1]) % 32 == 0) &&
+                     (p.out_stride0 % 16 == 0);
+  if (p.early_meta)
+    return vec32 ? launch_mode<true, true>(p, stream)
+                 : launch_mode<true, false>(p, stream);
+  return vec32 ? launch_mode<false, true>(p, stream)
+               : launch_mode<false, false>(p, stream);
+}
+
+}  // namespace kvq

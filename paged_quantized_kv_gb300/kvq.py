@@ -6,7 +6,8 @@ of the computation runs in the CUDA kernels behind ``include/kvq.h``.  If
 ``libkvq.so`` is missing or cannot be loaded the calls raise -- there is no
 fallback path.
 
-The two operations keep the argument order of the pages' ops:
+The operations keep the argument order of the pages' ops where there is
+one:
 
 * ``kvq_store_nvfp4(key, value, key_cache, value_cache, slot_mapping,
   k_scale, v_scale)`` -- vLLM ``reshape_and_cache_nvfp4_dispatch``
@@ -17,6 +18,8 @@ The two operations keep the argument order of the pages' ops:
 * ``kvq_gather_indexer_k(kv_cache, k_fp8, k_scale, block_table,
   cu_seq_lens)`` -- vLLM ``cp_gather_indexer_k_quant_cache`` (PR #25931,
   PR #26456).
+* ``kvq_load_nvfp4(key_cache, value_cache, block_table, cu_seq_lens,
+  k_scale, v_scale, key_out, value_out)`` -- the read side of the store.
 """
 from __future__ import annotations
 
@@ -82,6 +85,11 @@ def lib() -> ctypes.CDLL:
             P, c.c_int64, c.c_int64, c.c_int32, c.c_int32, P, c.c_int64,
             c.c_int32, P, c.c_int32, c.c_int64, P, P, c.c_uint32, P, P]
         L.kvq_gather_indexer_k.restype = c.c_int
+        L.kvq_load_nvfp4.argtypes = [
+            P, P, c.c_int64, c.c_int32, c.c_int64, c.c_int32, c.c_int32,
+            c.c_int32, P, c.c_int64, c.c_int32, P, c.c_int32, c.c_int64, P,
+            P, c.c_int32, P, P, c.c_int64, c.c_uint32, P, P]
+        L.kvq_load_nvfp4.restype = c.c_int
         L.kvq_status_string.argtypes = [c.c_int]
         L.kvq_status_string.restype = c.c_char_p
         L.kvq_version.argtypes = []
@@ -181,6 +189,42 @@ def kvq_gather_indexer_k(kv_cache: torch.Tensor, k_fp8: torch.Tensor,
         k_scale.data_ptr(), int(flags), _ptr(dev_error),
         _stream_of(kv_cache) if stream is None else stream)
     _check("kvq_gather_indexer_k", st)
+
+
+def kvq_load_nvfp4(key_cache: torch.Tensor, value_cache: torch.Tensor,
+                   block_table: torch.Tensor, cu_seq_lens: torch.Tensor,
+                   k_scale: torch.Tensor, v_scale: torch.Tensor,
+                   key_out: torch.Tensor, value_out: torch.Tensor,
+                   flags: int = 0, dev_error: torch.Tensor | None = None,
+                   stream: int | None = None) -> None:
+    """NVFP4 paged load (see ``include/kvq.h``): the tokens the block table
+    names, dequantised into key_out / value_out (bf16 [total, H, D], last two
+    dims contiguous; total = key_out.size(0)).  key_cache / value_cache are
+    the store's 4-D page views."""
+    if key_out.dtype != torch.bfloat16 or value_out.dtype != torch.bfloat16:
+        raise KvqError("kvq_load_nvfp4", KVQ_ERR_DTYPE)
+    T, H, D = key_out.shape
+    if (key_out.stride(2) != 1 or key_out.stride(1) != D
+            or tuple(value_out.shape) != (T, H, D)
+            or value_out.stride(0) != key_out.stride(0)
+            or value_out.stride(2) != 1 or value_out.stride(1) != D):
+        raise KvqError("kvq_load_nvfp4", KVQ_ERR_SHAPE)
+    if key_cache.dim() != 4 or key_cache.dtype != torch.uint8:
+        raise KvqError("kvq_load_nvfp4", KVQ_ERR_SHAPE)
+    if block_table.dtype != torch.int32 or cu_seq_lens.dtype != torch.int32:
+        raise KvqError("kvq_load_nvfp4", KVQ_ERR_DTYPE)
+    layout = (KVQ_LAYOUT_HND if key_cache.stride(2) > key_cache.stride(1)
+              else KVQ_LAYOUT_NHD)
+    st = lib().kvq_load_nvfp4(
+        key_cache.data_ptr(), value_cache.data_ptr(), key_cache.stride(0),
+        key_cache.size(1), key_cache.size(0), layout, H, D,
+        block_table.data_ptr(), block_table.stride(0), block_table.size(1),
+        cu_seq_lens.data_ptr(), cu_seq_lens.numel() - 1, T,
+        k_scale.data_ptr(), v_scale.data_ptr(), KVQ_DTYPE_BF16,
+        key_out.data_ptr(), value_out.data_ptr(), key_out.stride(0),
+        int(flags), _ptr(dev_error),
+        _stream_of(key_out) if stream is None else stream)
+    _check("kvq_load_nvfp4", st)
 
 
 def alloc_nvfp4_cache(num_blocks: int, block_size: int, num_heads: int,

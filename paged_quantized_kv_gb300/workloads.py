@@ -405,3 +405,17 @@ def shard_gather(wl: GatherWorkload, rank: int, world: int):
         cu_seq_lens=(cu - first).astype(np.int32),
         block_stride=wl.block_stride)
     return sub, first
+
+
+def sequences_of_store(wl: StoreWorkload, request_len: int):
+    """Block table and cu_seq_lens that name the requests a "runs" store
+    wrote (request r = tokens [r*request_len, (r+1)*request_len)), for
+    reading them back: returns (block_table int32 [n, blocks per request],
+    cu_seq_lens int32 [n + 1])."""
+    B = wl.block_size
+    n = wl.num_tokens // request_len
+    bpr = (request_len + B - 1) // B
+    first = wl.slot_mapping[: n * request_len].reshape(n, request_len)
+    bt = (first[:, ::B][:, :bpr] // B).astype(np.int32)
+    cu = (np.arange(n + 1, dtype=np.int64) * request_len).astype(np.int32)
+    return bt, cu

@@ -36,8 +36,8 @@ def header_functions():
 
 def test_exports_match_header(lib):
     declared = header_functions()
-    assert {"kvq_store_nvfp4", "kvq_gather_indexer_k", "kvq_status_string",
-            "kvq_version"} <= declared
+    assert {"kvq_store_nvfp4", "kvq_gather_indexer_k", "kvq_load_nvfp4",
+            "kvq_status_string", "kvq_version"} <= declared
     out = subprocess.run(["nm", "-D", "--defined-only", kvq.LIB_PATH],
                          capture_output=True, text=True, check=True).stdout
     exported = set(re.findall(r"\sT\s(kvq_\w+)$", out, flags=re.M))
@@ -144,3 +144,37 @@ def test_product_never_touches_oracle():
                 assert not re.search(
                     r"^\s*(import|from)\s+oracle\b|kvq_oracle|kvqo_", text,
                     flags=re.M), f
+
+
+def load(lib, **kw):
+    args = dict(key_cache=A, value_cache=A, page_stride=2 * 16 * 72,
+                block_size=16, num_blocks=8, layout=0, num_heads=1,
+                head_size=128, block_table=A, block_table_stride=4,
+                max_blocks_per_seq=4, cu_seq_lens=A, num_seqs=2,
+                total_tokens=100, k_scale=A, v_scale=A, out_dtype=0,
+                key_out=A, value_out=A, out_stride0=128, flags=0,
+                dev_error=None, stream=None)
+    args.update(kw)
+    return lib.kvq_load_nvfp4(*args.values())
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(out_dtype=1), kvq.KVQ_ERR_DTYPE),
+    (dict(layout=3), kvq.KVQ_ERR_LAYOUT),
+    (dict(flags=8), kvq.KVQ_ERR_ARG),
+    (dict(head_size=96), kvq.KVQ_ERR_SHAPE),
+    (dict(block_size=6), kvq.KVQ_ERR_SHAPE),
+    (dict(page_stride=64), kvq.KVQ_ERR_SHAPE),
+    (dict(out_stride0=64), kvq.KVQ_ERR_SHAPE),
+    (dict(block_table_stride=2), kvq.KVQ_ERR_SHAPE),
+    (dict(total_tokens=-1), kvq.KVQ_ERR_SHAPE),
+    (dict(num_seqs=0), kvq.KVQ_ERR_ARG),
+    (dict(key_out=None), kvq.KVQ_ERR_NULL),
+    (dict(v_scale=None), kvq.KVQ_ERR_NULL),
+    (dict(value_out=A + 8), kvq.KVQ_ERR_ALIGN),
+    (dict(out_stride0=132), kvq.KVQ_ERR_ALIGN),
+    (dict(key_cache=A + 4), kvq.KVQ_ERR_ALIGN),
+    (dict(total_tokens=0, key_out=None, key_cache=None), kvq.KVQ_OK),
+])
+def test_load_validation(lib, kw, code):
+    assert load(lib, **kw) == code
