@@ -310,6 +310,18 @@ def run_ours(args):
             dev_error=dev_err, stream=sh), K),
     }
     del key16, value16, kv_n, kc_n, vc_n
+    # the read side: the long-context pages read back to bf16 rows
+    from paged_quantized_kv_gb300 import workloads as W
+    lbt, lcu = W.sequences_of_store(st, 512)
+    lbt_d = torch.from_numpy(lbt).to(dev)
+    lcu_d = torch.from_numpy(lcu).to(dev)
+    k_out = torch.empty((T, H, D), dtype=torch.bfloat16, device=dev)
+    v_out = torch.empty((T, H, D), dtype=torch.bfloat16, device=dev)
+    load_ms = span_ms(lambda i: kvq.kvq_load_nvfp4(
+        kc, vc, lbt_d, lcu_d, ks, vs, k_out, v_out,
+        flags=kvq.KVQ_F_PDL_EARLY_META, dev_error=dev_err, stream=sh), K)
+    load_bytes = W.load_algorithmic_bytes(st, lbt, lcu)
+    del k_out, v_out
     # keep the same steps running so the clock sampler sees the load
     t1 = time.perf_counter()
     j = 0
@@ -388,6 +400,14 @@ def run_ours(args):
                 "algorithmic_bytes": ga_bytes},
         },
         "without_pdl": {k: round(v, 5) for k, v in plain.items()},
+        "load_nvfp4": {
+            "note": "read side: the long-context pages read back to bf16 "
+                    "rows through the block table (not part of the step)",
+            "ms": round(load_ms, 5),
+            "GB_s": round(load_bytes / load_ms / 1e6, 1),
+            "frac_of_peak": round(load_bytes / load_ms / 1e6 / peak, 4),
+            "tokens_per_s": round(T / (load_ms / 1e3), 1),
+            "algorithmic_bytes": load_bytes},
         "store_variants": {
             k: {"ms": round(v, 5),
                 "GB_s": round(st_bytes / v / 1e6, 1),

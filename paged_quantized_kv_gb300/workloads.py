@@ -419,3 +419,15 @@ def sequences_of_store(wl: StoreWorkload, request_len: int):
     bt = (first[:, ::B][:, :bpr] // B).astype(np.int32)
     cu = (np.arange(n + 1, dtype=np.int64) * request_len).astype(np.int32)
     return bt, cu
+
+
+def load_algorithmic_bytes(wl: StoreWorkload, block_table: np.ndarray,
+                           cu_seq_lens: np.ndarray) -> int:
+    """NVFP4 data + scale bytes read and bf16 rows written for every token
+    the sequences name, plus the block-table entries and cu_seq_lens read."""
+    H, D, B = wl.num_heads, wl.head_size, wl.block_size
+    lens = np.diff(cu_seq_lens.astype(np.int64))
+    n = int(lens.sum())
+    entries = int(((lens + B - 1) // B).sum())
+    return (n * 2 * H * (D // 2 + D // 16) + n * 2 * H * D * 2
+            + 4 * entries + 4 * cu_seq_lens.size)
