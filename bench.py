@@ -311,8 +311,8 @@ def run_ours(args):
     }
     del key16, value16, kv_n, kc_n, vc_n
     # the read side: the long-context pages read back to bf16 rows
-    from paged_quantized_kv_gb300 import workloads as W
-    lbt, lcu = W.sequences_of_store(st, 512)
+    from paged_quantized_kv_gb300 import workloads as wlmod
+    lbt, lcu = wlmod.sequences_of_store(st, 512)
     lbt_d = torch.from_numpy(lbt).to(dev)
     lcu_d = torch.from_numpy(lcu).to(dev)
     k_out = torch.empty((T, H, D), dtype=torch.bfloat16, device=dev)
@@ -320,7 +320,7 @@ def run_ours(args):
     load_ms = span_ms(lambda i: kvq.kvq_load_nvfp4(
         kc, vc, lbt_d, lcu_d, ks, vs, k_out, v_out,
         flags=kvq.KVQ_F_PDL_EARLY_META, dev_error=dev_err, stream=sh), K)
-    load_bytes = W.load_algorithmic_bytes(st, lbt, lcu)
+    load_bytes = wlmod.load_algorithmic_bytes(st, lbt, lcu)
     del k_out, v_out
     # keep the same steps running so the clock sampler sees the load
     t1 = time.perf_counter()
