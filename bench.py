@@ -54,7 +54,7 @@ def parse_args():
     ap.add_argument("--cpu-sample-tokens", type=int, default=65536)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--clock-window-s", type=float, default=1.5)
-    ap.add_argument("--kernel-only", choices=["store", "gather"],
+    ap.add_argument("--kernel-only", choices=["store", "gather", "load"],
                     help="launch only this kernel (each launch after an L2 "
                          "flush) and print its mean time; used for ncu")
     return ap.parse_args()
@@ -639,7 +639,7 @@ def run_kernel_only(args):
     dev = torch.device("cuda", 0)
     st, ga = make_workload(0)
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
-    if args.kernel_only == "store":
+    if args.kernel_only in ("store", "load"):
         T, H, D = st.num_tokens, st.num_heads, st.head_size
         src = torch.from_numpy(st.src.view(np.int16)).to(dev).view(
             torch.bfloat16)
@@ -656,6 +656,20 @@ def run_kernel_only(args):
         def launch():
             kvq.kvq_store_nvfp4(key, value, kc, vc, slots, ks, vs)
         byts = st.algorithmic_bytes()
+        if args.kernel_only == "load":
+            from paged_quantized_kv_gb300 import workloads as wlmod
+            launch()  # pages to read back
+            lbt, lcu = wlmod.sequences_of_store(st, 512)
+            lbt_d = torch.from_numpy(lbt).to(dev)
+            lcu_d = torch.from_numpy(lcu).to(dev)
+            k_out = torch.empty((T, H, D), dtype=torch.bfloat16, device=dev)
+            v_out = torch.empty((T, H, D), dtype=torch.bfloat16, device=dev)
+            del key, value, src
+
+            def launch():
+                kvq.kvq_load_nvfp4(kc, vc, lbt_d, lcu_d, ks, vs, k_out,
+                                   v_out)
+            byts = wlmod.load_algorithmic_bytes(st, lbt, lcu)
     else:
         gcache = torch.from_numpy(ga.cache).to(dev).view(ga.num_blocks, -1)
         bt = torch.from_numpy(ga.block_table).to(dev)
