@@ -14,13 +14,13 @@
 //
 // GB300 design: HBM-bound, 0.5625 B read and 2 B written per element.
 //   * Persistent grid; every thread owns one fixed 16-element group role
-//     (side, head, group) and walks output rows with a grid stride, kUnroll
-//     rows in flight (8 data bytes + 1 scale byte each) before any of them
-//     is used.
+//     (side, head, group); each CTA owns a contiguous range of output rows
+//     and its threads walk it kUnroll rows at a time (8 data bytes + 1 scale
+//     byte each in flight before any of them is used).
 //   * cu_seq_lens and the block table are staged in shared memory once per
-//     CTA (TMA bulk copies, shared with the indexer gather); each row is
-//     resolved with a binary search in shared memory, in lockstep across the
-//     lanes that share the row.
+//     CTA (TMA bulk copies, shared with the indexer gather); a thread finds
+//     its first row's sequence with one binary search and then only steps
+//     it forward, so row resolution costs a few instructions per row.
 //   * e2m1 -> f16x2 with cvt.rn.f16x2.e2m1x2 (exact), widened to fp32,
 //     times the group's fp32 scale with mul.rn.f32x2, packed to bf16x2 with
 //     cvt.rn.bf16x2.f32; each thread writes its group's 32 bytes with one
@@ -40,7 +40,10 @@ namespace {
 using namespace kvq::dev;
 
 constexpr int kThreads = 256;
-constexpr int kUnroll = 4;
+#ifndef KVQ_LOAD_UNROLL
+#define KVQ_LOAD_UNROLL 4
+#endif
+constexpr int kUnroll = KVQ_LOAD_UNROLL;
 
 __device__ __forceinline__ void ld_nc_8(const void* p, uint32_t& a,
                                         uint32_t& b) {
@@ -173,12 +176,28 @@ load_nvfp4_kernel(const LoadParams p) {
   uint16_t* const out_role = p.out[side] + head * p.D + j * 16;
   const float kscale = __ldg(p.scale[side]);
 
+  // ---- a contiguous range of rows per CTA ---------------------------------
+  // Rows are handed out in contiguous chunks, so a thread finds its first
+  // row's sequence with one binary search and afterwards only steps the
+  // sequence forward (usually not at all) as its rows advance by tpp.
   const int64_t T = p.total;
-  const int64_t tstep =
-      static_cast<int64_t>(gridDim.x >> p.slices_log2) * p.tpp;
-  for (int64_t t0 = static_cast<int64_t>(blockIdx.x >> p.slices_log2) *
-                        p.tpp + tok_sub;
-       t0 < T; t0 += kUnroll * tstep) {
+  const int64_t tgroups = (T + p.tpp - 1) / p.tpp;
+  const int64_t nchunks = gridDim.x >> p.slices_log2;
+  const int64_t per = (tgroups + nchunks - 1) / nchunks;
+  const int64_t g_lo = static_cast<int64_t>(blockIdx.x >> p.slices_log2) * per;
+  int64_t g_hi = g_lo + per;
+  if (g_hi > tgroups) g_hi = tgroups;
+  if (g_lo >= g_hi) return;
+  int64_t row_hi = g_hi * p.tpp;
+  if (row_hi > T) row_hi = T;
+  const int64_t row_lo = g_lo * p.tpp + tok_sub;
+  const int n = p.num_seqs;
+  int b = row_lo < row_hi ? find_seq<kMode != kMetaGlobal>(cu, n, row_lo) : n;
+  int64_t seq_lo = b < n ? cu[b] : 0;
+  int64_t seq_hi = b < n ? cu[b + 1] : 0;
+  const int64_t tstep = p.tpp;
+
+  for (int64_t t0 = row_lo; t0 < row_hi; t0 += kUnroll * tstep) {
     uint32_t d0[kUnroll], d1[kUnroll], sfb[kUnroll];
     bool ok[kUnroll];
 #pragma unroll
@@ -186,13 +205,17 @@ load_nvfp4_kernel(const LoadParams p) {
       const int64_t row = t0 + u * tstep;
       ok[u] = false;
       d0[u] = d1[u] = sfb[u] = 0u;
-      if (row >= T) continue;
-      const int b = find_seq<kMode != kMetaGlobal>(cu, p.num_seqs, row);
+      if (row >= row_hi) continue;
+      while (b < n && row >= seq_hi) {  // next non-empty sequence
+        ++b;
+        seq_lo = seq_hi;
+        if (b < n) seq_hi = cu[b + 1];
+      }
       int err = 0;
-      if (b >= p.num_seqs) {
-        err = KVQ_DEVERR_SEQ;
+      if (b >= n) {
+        err = KVQ_DEVERR_SEQ;  // no sequence covers this row
       } else {
-        const int64_t pos = row - cu[b];
+        const int64_t pos = row - seq_lo;
         int64_t kb, off;
         if (p.b_shift >= 0) {
           kb = pos >> p.b_shift;
