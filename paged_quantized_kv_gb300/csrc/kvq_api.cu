@@ -271,14 +271,15 @@ kvq_status kvq_load_nvfp4(const uint8_t* key_cache, const uint8_t* value_cache,
   p.S = static_cast<int32_t>(S);
   p.B = block_size;
   p.b_shift = ilog2_exact(B);
-  p.gpt = static_cast<int32_t>(gpt);
-  if (gpt <= 256) {
-    p.tpp = static_cast<int32_t>(256 / gpt);
+  const int64_t upt = gpt / 2;  // two groups per thread role
+  p.upt = static_cast<int32_t>(upt);
+  if (upt <= 256) {
+    p.tpp = static_cast<int32_t>(256 / upt);
     p.slices_log2 = 0;
   } else {
     p.tpp = 1;
     int sl = 0;
-    while ((int64_t{256} << sl) < gpt) ++sl;
+    while ((int64_t{256} << sl) < upt) ++sl;
     p.slices_log2 = sl;
   }
   const int64_t passes =

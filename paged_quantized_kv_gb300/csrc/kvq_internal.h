@@ -79,7 +79,8 @@ struct LoadParams {
   int64_t total;
   int32_t H, D, S, B;
   int32_t b_shift;
-  int32_t gpt, tpp, slices_log2, num_passes;
+  int32_t upt;             // thread roles per row (two groups each): H * S
+  int32_t tpp, slices_log2, num_passes;
   int32_t num_seqs, max_blocks;
   uint32_t swizzle_sides;
   bool pdl, early_meta;

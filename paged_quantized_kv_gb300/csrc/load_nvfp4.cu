@@ -13,10 +13,12 @@
 // from page block_table[b, p / B], offset p % B.
 //
 // GB300 design: HBM-bound, 0.5625 B read and 2 B written per element.
-//   * Persistent grid; every thread owns one fixed 16-element group role
-//     (side, head, group); each CTA owns a contiguous range of output rows
-//     and its threads walk it kUnroll rows at a time (8 data bytes + 1 scale
-//     byte each in flight before any of them is used).
+//   * Persistent grid; every thread owns one fixed role -- two adjacent
+//     16-element groups of one head and side -- so the per-row work (sequence
+//     step, bounds checks, page addressing) is shared by 32 elements; each
+//     CTA owns a contiguous range of output rows and its threads walk it
+//     kUnroll rows at a time (16 data bytes + 2 scale bytes each in flight
+//     before any of them is used).
 //   * cu_seq_lens and the block table are staged in shared memory once per
 //     CTA (TMA bulk copies, shared with the indexer gather); a thread finds
 //     its first row's sequence with one binary search and then only steps
@@ -45,11 +47,13 @@ constexpr int kThreads = 256;
 #endif
 constexpr int kUnroll = KVQ_LOAD_UNROLL;
 
-__device__ __forceinline__ void ld_nc_8(const void* p, uint32_t& a,
-                                        uint32_t& b) {
-  asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0, %1}, [%2];"
-               : "=r"(a), "=r"(b)
-               : "l"(p));
+__device__ __forceinline__ uint4 ld_nc_16(const void* p) {
+  uint4 v;
+  asm volatile(
+      "ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+      : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+      : "l"(p));
+  return v;
 }
 
 __device__ __forceinline__ uint32_t ld_nc_u8(const void* p) {
@@ -150,30 +154,38 @@ load_nvfp4_kernel(const LoadParams p) {
     atomicOr(p.dev_error, KVQ_DEVERR_SEQ);
 
   // ---- this thread's fixed role inside a row ------------------------------
+  // A thread owns two adjacent 16-element groups (j0, j0 + 1) of one head:
+  // 16 data bytes, two scale bytes, 64 output bytes per row.
   const int tid = threadIdx.x;
   const int slices = 1 << p.slices_log2;
-  int grp_in_tok, tok_sub;
+  int unit_in_tok, tok_sub;
   if (slices == 1) {
-    tok_sub = tid / p.gpt;
-    grp_in_tok = tid - tok_sub * p.gpt;
+    tok_sub = tid / p.upt;
+    unit_in_tok = tid - tok_sub * p.upt;
   } else {
     tok_sub = 0;
-    grp_in_tok = (static_cast<int>(blockIdx.x) & (slices - 1)) * kThreads + tid;
+    unit_in_tok = (static_cast<int>(blockIdx.x) & (slices - 1)) * kThreads + tid;
   }
-  if (tok_sub >= p.tpp || grp_in_tok >= p.gpt) return;  // idle role
-  const int gps = p.gpt >> 1;  // groups per side
-  const int side = grp_in_tok >= gps ? 1 : 0;
-  const int e = grp_in_tok - side * gps;
-  const int head = e / p.S;
-  const int j = e - head * p.S;
+  if (tok_sub >= p.tpp || unit_in_tok >= p.upt) return;  // idle role
+  const int ups = p.upt >> 1;  // units per side
+  const int side = unit_in_tok >= ups ? 1 : 0;
+  const int e = unit_in_tok - side * ups;
+  const int uph = p.S >> 1;  // units per head
+  const int head = e / uph;
+  const int j0 = 2 * (e - head * uph);
   const int q = p.S >> 2;
   const bool swz = (p.swizzle_sides >> side) & 1u;
 
-  const uint8_t* const data_role = p.side[side] + head * p.dhs + j * 8;
-  const uint8_t* const scale_role =
-      p.side[side] + p.data_per_side + head * p.shs +
-      (swz ? (j / q) * p.sts + (j % q) * 4 : static_cast<int64_t>(j));
-  uint16_t* const out_role = p.out[side] + head * p.D + j * 16;
+  const uint8_t* const data_role = p.side[side] + head * p.dhs + j0 * 8;
+  const uint8_t* const scale_base = p.side[side] + p.data_per_side +
+                                    head * p.shs;
+  const uint8_t* const scale_role0 =
+      scale_base + (swz ? (j0 / q) * p.sts + (j0 % q) * 4
+                        : static_cast<int64_t>(j0));
+  const uint8_t* const scale_role1 =
+      scale_base + (swz ? ((j0 + 1) / q) * p.sts + ((j0 + 1) % q) * 4
+                        : static_cast<int64_t>(j0 + 1));
+  uint16_t* const out_role = p.out[side] + head * p.D + j0 * 16;
   const float kscale = __ldg(p.scale[side]);
 
   // ---- a contiguous range of rows per CTA ---------------------------------
@@ -198,13 +210,15 @@ load_nvfp4_kernel(const LoadParams p) {
   const int64_t tstep = p.tpp;
 
   for (int64_t t0 = row_lo; t0 < row_hi; t0 += kUnroll * tstep) {
-    uint32_t d0[kUnroll], d1[kUnroll], sfb[kUnroll];
+    uint4 d[kUnroll];
+    uint32_t sf0[kUnroll], sf1[kUnroll];
     bool ok[kUnroll];
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
       const int64_t row = t0 + u * tstep;
       ok[u] = false;
-      d0[u] = d1[u] = sfb[u] = 0u;
+      d[u] = make_uint4(0u, 0u, 0u, 0u);
+      sf0[u] = sf1[u] = 0u;
       if (row >= row_hi) continue;
       while (b < n && row >= seq_hi) {  // next non-empty sequence
         ++b;
@@ -235,33 +249,49 @@ load_nvfp4_kernel(const LoadParams p) {
             err = KVQ_DEVERR_BLOCK;
           } else {
             const int64_t page = blk * p.page_stride;
-            ld_nc_8(data_role + page + off * p.dts, d0[u], d1[u]);
+            d[u] = ld_nc_16(data_role + page + off * p.dts);
             const int64_t soff =
-                swz ? (off & ~int64_t{3}) * p.sts + (off & 3) : off * p.sts;
-            sfb[u] = ld_nc_u8(scale_role + page + soff);
+                page + (swz ? (off & ~int64_t{3}) * p.sts + (off & 3)
+                            : off * p.sts);
+            sf0[u] = ld_nc_u8(scale_role0 + soff);
+            sf1[u] = ld_nc_u8(scale_role1 + soff);
             ok[u] = true;
           }
         }
       }
-      if (err != 0 && p.dev_error != nullptr && j == 0)
+      if (err != 0 && p.dev_error != nullptr && j0 == 0)
         atomicOr(p.dev_error, err);
     }
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
       if (!ok[u]) continue;
-      const float c = __fmul_rn(e4m3_value(sfb[u]), kscale);
-      const uint64_t cc = (static_cast<uint64_t>(__float_as_uint(c)) << 32) |
-                          __float_as_uint(c);
+      uint16_t* const dst = out_role + (t0 + u * tstep) * p.out_stride0;
+      const float c0 = __fmul_rn(e4m3_value(sf0[u]), kscale);
+      const float c1 = __fmul_rn(e4m3_value(sf1[u]), kscale);
+      const uint64_t cc0 =
+          (static_cast<uint64_t>(__float_as_uint(c0)) << 32) |
+          __float_as_uint(c0);
+      const uint64_t cc1 =
+          (static_cast<uint64_t>(__float_as_uint(c1)) << 32) |
+          __float_as_uint(c1);
       uint32_t w[8];
-      uint32_t lo[4], hi[4];
-      dequant4(d0[u], cc, lo);
-      dequant4(d1[u], cc, hi);
+      uint32_t a[4], b2[4];
+      dequant4(d[u].x, cc0, a);
+      dequant4(d[u].y, cc0, b2);
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
-        w[k] = lo[k];
-        w[4 + k] = hi[k];
+        w[k] = a[k];
+        w[4 + k] = b2[k];
       }
-      store_group<kVec32>(out_role + (t0 + u * tstep) * p.out_stride0, w);
+      store_group<kVec32>(dst, w);
+      dequant4(d[u].z, cc1, a);
+      dequant4(d[u].w, cc1, b2);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        w[k] = a[k];
+        w[4 + k] = b2[k];
+      }
+      store_group<kVec32>(dst + 16, w);
     }
   }
 }
