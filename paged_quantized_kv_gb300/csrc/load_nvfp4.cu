@@ -13,12 +13,13 @@
 // from page block_table[b, p / B], offset p % B.
 //
 // GB300 design: HBM-bound, 0.5625 B read and 2 B written per element.
-//   * Persistent grid; every thread owns one fixed role -- two adjacent
-//     16-element groups of one head and side -- so the per-row work (sequence
-//     step, bounds checks, page addressing) is shared by 32 elements; each
-//     CTA owns a contiguous range of output rows and its threads walk it
-//     kUnroll rows at a time (16 data bytes + 2 scale bytes each in flight
-//     before any of them is used).
+//   * Persistent grid; every thread owns one fixed role -- two 16-element
+//     groups of one side, 32 groups apart, so the per-row work (sequence
+//     step, bounds checks, page addressing) is shared by 32 elements and
+//     each warp store instruction writes 1 KB contiguous; each CTA owns a
+//     contiguous range of output rows and its threads walk it kUnroll rows at
+//     a time (16 data bytes + 2 scale bytes each in flight before any of
+//     them is used).
 //   * cu_seq_lens and the block table are staged in shared memory once per
 //     CTA (TMA bulk copies, shared with the indexer gather); a thread finds
 //     its first row's sequence with one binary search and then only steps
@@ -47,13 +48,11 @@ constexpr int kThreads = 256;
 #endif
 constexpr int kUnroll = KVQ_LOAD_UNROLL;
 
-__device__ __forceinline__ uint4 ld_nc_16(const void* p) {
-  uint4 v;
-  asm volatile(
-      "ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
-      : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-      : "l"(p));
-  return v;
+__device__ __forceinline__ void ld_nc_8(const void* p, uint32_t& a,
+                                        uint32_t& b) {
+  asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0, %1}, [%2];"
+               : "=r"(a), "=r"(b)
+               : "l"(p));
 }
 
 __device__ __forceinline__ uint32_t ld_nc_u8(const void* p) {
@@ -154,8 +153,10 @@ load_nvfp4_kernel(const LoadParams p) {
     atomicOr(p.dev_error, KVQ_DEVERR_SEQ);
 
   // ---- this thread's fixed role inside a row ------------------------------
-  // A thread owns two adjacent 16-element groups (j0, j0 + 1) of one head:
-  // 16 data bytes, two scale bytes, 64 output bytes per row.
+  // A thread owns two 16-element groups of one side, gA and gB = gA + P
+  // (P = 32 when the side has a multiple of 64 groups, else half the side),
+  // so each of a warp's two 256-bit store instructions writes one contiguous
+  // run of 32 groups' output (1 KB).
   const int tid = threadIdx.x;
   const int slices = 1 << p.slices_log2;
   int unit_in_tok, tok_sub;
@@ -169,23 +170,28 @@ load_nvfp4_kernel(const LoadParams p) {
   if (tok_sub >= p.tpp || unit_in_tok >= p.upt) return;  // idle role
   const int ups = p.upt >> 1;  // units per side
   const int side = unit_in_tok >= ups ? 1 : 0;
-  const int e = unit_in_tok - side * ups;
-  const int uph = p.S >> 1;  // units per head
-  const int head = e / uph;
-  const int j0 = 2 * (e - head * uph);
+  const int i = unit_in_tok - side * ups;
+  const int gps = 2 * ups;  // groups per side
+  const int P = (gps % 64 == 0) ? 32 : ups;
+  const int gA = (i / P) * 2 * P + (i % P);
+  const int gB = gA + P;
+  const int headA = gA / p.S, jA = gA - headA * p.S;
+  const int headB = gB / p.S, jB = gB - headB * p.S;
   const int q = p.S >> 2;
   const bool swz = (p.swizzle_sides >> side) & 1u;
 
-  const uint8_t* const data_role = p.side[side] + head * p.dhs + j0 * 8;
-  const uint8_t* const scale_base = p.side[side] + p.data_per_side +
-                                    head * p.shs;
-  const uint8_t* const scale_role0 =
-      scale_base + (swz ? (j0 / q) * p.sts + (j0 % q) * 4
-                        : static_cast<int64_t>(j0));
-  const uint8_t* const scale_role1 =
-      scale_base + (swz ? ((j0 + 1) / q) * p.sts + ((j0 + 1) % q) * 4
-                        : static_cast<int64_t>(j0 + 1));
-  uint16_t* const out_role = p.out[side] + head * p.D + j0 * 16;
+  const uint8_t* const side_base = p.side[side];
+  const uint8_t* const data_roleA = side_base + headA * p.dhs + jA * 8;
+  const uint8_t* const data_roleB = side_base + headB * p.dhs + jB * 8;
+  const uint8_t* const scale_side = side_base + p.data_per_side;
+  const uint8_t* const scale_roleA =
+      scale_side + headA * p.shs +
+      (swz ? (jA / q) * p.sts + (jA % q) * 4 : static_cast<int64_t>(jA));
+  const uint8_t* const scale_roleB =
+      scale_side + headB * p.shs +
+      (swz ? (jB / q) * p.sts + (jB % q) * 4 : static_cast<int64_t>(jB));
+  uint16_t* const out_roleA = p.out[side] + headA * p.D + jA * 16;
+  uint16_t* const out_roleB = p.out[side] + headB * p.D + jB * 16;
   const float kscale = __ldg(p.scale[side]);
 
   // ---- a contiguous range of rows per CTA ---------------------------------
@@ -249,23 +255,25 @@ load_nvfp4_kernel(const LoadParams p) {
             err = KVQ_DEVERR_BLOCK;
           } else {
             const int64_t page = blk * p.page_stride;
-            d[u] = ld_nc_16(data_role + page + off * p.dts);
+            const int64_t doff = page + off * p.dts;
+            ld_nc_8(data_roleA + doff, d[u].x, d[u].y);
+            ld_nc_8(data_roleB + doff, d[u].z, d[u].w);
             const int64_t soff =
                 page + (swz ? (off & ~int64_t{3}) * p.sts + (off & 3)
                             : off * p.sts);
-            sf0[u] = ld_nc_u8(scale_role0 + soff);
-            sf1[u] = ld_nc_u8(scale_role1 + soff);
+            sf0[u] = ld_nc_u8(scale_roleA + soff);
+            sf1[u] = ld_nc_u8(scale_roleB + soff);
             ok[u] = true;
           }
         }
       }
-      if (err != 0 && p.dev_error != nullptr && j0 == 0)
+      if (err != 0 && p.dev_error != nullptr && i == 0)
         atomicOr(p.dev_error, err);
     }
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
       if (!ok[u]) continue;
-      uint16_t* const dst = out_role + (t0 + u * tstep) * p.out_stride0;
+      const int64_t orow = (t0 + u * tstep) * p.out_stride0;
       const float c0 = __fmul_rn(e4m3_value(sf0[u]), kscale);
       const float c1 = __fmul_rn(e4m3_value(sf1[u]), kscale);
       const uint64_t cc0 =
@@ -283,7 +291,7 @@ load_nvfp4_kernel(const LoadParams p) {
         w[k] = a[k];
         w[4 + k] = b2[k];
       }
-      store_group<kVec32>(dst, w);
+      store_group<kVec32>(out_roleA + orow, w);
       dequant4(d[u].z, cc1, a);
       dequant4(d[u].w, cc1, b2);
 #pragma unroll
@@ -291,7 +299,7 @@ load_nvfp4_kernel(const LoadParams p) {
         w[k] = a[k];
         w[4 + k] = b2[k];
       }
-      store_group<kVec32>(dst + 16, w);
+      store_group<kVec32>(out_roleB + orow, w);
     }
   }
 }
