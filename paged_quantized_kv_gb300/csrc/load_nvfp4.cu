@@ -16,14 +16,15 @@
 //   * Persistent grid; every thread owns one fixed role -- two 16-element
 //     groups of one side, 32 groups apart, so the per-row work (sequence
 //     step, bounds checks, page addressing) is shared by 32 elements and
-//     each warp store instruction writes 1 KB contiguous; each CTA owns a
-//     contiguous range of output rows and its threads walk it kUnroll rows at
-//     a time (16 data bytes + 2 scale bytes each in flight before any of
-//     them is used).
+//     each warp store instruction writes 1 KB contiguous; output rows come in
+//     chunks of kChunk row groups dealt round-robin to the CTAs, walked
+//     kUnroll rows at a time (16 data bytes + 2 scale bytes each in flight
+//     before any of them is used).
 //   * cu_seq_lens and the block table are staged in shared memory once per
 //     CTA (TMA bulk copies, shared with the indexer gather); a thread finds
 //     its first row's sequence with one binary search and then only steps
-//     it forward, so row resolution costs a few instructions per row.
+//     it forward (its rows only increase), so row resolution costs a few
+//     instructions per row.
 //   * e2m1 -> f16x2 with cvt.rn.f16x2.e2m1x2 (exact), widened to fp32,
 //     times the group's fp32 scale with mul.rn.f32x2, packed to bf16x2 with
 //     cvt.rn.bf16x2.f32; each thread writes its group's 32 bytes with one
@@ -46,7 +47,11 @@ constexpr int kThreads = 256;
 #ifndef KVQ_LOAD_UNROLL
 #define KVQ_LOAD_UNROLL 4
 #endif
+#ifndef KVQ_LOAD_MIN_BLOCKS
+#define KVQ_LOAD_MIN_BLOCKS 3
+#endif
 constexpr int kUnroll = KVQ_LOAD_UNROLL;
+constexpr int kChunk = 16;  // row groups (tpp rows each) per chunk
 
 __device__ __forceinline__ void ld_nc_8(const void* p, uint32_t& a,
                                         uint32_t& b) {
@@ -125,7 +130,7 @@ __device__ __forceinline__ void store_group(uint16_t* p,
 }
 
 template <int kMode, bool kEarlyMeta, bool kVec32>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, KVQ_LOAD_MIN_BLOCKS)
 load_nvfp4_kernel(const LoadParams p) {
   extern __shared__ __align__(16) uint8_t s_raw[];
   __shared__ __align__(8) uint64_t s_bar;
@@ -194,28 +199,31 @@ load_nvfp4_kernel(const LoadParams p) {
   uint16_t* const out_roleB = p.out[side] + headB * p.D + jB * 16;
   const float kscale = __ldg(p.scale[side]);
 
-  // ---- a contiguous range of rows per CTA ---------------------------------
-  // Rows are handed out in contiguous chunks, so a thread finds its first
-  // row's sequence with one binary search and afterwards only steps the
-  // sequence forward (usually not at all) as its rows advance by tpp.
+  // ---- rows: small contiguous chunks dealt round-robin to CTAs -----------
+  // Within a chunk a thread's rows advance by tpp; across chunks they jump
+  // forward by the grid's span.  The thread finds its first row's sequence
+  // with one binary search and afterwards only steps the sequence forward,
+  // while the round-robin deal keeps every SM's share spread over the
+  // whole output (balanced across SMs and memory partitions).
   const int64_t T = p.total;
   const int64_t tgroups = (T + p.tpp - 1) / p.tpp;
-  const int64_t nchunks = gridDim.x >> p.slices_log2;
-  const int64_t per = (tgroups + nchunks - 1) / nchunks;
-  const int64_t g_lo = static_cast<int64_t>(blockIdx.x >> p.slices_log2) * per;
-  int64_t g_hi = g_lo + per;
-  if (g_hi > tgroups) g_hi = tgroups;
-  if (g_lo >= g_hi) return;
-  int64_t row_hi = g_hi * p.tpp;
-  if (row_hi > T) row_hi = T;
-  const int64_t row_lo = g_lo * p.tpp + tok_sub;
+  const int64_t nchunks = (tgroups + kChunk - 1) / kChunk;
+  const int64_t cstride = gridDim.x >> p.slices_log2;
+  const int64_t c_first = blockIdx.x >> p.slices_log2;
   const int n = p.num_seqs;
-  int b = row_lo < row_hi ? find_seq<kMode != kMetaGlobal>(cu, n, row_lo) : n;
+  int b = c_first < nchunks
+              ? find_seq<kMode != kMetaGlobal>(
+                    cu, n, c_first * kChunk * p.tpp + tok_sub)
+              : n;
   int64_t seq_lo = b < n ? cu[b] : 0;
   int64_t seq_hi = b < n ? cu[b + 1] : 0;
   const int64_t tstep = p.tpp;
 
-  for (int64_t t0 = row_lo; t0 < row_hi; t0 += kUnroll * tstep) {
+  for (int64_t c = c_first; c < nchunks; c += cstride) {
+   int64_t row_hi = (c + 1) * kChunk * p.tpp;
+   if (row_hi > T) row_hi = T;
+   for (int64_t t0 = c * kChunk * p.tpp + tok_sub; t0 < row_hi;
+        t0 += kUnroll * tstep) {
     uint4 d[kUnroll];
     uint32_t sf0[kUnroll], sf1[kUnroll];
     bool ok[kUnroll];
@@ -301,6 +309,7 @@ load_nvfp4_kernel(const LoadParams p) {
       }
       store_group<kVec32>(out_roleB + orow, w);
     }
+   }
   }
 }
 
