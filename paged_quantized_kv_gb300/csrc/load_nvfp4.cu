@@ -48,7 +48,7 @@ constexpr int kThreads = 256;
 #define KVQ_LOAD_UNROLL 4
 #endif
 #ifndef KVQ_LOAD_MIN_BLOCKS
-#define KVQ_LOAD_MIN_BLOCKS 3
+#define KVQ_LOAD_MIN_BLOCKS 1
 #endif
 constexpr int kUnroll = KVQ_LOAD_UNROLL;
 constexpr int kChunk = 16;  // row groups (tpp rows each) per chunk
