@@ -50,7 +50,7 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--e2e-steps", type=int, default=8)
     ap.add_argument("--cpu-sample-tokens", type=int, default=65536)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--clock-window-s", type=float, default=1.5)
@@ -470,9 +470,13 @@ def single_launch_cold(store, gather, dev, reps=20):
 
 
 def run_e2e(args, st, ga, dev, kvq):
-    """Same step through the public binding with pinned HOST buffers: H2D of
-    the step's inputs, both calls, D2H of the gathered rows and of the
-    written cache pages, all inside the timed region."""
+    """Same step through the public binding with pinned HOST buffers: every
+    step copies its inputs host->device, runs both calls, and reads the
+    gathered rows and the written cache pages back to the host.  Steps are
+    pipelined on three streams -- copy-in (double-buffered inputs),
+    compute, copy-out -- with events, so step i's copy-out overlaps step
+    i+1's copy-in; a store waits for the previous step's page copy-out, a
+    gather for its row copy-out."""
     import torch
     T, H, D = st.num_tokens, st.num_heads, st.head_size
     h_src = torch.from_numpy(st.src.view(np.int16)).pin_memory()
@@ -487,44 +491,68 @@ def run_e2e(args, st, ga, dev, kvq):
     kv, kc, vc = kvq.alloc_nvfp4_cache(st.num_blocks, st.block_size, H, D,
                                        device=dev, fill=0xAA)
     h_cache = torch.empty(kv.shape, dtype=torch.uint8).pin_memory()
-    d_src = torch.empty(h_src.shape, dtype=torch.int16, device=dev)
-    d_slots = torch.empty_like(h_slots, device=dev)
-    d_scales = torch.empty(2, dtype=torch.float32, device=dev)
-    d_bt = torch.empty_like(h_bt, device=dev)
-    d_cu = torch.empty_like(h_cu, device=dev)
+    ins = [dict(src=torch.empty(h_src.shape, dtype=torch.int16, device=dev),
+                slots=torch.empty_like(h_slots, device=dev),
+                scales=torch.empty(2, dtype=torch.float32, device=dev),
+                bt=torch.empty_like(h_bt, device=dev),
+                cu=torch.empty_like(h_cu, device=dev)) for _ in range(2)]
     gcache = torch.from_numpy(ga.cache).to(dev).view(ga.num_blocks, -1)
     k_fp8 = torch.empty((n, ga.head_dim), dtype=torch.uint8, device=dev)
     k_scale = torch.empty((n, 4), dtype=torch.uint8, device=dev)
-    stream = torch.cuda.current_stream(dev)
+    s_in, s_cp, s_out = (torch.cuda.Stream(dev) for _ in range(3))
+    ev = lambda: torch.cuda.Event(enable_timing=False)
+    state = {"out_done": None, "comp_done": [None, None]}
 
-    def step():
-        d_src.copy_(h_src, non_blocking=True)
-        d_slots.copy_(h_slots, non_blocking=True)
-        d_scales.copy_(h_scales, non_blocking=True)
-        d_bt.copy_(h_bt, non_blocking=True)
-        d_cu.copy_(h_cu, non_blocking=True)
-        src = d_src.view(torch.bfloat16)
-        key = src.as_strided((T, H, D), (st.key_stride0, D, 1), st.key_offset)
-        value = src.as_strided((T, H, D), (st.value_stride0, D, 1),
-                               st.value_offset)
-        kvq.kvq_store_nvfp4(key, value, kc, vc, d_slots, d_scales[0:1],
-                            d_scales[1:2])
-        kvq.kvq_gather_indexer_k(gcache, k_fp8, k_scale, d_bt, d_cu,
-                                 block_size=ga.block_size)
-        h_k.copy_(k_fp8, non_blocking=True)
-        h_s.copy_(k_scale, non_blocking=True)
-        h_cache.copy_(kv, non_blocking=True)
+    def step(i):
+        b = ins[i % 2]
+        with torch.cuda.stream(s_in):
+            if state["comp_done"][i % 2] is not None:  # buffer reuse
+                s_in.wait_event(state["comp_done"][i % 2])
+            b["src"].copy_(h_src, non_blocking=True)
+            b["slots"].copy_(h_slots, non_blocking=True)
+            b["scales"].copy_(h_scales, non_blocking=True)
+            b["bt"].copy_(h_bt, non_blocking=True)
+            b["cu"].copy_(h_cu, non_blocking=True)
+            in_done = ev()
+            in_done.record(s_in)
+        with torch.cuda.stream(s_cp):
+            s_cp.wait_event(in_done)
+            if state["out_done"] is not None:  # pages / rows read back
+                s_cp.wait_event(state["out_done"])
+            src = b["src"].view(torch.bfloat16)
+            key = src.as_strided((T, H, D), (st.key_stride0, D, 1),
+                                 st.key_offset)
+            value = src.as_strided((T, H, D), (st.value_stride0, D, 1),
+                                   st.value_offset)
+            kvq.kvq_store_nvfp4(key, value, kc, vc, b["slots"],
+                                b["scales"][0:1], b["scales"][1:2],
+                                stream=s_cp.cuda_stream)
+            kvq.kvq_gather_indexer_k(gcache, k_fp8, k_scale, b["bt"],
+                                     b["cu"], block_size=ga.block_size,
+                                     stream=s_cp.cuda_stream)
+            comp = ev()
+            comp.record(s_cp)
+            state["comp_done"][i % 2] = comp
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(comp)
+            h_k.copy_(k_fp8, non_blocking=True)
+            h_s.copy_(k_scale, non_blocking=True)
+            h_cache.copy_(kv, non_blocking=True)
+            out = ev()
+            out.record(s_out)
+            state["out_done"] = out
 
-    for _ in range(2):
-        step()
+    for i in range(2):
+        step(i)
     torch.cuda.synchronize(dev)
+    E = max(args.e2e_steps, 1)
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
-    E = max(args.e2e_steps, 1)
-    e0.record(stream)
-    for _ in range(E):
-        step()
-    e1.record(stream)
+    e0.record(s_in)
+    for i in range(E):
+        step(i)
+    s_in.wait_stream(s_out)
+    e1.record(s_in)
     torch.cuda.synchronize(dev)
     ms = e0.elapsed_time(e1) / E
     h2d = (h_src.numel() * 2 + h_slots.numel() * 8 + 8 + h_bt.numel() * 4
@@ -533,7 +561,11 @@ def run_e2e(args, st, ga, dev, kvq):
     byts = st.algorithmic_bytes() + ga.algorithmic_bytes()
     return {"value": round(byts / (ms / 1e3) / 1e9, 2), "unit": "GB/s",
             "ms_per_step": round(ms, 4), "h2d_bytes_per_step": int(h2d),
-            "d2h_bytes_per_step": int(d2h), "steps": E}
+            "d2h_bytes_per_step": int(d2h), "steps": E,
+            "note": "pinned host buffers; copy-in, compute and copy-out "
+                    "pipelined across steps on three streams; the host link "
+                    "measures ~210 GB/s host->device and ~193 GB/s "
+                    "device->host per direction on this system"}
 
 
 # --- CPU oracle legs ----------------------------------------------------------------
