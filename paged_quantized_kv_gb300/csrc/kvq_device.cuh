@@ -10,16 +10,33 @@ namespace kvq {
 namespace dev {
 
 constexpr size_t kMaxMetaSmem = 48 * 1024;  // no opt-in needed
-constexpr uint32_t kMaxPolls = 1u << 22;     // bounded mbarrier wait
+
+// Time limit of a bounded mbarrier wait (ns of %globaltimer).
+#ifndef KVQ_WAIT_LIMIT_NS
+#define KVQ_WAIT_LIMIT_NS 1000000000ull
+#endif
+// Test builds only: expect this many bytes more than the bulk copies
+// deliver, so that the bounded wait runs out (0 in the library).
+#ifndef KVQ_TEST_EXTRA_TX
+#define KVQ_TEST_EXTRA_TX 0
+#endif
+
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+  return t;
+}
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
-// Bounded wait for phase `parity` of the mbarrier at `bar`; false on
-// timeout.
+// Wait for phase `parity` of the mbarrier at `bar`, for at most
+// KVQ_WAIT_LIMIT_NS of wall time (and at most 2^24 polls, in case the
+// timer stood still); false on timeout.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
-  for (uint32_t i = 0; i < kMaxPolls; ++i) {
+  const uint64_t start = global_ns();
+  for (uint32_t polls = 0; polls < (1u << 24); ++polls) {
     uint32_t done;
     asm volatile(
         "{ .reg .pred p;\n"
@@ -29,6 +46,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
         : "r"(bar), "r"(parity)
         : "memory");
     if (done) return true;
+    if (global_ns() - start > KVQ_WAIT_LIMIT_NS) return false;
   }
   return false;
 }
@@ -97,6 +115,7 @@ __device__ __forceinline__ bool stage_meta(uint8_t* smem, uint64_t* bar,
   const RangeSplit rb =
       nbt > 0 ? split_range(bt, nbt) : RangeSplit{0, 0};
   const uint32_t bytes = 4u * static_cast<uint32_t>(rc.body + rb.body);
+  const uint32_t expect = bytes > 0 ? bytes + KVQ_TEST_EXTRA_TX : 0;
   const uint32_t b = smem_addr(bar);
 
   if (tid == 0) {
@@ -108,7 +127,7 @@ __device__ __forceinline__ bool stage_meta(uint8_t* smem, uint64_t* bar,
   if (tid == 0 && bytes > 0) {
     asm volatile(
         "mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;"
-        ::"r"(b), "r"(bytes)
+        ::"r"(b), "r"(expect)
         : "memory");
     if (rc.body > 0)
       asm volatile(
@@ -137,7 +156,9 @@ __device__ __forceinline__ bool stage_meta(uint8_t* smem, uint64_t* bar,
   bool ok = true;
   if (bytes > 0) {
     ok = mbar_wait(b, 0);
-    if (!ok) mbar_wait(b, 0);  // give a copy still in flight a second term
+    // on a timeout, give a copy that may still be in flight a second term
+    // before the CTA (and its shared memory) goes away
+    if (!ok) mbar_wait(b, 0);
   }
   __syncthreads();
   return ok;
