@@ -17,6 +17,9 @@ passage each function restates:
 * The NVFP4 paged load (the read side of the store) follows the same page
   layout and swizzle; its dequantisation rule is the plain inverse of the
   store's (the pages state none).
+* The indexer-K store (the write side of the gathered cache) uses a
+  per-token absmax rule (the pages state none): scale = amax / 448,
+  q = e4m3_rn_satfinite(k / scale).
 
 Parity status: every function here is pinned by ``tests/test_oracle_*.py``
 (format tables against closed forms and torch's float8 cast, hand-worked
@@ -112,6 +115,10 @@ class Oracle:
             c.c_int32, P, c.c_int64, c.c_int32, P, c.c_int32, c.c_int64,
             c.c_float, c.c_float, c.c_uint32, P, P, c.c_int64]
         lib.kvqo_load_nvfp4.restype = c.c_int
+        lib.kvqo_store_indexer_k.argtypes = [
+            P, c.c_int64, c.c_int32, c.c_int32, c.c_int32, P, c.c_int64,
+            c.c_int32, c.c_int64, P]
+        lib.kvqo_store_indexer_k.restype = c.c_int
         self.lib = lib
         self.path = lib_path
 
@@ -214,6 +221,23 @@ class Oracle:
             _ptr(k_scale))
         if rc != OK:
             raise ValueError(f"kvqo_gather_indexer_k failed: {rc}")
+
+    def store_indexer_k(self, k_bits: np.ndarray, k_stride0: int,
+                        num_tokens: int, head_dim: int, cache: np.ndarray,
+                        block_stride: int, block_size: int, num_blocks: int,
+                        slot_mapping: np.ndarray, dtype: int = DTYPE_BF16,
+                        k_base: int = 0) -> None:
+        """Indexer-K store into ``cache`` (uint8, modified in place): token
+        t (bits at ``k_base + t*k_stride0``) -> block slot / B, row slot % B
+        of [B*D fp8 K | B*4 fp32 scale] blocks."""
+        slots = np.ascontiguousarray(slot_mapping, dtype=np.int64)
+        assert cache.dtype == np.uint8 and cache.flags.c_contiguous
+        rc = self.lib.kvqo_store_indexer_k(
+            _ptr(k_bits, 2 * k_base), int(k_stride0), int(dtype),
+            int(num_tokens), int(head_dim), _ptr(cache), int(block_stride),
+            int(block_size), int(num_blocks), _ptr(slots))
+        if rc != OK:
+            raise ValueError(f"kvqo_store_indexer_k failed: {rc}")
 
     def load_nvfp4(self, kv_cache: np.ndarray, key_offset: int,
                    value_offset: int, page_stride: int, block_size: int,

@@ -416,3 +416,42 @@ int kvqo_load_nvfp4(const uint8_t* key_cache, const uint8_t* value_cache,
   }
   return KVQO_OK;
 }
+
+/* ------------------------------------------------------------------------ */
+/* Indexer-K store -- the write side of the cache the gather reads          */
+/* ([pr25931]: "quantized k/k_scale" in a paged indexer cache of blocks     */
+/* [B*D fp8 K | B*4 fp32 scale]).  The pages give no quantisation rule; the */
+/* reading taken is per-token absmax scaling: scale = amax / 448 (fp32      */
+/* IEEE division), q_i = e4m3_rn_satfinite(k_i / scale) (IEEE division),   */
+/* or q_i = 0 when amax = 0.  Token t with slot s >= 0 goes to block s / B, */
+/* row s % B; slot < 0 is skipped.                                          */
+/* ------------------------------------------------------------------------ */
+int kvqo_store_indexer_k(const uint16_t* k, int64_t k_stride0, int32_t dtype,
+                         int32_t num_tokens, int32_t head_dim, uint8_t* cache,
+                         int64_t block_stride, int32_t block_size,
+                         int64_t num_blocks, const int64_t* slot_mapping) {
+  if (num_tokens < 0 || head_dim <= 0 || block_size <= 0) return KVQO_ERR_ARG;
+  if (dtype != KVQO_DTYPE_BF16 && dtype != KVQO_DTYPE_F16) return KVQO_ERR_ARG;
+  const int64_t B = block_size, D = head_dim;
+  for (int64_t t = 0; t < num_tokens; ++t) {
+    const int64_t slot = slot_mapping[t];
+    if (slot < 0) continue;
+    const int64_t blk = slot / B, off = slot % B;
+    if (blk >= num_blocks) return KVQO_ERR_BOUNDS;
+    const uint16_t* row = k + t * k_stride0;
+    float amax = 0.0f;
+    for (int64_t d = 0; d < D; ++d) {
+      const float x = element_to_float(row[d], dtype);
+      if (!isfinite(x)) return KVQO_ERR_NONFINITE;
+      if (fabsf(x) > amax) amax = fabsf(x);
+    }
+    const float scale = amax / 448.0f; /* IEEE fp32 division */
+    uint8_t* dst = cache + blk * block_stride + off * D;
+    for (int64_t d = 0; d < D; ++d) {
+      const float x = element_to_float(row[d], dtype);
+      dst[d] = (amax == 0.0f) ? 0 : kvqo_e4m3_encode(x / scale);
+    }
+    memcpy(cache + blk * block_stride + B * D + off * 4, &scale, 4);
+  }
+  return KVQO_OK;
+}

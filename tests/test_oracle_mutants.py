@@ -8,10 +8,11 @@ import pytest
 import oracle
 from tests import test_oracle_formats as F
 from tests import test_oracle_gather as G
+from tests import test_oracle_indexer_store as I
 from tests import test_oracle_load as L
 from tests import test_oracle_store as S
 
-ALL_CHECKS = F.CHECKS + S.CHECKS + G.CHECKS + L.CHECKS
+ALL_CHECKS = F.CHECKS + S.CHECKS + G.CHECKS + L.CHECKS + I.CHECKS
 
 # (id, original text, planted mistake[, occurrence]) -- the mistake is
 # planted at the given occurrence of the original (default: the only one)
@@ -88,6 +89,17 @@ MUTANTS = [
      "const float c = (float)kvqo_e4m3_decode(*sptr) / side_scale[side];"),
     ("load_block_offset", "const int64_t off = p % B;\n      if (blk < 0",
      "const int64_t off = (p + 1) % B;\n      if (blk < 0", 1),
+    ("ik_wrong_format_max", "const float scale = amax / 448.0f;",
+     "const float scale = amax / 240.0f;"),
+    ("ik_multiplies_by_scale", "kvqo_e4m3_encode(x / scale)",
+     "kvqo_e4m3_encode(x * scale)"),
+    ("ik_signed_amax", "if (fabsf(x) > amax) amax = fabsf(x);",
+     "if (x > amax) amax = x;"),
+    ("ik_scale_slot",
+     "memcpy(cache + blk * block_stride + B * D + off * 4, &scale, 4);",
+     "memcpy(cache + blk * block_stride + B * D + (off ^ 1) * 4, &scale, 4);"),
+    ("ik_row_slot", "uint8_t* dst = cache + blk * block_stride + off * D;",
+     "uint8_t* dst = cache + blk * block_stride + (off ^ 1) * D;"),
     ("gather_row_bytes", "k_fp8[row * D + d] = block[off * D + d];",
      "k_fp8[row * D + d] = block[off * D + (d ^ 1)];"),
 ]
