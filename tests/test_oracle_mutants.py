@@ -63,7 +63,9 @@ MUTANTS = [
      "const float g_side[2] = {1.0f / k_scale, 1.0f / v_scale};",
      "const float g_side[2] = {1.0f / k_scale, 1.0f / k_scale};"),
     ("skip_rule_includes_zero", "if (slot < 0) continue;",
-     "if (slot <= 0) continue;"),
+     "if (slot <= 0) continue;", 0),
+    ("ik_skip_rule_includes_zero", "if (slot < 0) continue;",
+     "if (slot <= 0) continue;", 1),
     ("gather_offset", "const int64_t off = p % B;\n      if (blk < 0",
      "const int64_t off = (p + 1) % B;\n      if (blk < 0", 0),
     ("gather_scale_byte_order", "k_scale[row * 4 + k] = block[B * D + off * 4 + k];",
