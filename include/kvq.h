@@ -10,6 +10,8 @@
  *                         reshape_and_cache_nvfp4_dispatch).
  *   kvq_load_nvfp4        the read side of the store: NVFP4 pages named by a
  *                         block table -> bf16 K/V rows.
+ *   kvq_store_indexer_k   the write side of the indexer cache: bf16 K rows ->
+ *                         fp8 e4m3 + per-token fp32 scale, by slot.
  *   kvq_gather_indexer_k  fp8 indexer-K rows and per-token fp32 scales
  *                         gathered out of a paged cache (vLLM PR #25931 "Add
  *                         gather_indexer_k_quant_cache kernel"; PR #26456
@@ -235,6 +237,40 @@ kvq_status kvq_load_nvfp4(const uint8_t* key_cache, const uint8_t* value_cache,
                           const float* v_scale, int32_t out_dtype,
                           void* key_out, void* value_out, int64_t out_stride0,
                           uint32_t flags, int32_t* dev_error, void* stream);
+
+/*
+ * kvq_store_indexer_k -- the write side of the indexer cache that
+ * kvq_gather_indexer_k reads: quantise each token's K row to fp8 e4m3 with
+ * one fp32 scale and store both into the token's block slot.  (vLLM PR
+ * #25931: "quantized k/k_scale" in the indexer k cache.  The pages give no
+ * quantisation rule; per-token absmax scaling is taken.)
+ *
+ * For token t with s = slot_mapping[t] >= 0 (s < 0: skipped),
+ * blk = s / block_size, off = s % block_size:
+ *   amax  = max |k[t, d]|;  scale = amax / 448   (fp32 IEEE division)
+ *   q[d]  = amax == 0 ? 0 : e4m3_rn_satfinite(k[t, d] / scale)  (IEEE div)
+ *   block blk bytes [off*head_dim, +head_dim) = q;
+ *   bytes [block_size*head_dim + 4*off, +4)   = scale (fp32).
+ *
+ * k             bf16 or fp16 [num_tokens, head_dim], rows k_stride0
+ *               elements apart (multiple of 8); 16-byte aligned.
+ * head_dim      16, 32, 64, 128 or 256.
+ * kv_cache      block 0 of [block_size*head_dim | block_size*4] blocks,
+ *               block_stride bytes apart (multiple of 16, >= block_size *
+ *               (head_dim + 4)); 16-byte aligned.
+ * slot_mapping  int64 [num_tokens], distinct slots (duplicates race).
+ * flags         KVQ_F_PDL or 0.
+ * dev_error     nullable (KVQ_DEVERR_SLOT for slots >= num_blocks *
+ *               block_size, which are skipped).
+ * num_tokens == 0 returns KVQ_OK without launching.
+ */
+kvq_status kvq_store_indexer_k(const void* k, int64_t k_stride0,
+                               int32_t dtype, int32_t num_tokens,
+                               int32_t head_dim, uint8_t* kv_cache,
+                               int64_t block_stride, int32_t block_size,
+                               int64_t num_blocks,
+                               const int64_t* slot_mapping, uint32_t flags,
+                               int32_t* dev_error, void* stream);
 
 /* Static text for a status code. */
 const char* kvq_status_string(kvq_status status);

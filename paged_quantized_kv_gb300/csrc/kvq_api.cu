@@ -296,6 +296,48 @@ kvq_status kvq_load_nvfp4(const uint8_t* key_cache, const uint8_t* value_cache,
   return err == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
 }
 
+kvq_status kvq_store_indexer_k(const void* k, int64_t k_stride0,
+                               int32_t dtype, int32_t num_tokens,
+                               int32_t head_dim, uint8_t* kv_cache,
+                               int64_t block_stride, int32_t block_size,
+                               int64_t num_blocks,
+                               const int64_t* slot_mapping, uint32_t flags,
+                               int32_t* dev_error, void* stream) {
+  using namespace kvq;
+  if (dtype != KVQ_DTYPE_BF16 && dtype != KVQ_DTYPE_FP16) return KVQ_ERR_DTYPE;
+  if ((flags & ~static_cast<uint32_t>(KVQ_F_PDL)) != 0u) return KVQ_ERR_ARG;
+  if (num_tokens < 0 || block_size <= 0 || num_blocks < 0 || k_stride0 < 0)
+    return KVQ_ERR_SHAPE;
+  if (head_dim != 16 && head_dim != 32 && head_dim != 64 && head_dim != 128 &&
+      head_dim != 256)
+    return KVQ_ERR_SHAPE;
+  if (block_stride < static_cast<int64_t>(block_size) * (head_dim + 4))
+    return KVQ_ERR_SHAPE;
+  if (num_tokens == 0) return KVQ_OK;
+  if (k == nullptr || kv_cache == nullptr || slot_mapping == nullptr)
+    return KVQ_ERR_NULL;
+  if (!aligned(k, 16) || k_stride0 % 8 != 0 || !aligned(kv_cache, 16) ||
+      block_stride % 16 != 0 || !aligned(slot_mapping, 8))
+    return KVQ_ERR_ALIGN;
+  IndexerStoreParams p{};
+  p.k = static_cast<const uint16_t*>(k);
+  p.k_stride0 = k_stride0;
+  p.cache = kv_cache;
+  p.block_stride = block_stride;
+  p.slots = slot_mapping;
+  p.dev_error = dev_error;
+  p.num_slots = num_blocks * block_size;
+  p.num_tokens = num_tokens;
+  p.D = head_dim;
+  p.B = block_size;
+  p.b_shift = ilog2_exact(block_size);
+  p.f16 = dtype == KVQ_DTYPE_FP16;
+  p.pdl = (flags & KVQ_F_PDL) != 0u;
+  const cudaError_t err =
+      launch_store_indexer_k(p, static_cast<cudaStream_t>(stream));
+  return err == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
+}
+
 const char* kvq_status_string(kvq_status status) {
   switch (status) {
     case KVQ_OK: return "ok";

@@ -88,6 +88,25 @@ struct LoadParams {
 
 cudaError_t launch_load_nvfp4(const LoadParams& p, cudaStream_t stream);
 
+// ---------------------------------------------------------------------------
+// Indexer-K store (bf16/fp16 K -> e4m3 row + fp32 scale per token)
+// ---------------------------------------------------------------------------
+struct IndexerStoreParams {
+  const uint16_t* k;       // [num_tokens, D] bit patterns, row stride below
+  int64_t k_stride0;       // elements
+  uint8_t* cache;          // block 0: [B*D e4m3 | B*4 scale bytes]
+  int64_t block_stride;
+  const int64_t* slots;
+  int32_t* dev_error;      // nullable
+  int64_t num_slots;       // num_blocks * B
+  int64_t num_tokens;
+  int32_t D, B, b_shift;
+  bool f16, pdl;
+};
+
+cudaError_t launch_store_indexer_k(const IndexerStoreParams& p,
+                                   cudaStream_t stream);
+
 // Streaming-multiprocessor count of the current device (cached per device).
 int sm_count();
 

@@ -1,0 +1,203 @@
+// store_indexer_k.cu -- bf16/fp16 indexer K -> fp8 e4m3 + per-token fp32
+// scale in a paged indexer cache, sm_103a.  The write side of the cache
+// that cp_gather_indexer_k_quant_cache reads (vLLM PR #25931 "Add
+// gather_indexer_k_quant_cache kernel": "quantized k/k_scale" in blocks of
+// [block_size * head_dim fp8 K | block_size * 4 scale bytes]).
+//
+// The pages give no quantisation rule; per-token absmax scaling is taken:
+// scale = amax / 448 (IEEE fp32 division), q_i = e4m3_rn_satfinite(k_i /
+// scale) (IEEE division), q = 0 when amax = 0.  Token t with slot s >= 0
+// goes to block s / B, row s % B; s < 0 is skipped.
+//
+// GB300 design: HBM-bound, ~2 bytes read and ~1.03 written per element.
+// A token is L = head_dim / 8 lanes (16 for head_dim 128), each holding 8
+// elements from one 16-byte load; amax is a packed max.bf16x2 / max.f16x2
+// tree plus an xor-shuffle reduction over the L lanes; the quotients are
+// IEEE divisions (__fdiv_rn) and pairs are converted with
+// cvt.rn.satfinite.e4m3x2.f32.  Each lane writes its 8 code bytes (the
+// token's row is one contiguous run) and the first lane the scale.  The
+// grid is persistent; each lane keeps kUnroll tokens' loads in flight.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "kvq_internal.h"
+#include "kvq.h"
+
+namespace kvq {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kUnroll = 4;
+
+__device__ __forceinline__ uint4 ld_nc_16(const void* p) {
+  uint4 v;
+  asm volatile(
+      "ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+      : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+      : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ int64_t ld_nc_s64(const int64_t* p) {
+  int64_t v;
+  asm volatile("ld.global.nc.s64 %0, [%1];" : "=l"(v) : "l"(p));
+  return v;
+}
+
+template <bool kF16>
+__device__ __forceinline__ uint32_t half2_max(uint32_t a, uint32_t b) {
+  uint32_t d;
+  if constexpr (kF16)
+    asm("max.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  else
+    asm("max.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+// Packed pair -> two fp32 values (exact for both element types).
+template <bool kF16>
+__device__ __forceinline__ void widen2(uint32_t w, float& lo, float& hi) {
+  if constexpr (kF16) {
+    asm("{ .reg .f16 a, b;\n"
+        "  mov.b32 {a, b}, %2;\n"
+        "  cvt.f32.f16 %0, a;\n"
+        "  cvt.f32.f16 %1, b; }"
+        : "=f"(lo), "=f"(hi)
+        : "r"(w));
+  } else {
+    lo = __uint_as_float(w << 16);
+    hi = __uint_as_float(w & 0xFFFF0000u);
+  }
+}
+
+// Two fp32 -> e4m3 codes, rn, satfinite; `lo` in the low byte.
+__device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
+  uint16_t pair;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(pair) : "f"(hi),
+      "f"(lo));
+  return pair;
+}
+
+template <bool kF16, int L>
+__global__ void __launch_bounds__(kThreads)
+store_indexer_k_kernel(const IndexerStoreParams p) {
+  pdl_prologue();
+  constexpr int kTokPerWarp = 32 / L;
+  const int lane = threadIdx.x & 31;
+  const int sub = lane / L;      // token slot inside the warp
+  const int part = lane % L;     // 8-element chunk of the row
+  const int64_t warps = static_cast<int64_t>(gridDim.x) * (kThreads / 32);
+  const int64_t warp = static_cast<int64_t>(blockIdx.x) * (kThreads / 32) +
+                       (threadIdx.x >> 5);
+  const int64_t tstep = warps * kTokPerWarp;
+  const uint32_t seg_mask =
+      L == 32 ? 0xFFFFFFFFu : (((1u << L) - 1u) << (sub * L));
+
+  for (int64_t t0 = warp * kTokPerWarp + sub; t0 - sub < p.num_tokens;
+       t0 += kUnroll * tstep) {
+    uint4 raw[kUnroll];
+    int64_t slot[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int64_t t = t0 + u * tstep;
+      raw[u] = make_uint4(0u, 0u, 0u, 0u);
+      slot[u] = -1;
+      if (t < p.num_tokens) {
+        slot[u] = ld_nc_s64(p.slots + t);
+        raw[u] = ld_nc_16(p.k + t * p.k_stride0 + part * 8);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      // amax over the token's L lanes (every lane of the segment takes part)
+      const uint32_t m = half2_max<kF16>(
+          half2_max<kF16>(raw[u].x & 0x7FFF7FFFu, raw[u].y & 0x7FFF7FFFu),
+          half2_max<kF16>(raw[u].z & 0x7FFF7FFFu, raw[u].w & 0x7FFF7FFFu));
+      float lo, hi;
+      widen2<kF16>(m, lo, hi);
+      float amax = fmaxf(lo, hi);
+#pragma unroll
+      for (int o = L / 2; o > 0; o >>= 1)
+        amax = fmaxf(amax, __shfl_xor_sync(seg_mask, amax, o));
+      if (slot[u] < 0) continue;
+      if (slot[u] >= p.num_slots) {
+        if (p.dev_error != nullptr && part == 0)
+          atomicOr(p.dev_error, KVQ_DEVERR_SLOT);
+        continue;
+      }
+      const float scale = __fdiv_rn(amax, 448.0f);
+      float x[8];
+      widen2<kF16>(raw[u].x, x[0], x[1]);
+      widen2<kF16>(raw[u].y, x[2], x[3]);
+      widen2<kF16>(raw[u].z, x[4], x[5]);
+      widen2<kF16>(raw[u].w, x[6], x[7]);
+      uint32_t c01 = 0u, c23 = 0u, c45 = 0u, c67 = 0u;
+      if (amax != 0.0f) {
+        c01 = e4m3x2(__fdiv_rn(x[0], scale), __fdiv_rn(x[1], scale));
+        c23 = e4m3x2(__fdiv_rn(x[2], scale), __fdiv_rn(x[3], scale));
+        c45 = e4m3x2(__fdiv_rn(x[4], scale), __fdiv_rn(x[5], scale));
+        c67 = e4m3x2(__fdiv_rn(x[6], scale), __fdiv_rn(x[7], scale));
+      }
+      int64_t blk, off;
+      if (p.b_shift >= 0) {
+        blk = slot[u] >> p.b_shift;
+        off = slot[u] & (p.B - 1);
+      } else {
+        blk = slot[u] / p.B;
+        off = slot[u] - blk * p.B;
+      }
+      uint8_t* const base = p.cache + blk * p.block_stride;
+      const uint32_t w0 = c01 | (c23 << 16), w1 = c45 | (c67 << 16);
+      asm volatile("st.global.v2.u32 [%0], {%1, %2};" ::"l"(
+                       base + off * L * 8 + part * 8),
+                   "r"(w0), "r"(w1)
+                   : "memory");
+      if (part == 0)
+        *reinterpret_cast<float*>(base + static_cast<int64_t>(p.B) * L * 8 +
+                                  off * 4) = scale;
+    }
+  }
+}
+
+template <bool kF16, int L>
+cudaError_t launch(const IndexerStoreParams& p, cudaStream_t stream) {
+  static int ctas_per_sm[64] = {0};
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  int& occ = ctas_per_sm[dev & 63];
+  if (occ == 0) {
+    err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+        &occ, store_indexer_k_kernel<kF16, L>, kThreads, 0);
+    if (err != cudaSuccess) return err;
+    if (occ < 1) occ = 1;
+  }
+  const int64_t per_cta = (kThreads / 32) * (32 / L);
+  int64_t grid = static_cast<int64_t>(sm_count()) * occ;
+  const int64_t need = (p.num_tokens + per_cta - 1) / per_cta;
+  if (grid > need) grid = need;
+  if (grid < 1) grid = 1;
+  return launch_kernel(store_indexer_k_kernel<kF16, L>,
+                       static_cast<unsigned>(grid), kThreads, 0, stream,
+                       p.pdl, p);
+}
+
+template <bool kF16>
+cudaError_t launch_dim(const IndexerStoreParams& p, cudaStream_t stream) {
+  switch (p.D) {
+    case 16: return launch<kF16, 2>(p, stream);
+    case 32: return launch<kF16, 4>(p, stream);
+    case 64: return launch<kF16, 8>(p, stream);
+    case 128: return launch<kF16, 16>(p, stream);
+    default: return launch<kF16, 32>(p, stream);  // 256
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_store_indexer_k(const IndexerStoreParams& p,
+                                   cudaStream_t stream) {
+  return p.f16 ? launch_dim<true>(p, stream) : launch_dim<false>(p, stream);
+}
+
+}  // namespace kvq

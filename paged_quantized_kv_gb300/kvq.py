@@ -20,6 +20,8 @@ one:
   PR #26456).
 * ``kvq_load_nvfp4(key_cache, value_cache, block_table, cu_seq_lens,
   k_scale, v_scale, key_out, value_out)`` -- the read side of the store.
+* ``kvq_store_indexer_k(k, kv_cache, slot_mapping)`` -- the write side of
+  the indexer cache the gather reads.
 """
 from __future__ import annotations
 
@@ -90,6 +92,10 @@ def lib() -> ctypes.CDLL:
             c.c_int32, P, c.c_int64, c.c_int32, P, c.c_int32, c.c_int64, P,
             P, c.c_int32, P, P, c.c_int64, c.c_uint32, P, P]
         L.kvq_load_nvfp4.restype = c.c_int
+        L.kvq_store_indexer_k.argtypes = [
+            P, c.c_int64, c.c_int32, c.c_int32, c.c_int32, P, c.c_int64,
+            c.c_int32, c.c_int64, P, c.c_uint32, P, P]
+        L.kvq_store_indexer_k.restype = c.c_int
         L.kvq_status_string.argtypes = [c.c_int]
         L.kvq_status_string.restype = c.c_char_p
         L.kvq_version.argtypes = []
@@ -225,6 +231,33 @@ def kvq_load_nvfp4(key_cache: torch.Tensor, value_cache: torch.Tensor,
         int(flags), _ptr(dev_error),
         _stream_of(key_out) if stream is None else stream)
     _check("kvq_load_nvfp4", st)
+
+
+def kvq_store_indexer_k(k: torch.Tensor, kv_cache: torch.Tensor,
+                        slot_mapping: torch.Tensor,
+                        block_size: int | None = None, flags: int = 0,
+                        dev_error: torch.Tensor | None = None,
+                        stream: int | None = None) -> None:
+    """Indexer-K store (see ``include/kvq.h``): k bf16/fp16 [T, head_dim]
+    (last dim contiguous) into kv_cache uint8 [num_blocks, block_size,
+    head_dim + 4] (or [num_blocks, bytes] with ``block_size`` given)."""
+    dtypes = {torch.bfloat16: KVQ_DTYPE_BF16, torch.float16: KVQ_DTYPE_FP16}
+    if k.dtype not in dtypes or kv_cache.element_size() != 1:
+        raise KvqError("kvq_store_indexer_k", KVQ_ERR_DTYPE)
+    T, D = k.shape
+    if block_size is None:
+        if kv_cache.dim() != 3:
+            raise KvqError("kvq_store_indexer_k", KVQ_ERR_SHAPE)
+        block_size = kv_cache.size(1)
+    if (k.stride(1) != 1 or slot_mapping.dtype != torch.int64
+            or slot_mapping.numel() < T):
+        raise KvqError("kvq_store_indexer_k", KVQ_ERR_SHAPE)
+    st = lib().kvq_store_indexer_k(
+        k.data_ptr(), k.stride(0), dtypes[k.dtype], T, D,
+        kv_cache.data_ptr(), kv_cache.stride(0), int(block_size),
+        kv_cache.size(0), slot_mapping.data_ptr(), int(flags),
+        _ptr(dev_error), _stream_of(k) if stream is None else stream)
+    _check("kvq_store_indexer_k", st)
 
 
 def alloc_nvfp4_cache(num_blocks: int, block_size: int, num_heads: int,

@@ -431,3 +431,62 @@ def load_algorithmic_bytes(wl: StoreWorkload, block_table: np.ndarray,
     entries = int(((lens + B - 1) // B).sum())
     return (n * 2 * H * (D // 2 + D // 16) + n * 2 * H * D * 2
             + 4 * entries + 4 * cu_seq_lens.size)
+
+
+@dataclass
+class IndexerStoreWorkload:
+    """Inputs of one indexer-K store: K rows (bf16/fp16 bits, [T, D]) and
+    their slots in a [num_blocks] cache of [B*D | B*4] blocks; the slots
+    follow ``block_table`` / ``cu_seq_lens`` so a gather reads them back."""
+    name: str
+    k: np.ndarray
+    num_tokens: int
+    head_dim: int
+    block_size: int
+    num_blocks: int
+    slot_mapping: np.ndarray
+    block_table: np.ndarray
+    cu_seq_lens: np.ndarray
+    dtype: int = DTYPE_BF16
+
+    @property
+    def block_stride(self) -> int:
+        return self.block_size * (self.head_dim + 4)
+
+    def algorithmic_bytes(self) -> int:
+        """K rows read, slots read, e4m3 rows and scales written."""
+        n = int((self.slot_mapping >= 0).sum())
+        return (self.num_tokens * (self.head_dim * 2 + 8)
+                + n * (self.head_dim + 4))
+
+
+def make_indexer_store(name: str, seed: int, seq_lens, block_size: int,
+                       head_dim: int, num_blocks: int,
+                       dtype: int = DTYPE_BF16,
+                       spread: float = 2.0) -> IndexerStoreWorkload:
+    """K rows N(0,1) times a per-token magnitude 10^U(-spread, spread), on
+    the blocks of a random block table (sequences in cu order)."""
+    rng = np.random.default_rng(seed)
+    B, D = block_size, head_dim
+    lens = np.asarray(seq_lens, dtype=np.int64)
+    n = lens.size
+    need = (lens + B - 1) // B
+    mb = max(int(need.max()) if n else 1, 1)
+    assert n * mb <= num_blocks
+    bt = rng.permutation(num_blocks)[: n * mb].reshape(n, mb).astype(
+        np.int32)
+    cu = np.zeros(n + 1, dtype=np.int32)
+    cu[1:] = np.cumsum(lens)
+    T = int(cu[-1])
+    slots = np.concatenate(
+        [bt[b, np.arange(m) // B].astype(np.int64) * B + np.arange(m) % B
+         for b, m in enumerate(lens)] or [np.zeros(0, np.int64)])
+    x = rng.standard_normal((T, D)).astype(np.float32)
+    x *= (10.0 ** rng.uniform(-spread, spread, (T, 1))).astype(np.float32)
+    if dtype == DTYPE_F16:
+        x = np.clip(x, -60000, 60000)
+    return IndexerStoreWorkload(
+        name=name, k=element_bits(x.reshape(-1), dtype).reshape(T, D),
+        num_tokens=T, head_dim=D, block_size=B, num_blocks=num_blocks,
+        slot_mapping=slots.astype(np.int64), block_table=bt, cu_seq_lens=cu,
+        dtype=dtype)

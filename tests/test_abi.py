@@ -37,7 +37,8 @@ def header_functions():
 def test_exports_match_header(lib):
     declared = header_functions()
     assert {"kvq_store_nvfp4", "kvq_gather_indexer_k", "kvq_load_nvfp4",
-            "kvq_status_string", "kvq_version"} <= declared
+            "kvq_store_indexer_k", "kvq_status_string",
+            "kvq_version"} <= declared
     out = subprocess.run(["nm", "-D", "--defined-only", kvq.LIB_PATH],
                          capture_output=True, text=True, check=True).stdout
     exported = set(re.findall(r"\sT\s(kvq_\w+)$", out, flags=re.M))
@@ -178,3 +179,32 @@ def load(lib, **kw):
 ])
 def test_load_validation(lib, kw, code):
     assert load(lib, **kw) == code
+
+
+def istore(lib, **kw):
+    args = dict(k=A, k_stride0=128, dtype=0, num_tokens=10, head_dim=128,
+                kv_cache=A, block_stride=64 * 132, block_size=64,
+                num_blocks=4, slot_mapping=A, flags=0, dev_error=None,
+                stream=None)
+    args.update(kw)
+    return lib.kvq_store_indexer_k(*args.values())
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(dtype=2), kvq.KVQ_ERR_DTYPE),
+    (dict(flags=1), kvq.KVQ_ERR_ARG),
+    (dict(head_dim=96), kvq.KVQ_ERR_SHAPE),
+    (dict(head_dim=512), kvq.KVQ_ERR_SHAPE),
+    (dict(block_stride=64 * 131), kvq.KVQ_ERR_SHAPE),
+    (dict(num_tokens=-2), kvq.KVQ_ERR_SHAPE),
+    (dict(block_size=0), kvq.KVQ_ERR_SHAPE),
+    (dict(k=None), kvq.KVQ_ERR_NULL),
+    (dict(slot_mapping=None), kvq.KVQ_ERR_NULL),
+    (dict(k=A + 8), kvq.KVQ_ERR_ALIGN),
+    (dict(k_stride0=132), kvq.KVQ_ERR_ALIGN),
+    (dict(block_stride=64 * 132 + 8), kvq.KVQ_ERR_ALIGN),
+    (dict(slot_mapping=A + 4), kvq.KVQ_ERR_ALIGN),
+    (dict(num_tokens=0, k=None), kvq.KVQ_OK),
+])
+def test_indexer_store_validation(lib, kw, code):
+    assert istore(lib, **kw) == code
