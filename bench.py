@@ -322,6 +322,20 @@ def run_ours(args):
         flags=kvq.KVQ_F_PDL_EARLY_META, dev_error=dev_err, stream=sh), K)
     load_bytes = wlmod.load_algorithmic_bytes(st, lbt, lcu)
     del k_out, v_out
+    # the indexer cache's write side on the gather's shape (K rows rotated
+    # over GATHER_SETS copies: 33.5 MB each, none L2-resident at launch)
+    iw = wlmod.make_indexer_store("long_indexer_store", rank_seed(4, rank),
+                                  [512] * 256, 64, 128, 8192)
+    ik = [torch.from_numpy(iw.k.view(np.int16)).to(dev).view(torch.bfloat16)
+          for _ in range(GATHER_SETS)]
+    islots = torch.from_numpy(iw.slot_mapping).to(dev)
+    icache = torch.empty((iw.num_blocks, iw.block_size, iw.head_dim + 4),
+                         dtype=torch.uint8, device=dev)
+    istore_ms = span_ms(lambda i: kvq.kvq_store_indexer_k(
+        ik[i % GATHER_SETS], icache, islots, flags=PDL, dev_error=dev_err,
+        stream=sh), K)
+    istore_bytes = iw.algorithmic_bytes()
+    del ik, icache
     # keep the same steps running so the clock sampler sees the load
     t1 = time.perf_counter()
     j = 0
@@ -413,6 +427,15 @@ def run_ours(args):
                 "GB_s": round(st_bytes / v / 1e6, 1),
                 "frac_of_peak": round(st_bytes / v / 1e6 / peak, 4)}
             for k, v in variants_ms.items()},
+        "store_indexer_k": {
+            "note": "write side of the indexer cache on the gather's shape "
+                    "(131072 tokens, head_dim 128, block_size 64), not part "
+                    "of the step",
+            "ms": round(istore_ms, 5),
+            "GB_s": round(istore_bytes / istore_ms / 1e6, 1),
+            "frac_of_peak": round(istore_bytes / istore_ms / 1e6 / peak, 4),
+            "tokens_per_s": round(iw.num_tokens / (istore_ms / 1e3), 1),
+            "algorithmic_bytes": istore_bytes},
         "single_launch_after_l2_write_flush": {
             "note": "each kernel alone after writing a 256 MiB buffer "
                     "(L2 left dirty), events around the launch; includes "
