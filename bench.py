@@ -54,7 +54,8 @@ def parse_args():
     ap.add_argument("--cpu-sample-tokens", type=int, default=65536)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--clock-window-s", type=float, default=1.5)
-    ap.add_argument("--kernel-only", choices=["store", "gather", "load"],
+    ap.add_argument("--kernel-only",
+                    choices=["store", "gather", "load", "istore"],
                     help="launch only this kernel (each launch after an L2 "
                          "flush) and print its mean time; used for ncu")
     return ap.parse_args()
@@ -725,6 +726,19 @@ def run_kernel_only(args):
                 kvq.kvq_load_nvfp4(kc, vc, lbt_d, lcu_d, ks, vs, k_out,
                                    v_out)
             byts = wlmod.load_algorithmic_bytes(st, lbt, lcu)
+    elif args.kernel_only == "istore":
+        from paged_quantized_kv_gb300 import workloads as wlmod
+        iw = wlmod.make_indexer_store("long_indexer_store", 4, [512] * 256,
+                                      64, 128, 8192)
+        ik = torch.from_numpy(iw.k.view(np.int16)).to(dev).view(
+            torch.bfloat16)
+        islots = torch.from_numpy(iw.slot_mapping).to(dev)
+        icache = torch.empty((iw.num_blocks, iw.block_size, iw.head_dim + 4),
+                             dtype=torch.uint8, device=dev)
+
+        def launch():
+            kvq.kvq_store_indexer_k(ik, icache, islots)
+        byts = iw.algorithmic_bytes()
     else:
         gcache = torch.from_numpy(ga.cache).to(dev).view(ga.num_blocks, -1)
         bt = torch.from_numpy(ga.block_table).to(dev)
