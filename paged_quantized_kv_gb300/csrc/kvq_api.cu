@@ -333,6 +333,7 @@ kvq_status kvq_store_indexer_k(const void* k, int64_t k_stride0,
   p.b_shift = ilog2_exact(block_size);
   p.f16 = dtype == KVQ_DTYPE_FP16;
   p.pdl = (flags & KVQ_F_PDL) != 0u;
+  p.vec32 = aligned(k, 32) && k_stride0 % 16 == 0;
   const cudaError_t err =
       launch_store_indexer_k(p, static_cast<cudaStream_t>(stream));
   return err == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;

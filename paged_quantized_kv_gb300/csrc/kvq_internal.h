@@ -102,6 +102,7 @@ struct IndexerStoreParams {
   int64_t num_tokens;
   int32_t D, B, b_shift;
   bool f16, pdl;
+  bool vec32;              // rows start 32-byte aligned (256-bit loads)
 };
 
 cudaError_t launch_store_indexer_k(const IndexerStoreParams& p,

@@ -9,14 +9,17 @@
 // scale) (IEEE division), q = 0 when amax = 0.  Token t with slot s >= 0
 // goes to block s / B, row s % B; s < 0 is skipped.
 //
-// GB300 design: HBM-bound, ~2 bytes read and ~1.03 written per element.
-// A token is L = head_dim / 8 lanes (16 for head_dim 128), each holding 8
-// elements from one 16-byte load; amax is a packed max.bf16x2 / max.f16x2
-// tree plus an xor-shuffle reduction over the L lanes; the quotients are
-// IEEE divisions (__fdiv_rn) and pairs are converted with
-// cvt.rn.satfinite.e4m3x2.f32.  Each lane writes its 8 code bytes (the
-// token's row is one contiguous run) and the first lane the scale.  The
-// grid is persistent; each lane keeps kUnroll tokens' loads in flight.
+// GB300 design: HBM-bound, ~2 bytes read and ~1.03 written per element, and
+// without care issue-bound on the per-element divisions.  A token is
+// L = head_dim / 16 lanes (8 for head_dim 128; 4 tokens per warp), each
+// holding 16 elements from one 256-bit load; amax is a packed max.bf16x2 /
+// max.f16x2 tree plus an xor-shuffle reduction over the L lanes; the
+// quotients take a fast path that is proven to give the IEEE quotient's
+// e4m3 code (see quotients_fast) and fall back to __fdiv_rn otherwise;
+// pairs are converted with cvt.rn.satfinite.e4m3x2.f32.  Each lane writes
+// its 16 code bytes (the token's row is one contiguous run) and the first
+// lane the scale.  The grid is persistent; each lane keeps kUnroll tokens'
+// loads in flight.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -29,13 +32,26 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kUnroll = 4;
 
-__device__ __forceinline__ uint4 ld_nc_16(const void* p) {
-  uint4 v;
-  asm volatile(
-      "ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
-      : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-      : "l"(p));
-  return v;
+// 16 elements (32 bytes) of a row: one 256-bit load when 32-byte aligned.
+__device__ __forceinline__ void load16(const uint16_t* p, uint32_t (&w)[8],
+                                       bool vec32) {
+  if (vec32) {
+    asm volatile(
+        "ld.global.nc.L1::no_allocate.v8.u32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+        : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]), "=r"(w[4]),
+          "=r"(w[5]), "=r"(w[6]), "=r"(w[7])
+        : "l"(p));
+  } else {
+    asm volatile(
+        "ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+        : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
+        : "l"(p));
+    asm volatile(
+        "ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+        : "=r"(w[4]), "=r"(w[5]), "=r"(w[6]), "=r"(w[7])
+        : "l"(p + 8));
+  }
 }
 
 __device__ __forceinline__ int64_t ld_nc_s64(const int64_t* p) {
@@ -78,6 +94,49 @@ __device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
   return pair;
 }
 
+// x / scale for four pairs, into e4m3 codes, bit-identical to the IEEE
+// quotients rounded to e4m3.  Fast path (P. Markstein, "Computation of
+// elementary functions on the IBM RISC System/6000 processor", IBM J. Res.
+// Dev. 34(1), 1990): with y = RN(1/scale), q0 = RN(x*y) is within an ulp of
+// x/scale, the residual r = x - q0*scale is exact (fma), and
+// q = RN(q0 + r*y) is within one ulp of x/scale.  The IEEE quotient is
+// within half an ulp, so both round to the same e4m3 code unless q lies
+// within one ulp of an e4m3 rounding midpoint (mantissa bits 19..0 of q
+// equal to 0x7FFFF, 0x80000 or 0x80001) or in the e4m3 subnormal range
+// (|q| < 2^-6); then the lane recomputes every quotient with __fdiv_rn.
+// Exact zeros keep their sign (x / scale = +-0).
+__device__ __forceinline__ bool quotients_fast(const float (&x)[16], float y,
+                                               float scale, float (&q)[16]) {
+  uint32_t bad = 0u;
+#pragma unroll
+  for (int i = 0; i < 16; i += 2) {
+    const uint64_t xx = (static_cast<uint64_t>(__float_as_uint(x[i + 1]))
+                         << 32) | __float_as_uint(x[i]);
+    const uint64_t yy = (static_cast<uint64_t>(__float_as_uint(y)) << 32) |
+                        __float_as_uint(y);
+    const uint64_t ns = (static_cast<uint64_t>(__float_as_uint(-scale))
+                         << 32) | __float_as_uint(-scale);
+    uint64_t q0, r, q1;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(q0) : "l"(xx), "l"(yy));
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(q0), "l"(ns),
+        "l"(xx));
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(q1) : "l"(r), "l"(yy),
+        "l"(q0));
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const uint32_t b = static_cast<uint32_t>(q1 >> (32 * h));
+      const float xv = x[i + h];
+      const float qv = xv == 0.0f ? xv : __uint_as_float(b);
+      q[i + h] = qv;
+      const uint32_t a = b & 0x7FFFFFFFu;
+      // near a midpoint: (mantissa - 0x7FFFF) mod 2^20 <= 2
+      bad |= (((b + 0x80001u) & 0xFFFFFu) <= 2u) ? 1u : 0u;
+      bad |= (xv != 0.0f && a < 0x3C800000u) ? 1u : 0u;  // |q| < 2^-6
+    }
+  }
+  return bad == 0u;
+}
+
 template <bool kF16, int L>
 __global__ void __launch_bounds__(kThreads)
 store_indexer_k_kernel(const IndexerStoreParams p) {
@@ -85,7 +144,7 @@ store_indexer_k_kernel(const IndexerStoreParams p) {
   constexpr int kTokPerWarp = 32 / L;
   const int lane = threadIdx.x & 31;
   const int sub = lane / L;      // token slot inside the warp
-  const int part = lane % L;     // 8-element chunk of the row
+  const int part = lane % L;     // 16-element chunk of the row
   const int64_t warps = static_cast<int64_t>(gridDim.x) * (kThreads / 32);
   const int64_t warp = static_cast<int64_t>(blockIdx.x) * (kThreads / 32) +
                        (threadIdx.x >> 5);
@@ -95,24 +154,26 @@ store_indexer_k_kernel(const IndexerStoreParams p) {
 
   for (int64_t t0 = warp * kTokPerWarp + sub; t0 - sub < p.num_tokens;
        t0 += kUnroll * tstep) {
-    uint4 raw[kUnroll];
+    uint32_t raw[kUnroll][8];
     int64_t slot[kUnroll];
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
       const int64_t t = t0 + u * tstep;
-      raw[u] = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) raw[u][k] = 0u;
       slot[u] = -1;
       if (t < p.num_tokens) {
         slot[u] = ld_nc_s64(p.slots + t);
-        raw[u] = ld_nc_16(p.k + t * p.k_stride0 + part * 8);
+        load16(p.k + t * p.k_stride0 + part * 16, raw[u], p.vec32);
       }
     }
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
       // amax over the token's L lanes (every lane of the segment takes part)
-      const uint32_t m = half2_max<kF16>(
-          half2_max<kF16>(raw[u].x & 0x7FFF7FFFu, raw[u].y & 0x7FFF7FFFu),
-          half2_max<kF16>(raw[u].z & 0x7FFF7FFFu, raw[u].w & 0x7FFF7FFFu));
+      uint32_t m = raw[u][0] & 0x7FFF7FFFu;
+#pragma unroll
+      for (int k = 1; k < 8; ++k)
+        m = half2_max<kF16>(m, raw[u][k] & 0x7FFF7FFFu);
       float lo, hi;
       widen2<kF16>(m, lo, hi);
       float amax = fmaxf(lo, hi);
@@ -126,17 +187,22 @@ store_indexer_k_kernel(const IndexerStoreParams p) {
         continue;
       }
       const float scale = __fdiv_rn(amax, 448.0f);
-      float x[8];
-      widen2<kF16>(raw[u].x, x[0], x[1]);
-      widen2<kF16>(raw[u].y, x[2], x[3]);
-      widen2<kF16>(raw[u].z, x[4], x[5]);
-      widen2<kF16>(raw[u].w, x[6], x[7]);
-      uint32_t c01 = 0u, c23 = 0u, c45 = 0u, c67 = 0u;
+      uint32_t codes[4] = {0u, 0u, 0u, 0u};
       if (amax != 0.0f) {
-        c01 = e4m3x2(__fdiv_rn(x[0], scale), __fdiv_rn(x[1], scale));
-        c23 = e4m3x2(__fdiv_rn(x[2], scale), __fdiv_rn(x[3], scale));
-        c45 = e4m3x2(__fdiv_rn(x[4], scale), __fdiv_rn(x[5], scale));
-        c67 = e4m3x2(__fdiv_rn(x[6], scale), __fdiv_rn(x[7], scale));
+        float x[16], q[16];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) widen2<kF16>(raw[u][k], x[2 * k],
+                                                 x[2 * k + 1]);
+        bool fast = scale >= 0x1p-90f && scale < 0x1p100f;
+        if (fast) fast = quotients_fast(x, __fdiv_rn(1.0f, scale), scale, q);
+        if (!fast) {
+#pragma unroll
+          for (int k = 0; k < 16; ++k) q[k] = __fdiv_rn(x[k], scale);
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          codes[k] = e4m3x2(q[4 * k], q[4 * k + 1]) |
+                     (e4m3x2(q[4 * k + 2], q[4 * k + 3]) << 16);
       }
       int64_t blk, off;
       if (p.b_shift >= 0) {
@@ -147,13 +213,13 @@ store_indexer_k_kernel(const IndexerStoreParams p) {
         off = slot[u] - blk * p.B;
       }
       uint8_t* const base = p.cache + blk * p.block_stride;
-      const uint32_t w0 = c01 | (c23 << 16), w1 = c45 | (c67 << 16);
-      asm volatile("st.global.v2.u32 [%0], {%1, %2};" ::"l"(
-                       base + off * L * 8 + part * 8),
-                   "r"(w0), "r"(w1)
+      asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(
+                       base + off * L * 16 + part * 16),
+                   "r"(codes[0]), "r"(codes[1]), "r"(codes[2]),
+                   "r"(codes[3])
                    : "memory");
       if (part == 0)
-        *reinterpret_cast<float*>(base + static_cast<int64_t>(p.B) * L * 8 +
+        *reinterpret_cast<float*>(base + static_cast<int64_t>(p.B) * L * 16 +
                                   off * 4) = scale;
     }
   }
@@ -172,7 +238,7 @@ cudaError_t launch(const IndexerStoreParams& p, cudaStream_t stream) {
     if (err != cudaSuccess) return err;
     if (occ < 1) occ = 1;
   }
-  const int64_t per_cta = (kThreads / 32) * (32 / L);
+  const int64_t per_cta = (kThreads / 32) * (32 / L);  // tokens per step
   int64_t grid = static_cast<int64_t>(sm_count()) * occ;
   const int64_t need = (p.num_tokens + per_cta - 1) / per_cta;
   if (grid > need) grid = need;
@@ -184,12 +250,12 @@ cudaError_t launch(const IndexerStoreParams& p, cudaStream_t stream) {
 
 template <bool kF16>
 cudaError_t launch_dim(const IndexerStoreParams& p, cudaStream_t stream) {
-  switch (p.D) {
-    case 16: return launch<kF16, 2>(p, stream);
-    case 32: return launch<kF16, 4>(p, stream);
-    case 64: return launch<kF16, 8>(p, stream);
-    case 128: return launch<kF16, 16>(p, stream);
-    default: return launch<kF16, 32>(p, stream);  // 256
+  switch (p.D) {  // L = head_dim / 16 lanes per token
+    case 16: return launch<kF16, 1>(p, stream);
+    case 32: return launch<kF16, 2>(p, stream);
+    case 64: return launch<kF16, 4>(p, stream);
+    case 128: return launch<kF16, 8>(p, stream);
+    default: return launch<kF16, 16>(p, stream);  // 256
   }
 }
 

@@ -108,3 +108,32 @@ def test_pdl_gather_reads_rows_just_stored(orc):
                        "rows")
     assert_bytes_equal(out_s.cpu().numpy().reshape(-1), scs.reshape(-1),
                        "scales")
+
+
+@pytest.mark.parametrize("amax_mult", [1.0, 1.1, 0.73])
+def test_quotients_on_e4m3_midpoints(orc, amax_mult):
+    """Rows whose quotients k / scale fall exactly on e4m3 rounding
+    midpoints (ties, where the kernel's division fast path must hand over to
+    the IEEE division) and one bf16 step either side of them."""
+    e4 = torch.arange(127, dtype=torch.int32).to(torch.uint8).view(
+        torch.float8_e4m3fn).float().numpy().astype(np.float64)
+    mids = (e4[8:-1] + e4[9:]) / 2          # normal-range midpoints
+    rng = np.random.default_rng(84)
+    T, D = 64, 128
+    x = np.zeros((T, D), np.float64)
+    for t in range(T):
+        e = 2.0 ** rng.integers(-8, 8)
+        row = rng.choice(mids, D) * np.where(rng.random(D) < .5, -1, 1) * e
+        row[0] = 448.0 * e * amax_mult
+        x[t] = row
+    bits = W.bf16_bits(x.astype(np.float32).reshape(-1)).reshape(T, D)
+    near = bits.astype(np.int32) + rng.integers(-1, 2, size=bits.shape)
+    near[:, 0] = bits[:, 0]
+    bits[T // 2:] = near[T // 2:].astype(np.uint16)
+    slots = np.arange(T, dtype=np.int64)
+    wl = W.IndexerStoreWorkload(
+        name="midpoints", k=bits, num_tokens=T, head_dim=D, block_size=16,
+        num_blocks=T // 16, slot_mapping=slots,
+        block_table=np.arange(T // 16, dtype=np.int32)[None, :],
+        cu_seq_lens=np.array([0, T], np.int32))
+    _compare(orc, wl)
