@@ -10,16 +10,15 @@
 // goes to block s / B, row s % B; s < 0 is skipped.
 //
 // GB300 design: HBM-bound, ~2 bytes read and ~1.03 written per element, and
-// without care issue-bound on the per-element divisions.  A token is
+// close to issue-bound on the per-element divisions.  A token is
 // L = head_dim / 16 lanes (8 for head_dim 128; 4 tokens per warp), each
 // holding 16 elements from one 256-bit load; amax is a packed max.bf16x2 /
 // max.f16x2 tree plus an xor-shuffle reduction over the L lanes; the
-// quotients take a fast path that is proven to give the IEEE quotient's
-// e4m3 code (see quotients_fast) and fall back to __fdiv_rn otherwise;
-// pairs are converted with cvt.rn.satfinite.e4m3x2.f32.  Each lane writes
-// its 16 code bytes (the token's row is one contiguous run) and the first
-// lane the scale.  The grid is persistent; each lane keeps kUnroll tokens'
-// loads in flight.
+// quotients are IEEE divisions (__fdiv_rn) and pairs are converted with
+// cvt.rn.satfinite.e4m3x2.f32.  Each lane writes its 16 code bytes (the
+// token's row is one contiguous run) and the first lane the scale.  The
+// grid is persistent, trimmed so its last iteration is as full as the
+// others; each lane keeps kUnroll tokens' loads in flight.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -30,7 +29,10 @@ namespace kvq {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kUnroll = 4;
+#ifndef KVQ_ISTORE_UNROLL
+#define KVQ_ISTORE_UNROLL 2
+#endif
+constexpr int kUnroll = KVQ_ISTORE_UNROLL;
 
 // 16 elements (32 bytes) of a row: one 256-bit load when 32-byte aligned.
 __device__ __forceinline__ void load16(const uint16_t* p, uint32_t (&w)[8],
@@ -94,49 +96,6 @@ __device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
   return pair;
 }
 
-// x / scale for four pairs, into e4m3 codes, bit-identical to the IEEE
-// quotients rounded to e4m3.  Fast path (P. Markstein, "Computation of
-// elementary functions on the IBM RISC System/6000 processor", IBM J. Res.
-// Dev. 34(1), 1990): with y = RN(1/scale), q0 = RN(x*y) is within an ulp of
-// x/scale, the residual r = x - q0*scale is exact (fma), and
-// q = RN(q0 + r*y) is within one ulp of x/scale.  The IEEE quotient is
-// within half an ulp, so both round to the same e4m3 code unless q lies
-// within one ulp of an e4m3 rounding midpoint (mantissa bits 19..0 of q
-// equal to 0x7FFFF, 0x80000 or 0x80001) or in the e4m3 subnormal range
-// (|q| < 2^-6); then the lane recomputes every quotient with __fdiv_rn.
-// Exact zeros keep their sign (x / scale = +-0).
-__device__ __forceinline__ bool quotients_fast(const float (&x)[16], float y,
-                                               float scale, float (&q)[16]) {
-  uint32_t bad = 0u;
-#pragma unroll
-  for (int i = 0; i < 16; i += 2) {
-    const uint64_t xx = (static_cast<uint64_t>(__float_as_uint(x[i + 1]))
-                         << 32) | __float_as_uint(x[i]);
-    const uint64_t yy = (static_cast<uint64_t>(__float_as_uint(y)) << 32) |
-                        __float_as_uint(y);
-    const uint64_t ns = (static_cast<uint64_t>(__float_as_uint(-scale))
-                         << 32) | __float_as_uint(-scale);
-    uint64_t q0, r, q1;
-    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(q0) : "l"(xx), "l"(yy));
-    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(q0), "l"(ns),
-        "l"(xx));
-    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(q1) : "l"(r), "l"(yy),
-        "l"(q0));
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const uint32_t b = static_cast<uint32_t>(q1 >> (32 * h));
-      const float xv = x[i + h];
-      const float qv = xv == 0.0f ? xv : __uint_as_float(b);
-      q[i + h] = qv;
-      const uint32_t a = b & 0x7FFFFFFFu;
-      // near a midpoint: (mantissa - 0x7FFFF) mod 2^20 <= 2
-      bad |= (((b + 0x80001u) & 0xFFFFFu) <= 2u) ? 1u : 0u;
-      bad |= (xv != 0.0f && a < 0x3C800000u) ? 1u : 0u;  // |q| < 2^-6
-    }
-  }
-  return bad == 0u;
-}
-
 template <bool kF16, int L>
 __global__ void __launch_bounds__(kThreads)
 store_indexer_k_kernel(const IndexerStoreParams p) {
@@ -189,20 +148,17 @@ store_indexer_k_kernel(const IndexerStoreParams p) {
       const float scale = __fdiv_rn(amax, 448.0f);
       uint32_t codes[4] = {0u, 0u, 0u, 0u};
       if (amax != 0.0f) {
-        float x[16], q[16];
+        float x[16];
 #pragma unroll
         for (int k = 0; k < 8; ++k) widen2<kF16>(raw[u][k], x[2 * k],
                                                  x[2 * k + 1]);
-        bool fast = scale >= 0x1p-90f && scale < 0x1p100f;
-        if (fast) fast = quotients_fast(x, __fdiv_rn(1.0f, scale), scale, q);
-        if (!fast) {
-#pragma unroll
-          for (int k = 0; k < 16; ++k) q[k] = __fdiv_rn(x[k], scale);
-        }
 #pragma unroll
         for (int k = 0; k < 4; ++k)
-          codes[k] = e4m3x2(q[4 * k], q[4 * k + 1]) |
-                     (e4m3x2(q[4 * k + 2], q[4 * k + 3]) << 16);
+          codes[k] =
+              e4m3x2(__fdiv_rn(x[4 * k], scale),
+                     __fdiv_rn(x[4 * k + 1], scale)) |
+              (e4m3x2(__fdiv_rn(x[4 * k + 2], scale),
+                      __fdiv_rn(x[4 * k + 3], scale)) << 16);
       }
       int64_t blk, off;
       if (p.b_shift >= 0) {
@@ -238,10 +194,13 @@ cudaError_t launch(const IndexerStoreParams& p, cudaStream_t stream) {
     if (err != cudaSuccess) return err;
     if (occ < 1) occ = 1;
   }
-  const int64_t per_cta = (kThreads / 32) * (32 / L);  // tokens per step
-  int64_t grid = static_cast<int64_t>(sm_count()) * occ;
-  const int64_t need = (p.num_tokens + per_cta - 1) / per_cta;
-  if (grid > need) grid = need;
+  // tokens per CTA per loop iteration; the grid is trimmed so the last
+  // iteration is as full as the others
+  const int64_t per_cta = (kThreads / 32) * (32 / L) * kUnroll;
+  const int64_t resident = static_cast<int64_t>(sm_count()) * occ;
+  const int64_t iters =
+      (p.num_tokens + resident * per_cta - 1) / (resident * per_cta);
+  int64_t grid = (p.num_tokens + iters * per_cta - 1) / (iters * per_cta);
   if (grid < 1) grid = 1;
   return launch_kernel(store_indexer_k_kernel<kF16, L>,
                        static_cast<unsigned>(grid), kThreads, 0, stream,
