@@ -20,6 +20,9 @@ passage each function restates:
 * The indexer-K store (the write side of the gathered cache) uses a
   per-token absmax rule (the pages state none): scale = amax / 448,
   q = e4m3_rn_satfinite(k / scale).
+* Paged decode attention over the NVFP4 cache (vLLM PR #12348 "[ROCm]
+  Faster Custom Paged Attention kernels" shows the op's signature only):
+  plain softmax attention in double over the exactly dequantised cache.
 
 Parity status: every function here is pinned by ``tests/test_oracle_*.py``
 (format tables against closed forms and torch's float8 cast, hand-worked
@@ -119,6 +122,12 @@ class Oracle:
             P, c.c_int64, c.c_int32, c.c_int32, c.c_int32, P, c.c_int64,
             c.c_int32, c.c_int64, P]
         lib.kvqo_store_indexer_k.restype = c.c_int
+        lib.kvqo_paged_attention_nvfp4.argtypes = [
+            P, c.c_int64, c.c_int32, c.c_int32, c.c_int32, c.c_int32,
+            c.c_int32, P, P, c.c_int64, c.c_int32, c.c_int64, c.c_int32, P,
+            c.c_int64, c.c_int32, P, c.c_float, c.c_float, c.c_float,
+            c.c_uint32, P, P]
+        lib.kvqo_paged_attention_nvfp4.restype = c.c_int
         self.lib = lib
         self.path = lib_path
 
@@ -263,6 +272,40 @@ class Oracle:
         if rc != OK:
             raise ValueError(f"kvqo_load_nvfp4 failed: {rc}")
         return k[:total_tokens], v[:total_tokens]
+
+    def paged_attention_nvfp4(self, query_bits: np.ndarray, kv_cache: np.ndarray,
+                              key_offset: int, value_offset: int,
+                              page_stride: int, block_size: int,
+                              num_blocks: int, layout: int, num_kv_heads: int,
+                              block_table: np.ndarray,
+                              context_lens: np.ndarray, k_scale: float,
+                              v_scale: float, scale: float, flags: int = 0,
+                              dtype: int = DTYPE_BF16):
+        """Paged decode attention over the NVFP4 cache.
+
+        ``query_bits``: uint16 bf16 (or fp16) bits [num_seqs, Hq, D].
+        Returns (out, mag), float64 [num_seqs, Hq, D]: the exact attention
+        output and sum_t p_t |V^[t, d]|."""
+        q = np.ascontiguousarray(query_bits, dtype=np.uint16)
+        assert q.ndim == 3
+        n, Hq, D = q.shape
+        bt = np.ascontiguousarray(block_table, dtype=np.int32)
+        assert bt.ndim == 2 and bt.shape[0] >= n
+        lens = np.ascontiguousarray(context_lens, dtype=np.int32)
+        assert lens.size >= n
+        out = np.zeros((max(n, 1), Hq, D), dtype=np.float64)
+        mag = np.zeros((max(n, 1), Hq, D), dtype=np.float64)
+        rc = self.lib.kvqo_paged_attention_nvfp4(
+            _ptr(q), Hq * D, int(dtype), int(n), int(Hq), int(num_kv_heads),
+            int(D), _ptr(kv_cache, key_offset), _ptr(kv_cache, value_offset),
+            int(page_stride), int(block_size), int(num_blocks), int(layout),
+            _ptr(bt), int(bt.shape[1]), int(bt.shape[1]), _ptr(lens),
+            float(np.float32(k_scale)), float(np.float32(v_scale)),
+            float(np.float32(scale)), int(flags), _ptr(out), _ptr(mag))
+        if rc != OK:
+            raise ValueError(f"kvqo_paged_attention_nvfp4 failed: {rc}")
+        return out[:n], mag[:n]
+
 
 _default = None
 _lock = threading.Lock()

@@ -13,6 +13,9 @@
  *   [pr25931]   vLLM PR #25931 "Add gather_indexer_k_quant_cache kernel".
  *   [pr26456]   vLLM PR #26456 "[Deepseek-V3.2][Kernel] Integrate cuda
  *               indexer k cache gather" (k_scale viewed as float32).
+ *   [rocm-cpa]  vLLM PR #12348 "[ROCm] Faster Custom Paged Attention
+ *               kernels": the paged_attention op signature (decode
+ *               attention over a paged, quantised KV cache).
  *
  * The per-group quantiser (cvt_warp_fp16_to_fp4) is named but not shown on
  * the pages; its rule is taken as: amax over the 16 values,
@@ -32,6 +35,7 @@
  */
 #include <math.h>
 #include <stdint.h>
+#include <stdlib.h>
 #include <string.h>
 
 #define KVQO_OK 0
@@ -454,4 +458,134 @@ int kvqo_store_indexer_k(const uint16_t* k, int64_t k_stride0, int32_t dtype,
     memcpy(cache + blk * block_stride + B * D + off * 4, &scale, 4);
   }
   return KVQO_OK;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Paged decode attention over the NVFP4 cache ([rocm-cpa]: vLLM PR #12348  */
+/* "[ROCm] Faster Custom Paged Attention kernels", the paged_attention op   */
+/* signature: out, query, key_cache, value_cache, num_kv_heads, scale,      */
+/* block_tables, context_lens, block_size, k_scale, v_scale).  The page     */
+/* shows the signature only; the computation taken is plain softmax         */
+/* attention of each sequence's one query token over its first              */
+/* context_lens[b] cached tokens, on the cache dequantised exactly:         */
+/*   K^[t, d] = e2m1(q) * float(sf) * k_scale  (V^ with v_scale),           */
+/* sf read where the store put it (K linear unless KVQO_F_SWIZZLE_K_SCALE,  */
+/* V swizzled).  Query head h reads KV head h / (Hq / Hkv).  Everything in  */
+/* double:                                                                  */
+/*   s_t = scale * sum_d q[h, d] * K^[t, d];   m = max_t s_t                */
+/*   p_t = exp(s_t - m) / sum_u exp(s_u - m);  out[h, d] = sum_t p_t V^[t,d] */
+/* context_lens[b] == 0 gives out = 0.  mag[h, d] = sum_t p_t |V^[t, d]|    */
+/* is returned beside out (the scale of the rounding error of any          */
+/* finite-precision evaluation).  query: bf16 / fp16 bits [num_seqs, Hq, D] */
+/* with row stride q_stride0 elements; out, mag: double [num_seqs, Hq, D].  */
+/* ------------------------------------------------------------------------ */
+
+/* One token's dequantised row (head h, page blk, offset off) of one side. */
+static void nvfp4_row_exact(const uint8_t* side_base, int64_t page_stride,
+                            int64_t blk, int64_t off, int64_t h, int64_t H,
+                            int64_t B, int64_t D, int32_t layout,
+                            int swizzle, double side_scale, double* row) {
+  const int64_t data_dim = D / 2, S = D / 16;
+  int64_t dhs, dts, shs, sts;
+  if (layout == KVQO_LAYOUT_HND) {
+    dhs = B * data_dim; dts = data_dim;
+    shs = B * S;        sts = S;
+  } else {
+    dhs = data_dim;     dts = H * data_dim;
+    shs = S;            sts = H * S;
+  }
+  const uint8_t* page = side_base + blk * page_stride;
+  const uint8_t* scale_page = page + H * B * data_dim;
+  for (int64_t j = 0; j < S; ++j) {
+    const uint8_t* sptr;
+    if (!swizzle) {
+      sptr = scale_page + h * shs + off * sts + j;
+    } else {
+      int pos = kvqo_swizzle((int)off, (int)j, (int)S);
+      sptr = scale_page + h * shs + (pos / S) * sts + pos % S;
+    }
+    const double sf = kvqo_e4m3_decode(*sptr);
+    const uint8_t* dptr = page + h * dhs + off * dts + 8 * j;
+    for (int k = 0; k < 16; ++k) {
+      const uint8_t byte = dptr[k / 2];
+      const uint8_t nib = (k % 2 == 0) ? (byte & 0xF) : (byte >> 4);
+      row[16 * j + k] = kvqo_e2m1_decode(nib) * sf * side_scale;
+    }
+  }
+}
+
+int kvqo_paged_attention_nvfp4(
+    const uint16_t* query, int64_t q_stride0, int32_t q_dtype,
+    int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+    int32_t head_size, const uint8_t* key_cache, const uint8_t* value_cache,
+    int64_t page_stride, int32_t block_size, int64_t num_blocks,
+    int32_t layout, const int32_t* block_table, int64_t bt_stride,
+    int32_t max_blocks_per_seq, const int32_t* context_lens, float k_scale,
+    float v_scale, float scale, uint32_t flags, double* out, double* mag) {
+  if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 ||
+      head_size <= 0 || block_size <= 0)
+    return KVQO_ERR_ARG;
+  if (num_q_heads % num_kv_heads != 0) return KVQO_ERR_ARG;
+  if (head_size % 64 != 0 || block_size % 4 != 0) return KVQO_ERR_ARG;
+  if (layout != KVQO_LAYOUT_HND && layout != KVQO_LAYOUT_NHD)
+    return KVQO_ERR_ARG;
+  if (q_dtype != KVQO_DTYPE_BF16 && q_dtype != KVQO_DTYPE_F16)
+    return KVQO_ERR_ARG;
+  const int64_t Hq = num_q_heads, Hkv = num_kv_heads, D = head_size;
+  const int64_t B = block_size, G = Hq / Hkv;
+  const int k_swizzle = (flags & KVQO_F_SWIZZLE_K_SCALE) != 0;
+  double* krow = malloc(sizeof(double) * D);
+  double* vrow = malloc(sizeof(double) * D);
+  if (!krow || !vrow) { free(krow); free(vrow); return KVQO_ERR_ARG; }
+  int rc = KVQO_OK;
+
+  for (int32_t b = 0; b < num_seqs && rc == KVQO_OK; ++b) {
+    const int64_t L = context_lens[b];
+    if (L < 0 || (L + B - 1) / B > max_blocks_per_seq) {
+      rc = KVQO_ERR_BOUNDS;
+      break;
+    }
+    double* s = malloc(sizeof(double) * (L > 0 ? L : 1));
+    if (!s) { rc = KVQO_ERR_ARG; break; }
+    for (int64_t h = 0; h < Hq && rc == KVQO_OK; ++h) {
+      const int64_t kh = h / G;
+      const uint16_t* q = query + b * q_stride0 + h * D;
+      double* o = out + (b * Hq + h) * D;
+      double* mg = mag + (b * Hq + h) * D;
+      for (int64_t d = 0; d < D; ++d) { o[d] = 0.0; mg[d] = 0.0; }
+      if (L == 0) continue;
+      /* logits */
+      for (int64_t t = 0; t < L; ++t) {
+        const int64_t blk = block_table[b * bt_stride + t / B];
+        if (blk < 0 || blk >= num_blocks) { rc = KVQO_ERR_BOUNDS; break; }
+        nvfp4_row_exact(key_cache, page_stride, blk, t % B, kh, Hkv, B, D,
+                        layout, k_swizzle, (double)k_scale, krow);
+        double dot = 0.0;
+        for (int64_t d = 0; d < D; ++d)
+          dot += (double)element_to_float(q[d], q_dtype) * krow[d];
+        s[t] = (double)scale * dot;
+      }
+      if (rc != KVQO_OK) break;
+      /* softmax */
+      double m = s[0];
+      for (int64_t t = 1; t < L; ++t) if (s[t] > m) m = s[t];
+      double l = 0.0;
+      for (int64_t t = 0; t < L; ++t) l += exp(s[t] - m);
+      /* weighted sum of values */
+      for (int64_t t = 0; t < L; ++t) {
+        const int64_t blk = block_table[b * bt_stride + t / B];
+        nvfp4_row_exact(value_cache, page_stride, blk, t % B, kh, Hkv, B, D,
+                        layout, 1, (double)v_scale, vrow);
+        const double p = exp(s[t] - m) / l;
+        for (int64_t d = 0; d < D; ++d) {
+          o[d] += p * vrow[d];
+          mg[d] += p * fabs(vrow[d]);
+        }
+      }
+    }
+    free(s);
+  }
+  free(krow);
+  free(vrow);
+  return rc;
 }

@@ -490,3 +490,123 @@ def make_indexer_store(name: str, seed: int, seq_lens, block_size: int,
         num_tokens=T, head_dim=D, block_size=B, num_blocks=num_blocks,
         slot_mapping=slots.astype(np.int64), block_table=bt, cu_seq_lens=cu,
         dtype=dtype)
+
+
+@dataclass
+class AttentionWorkload:
+    """Inputs of one paged decode-attention step over an NVFP4 cache: one
+    query token per sequence (bf16/fp16 bits [n, Hq, D]), the cache pages
+    (``num_blocks`` pages of ``page_stride`` bytes, K side at byte 0 of a
+    page, V side at ``side_bytes``, HND unless ``layout``), the block table
+    and the context lengths."""
+    name: str
+    query: np.ndarray
+    num_kv_heads: int
+    block_size: int
+    num_blocks: int
+    cache: np.ndarray
+    block_table: np.ndarray
+    context_lens: np.ndarray
+    k_scale: np.float32
+    v_scale: np.float32
+    scale: np.float32
+    layout: int = LAYOUT_HND
+    flags: int = 0
+    dtype: int = DTYPE_BF16
+
+    @property
+    def num_seqs(self) -> int:
+        return self.query.shape[0]
+
+    @property
+    def num_q_heads(self) -> int:
+        return self.query.shape[1]
+
+    @property
+    def head_size(self) -> int:
+        return self.query.shape[2]
+
+    @property
+    def side_bytes(self) -> int:
+        D = self.head_size
+        return self.num_kv_heads * self.block_size * (D // 2 + D // 16)
+
+    @property
+    def page_stride(self) -> int:
+        return 2 * self.side_bytes
+
+    def algorithmic_bytes(self) -> int:
+        """Every context token's NVFP4 K and V (data + scales) of every KV
+        head read once, the queries read and the outputs written (2 bytes
+        per element), block-table entries and context lengths read."""
+        D, Hkv, B = self.head_size, self.num_kv_heads, self.block_size
+        lens = self.context_lens.astype(np.int64)
+        kv = int(lens.sum()) * Hkv * 2 * (D // 2 + D // 16)
+        qo = 2 * self.query.size * 2
+        meta = 4 * int(((lens + B - 1) // B).sum()) + 4 * lens.size
+        return kv + qo + meta
+
+
+def random_nvfp4_cache(rng, num_blocks: int, page_stride: int,
+                       num_kv_heads: int, block_size: int, head_size: int,
+                       sf_lo: int = 0x60, sf_hi: int = 0x7E) -> np.ndarray:
+    """NVFP4 pages with uniform random data bytes (every e2m1 code) and
+    scale bytes uniform over the e4m3 codes [sf_lo, sf_hi] (positive,
+    never NaN) -- the range a per-tensor scale of amax/(448*6) gives
+    N(0, 1) groups.  Bytes beyond 2*H*B*(D/2+S) per page are zero."""
+    H, B, D = num_kv_heads, block_size, head_size
+    data = H * B * D // 2
+    side = data + H * B * D // 16
+    cache = np.zeros((num_blocks, page_stride), dtype=np.uint8)
+    for s in range(2):
+        base = s * side
+        cache[:, base:base + data] = rng.integers(
+            0, 256, size=(num_blocks, data), dtype=np.uint8)
+        cache[:, base + data:base + side] = rng.integers(
+            sf_lo, sf_hi + 1, size=(num_blocks, side - data), dtype=np.uint8)
+    return cache.reshape(-1)
+
+
+def make_attention(name: str, seed: int, context_lens, num_q_heads: int,
+                   num_kv_heads: int, head_size: int, block_size: int,
+                   num_blocks: int = 0, dtype: int = DTYPE_BF16,
+                   k_scale: float = 1.0 / 600.0, v_scale: float = 1.0 / 600.0,
+                   scale: float | None = None, layout: int = LAYOUT_HND,
+                   flags: int = 0, query_mult: float = 1.0,
+                   extra_blocks: int = 0) -> AttentionWorkload:
+    """Queries N(0, 1) x ``query_mult``; each sequence's pages are distinct
+    random blocks of the cache (block table rows padded with further random
+    blocks up to the longest sequence); cache bytes from
+    ``random_nvfp4_cache``; softmax scale 1/sqrt(head_size) unless given."""
+    rng = np.random.default_rng(seed)
+    lens = np.asarray(context_lens, dtype=np.int64)
+    n, B = lens.size, block_size
+    mb = max(int(((lens + B - 1) // B).max()) if n else 1, 1)
+    nb = num_blocks or n * mb + extra_blocks
+    assert n * mb <= nb
+    bt = rng.permutation(nb)[: n * mb].reshape(n, mb).astype(np.int32)
+    D = head_size
+    page_stride = 2 * num_kv_heads * B * (D // 2 + D // 16)
+    cache = random_nvfp4_cache(rng, nb, page_stride, num_kv_heads, B, D)
+    q = rng.standard_normal((n, num_q_heads, D)).astype(np.float32)
+    q *= np.float32(query_mult)
+    if scale is None:
+        scale = 1.0 / np.sqrt(D)
+    return AttentionWorkload(
+        name=name, query=element_bits(q.reshape(-1), dtype).reshape(q.shape),
+        num_kv_heads=num_kv_heads, block_size=B, num_blocks=nb, cache=cache,
+        block_table=bt, context_lens=lens.astype(np.int32),
+        k_scale=np.float32(k_scale), v_scale=np.float32(v_scale),
+        scale=np.float32(scale), layout=layout, flags=flags, dtype=dtype)
+
+
+def attention_workload(seed: int = 5, num_seqs: int = 200) -> AttentionWorkload:
+    """``llama70b_decode`` -- one decode step of Llama-3.1-70B-shaped
+    attention (64 query heads, 8 KV heads, head_size 128) over an NVFP4
+    cache with block_size 16: ``num_seqs`` sequences (the 200-prompt
+    serving runs) whose contexts are a 512-token prompt plus U[0, 2048]
+    generated tokens."""
+    rng = np.random.default_rng(seed)
+    lens = 512 + rng.integers(0, 2049, size=num_seqs)
+    return make_attention("llama70b_decode", seed, lens, num_q_heads=64,
+                          num_kv_heads=8, head_size=128, block_size=16)

@@ -7,12 +7,14 @@ import pytest
 
 import oracle
 from tests import test_oracle_formats as F
+from tests import test_oracle_attention as A
 from tests import test_oracle_gather as G
 from tests import test_oracle_indexer_store as I
 from tests import test_oracle_load as L
 from tests import test_oracle_store as S
 
-ALL_CHECKS = F.CHECKS + S.CHECKS + G.CHECKS + L.CHECKS + I.CHECKS
+ALL_CHECKS = (F.CHECKS + S.CHECKS + G.CHECKS + L.CHECKS + I.CHECKS
+              + A.CHECKS)
 
 # (id, original text, planted mistake[, occurrence]) -- the mistake is
 # planted at the given occurrence of the original (default: the only one)
@@ -76,13 +78,16 @@ MUTANTS = [
      "v = ldexp((double)m, -23);"),
     ("load_unswizzle_transposed",
      "sptr = scale_page + h * shs + (pos / S) * sts + pos % S;",
-     "sptr = scale_page + h * shs + (pos % S) * sts + pos / S;"),
+     "sptr = scale_page + h * shs + (pos % S) * sts + pos / S;", 0),
     ("load_k_uses_v_scale",
      "const float side_scale[2] = {k_scale, v_scale};",
      "const float side_scale[2] = {v_scale, v_scale};"),
     ("load_nibble_order",
      "(k % 2 == 0) ? (byte & 0xF) : (byte >> 4)",
-     "(k % 2 == 0) ? (byte >> 4) : (byte & 0xF)"),
+     "(k % 2 == 0) ? (byte >> 4) : (byte & 0xF)", 0),
+    ("attn_nibble_order",
+     "(k % 2 == 0) ? (byte & 0xF) : (byte >> 4)",
+     "(k % 2 == 0) ? (byte >> 4) : (byte & 0xF)", 1),
     ("bf16_cast_truncates",
      "return (uint16_t)((u + 0x7FFFu + lsb) >> 16);",
      "return (uint16_t)(u >> 16);"),
@@ -104,6 +109,41 @@ MUTANTS = [
      "uint8_t* dst = cache + blk * block_stride + (off ^ 1) * D;"),
     ("gather_row_bytes", "k_fp8[row * D + d] = block[off * D + d];",
      "k_fp8[row * D + d] = block[off * D + (d ^ 1)];"),
+    ("attn_kv_head_modulo", "const int64_t kh = h / G;",
+     "const int64_t kh = h % Hkv;"),
+    ("attn_sum_drops_last_token",
+     "for (int64_t t = 0; t < L; ++t) l += exp(s[t] - m);",
+     "for (int64_t t = 0; t < L - 1; ++t) l += exp(s[t] - m);"),
+    ("attn_values_drop_last_token",
+     "for (int64_t t = 0; t < L; ++t) {\n        const int64_t blk = "
+     "block_table[b * bt_stride + t / B];\n        nvfp4_row_exact(value",
+     "for (int64_t t = 0; t < L - 1; ++t) {\n        const int64_t blk = "
+     "block_table[b * bt_stride + t / B];\n        nvfp4_row_exact(value"),
+    ("attn_no_max_shift",
+     "double m = s[0];\n      for (int64_t t = 1; t < L; ++t) "
+     "if (s[t] > m) m = s[t];",
+     "double m = 0.0;"),
+    ("attn_drops_k_scale", "layout, k_swizzle, (double)k_scale, krow);",
+     "layout, k_swizzle, 1.0, krow);"),
+    ("attn_k_scales_always_swizzled",
+     "layout, k_swizzle, (double)k_scale, krow);",
+     "layout, 1, (double)k_scale, krow);"),
+    ("attn_v_scales_linear", "layout, 1, (double)v_scale, vrow);",
+     "layout, 0, (double)v_scale, vrow);"),
+    ("attn_scale_squared", "s[t] = (double)scale * dot;",
+     "s[t] = (double)scale * (double)scale * dot;"),
+    ("attn_mag_signed", "mg[d] += p * fabs(vrow[d]);",
+     "mg[d] += p * vrow[d];"),
+    ("attn_token_offset",
+     "nvfp4_row_exact(key_cache, page_stride, blk, t % B,",
+     "nvfp4_row_exact(key_cache, page_stride, blk, (t + 1) % B,"),
+    ("attn_query_head", "const uint16_t* q = query + b * q_stride0 + h * D;",
+     "const uint16_t* q = query + b * q_stride0 + kh * D;"),
+    ("attn_nhd_as_hnd", "dhs = data_dim;     dts = H * data_dim;",
+     "dhs = B * data_dim; dts = data_dim;", 2),
+    ("attn_unswizzle_transposed",
+     "sptr = scale_page + h * shs + (pos / S) * sts + pos % S;",
+     "sptr = scale_page + h * shs + (pos % S) * sts + pos / S;", 1),
 ]
 
 
