@@ -17,6 +17,10 @@
  *                         gather_indexer_k_quant_cache kernel"; PR #26456
  *                         "[Deepseek-V3.2][Kernel] Integrate cuda indexer k
  *                         cache gather").
+ *   kvq_paged_attention_nvfp4  decode attention (one query token per
+ *                         sequence) over the NVFP4 pages (vLLM PR #12348
+ *                         "[ROCm] Faster Custom Paged Attention kernels":
+ *                         the paged_attention op).
  *
  * Conventions shared by every entry point:
  *   - Every buffer pointer is DEVICE memory owned by the caller, on the
@@ -68,7 +72,7 @@ enum {
      default K scales are linear and only V scales are swizzled, as the
      page's kernel does). */
   KVQ_F_SWIZZLE_K_SCALE = 1u << 0,
-  /* Both calls: launch with programmatic dependent launch.  The kernel may
+  /* Every call: launch with programmatic dependent launch.  The kernel may
      become resident while the previous kernel on the stream is finishing;
      it waits (griddepcontrol.wait, in hardware) for that kernel to complete
      and its writes to be visible before it touches any memory, so the
@@ -271,6 +275,68 @@ kvq_status kvq_store_indexer_k(const void* k, int64_t k_stride0,
                                int64_t num_blocks,
                                const int64_t* slot_mapping, uint32_t flags,
                                int32_t* dev_error, void* stream);
+
+/*
+ * kvq_paged_attention_nvfp4 -- paged decode attention over the NVFP4 cache
+ * that kvq_store_nvfp4 writes.  (vLLM PR #12348 "[ROCm] Faster Custom Paged
+ * Attention kernels": paged_attention(out, exp_sums, max_logits, tmp_out,
+ * query, key_cache, value_cache, num_kv_heads, scale, block_tables,
+ * context_lens, block_size, max_context_len, alibi_slopes, kv_cache_dtype,
+ * k_scale, v_scale, partition_size).  The page shows the signature only;
+ * the computation is plain softmax attention on the dequantised cache.)
+ *
+ * For sequence b (one query token) with L = context_lens[b] and query head
+ * h, reading KV head h / (num_q_heads / num_kv_heads):
+ *   K^[t, d] = e2m1(q) * float(sf) * k_scale[0]   (V^ with v_scale[0]; sf at
+ *              its stored position: K linear unless KVQ_F_SWIZZLE_K_SCALE,
+ *              V swizzled), token t of page block_table[b*stride + t/B],
+ *              offset t % B, for t < L;
+ *   s_t = scale * sum_d q[b, h, d] K^[t, d];  out[b, h, :] =
+ *   sum_t softmax(s)_t V^[t, :];  L == 0 gives zeros.
+ * Arithmetic (the tolerance of any comparison follows from it): the query
+ * is rounded to fp16, e2m1 * sf is exact in fp16, q . (e2m1 * sf) and
+ * P . V' accumulate in fp32 on the tensor cores, P = exp2 of the scaled
+ * logits minus the partition max is rounded to fp16 and the denominator
+ * sums the rounded values; partitions merge in fp32; out is rounded once.
+ *
+ * query          bf16 / fp16 (dtype) [num_seqs, num_q_heads, 128], rows
+ *                query_stride0 elements apart (multiple of 8), 16-byte
+ *                aligned; |q| < 65504 (fp16 range).
+ * head_size      128.   num_q_heads / num_kv_heads <= 16 (and divides).
+ * key_cache, value_cache, page_stride, block_size, num_blocks, layout
+ *                as for kvq_store_nvfp4 (num_kv_heads heads per page).
+ * block_table    int32, rows block_table_stride apart, first
+ *                max_blocks_per_seq entries used.
+ * context_lens   int32 [num_seqs]; values above min(max_context_len,
+ *                max_blocks_per_seq * block_size) are clamped to it and
+ *                flagged (KVQ_DEVERR_SEQ).
+ * k_scale, v_scale  device fp32 scalars (the store's).
+ * scale          softmax scale, finite.
+ * partition_size 128, 256, 384 or 512 tokens.
+ * exp_sums, max_logits  fp32 [num_seqs, num_q_heads, max_parts] scratch,
+ * tmp_out        fp32 [num_seqs, num_q_heads, max_parts, 128] scratch, with
+ *                max_parts = ceil(max_context_len / partition_size); needed
+ *                (non-NULL) only when max_parts > 1.  Nothing in them has to
+ *                be initialised; their contents afterwards are unspecified.
+ * out            dtype [num_seqs, num_q_heads, 128], rows out_stride0
+ *                elements apart (multiple of 8), 16-byte aligned.
+ * flags          KVQ_F_SWIZZLE_K_SCALE, KVQ_F_PDL, or 0.
+ * dev_error      nullable (KVQ_DEVERR_BLOCK: the token is left out;
+ *                KVQ_DEVERR_SEQ; KVQ_DEVERR_TIMEOUT: nothing of that
+ *                (sequence, KV head, partition) is written).
+ * num_seqs == 0 returns KVQ_OK without launching.
+ */
+kvq_status kvq_paged_attention_nvfp4(
+    const void* query, int64_t query_stride0, int32_t dtype, int32_t num_seqs,
+    int32_t num_q_heads, int32_t num_kv_heads, int32_t head_size,
+    const uint8_t* key_cache, const uint8_t* value_cache, int64_t page_stride,
+    int32_t block_size, int64_t num_blocks, int32_t layout,
+    const int32_t* block_table, int64_t block_table_stride,
+    int32_t max_blocks_per_seq, const int32_t* context_lens,
+    int32_t max_context_len, const float* k_scale, const float* v_scale,
+    float scale, int32_t partition_size, float* exp_sums, float* max_logits,
+    float* tmp_out, void* out, int64_t out_stride0, uint32_t flags,
+    int32_t* dev_error, void* stream);
 
 /* Static text for a status code. */
 const char* kvq_status_string(kvq_status status);

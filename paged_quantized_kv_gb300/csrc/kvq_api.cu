@@ -3,7 +3,10 @@
 // vLLM reshape_and_cache_nvfp4_dispatch (nvfp4_kv_cache_kernels.cu, commit
 // 7ce4c8e), and the launch on the caller's stream.
 #include <cuda_runtime.h>
+#include <math.h>
 #include <stdint.h>
+
+#include <algorithm>
 
 #include "kvq.h"
 #include "kvq_internal.h"
@@ -336,6 +339,115 @@ kvq_status kvq_store_indexer_k(const void* k, int64_t k_stride0,
   p.vec32 = aligned(k, 32) && k_stride0 % 16 == 0;
   const cudaError_t err =
       launch_store_indexer_k(p, static_cast<cudaStream_t>(stream));
+  return err == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
+}
+
+kvq_status kvq_paged_attention_nvfp4(
+    const void* query, int64_t query_stride0, int32_t dtype, int32_t num_seqs,
+    int32_t num_q_heads, int32_t num_kv_heads, int32_t head_size,
+    const uint8_t* key_cache, const uint8_t* value_cache, int64_t page_stride,
+    int32_t block_size, int64_t num_blocks, int32_t layout,
+    const int32_t* block_table, int64_t block_table_stride,
+    int32_t max_blocks_per_seq, const int32_t* context_lens,
+    int32_t max_context_len, const float* k_scale, const float* v_scale,
+    float scale, int32_t partition_size, float* exp_sums, float* max_logits,
+    float* tmp_out, void* out, int64_t out_stride0, uint32_t flags,
+    int32_t* dev_error, void* stream) {
+  using namespace kvq;
+  if (dtype != KVQ_DTYPE_BF16 && dtype != KVQ_DTYPE_FP16) return KVQ_ERR_DTYPE;
+  if (layout != KVQ_LAYOUT_HND && layout != KVQ_LAYOUT_NHD)
+    return KVQ_ERR_LAYOUT;
+  if ((flags & ~static_cast<uint32_t>(KVQ_F_SWIZZLE_K_SCALE | KVQ_F_PDL)) !=
+      0u)
+    return KVQ_ERR_ARG;
+  if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 ||
+      head_size <= 0 || block_size <= 0 || num_blocks < 0 ||
+      max_blocks_per_seq < 0 || block_table_stride < max_blocks_per_seq ||
+      max_context_len < 0)
+    return KVQ_ERR_SHAPE;
+  if (head_size != 128 || block_size % 4 != 0) return KVQ_ERR_SHAPE;
+  if (num_q_heads % num_kv_heads != 0 || num_q_heads / num_kv_heads > 16)
+    return KVQ_ERR_SHAPE;
+  if (partition_size <= 0 || partition_size % 128 != 0 ||
+      partition_size > 512)
+    return KVQ_ERR_SHAPE;
+  if (!(scale == scale) || scale == INFINITY || scale == -INFINITY)
+    return KVQ_ERR_ARG;
+  const int64_t H = num_kv_heads, D = head_size, B = block_size;
+  const int64_t S = D / 16;
+  if (page_stride < H * B * (D / 2 + S)) return KVQ_ERR_SHAPE;
+  if (query_stride0 < num_q_heads * D || out_stride0 < num_q_heads * D)
+    return KVQ_ERR_SHAPE;
+  const int64_t max_parts =
+      (static_cast<int64_t>(max_context_len) + partition_size - 1) /
+      partition_size;
+  if (num_seqs > 65535 || num_kv_heads > 65535 || max_parts > (1 << 20))
+    return KVQ_ERR_SHAPE;
+  if (num_seqs == 0) return KVQ_OK;
+  if (query == nullptr || key_cache == nullptr || value_cache == nullptr ||
+      block_table == nullptr || context_lens == nullptr ||
+      k_scale == nullptr || v_scale == nullptr || out == nullptr)
+    return KVQ_ERR_NULL;
+  if (max_parts > 1 &&
+      (exp_sums == nullptr || max_logits == nullptr || tmp_out == nullptr))
+    return KVQ_ERR_NULL;
+  if (!aligned(query, 16) || query_stride0 % 8 != 0 || !aligned(out, 16) ||
+      out_stride0 % 8 != 0 || !aligned(key_cache, 16) ||
+      !aligned(value_cache, 16) || page_stride % 16 != 0 ||
+      !aligned(block_table, 4) || !aligned(context_lens, 4) ||
+      !aligned(k_scale, 4) || !aligned(v_scale, 4))
+    return KVQ_ERR_ALIGN;
+  if (max_parts > 1 && (!aligned(exp_sums, 4) || !aligned(max_logits, 4) ||
+                        !aligned(tmp_out, 16)))
+    return KVQ_ERR_ALIGN;
+
+  AttnParams p{};
+  p.q = static_cast<const uint16_t*>(query);
+  p.q_stride0 = query_stride0;
+  p.side[0] = key_cache;
+  p.side[1] = value_cache;
+  p.page_stride = page_stride;
+  p.num_blocks = num_blocks;
+  p.scale_off = H * B * (D / 2);
+  if (layout == KVQ_LAYOUT_HND) {
+    p.dhs = B * (D / 2);
+    p.dts = D / 2;
+    p.shs = B * S;
+    p.sts = S;
+  } else {
+    p.dhs = D / 2;
+    p.dts = H * (D / 2);
+    p.shs = S;
+    p.sts = H * S;
+  }
+  p.block_table = block_table;
+  p.bt_stride = block_table_stride;
+  p.lens = context_lens;
+  p.k_scale = k_scale;
+  p.v_scale = v_scale;
+  p.scale = scale;
+  p.exp_sums = exp_sums;
+  p.max_logits = max_logits;
+  p.tmp_out = tmp_out;
+  p.out = static_cast<uint16_t*>(out);
+  p.out_stride0 = out_stride0;
+  p.dev_error = dev_error;
+  p.num_seqs = num_seqs;
+  p.Hq = num_q_heads;
+  p.Hkv = num_kv_heads;
+  p.G = num_q_heads / num_kv_heads;
+  p.B = block_size;
+  p.b_shift = ilog2_exact(B);
+  p.part = partition_size;
+  p.max_parts = static_cast<int32_t>(max_parts > 0 ? max_parts : 1);
+  const int64_t cap = std::min<int64_t>(
+      max_context_len, static_cast<int64_t>(max_blocks_per_seq) * B);
+  p.len_cap = static_cast<int32_t>(std::min<int64_t>(cap, INT32_MAX));
+  p.swizzle_k = (flags & KVQ_F_SWIZZLE_K_SCALE) != 0u;
+  p.f16 = dtype == KVQ_DTYPE_FP16;
+  p.pdl = (flags & KVQ_F_PDL) != 0u;
+  const cudaError_t err =
+      launch_paged_attention_nvfp4(p, static_cast<cudaStream_t>(stream));
   return err == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
 }
 

@@ -108,17 +108,52 @@ struct IndexerStoreParams {
 cudaError_t launch_store_indexer_k(const IndexerStoreParams& p,
                                    cudaStream_t stream);
 
+// ---------------------------------------------------------------------------
+// Paged decode attention over the NVFP4 cache
+// ---------------------------------------------------------------------------
+struct AttnParams {
+  const uint16_t* q;       // [num_seqs, Hq, D] bf16/fp16 bits
+  int64_t q_stride0;       // elements
+  const uint8_t* side[2];  // page 0 of the K side / V side
+  int64_t page_stride;
+  int64_t num_blocks;
+  int64_t scale_off;       // H * B * D/2: offset of a side's scale region
+  int64_t dhs, dts, shs, sts;
+  const int32_t* block_table;
+  int64_t bt_stride;
+  const int32_t* lens;     // context_lens [num_seqs]
+  const float* k_scale;    // device scalars
+  const float* v_scale;
+  float scale;             // softmax scale
+  float* exp_sums;         // [num_seqs, Hq, max_parts]  (max_parts > 1)
+  float* max_logits;       // [num_seqs, Hq, max_parts]
+  float* tmp_out;          // [num_seqs, Hq, max_parts, D]
+  uint16_t* out;           // [num_seqs, Hq, D], rows out_stride0 apart
+  int64_t out_stride0;
+  int32_t* dev_error;      // nullable
+  int32_t num_seqs, Hq, Hkv, G, B, b_shift;
+  int32_t part;            // partition size (multiple of 128, <= 512)
+  int32_t max_parts;       // partitions of the longest allowed context
+  int32_t len_cap;         // min(max_context_len, max_blocks * B)
+  bool swizzle_k;          // K scales stored swizzled too
+  bool f16;                // query / out are fp16 (else bf16)
+  bool pdl;
+};
+
+cudaError_t launch_paged_attention_nvfp4(const AttnParams& p,
+                                         cudaStream_t stream);
+
 // Streaming-multiprocessor count of the current device (cached per device).
 int sm_count();
 
 // Launch `kernel<<<grid, block, smem, stream>>>(params)`, with programmatic
 // dependent launch when `pdl` is set.
 template <typename Params>
-cudaError_t launch_kernel(void (*kernel)(Params), unsigned grid,
+cudaError_t launch_kernel(void (*kernel)(Params), dim3 grid,
                           unsigned block, size_t smem, cudaStream_t stream,
                           bool pdl, const Params& params) {
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(grid);
+  cfg.gridDim = grid;
   cfg.blockDim = dim3(block);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;

@@ -96,6 +96,12 @@ def lib() -> ctypes.CDLL:
             P, c.c_int64, c.c_int32, c.c_int32, c.c_int32, P, c.c_int64,
             c.c_int32, c.c_int64, P, c.c_uint32, P, P]
         L.kvq_store_indexer_k.restype = c.c_int
+        L.kvq_paged_attention_nvfp4.argtypes = [
+            P, c.c_int64, c.c_int32, c.c_int32, c.c_int32, c.c_int32,
+            c.c_int32, P, P, c.c_int64, c.c_int32, c.c_int64, c.c_int32, P,
+            c.c_int64, c.c_int32, P, c.c_int32, P, P, c.c_float, c.c_int32,
+            P, P, P, P, c.c_int64, c.c_uint32, P, P]
+        L.kvq_paged_attention_nvfp4.restype = c.c_int
         L.kvq_status_string.argtypes = [c.c_int]
         L.kvq_status_string.restype = c.c_char_p
         L.kvq_version.argtypes = []
@@ -258,6 +264,72 @@ def kvq_store_indexer_k(k: torch.Tensor, kv_cache: torch.Tensor,
         kv_cache.size(0), slot_mapping.data_ptr(), int(flags),
         _ptr(dev_error), _stream_of(k) if stream is None else stream)
     _check("kvq_store_indexer_k", st)
+
+
+def attention_scratch(num_seqs: int, num_q_heads: int, max_context_len: int,
+                      partition_size: int = 512, head_size: int = 128,
+                      device="cuda"):
+    """(exp_sums, max_logits, tmp_out) fp32 scratch for
+    kvq_paged_attention_nvfp4, or (None, None, None) when every context fits
+    one partition."""
+    parts = -(-int(max_context_len) // int(partition_size))
+    if parts <= 1:
+        return None, None, None
+    shape = (num_seqs, num_q_heads, parts)
+    return (torch.empty(shape, dtype=torch.float32, device=device),
+            torch.empty(shape, dtype=torch.float32, device=device),
+            torch.empty(shape + (head_size,), dtype=torch.float32,
+                        device=device))
+
+
+def kvq_paged_attention_nvfp4(query: torch.Tensor, key_cache: torch.Tensor,
+                              value_cache: torch.Tensor,
+                              block_table: torch.Tensor,
+                              context_lens: torch.Tensor,
+                              k_scale: torch.Tensor, v_scale: torch.Tensor,
+                              scale: float, out: torch.Tensor,
+                              max_context_len: int,
+                              partition_size: int = 512,
+                              exp_sums: torch.Tensor | None = None,
+                              max_logits: torch.Tensor | None = None,
+                              tmp_out: torch.Tensor | None = None,
+                              flags: int = 0,
+                              dev_error: torch.Tensor | None = None,
+                              stream: int | None = None) -> None:
+    """Paged decode attention over the NVFP4 cache (see ``include/kvq.h``).
+
+    query / out: bf16 or fp16 [num_seqs, Hq, 128] (last two dims
+    contiguous); key_cache / value_cache: the store's 4-D page views;
+    block_table int32 [num_seqs, max_blocks]; context_lens int32
+    [num_seqs].  The fp32 scratch (``attention_scratch``) is allocated here
+    when it is needed and not given."""
+    dtypes = {torch.bfloat16: KVQ_DTYPE_BF16, torch.float16: KVQ_DTYPE_FP16}
+    if query.dtype not in dtypes or out.dtype != query.dtype:
+        raise KvqError("kvq_paged_attention_nvfp4", KVQ_ERR_DTYPE)
+    n, Hq, D = query.shape
+    if (query.stride(2) != 1 or query.stride(1) != D or out.stride(2) != 1
+            or out.stride(1) != D or tuple(out.shape) != (n, Hq, D)):
+        raise KvqError("kvq_paged_attention_nvfp4", KVQ_ERR_SHAPE)
+    if key_cache.dim() != 4 or key_cache.dtype != torch.uint8:
+        raise KvqError("kvq_paged_attention_nvfp4", KVQ_ERR_SHAPE)
+    if block_table.dtype != torch.int32 or context_lens.dtype != torch.int32:
+        raise KvqError("kvq_paged_attention_nvfp4", KVQ_ERR_DTYPE)
+    layout = (KVQ_LAYOUT_HND if key_cache.stride(2) > key_cache.stride(1)
+              else KVQ_LAYOUT_NHD)
+    if exp_sums is None and max_logits is None and tmp_out is None:
+        exp_sums, max_logits, tmp_out = attention_scratch(
+            n, Hq, max_context_len, partition_size, D, query.device)
+    st = lib().kvq_paged_attention_nvfp4(
+        query.data_ptr(), query.stride(0), dtypes[query.dtype], n, Hq,
+        key_cache.size(2), D, key_cache.data_ptr(), value_cache.data_ptr(),
+        key_cache.stride(0), key_cache.size(1), key_cache.size(0), layout,
+        block_table.data_ptr(), block_table.stride(0), block_table.size(1),
+        context_lens.data_ptr(), int(max_context_len), k_scale.data_ptr(),
+        v_scale.data_ptr(), float(scale), int(partition_size),
+        _ptr(exp_sums), _ptr(max_logits), _ptr(tmp_out), out.data_ptr(),
+        out.stride(0), int(flags), _ptr(dev_error),
+        _stream_of(query) if stream is None else stream)
+    _check("kvq_paged_attention_nvfp4", st)
 
 
 def alloc_nvfp4_cache(num_blocks: int, block_size: int, num_heads: int,

@@ -37,8 +37,8 @@ def header_functions():
 def test_exports_match_header(lib):
     declared = header_functions()
     assert {"kvq_store_nvfp4", "kvq_gather_indexer_k", "kvq_load_nvfp4",
-            "kvq_store_indexer_k", "kvq_status_string",
-            "kvq_version"} <= declared
+            "kvq_store_indexer_k", "kvq_paged_attention_nvfp4",
+            "kvq_status_string", "kvq_version"} <= declared
     out = subprocess.run(["nm", "-D", "--defined-only", kvq.LIB_PATH],
                          capture_output=True, text=True, check=True).stdout
     exported = set(re.findall(r"\sT\s(kvq_\w+)$", out, flags=re.M))
@@ -208,3 +208,46 @@ def istore(lib, **kw):
 ])
 def test_indexer_store_validation(lib, kw, code):
     assert istore(lib, **kw) == code
+
+
+def attn(lib, **kw):
+    args = dict(query=A, query_stride0=8 * 128, dtype=0, num_seqs=2,
+                num_q_heads=8, num_kv_heads=1, head_size=128, key_cache=A,
+                value_cache=A, page_stride=2 * 16 * 72, block_size=16,
+                num_blocks=8, layout=0, block_table=A, block_table_stride=4,
+                max_blocks_per_seq=4, context_lens=A, max_context_len=600,
+                k_scale=A, v_scale=A, scale=0.088, partition_size=512,
+                exp_sums=A, max_logits=A, tmp_out=A, out=A,
+                out_stride0=8 * 128, flags=0, dev_error=None, stream=None)
+    args.update(kw)
+    return lib.kvq_paged_attention_nvfp4(*args.values())
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(dtype=2), kvq.KVQ_ERR_DTYPE),
+    (dict(layout=2), kvq.KVQ_ERR_LAYOUT),
+    (dict(flags=4), kvq.KVQ_ERR_ARG),
+    (dict(scale=float("nan")), kvq.KVQ_ERR_ARG),
+    (dict(scale=float("inf")), kvq.KVQ_ERR_ARG),
+    (dict(head_size=64), kvq.KVQ_ERR_SHAPE),
+    (dict(num_q_heads=6, num_kv_heads=4), kvq.KVQ_ERR_SHAPE),
+    (dict(num_q_heads=17 * 2, num_kv_heads=2, query_stride0=34 * 128,
+          out_stride0=34 * 128), kvq.KVQ_ERR_SHAPE),
+    (dict(block_size=6), kvq.KVQ_ERR_SHAPE),
+    (dict(partition_size=192), kvq.KVQ_ERR_SHAPE),
+    (dict(partition_size=640), kvq.KVQ_ERR_SHAPE),
+    (dict(page_stride=64), kvq.KVQ_ERR_SHAPE),
+    (dict(query_stride0=4 * 128), kvq.KVQ_ERR_SHAPE),
+    (dict(block_table_stride=2), kvq.KVQ_ERR_SHAPE),
+    (dict(max_context_len=-1), kvq.KVQ_ERR_SHAPE),
+    (dict(num_seqs=70000), kvq.KVQ_ERR_SHAPE),
+    (dict(query=None), kvq.KVQ_ERR_NULL),
+    (dict(tmp_out=None), kvq.KVQ_ERR_NULL),
+    (dict(out=A + 8), kvq.KVQ_ERR_ALIGN),
+    (dict(out_stride0=8 * 128 + 4), kvq.KVQ_ERR_ALIGN),
+    (dict(key_cache=A + 4), kvq.KVQ_ERR_ALIGN),
+    (dict(tmp_out=A + 4), kvq.KVQ_ERR_ALIGN),
+    (dict(num_seqs=0, query=None, out=None), kvq.KVQ_OK),
+])
+def test_attention_validation(lib, kw, code):
+    assert attn(lib, **kw) == code
