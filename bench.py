@@ -55,7 +55,7 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--clock-window-s", type=float, default=1.5)
     ap.add_argument("--kernel-only",
-                    choices=["store", "gather", "load", "istore"],
+                    choices=["store", "gather", "load", "istore", "attn"],
                     help="launch only this kernel (each launch after an L2 "
                          "flush) and print its mean time; used for ncu")
     return ap.parse_args()
@@ -337,6 +337,16 @@ def run_ours(args):
         stream=sh), K)
     istore_bytes = iw.algorithmic_bytes()
     del ik, icache
+    # decode attention over NVFP4 pages: one step of Llama-3.1-70B-shaped
+    # attention (200 sequences, 64 query / 8 KV heads, contexts 512..2560;
+    # 359 MB of pages per call, larger than L2)
+    aw = wlmod.attention_workload(rank_seed(5, rank))
+    attn = attention_inputs(aw, kvq, dev)
+    attn_ms = span_ms(lambda i: run_attention(attn, kvq, PDL, dev_err, sh),
+                      K)
+    attn_bytes = aw.algorithmic_bytes()
+    attn_ctx = int(aw.context_lens.astype(np.int64).sum())
+    del attn
     # keep the same steps running so the clock sampler sees the load
     t1 = time.perf_counter()
     j = 0
@@ -437,6 +447,18 @@ def run_ours(args):
             "frac_of_peak": round(istore_bytes / istore_ms / 1e6 / peak, 4),
             "tokens_per_s": round(iw.num_tokens / (istore_ms / 1e3), 1),
             "algorithmic_bytes": istore_bytes},
+        "paged_attention_nvfp4": {
+            "note": "decode attention over the NVFP4 pages, one step of "
+                    "Llama-3.1-70B-shaped attention: 200 sequences, 64 "
+                    "query / 8 KV heads, head_size 128, block_size 16, "
+                    "contexts 512 + U[0, 2048]; partition 512 (main kernel "
+                    "+ partition merge per call); not part of the step",
+            "ms": round(attn_ms, 5),
+            "GB_s": round(attn_bytes / attn_ms / 1e6, 1),
+            "frac_of_peak": round(attn_bytes / attn_ms / 1e6 / peak, 4),
+            "decode_tokens_per_s": round(aw.num_seqs / (attn_ms / 1e3), 1),
+            "context_tokens_per_s": round(attn_ctx / (attn_ms / 1e3), 1),
+            "algorithmic_bytes": attn_bytes},
         "single_launch_after_l2_write_flush": {
             "note": "each kernel alone after writing a 256 MiB buffer "
                     "(L2 left dirty), events around the launch; includes "
@@ -458,8 +480,9 @@ def run_ours(args):
         "wall_s_timed_region": round(wall, 4),
         "e2e": e2e,
         "gpu_launches": 2 * K,
-        "gpu_launches_note": "in the timed step region; the per-kernel and "
-                             "no-PDL loops after it launch 6K more",
+        "gpu_launches_note": "in the timed step region (store + gather per "
+                             "step); the per-kernel loops after it launch "
+                             "their own",
         "clocks": clocks,
     }
     if rank == 0 and not args.no_cpu_baseline:
@@ -469,6 +492,34 @@ def run_ours(args):
         torch.distributed.destroy_process_group()
     if rank == 0:
         print(json.dumps(line), flush=True)
+
+
+def attention_inputs(aw, kvq, dev):
+    """Device copies of an attention workload's inputs, output and
+    scratch."""
+    import torch
+    kv, kc, vc = kvq.alloc_nvfp4_cache(aw.num_blocks, aw.block_size,
+                                       aw.num_kv_heads, aw.head_size,
+                                       device=dev)
+    kv.view(-1).copy_(torch.from_numpy(aw.cache))
+    q = torch.from_numpy(aw.query.view(np.int16)).to(dev).view(torch.bfloat16)
+    mcl = int(aw.context_lens.max())
+    return dict(kv=kv, kc=kc, vc=vc, q=q, out=torch.empty_like(q),
+                bt=torch.from_numpy(aw.block_table).to(dev),
+                lens=torch.from_numpy(aw.context_lens).to(dev),
+                ks=torch.tensor([float(aw.k_scale)], device=dev),
+                vs=torch.tensor([float(aw.v_scale)], device=dev),
+                scale=float(aw.scale), mcl=mcl,
+                scratch=kvq.attention_scratch(aw.num_seqs, aw.num_q_heads,
+                                              mcl, 512, aw.head_size, dev))
+
+
+def run_attention(a, kvq, flags, dev_err, stream):
+    es, ml, tmp = a["scratch"]
+    kvq.kvq_paged_attention_nvfp4(
+        a["q"], a["kc"], a["vc"], a["bt"], a["lens"], a["ks"], a["vs"],
+        a["scale"], a["out"], a["mcl"], 512, es, ml, tmp, flags=flags,
+        dev_error=dev_err, stream=stream)
 
 
 def single_launch_cold(store, gather, dev, reps=20):
@@ -739,6 +790,14 @@ def run_kernel_only(args):
         def launch():
             kvq.kvq_store_indexer_k(ik, icache, islots)
         byts = iw.algorithmic_bytes()
+    elif args.kernel_only == "attn":
+        from paged_quantized_kv_gb300 import workloads as wlmod
+        aw = wlmod.attention_workload(5)
+        attn = attention_inputs(aw, kvq, dev)
+
+        def launch():
+            run_attention(attn, kvq, 0, None, None)
+        byts = aw.algorithmic_bytes()
     else:
         gcache = torch.from_numpy(ga.cache).to(dev).view(ga.num_blocks, -1)
         bt = torch.from_numpy(ga.block_table).to(dev)

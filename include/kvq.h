@@ -87,7 +87,12 @@ enum {
      just before this call on the stream (they are ready before it starts),
      so the kernel stages them while that kernel finishes and waits only
      before it reads the cache or the scales, or writes anything. */
-  KVQ_F_PDL_EARLY_META = 1u << 2
+  KVQ_F_PDL_EARLY_META = 1u << 2,
+  /* kvq_paged_attention_nvfp4 only: run the persistent, warp-specialised
+     kernel (one CTA per SM, K' in tensor memory, a dedicated MMA warp)
+     instead of the default one (several CTAs per SM).  Same result
+     contract; the default measured faster on the decode workloads. */
+  KVQ_F_ATTN_PIPELINED = 1u << 3
 };
 
 /* Bits OR-ed into *dev_error by the kernels. */
@@ -320,7 +325,7 @@ kvq_status kvq_store_indexer_k(const void* k, int64_t k_stride0,
  *                be initialised; their contents afterwards are unspecified.
  * out            dtype [num_seqs, num_q_heads, 128], rows out_stride0
  *                elements apart (multiple of 8), 16-byte aligned.
- * flags          KVQ_F_SWIZZLE_K_SCALE, KVQ_F_PDL, or 0.
+ * flags          KVQ_F_SWIZZLE_K_SCALE, KVQ_F_PDL, KVQ_F_ATTN_PIPELINED, or 0.
  * dev_error      nullable (KVQ_DEVERR_BLOCK: the token is left out;
  *                KVQ_DEVERR_SEQ; KVQ_DEVERR_TIMEOUT: nothing of that
  *                (sequence, KV head, partition) is written).

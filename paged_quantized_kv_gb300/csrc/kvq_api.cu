@@ -357,8 +357,8 @@ kvq_status kvq_paged_attention_nvfp4(
   if (dtype != KVQ_DTYPE_BF16 && dtype != KVQ_DTYPE_FP16) return KVQ_ERR_DTYPE;
   if (layout != KVQ_LAYOUT_HND && layout != KVQ_LAYOUT_NHD)
     return KVQ_ERR_LAYOUT;
-  if ((flags & ~static_cast<uint32_t>(KVQ_F_SWIZZLE_K_SCALE | KVQ_F_PDL)) !=
-      0u)
+  if ((flags & ~static_cast<uint32_t>(KVQ_F_SWIZZLE_K_SCALE | KVQ_F_PDL |
+                                      KVQ_F_ATTN_PIPELINED)) != 0u)
     return KVQ_ERR_ARG;
   if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 ||
       head_size <= 0 || block_size <= 0 || num_blocks < 0 ||
@@ -381,7 +381,8 @@ kvq_status kvq_paged_attention_nvfp4(
   const int64_t max_parts =
       (static_cast<int64_t>(max_context_len) + partition_size - 1) /
       partition_size;
-  if (num_seqs > 65535 || num_kv_heads > 65535 || max_parts > (1 << 20))
+  if (num_seqs > 65535 || num_kv_heads > 65535 || max_parts > (1 << 20) ||
+      static_cast<int64_t>(num_seqs) * num_kv_heads * max_parts >= INT32_MAX)
     return KVQ_ERR_SHAPE;
   if (num_seqs == 0) return KVQ_OK;
   if (query == nullptr || key_cache == nullptr || value_cache == nullptr ||
@@ -446,6 +447,7 @@ kvq_status kvq_paged_attention_nvfp4(
   p.swizzle_k = (flags & KVQ_F_SWIZZLE_K_SCALE) != 0u;
   p.f16 = dtype == KVQ_DTYPE_FP16;
   p.pdl = (flags & KVQ_F_PDL) != 0u;
+  p.pipelined = (flags & KVQ_F_ATTN_PIPELINED) != 0u;
   const cudaError_t err =
       launch_paged_attention_nvfp4(p, static_cast<cudaStream_t>(stream));
   return err == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;

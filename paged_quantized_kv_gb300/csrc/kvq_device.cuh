@@ -31,21 +31,28 @@ __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// One non-blocking test of phase `parity` of the mbarrier at `bar`.
+__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{ .reg .pred p;\n"
+      "  mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      "  selp.u32 %0, 1, 0, p; }"
+      : "=r"(done)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+
 // Wait for phase `parity` of the mbarrier at `bar`, for at most
 // KVQ_WAIT_LIMIT_NS of wall time (and at most 2^24 polls, in case the
-// timer stood still); false on timeout.
+// timer stood still); false on timeout.  The timer is read only once the
+// first test has failed.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+  if (mbar_try(bar, parity)) return true;
   const uint64_t start = global_ns();
   for (uint32_t polls = 0; polls < (1u << 24); ++polls) {
-    uint32_t done;
-    asm volatile(
-        "{ .reg .pred p;\n"
-        "  mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-        "  selp.u32 %0, 1, 0, p; }"
-        : "=r"(done)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    if (done) return true;
+    if (mbar_try(bar, parity)) return true;
     if (global_ns() - start > KVQ_WAIT_LIMIT_NS) return false;
   }
   return false;

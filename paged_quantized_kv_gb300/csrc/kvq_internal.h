@@ -138,6 +138,7 @@ struct AttnParams {
   bool swizzle_k;          // K scales stored swizzled too
   bool f16;                // query / out are fp16 (else bf16)
   bool pdl;
+  bool pipelined;          // the persistent pipelined kernel (else general)
 };
 
 cudaError_t launch_paged_attention_nvfp4(const AttnParams& p,

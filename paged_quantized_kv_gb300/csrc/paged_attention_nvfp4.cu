@@ -39,9 +39,16 @@
 //     denominator sums the rounded values (the weights sum to one).
 //   * Every mbarrier wait is bounded (KVQ_DEVERR_TIMEOUT); on a timeout the
 //     CTA waits once more, frees its tensor memory and writes nothing.
+// KVQ_F_ATTN_PIPELINED selects the persistent, warp-specialised kernel
+// further down instead (same contract).  Measured on GB300, the default one
+// is faster: per 128-token tile a single thread's 8 tcgen05.mma issues cost
+// ~750 cycles and each mbarrier test ~300, which four independent CTAs per
+// SM hide better than one pipelined CTA does.
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdint.h>
+
+#include <algorithm>
 
 #include "kvq_device.cuh"
 #include "kvq_internal.h"
@@ -114,7 +121,12 @@ __device__ __forceinline__ void tc_fence_after() {
 template <int N>
 __device__ __forceinline__ void tmem_ld(uint32_t addr, float (&v)[N]) {
   uint32_t r[N];
-  if constexpr (N == 8) {
+  if constexpr (N == 4) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0, %1, %2, %3}, [%4];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+        : "r"(addr));
+  } else if constexpr (N == 8) {
     asm volatile(
         "tcgen05.ld.sync.aligned.32x32b.x8.b32 "
         "{%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
@@ -122,7 +134,7 @@ __device__ __forceinline__ void tmem_ld(uint32_t addr, float (&v)[N]) {
           "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
         : "r"(addr));
   } else {
-    static_assert(N == 16, "8 or 16 columns");
+    static_assert(N == 16, "4, 8 or 16 columns");
     asm volatile(
         "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
         "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
@@ -322,7 +334,7 @@ __device__ __forceinline__ void convert_raw(const Raw& raw, bool linear,
 template <int NG, bool kF16>
 __global__ void __launch_bounds__(kThreads, 4)
 paged_attention_kernel(const AttnParams p) {
-  extern __shared__ __align__(128) uint8_t smem[];
+  extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t* kv_s = smem;
   uint8_t* p_s = smem + kKVBytes;
   uint8_t* q_s = p_s + kPBytes;
@@ -407,6 +419,7 @@ paged_attention_kernel(const AttnParams p) {
   const float k_scale = __ldg(p.k_scale);
   const int nu = 2 * ntiles;
   bool bad = false;
+  uint32_t kvalid = 0;  // bit i: this thread's token of K tile i is usable
   for (int u = 0; u < nu; ++u) {
     const bool is_v = u >= ntiles;
     const int tile = is_v ? u - ntiles : u;
@@ -429,7 +442,7 @@ paged_attention_kernel(const AttnParams p) {
       const float c2 = p.scale * k_scale * kLog2e;
 #pragma unroll
       for (int i = 0; i < kMaxTiles; ++i) {
-        const bool valid = i < ntiles && i * kTile + tid < ntok;
+        const bool valid = i < ntiles && ((kvalid >> i) & 1u);
 #pragma unroll
         for (int g = 0; g < NG; ++g)
           x[i][g] = valid ? x[i][g] * c2 : -INFINITY;
@@ -496,6 +509,7 @@ paged_attention_kernel(const AttnParams p) {
         is_v ? kv_a + (tid >> 3) * 128 + (tid & 7) * 16
              : kv_a + (tid >> 3) * 2048 + (tid & 7) * 16;
     convert_raw(cur, !is_v && !p.swizzle_k, tbase, is_v ? 2048u : 128u);
+    if (!is_v) kvalid |= static_cast<uint32_t>(cur.ok) << tile;
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     tc_fence_before();
     __syncthreads();
@@ -566,6 +580,620 @@ paged_attention_kernel(const AttnParams p) {
 }
 
 // ---------------------------------------------------------------------------
+// Pipelined kernel: one persistent CTA per SM, 8 converter warps and one MMA
+// warp.
+//
+// Converters (256 threads, two per token of a 128-token tile: dims 0..63
+// and 64..127) walk this CTA's work units tile by tile -- the unit's K
+// tiles, then its V tiles -- and for each tile
+//   * copy their own half row (32 code bytes, the 4 scale bytes or the 16
+//     band bytes) global -> shared with cp.async, kDepth tiles ahead, into
+//     a private slot (each thread reads back only what it copied, so the
+//     slots need no barrier and their reads are conflict-free); the
+//     block-table entry of a tile is fetched the same way kDepth tiles
+//     before its data;
+//   * dequantise the half row and write K' into tensor memory (tcgen05.st,
+//     lane = token: the MMA reads its A operand there) or V' into one of two
+//     shared-memory buffers (MN-major A operand of O^T = V'^T . P^T);
+//   * arrive on the buffer's "ready" mbarrier.
+// The MMA warp waits for "ready", issues the tile's MMAs from one thread and
+// commits them to the buffer's "done" mbarrier, which the converters wait
+// on before reusing the buffer, before the softmax (last K tile) and before
+// the output (last V tile).  Softmax and output are split by head columns:
+// warps 0..3 take the first half, warps 4..7 the second.
+// Context lengths are staged in shared memory once; a unit's query rows are
+// loaded while the previous unit runs.  Every wait is bounded; after a
+// timeout the CTA stops waiting, still walks its units to the end (so every
+// barrier is reached), writes no output and flags KVQ_DEVERR_TIMEOUT.
+// ---------------------------------------------------------------------------
+constexpr int kDepth = 6;            // tiles in flight per thread
+constexpr int kConsumers = 256;
+constexpr int kPipeThreads = kConsumers + 32;
+constexpr int kMaxLensSmem = 4096;   // context lengths staged when they fit
+constexpr uint32_t kPipeTmemCols = 256;  // S 0..63, O 64..79, K' 128..255
+constexpr uint32_t kKCol = 128;
+constexpr int kSlotBytes = 3 * kConsumers * 16;          // one tile, 12 KB
+constexpr int kOffSlots = 0;
+constexpr int kOffBt = kOffSlots + kDepth * kSlotBytes;  // [2*kDepth][256]
+constexpr int kOffV = kOffBt + 2 * kDepth * kConsumers * 4;
+constexpr int kOffP = kOffV + 2 * kKVBytes;
+constexpr int kOffQ = kOffP + kPBytes;
+constexpr int kOffLens = kOffQ + kQBytes;
+constexpr int kOffRed = kOffLens + kMaxLensSmem * 4;     // [2][8 warps][8]
+constexpr int kOffBar = kOffRed + 2 * 8 * 8 * 4;         // ready[2], done[2]
+constexpr int kOffSlot = kOffBar + 4 * 8;
+constexpr int kOffAbort = kOffSlot + 4;
+constexpr int kPipeSmem = kOffAbort + 4;
+static_assert(kOffBar % 8 == 0, "mbarrier alignment");
+static_assert(kOffV % 1024 == 0, "operand alignment");
+
+struct Unit {
+  int b, kh, part, L, p0, ntok, nt;
+};
+
+// Work unit u (partition fastest, then KV head, then sequence); false when
+// the partition starts past the (clamped) context.
+__device__ __forceinline__ bool unit_at(const AttnParams& p,
+                                        const int32_t* lens, int u, Unit& w) {
+  w.part = u % p.max_parts;
+  const int r = u / p.max_parts;
+  w.kh = r % p.Hkv;
+  w.b = r / p.Hkv;
+  int L = lens[w.b];
+  L = L < 0 ? 0 : (L > p.len_cap ? p.len_cap : L);
+  w.L = L;
+  w.p0 = w.part * p.part;
+  if (w.p0 >= L) return false;
+  w.ntok = min(p.part, L - w.p0);
+  w.nt = (w.ntok + kTile - 1) / kTile;
+  return true;
+}
+
+// Position in this CTA's walk: tile k (K tiles, then V tiles) of unit u.
+struct Cursor {
+  int u, k;
+  Unit w;
+};
+
+__device__ __forceinline__ void cursor_seek(const AttnParams& p,
+                                            const int32_t* lens, int U,
+                                            Cursor& c) {
+  while (c.u < U && !unit_at(p, lens, c.u, c.w)) c.u += gridDim.x;
+}
+
+__device__ __forceinline__ void cursor_next(const AttnParams& p,
+                                            const int32_t* lens, int U,
+                                            Cursor& c) {
+  if (c.u >= U) return;
+  if (++c.k < 2 * c.w.nt) return;
+  c.k = 0;
+  c.u += gridDim.x;
+  cursor_seek(p, lens, U, c);
+}
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst),
+               "l"(src)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async8(uint32_t dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(dst),
+               "l"(src)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst),
+               "l"(src)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(
+                   bar)
+               : "memory");
+}
+
+__device__ __forceinline__ void consumers_sync() {
+  asm volatile("bar.sync 1, 256;" ::: "memory");
+}
+
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t a) {
+  uint4 v;
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(a));
+  return v;
+}
+
+__device__ __forceinline__ uint32_t ld_shared_u32(uint32_t a) {
+  uint32_t v;
+  asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(a));
+  return v;
+}
+
+// A operand in tensor memory: kind::f16, fp32 accumulate.
+__device__ __forceinline__ void mma_f16_ta(uint32_t d_tmem, uint32_t a_tmem,
+                                           uint64_t b, uint32_t idesc,
+                                           uint32_t accumulate) {
+  asm volatile(
+      "{ .reg .pred p;\n"
+      "  setp.ne.b32 p, %4, 0;\n"
+      "  tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p; }"
+      ::"r"(d_tmem), "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate));
+}
+
+// 32 columns of this warp's 32 TMEM lanes, one lane per thread.
+__device__ __forceinline__ void tmem_st32(uint32_t addr,
+                                          const uint32_t (&w)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, "
+      "%30, %31, %32};" ::"r"(addr),
+      "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]),
+      "r"(w[6]), "r"(w[7]), "r"(w[8]), "r"(w[9]), "r"(w[10]), "r"(w[11]),
+      "r"(w[12]), "r"(w[13]), "r"(w[14]), "r"(w[15]), "r"(w[16]), "r"(w[17]),
+      "r"(w[18]), "r"(w[19]), "r"(w[20]), "r"(w[21]), "r"(w[22]), "r"(w[23]),
+      "r"(w[24]), "r"(w[25]), "r"(w[26]), "r"(w[27]), "r"(w[28]), "r"(w[29]),
+      "r"(w[30]), "r"(w[31])
+      : "memory");
+}
+
+// Half a token row (4 groups = 64 dims) -> 32 f16x2 words, dims 2c, 2c+1 in
+// word c.  d0, d1: the 32 code bytes; sw: the scale words (linear: one word
+// whose bytes are the 4 groups' scales; swizzled: 4 band words, scale =
+// byte r of each).
+__device__ __forceinline__ void dequant_half(uint4 d0, uint4 d1,
+                                             const uint32_t (&sw)[4],
+                                             bool linear, uint32_t r,
+                                             uint32_t (&w)[32]) {
+  const uint32_t sel = r | ((r + 4u) << 4);
+#pragma unroll
+  for (int m = 0; m < 2; ++m) {  // groups 2m, 2m+1 of this half
+    const uint32_t pair =
+        linear ? (m ? sw[0] >> 16 : sw[0]) : prmt(sw[2 * m], sw[2 * m + 1], sel);
+    const uint32_t sf = e4m3x2_to_f16x2(pair);
+    const uint32_t sf_even = prmt(sf, sf, 0x1010u);
+    const uint32_t sf_odd = prmt(sf, sf, 0x3232u);
+    const uint4 d = m ? d1 : d0;
+    uint32_t o[4];
+    dequant_word(d.x, sf_even, o);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) w[16 * m + i] = o[i];
+    dequant_word(d.y, sf_even, o);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) w[16 * m + 4 + i] = o[i];
+    dequant_word(d.z, sf_odd, o);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) w[16 * m + 8 + i] = o[i];
+    dequant_word(d.w, sf_odd, o);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) w[16 * m + 12 + i] = o[i];
+  }
+}
+
+// Token of this thread in the cursor's tile, or -1 past the partition.
+__device__ __forceinline__ int cursor_token(const Cursor& c, int U, int r) {
+  if (c.u >= U) return -1;
+  const int tile = c.k >= c.w.nt ? c.k - c.w.nt : c.k;
+  const int t = c.w.p0 + tile * kTile + r;
+  return t < c.w.p0 + c.w.ntok ? t : -1;
+}
+
+template <int NG, bool kF16>
+__global__ void __launch_bounds__(kPipeThreads, 1)
+paged_attention_pipe_kernel(const AttnParams p) {
+  constexpr int NH = NG / 2;  // head columns per half
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const uint32_t s_a = smem_addr(smem);
+  const uint32_t v_a = s_a + kOffV, p_a = s_a + kOffP, q_a = s_a + kOffQ;
+  float* red = reinterpret_cast<float*>(smem + kOffRed);
+  const uint32_t bar0 = s_a + kOffBar;
+  auto ready = [&](uint32_t x) { return bar0 + 8u * x; };
+  auto done = [&](uint32_t x) { return bar0 + 16u + 8u * x; };
+  uint32_t* slot = reinterpret_cast<uint32_t*>(smem + kOffSlot);
+  volatile int* abort_flag = reinterpret_cast<int*>(smem + kOffAbort);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int U = p.num_seqs * p.Hkv * p.max_parts;
+  pdl_prologue();
+
+  const int32_t* lens = p.lens;
+  if (p.num_seqs <= kMaxLensSmem) {
+    int32_t* s_lens = reinterpret_cast<int32_t*>(smem + kOffLens);
+    for (int i = tid; i < p.num_seqs; i += kPipeThreads)
+      s_lens[i] = __ldg(p.lens + i);
+    lens = s_lens;
+  }
+  if (warp == 0) {
+    asm volatile(
+        "tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+        ::"r"(smem_addr(slot)), "r"(kPipeTmemCols));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+  if (tid == 0) {
+    for (int x = 0; x < 2; ++x) {
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], 8;" ::"r"(ready(x)));
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(done(x)));
+    }
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if constexpr (NG == 8) {  // heads 8..15 of P^T stay zero
+    if (tid < kConsumers)
+#pragma unroll
+      for (int i = 0; i < 2; ++i)
+        st_shared_v4(p_a + kPGroup + (tid * 2 + i) * 16, 0, 0, 0, 0);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *slot;
+
+  // bounded wait; after any timeout in the CTA every wait fails at once
+  auto wait_ok = [&](uint32_t bar, uint32_t parity) -> bool {
+    if (*abort_flag) return false;
+    if (mbar_wait(bar, parity)) return true;
+    *abort_flag = 1;
+    if (p.dev_error != nullptr) atomicOr(p.dev_error, KVQ_DEVERR_TIMEOUT);
+    return false;
+  };
+
+  if (warp == kConsumers / 32) {
+    // =========================== MMA warp ================================
+    Cursor c{static_cast<int>(blockIdx.x), 0, {}};
+    cursor_seek(p, lens, U, c);
+    uint32_t g = 0;
+    while (c.u < U) {
+      const uint32_t x = g & 1u;
+      int go = 1;
+      if (lane == 0) go = wait_ok(ready(x), (g >> 1) & 1u);
+      if (!__shfl_sync(0xFFFFFFFFu, go, 0)) break;
+      tc_fence_after();
+      if (lane == 0) {
+        const bool is_v = c.k >= c.w.nt;
+        const int tile = is_v ? c.k - c.w.nt : c.k;
+        const uint32_t buf = v_a + x * kKVBytes;
+        if (!is_v) {
+          constexpr uint32_t id = instr_desc(false, false);
+#pragma unroll
+          for (int ks = 0; ks < kD / 16; ++ks)
+            mma_f16_ta(tmem + 16 * tile, tmem + kKCol + 64 * x + 8 * ks,
+                       smem_desc(q_a + ks * 256, 128, 2048), id, ks > 0);
+        } else {
+          constexpr uint32_t id = instr_desc(true, true);
+#pragma unroll
+          for (int ks = 0; ks < kTile / 16; ++ks)
+            mma_f16(tmem + kOCol, smem_desc(buf + ks * 256, 128, 2048),
+                    smem_desc(p_a + (16 * tile + 2 * ks) * 128, 128, kPGroup),
+                    id, (tile > 0 || ks > 0) ? 1u : 0u);
+        }
+        mma_commit(done(x));
+      }
+      __syncwarp();
+      cursor_next(p, lens, U, c);
+      ++g;
+    }
+    // the last commits complete before the CTA can free tensor memory
+    if (lane == 0 && g > 0) {
+      mbar_wait(done((g - 1) & 1u), ((g - 1) >> 1) & 1u);
+      if (g > 1) mbar_wait(done(g & 1u), ((g - 2) >> 1) & 1u);
+    }
+  } else {
+    // ========================== converter warps ==========================
+    const int r = tid & (kTile - 1);  // token of the tile
+    const int h = tid >> 7;           // dims 64h .. 64h+63
+    const int wq = warp & 3;          // TMEM lane quarter
+    const int half = warp >> 2;       // head columns [half*NH, half*NH+NH)
+    const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
+    const float k_scale = __ldg(p.k_scale);
+    const float v_scale = __ldg(p.v_scale);
+    const float c2 = p.scale * k_scale * kLog2e;
+    const int qn = tid >> 4, qkc = tid & 15;  // this thread's Q' chunk
+    const uint32_t my_slot = s_a + kOffSlots + tid * 16;
+    const uint32_t my_bt = s_a + kOffBt + tid * 4;
+
+    // empty contexts: zero output; contexts past the cap: flagged
+    for (int u = blockIdx.x; u < U; u += gridDim.x) {
+      Unit w;
+      if (unit_at(p, lens, u, w) || w.part != 0) continue;
+      if (w.L == 0)
+        for (int i = tid; i < p.G * kD; i += kConsumers)
+          p.out[w.b * p.out_stride0 + (w.kh * p.G) * kD + i] = 0;
+    }
+    if (tid == 0 && p.dev_error != nullptr) {
+      for (int u = blockIdx.x; u < U; u += gridDim.x) {
+        if (u % p.max_parts != 0 || (u / p.max_parts) % p.Hkv != 0) continue;
+        const int raw = lens[u / p.max_parts / p.Hkv];
+        if (raw < 0 || raw > p.len_cap) atomicOr(p.dev_error, KVQ_DEVERR_SEQ);
+      }
+    }
+
+    // block-table entry of this thread's token of the cursor's tile
+    auto issue_bt = [&](const Cursor& c, int slot_i) {
+      const int t = cursor_token(c, U, r);
+      if (t < 0) return;
+      const int idx = p.b_shift >= 0 ? t >> p.b_shift : t / p.B;
+      cp_async4(my_bt + slot_i * (kConsumers * 4),
+                p.block_table + c.w.b * p.bt_stride + idx);
+    };
+    // this thread's half row of the cursor's tile; false if nothing copied
+    auto issue_data = [&](const Cursor& c, int slot_i, int bt_i) -> bool {
+      const int t = cursor_token(c, U, r);
+      if (t < 0) return false;
+      const int32_t blk = static_cast<int32_t>(
+          ld_shared_u32(my_bt + bt_i * (kConsumers * 4)));
+      if (blk < 0 || blk >= p.num_blocks) {
+        if (p.dev_error != nullptr) atomicOr(p.dev_error, KVQ_DEVERR_BLOCK);
+        return false;
+      }
+      const bool is_v = c.k >= c.w.nt;
+      const int idx = p.b_shift >= 0 ? t >> p.b_shift : t / p.B;
+      const int off = t - idx * p.B;
+      const uint8_t* page =
+          p.side[is_v ? 1 : 0] + static_cast<int64_t>(blk) * p.page_stride;
+      const uint8_t* dp = page + c.w.kh * p.dhs + off * p.dts + h * 32;
+      const uint32_t dst = my_slot + slot_i * kSlotBytes;
+      cp_async16(dst, dp);
+      cp_async16(dst + kConsumers * 16, dp + 16);
+      const uint8_t* sp = page + p.scale_off + c.w.kh * p.shs;
+      if (!is_v && !p.swizzle_k) {
+        cp_async4(dst + 2 * kConsumers * 16, sp + off * p.sts + h * 4);
+      } else {  // band rows 2h and 2h+1 of the token's 4-row band
+        const uint8_t* band = sp + (off & ~3) * p.sts;
+        cp_async8(dst + 2 * kConsumers * 16, band + (2 * h) * p.sts);
+        cp_async8(dst + 2 * kConsumers * 16 + 8, band + (2 * h + 1) * p.sts);
+      }
+      return true;
+    };
+
+    Cursor cp{static_cast<int>(blockIdx.x), 0, {}};
+    cursor_seek(p, lens, U, cp);
+    Cursor cd = cp, cb = cp;
+    // prologue: entries of tiles 0 .. 2D-1, then data of tiles 0 .. D-1
+    for (int i = 0; i < 2 * kDepth; ++i) {
+      issue_bt(cb, i);
+      cursor_next(p, lens, U, cb);
+    }
+    cp_async_commit();
+    cp_async_wait<0>();
+    uint32_t okmask = 0;  // bit j: data slot j holds a copied half row
+    for (int i = 0; i < kDepth; ++i) {
+      okmask |= static_cast<uint32_t>(issue_data(cd, i, i)) << i;
+      cursor_next(p, lens, U, cd);
+      cp_async_commit();
+    }
+    uint4 qv = make_uint4(0, 0, 0, 0);
+    auto load_q = [&](const Unit& w) {
+      qv = make_uint4(0, 0, 0, 0);
+      if (qn < p.G)
+        qv = *reinterpret_cast<const uint4*>(
+            p.q + w.b * p.q_stride0 + (w.kh * p.G + qn) * kD + qkc * 8);
+    };
+    if (cp.u < U) load_q(cp.w);
+
+    uint32_t g = 0;          // tiles processed
+    int ds = 0, bs = 0;      // data slot g % D, entry slot g % 2D
+    uint32_t kvalid = 0;
+    float m[NH], l[NH];
+#pragma unroll
+    for (int i = 0; i < NH; ++i) { m[i] = 0.f; l[i] = 0.f; }
+    while (cp.u < U) {
+      // ---- keep kDepth tiles in flight --------------------------------
+      cp_async_wait<kDepth - 1>();  // tile g's data and tile g+D's entry
+      {
+        const int ds_new = ds;  // slot of tile g, reused by tile g + D
+        const int bt_new = bs + kDepth >= 2 * kDepth ? bs - kDepth
+                                                     : bs + kDepth;
+        const uint4 d0 = ld_shared_v4(my_slot + ds * kSlotBytes);
+        const uint4 d1 =
+            ld_shared_v4(my_slot + ds * kSlotBytes + kConsumers * 16);
+        const uint4 sc =
+            ld_shared_v4(my_slot + ds * kSlotBytes + 2 * kConsumers * 16);
+        const bool ok_g = (okmask >> ds) & 1u;
+        // tile g's bytes are in registers: the slot takes tile g + D
+        okmask &= ~(1u << ds_new);
+        okmask |= static_cast<uint32_t>(issue_data(cd, ds_new, bt_new))
+                  << ds_new;
+        issue_bt(cb, bs);  // tile g + 2D into the entry slot of tile g
+        cp_async_commit();
+        cursor_next(p, lens, U, cd);
+        cursor_next(p, lens, U, cb);
+
+        const Unit& w = cp.w;
+        const bool is_v = cp.k >= w.nt;
+        const int tile = is_v ? cp.k - w.nt : cp.k;
+        const uint32_t x = g & 1u;
+        if (cp.k == 0) {
+          // a new unit: its query rows (every MMA of the previous unit has
+          // completed), and the next unit's rows start loading
+          if constexpr (!kF16) {
+            qv.x = bf16x2_to_f16x2(qv.x);
+            qv.y = bf16x2_to_f16x2(qv.y);
+            qv.z = bf16x2_to_f16x2(qv.z);
+            qv.w = bf16x2_to_f16x2(qv.w);
+          }
+          st_shared_v4(q_a + (qn >> 3) * 2048 + qkc * 128 + (qn & 7) * 16,
+                       qv.x, qv.y, qv.z, qv.w);
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          Cursor nx = cp;
+          nx.k = 0;
+          nx.u += gridDim.x;
+          cursor_seek(p, lens, U, nx);
+          if (nx.u < U) load_q(nx.w);
+          kvalid = 0;
+        }
+        if (is_v && tile == 0) {
+          // ---- softmax, once the last K tile's MMAs have completed ------
+          wait_ok(done((g - 1) & 1u), ((g - 1) >> 1) & 1u);
+          tc_fence_after();
+          float xv[kMaxTiles][NH];
+#pragma unroll
+          for (int i = 0; i < kMaxTiles; ++i)
+            if (i < w.nt)
+              tmem_ld<NH>(tmem + lane_base + 16 * i + half * NH, xv[i]);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < kMaxTiles; ++i) {
+            const bool valid = i < w.nt && ((kvalid >> i) & 1u);
+#pragma unroll
+            for (int gg = 0; gg < NH; ++gg)
+              xv[i][gg] = valid ? xv[i][gg] * c2 : -INFINITY;
+          }
+#pragma unroll
+          for (int gg = 0; gg < NH; ++gg) {
+            float v = xv[0][gg];
+#pragma unroll
+            for (int i = 1; i < kMaxTiles; ++i) v = fmaxf(v, xv[i][gg]);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1)
+              v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+            if (lane == 0) red[warp * 8 + gg] = v;
+          }
+          consumers_sync();
+#pragma unroll
+          for (int gg = 0; gg < NH; ++gg) {
+            const float* rr = red + half * 32 + gg;
+            const float v = fmaxf(fmaxf(rr[0], rr[8]), fmaxf(rr[16], rr[24]));
+            m[gg] = v == -INFINITY ? 0.f : v;
+            l[gg] = 0.f;
+          }
+#pragma unroll
+          for (int i = 0; i < kMaxTiles; ++i) {
+            if (i >= w.nt) break;
+            uint32_t hh[NH / 2];
+#pragma unroll
+            for (int gg = 0; gg < NH; gg += 2) {
+              hh[gg / 2] = pack_f16x2(ex2(xv[i][gg] - m[gg]),
+                                      ex2(xv[i][gg + 1] - m[gg + 1]));
+              float lo, hi;
+              unpack_f16x2(hh[gg / 2], lo, hi);
+              l[gg] += lo;
+              l[gg + 1] += hi;
+            }
+            const int kt = i * kTile + r;  // token of the partition
+            const uint32_t row = p_a + (kt >> 3) * 128 + (kt & 7) * 16;
+            if constexpr (NH == 4) {
+              asm volatile("st.shared.v2.b32 [%0], {%1, %2};" ::"r"(
+                               row + half * 8),
+                           "r"(hh[0]), "r"(hh[1])
+                           : "memory");
+            } else {
+              st_shared_v4(row + half * kPGroup, hh[0], hh[1], hh[2], hh[3]);
+            }
+          }
+#pragma unroll
+          for (int gg = 0; gg < NH; ++gg) {
+            float v = l[gg];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1)
+              v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+            if (lane == 0) red[64 + warp * 8 + gg] = v;
+          }
+          consumers_sync();
+#pragma unroll
+          for (int gg = 0; gg < NH; ++gg) {
+            const float* rr = red + 64 + half * 32 + gg;
+            l[gg] = (rr[0] + rr[8]) + (rr[16] + rr[24]);
+          }
+        }
+
+        // ---- the operand buffer of tile g is free once tile g-2's MMAs
+        // have completed ------------------------------------------------
+        if (g >= 2) wait_ok(done(x), ((g >> 1) - 1) & 1u);
+        uint32_t wv[32];
+        if (ok_g) {
+          const bool linear = !is_v && !p.swizzle_k;
+          const uint32_t sw[4] = {sc.x, sc.y, sc.z, sc.w};
+          dequant_half(d0, d1, sw, linear,
+                       static_cast<uint32_t>((w.p0 + r) & 3), wv);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) wv[i] = 0;
+        }
+        if (!is_v) {
+          // K' -> tensor memory: lane = token, 32 columns per half row
+          tmem_st32(tmem + lane_base + kKCol + 64 * x + 32 * h, wv);
+          asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+          kvalid |= static_cast<uint32_t>(ok_g) << tile;
+        } else {
+          // V' -> shared memory, MN-major for O^T = V'^T . P^T
+          const uint32_t tb =
+              v_a + x * kKVBytes + (r >> 3) * 128 + (r & 7) * 16;
+#pragma unroll
+          for (int c = 0; c < 8; ++c)
+            st_shared_v4(tb + (8 * h + c) * 2048, wv[4 * c], wv[4 * c + 1],
+                         wv[4 * c + 2], wv[4 * c + 3]);
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(ready(x));
+
+        if (is_v && tile == w.nt - 1) {
+          // ---- output of this unit -------------------------------------
+          const bool ok = wait_ok(done(x), (g >> 1) & 1u);
+          tc_fence_after();
+          float o[NH];
+          tmem_ld<NH>(tmem + lane_base + kOCol + half * NH, o);
+          tmem_wait_ld();
+          tc_fence_before();
+          const int d = wq * 32 + lane;
+          const int nparts = (w.L + p.part - 1) / p.part;
+          if (ok && nparts == 1) {
+#pragma unroll
+            for (int gg = 0; gg < NH; ++gg) {
+              const int hg = half * NH + gg;
+              if (hg < p.G) {
+                const float y =
+                    l[gg] > 0.f ? o[gg] * (1.0f / l[gg]) * v_scale : 0.f;
+                p.out[w.b * p.out_stride0 + (w.kh * p.G + hg) * kD + d] =
+                    float_to_out<kF16>(y);
+              }
+            }
+          } else if (ok) {
+            const int64_t row0 =
+                (static_cast<int64_t>(w.b) * p.Hq + w.kh * p.G) *
+                    p.max_parts + w.part;
+#pragma unroll
+            for (int gg = 0; gg < NH; ++gg) {
+              const int hg = half * NH + gg;
+              if (hg < p.G) {
+                const int64_t rr =
+                    row0 + static_cast<int64_t>(hg) * p.max_parts;
+                p.tmp_out[rr * kD + d] =
+                    l[gg] > 0.f ? o[gg] * (1.0f / l[gg]) : 0.f;
+                if (wq == 0 && lane == gg) {
+                  p.max_logits[rr] = m[gg];
+                  p.exp_sums[rr] = l[gg];
+                }
+              }
+            }
+          }
+        }
+        ds = ds + 1 == kDepth ? 0 : ds + 1;
+        bs = bs + 1 == 2 * kDepth ? 0 : bs + 1;
+        cursor_next(p, lens, U, cp);
+        ++g;
+      }
+    }
+    cp_async_wait<0>();  // no copy may land after the CTA exits
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0)
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;"
+                 ::"r"(tmem), "r"(kPipeTmemCols));
+}
+
+// ---------------------------------------------------------------------------
 // Merge of the partitions of contexts longer than one partition
 // ---------------------------------------------------------------------------
 template <bool kF16>
@@ -591,7 +1219,38 @@ attention_merge_kernel(const AttnParams p) {
 }
 
 template <int NG, bool kF16>
+cudaError_t launch_pipe(const AttnParams& p, cudaStream_t stream) {
+  auto kernel = paged_attention_pipe_kernel<NG, kF16>;
+  static bool configured[64] = {false};
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  if (!configured[dev & 63]) {
+    err = cudaFuncSetAttribute(
+        kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kPipeSmem);
+    if (err != cudaSuccess) return err;
+    int occ = 0;
+    err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel,
+                                                        kPipeThreads, kPipeSmem);
+    if (err != cudaSuccess) return err;
+    if (occ < 1 || occ * kPipeTmemCols > 512)
+      return cudaErrorInvalidConfiguration;
+    configured[dev & 63] = true;
+  }
+  const int64_t units =
+      static_cast<int64_t>(p.num_seqs) * p.Hkv * p.max_parts;
+  const unsigned grid =
+      static_cast<unsigned>(std::min<int64_t>(units, sm_count()));
+  err = launch_kernel(kernel, dim3(grid), kPipeThreads, kPipeSmem, stream,
+                      p.pdl, p);
+  if (err != cudaSuccess || p.max_parts <= 1) return err;
+  return launch_kernel(attention_merge_kernel<kF16>, dim3(p.Hq, p.num_seqs),
+                       kD, 0, stream, true, p);
+}
+
+template <int NG, bool kF16>
 cudaError_t launch_ng(const AttnParams& p, cudaStream_t stream) {
+  if (p.pipelined) return launch_pipe<NG, kF16>(p, stream);
   auto kernel = paged_attention_kernel<NG, kF16>;
   static bool configured[64] = {false};
   int dev = 0;
