@@ -54,8 +54,15 @@ typedef enum {
   KVQ_ERR_DTYPE = -4,   /* unsupported input element type */
   KVQ_ERR_LAYOUT = -5,  /* layout is neither HND nor NHD */
   KVQ_ERR_CUDA = -6,    /* the CUDA runtime reported an error at launch */
-  KVQ_ERR_ARG = -7      /* unknown flag bits or inconsistent arguments */
+  KVQ_ERR_ARG = -7,     /* unknown flag bits or inconsistent arguments */
+  KVQ_ERR_SCRATCH = -8  /* kvq_paged_attention_nvfp4_noalloc: the call needs
+                           more scratch than the built-in array holds */
 } kvq_status;
+
+/* Size of the scratch array built into the library for
+   kvq_paged_attention_nvfp4_noalloc (held on every GPU that loads the
+   library until the process exits). */
+#define KVQ_NOALLOC_SCRATCH_BYTES (32u << 20)
 
 /* Physical layout of one side (K or V) of a cache page. */
 enum {
@@ -342,6 +349,46 @@ kvq_status kvq_paged_attention_nvfp4(
     float scale, int32_t partition_size, float* exp_sums, float* max_logits,
     float* tmp_out, void* out, int64_t out_stride0, uint32_t flags,
     int32_t* dev_error, void* stream);
+
+/*
+ * kvq_paged_attention_nvfp4_noalloc -- kvq_paged_attention_nvfp4 for callers
+ * that cannot allocate device memory.  The source material has no
+ * counterpart; this entry point is an addition of this library.
+ *
+ * Who needs it: the attention needs fp32 scratch whenever a context spans
+ * more than one partition, and the plain entry point takes it from the
+ * caller.  A caller that runs after an engine has reserved all device
+ * memory for itself, or inside a runtime that forbids device allocation
+ * once it is serving, has no way to provide it.  This entry point takes no
+ * scratch arguments and allocates nothing (no cudaMalloc, no cudaFree, no
+ * allocating library routine): it uses an array of
+ * KVQ_NOALLOC_SCRATCH_BYTES (32 MiB) built into the library, which every
+ * GPU that loads the library holds until the process exits.
+ *
+ * Arguments, result and errors: as kvq_paged_attention_nvfp4 without
+ * exp_sums, max_logits and tmp_out.  A call that needs more than the array
+ * holds -- num_seqs * num_q_heads * ceil(max_context_len / partition_size)
+ * * (head_size + 2) * 4 bytes, when that ceiling is above 1 -- returns
+ * KVQ_ERR_SCRATCH and launches nothing.
+ *
+ * The first call on a device looks up the array's device address (with that
+ * device current) and keeps it; make that first call outside any stream
+ * capture.  All calls share the one array, which keeps whatever the last
+ * call left in it; nothing in it needs to start at zero, since every entry
+ * a call reads it has written first.  Calls whose kernels can overlap on
+ * the GPU (other streams, other host threads) race on the array and must be
+ * ordered by the caller.
+ */
+kvq_status kvq_paged_attention_nvfp4_noalloc(
+    const void* query, int64_t query_stride0, int32_t dtype, int32_t num_seqs,
+    int32_t num_q_heads, int32_t num_kv_heads, int32_t head_size,
+    const uint8_t* key_cache, const uint8_t* value_cache, int64_t page_stride,
+    int32_t block_size, int64_t num_blocks, int32_t layout,
+    const int32_t* block_table, int64_t block_table_stride,
+    int32_t max_blocks_per_seq, const int32_t* context_lens,
+    int32_t max_context_len, const float* k_scale, const float* v_scale,
+    float scale, int32_t partition_size, void* out, int64_t out_stride0,
+    uint32_t flags, int32_t* dev_error, void* stream);
 
 /* Static text for a status code. */
 const char* kvq_status_string(kvq_status status);

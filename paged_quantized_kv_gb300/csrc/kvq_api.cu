@@ -463,6 +463,7 @@ const char* kvq_status_string(kvq_status status) {
     case KVQ_ERR_LAYOUT: return "unknown cache layout";
     case KVQ_ERR_CUDA: return "CUDA launch error";
     case KVQ_ERR_ARG: return "invalid flags or inconsistent arguments";
+    case KVQ_ERR_SCRATCH: return "needs more than the built-in scratch array";
   }
   return "unknown status";
 }

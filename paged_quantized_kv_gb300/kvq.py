@@ -42,6 +42,8 @@ KVQ_ERR_DTYPE = -4
 KVQ_ERR_LAYOUT = -5
 KVQ_ERR_CUDA = -6
 KVQ_ERR_ARG = -7
+KVQ_ERR_SCRATCH = -8
+KVQ_NOALLOC_SCRATCH_BYTES = 32 << 20
 
 KVQ_LAYOUT_HND = 0
 KVQ_LAYOUT_NHD = 1
@@ -103,6 +105,12 @@ def lib() -> ctypes.CDLL:
             c.c_int64, c.c_int32, P, c.c_int32, P, P, c.c_float, c.c_int32,
             P, P, P, P, c.c_int64, c.c_uint32, P, P]
         L.kvq_paged_attention_nvfp4.restype = c.c_int
+        L.kvq_paged_attention_nvfp4_noalloc.argtypes = [
+            P, c.c_int64, c.c_int32, c.c_int32, c.c_int32, c.c_int32,
+            c.c_int32, P, P, c.c_int64, c.c_int32, c.c_int64, c.c_int32, P,
+            c.c_int64, c.c_int32, P, c.c_int32, P, P, c.c_float, c.c_int32,
+            P, c.c_int64, c.c_uint32, P, P]
+        L.kvq_paged_attention_nvfp4_noalloc.restype = c.c_int
         L.kvq_status_string.argtypes = [c.c_int]
         L.kvq_status_string.restype = c.c_char_p
         L.kvq_version.argtypes = []
@@ -331,6 +339,47 @@ def kvq_paged_attention_nvfp4(query: torch.Tensor, key_cache: torch.Tensor,
         out.stride(0), int(flags), _ptr(dev_error),
         _stream_of(query) if stream is None else stream)
     _check("kvq_paged_attention_nvfp4", st)
+
+
+def kvq_paged_attention_nvfp4_noalloc(query: torch.Tensor,
+                                      key_cache: torch.Tensor,
+                                      value_cache: torch.Tensor,
+                                      block_table: torch.Tensor,
+                                      context_lens: torch.Tensor,
+                                      k_scale: torch.Tensor,
+                                      v_scale: torch.Tensor, scale: float,
+                                      out: torch.Tensor, max_context_len: int,
+                                      partition_size: int = 512,
+                                      flags: int = 0,
+                                      dev_error: torch.Tensor | None = None,
+                                      stream: int | None = None) -> None:
+    """kvq_paged_attention_nvfp4 for callers that cannot allocate device
+    memory (see ``include/kvq.h``): the same arguments without the scratch
+    tensors; the library's built-in scratch array is used instead, and
+    nothing is allocated here either."""
+    dtypes = {torch.bfloat16: KVQ_DTYPE_BF16, torch.float16: KVQ_DTYPE_FP16}
+    if query.dtype not in dtypes or out.dtype != query.dtype:
+        raise KvqError("kvq_paged_attention_nvfp4_noalloc", KVQ_ERR_DTYPE)
+    n, Hq, D = query.shape
+    if (query.stride(2) != 1 or query.stride(1) != D or out.stride(2) != 1
+            or out.stride(1) != D or tuple(out.shape) != (n, Hq, D)):
+        raise KvqError("kvq_paged_attention_nvfp4_noalloc", KVQ_ERR_SHAPE)
+    if key_cache.dim() != 4 or key_cache.dtype != torch.uint8:
+        raise KvqError("kvq_paged_attention_nvfp4_noalloc", KVQ_ERR_SHAPE)
+    if block_table.dtype != torch.int32 or context_lens.dtype != torch.int32:
+        raise KvqError("kvq_paged_attention_nvfp4_noalloc", KVQ_ERR_DTYPE)
+    layout = (KVQ_LAYOUT_HND if key_cache.stride(2) > key_cache.stride(1)
+              else KVQ_LAYOUT_NHD)
+    st = lib().kvq_paged_attention_nvfp4_noalloc(
+        query.data_ptr(), query.stride(0), dtypes[query.dtype], n, Hq,
+        key_cache.size(2), D, key_cache.data_ptr(), value_cache.data_ptr(),
+        key_cache.stride(0), key_cache.size(1), key_cache.size(0), layout,
+        block_table.data_ptr(), block_table.stride(0), block_table.size(1),
+        context_lens.data_ptr(), int(max_context_len), k_scale.data_ptr(),
+        v_scale.data_ptr(), float(scale), int(partition_size),
+        out.data_ptr(), out.stride(0), int(flags), _ptr(dev_error),
+        _stream_of(query) if stream is None else stream)
+    _check("kvq_paged_attention_nvfp4_noalloc", st)
 
 
 def alloc_nvfp4_cache(num_blocks: int, block_size: int, num_heads: int,
