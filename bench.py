@@ -344,6 +344,8 @@ def run_ours(args):
     attn = attention_inputs(aw, kvq, dev)
     attn_ms = span_ms(lambda i: run_attention(attn, kvq, PDL, dev_err, sh),
                       K)
+    attn_pipe_ms = span_ms(lambda i: run_attention(
+        attn, kvq, PDL | kvq.KVQ_F_ATTN_PIPELINED, dev_err, sh), K)
     attn_bytes = aw.algorithmic_bytes()
     attn_ctx = int(aw.context_lens.astype(np.int64).sum())
     del attn
@@ -458,7 +460,10 @@ def run_ours(args):
             "frac_of_peak": round(attn_bytes / attn_ms / 1e6 / peak, 4),
             "decode_tokens_per_s": round(aw.num_seqs / (attn_ms / 1e3), 1),
             "context_tokens_per_s": round(attn_ctx / (attn_ms / 1e3), 1),
-            "algorithmic_bytes": attn_bytes},
+            "algorithmic_bytes": attn_bytes,
+            "pipelined_kernel_ms": round(attn_pipe_ms, 5),
+            "pipelined_kernel_frac_of_peak": round(
+                attn_bytes / attn_pipe_ms / 1e6 / peak, 4)},
         "single_launch_after_l2_write_flush": {
             "note": "each kernel alone after writing a 256 MiB buffer "
                     "(L2 left dirty), events around the launch; includes "
