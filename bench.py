@@ -492,6 +492,8 @@ def run_ours(args):
     }
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(st, ga, args.cpu_sample_tokens)
+        line["paged_attention_nvfp4"]["cpu_oracle"] = cpu_attention_baseline(
+            aw)
     if world > 1:
         torch.distributed.barrier()
         torch.distributed.destroy_process_group()
@@ -703,6 +705,36 @@ def cpu_baseline(st, ga, sample_tokens):
                       f"({sub.num_tokens // 512} requests) and first "
                       f"{gsub.num_seqs} gather sequences of the same "
                       f"workload, single-threaded plain C oracle"}
+
+
+def cpu_attention_baseline(aw, nseq=4):
+    """The attention oracle (plain C, double, one thread) on the first
+    `nseq` sequences of the attention workload: algorithmic GB/s and
+    context tokens/s of that sample."""
+    import oracle
+    from paged_quantized_kv_gb300 import workloads as wlmod
+    o = oracle.get()
+    sub = wlmod.AttentionWorkload(
+        name="sample", query=aw.query[:nseq], num_kv_heads=aw.num_kv_heads,
+        block_size=aw.block_size, num_blocks=aw.num_blocks, cache=aw.cache,
+        block_table=aw.block_table[:nseq],
+        context_lens=aw.context_lens[:nseq], k_scale=aw.k_scale,
+        v_scale=aw.v_scale, scale=aw.scale)
+    t = time.perf_counter()
+    o.paged_attention_nvfp4(sub.query, sub.cache, 0, sub.side_bytes,
+                            sub.page_stride, sub.block_size, sub.num_blocks,
+                            sub.layout, sub.num_kv_heads, sub.block_table,
+                            sub.context_lens, sub.k_scale, sub.v_scale,
+                            sub.scale, 0, sub.dtype)
+    dt = time.perf_counter() - t
+    ctx = int(sub.context_lens.astype(np.int64).sum())
+    return {"value": round(sub.algorithmic_bytes() / dt / 1e9, 4),
+            "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "seconds": round(dt, 3),
+            "context_tokens_per_s": round(ctx / dt, 1),
+            "sample": f"first {nseq} sequences ({ctx} context tokens, all "
+                      f"{aw.num_q_heads} query heads) of the same step, "
+                      "single-threaded plain C oracle in double"}
 
 
 def run_reference(args):
