@@ -6,6 +6,7 @@ compiled in parallel, static CUDA runtime, no torch headers.
 from __future__ import annotations
 
 import concurrent.futures as cf
+import fcntl
 import os
 import subprocess
 import sys
@@ -54,6 +55,16 @@ def build(force: bool = False, ptxas_verbose: bool = False,
         return LIB
     bdir = BUILD if out is None else out + ".build"
     os.makedirs(bdir, exist_ok=True)
+    # one build at a time per output (test workers may all ask at once);
+    # whoever waited finds the library fresh and returns
+    with open(os.path.join(bdir, ".lock"), "w") as lock:
+        fcntl.flock(lock, fcntl.LOCK_EX)
+        if not force and not defines and out is None and not _stale():
+            return LIB
+        return _build_locked(lib, bdir, ptxas_verbose, defines)
+
+
+def _build_locked(lib, bdir, ptxas_verbose, defines):
     nvcc = _nvcc()
     extra = ["-Xptxas", "-v"] if ptxas_verbose else []
     extra += [f"-D{k}={v}" for k, v in (defines or {}).items()]
