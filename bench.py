@@ -255,7 +255,7 @@ def run_ours(args):
 
     def step(i, flags):
         store(flags)
-        gather(i, flags | (kvq.KVQ_F_PDL_EARLY_META if flags else 0))
+        gather(i, flags | (kvq.KVQ_F_PDL_EARLY_READ if flags else 0))
 
     def span_ms(fn, count):
         """Mean time per call of `count` back-to-back calls (two events)."""
@@ -292,7 +292,8 @@ def run_ours(args):
     # than L2: the store streams 689 MB per call; the gather rotates over
     # GATHER_SETS buffer sets)
     store_ms = span_ms(lambda i: store(PDL), K)
-    gather_ms = span_ms(lambda i: gather(i, kvq.KVQ_F_PDL_EARLY_META), K)
+    gather_ms = span_ms(lambda i: gather(i, kvq.KVQ_F_PDL_EARLY_READ), K)
+    gather_meta_ms = span_ms(lambda i: gather(i, kvq.KVQ_F_PDL_EARLY_META), K)
     plain = {"step_ms": span_ms(lambda i: step(i, 0), K),
              "store_ms": span_ms(lambda i: store(0), K),
              "gather_ms": span_ms(lambda i: gather(i, 0), K)}
@@ -405,8 +406,9 @@ def run_ours(args):
                   "data in L2",
             "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
             "timing": "K steps (store with KVQ_F_PDL, gather with "
-                      "KVQ_F_PDL_EARLY_META: its metadata is not written by "
-                      "the kernel before it) back to back on one stream "
+                      "KVQ_F_PDL_EARLY_READ: none of its inputs -- indexer "
+                      "cache, block table, cu_seq_lens -- is written by the "
+                      "store before it) back to back on one stream "
                       "between two CUDA events; ms_per_step = span / K, max "
                       "over ranks.  Per-kernel times: K launches of that "
                       "kernel alone, back to back, same flags",
@@ -424,7 +426,8 @@ def run_ours(args):
                 "GB_s": round(gather_gbs, 1),
                 "frac_of_peak": round(gather_gbs / peak, 4),
                 "tokens_per_s": round(n / (gather_ms / 1e3), 1),
-                "algorithmic_bytes": ga_bytes},
+                "algorithmic_bytes": ga_bytes,
+                "early_meta_only_ms": round(gather_meta_ms, 5)},
         },
         "without_pdl": {k: round(v, 5) for k, v in plain.items()},
         "load_nvfp4": {

@@ -95,6 +95,13 @@ enum {
      so the kernel stages them while that kernel finishes and waits only
      before it reads the cache or the scales, or writes anything. */
   KVQ_F_PDL_EARLY_META = 1u << 2,
+  /* kvq_gather_indexer_k only; implies KVQ_F_PDL_EARLY_META.  The caller
+     promises that the kernel that runs just before this call on the stream
+     writes none of this call's inputs (kv_cache, block_table, cu_seq_lens):
+     the kernel then also issues its cache reads while that kernel finishes
+     and waits for it only before its first write (its outputs and
+     dev_error are still written strictly after it). */
+  KVQ_F_PDL_EARLY_READ = 1u << 4,
   /* kvq_paged_attention_nvfp4 only: run the persistent, warp-specialised
      kernel (one CTA per SM, K' in tensor memory, a dedicated MMA warp)
      instead of the default one (several CTAs per SM).  Same result
@@ -195,7 +202,7 @@ kvq_status kvq_store_nvfp4(const void* key, int64_t key_stride0,
  *                 flags KVQ_DEVERR_SEQ if the two disagree).
  * k_fp8           [total_tokens, head_dim] bytes, 16-byte aligned.
  * k_scale         [total_tokens * 4] bytes, 4-byte aligned.
- * flags           KVQ_F_PDL, KVQ_F_PDL_EARLY_META, or 0.
+ * flags           KVQ_F_PDL, KVQ_F_PDL_EARLY_META, KVQ_F_PDL_EARLY_READ, or 0.
  * dev_error       nullable device int32 (KVQ_DEVERR_BLOCK | KVQ_DEVERR_SEQ |
  *                 KVQ_DEVERR_TIMEOUT).
  * total_tokens == 0 returns KVQ_OK without launching.

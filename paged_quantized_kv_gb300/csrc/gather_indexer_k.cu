@@ -23,7 +23,9 @@
 //   * With KVQ_F_PDL the kernel waits for its predecessor (griddepcontrol)
 //     before touching memory; with KVQ_F_PDL_EARLY_META it stages and
 //     resolves the metadata first and waits only before the cache reads and
-//     any write, overlapping that round trip with the predecessor's tail.
+//     any write, overlapping that round trip with the predecessor's tail;
+//     with KVQ_F_PDL_EARLY_READ it also issues the cache reads first and
+//     waits only before its first write.
 //   * One warp owns 32 consecutive output rows: lane l resolves row r0 + l,
 //     then the warp moves the 32 rows as 16-byte vectors -- all loads of the
 //     unit issued before its stores, 32 x D bytes in flight per warp -- and
@@ -68,14 +70,21 @@ __device__ __forceinline__ void st_16(void* p, const uint4& v) {
                : "memory");
 }
 
+// When the kernel waits for its predecessor (programmatic dependent
+// launch): before anything (0), after resolving its rows from the
+// metadata (1, KVQ_F_PDL_EARLY_META), or after issuing its cache reads,
+// just before its first write (2, KVQ_F_PDL_EARLY_READ; with a runtime row
+// width it waits before the reads instead).
+enum { kWaitFirst = 0, kWaitMeta = 1, kWaitWrites = 2 };
+
 // CPR = 16-byte chunks per K row (head_dim / 16); 0 = runtime value.
-template <int CPR, int kMode, bool kEarlyMeta>
+template <int CPR, int kMode, int kEarly>
 __global__ void __launch_bounds__(kThreads)
 gather_indexer_k_kernel(const GatherParams p) {
   extern __shared__ __align__(16) uint8_t s_raw[];
   __shared__ __align__(8) uint64_t s_bar;
 
-  if constexpr (!kEarlyMeta) pdl_prologue();
+  if constexpr (kEarly == kWaitFirst) pdl_prologue();
   const int32_t* cu = p.cu;
   int32_t* s_cu = nullptr;
   int32_t* s_bt = nullptr;
@@ -129,12 +138,27 @@ gather_indexer_k_kernel(const GatherParams p) {
                               static_cast<int64_t>(cu[p.num_seqs]) != p.total;
 
   // ---- from here on: cache reads and writes ------------------------------
-  if constexpr (kEarlyMeta) pdl_prologue();
-  if (p.dev_error != nullptr) {
-    if (err != 0) atomicOr(p.dev_error, err);
-    if (total_mismatch) atomicOr(p.dev_error, KVQ_DEVERR_SEQ);
+  constexpr bool kWaitBeforeReads =
+      kEarly == kWaitMeta || (kEarly == kWaitWrites && CPR == 0);
+  if constexpr (kWaitBeforeReads) pdl_prologue();
+  auto flag_errors = [&]() {
+    if (p.dev_error != nullptr) {
+      if (err != 0) atomicOr(p.dev_error, err);
+      if (total_mismatch) atomicOr(p.dev_error, KVQ_DEVERR_SEQ);
+    }
+  };
+  constexpr bool kFlagAfterReads = kEarly == kWaitWrites && CPR > 0;
+  if constexpr (!kFlagAfterReads) flag_errors();
+  // whole warp leaves together (a warp past the last row has nothing to
+  // flag: its rows do not exist)
+  if (r0 >= p.total) return;
+  if (!staged) {
+    if constexpr (kFlagAfterReads) {
+      pdl_prologue();  // the timeout flag is a write: after the wait
+      flag_errors();
+    }
+    return;
   }
-  if (r0 >= p.total || !staged) return;  // whole warp leaves together
 
   // the scale load goes out first, alongside the row loads below
   uint32_t scale_bits = 0;
@@ -155,6 +179,10 @@ gather_indexer_k_kernel(const GatherParams p) {
       s[i] = reinterpret_cast<const uint8_t*>(
           __shfl_sync(0xFFFFFFFFu, my_src, row));
       if (s[i] != nullptr) v[i] = ld_nc_16(s[i] + (c % CPR) * 16);
+    }
+    if constexpr (kEarly == kWaitWrites) {
+      pdl_prologue();  // the reads are in flight; no write before the wait
+      flag_errors();
     }
 #pragma unroll
     for (int i = 0; i < CPR; ++i) {
@@ -180,7 +208,7 @@ gather_indexer_k_kernel(const GatherParams p) {
     *reinterpret_cast<uint32_t*>(p.k_scale + r * 4) = scale_bits;
 }
 
-template <int CPR, bool kEarlyMeta>
+template <int CPR, int kEarly>
 cudaError_t launch_mode(const GatherParams& p, unsigned grid,
                         cudaStream_t stream) {
   const int64_t ncu = static_cast<int64_t>(p.num_seqs) + 1;
@@ -188,21 +216,22 @@ cudaError_t launch_mode(const GatherParams& p, unsigned grid,
   const size_t both = region_bytes(ncu) + region_bytes(nbt);
   if (p.bt_stride == p.max_blocks && both <= kMaxMetaSmem)
     return launch_kernel(
-        gather_indexer_k_kernel<CPR, kMetaSharedCuBt, kEarlyMeta>, grid,
+        gather_indexer_k_kernel<CPR, kMetaSharedCuBt, kEarly>, grid,
         kThreads, both, stream, p.pdl, p);
   if (region_bytes(ncu) <= kMaxMetaSmem)
     return launch_kernel(
-        gather_indexer_k_kernel<CPR, kMetaSharedCu, kEarlyMeta>, grid,
+        gather_indexer_k_kernel<CPR, kMetaSharedCu, kEarly>, grid,
         kThreads, region_bytes(ncu), stream, p.pdl, p);
-  return launch_kernel(gather_indexer_k_kernel<CPR, kMetaGlobal, kEarlyMeta>,
+  return launch_kernel(gather_indexer_k_kernel<CPR, kMetaGlobal, kEarly>,
                        grid, kThreads, 0, stream, p.pdl, p);
 }
 
 template <int CPR>
 cudaError_t launch_cpr(const GatherParams& p, unsigned grid,
                        cudaStream_t stream) {
-  return p.early_meta ? launch_mode<CPR, true>(p, grid, stream)
-                      : launch_mode<CPR, false>(p, grid, stream);
+  if (p.early_read) return launch_mode<CPR, kWaitWrites>(p, grid, stream);
+  if (p.early_meta) return launch_mode<CPR, kWaitMeta>(p, grid, stream);
+  return launch_mode<CPR, kWaitFirst>(p, grid, stream);
 }
 
 }  // namespace

@@ -154,7 +154,8 @@ kvq_status kvq_gather_indexer_k(const uint8_t* kv_cache, int64_t block_stride,
                                 uint8_t* k_scale, uint32_t flags,
                                 int32_t* dev_error, void* stream) {
   using namespace kvq;
-  if ((flags & ~static_cast<uint32_t>(KVQ_F_PDL | KVQ_F_PDL_EARLY_META)) !=
+  if ((flags & ~static_cast<uint32_t>(KVQ_F_PDL | KVQ_F_PDL_EARLY_META |
+                                      KVQ_F_PDL_EARLY_READ)) !=
       0u)
     return KVQ_ERR_ARG;
   if (block_size <= 0 || head_dim <= 0 || num_seqs < 0 || total_tokens < 0 ||
@@ -190,7 +191,8 @@ kvq_status kvq_gather_indexer_k(const uint8_t* kv_cache, int64_t block_stride,
   p.D = head_dim;
   p.max_blocks = max_blocks_per_seq;
   p.num_seqs = num_seqs;
-  p.early_meta = (flags & KVQ_F_PDL_EARLY_META) != 0u;
+  p.early_read = (flags & KVQ_F_PDL_EARLY_READ) != 0u;
+  p.early_meta = p.early_read || (flags & KVQ_F_PDL_EARLY_META) != 0u;
   p.pdl = p.early_meta || (flags & KVQ_F_PDL) != 0u;
   const cudaError_t err =
       launch_gather_indexer_k(p, static_cast<cudaStream_t>(stream));

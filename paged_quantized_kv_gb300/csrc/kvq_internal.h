@@ -55,6 +55,7 @@ struct GatherParams {
   int32_t num_seqs;
   bool pdl;                // launch with programmatic dependent launch
   bool early_meta;         // read metadata before waiting on the predecessor
+  bool early_read;         // ... and the cache rows too (wait before writes)
 };
 
 cudaError_t launch_gather_indexer_k(const GatherParams& p,

@@ -43,7 +43,7 @@ def gpu_store(wl, sentinel=0xAA, slot_mapping=None):
 
 
 def gpu_gather(wl, total=None, sentinel=0xCD, block_table=None,
-               bt_cols=None):
+               bt_cols=None, flags=0):
     """bt_cols: hand the kernel only the first bt_cols columns of the block
     table (a view whose row stride is wider than its used part)."""
     total = wl.total_tokens if total is None else total
@@ -58,7 +58,7 @@ def gpu_gather(wl, total=None, sentinel=0xCD, block_table=None,
                    device="cuda")[:total]
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     kvq.kvq_gather_indexer_k(cache, k, s, bt, cu, block_size=wl.block_size,
-                             dev_error=err)
+                             flags=flags, dev_error=err)
     torch.cuda.synchronize()
     return (k.cpu().numpy().reshape(-1), s.cpu().numpy().reshape(-1),
             int(err.item()))

@@ -6,7 +6,10 @@ Covers the named workloads' gather parts at full size, sequences of 0, 1,
 long sequences), head_dim other than 128 (the generic copy path), a block
 table with a row stride wider than its used part, a total larger than
 cu_seq_lens[-1] (flagged, extra rows untouched), and an out-of-range block
-id (flagged, row untouched).
+id (flagged, row untouched).  Each case also runs with
+KVQ_F_PDL_EARLY_READ (cache reads issued before the wait on the
+predecessor, every write after it), which must give the same bytes and
+flags.
 """
 import numpy as np
 import pytest
@@ -17,10 +20,12 @@ from tests.gpu_helpers import assert_bytes_equal, gpu_gather
 from tests.test_oracle_gather import run_gather
 
 pytestmark = pytest.mark.gpu
+FLAGS = [0, kvq.KVQ_F_PDL_EARLY_READ]
+FLAG_IDS = ["plain", "early_read"]
 
 
-def _compare(orc, wl, total=None, bt_cols=None):
-    k, s, err = gpu_gather(wl, total=total, bt_cols=bt_cols)
+def _compare(orc, wl, total=None, bt_cols=None, flags=0):
+    k, s, err = gpu_gather(wl, total=total, bt_cols=bt_cols, flags=flags)
     wk, ws = run_gather(orc, wl, total=total)
     n = wl.total_tokens if total is None else total
     assert_bytes_equal(k, wk[: n * wl.head_dim], wl.name + " k_fp8")
@@ -28,9 +33,10 @@ def _compare(orc, wl, total=None, bt_cols=None):
     return err
 
 
+@pytest.mark.parametrize("flags", FLAGS, ids=FLAG_IDS)
 @pytest.mark.parametrize("index", [0, 3, 4])
-def test_named_workload(orc, index):
-    assert _compare(orc, W.gather_workload(index)) == 0
+def test_named_workload(orc, index, flags):
+    assert _compare(orc, W.gather_workload(index), flags=flags) == 0
 
 
 CASES = [
@@ -50,27 +56,30 @@ CASES = [
 ]
 
 
+@pytest.mark.parametrize("flags", FLAGS, ids=FLAG_IDS)
 @pytest.mark.parametrize("name,lens,B,D,nb,mb", CASES,
                          ids=[c[0] for c in CASES])
-def test_case(orc, name, lens, B, D, nb, mb):
+def test_case(orc, name, lens, B, D, nb, mb, flags):
     wl = W.make_gather(name, 30, lens, B, D, nb, max_blocks=mb)
     cols = None
     if mb and name == "d256_wide_table":
         cols = int(((np.asarray(lens) + B - 1) // B).max())
-    assert _compare(orc, wl, bt_cols=cols) == 0
+    assert _compare(orc, wl, bt_cols=cols, flags=flags) == 0
 
 
-def test_total_beyond_cu_is_flagged(orc):
+@pytest.mark.parametrize("flags", FLAGS, ids=FLAG_IDS)
+def test_total_beyond_cu_is_flagged(orc, flags):
     wl = W.make_gather("beyond", 31, [20, 45], 16, 128, 8)
-    err = _compare(orc, wl, total=wl.total_tokens + 5)
+    err = _compare(orc, wl, total=wl.total_tokens + 5, flags=flags)
     assert err == kvq.KVQ_DEVERR_SEQ
 
 
-def test_bad_block_id_is_flagged(orc):
+@pytest.mark.parametrize("flags", FLAGS, ids=FLAG_IDS)
+def test_bad_block_id_is_flagged(orc, flags):
     wl = W.make_gather("badblk", 32, [20, 45], 16, 128, 8)
     bt = wl.block_table.copy()
     bt[1, 1] = 10_000
-    k, s, err = gpu_gather(wl, block_table=bt)
+    k, s, err = gpu_gather(wl, block_table=bt, flags=flags)
     assert err == kvq.KVQ_DEVERR_BLOCK
     # rows of the bad block stay untouched; the rest match the oracle
     wk, ws = run_gather(orc, wl)

@@ -128,3 +128,73 @@ def test_early_meta_gather_reads_bytes_the_store_just_wrote(orc):
     wk, ws = run_gather(orc, g)
     assert_bytes_equal(k.cpu().numpy().reshape(-1), wk, "k over store")
     assert_bytes_equal(s.cpu().numpy().reshape(-1), ws, "s over store")
+
+
+EARLY_READ = kvq.KVQ_F_PDL_EARLY_READ
+
+
+@pytest.mark.parametrize("index", [0, 4])
+def test_store_then_early_read_gather(orc, index):
+    """The step's order: a PDL store into the NVFP4 pages, then an
+    early-read gather from the (separate) indexer cache, three times back
+    to back; the gather's cache reads may overlap the store, its writes
+    may not."""
+    st = W.store_workload(index)
+    ga = W.gather_workload(index)
+    key, value, slots, ks, vs = store_inputs(st)
+    kv, kc, vc = kvq.alloc_nvfp4_cache(st.num_blocks, st.block_size,
+                                       st.num_heads, st.head_size, fill=0xAA)
+    cache, k, s, bt, cu = _gather_args(ga)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    for _ in range(3):
+        kvq.kvq_store_nvfp4(key, value, kc, vc, slots, ks, vs, flags=PDL,
+                            dev_error=err)
+        kvq.kvq_gather_indexer_k(cache, k, s, bt, cu,
+                                 block_size=ga.block_size, flags=EARLY_READ,
+                                 dev_error=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert_bytes_equal(kv.cpu().numpy().reshape(-1), run_store(orc, st),
+                       st.name)
+    wk, ws = run_gather(orc, ga)
+    assert_bytes_equal(k.cpu().numpy().reshape(-1), wk, ga.name + " k")
+    assert_bytes_equal(s.cpu().numpy().reshape(-1), ws, ga.name + " s")
+
+
+def test_early_read_gathers_back_to_back(orc):
+    """Early-read gathers in a row (twice over four buffer sets), each
+    from its own cache copy into its own outputs: every output matches the
+    oracle."""
+    ga = W.gather_workload(4)
+    sets = [_gather_args(ga) for _ in range(4)]
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    for _ in range(2):
+        for cache, k, s, bt, cu in sets:
+            kvq.kvq_gather_indexer_k(cache, k, s, bt, cu,
+                                     block_size=ga.block_size,
+                                     flags=EARLY_READ, dev_error=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    wk, ws = run_gather(orc, ga)
+    for _, k, s, _, _ in sets:
+        assert_bytes_equal(k.cpu().numpy().reshape(-1), wk, "k")
+        assert_bytes_equal(s.cpu().numpy().reshape(-1), ws, "s")
+
+
+def test_early_read_gather_after_torch_write(orc):
+    """An early-read gather right after an ordinary torch kernel that
+    writes a buffer the gather does not read (its contract) gives the
+    oracle's bytes, and the torch kernel's result is intact."""
+    ga = W.gather_workload(3)
+    cache, k, s, bt, cu = _gather_args(ga)
+    other = torch.zeros(1 << 24, dtype=torch.uint8, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    other.fill_(7)
+    kvq.kvq_gather_indexer_k(cache, k, s, bt, cu, block_size=ga.block_size,
+                             flags=EARLY_READ, dev_error=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert int((other != 7).sum().item()) == 0
+    wk, ws = run_gather(orc, ga)
+    assert_bytes_equal(k.cpu().numpy().reshape(-1), wk, "k")
+    assert_bytes_equal(s.cpu().numpy().reshape(-1), ws, "s")
