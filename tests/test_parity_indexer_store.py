@@ -137,3 +137,96 @@ def test_quotients_on_e4m3_midpoints(orc, amax_mult):
         block_table=np.arange(T // 16, dtype=np.int32)[None, :],
         cu_seq_lens=np.array([0, T], np.int32))
     _compare(orc, wl)
+
+
+@pytest.mark.parametrize("f16", [False, True], ids=["bf16", "fp16"])
+@pytest.mark.parametrize("mult", [3.0, 5.0, 0.75, 1.25])
+def test_midpoints_with_exact_non_power_of_two_scale(orc, mult, f16):
+    """Rows whose amax is 448 * mult * 2^e, so that scale = amax / 448 is
+    exact but not a power of two, and whose other elements are e4m3
+    midpoints times mult * 2^e (exact in bf16): every quotient is exactly a
+    rounding midpoint (ties to even), the case in which the kernel's
+    division-free products cannot decide and the IEEE quotient must."""
+    e4 = torch.arange(127, dtype=torch.int32).to(torch.uint8).view(
+        torch.float8_e4m3fn).float().numpy().astype(np.float64)
+    mids = (e4[8:-1] + e4[9:]) / 2
+    rng = np.random.default_rng(85)
+    T, D = 64, 128
+    x = np.zeros((T, D), np.float64)
+    for t in range(T):
+        e = 2.0 ** (rng.integers(-6, 4) if f16 else rng.integers(-8, 8))
+        row = rng.choice(mids, D) * np.where(rng.random(D) < .5, -1, 1)
+        row = row * mult * e
+        row[0] = 448.0 * mult * e
+        x[t] = row
+    xf = x.astype(np.float32)
+    if f16:
+        bits = xf.astype(np.float16).view(np.uint16)
+        back = bits.view(np.float16).astype(np.float32)
+    else:
+        bits = W.bf16_bits(xf.reshape(-1)).reshape(T, D)
+        back = (bits.astype(np.uint32) << 16).view(np.float32)
+    # every value above is exact in the input type (<= 8 significant bits)
+    assert np.array_equal(back, xf)
+    slots = np.arange(T, dtype=np.int64)
+    wl = W.IndexerStoreWorkload(
+        name="exact_mid", k=bits, num_tokens=T, head_dim=D, block_size=16,
+        num_blocks=T // 16, slot_mapping=slots,
+        block_table=np.arange(T // 16, dtype=np.int32)[None, :],
+        cu_seq_lens=np.array([0, T], np.int32),
+        dtype=W.DTYPE_F16 if f16 else W.DTYPE_BF16)
+    _compare(orc, wl)
+
+
+def test_tiny_scales_take_the_exact_path(orc):
+    """Rows whose amax is so small that scale = amax / 448 is below 2^-125
+    (1 / scale may overflow), mixed with ordinary rows, and rows of bf16
+    subnormals beside large values."""
+    rng = np.random.default_rng(86)
+    T, D = 48, 128
+    x = rng.standard_normal((T, D)).astype(np.float32)
+    x[0:8] *= np.float32(2.0 ** -118)
+    x[8:16] *= np.float32(2.0 ** -126)
+    x[16:24, :5] = np.float32(2.0 ** -130)
+    x[16:24, 5] = np.float32(3.0e4)
+    bits = W.bf16_bits(x.reshape(-1)).reshape(T, D)
+    slots = np.arange(T, dtype=np.int64)
+    wl = W.IndexerStoreWorkload(
+        name="tiny_scale", k=bits, num_tokens=T, head_dim=D, block_size=16,
+        num_blocks=T // 16, slot_mapping=slots,
+        block_table=np.arange(T // 16, dtype=np.int32)[None, :],
+        cu_seq_lens=np.array([0, T], np.int32))
+    _compare(orc, wl)
+
+
+def test_quotients_within_an_ulp_of_a_midpoint(orc):
+    """Rows where 448 * k == m * amax exactly for the e4m3 midpoint
+    m = 1.3125 * 2^j while amax / 448 is inexact (amax has no factor 7):
+    k / scale then lies within one fp32 ulp of m without equalling it, so
+    the fp32 quotient lands on m (an e4m3 tie) for some elements and next
+    to it for others -- the double-rounding case the kernel's products must
+    settle exactly."""
+    rng = np.random.default_rng(87)
+    T, D = 256, 128
+    x = np.zeros((T, D), np.float64)
+    for t in range(T):
+        a_int = int(rng.integers(32, 64))
+        while a_int % 7 == 0:
+            a_int = int(rng.integers(32, 64))
+        a = a_int * 2.0 ** int(rng.integers(-20, 10))
+        x[t, 0] = a
+        j = rng.integers(-6, 9, size=D - 1)
+        x[t, 1:] = (3 * a / 1024 * 2.0 ** j
+                    * np.where(rng.random(D - 1) < .5, -1, 1))
+    xf = x.astype(np.float32)
+    assert np.array_equal(xf.astype(np.float64), x)
+    bits = W.bf16_bits(xf.reshape(-1)).reshape(T, D)
+    assert np.array_equal((bits.astype(np.uint32) << 16).view(np.float32),
+                          xf)
+    slots = np.arange(T, dtype=np.int64)
+    wl = W.IndexerStoreWorkload(
+        name="near_mid", k=bits, num_tokens=T, head_dim=D, block_size=16,
+        num_blocks=T // 16, slot_mapping=slots,
+        block_table=np.arange(T // 16, dtype=np.int32)[None, :],
+        cu_seq_lens=np.array([0, T], np.int32))
+    _compare(orc, wl)
