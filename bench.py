@@ -199,6 +199,7 @@ class ClockSampler:
 
 # --- our arm ----------------------------------------------------------------------
 
+QUEUE_S_PER_CALL = 40e-6  # GPU sleep per queued call (host enqueue time)
 GATHER_SETS = 8  # gather buffer sets rotated so no launch finds its data in
 # L2 (8 x 35 MB > the 129 MB L2, even in the gather-only loop)
 
@@ -258,9 +259,14 @@ def run_ours(args):
         gather(i, flags | (kvq.KVQ_F_PDL_EARLY_READ if flags else 0))
 
     def span_ms(fn, count):
-        """Mean time per call of `count` back-to-back calls (two events)."""
+        """Mean GPU time per call of `count` back-to-back calls between two
+        events.  The calls are queued behind a GPU sleep long enough for the
+        host to enqueue all of them: the binding spends ~10 us of host time
+        per call, more than a short kernel's GPU time, and would otherwise
+        pace the GPU.  The sleep runs before the first event."""
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
+        torch.cuda._sleep(int(2e9 * max(0.005, count * QUEUE_S_PER_CALL)))
         e0.record(stream)
         for i in range(count):
             fn(i)
@@ -409,9 +415,12 @@ def run_ours(args):
                       "KVQ_F_PDL_EARLY_READ: none of its inputs -- indexer "
                       "cache, block table, cu_seq_lens -- is written by the "
                       "store before it) back to back on one stream "
-                      "between two CUDA events; ms_per_step = span / K, max "
-                      "over ranks.  Per-kernel times: K launches of that "
-                      "kernel alone, back to back, same flags",
+                      "between two CUDA events, all K queued behind a GPU "
+                      "sleep before the first event (so the binding's host "
+                      "time per call does not pace the GPU); ms_per_step = "
+                      "span / K, max over ranks.  Per-kernel times: K "
+                      "launches of that kernel alone, back to back, same "
+                      "flags, queued the same way",
         },
         "tokens_per_s": round(total_tokens / step_s, 1),
         "kernels": {
