@@ -103,10 +103,16 @@ enum {
      dev_error are still written strictly after it). */
   KVQ_F_PDL_EARLY_READ = 1u << 4,
   /* kvq_paged_attention_nvfp4 only: run the persistent, warp-specialised
-     kernel (one CTA per SM, K' in tensor memory, a dedicated MMA warp)
-     instead of the default one (several CTAs per SM).  Same result
-     contract; the default measured faster on the decode workloads. */
-  KVQ_F_ATTN_PIPELINED = 1u << 3
+     tcgen05 kernel (one CTA per SM, K' in tensor memory, a dedicated MMA
+     warp) instead of the default one.  Same result contract; the default
+     measured faster on the decode workloads. */
+  KVQ_F_ATTN_PIPELINED = 1u << 3,
+  /* kvq_paged_attention_nvfp4 only: run the tcgen05 kernel with one CTA
+     per (partition, KV head, sequence) (operands staged in shared memory,
+     accumulators in tensor memory) instead of the default one (warp-level
+     MMAs on register fragments).  Same result contract; not together with
+     KVQ_F_ATTN_PIPELINED. */
+  KVQ_F_ATTN_TCGEN05 = 1u << 5
 };
 
 /* Bits OR-ed into *dev_error by the kernels. */
@@ -315,8 +321,10 @@ kvq_status kvq_store_indexer_k(const void* k, int64_t k_stride0,
  * Arithmetic (the tolerance of any comparison follows from it): the query
  * is rounded to fp16, e2m1 * sf is exact in fp16, q . (e2m1 * sf) and
  * P . V' accumulate in fp32 on the tensor cores, P = exp2 of the scaled
- * logits minus the partition max is rounded to fp16 and the denominator
- * sums the rounded values; partitions merge in fp32; out is rounded once.
+ * logits minus a maximum over the stretch of context being accumulated
+ * (never below the logits it is applied to) is rounded to fp16 and the
+ * denominator sums the rounded values; stretches merge in fp32 (rescaled
+ * by exp2 of the difference of their maxima); out is rounded once.
  *
  * query          bf16 / fp16 (dtype) [num_seqs, num_q_heads, 128], rows
  *                query_stride0 elements apart (multiple of 8), 16-byte
@@ -339,7 +347,8 @@ kvq_status kvq_store_indexer_k(const void* k, int64_t k_stride0,
  *                be initialised; their contents afterwards are unspecified.
  * out            dtype [num_seqs, num_q_heads, 128], rows out_stride0
  *                elements apart (multiple of 8), 16-byte aligned.
- * flags          KVQ_F_SWIZZLE_K_SCALE, KVQ_F_PDL, KVQ_F_ATTN_PIPELINED, or 0.
+ * flags          KVQ_F_SWIZZLE_K_SCALE, KVQ_F_PDL, and at most one of
+ *                KVQ_F_ATTN_PIPELINED and KVQ_F_ATTN_TCGEN05, or 0.
  * dev_error      nullable (KVQ_DEVERR_BLOCK: the token is left out;
  *                KVQ_DEVERR_SEQ; KVQ_DEVERR_TIMEOUT: nothing of that
  *                (sequence, KV head, partition) is written).

@@ -360,7 +360,9 @@ kvq_status kvq_paged_attention_nvfp4(
   if (layout != KVQ_LAYOUT_HND && layout != KVQ_LAYOUT_NHD)
     return KVQ_ERR_LAYOUT;
   if ((flags & ~static_cast<uint32_t>(KVQ_F_SWIZZLE_K_SCALE | KVQ_F_PDL |
-                                      KVQ_F_ATTN_PIPELINED)) != 0u)
+                                      KVQ_F_ATTN_PIPELINED |
+                                      KVQ_F_ATTN_TCGEN05)) != 0u ||
+      ((flags & KVQ_F_ATTN_PIPELINED) && (flags & KVQ_F_ATTN_TCGEN05)))
     return KVQ_ERR_ARG;
   if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 ||
       head_size <= 0 || block_size <= 0 || num_blocks < 0 ||
@@ -449,7 +451,9 @@ kvq_status kvq_paged_attention_nvfp4(
   p.swizzle_k = (flags & KVQ_F_SWIZZLE_K_SCALE) != 0u;
   p.f16 = dtype == KVQ_DTYPE_FP16;
   p.pdl = (flags & KVQ_F_PDL) != 0u;
-  p.pipelined = (flags & KVQ_F_ATTN_PIPELINED) != 0u;
+  p.kernel = (flags & KVQ_F_ATTN_PIPELINED) != 0u   ? kAttnPipelined
+             : (flags & KVQ_F_ATTN_TCGEN05) != 0u ? kAttnTcgen05
+                                                  : kAttnWarpMma;
   const cudaError_t err =
       launch_paged_attention_nvfp4(p, static_cast<cudaStream_t>(stream));
   return err == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;

@@ -139,11 +139,21 @@ struct AttnParams {
   bool swizzle_k;          // K scales stored swizzled too
   bool f16;                // query / out are fp16 (else bf16)
   bool pdl;
-  bool pipelined;          // the persistent pipelined kernel (else general)
+  int32_t kernel;          // kAttnWarpMma, kAttnTcgen05 or kAttnPipelined
+};
+
+enum {
+  kAttnWarpMma = 0,    // warp-level MMAs on register fragments (default)
+  kAttnTcgen05 = 1,    // tcgen05 per (partition, KV head, sequence) CTA
+  kAttnPipelined = 2   // tcgen05, persistent and warp-specialised
 };
 
 cudaError_t launch_paged_attention_nvfp4(const AttnParams& p,
                                          cudaStream_t stream);
+cudaError_t launch_paged_attention_mma(const AttnParams& p,
+                                       cudaStream_t stream);
+// The partition merge shared by the attention kernels (PDL launch).
+cudaError_t launch_attention_merge(const AttnParams& p, cudaStream_t stream);
 
 // Streaming-multiprocessor count of the current device (cached per device).
 int sm_count();

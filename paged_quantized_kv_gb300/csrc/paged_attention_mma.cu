@@ -1,0 +1,742 @@
+// paged_attention_mma.cu -- paged decode attention over the NVFP4 KV cache,
+// sm_103a, on warp-level tensor-core MMAs (mma.sync m16n8k16, fp16
+// operands, fp32 accumulators) with register fragments.
+//
+// Operation: the same as paged_attention_nvfp4.cu (the paged_attention op of
+// vLLM PR #12348 "[ROCm] Faster Custom Paged Attention kernels", read over
+// the NVFP4 pages of vLLM nvfp4_kv_cache_kernels.cu, commit 7ce4c8e): for
+// sequence b and query head h (KV head h / G) over the first
+// context_lens[b] tokens, out = softmax(scale * q . K^) V^ with
+// K^ = e2m1(code) * float(sf) * k_scale (V^ with v_scale).
+//
+// Why warp-level MMAs here: a decode step multiplies each 128-token tile by
+// at most 16 query heads, so every MMA is tiny (N = 8 or 16).  Measured on
+// GB300, one thread issues tcgen05.mma at 43-89 cycles per instruction at
+// that shape (the tensor core finishes each in ~25), and the handshakes
+// around tensor memory (commit, mbarrier wake-up ~300 cycles) sit on every
+// tile's critical path; mma.sync.m16n8k16 runs at 2 cycles per instruction
+// per SM with its operands already in registers and needs no handshake.
+//
+// Design, per CTA of 4 warps = one (partition of <= 512 tokens, KV head,
+// sequence); warp w owns a quarter of the partition and walks it in steps
+// of 32 tokens:
+//   * Loads: every thread copies, with cp.async (zero-filled for tokens past
+//     the context or with a bad block id), exactly the bytes its own MMA
+//     fragments need into a private shared-memory slot, kDepth steps ahead;
+//     the warp waits with cp.async.wait_group only.  Block ids of the warp's
+//     range are loaded once (one per lane) and shuffled.
+//   * Logits S^T[16 tokens x 8 heads] = K' Q'^T per n-block of 8 query
+//     heads: A = K' (rows = tokens), B = Q'^T (k = head dims).  The head
+//     dims are permuted (the same way for K and Q): in k-step s, lane
+//     (g, t) holds dims 32t + 4s .. 32t + 4s + 3, so one lane's bytes of a
+//     token are the contiguous 16 bytes 16t .. 16t + 15 (groups 2t, 2t+1).
+//   * e2m1 -> fp16 with cvt.rn.f16x2.e2m1x2 times the group scale
+//     (cvt.rn.f16x2.e4m3x2, one packed multiply): e2m1 * sf has at most 6
+//     significant bits and lies in [2^-10, 2688], so the operand is exact.
+//   * Online softmax over the warp's steps (exp2 of the scaled logits minus
+//     the running max, rounded to fp16; the denominator sums the rounded
+//     weights; the accumulator is rescaled when the max grows).  The fp16
+//     weights P^T (tokens x heads, in the logits' accumulator layout) are
+//     transposed into the B fragment of the second product with
+//     movmatrix.
+//   * O^T[16 dims x 8 heads] += V'^T P^T per m-block of 16 head dims, the
+//     dims permuted so that lane (g, t) reads the 8 contiguous bytes
+//     8g .. 8g+7 (group g) of each of its 4 tokens.
+//   * The 4 warps' (max, sum, O) merge in shared memory; a partition of a
+//     longer context is written to the caller's scratch and merged by the
+//     partition-merge kernel.
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+
+#include "kvq_internal.h"
+#include "kvq.h"
+
+namespace kvq {
+namespace {
+
+constexpr int kWarps = 4;
+constexpr int kThreads = 32 * kWarps;
+constexpr int kD = 128;          // head_size
+constexpr int kStep = 32;        // tokens per warp step
+#ifndef KVQ_ATTN_MMA_DEPTH
+#define KVQ_ATTN_MMA_DEPTH 2
+#endif
+constexpr int kDepth = KVQ_ATTN_MMA_DEPTH;  // steps in flight per warp
+// Tokens per CTA on contiguous pages (a multiple of 4 x 32; at most
+// 4 x 32 blocks of 16 tokens).
+#ifndef KVQ_ATTN_MMA_PART
+#define KVQ_ATTN_MMA_PART 1024
+#endif
+// One step's private slots of one warp, lane-contiguous per piece:
+//   K data  4 x 16 B (tokens g + 8j, bytes 16t .. 16t+15)
+//   V data  8 x  8 B (tokens 16h + {2t, 2t+1, 2t+8, 2t+9}, bytes 8g .. 8g+7)
+//   K scale 4 x  8 B (the 8-byte scale row holding groups 2t, 2t+1)
+//   V scale 4 x  4 B (the word holding group g of a token pair)
+constexpr int kKdOff = 0;
+constexpr int kVdOff = kKdOff + 4 * 16 * 32;
+constexpr int kKsOff = kVdOff + 8 * 8 * 32;
+constexpr int kVsOff = kKsOff + 4 * 8 * 32;
+constexpr int kStageBytes = kVsOff + 4 * 4 * 32;     // 5632
+constexpr int kWarpBytes = kDepth * kStageBytes;
+constexpr int kSmemBytes = kWarps * kWarpBytes;
+constexpr float kLog2e = 1.4426950408889634f;
+
+static_assert(kSmemBytes >= kWarps * 16 * kD * 4 + 2 * kWarps * 16 * 4,
+              "the merge buffers reuse the copy slots");
+
+// ---------------------------------------------------------------------------
+// Small device helpers
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// cp.async of `bytes` (4, 8 or 16) from src to dst; src_bytes = 0 fills the
+// destination with zeros and reads nothing.
+template <int kBytes>
+__device__ __forceinline__ void cp_async(uint32_t dst, const void* src,
+                                         bool valid) {
+  const uint32_t n = valid ? kBytes : 0u;
+  if constexpr (kBytes == 16)
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst),
+                 "l"(src), "r"(n)
+                 : "memory");
+  else
+    asm volatile("cp.async.ca.shared.global [%0], [%1], %2, %3;" ::"r"(dst),
+                 "l"(src), "n"(kBytes), "r"(n)
+                 : "memory");
+}
+
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+__device__ __forceinline__ uint4 lds128(uint32_t a) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(a));
+  return v;
+}
+
+__device__ __forceinline__ uint2 lds64(uint32_t a) {
+  uint2 v;
+  asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];"
+               : "=r"(v.x), "=r"(v.y)
+               : "r"(a));
+  return v;
+}
+
+__device__ __forceinline__ uint32_t lds32(uint32_t a) {
+  uint32_t v;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
+  return v;
+}
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b,
+                                         uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  return d;
+}
+
+// Two e4m3 codes (low byte first) -> f16x2 (exact).
+__device__ __forceinline__ uint32_t e4m3x2_f16x2(uint32_t pair) {
+  uint32_t h;
+  const uint16_t in = static_cast<uint16_t>(pair & 0xFFFFu);
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"(in));
+  return h;
+}
+
+// Four bytes of e2m1 pairs (element 2k in the low nibble of byte k) times
+// the f16x2 scale `sf2` -> four f16x2 words, element 2k in the low half.
+// Exact: the products have at most 6 significant bits.
+__device__ __forceinline__ void dequant_word(uint32_t w, uint32_t sf2,
+                                             uint32_t (&o)[4]) {
+  asm("{ .reg .b8 q0, q1, q2, q3;\n"
+      "  .reg .b32 h0, h1, h2, h3;\n"
+      "  mov.b32 {q0, q1, q2, q3}, %4;\n"
+      "  cvt.rn.f16x2.e2m1x2 h0, q0;  cvt.rn.f16x2.e2m1x2 h1, q1;\n"
+      "  cvt.rn.f16x2.e2m1x2 h2, q2;  cvt.rn.f16x2.e2m1x2 h3, q3;\n"
+      "  mul.rn.f16x2 %0, h0, %5;  mul.rn.f16x2 %1, h1, %5;\n"
+      "  mul.rn.f16x2 %2, h2, %5;  mul.rn.f16x2 %3, h3, %5; }"
+      : "=r"(o[0]), "=r"(o[1]), "=r"(o[2]), "=r"(o[3])
+      : "r"(w), "r"(sf2));
+}
+
+// Four bytes of e2m1 pairs -> four f16x2 words (exact), byte k -> o[k],
+// the even element in the low half.
+__device__ __forceinline__ void e2m1_word(uint32_t w, uint32_t (&o)[4]) {
+  asm("{ .reg .b8 q0, q1, q2, q3;\n"
+      "  mov.b32 {q0, q1, q2, q3}, %4;\n"
+      "  cvt.rn.f16x2.e2m1x2 %0, q0;  cvt.rn.f16x2.e2m1x2 %1, q1;\n"
+      "  cvt.rn.f16x2.e2m1x2 %2, q2;  cvt.rn.f16x2.e2m1x2 %3, q3; }"
+      : "=r"(o[0]), "=r"(o[1]), "=r"(o[2]), "=r"(o[3])
+      : "r"(w));
+}
+
+__device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Two fp32 -> f16x2, round to nearest even; `lo` in the low half.
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  uint32_t d;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+  return d;
+}
+
+__device__ __forceinline__ void unpack_f16x2(uint32_t h, float& lo,
+                                             float& hi) {
+  asm("{ .reg .f16 a, b;\n"
+      "  mov.b32 {a, b}, %2;\n"
+      "  cvt.f32.f16 %0, a;\n"
+      "  cvt.f32.f16 %1, b; }"
+      : "=f"(lo), "=f"(hi)
+      : "r"(h));
+}
+
+// bf16x2 -> f16x2 (round to nearest; exact for bf16 values inside the fp16
+// normal range).
+__device__ __forceinline__ uint32_t bf16x2_f16x2(uint32_t w) {
+  const float lo = __uint_as_float(w << 16);
+  const float hi = __uint_as_float(w & 0xFFFF0000u);
+  return pack_f16x2(lo, hi);
+}
+
+// The 8 x 8 b16 matrix whose row r / columns (2c, 2c+1) lane 4r + c holds,
+// transposed (mma fragment layout in and out).
+__device__ __forceinline__ uint32_t transpose8x8(uint32_t x) {
+  uint32_t d;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;"
+               : "=r"(d)
+               : "r"(x));
+  return d;
+}
+
+// D += A . B, m16n8k16, fp16 A/B, fp32 D.
+__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0,
+                                         uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0,
+                                         uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+      "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+template <bool kF16>
+__device__ __forceinline__ uint16_t float_to_out(float f) {
+  uint16_t h;
+  if constexpr (kF16)
+    asm("cvt.rn.f16.f32 %0, %1;" : "=h"(h) : "f"(f));
+  else
+    asm("cvt.rn.bf16.f32 %0, %1;" : "=h"(h) : "f"(f));
+  return h;
+}
+
+// ---------------------------------------------------------------------------
+// The kernel: one (partition, KV head, sequence) per CTA of 4 warps
+// ---------------------------------------------------------------------------
+// Logits of an empty (or fully invalid) range: ex2 of it minus any finite
+// maximum is 0, and ex2(0) times a zero sum stays 0 when every range is
+// empty.
+constexpr float kNoLogit = -3.0e38f;
+
+// kContig: HND pages with block_size % 16 == 0, so each 16 tokens of a
+// step lie in one block and their rows (and scale rows) are contiguous: one
+// block id and lane-constant offsets per 16 tokens.
+template <int NG, bool kF16, bool kContig>
+__global__ void __launch_bounds__(kThreads, NG == 8 ? 4 : 2)
+paged_attention_mma_kernel(const AttnParams p) {
+  constexpr int NB = NG / 8;  // n-blocks of 8 query heads
+  extern __shared__ __align__(16) uint8_t smem[];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int g = lane >> 2, t = lane & 3;
+  const int part = blockIdx.x, kh = blockIdx.y, b = blockIdx.z;
+  pdl_prologue();
+
+  int L = __ldg(p.lens + b);
+  if (L < 0 || L > p.len_cap) {
+    if (p.dev_error != nullptr && part == 0 && kh == 0 && tid == 0)
+      atomicOr(p.dev_error, KVQ_DEVERR_SEQ);
+    L = L < 0 ? 0 : p.len_cap;
+  }
+  const int p0 = part * p.part;
+  if (p0 >= L) {
+    if (part == 0) {  // empty context: the output is zero
+      for (int i = tid; i < p.G * kD; i += kThreads)
+        p.out[b * p.out_stride0 + (kh * p.G) * kD + i] = 0;
+    }
+    return;
+  }
+  const int nparts = (L + p.part - 1) / p.part;
+  // the partition's tokens split evenly over the warps, in whole steps
+  const int ntok = min(p.part, L - p0);
+  const int quarter =
+      (ntok + kWarps * kStep - 1) / (kWarps * kStep) * kStep;
+  const int w0 = p0 + warp * quarter;
+  const int w1 = min(w0 + quarter, L);
+  const int nsteps = w1 > w0 ? (w1 - w0 + kStep - 1) / kStep : 0;
+
+  // block ids of the warp's range (at most 32 blocks), one per lane
+  const int e0 = p.b_shift >= 0 ? (w0 >> p.b_shift) : w0 / p.B;
+  int32_t bt_lane = -1;
+  if (nsteps > 0) {
+    const int e1 = p.b_shift >= 0 ? ((w1 - 1) >> p.b_shift) : (w1 - 1) / p.B;
+    if (e0 + lane <= e1)
+      bt_lane = __ldg(p.block_table + b * p.bt_stride + e0 + lane);
+  }
+
+  // query fragments: lane (g, t) holds dims 32t .. 32t+31 of head 8n + g
+  uint32_t qb[NB][8][2];
+#pragma unroll
+  for (int n = 0; n < NB; ++n) {
+    const int hq = 8 * n + g;
+    uint32_t w[16];
+    if (hq < p.G) {
+      const uint4* src = reinterpret_cast<const uint4*>(
+          p.q + b * p.q_stride0 + (kh * p.G + hq) * kD + 32 * t);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint4 v = __ldg(src + i);
+        w[4 * i] = v.x;
+        w[4 * i + 1] = v.y;
+        w[4 * i + 2] = v.z;
+        w[4 * i + 3] = v.w;
+      }
+      if constexpr (!kF16) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) w[i] = bf16x2_f16x2(w[i]);
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) w[i] = 0u;
+    }
+#pragma unroll
+    for (int s = 0; s < 8; ++s) {
+      qb[n][s][0] = w[2 * s];
+      qb[n][s][1] = w[2 * s + 1];
+    }
+  }
+
+  const uint32_t wbase = smem_u32(smem) + warp * kWarpBytes;
+  const uint8_t* const kside = p.side[0];
+  const uint8_t* const vside = p.side[1];
+
+  // Where token `tok` of a side lives; every lane of the warp must call it
+  // (the block id comes by shuffle).  ok: inside the range, valid block.
+  auto locate = [&](int tok, const uint8_t* side, const uint8_t*& data,
+                    const uint8_t*& sc, int& off) -> bool {
+    const int idx = p.b_shift >= 0 ? (tok >> p.b_shift) : tok / p.B;
+    const int32_t blk = __shfl_sync(0xFFFFFFFFu, bt_lane, (idx - e0) & 31);
+    off = tok - idx * p.B;
+    const bool in = tok < w1;
+    const bool ok = in && blk >= 0 && blk < p.num_blocks;
+    if (in && !ok && p.dev_error != nullptr)
+      atomicOr(p.dev_error, KVQ_DEVERR_BLOCK);
+    const uint8_t* page =
+        side + (ok ? static_cast<int64_t>(blk) * p.page_stride : 0);
+    data = page + kh * p.dhs + static_cast<int64_t>(off) * p.dts;
+    sc = page + p.scale_off + kh * p.shs;
+    return ok;
+  };
+
+  // Whether token `tok` takes part (inside the range, valid block id);
+  // every lane must call it.
+  auto usable = [&](int tok) -> bool {
+    const int idx = p.b_shift >= 0 ? (tok >> p.b_shift) : tok / p.B;
+    const int32_t blk = __shfl_sync(0xFFFFFFFFu, bt_lane, (idx - e0) & 31);
+    return tok < w1 && blk >= 0 && blk < p.num_blocks;
+  };
+
+  // lane-constant byte offsets inside 16 contiguous tokens (kContig)
+  const int kd_off = g * 64 + 16 * t;  // + 512 for token g + 8
+  const int ks_off = p.swizzle_k ? ((g & ~3) + t) * 8 : g * 8;  // + 64
+  const int vd_off = (2 * t) * 64 + 8 * g;  // + 64 for 2t+1, + 512 for 8q
+  const int vs_off = ((2 * t) & ~3) * 8 + (g >> 1) * 8 + (g & 1) * 4;
+
+  // Issue the copies of step i (tokens w0 + 32i ..) into its slots and
+  // commit them as one group (an empty group past the last step).
+  auto issue = [&](int i) {
+    if (i >= nsteps) {
+      // nothing to copy
+    } else if constexpr (kContig) {
+      const uint32_t st = wbase + (i % kDepth) * kStageBytes;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int T = w0 + kStep * i + 16 * h;
+        const int idx = p.b_shift >= 0 ? (T >> p.b_shift) : T / p.B;
+        const int32_t blk = __shfl_sync(0xFFFFFFFFu, bt_lane, (idx - e0) & 31);
+        const bool bok = blk >= 0 && blk < p.num_blocks;
+        if (T < w1 && !bok && t == 0 && g == 0 && p.dev_error != nullptr)
+          atomicOr(p.dev_error, KVQ_DEVERR_BLOCK);
+        const int64_t rel = (bok ? static_cast<int64_t>(blk) * p.page_stride
+                                 : 0) +
+                            kh * p.dhs + static_cast<int64_t>(T - idx * p.B) * 64;
+        const int64_t srel = (bok ? static_cast<int64_t>(blk) * p.page_stride
+                                  : 0) +
+                             p.scale_off + kh * p.shs +
+                             static_cast<int64_t>(T - idx * p.B) * 8;
+        const uint8_t* kd = kside + rel;
+        const uint8_t* ks = kside + srel;
+        const uint8_t* vd = vside + rel;
+        const uint8_t* vs = vside + srel;
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {  // K: tokens T + g + 8r
+          const bool ok = bok && T + g + 8 * r < w1;
+          const int j = 2 * h + r;
+          cp_async<16>(st + kKdOff + j * 512 + lane * 16,
+                       kd + kd_off + 512 * r, ok);
+          cp_async<8>(st + kKsOff + j * 256 + lane * 8, ks + ks_off + 64 * r,
+                      ok);
+        }
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {  // V: tokens T + 8q + 2t (+1)
+          const int tok = T + 8 * q + 2 * t;
+          const int piece = 4 * h + 2 * q;
+          cp_async<8>(st + kVdOff + piece * 256 + lane * 8,
+                      vd + vd_off + 512 * q, bok && tok < w1);
+          cp_async<8>(st + kVdOff + (piece + 1) * 256 + lane * 8,
+                      vd + vd_off + 512 * q + 64, bok && tok + 1 < w1);
+          cp_async<4>(st + kVsOff + (2 * h + q) * 128 + lane * 4,
+                      vs + vs_off + 64 * q, bok && tok < w1);
+        }
+      }
+    } else {
+      const uint32_t st = wbase + (i % kDepth) * kStageBytes;
+      const int T0 = w0 + kStep * i;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {  // K: tokens T0 + g + 8j
+        const uint8_t *data, *sc;
+        int off;
+        const bool ok = locate(T0 + g + 8 * j, kside, data, sc, off);
+        cp_async<16>(st + kKdOff + j * 512 + lane * 16, data + 16 * t, ok);
+        const uint8_t* srow =
+            p.swizzle_k ? sc + static_cast<int64_t>((off & ~3) + t) * p.sts
+                        : sc + static_cast<int64_t>(off) * p.sts;
+        cp_async<8>(st + kKsOff + j * 256 + lane * 8, srow, ok);
+      }
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {  // V: tokens T0 + 16h + 8q + 2t (+1)
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+          const uint8_t *data, *sc;
+          int off;
+          const int tok = T0 + 16 * h + 8 * q + 2 * t;
+          const bool ok0 = locate(tok, vside, data, sc, off);
+          const bool ok1 = ok0 && tok + 1 < w1;
+          const int piece = 4 * h + 2 * q;
+          cp_async<8>(st + kVdOff + piece * 256 + lane * 8, data + 8 * g, ok0);
+          cp_async<8>(st + kVdOff + (piece + 1) * 256 + lane * 8,
+                      data + p.dts + 8 * g, ok1);
+          cp_async<4>(st + kVsOff + (2 * h + q) * 128 + lane * 4,
+                      sc + static_cast<int64_t>((off & ~3) + (g >> 1)) * p.sts +
+                          (g & 1) * 4,
+                      ok0);
+        }
+      }
+    }
+    cp_async_commit();
+  };
+
+  // running softmax state of heads 8n + 2t + c, and O^T fragments: o[mb][n]
+  // = rows dims 16g + 2mb (c0, c1) and 16g + 2mb + 1 (c2, c3), columns heads
+  // 8n + 2t, 8n + 2t + 1
+  float m_run[NB][2], l_run[NB][2];
+  float o[8][NB][4];
+#pragma unroll
+  for (int n = 0; n < NB; ++n) {
+    m_run[n][0] = m_run[n][1] = -INFINITY;
+    l_run[n][0] = l_run[n][1] = 0.f;
+#pragma unroll
+    for (int mb = 0; mb < 8; ++mb)
+      o[mb][n][0] = o[mb][n][1] = o[mb][n][2] = o[mb][n][3] = 0.f;
+  }
+  const float c2 = p.scale * __ldg(p.k_scale) * kLog2e;
+  // byte selectors: K scales of groups 2t, 2t+1 (linear: bytes 2t, 2t+1 of
+  // the row; swizzled: bytes off%4 and 4 + off%4 of the band row, off%4 =
+  // g%4 because steps start at multiples of 32 and B % 4 == 0); V scales of
+  // a token pair: bytes 2t%4, 2t%4 + 1 of the word
+  const uint32_t ksel =
+      p.swizzle_k ? static_cast<uint32_t>((g & 3) | ((4 + (g & 3)) << 4))
+                  : static_cast<uint32_t>((2 * t) | ((2 * t + 1) << 4));
+  const uint32_t vsel =
+      static_cast<uint32_t>(((2 * t) & 3) | ((((2 * t) & 3) + 1) << 4));
+
+#pragma unroll
+  for (int i = 0; i < kDepth - 1; ++i) issue(i);
+
+  for (int i = 0; i < nsteps; ++i) {
+    issue(i + kDepth - 1);
+    cp_async_wait<kDepth - 1>();
+    const uint32_t st = wbase + (i % kDepth) * kStageBytes;
+    const int T0 = w0 + kStep * i;
+
+    // ---- logits S^T[16 tokens x 8 heads] of the two 16-token halves -------
+    float sacc[2][NB][4];
+    uint32_t kvalid = 0;  // bit j: K token T0 + g + 8j is usable
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      uint32_t a[2][8][2];  // [row g / g+8][k-step][a0|a2 or a1|a3]
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        const int j = 2 * h + r;
+        const uint4 kd = lds128(st + kKdOff + j * 512 + lane * 16);
+        const uint2 ks = lds64(st + kKsOff + j * 256 + lane * 8);
+        const uint32_t pair = prmt(ks.x, ks.y, ksel);
+        kvalid |= static_cast<uint32_t>(usable(T0 + g + 8 * j)) << j;
+        const uint32_t sfp = e4m3x2_f16x2(pair);
+        const uint32_t sfa = prmt(sfp, sfp, 0x1010u);
+        const uint32_t sfb = prmt(sfp, sfp, 0x3232u);
+        uint32_t x[4];
+        dequant_word(kd.x, sfa, x);
+        a[r][0][0] = x[0]; a[r][0][1] = x[1];
+        a[r][1][0] = x[2]; a[r][1][1] = x[3];
+        dequant_word(kd.y, sfa, x);
+        a[r][2][0] = x[0]; a[r][2][1] = x[1];
+        a[r][3][0] = x[2]; a[r][3][1] = x[3];
+        dequant_word(kd.z, sfb, x);
+        a[r][4][0] = x[0]; a[r][4][1] = x[1];
+        a[r][5][0] = x[2]; a[r][5][1] = x[3];
+        dequant_word(kd.w, sfb, x);
+        a[r][6][0] = x[0]; a[r][6][1] = x[1];
+        a[r][7][0] = x[2]; a[r][7][1] = x[3];
+      }
+#pragma unroll
+      for (int n = 0; n < NB; ++n) {
+        // two accumulators (even / odd k-steps) halve the dependent chain
+        float e2[4] = {0.f, 0.f, 0.f, 0.f};
+        sacc[h][n][0] = sacc[h][n][1] = sacc[h][n][2] = sacc[h][n][3] = 0.f;
+#pragma unroll
+        for (int s = 0; s < 8; s += 2) {
+          mma16816(sacc[h][n], a[0][s][0], a[1][s][0], a[0][s][1],
+                   a[1][s][1], qb[n][s][0], qb[n][s][1]);
+          mma16816(e2, a[0][s + 1][0], a[1][s + 1][0], a[0][s + 1][1],
+                   a[1][s + 1][1], qb[n][s + 1][0], qb[n][s + 1][1]);
+        }
+#pragma unroll
+        for (int r = 0; r < 4; ++r) sacc[h][n][r] += e2[r];
+      }
+    }
+
+    // ---- online softmax over the 32 tokens --------------------------------
+    uint32_t pb[2][NB][2];  // B fragments of P^T: [half][n][tokens 2t | 2t+8]
+#pragma unroll
+    for (int n = 0; n < NB; ++n) {
+      float v[2][4];
+#pragma unroll
+      for (int h = 0; h < 2; ++h)
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+          const bool ok = (kvalid >> (2 * h + (r >> 1))) & 1u;
+          v[h][r] = ok ? sacc[h][n][r] * c2 : -INFINITY;
+        }
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {  // head 8n + 2t + c
+        float bm = fmaxf(fmaxf(v[0][c], v[0][2 + c]),
+                         fmaxf(v[1][c], v[1][2 + c]));
+        bm = fmaxf(bm, __shfl_xor_sync(0xFFFFFFFFu, bm, 4));
+        bm = fmaxf(bm, __shfl_xor_sync(0xFFFFFFFFu, bm, 8));
+        bm = fmaxf(bm, __shfl_xor_sync(0xFFFFFFFFu, bm, 16));
+        const float mnew = fmaxf(m_run[n][c], bm);
+        const bool none = mnew == -INFINITY;  // no usable token yet
+        const float alpha = none ? 1.f : ex2(m_run[n][c] - mnew);
+        m_run[n][c] = mnew;
+        l_run[n][c] *= alpha;
+#pragma unroll
+        for (int mb = 0; mb < 8; ++mb) {
+          o[mb][n][c] *= alpha;
+          o[mb][n][2 + c] *= alpha;
+        }
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          v[h][c] = none ? 0.f : ex2(v[h][c] - mnew);
+          v[h][2 + c] = none ? 0.f : ex2(v[h][2 + c] - mnew);
+        }
+      }
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const uint32_t pl = pack_f16x2(v[h][0], v[h][1]);  // token g
+        const uint32_t ph = pack_f16x2(v[h][2], v[h][3]);  // token g + 8
+        float a0, a1, b0, b1;
+        unpack_f16x2(pl, a0, a1);
+        unpack_f16x2(ph, b0, b1);
+        l_run[n][0] += a0 + b0;
+        l_run[n][1] += a1 + b1;
+        pb[h][n][0] = transpose8x8(pl);
+        pb[h][n][1] = transpose8x8(ph);
+      }
+    }
+
+    // ---- O^T[16 dims x 8 heads] += V'^T P^T per 16-token half --------------
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      uint2 vd[2][2];     // [pair q][token 2t+8q+e]
+      uint32_t sfp[2];    // [pair q]: {sf(2t+8q), sf(2t+8q+1)} as f16x2
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        vd[q][0] = lds64(st + kVdOff + (4 * h + 2 * q) * 256 + lane * 8);
+        vd[q][1] = lds64(st + kVdOff + (4 * h + 2 * q + 1) * 256 + lane * 8);
+        const uint32_t w = lds32(st + kVsOff + (2 * h + q) * 128 + lane * 4);
+        // a token past the range may share the word: zero its scale (its
+        // data are zero already), so no stray NaN code meets a zero weight
+        const int tok = T0 + 16 * h + 8 * q + 2 * t;
+        uint32_t pair = prmt(w, 0u, vsel);
+        if (tok + 1 >= w1) pair &= 0x00FFu;
+        if (tok >= w1) pair = 0u;
+        sfp[q] = e4m3x2_f16x2(pair);
+      }
+#pragma unroll
+      for (int wi = 0; wi < 2; ++wi) {  // bytes 0..3, then 4..7: m-blocks
+        // interleave the two tokens of a pair nibble by nibble: byte k of
+        // ev holds dim 16g + 8wi + 2k of token 2t+8q (low nibble) and of
+        // token 2t+8q+1 (high nibble); od the odd dims.  One conversion then
+        // gives the A-fragment pair of the two tokens.
+        uint32_t ev[2][4], od[2][4];
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+          const uint32_t wa = wi == 0 ? vd[q][0].x : vd[q][0].y;
+          const uint32_t wb = wi == 0 ? vd[q][1].x : vd[q][1].y;
+          e2m1_word((wa & 0x0F0F0F0Fu) | ((wb << 4) & 0xF0F0F0F0u), ev[q]);
+          e2m1_word(((wa >> 4) & 0x0F0F0F0Fu) | (wb & 0xF0F0F0F0u), od[q]);
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int mb = 4 * wi + k;
+          const uint32_t a0 = hmul2(ev[0][k], sfp[0]);
+          const uint32_t a1 = hmul2(od[0][k], sfp[0]);
+          const uint32_t a2 = hmul2(ev[1][k], sfp[1]);
+          const uint32_t a3 = hmul2(od[1][k], sfp[1]);
+#pragma unroll
+          for (int n = 0; n < NB; ++n)
+            mma16816(o[mb][n], a0, a1, a2, a3, pb[h][n][0], pb[h][n][1]);
+        }
+      }
+    }
+  }
+  cp_async_wait<0>();  // nothing may land after the slots are reused
+
+  // ---- merge the 4 warps' partial results in shared memory ----------------
+#pragma unroll
+  for (int n = 0; n < NB; ++n)
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+      float l = l_run[n][c];
+      l += __shfl_xor_sync(0xFFFFFFFFu, l, 4);
+      l += __shfl_xor_sync(0xFFFFFFFFu, l, 8);
+      l += __shfl_xor_sync(0xFFFFFFFFu, l, 16);
+      l_run[n][c] = l;
+    }
+  __syncthreads();  // every warp is done with its copy slots
+  float* sO = reinterpret_cast<float*>(smem);        // [warp][16][kD]
+  float* sM = sO + kWarps * 16 * kD;                 // [warp][16]
+  float* sL = sM + kWarps * 16;                      // [warp][16]
+#pragma unroll
+  for (int n = 0; n < NB; ++n)
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+      const int hh = 8 * n + 2 * t + c;
+      float* row = sO + (warp * 16 + hh) * kD + 16 * g;
+#pragma unroll
+      for (int mb = 0; mb < 8; ++mb)
+        *reinterpret_cast<float2*>(row + 2 * mb) =
+            make_float2(o[mb][n][c], o[mb][n][2 + c]);
+      if (g == 0) {
+        sM[warp * 16 + hh] =
+            m_run[n][c] == -INFINITY ? kNoLogit : m_run[n][c];
+        sL[warp * 16 + hh] = l_run[n][c];
+      }
+    }
+  __syncthreads();
+  const int d = tid;  // one head dim per thread
+  const float v_scale = __ldg(p.v_scale);
+  for (int hh = 0; hh < p.G; ++hh) {
+    float M = sM[hh];
+#pragma unroll
+    for (int w = 1; w < kWarps; ++w) M = fmaxf(M, sM[w * 16 + hh]);
+    float den = 0.f, acc = 0.f;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+      const float f = ex2(sM[w * 16 + hh] - M);
+      den += sL[w * 16 + hh] * f;
+      acc += sO[(w * 16 + hh) * kD + d] * f;
+    }
+    if (nparts == 1) {
+      const float y = den > 0.f ? acc * (1.0f / den) * v_scale : 0.f;
+      p.out[b * p.out_stride0 + (kh * p.G + hh) * kD + d] =
+          float_to_out<kF16>(y);
+    } else {
+      const int64_t r =
+          (static_cast<int64_t>(b) * p.Hq + kh * p.G + hh) * p.max_parts +
+          part;
+      p.tmp_out[r * kD + d] = den > 0.f ? acc * (1.0f / den) : 0.f;
+      if (d == 0) {
+        p.max_logits[r] = M;
+        p.exp_sums[r] = den;
+      }
+    }
+  }
+}
+
+template <int NG, bool kF16, bool kContig>
+cudaError_t launch_mma(const AttnParams& caller, cudaStream_t stream) {
+  auto kernel = paged_attention_mma_kernel<NG, kF16, kContig>;
+  // A CTA may cover a longer partition than the caller's (fewer, longer
+  // warp ranges; the scratch rows keep the caller's max_parts stride and
+  // need fewer entries).  A warp range must span at most 32 blocks.
+  AttnParams p = caller;
+  if (kContig && p.part < KVQ_ATTN_MMA_PART) p.part = KVQ_ATTN_MMA_PART;
+  const int parts =
+      static_cast<int>((static_cast<int64_t>(p.len_cap) + p.part - 1) / p.part);
+  static bool configured[64] = {false};  // per instantiation and device
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  if (!configured[dev & 63]) {
+    err = cudaFuncSetAttribute(
+        kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (err != cudaSuccess) return err;
+    configured[dev & 63] = true;
+  }
+  const dim3 grid(parts > 0 ? parts : 1, p.Hkv, p.num_seqs);
+  err = launch_kernel(kernel, grid, kThreads, kSmemBytes, stream, p.pdl, p);
+  if (err != cudaSuccess || parts <= 1) return err;
+  return launch_attention_merge(p, stream);
+}
+
+template <int NG, bool kF16>
+cudaError_t launch_layout(const AttnParams& p, cudaStream_t stream) {
+  const bool contig = p.dts == kD / 2 && p.sts == kD / 16 &&
+                      p.B % 16 == 0;
+  return contig ? launch_mma<NG, kF16, true>(p, stream)
+                : launch_mma<NG, kF16, false>(p, stream);
+}
+
+}  // namespace
+
+cudaError_t launch_paged_attention_mma(const AttnParams& p,
+                                       cudaStream_t stream) {
+  if (p.G <= 8)
+    return p.f16 ? launch_layout<8, true>(p, stream)
+                 : launch_layout<8, false>(p, stream);
+  return p.f16 ? launch_layout<16, true>(p, stream)
+               : launch_layout<16, false>(p, stream);
+}
+
+}  // namespace kvq

@@ -14,6 +14,10 @@
 // partition's max logit, exp-sum and normalised output to the caller's
 // scratch, and a second small kernel merges the partitions.
 //
+// This file holds the two tcgen05 kernels (KVQ_F_ATTN_TCGEN05 and
+// KVQ_F_ATTN_PIPELINED) and the partition merge; the default kernel, on
+// warp-level MMAs, is in paged_attention_mma.cu.
+//
 // GB300 design -- one CTA of 4 warps per (partition of <= 512 tokens, KV
 // head, sequence), 3 CTAs per SM (56 KB of shared memory, 128 TMEM columns
 // each):
@@ -41,10 +45,10 @@
 //   * Every mbarrier wait is bounded (KVQ_DEVERR_TIMEOUT); on a timeout the
 //     CTA waits once more, frees its tensor memory and writes nothing.
 // KVQ_F_ATTN_PIPELINED selects the persistent, warp-specialised kernel
-// further down instead (same contract).  Measured on GB300, the default one
-// is faster: per 128-token tile a single thread's 8 tcgen05.mma issues cost
-// ~750 cycles and each mbarrier test ~300, which four independent CTAs per
-// SM hide better than one pipelined CTA does.
+// further down instead (same contract).  Measured on GB300, the per-CTA one
+// is the faster of the two: per 128-token tile a single thread's 8
+// tcgen05.mma issues cost ~750 cycles and each mbarrier test ~300, which
+// several independent CTAs per SM hide better than one pipelined CTA does.
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdint.h>
@@ -1257,7 +1261,7 @@ cudaError_t launch_pipe(const AttnParams& p, cudaStream_t stream) {
 
 template <int NG, bool kF16>
 cudaError_t launch_ng(const AttnParams& p, cudaStream_t stream) {
-  if (p.pipelined) return launch_pipe<NG, kF16>(p, stream);
+  if (p.kernel == kAttnPipelined) return launch_pipe<NG, kF16>(p, stream);
   auto kernel = paged_attention_kernel<NG, kF16>;
   static bool configured[64] = {false};
   int dev = 0;
@@ -1284,8 +1288,16 @@ cudaError_t launch_ng(const AttnParams& p, cudaStream_t stream) {
 
 }  // namespace
 
+cudaError_t launch_attention_merge(const AttnParams& p, cudaStream_t stream) {
+  return p.f16 ? launch_kernel(attention_merge_kernel<true>,
+                               dim3(p.Hq, p.num_seqs), kD, 0, stream, true, p)
+               : launch_kernel(attention_merge_kernel<false>,
+                               dim3(p.Hq, p.num_seqs), kD, 0, stream, true, p);
+}
+
 cudaError_t launch_paged_attention_nvfp4(const AttnParams& p,
                                          cudaStream_t stream) {
+  if (p.kernel == kAttnWarpMma) return launch_paged_attention_mma(p, stream);
   if (p.G <= 8)
     return p.f16 ? launch_ng<8, true>(p, stream)
                  : launch_ng<8, false>(p, stream);

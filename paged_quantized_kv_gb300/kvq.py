@@ -54,6 +54,7 @@ KVQ_F_PDL = 2
 KVQ_F_PDL_EARLY_META = 4
 KVQ_F_ATTN_PIPELINED = 1 << 3
 KVQ_F_PDL_EARLY_READ = 1 << 4
+KVQ_F_ATTN_TCGEN05 = 1 << 5
 KVQ_DEVERR_SLOT = 1
 KVQ_DEVERR_BLOCK = 2
 KVQ_DEVERR_SEQ = 4

@@ -21,7 +21,8 @@ swizzled K scales, block sizes 4 to 384 (12 and 384 not powers of two),
 large logits (one-hot weights), pages written by the GPU store, a PDL chain
 store -> attention, the Llama-3.1-70B-shaped decode batch (sampled rows),
 clamped contexts and invalid block ids (flags), and bitwise determinism --
-for both kernels (the default one and KVQ_F_ATTN_PIPELINED)."""
+for all three kernels (the default warp-level-MMA one,
+KVQ_F_ATTN_PIPELINED and KVQ_F_ATTN_TCGEN05)."""
 import numpy as np
 import pytest
 import torch
@@ -44,7 +45,7 @@ def _upload(wl):
 
 
 def gpu_attention(wl, partition_size=512, max_context_len=None, flags=None,
-                  dev_error=None, caches=None, pipelined=False):
+                  dev_error=None, caches=None, kernel=0):
     kv, kc, vc = _upload(wl) if caches is None else caches
     tdt = torch.float16 if wl.dtype == W.DTYPE_F16 else torch.bfloat16
     q = torch.from_numpy(wl.query.view(np.int16)).cuda().view(tdt)
@@ -58,8 +59,8 @@ def gpu_attention(wl, partition_size=512, max_context_len=None, flags=None,
     kvq.kvq_paged_attention_nvfp4(
         q, kc, vc, bt, lens, ks, vs, float(wl.scale), out, mcl,
         partition_size=partition_size,
-        flags=(wl.flags if flags is None else flags)
-        | (kvq.KVQ_F_ATTN_PIPELINED if pipelined else 0), dev_error=dev_error)
+        flags=(wl.flags if flags is None else flags) | kernel,
+        dev_error=dev_error)
     torch.cuda.synchronize()
     return out.float().cpu().numpy().astype(np.float64)
 
@@ -113,57 +114,59 @@ LENS = [1, 15, 16, 17, 127, 128, 129, 255, 300, 511, 512, 513, 700, 1025,
         2049, 0]
 
 
-KERNELS = [False, True]  # default, persistent pipelined
-KIDS = ["default", "pipelined"]
+# kernel flags: the default (warp-level MMAs), the persistent pipelined
+# tcgen05 kernel, the per-partition tcgen05 kernel
+KERNELS = [0, kvq.KVQ_F_ATTN_PIPELINED, kvq.KVQ_F_ATTN_TCGEN05]
+KIDS = ["warp_mma", "pipelined", "tcgen05"]
 
 
-@pytest.mark.parametrize("pipelined", KERNELS, ids=KIDS)
+@pytest.mark.parametrize("kernel", KERNELS, ids=KIDS)
 @pytest.mark.parametrize("part", [512, 256, 128, 384])
-def test_contexts_and_partitions(orc, part, pipelined):
+def test_contexts_and_partitions(orc, part, kernel):
     wl = W.make_attention("ctx", 21, LENS, num_q_heads=16, num_kv_heads=2,
                           head_size=128, block_size=16)
-    _check(orc, wl, partition_size=part, pipelined=pipelined)
+    _check(orc, wl, partition_size=part, kernel=kernel)
 
 
-@pytest.mark.parametrize("pipelined", KERNELS, ids=KIDS)
+@pytest.mark.parametrize("kernel", KERNELS, ids=KIDS)
 @pytest.mark.parametrize("G", [1, 2, 4, 8, 16])
-def test_group_sizes(orc, G, pipelined):
+def test_group_sizes(orc, G, kernel):
     Hkv = 2
     wl = W.make_attention(f"g{G}", 30 + G, [3, 200, 640, 129],
                           num_q_heads=G * Hkv, num_kv_heads=Hkv,
                           head_size=128, block_size=16)
-    _check(orc, wl, pipelined=pipelined)
+    _check(orc, wl, kernel=kernel)
 
 
-@pytest.mark.parametrize("pipelined", KERNELS, ids=KIDS)
+@pytest.mark.parametrize("kernel", KERNELS, ids=KIDS)
 @pytest.mark.parametrize("dtype", [W.DTYPE_BF16, W.DTYPE_F16])
 @pytest.mark.parametrize("layout", [W.LAYOUT_HND, W.LAYOUT_NHD])
 @pytest.mark.parametrize("swz", [0, oracle.F_SWIZZLE_K_SCALE])
-def test_layouts_dtypes_swizzle(orc, dtype, layout, swz, pipelined):
+def test_layouts_dtypes_swizzle(orc, dtype, layout, swz, kernel):
     wl = W.make_attention("lay", 40, [77, 600, 5, 1000], num_q_heads=8,
                           num_kv_heads=4, head_size=128, block_size=16,
                           dtype=dtype, flags=swz)
     if layout == W.LAYOUT_NHD:
         wl = _nhd(wl)
-    _check(orc, wl, pipelined=pipelined)
+    _check(orc, wl, kernel=kernel)
 
 
-@pytest.mark.parametrize("pipelined", KERNELS, ids=KIDS)
+@pytest.mark.parametrize("kernel", KERNELS, ids=KIDS)
 @pytest.mark.parametrize("B", [4, 8, 12, 32, 64, 128, 256, 384])
-def test_block_sizes(orc, B, pipelined):
+def test_block_sizes(orc, B, kernel):
     lens = [B - 1, B, B + 1, 4 * B + 3, 900]
     wl = W.make_attention(f"B{B}", 50 + B, [n for n in lens if n <= 2100],
                           num_q_heads=8, num_kv_heads=1, head_size=128,
                           block_size=B)
-    _check(orc, wl, pipelined=pipelined)
+    _check(orc, wl, kernel=kernel)
 
 
-@pytest.mark.parametrize("pipelined", KERNELS, ids=KIDS)
-def test_one_hot_logits(orc, pipelined):
+@pytest.mark.parametrize("kernel", KERNELS, ids=KIDS)
+def test_one_hot_logits(orc, kernel):
     wl = W.make_attention("hot", 60, [300, 1200, 40], num_q_heads=8,
                           num_kv_heads=2, head_size=128, block_size=16,
                           scale=50.0)
-    _check(orc, wl, pipelined=pipelined)
+    _check(orc, wl, kernel=kernel)
 
 
 def test_store_then_attention(orc):
@@ -208,12 +211,12 @@ def test_store_then_attention(orc):
     assert np.array_equal(outs[0], outs[1])
 
 
-@pytest.mark.parametrize("pipelined", KERNELS, ids=KIDS)
-def test_llama70b_decode_batch_sampled(orc, pipelined):
+@pytest.mark.parametrize("kernel", KERNELS, ids=KIDS)
+def test_llama70b_decode_batch_sampled(orc, kernel):
     """The benchmark's decode step (200 sequences, 64 query / 8 KV heads),
     run in full on the GPU; eight sequences checked against the oracle."""
     wl = W.attention_workload()
-    got = gpu_attention(wl, pipelined=pipelined)
+    got = gpu_attention(wl, kernel=kernel)
     rng = np.random.default_rng(72)
     pick = np.sort(rng.choice(wl.num_seqs, size=8, replace=False))
     pick[0] = int(np.argmax(wl.context_lens))       # the longest context
@@ -227,35 +230,33 @@ def test_llama70b_decode_batch_sampled(orc, pipelined):
                  "llama70b_decode")
 
 
-@pytest.mark.parametrize("pipelined", KERNELS, ids=KIDS)
-def test_deterministic(orc, pipelined):
+@pytest.mark.parametrize("kernel", KERNELS, ids=KIDS)
+def test_deterministic(orc, kernel):
     wl = W.make_attention("det", 80, [900, 33, 1500], num_q_heads=16,
                           num_kv_heads=2, head_size=128, block_size=16)
-    a = gpu_attention(wl, pipelined=pipelined)
-    b = gpu_attention(wl, pipelined=pipelined)
+    a = gpu_attention(wl, kernel=kernel)
+    b = gpu_attention(wl, kernel=kernel)
     assert np.array_equal(a, b)
 
 
 def test_kernels_agree(orc):
-    """Both kernels on the same inputs, each within the bound of the
+    """The three kernels on the same inputs, each within the bound of the
     oracle."""
     wl = W.make_attention("agree", 81, [1, 200, 513, 2000, 64], num_q_heads=32,
                           num_kv_heads=4, head_size=128, block_size=16)
-    a = gpu_attention(wl)
-    b = gpu_attention(wl, pipelined=True)
     ref, mag = oracle_attention(orc, wl)
     vmax = _vmax(wl, wl.context_lens)
-    assert_close(a, ref, mag, vmax, "default")
-    assert_close(b, ref, mag, vmax, "pipelined")
+    for k, name in zip(KERNELS, KIDS):
+        assert_close(gpu_attention(wl, kernel=k), ref, mag, vmax, name)
 
 
-@pytest.mark.parametrize("pipelined", KERNELS, ids=KIDS)
-def test_clamped_context_and_flags(orc, pipelined):
+@pytest.mark.parametrize("kernel", KERNELS, ids=KIDS)
+def test_clamped_context_and_flags(orc, kernel):
     wl = W.make_attention("clamp", 90, [700, 100], num_q_heads=8,
                           num_kv_heads=1, head_size=128, block_size=16)
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     got = gpu_attention(wl, max_context_len=600, dev_error=err,
-                        pipelined=pipelined)
+                        kernel=kernel)
     assert int(err.item()) & kvq.KVQ_DEVERR_SEQ
     ref, mag = oracle_attention(orc, wl, np.array([600, 100], np.int32))
     assert_close(got, ref, mag, _vmax(wl, [600, 100]), "clamped")
@@ -266,7 +267,7 @@ def test_clamped_context_and_flags(orc, pipelined):
                            num_kv_heads=1, head_size=128, block_size=16)
     bad.block_table[0, 3] = bad.num_blocks + 5
     err.zero_()
-    got = gpu_attention(bad, dev_error=err, pipelined=pipelined)
+    got = gpu_attention(bad, dev_error=err, kernel=kernel)
     assert int(err.item()) & kvq.KVQ_DEVERR_BLOCK
     lens = np.array([48, 40], np.int32)
     ref, mag = oracle_attention(orc, bad, lens)
