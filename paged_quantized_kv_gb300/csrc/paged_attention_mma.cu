@@ -108,6 +108,19 @@ __device__ __forceinline__ void cp_async(uint32_t dst, const void* src,
                  : "memory");
 }
 
+// cp.async of `kBytes` that are all inside the source.
+template <int kBytes>
+__device__ __forceinline__ void cp_async_full(uint32_t dst, const void* src) {
+  if constexpr (kBytes == 16)
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst),
+                 "l"(src)
+                 : "memory");
+  else
+    asm volatile("cp.async.ca.shared.global [%0], [%1], %2;" ::"r"(dst),
+                 "l"(src), "n"(kBytes)
+                 : "memory");
+}
+
 __device__ __forceinline__ void cp_async_commit() {
   asm volatile("cp.async.commit_group;" ::: "memory");
 }
@@ -357,12 +370,15 @@ paged_attention_mma_kernel(const AttnParams p) {
     return ok;
   };
 
+  // bit e: the warp's block e0 + e has a valid id
+  const uint32_t bmask =
+      __ballot_sync(0xFFFFFFFFu, bt_lane >= 0 && bt_lane < p.num_blocks);
+
   // Whether token `tok` takes part (inside the range, valid block id);
   // every lane must call it.
   auto usable = [&](int tok) -> bool {
     const int idx = p.b_shift >= 0 ? (tok >> p.b_shift) : tok / p.B;
-    const int32_t blk = __shfl_sync(0xFFFFFFFFu, bt_lane, (idx - e0) & 31);
-    return tok < w1 && blk >= 0 && blk < p.num_blocks;
+    return tok < w1 && ((bmask >> ((idx - e0) & 31)) & 1u) != 0u;
   };
 
   // lane-constant byte offsets inside 16 contiguous tokens (kContig)
@@ -393,10 +409,31 @@ paged_attention_mma_kernel(const AttnParams p) {
                                   : 0) +
                              p.scale_off + kh * p.shs +
                              static_cast<int64_t>(T - idx * p.B) * 8;
-        const uint8_t* kd = kside + rel;
-        const uint8_t* ks = kside + srel;
-        const uint8_t* vd = vside + rel;
-        const uint8_t* vs = vside + srel;
+        const uint8_t* kd = kside + rel + kd_off;  // this lane's sources
+        const uint8_t* ks = kside + srel + ks_off;
+        const uint8_t* vd = vside + rel + vd_off;
+        const uint8_t* vs = vside + srel + vs_off;
+        if (bok && T + 16 <= w1) {  // all 16 tokens usable: no zero fill
+          const uint32_t d16 = st + lane * 16, d8 = st + lane * 8;
+          const uint32_t d4 = st + lane * 4;
+#pragma unroll
+          for (int r = 0; r < 2; ++r) {
+            cp_async_full<16>(d16 + kKdOff + (2 * h + r) * 512, kd + 512 * r);
+            cp_async_full<8>(d8 + kKsOff + (2 * h + r) * 256, ks + 64 * r);
+          }
+#pragma unroll
+          for (int q = 0; q < 2; ++q) {
+            cp_async_full<8>(d8 + kVdOff + (4 * h + 2 * q) * 256, vd + 512 * q);
+            cp_async_full<8>(d8 + kVdOff + (4 * h + 2 * q + 1) * 256,
+                             vd + 512 * q + 64);
+            cp_async_full<4>(d4 + kVsOff + (2 * h + q) * 128, vs + 64 * q);
+          }
+          continue;
+        }
+        kd -= kd_off;
+        ks -= ks_off;
+        vd -= vd_off;
+        vs -= vs_off;
 #pragma unroll
         for (int r = 0; r < 2; ++r) {  // K: tokens T + g + 8r
           const bool ok = bok && T + g + 8 * r < w1;
