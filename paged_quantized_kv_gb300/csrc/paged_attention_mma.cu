@@ -71,19 +71,30 @@ constexpr int kDepth = KVQ_ATTN_MMA_DEPTH;  // steps in flight per warp
 // One step's private slots of one warp, lane-contiguous per piece:
 //   K data  4 x 16 B (tokens g + 8j, bytes 16t .. 16t+15)
 //   V data  8 x  8 B (tokens 16h + {2t, 2t+1, 2t+8, 2t+9}, bytes 8g .. 8g+7)
-//   K scale 4 x  8 B (the 8-byte scale row holding groups 2t, 2t+1)
+//   K scale 4 x  8 B (the 8-byte scale row holding groups 2t, 2t+1), or
+//           4 x  4 B on contiguous pages with linear K scales (the word
+//           holding bytes 2t, 2t+1)
 //   V scale 4 x  4 B (the word holding group g of a token pair)
+// followed, after every warp's slots, by the query fragments of the CTA:
+// [n-block][i][lane] x 16 B = lane (g, t)'s dims 32t + 8i .. + 7 of query
+// head 8n + g as fp16.
 constexpr int kKdOff = 0;
 constexpr int kVdOff = kKdOff + 4 * 16 * 32;
 constexpr int kKsOff = kVdOff + 8 * 8 * 32;
-constexpr int kVsOff = kKsOff + 4 * 8 * 32;
-constexpr int kStageBytes = kVsOff + 4 * 4 * 32;     // 5632
-constexpr int kWarpBytes = kDepth * kStageBytes;
-constexpr int kSmemBytes = kWarps * kWarpBytes;
+template <bool kNarrowKs>
+struct Slots {
+  static constexpr int kKsBytes = kNarrowKs ? 4 : 8;
+  static constexpr int kVsOff = kKsOff + 4 * kKsBytes * 32;
+  static constexpr int kStage = kVsOff + 4 * 4 * 32;
+  static constexpr int kWarp = kDepth * kStage;
+  static constexpr int kQOff = kWarps * kWarp;
+  template <int NB>
+  static constexpr int smem() { return kQOff + NB * 4 * 32 * 16; }
+  // the merge buffers reuse the copy slots
+  static_assert(kQOff >= kWarps * 16 * kD * 4 + 2 * kWarps * 16 * 4, "");
+};
 constexpr float kLog2e = 1.4426950408889634f;
 
-static_assert(kSmemBytes >= kWarps * 16 * kD * 4 + 2 * kWarps * 16 * 4,
-              "the merge buffers reuse the copy slots");
 
 // ---------------------------------------------------------------------------
 // Small device helpers
@@ -278,6 +289,7 @@ template <int NG, bool kF16, bool kContig>
 __global__ void __launch_bounds__(kThreads, NG == 8 ? 4 : 2)
 paged_attention_mma_kernel(const AttnParams p) {
   constexpr int NB = NG / 8;  // n-blocks of 8 query heads
+  using SL = Slots<kContig>;  // contiguous pages have linear K scales
   extern __shared__ __align__(16) uint8_t smem[];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, t = lane & 3;
@@ -316,39 +328,32 @@ paged_attention_mma_kernel(const AttnParams p) {
       bt_lane = __ldg(p.block_table + b * p.bt_stride + e0 + lane);
   }
 
-  // query fragments: lane (g, t) holds dims 32t .. 32t+31 of head 8n + g
-  uint32_t qb[NB][8][2];
-#pragma unroll
-  for (int n = 0; n < NB; ++n) {
-    const int hq = 8 * n + g;
-    uint32_t w[16];
+  // query fragments into shared memory, once per CTA: entry (n, i, lane)
+  // = lane (g, t)'s dims 32t + 8i .. + 7 of head 8n + g, as fp16
+  const uint32_t qbase = smem_u32(smem) + SL::kQOff;
+  for (int e = tid; e < NB * 128; e += kThreads) {
+    const int n = e >> 7, i = (e >> 5) & 3, ln = e & 31;
+    const int hq = 8 * n + (ln >> 2);
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
     if (hq < p.G) {
-      const uint4* src = reinterpret_cast<const uint4*>(
-          p.q + b * p.q_stride0 + (kh * p.G + hq) * kD + 32 * t);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const uint4 v = __ldg(src + i);
-        w[4 * i] = v.x;
-        w[4 * i + 1] = v.y;
-        w[4 * i + 2] = v.z;
-        w[4 * i + 3] = v.w;
-      }
+      v = __ldg(reinterpret_cast<const uint4*>(
+          p.q + b * p.q_stride0 + (kh * p.G + hq) * kD + 32 * (ln & 3) +
+          8 * i));
       if constexpr (!kF16) {
-#pragma unroll
-        for (int i = 0; i < 16; ++i) w[i] = bf16x2_f16x2(w[i]);
+        v.x = bf16x2_f16x2(v.x);
+        v.y = bf16x2_f16x2(v.y);
+        v.z = bf16x2_f16x2(v.z);
+        v.w = bf16x2_f16x2(v.w);
       }
-    } else {
-#pragma unroll
-      for (int i = 0; i < 16; ++i) w[i] = 0u;
     }
-#pragma unroll
-    for (int s = 0; s < 8; ++s) {
-      qb[n][s][0] = w[2 * s];
-      qb[n][s][1] = w[2 * s + 1];
-    }
+    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(
+                     qbase + e * 16),
+                 "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                 : "memory");
   }
+  __syncthreads();
 
-  const uint32_t wbase = smem_u32(smem) + warp * kWarpBytes;
+  const uint32_t wbase = smem_u32(smem) + warp * SL::kWarp;
   const uint8_t* const kside = p.side[0];
   const uint8_t* const vside = p.side[1];
 
@@ -383,7 +388,7 @@ paged_attention_mma_kernel(const AttnParams p) {
 
   // lane-constant byte offsets inside 16 contiguous tokens (kContig)
   const int kd_off = g * 64 + 16 * t;  // + 512 for token g + 8
-  const int ks_off = p.swizzle_k ? ((g & ~3) + t) * 8 : g * 8;  // + 64
+  const int ks_off = g * 8 + (t >> 1) * 4;  // linear: + 64 for g + 8
   const int vd_off = (2 * t) * 64 + 8 * g;  // + 64 for 2t+1, + 512 for 8q
   const int vs_off = ((2 * t) & ~3) * 8 + (g >> 1) * 8 + (g & 1) * 4;
 
@@ -393,7 +398,7 @@ paged_attention_mma_kernel(const AttnParams p) {
     if (i >= nsteps) {
       // nothing to copy
     } else if constexpr (kContig) {
-      const uint32_t st = wbase + (i % kDepth) * kStageBytes;
+      const uint32_t st = wbase + (i % kDepth) * SL::kStage;
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         const int T = w0 + kStep * i + 16 * h;
@@ -419,14 +424,14 @@ paged_attention_mma_kernel(const AttnParams p) {
 #pragma unroll
           for (int r = 0; r < 2; ++r) {
             cp_async_full<16>(d16 + kKdOff + (2 * h + r) * 512, kd + 512 * r);
-            cp_async_full<8>(d8 + kKsOff + (2 * h + r) * 256, ks + 64 * r);
+            cp_async_full<4>(d4 + kKsOff + (2 * h + r) * 128, ks + 64 * r);
           }
 #pragma unroll
           for (int q = 0; q < 2; ++q) {
             cp_async_full<8>(d8 + kVdOff + (4 * h + 2 * q) * 256, vd + 512 * q);
             cp_async_full<8>(d8 + kVdOff + (4 * h + 2 * q + 1) * 256,
                              vd + 512 * q + 64);
-            cp_async_full<4>(d4 + kVsOff + (2 * h + q) * 128, vs + 64 * q);
+            cp_async_full<4>(d4 + SL::kVsOff + (2 * h + q) * 128, vs + 64 * q);
           }
           continue;
         }
@@ -440,7 +445,7 @@ paged_attention_mma_kernel(const AttnParams p) {
           const int j = 2 * h + r;
           cp_async<16>(st + kKdOff + j * 512 + lane * 16,
                        kd + kd_off + 512 * r, ok);
-          cp_async<8>(st + kKsOff + j * 256 + lane * 8, ks + ks_off + 64 * r,
+          cp_async<4>(st + kKsOff + j * 128 + lane * 4, ks + ks_off + 64 * r,
                       ok);
         }
 #pragma unroll
@@ -451,12 +456,12 @@ paged_attention_mma_kernel(const AttnParams p) {
                       vd + vd_off + 512 * q, bok && tok < w1);
           cp_async<8>(st + kVdOff + (piece + 1) * 256 + lane * 8,
                       vd + vd_off + 512 * q + 64, bok && tok + 1 < w1);
-          cp_async<4>(st + kVsOff + (2 * h + q) * 128 + lane * 4,
+          cp_async<4>(st + SL::kVsOff + (2 * h + q) * 128 + lane * 4,
                       vs + vs_off + 64 * q, bok && tok < w1);
         }
       }
     } else {
-      const uint32_t st = wbase + (i % kDepth) * kStageBytes;
+      const uint32_t st = wbase + (i % kDepth) * SL::kStage;
       const int T0 = w0 + kStep * i;
 #pragma unroll
       for (int j = 0; j < 4; ++j) {  // K: tokens T0 + g + 8j
@@ -482,7 +487,7 @@ paged_attention_mma_kernel(const AttnParams p) {
           cp_async<8>(st + kVdOff + piece * 256 + lane * 8, data + 8 * g, ok0);
           cp_async<8>(st + kVdOff + (piece + 1) * 256 + lane * 8,
                       data + p.dts + 8 * g, ok1);
-          cp_async<4>(st + kVsOff + (2 * h + q) * 128 + lane * 4,
+          cp_async<4>(st + SL::kVsOff + (2 * h + q) * 128 + lane * 4,
                       sc + static_cast<int64_t>((off & ~3) + (g >> 1)) * p.sts +
                           (g & 1) * 4,
                       ok0);
@@ -511,8 +516,10 @@ paged_attention_mma_kernel(const AttnParams p) {
   // g%4 because steps start at multiples of 32 and B % 4 == 0); V scales of
   // a token pair: bytes 2t%4, 2t%4 + 1 of the word
   const uint32_t ksel =
-      p.swizzle_k ? static_cast<uint32_t>((g & 3) | ((4 + (g & 3)) << 4))
-                  : static_cast<uint32_t>((2 * t) | ((2 * t + 1) << 4));
+      kContig ? static_cast<uint32_t>(((2 * t) & 3) | ((((2 * t) & 3) + 1) << 4))
+      : p.swizzle_k
+          ? static_cast<uint32_t>((g & 3) | ((4 + (g & 3)) << 4))
+          : static_cast<uint32_t>((2 * t) | ((2 * t + 1) << 4));
   const uint32_t vsel =
       static_cast<uint32_t>(((2 * t) & 3) | ((((2 * t) & 3) + 1) << 4));
 
@@ -522,10 +529,21 @@ paged_attention_mma_kernel(const AttnParams p) {
   for (int i = 0; i < nsteps; ++i) {
     issue(i + kDepth - 1);
     cp_async_wait<kDepth - 1>();
-    const uint32_t st = wbase + (i % kDepth) * kStageBytes;
+    const uint32_t st = wbase + (i % kDepth) * SL::kStage;
     const int T0 = w0 + kStep * i;
 
     // ---- logits S^T[16 tokens x 8 heads] of the two 16-token halves -------
+    uint32_t qb[NB][8][2];
+#pragma unroll
+    for (int n = 0; n < NB; ++n)
+#pragma unroll
+      for (int i4 = 0; i4 < 4; ++i4) {
+        const uint4 v = lds128(qbase + (n * 128 + i4 * 32 + lane) * 16);
+        qb[n][2 * i4][0] = v.x;
+        qb[n][2 * i4][1] = v.y;
+        qb[n][2 * i4 + 1][0] = v.z;
+        qb[n][2 * i4 + 1][1] = v.w;
+      }
     float sacc[2][NB][4];
     uint32_t kvalid = 0;  // bit j: K token T0 + g + 8j is usable
 #pragma unroll
@@ -535,8 +553,13 @@ paged_attention_mma_kernel(const AttnParams p) {
       for (int r = 0; r < 2; ++r) {
         const int j = 2 * h + r;
         const uint4 kd = lds128(st + kKdOff + j * 512 + lane * 16);
-        const uint2 ks = lds64(st + kKsOff + j * 256 + lane * 8);
-        const uint32_t pair = prmt(ks.x, ks.y, ksel);
+        uint32_t pair;
+        if constexpr (kContig) {
+          pair = prmt(lds32(st + kKsOff + j * 128 + lane * 4), 0u, ksel);
+        } else {
+          const uint2 ks = lds64(st + kKsOff + j * 256 + lane * 8);
+          pair = prmt(ks.x, ks.y, ksel);
+        }
         kvalid |= static_cast<uint32_t>(usable(T0 + g + 8 * j)) << j;
         const uint32_t sfp = e4m3x2_f16x2(pair);
         const uint32_t sfa = prmt(sfp, sfp, 0x1010u);
@@ -630,7 +653,8 @@ paged_attention_mma_kernel(const AttnParams p) {
       for (int q = 0; q < 2; ++q) {
         vd[q][0] = lds64(st + kVdOff + (4 * h + 2 * q) * 256 + lane * 8);
         vd[q][1] = lds64(st + kVdOff + (4 * h + 2 * q + 1) * 256 + lane * 8);
-        const uint32_t w = lds32(st + kVsOff + (2 * h + q) * 128 + lane * 4);
+        const uint32_t w =
+            lds32(st + SL::kVsOff + (2 * h + q) * 128 + lane * 4);
         // a token past the range may share the word: zero its scale (its
         // data are zero already), so no stray NaN code meets a zero weight
         const int tok = T0 + 16 * h + 8 * q + 2 * t;
@@ -747,12 +771,15 @@ cudaError_t launch_mma(const AttnParams& caller, cudaStream_t stream) {
   if (err != cudaSuccess) return err;
   if (!configured[dev & 63]) {
     err = cudaFuncSetAttribute(
-        kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+        kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        Slots<kContig>::template smem<NG / 8>());
     if (err != cudaSuccess) return err;
     configured[dev & 63] = true;
   }
   const dim3 grid(parts > 0 ? parts : 1, p.Hkv, p.num_seqs);
-  err = launch_kernel(kernel, grid, kThreads, kSmemBytes, stream, p.pdl, p);
+  err = launch_kernel(kernel, grid, kThreads,
+                      Slots<kContig>::template smem<NG / 8>(), stream, p.pdl,
+                      p);
   if (err != cudaSuccess || parts <= 1) return err;
   return launch_attention_merge(p, stream);
 }
@@ -760,7 +787,7 @@ cudaError_t launch_mma(const AttnParams& caller, cudaStream_t stream) {
 template <int NG, bool kF16>
 cudaError_t launch_layout(const AttnParams& p, cudaStream_t stream) {
   const bool contig = p.dts == kD / 2 && p.sts == kD / 16 &&
-                      p.B % 16 == 0;
+                      p.B % 16 == 0 && !p.swizzle_k;
   return contig ? launch_mma<NG, kF16, true>(p, stream)
                 : launch_mma<NG, kF16, false>(p, stream);
 }
