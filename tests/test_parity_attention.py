@@ -272,3 +272,14 @@ def test_clamped_context_and_flags(orc, kernel):
     lens = np.array([48, 40], np.int32)
     ref, mag = oracle_attention(orc, bad, lens)
     assert_close(got, ref, mag, _vmax(bad, lens), "bad block")
+
+
+@pytest.mark.parametrize("kernel", KERNELS, ids=KIDS)
+def test_long_contexts_many_partitions(orc, kernel):
+    """Contexts of several thousand tokens (up to 17 partitions of 512; the
+    default kernel's CTAs cover 1024 tokens each) with a max_context_len
+    above the longest context, so the scratch has more rows than used."""
+    wl = W.make_attention("long", 95, [4097, 8191, 3000, 1, 1024, 2048],
+                          num_q_heads=16, num_kv_heads=2, head_size=128,
+                          block_size=16)
+    _check(orc, wl, partition_size=512, max_context_len=9000, kernel=kernel)
