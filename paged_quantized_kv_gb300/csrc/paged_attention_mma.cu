@@ -368,10 +368,14 @@ paged_attention_mma_kernel(const AttnParams p) {
     const bool ok = in && blk >= 0 && blk < p.num_blocks;
     if (in && !ok && p.dev_error != nullptr)
       atomicOr(p.dev_error, KVQ_DEVERR_BLOCK);
-    const uint8_t* page =
-        side + (ok ? static_cast<int64_t>(blk) * p.page_stride : 0);
+    const uint8_t* page = side + static_cast<int64_t>(blk) * p.page_stride;
     data = page + kh * p.dhs + static_cast<int64_t>(off) * p.dts;
     sc = page + p.scale_off + kh * p.shs;
+    if (!ok) {  // zero-filled copy: point it at memory that surely exists
+      data = reinterpret_cast<const uint8_t*>(p.q);
+      sc = data;
+      off = 0;
+    }
     return ok;
   };
 
@@ -407,17 +411,19 @@ paged_attention_mma_kernel(const AttnParams p) {
         const bool bok = blk >= 0 && blk < p.num_blocks;
         if (T < w1 && !bok && t == 0 && g == 0 && p.dev_error != nullptr)
           atomicOr(p.dev_error, KVQ_DEVERR_BLOCK);
-        const int64_t rel = (bok ? static_cast<int64_t>(blk) * p.page_stride
-                                 : 0) +
+        const int64_t rel = static_cast<int64_t>(blk) * p.page_stride +
                             kh * p.dhs + static_cast<int64_t>(T - idx * p.B) * 64;
-        const int64_t srel = (bok ? static_cast<int64_t>(blk) * p.page_stride
-                                  : 0) +
+        const int64_t srel = static_cast<int64_t>(blk) * p.page_stride +
                              p.scale_off + kh * p.shs +
                              static_cast<int64_t>(T - idx * p.B) * 8;
-        const uint8_t* kd = kside + rel + kd_off;  // this lane's sources
-        const uint8_t* ks = kside + srel + ks_off;
-        const uint8_t* vd = vside + rel + vd_off;
-        const uint8_t* vs = vside + srel + vs_off;
+        // a bad block's copies are zero-filled from memory that surely
+        // exists (the query); in-range tokens past the context still lie
+        // inside their (valid) block
+        const uint8_t* qz = reinterpret_cast<const uint8_t*>(p.q);
+        const uint8_t* kd = bok ? kside + rel + kd_off : qz;
+        const uint8_t* ks = bok ? kside + srel + ks_off : qz;
+        const uint8_t* vd = bok ? vside + rel + vd_off : qz;
+        const uint8_t* vs = bok ? vside + srel + vs_off : qz;
         if (bok && T + 16 <= w1) {  // all 16 tokens usable: no zero fill
           const uint32_t d16 = st + lane * 16, d8 = st + lane * 8;
           const uint32_t d4 = st + lane * 4;
@@ -435,29 +441,25 @@ paged_attention_mma_kernel(const AttnParams p) {
           }
           continue;
         }
-        kd -= kd_off;
-        ks -= ks_off;
-        vd -= vd_off;
-        vs -= vs_off;
+        const int64_t dk = bok ? 1 : 0;  // lane offsets only inside a block
 #pragma unroll
         for (int r = 0; r < 2; ++r) {  // K: tokens T + g + 8r
           const bool ok = bok && T + g + 8 * r < w1;
           const int j = 2 * h + r;
-          cp_async<16>(st + kKdOff + j * 512 + lane * 16,
-                       kd + kd_off + 512 * r, ok);
-          cp_async<4>(st + kKsOff + j * 128 + lane * 4, ks + ks_off + 64 * r,
-                      ok);
+          cp_async<16>(st + kKdOff + j * 512 + lane * 16, kd + dk * 512 * r,
+                       ok);
+          cp_async<4>(st + kKsOff + j * 128 + lane * 4, ks + dk * 64 * r, ok);
         }
 #pragma unroll
         for (int q = 0; q < 2; ++q) {  // V: tokens T + 8q + 2t (+1)
           const int tok = T + 8 * q + 2 * t;
           const int piece = 4 * h + 2 * q;
           cp_async<8>(st + kVdOff + piece * 256 + lane * 8,
-                      vd + vd_off + 512 * q, bok && tok < w1);
+                      vd + dk * 512 * q, bok && tok < w1);
           cp_async<8>(st + kVdOff + (piece + 1) * 256 + lane * 8,
-                      vd + vd_off + 512 * q + 64, bok && tok + 1 < w1);
+                      vd + dk * (512 * q + 64), bok && tok + 1 < w1);
           cp_async<4>(st + SL::kVsOff + (2 * h + q) * 128 + lane * 4,
-                      vs + vs_off + 64 * q, bok && tok < w1);
+                      vs + dk * 64 * q, bok && tok < w1);
         }
       }
     } else {
