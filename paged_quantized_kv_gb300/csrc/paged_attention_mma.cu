@@ -17,14 +17,18 @@
 // tile's critical path; mma.sync.m16n8k16 runs at 2 cycles per instruction
 // per SM with its operands already in registers and needs no handshake.
 //
-// Design, per CTA of 4 warps = one (partition of <= 512 tokens, KV head,
-// sequence); warp w owns a quarter of the partition and walks it in steps
-// of 32 tokens:
+// Design, per CTA of 4 warps = one (stretch of context, KV head, sequence):
+// a stretch is KVQ_ATTN_MMA_PART (1024) tokens on contiguous pages (HND,
+// block_size % 16 == 0, linear K scales), else the caller's partition
+// (<= 512); its tokens are split evenly over the warps, which walk them in
+// steps of 32 tokens:
 //   * Loads: every thread copies, with cp.async (zero-filled for tokens past
 //     the context or with a bad block id), exactly the bytes its own MMA
 //     fragments need into a private shared-memory slot, kDepth steps ahead;
 //     the warp waits with cp.async.wait_group only.  Block ids of the warp's
-//     range are loaded once (one per lane) and shuffled.
+//     range are loaded once (one per lane) and shuffled; on contiguous pages
+//     one block id and lane-constant offsets serve 16 tokens.  The query
+//     fragments are staged in shared memory once per CTA.
 //   * Logits S^T[16 tokens x 8 heads] = K' Q'^T per n-block of 8 query
 //     heads: A = K' (rows = tokens), B = Q'^T (k = head dims).  The head
 //     dims are permuted (the same way for K and Q): in k-step s, lane
@@ -42,9 +46,11 @@
 //   * O^T[16 dims x 8 heads] += V'^T P^T per m-block of 16 head dims, the
 //     dims permuted so that lane (g, t) reads the 8 contiguous bytes
 //     8g .. 8g+7 (group g) of each of its 4 tokens.
-//   * The 4 warps' (max, sum, O) merge in shared memory; a partition of a
-//     longer context is written to the caller's scratch and merged by the
-//     partition-merge kernel.
+//   * The 4 warps' (max, sum, O) merge in shared memory; a stretch of a
+//     longer context is written to the caller's scratch (rows max_parts
+//     apart, as for the caller's partitions: a stretch covers at least one
+//     partition, so fewer rows are used) and merged by the partition-merge
+//     kernel.
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdint.h>
