@@ -340,6 +340,9 @@ def run_ours(args):
     icache = torch.empty((iw.num_blocks, iw.block_size, iw.head_dim + 4),
                          dtype=torch.uint8, device=dev)
     istore_ms = span_ms(lambda i: kvq.kvq_store_indexer_k(
+        ik[i % GATHER_SETS], icache, islots, flags=kvq.KVQ_F_PDL_EARLY_READ,
+        dev_error=dev_err, stream=sh), K)
+    istore_pdl_ms = span_ms(lambda i: kvq.kvq_store_indexer_k(
         ik[i % GATHER_SETS], icache, islots, flags=PDL, dev_error=dev_err,
         stream=sh), K)
     istore_bytes = iw.algorithmic_bytes()
@@ -457,8 +460,11 @@ def run_ours(args):
         "store_indexer_k": {
             "note": "write side of the indexer cache on the gather's shape "
                     "(131072 tokens, head_dim 128, block_size 64), not part "
-                    "of the step",
+                    "of the step; back to back with KVQ_F_PDL_EARLY_READ "
+                    "(K rotated over the buffer sets, the kernel before "
+                    "writes only the cache)",
             "ms": round(istore_ms, 5),
+            "pdl_only_ms": round(istore_pdl_ms, 5),
             "GB_s": round(istore_bytes / istore_ms / 1e6, 1),
             "frac_of_peak": round(istore_bytes / istore_ms / 1e6 / peak, 4),
             "tokens_per_s": round(iw.num_tokens / (istore_ms / 1e3), 1),

@@ -95,12 +95,13 @@ enum {
      so the kernel stages them while that kernel finishes and waits only
      before it reads the cache or the scales, or writes anything. */
   KVQ_F_PDL_EARLY_META = 1u << 2,
-  /* kvq_gather_indexer_k only; implies KVQ_F_PDL_EARLY_META.  The caller
-     promises that the kernel that runs just before this call on the stream
-     writes none of this call's inputs (kv_cache, block_table, cu_seq_lens):
-     the kernel then also issues its cache reads while that kernel finishes
-     and waits for it only before its first write (its outputs and
-     dev_error are still written strictly after it). */
+  /* kvq_gather_indexer_k (implies KVQ_F_PDL_EARLY_META) and
+     kvq_store_indexer_k (implies KVQ_F_PDL).  The caller promises that the
+     kernel that runs just before this call on the stream writes none of
+     this call's inputs (gather: kv_cache, block_table, cu_seq_lens; store:
+     k, slot_mapping): the kernel then also issues its first reads while
+     that kernel finishes and waits for it only before its first write (its
+     outputs and dev_error are still written strictly after it). */
   KVQ_F_PDL_EARLY_READ = 1u << 4,
   /* kvq_paged_attention_nvfp4 only: run the persistent, warp-specialised
      tcgen05 kernel (one CTA per SM, K' in tensor memory, a dedicated MMA
@@ -288,7 +289,7 @@ kvq_status kvq_load_nvfp4(const uint8_t* key_cache, const uint8_t* value_cache,
  *               block_stride bytes apart (multiple of 16, >= block_size *
  *               (head_dim + 4)); 16-byte aligned.
  * slot_mapping  int64 [num_tokens], distinct slots (duplicates race).
- * flags         KVQ_F_PDL or 0.
+ * flags         KVQ_F_PDL, KVQ_F_PDL_EARLY_READ, or 0.
  * dev_error     nullable (KVQ_DEVERR_SLOT for slots >= num_blocks *
  *               block_size, which are skipped).
  * num_tokens == 0 returns KVQ_OK without launching.

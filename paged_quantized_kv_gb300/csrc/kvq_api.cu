@@ -310,7 +310,9 @@ kvq_status kvq_store_indexer_k(const void* k, int64_t k_stride0,
                                int32_t* dev_error, void* stream) {
   using namespace kvq;
   if (dtype != KVQ_DTYPE_BF16 && dtype != KVQ_DTYPE_FP16) return KVQ_ERR_DTYPE;
-  if ((flags & ~static_cast<uint32_t>(KVQ_F_PDL)) != 0u) return KVQ_ERR_ARG;
+  if ((flags & ~static_cast<uint32_t>(KVQ_F_PDL | KVQ_F_PDL_EARLY_READ)) !=
+      0u)
+    return KVQ_ERR_ARG;
   if (num_tokens < 0 || block_size <= 0 || num_blocks < 0 || k_stride0 < 0)
     return KVQ_ERR_SHAPE;
   if (head_dim != 16 && head_dim != 32 && head_dim != 64 && head_dim != 128 &&
@@ -337,7 +339,8 @@ kvq_status kvq_store_indexer_k(const void* k, int64_t k_stride0,
   p.B = block_size;
   p.b_shift = ilog2_exact(block_size);
   p.f16 = dtype == KVQ_DTYPE_FP16;
-  p.pdl = (flags & KVQ_F_PDL) != 0u;
+  p.early_read = (flags & KVQ_F_PDL_EARLY_READ) != 0u;
+  p.pdl = p.early_read || (flags & KVQ_F_PDL) != 0u;
   p.vec32 = aligned(k, 32) && k_stride0 % 16 == 0;
   const cudaError_t err =
       launch_store_indexer_k(p, static_cast<cudaStream_t>(stream));

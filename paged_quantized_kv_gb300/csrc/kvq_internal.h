@@ -104,6 +104,7 @@ struct IndexerStoreParams {
   int32_t D, B, b_shift;
   bool f16, pdl;
   bool vec32;              // rows start 32-byte aligned (256-bit loads)
+  bool early_read;         // load the first rows before waiting (PDL)
 };
 
 cudaError_t launch_store_indexer_k(const IndexerStoreParams& p,

@@ -162,10 +162,16 @@ __device__ __noinline__ uint4 codes16_exact(uint4 w0, uint4 w1,
   return make_uint4(c[0], c[1], c[2], c[3]);
 }
 
-template <bool kF16, int L>
+// kEarlyRead (KVQ_F_PDL_EARLY_READ): the first iteration's slot and row
+// loads go out before the wait on the predecessor kernel; every write
+// (cache bytes, dev_error) comes after it.  A thread with no token writes
+// nothing and needs no wait.  Measured back to back on the long-context
+// shape: 10.2 us with the wait first, 9.0 us with the reads first.
+template <bool kF16, int L, bool kEarlyRead>
 __global__ void __launch_bounds__(kThreads)
 store_indexer_k_kernel(const IndexerStoreParams p) {
-  pdl_prologue();
+  if constexpr (!kEarlyRead) pdl_prologue();
+  bool waited = !kEarlyRead;
   constexpr int kTokPerWarp = 32 / L;
   const int lane = threadIdx.x & 31;
   const int sub = lane / L;      // token slot inside the warp
@@ -191,6 +197,10 @@ store_indexer_k_kernel(const IndexerStoreParams p) {
         slot[u] = ld_nc_s64(p.slots + t);
         load16(p.k + t * p.k_stride0 + part * 16, raw[u], p.vec32);
       }
+    }
+    if (!waited) {  // reads of the first tokens are in flight
+      pdl_prologue();
+      waited = true;
     }
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
@@ -257,7 +267,7 @@ store_indexer_k_kernel(const IndexerStoreParams p) {
   }
 }
 
-template <bool kF16, int L>
+template <bool kF16, int L, bool kEarlyRead>
 cudaError_t launch(const IndexerStoreParams& p, cudaStream_t stream) {
   static int ctas_per_sm[64] = {0};
   int dev = 0;
@@ -266,7 +276,7 @@ cudaError_t launch(const IndexerStoreParams& p, cudaStream_t stream) {
   int& occ = ctas_per_sm[dev & 63];
   if (occ == 0) {
     err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-        &occ, store_indexer_k_kernel<kF16, L>, kThreads, 0);
+        &occ, store_indexer_k_kernel<kF16, L, kEarlyRead>, kThreads, 0);
     if (err != cudaSuccess) return err;
     if (occ < 1) occ = 1;
   }
@@ -278,19 +288,19 @@ cudaError_t launch(const IndexerStoreParams& p, cudaStream_t stream) {
       (p.num_tokens + resident * per_cta - 1) / (resident * per_cta);
   int64_t grid = (p.num_tokens + iters * per_cta - 1) / (iters * per_cta);
   if (grid < 1) grid = 1;
-  return launch_kernel(store_indexer_k_kernel<kF16, L>,
+  return launch_kernel(store_indexer_k_kernel<kF16, L, kEarlyRead>,
                        static_cast<unsigned>(grid), kThreads, 0, stream,
                        p.pdl, p);
 }
 
-template <bool kF16>
+template <bool kF16, bool kEarlyRead>
 cudaError_t launch_dim(const IndexerStoreParams& p, cudaStream_t stream) {
   switch (p.D) {  // L = head_dim / 16 lanes per token
-    case 16: return launch<kF16, 1>(p, stream);
-    case 32: return launch<kF16, 2>(p, stream);
-    case 64: return launch<kF16, 4>(p, stream);
-    case 128: return launch<kF16, 8>(p, stream);
-    default: return launch<kF16, 16>(p, stream);  // 256
+    case 16: return launch<kF16, 1, kEarlyRead>(p, stream);
+    case 32: return launch<kF16, 2, kEarlyRead>(p, stream);
+    case 64: return launch<kF16, 4, kEarlyRead>(p, stream);
+    case 128: return launch<kF16, 8, kEarlyRead>(p, stream);
+    default: return launch<kF16, 16, kEarlyRead>(p, stream);  // 256
   }
 }
 
@@ -298,7 +308,11 @@ cudaError_t launch_dim(const IndexerStoreParams& p, cudaStream_t stream) {
 
 cudaError_t launch_store_indexer_k(const IndexerStoreParams& p,
                                    cudaStream_t stream) {
-  return p.f16 ? launch_dim<true>(p, stream) : launch_dim<false>(p, stream);
+  if (p.early_read)
+    return p.f16 ? launch_dim<true, true>(p, stream)
+                 : launch_dim<false, true>(p, stream);
+  return p.f16 ? launch_dim<true, false>(p, stream)
+               : launch_dim<false, false>(p, stream);
 }
 
 }  // namespace kvq

@@ -230,3 +230,34 @@ def test_quotients_within_an_ulp_of_a_midpoint(orc):
         block_table=np.arange(T // 16, dtype=np.int32)[None, :],
         cu_seq_lens=np.array([0, T], np.int32))
     _compare(orc, wl)
+
+
+def test_long_context_early_read(orc):
+    """KVQ_F_PDL_EARLY_READ: the first rows are loaded before the wait on
+    the predecessor, every write after it -- same bytes as the oracle."""
+    wl = W.make_indexer_store("long_er", 88, [512] * 256, 64, 128, 8192)
+    cache, err = _gpu(wl, flags=kvq.KVQ_F_PDL_EARLY_READ)
+    assert err == 0
+    assert_bytes_equal(cache.cpu().numpy().reshape(-1), _oracle(orc, wl),
+                       wl.name)
+
+
+def test_early_read_chain_of_stores(orc):
+    """Early-read stores back to back into the same slots, alternating two
+    inputs (the kernel before each writes the cache, none of its inputs):
+    the cache holds exactly the last store's bytes."""
+    a = W.make_indexer_store("a", 89, [512] * 64, 64, 128, 1024)
+    b = W.make_indexer_store("b", 90, [512] * 64, 64, 128, 1024)
+    b.slot_mapping = a.slot_mapping.copy()
+    ks = [torch.from_numpy(w.k.view(np.int16)).cuda().view(torch.bfloat16)
+          for w in (a, b)]
+    cache = torch.full((a.num_blocks, a.block_size, a.head_dim + 4), 0xAA,
+                       dtype=torch.uint8, device="cuda")
+    sm = to_dev(a.slot_mapping)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    for i in range(7):
+        kvq.kvq_store_indexer_k(ks[i % 2], cache, sm,
+                                flags=kvq.KVQ_F_PDL_EARLY_READ, dev_error=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert_bytes_equal(cache.cpu().numpy().reshape(-1), _oracle(orc, a), "a")
