@@ -255,8 +255,8 @@ def run_ours(args):
                                  dev_error=dev_err, stream=sh)
 
     def step(i, flags):
-        store(flags)
-        gather(i, flags | (kvq.KVQ_F_PDL_EARLY_READ if flags else 0))
+        store(kvq.KVQ_F_PDL_EARLY_READ if flags else 0)
+        gather(i, kvq.KVQ_F_PDL_EARLY_READ if flags else 0)
 
     def span_ms(fn, count):
         """Mean GPU time per call of `count` back-to-back calls between two
@@ -297,7 +297,8 @@ def run_ours(args):
     # per-kernel averages: each kernel alone, back to back (inputs larger
     # than L2: the store streams 689 MB per call; the gather rotates over
     # GATHER_SETS buffer sets)
-    store_ms = span_ms(lambda i: store(PDL), K)
+    store_ms = span_ms(lambda i: store(kvq.KVQ_F_PDL_EARLY_READ), K)
+    store_pdl_ms = span_ms(lambda i: store(PDL), K)
     gather_ms = span_ms(lambda i: gather(i, kvq.KVQ_F_PDL_EARLY_READ), K)
     gather_meta_ms = span_ms(lambda i: gather(i, kvq.KVQ_F_PDL_EARLY_META), K)
     plain = {"step_ms": span_ms(lambda i: step(i, 0), K),
@@ -416,10 +417,10 @@ def run_ours(args):
                   f"{GATHER_SETS * 35} MB in all), so no launch finds its "
                   "data in L2",
             "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
-            "timing": "K steps (store with KVQ_F_PDL, gather with "
-                      "KVQ_F_PDL_EARLY_READ: none of its inputs -- indexer "
-                      "cache, block table, cu_seq_lens -- is written by the "
-                      "store before it) back to back on one stream "
+            "timing": "K steps (store and gather both with "
+                      "KVQ_F_PDL_EARLY_READ: the gather writes none of the "
+                      "store's inputs, the store none of the gather's) back "
+                      "to back on one stream "
                       "between two CUDA events, all K queued behind a GPU "
                       "sleep before the first event (so the binding's host "
                       "time per call does not pace the GPU); ms_per_step = "
@@ -431,6 +432,7 @@ def run_ours(args):
         "kernels": {
             "store_nvfp4": {
                 "ms": round(store_ms, 5),
+                "pdl_only_ms": round(store_pdl_ms, 5),
                 "GB_s": round(store_gbs, 1),
                 "frac_of_peak": round(store_gbs / peak, 4),
                 "tokens_per_s": round(T / (store_ms / 1e3), 1),

@@ -95,13 +95,15 @@ enum {
      so the kernel stages them while that kernel finishes and waits only
      before it reads the cache or the scales, or writes anything. */
   KVQ_F_PDL_EARLY_META = 1u << 2,
-  /* kvq_gather_indexer_k (implies KVQ_F_PDL_EARLY_META) and
-     kvq_store_indexer_k (implies KVQ_F_PDL).  The caller promises that the
+  /* kvq_gather_indexer_k (implies KVQ_F_PDL_EARLY_META), kvq_store_nvfp4
+     and kvq_store_indexer_k (imply KVQ_F_PDL).  The caller promises that the
      kernel that runs just before this call on the stream writes none of
-     this call's inputs (gather: kv_cache, block_table, cu_seq_lens; store:
-     k, slot_mapping): the kernel then also issues its first reads while
-     that kernel finishes and waits for it only before its first write (its
-     outputs and dev_error are still written strictly after it). */
+     this call's inputs (gather: kv_cache, block_table, cu_seq_lens;
+     store_nvfp4: key, value, slot_mapping, k_scale, v_scale;
+     store_indexer_k: k, slot_mapping): the kernel then also issues its
+     first reads while that kernel finishes and waits for it only before its
+     first write (its outputs and dev_error are still written strictly after
+     it). */
   KVQ_F_PDL_EARLY_READ = 1u << 4,
   /* kvq_paged_attention_nvfp4 only: run the persistent, warp-specialised
      tcgen05 kernel (one CTA per SM, K' in tensor memory, a dedicated MMA
@@ -167,7 +169,8 @@ enum {
  * slot_mapping    int64 [num_tokens]; distinct non-negative slots
  *                 (duplicates race; the result is then unspecified).
  * k_scale, v_scale  device fp32 scalars, finite and > 0.
- * flags           KVQ_F_SWIZZLE_K_SCALE | KVQ_F_PDL, or 0.
+ * flags           KVQ_F_SWIZZLE_K_SCALE, KVQ_F_PDL or KVQ_F_PDL_EARLY_READ,
+ *                 or 0.
  * dev_error       nullable device int32 (KVQ_DEVERR_SLOT).
  * stream          cudaStream_t.
  * num_tokens == 0 returns KVQ_OK without launching.

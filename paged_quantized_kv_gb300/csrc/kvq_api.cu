@@ -61,7 +61,8 @@ kvq_status kvq_store_nvfp4(const void* key, int64_t key_stride0,
   if (dtype != KVQ_DTYPE_BF16 && dtype != KVQ_DTYPE_FP16) return KVQ_ERR_DTYPE;
   if (layout != KVQ_LAYOUT_HND && layout != KVQ_LAYOUT_NHD)
     return KVQ_ERR_LAYOUT;
-  if ((flags & ~static_cast<uint32_t>(KVQ_F_SWIZZLE_K_SCALE | KVQ_F_PDL)) !=
+  if ((flags & ~static_cast<uint32_t>(KVQ_F_SWIZZLE_K_SCALE | KVQ_F_PDL |
+                                      KVQ_F_PDL_EARLY_READ)) !=
       0u)
     return KVQ_ERR_ARG;
   if (num_tokens < 0 || num_heads <= 0 || head_size <= 0 || block_size <= 0 ||
@@ -136,7 +137,8 @@ kvq_status kvq_store_nvfp4(const void* key, int64_t key_stride0,
   if (passes >= (int64_t{1} << 31)) return KVQ_ERR_SHAPE;
   p.num_passes = static_cast<int32_t>(passes);
   p.swizzle_sides = 2u | ((flags & KVQ_F_SWIZZLE_K_SCALE) ? 1u : 0u);
-  p.pdl = (flags & KVQ_F_PDL) != 0u;
+  p.early_read = (flags & KVQ_F_PDL_EARLY_READ) != 0u;
+  p.pdl = p.early_read || (flags & KVQ_F_PDL) != 0u;
   p.f16 = dtype == KVQ_DTYPE_FP16;
 
   const cudaError_t err =

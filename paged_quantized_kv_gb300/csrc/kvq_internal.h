@@ -31,6 +31,7 @@ struct StoreParams {
   int32_t num_passes;
   uint32_t swizzle_sides;  // bit s set: side s's scales are swizzled
   bool pdl;                // launch with programmatic dependent launch
+  bool early_read;         // load the first groups before waiting (PDL)
   bool f16;                // inputs are IEEE fp16 (else bf16)
 };
 

@@ -193,12 +193,19 @@ __device__ __forceinline__ void st_v2(uint8_t* p, uint32_t a, uint32_t b) {
                : "memory");
 }
 
-template <bool kVec32, bool kF16>
+// kEarlyRead (KVQ_F_PDL_EARLY_READ): the scale table and the first
+// iteration's slot and row loads happen before the wait on the predecessor
+// kernel; every write (cache bytes, dev_error) after it.  An idle role
+// writes nothing and needs no wait.  Measured back to back on the
+// long-context store: 105.5 us with the wait first, 102.8 us with the reads
+// first (the step with the early-read gather: 110.0 -> 108.0 us).
+template <bool kVec32, bool kF16, bool kEarlyRead>
 __global__ void __launch_bounds__(kThreads, KVQ_STORE_MIN_BLOCKS)
 store_nvfp4_kernel(const StoreParams p) {
   __shared__ float s_ratio[2][256];  // g_side / float(e4m3 code)
 
-  pdl_prologue();
+  if constexpr (!kEarlyRead) pdl_prologue();
+  bool waited = !kEarlyRead;
   const int tid = threadIdx.x;
   {
     const float g0 = __fdiv_rn(1.0f, __ldg(p.scale[0]));
@@ -258,6 +265,10 @@ store_nvfp4_kernel(const StoreParams p) {
         load_group<kVec32>(src_role + t * src_stride, w[u]);
       }
     }
+    if (!waited) {  // reads of the first tokens are in flight
+      pdl_prologue();
+      waited = true;
+    }
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
       if (slot[u] < 0) continue;  // skipped token, or past the end
@@ -306,7 +317,7 @@ store_nvfp4_kernel(const StoreParams p) {
   }
 }
 
-template <bool kVec32, bool kF16>
+template <bool kVec32, bool kF16, bool kEarlyRead>
 cudaError_t launch(const StoreParams& p, cudaStream_t stream) {
   static int ctas_per_sm[64] = {0};
   int dev = 0;
@@ -315,7 +326,7 @@ cudaError_t launch(const StoreParams& p, cudaStream_t stream) {
   int& occ = ctas_per_sm[dev & 63];
   if (occ == 0) {
     err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-        &occ, store_nvfp4_kernel<kVec32, kF16>, kThreads, 0);
+        &occ, store_nvfp4_kernel<kVec32, kF16, kEarlyRead>, kThreads, 0);
     if (err != cudaSuccess) return err;
     if (occ < 1) occ = 1;
   }
@@ -324,7 +335,7 @@ cudaError_t launch(const StoreParams& p, cudaStream_t stream) {
   if (grid > p.num_passes) grid = p.num_passes;
   grid = (grid / slices) * slices;  // every CTA keeps one slice of a token
   if (grid < slices) grid = slices;
-  return launch_kernel(store_nvfp4_kernel<kVec32, kF16>,
+  return launch_kernel(store_nvfp4_kernel<kVec32, kF16, kEarlyRead>,
                        static_cast<unsigned>(grid), kThreads, 0, stream,
                        p.pdl, p);
 }
@@ -337,9 +348,18 @@ cudaError_t launch_store_nvfp4(const StoreParams& p, cudaStream_t stream) {
       (reinterpret_cast<uintptr_t>(p.src[0]) % 32 == 0) &&
       (reinterpret_cast<uintptr_t>(p.src[1]) % 32 == 0) &&
       (p.src_stride[0] % 16 == 0) && (p.src_stride[1] % 16 == 0);
+  if (p.early_read) {
+    if (p.f16)
+      return vec32 ? launch<true, true, true>(p, stream)
+                   : launch<false, true, true>(p, stream);
+    return vec32 ? launch<true, false, true>(p, stream)
+                 : launch<false, false, true>(p, stream);
+  }
   if (p.f16)
-    return vec32 ? launch<true, true>(p, stream) : launch<false, true>(p, stream);
-  return vec32 ? launch<true, false>(p, stream) : launch<false, false>(p, stream);
+    return vec32 ? launch<true, true, false>(p, stream)
+                 : launch<false, true, false>(p, stream);
+  return vec32 ? launch<true, false, false>(p, stream)
+               : launch<false, false, false>(p, stream);
 }
 
 }  // namespace kvq

@@ -198,3 +198,50 @@ def test_early_read_gather_after_torch_write(orc):
     wk, ws = run_gather(orc, ga)
     assert_bytes_equal(k.cpu().numpy().reshape(-1), wk, "k")
     assert_bytes_equal(s.cpu().numpy().reshape(-1), ws, "s")
+
+
+@pytest.mark.parametrize("index", [0, 4])
+def test_early_read_step(orc, index):
+    """The bench's step with both calls in early-read mode, three times back
+    to back: each store's inputs are not written by the gather before it,
+    and each gather's inputs are not written by the store before it."""
+    st = W.store_workload(index)
+    ga = W.gather_workload(index)
+    key, value, slots, ks, vs = store_inputs(st)
+    kv, kc, vc = kvq.alloc_nvfp4_cache(st.num_blocks, st.block_size,
+                                       st.num_heads, st.head_size, fill=0xAA)
+    cache, k, s, bt, cu = _gather_args(ga)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    for _ in range(3):
+        kvq.kvq_store_nvfp4(key, value, kc, vc, slots, ks, vs,
+                            flags=EARLY_READ, dev_error=err)
+        kvq.kvq_gather_indexer_k(cache, k, s, bt, cu,
+                                 block_size=ga.block_size, flags=EARLY_READ,
+                                 dev_error=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert_bytes_equal(kv.cpu().numpy().reshape(-1), run_store(orc, st),
+                       st.name)
+    wk, ws = run_gather(orc, ga)
+    assert_bytes_equal(k.cpu().numpy().reshape(-1), wk, ga.name + " k")
+    assert_bytes_equal(s.cpu().numpy().reshape(-1), ws, ga.name + " s")
+
+
+def test_early_read_chain_of_stores(orc):
+    """Early-read stores alternating two inputs into the same slots 9
+    times: each store's writes still follow its predecessor's, so the pages
+    hold exactly the last store's result."""
+    a = W.make_store("a", 44, 4096, 4, 256, 32, 128, slots="runs",
+                     request_len=512)
+    b = W.make_store("b", 45, 4096, 4, 256, 32, 128, slots="runs",
+                     request_len=512)
+    b.slot_mapping = a.slot_mapping.copy()
+    ins = [store_inputs(a), store_inputs(b)]
+    kv, kc, vc = kvq.alloc_nvfp4_cache(a.num_blocks, a.block_size,
+                                       a.num_heads, a.head_size, fill=0xAA)
+    for i in range(9):
+        key, value, slots, ks, vs = ins[i % 2]
+        kvq.kvq_store_nvfp4(key, value, kc, vc, slots, ks, vs,
+                            flags=EARLY_READ)
+    torch.cuda.synchronize()
+    assert_bytes_equal(kv.cpu().numpy().reshape(-1), run_store(orc, a), "a")
