@@ -541,26 +541,19 @@ paged_attention_mma_kernel(const AttnParams p) {
     const int T0 = w0 + kStep * i;
 
     // ---- logits S^T[16 tokens x 8 heads] of the two 16-token halves -------
-    uint32_t qb[NB][8][2];
-#pragma unroll
-    for (int n = 0; n < NB; ++n)
-#pragma unroll
-      for (int i4 = 0; i4 < 4; ++i4) {
-        const uint4 v = lds128(qbase + (n * 128 + i4 * 32 + lane) * 16);
-        qb[n][2 * i4][0] = v.x;
-        qb[n][2 * i4][1] = v.y;
-        qb[n][2 * i4 + 1][0] = v.z;
-        qb[n][2 * i4 + 1][1] = v.w;
-      }
+    // word by word: the query fragments of two k-steps (one 16-byte shared
+    // load), the two tokens' e2m1 words dequantised, two MMAs -- few
+    // registers live at a time
     float sacc[2][NB][4];
     uint32_t kvalid = 0;  // bit j: K token T0 + g + 8j is usable
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
-      uint32_t a[2][8][2];  // [row g / g+8][k-step][a0|a2 or a1|a3]
+      uint4 kd[2];
+      uint32_t sfw[2][2];  // [row][groups 2t | 2t+1] scale as f16x2
 #pragma unroll
       for (int r = 0; r < 2; ++r) {
         const int j = 2 * h + r;
-        const uint4 kd = lds128(st + kKdOff + j * 512 + lane * 16);
+        kd[r] = lds128(st + kKdOff + j * 512 + lane * 16);
         uint32_t pair;
         if constexpr (kContig) {
           pair = prmt(lds32(st + kKsOff + j * 128 + lane * 4), 0u, ksel);
@@ -570,37 +563,35 @@ paged_attention_mma_kernel(const AttnParams p) {
         }
         kvalid |= static_cast<uint32_t>(usable(T0 + g + 8 * j)) << j;
         const uint32_t sfp = e4m3x2_f16x2(pair);
-        const uint32_t sfa = prmt(sfp, sfp, 0x1010u);
-        const uint32_t sfb = prmt(sfp, sfp, 0x3232u);
-        uint32_t x[4];
-        dequant_word(kd.x, sfa, x);
-        a[r][0][0] = x[0]; a[r][0][1] = x[1];
-        a[r][1][0] = x[2]; a[r][1][1] = x[3];
-        dequant_word(kd.y, sfa, x);
-        a[r][2][0] = x[0]; a[r][2][1] = x[1];
-        a[r][3][0] = x[2]; a[r][3][1] = x[3];
-        dequant_word(kd.z, sfb, x);
-        a[r][4][0] = x[0]; a[r][4][1] = x[1];
-        a[r][5][0] = x[2]; a[r][5][1] = x[3];
-        dequant_word(kd.w, sfb, x);
-        a[r][6][0] = x[0]; a[r][6][1] = x[1];
-        a[r][7][0] = x[2]; a[r][7][1] = x[3];
+        sfw[r][0] = prmt(sfp, sfp, 0x1010u);
+        sfw[r][1] = prmt(sfp, sfp, 0x3232u);
       }
+      // two accumulators (even / odd k-steps) halve the dependent chain
+      float e2[NB][4];
 #pragma unroll
-      for (int n = 0; n < NB; ++n) {
-        // two accumulators (even / odd k-steps) halve the dependent chain
-        float e2[4] = {0.f, 0.f, 0.f, 0.f};
-        sacc[h][n][0] = sacc[h][n][1] = sacc[h][n][2] = sacc[h][n][3] = 0.f;
+      for (int n = 0; n < NB; ++n)
 #pragma unroll
-        for (int s = 0; s < 8; s += 2) {
-          mma16816(sacc[h][n], a[0][s][0], a[1][s][0], a[0][s][1],
-                   a[1][s][1], qb[n][s][0], qb[n][s][1]);
-          mma16816(e2, a[0][s + 1][0], a[1][s + 1][0], a[0][s + 1][1],
-                   a[1][s + 1][1], qb[n][s + 1][0], qb[n][s + 1][1]);
+        for (int r = 0; r < 4; ++r) sacc[h][n][r] = e2[n][r] = 0.f;
+#pragma unroll
+      for (int wd = 0; wd < 4; ++wd) {  // word wd: k-steps 2wd, 2wd+1
+        uint32_t x0[4], x1[4];
+        const uint32_t w0 = wd == 0 ? kd[0].x : wd == 1 ? kd[0].y
+                            : wd == 2 ? kd[0].z : kd[0].w;
+        const uint32_t w1r = wd == 0 ? kd[1].x : wd == 1 ? kd[1].y
+                             : wd == 2 ? kd[1].z : kd[1].w;
+        dequant_word(w0, sfw[0][wd >> 1], x0);
+        dequant_word(w1r, sfw[1][wd >> 1], x1);
+#pragma unroll
+        for (int n = 0; n < NB; ++n) {
+          const uint4 q4 = lds128(qbase + (n * 128 + wd * 32 + lane) * 16);
+          mma16816(sacc[h][n], x0[0], x1[0], x0[1], x1[1], q4.x, q4.y);
+          mma16816(e2[n], x0[2], x1[2], x0[3], x1[3], q4.z, q4.w);
         }
-#pragma unroll
-        for (int r = 0; r < 4; ++r) sacc[h][n][r] += e2[r];
       }
+#pragma unroll
+      for (int n = 0; n < NB; ++n)
+#pragma unroll
+        for (int r = 0; r < 4; ++r) sacc[h][n][r] += e2[n][r];
     }
 
     // ---- online softmax over the 32 tokens --------------------------------
