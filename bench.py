@@ -731,7 +731,62 @@ def cpu_baseline(st, ga, sample_tokens):
             "sample": f"first {sub.num_tokens} store tokens "
                       f"({sub.num_tokens // 512} requests) and first "
                       f"{gsub.num_seqs} gather sequences of the same "
-                      f"workload, single-threaded plain C oracle"}
+                      f"workload, single-threaded plain C oracle",
+            "all_cores": cpu_baseline_all_cores(o, sub, gsub, byts)}
+
+
+def oracle_step_threaded(o, sub, gsub, cache, k, s, threads):
+    """`oracle_step` with the oracle's calls split over `threads` host
+    threads: the store by tokens (slots are distinct, so the pieces write
+    disjoint bytes), the gather by sequences (each piece writes its own rows).
+    The oracle is unchanged; each thread calls it on its own piece (ctypes
+    releases the GIL during the call)."""
+    import concurrent.futures as cf
+    D = gsub.head_dim
+    cu = gsub.cu_seq_lens.astype(np.int64)
+
+    def store_piece(c):
+        t0 = sub.num_tokens * c // threads
+        t1 = sub.num_tokens * (c + 1) // threads
+        if t1 > t0:
+            o.store_nvfp4(sub.src, sub.key_stride0, sub.src, sub.value_stride0,
+                          t1 - t0, sub.num_heads, sub.head_size, cache, 0,
+                          sub.value_side_offset, sub.page_stride,
+                          sub.block_size, sub.num_blocks, sub.layout,
+                          sub.slot_mapping[t0:t1], sub.k_scale, sub.v_scale,
+                          sub.flags,
+                          key_base=sub.key_offset + t0 * sub.key_stride0,
+                          value_base=sub.value_offset + t0 * sub.value_stride0)
+
+    def gather_piece(c):
+        b0 = gsub.num_seqs * c // threads
+        b1 = gsub.num_seqs * (c + 1) // threads
+        if b1 > b0:
+            r0, r1 = int(cu[b0]), int(cu[b1])
+            o.gather_indexer_k(gsub.cache, gsub.block_stride, gsub.num_blocks,
+                               gsub.block_size, D,
+                               np.ascontiguousarray(gsub.block_table[b0:b1]),
+                               (cu[b0:b1 + 1] - r0).astype(np.int32),
+                               r1 - r0, k[r0 * D:r1 * D], s[r0 * 4:r1 * 4])
+
+    with cf.ThreadPoolExecutor(threads) as ex:
+        list(ex.map(store_piece, range(threads)))
+        list(ex.map(gather_piece, range(threads)))
+
+
+def cpu_baseline_all_cores(o, sub, gsub, byts):
+    """The single-thread sample again, split over every host core."""
+    threads = max(1, os.cpu_count() or 1)
+    cache = np.full(sub.cache_bytes, 0xAA, dtype=np.uint8)
+    k = np.empty(gsub.total_tokens * gsub.head_dim, dtype=np.uint8)
+    s = np.empty(gsub.total_tokens * 4, dtype=np.uint8)
+    t = time.perf_counter()
+    oracle_step_threaded(o, sub, gsub, cache, k, s, threads)
+    dt = time.perf_counter() - t
+    return {"value": round(byts / dt / 1e9, 4), "unit": "GB/s",
+            "cores": threads, "seconds": round(dt, 3),
+            "sample": "the same sample, store tokens and gather sequences "
+                      f"split evenly over {threads} threads"}
 
 
 def cpu_attention_baseline(aw, nseq=4):
