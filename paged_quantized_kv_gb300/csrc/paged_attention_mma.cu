@@ -39,7 +39,8 @@
 //     significant bits and lies in [2^-10, 2688], so the operand is exact.
 //   * Online softmax over the warp's steps (exp2 of the scaled logits minus
 //     the running max, rounded to fp16; the denominator sums the rounded
-//     weights; the accumulator is rescaled when the max grows).  The fp16
+//     weights, by an MMA of an all-ones A with the weights; the
+//     accumulators are rescaled when the max grows).  The fp16
 //     weights P^T (tokens x heads, in the logits' accumulator layout) are
 //     transposed into the B fragment of the second product with
 //     movmatrix.
@@ -84,6 +85,15 @@ constexpr int kDepth = KVQ_ATTN_MMA_DEPTH;  // steps in flight per warp
 // followed, after every warp's slots, by the query fragments of the CTA:
 // [n-block][i][lane] x 16 B = lane (g, t)'s dims 32t + 8i .. + 7 of query
 // head 8n + g as fp16.
+// The warps' partial outputs at the end, one row of head dims per (warp,
+// head): rows kMergeRow floats apart and dim d at column merge_col(d) (bits
+// 1-2 of d XOR bits 5-6), so that both the fragment-layout float2 stores
+// (lane (g, t) writes dims 16g + 2mb, +1 of head 2t + c) and the readers
+// (one dim per thread) meet no bank conflict.
+constexpr int kMergeRow = kD + 4;
+__host__ __device__ constexpr int merge_col(int d) {
+  return d ^ (((d >> 5) & 3) << 1);
+}
 constexpr int kKdOff = 0;
 constexpr int kVdOff = kKdOff + 4 * 16 * 32;
 constexpr int kKsOff = kVdOff + 8 * 8 * 32;
@@ -97,7 +107,8 @@ struct Slots {
   template <int NB>
   static constexpr int smem() { return kQOff + NB * 4 * 32 * 16; }
   // the merge buffers reuse the copy slots
-  static_assert(kQOff >= kWarps * 16 * kD * 4 + 2 * kWarps * 16 * 4, "");
+  static_assert(kQOff >= kWarps * 16 * kMergeRow * 4 + 2 * kWarps * 16 * 4,
+                "");
 };
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -230,16 +241,6 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
   return d;
 }
 
-__device__ __forceinline__ void unpack_f16x2(uint32_t h, float& lo,
-                                             float& hi) {
-  asm("{ .reg .f16 a, b;\n"
-      "  mov.b32 {a, b}, %2;\n"
-      "  cvt.f32.f16 %0, a;\n"
-      "  cvt.f32.f16 %1, b; }"
-      : "=f"(lo), "=f"(hi)
-      : "r"(h));
-}
-
 // bf16x2 -> f16x2 (round to nearest; exact for bf16 values inside the fp16
 // normal range).
 __device__ __forceinline__ uint32_t bf16x2_f16x2(uint32_t w) {
@@ -287,6 +288,7 @@ __device__ __forceinline__ uint16_t float_to_out(float f) {
 // maximum is 0, and ex2(0) times a zero sum stays 0 when every range is
 // empty.
 constexpr float kNoLogit = -3.0e38f;
+constexpr uint32_t kOnes2 = 0x3C003C00u;  // f16x2 {1, 1}
 
 // kContig: HND pages with block_size % 16 == 0, so each 16 tokens of a
 // step lie in one block and their rows (and scale rows) are contiguous: one
@@ -508,12 +510,15 @@ paged_attention_mma_kernel(const AttnParams p) {
   // running softmax state of heads 8n + 2t + c, and O^T fragments: o[mb][n]
   // = rows dims 16g + 2mb (c0, c1) and 16g + 2mb + 1 (c2, c3), columns heads
   // 8n + 2t, 8n + 2t + 1
-  float m_run[NB][2], l_run[NB][2];
+  // lacc[n][c]: running denominator of head 8n + 2t + c, already summed
+  // over the warp's tokens by the tensor cores (c2, c3 repeat it and are
+  // not read)
+  float m_run[NB][2], lacc[NB][4];
   float o[8][NB][4];
 #pragma unroll
   for (int n = 0; n < NB; ++n) {
     m_run[n][0] = m_run[n][1] = -INFINITY;
-    l_run[n][0] = l_run[n][1] = 0.f;
+    lacc[n][0] = lacc[n][1] = lacc[n][2] = lacc[n][3] = 0.f;
 #pragma unroll
     for (int mb = 0; mb < 8; ++mb)
       o[mb][n][0] = o[mb][n][1] = o[mb][n][2] = o[mb][n][3] = 0.f;
@@ -617,7 +622,7 @@ paged_attention_mma_kernel(const AttnParams p) {
         const bool none = mnew == -INFINITY;  // no usable token yet
         const float alpha = none ? 1.f : ex2(m_run[n][c] - mnew);
         m_run[n][c] = mnew;
-        l_run[n][c] *= alpha;
+        lacc[n][c] *= alpha;
 #pragma unroll
         for (int mb = 0; mb < 8; ++mb) {
           o[mb][n][c] *= alpha;
@@ -633,11 +638,6 @@ paged_attention_mma_kernel(const AttnParams p) {
       for (int h = 0; h < 2; ++h) {
         const uint32_t pl = pack_f16x2(v[h][0], v[h][1]);  // token g
         const uint32_t ph = pack_f16x2(v[h][2], v[h][3]);  // token g + 8
-        float a0, a1, b0, b1;
-        unpack_f16x2(pl, a0, a1);
-        unpack_f16x2(ph, b0, b1);
-        l_run[n][0] += a0 + b0;
-        l_run[n][1] += a1 + b1;
         pb[h][n][0] = transpose8x8(pl);
         pb[h][n][1] = transpose8x8(ph);
       }
@@ -688,43 +688,40 @@ paged_attention_mma_kernel(const AttnParams p) {
             mma16816(o[mb][n], a0, a1, a2, a3, pb[h][n][0], pb[h][n][1]);
         }
       }
+      // the denominators: an all-ones A times P^T sums the half's 16
+      // rounded weights of each head (every row holds the sum)
+#pragma unroll
+      for (int n = 0; n < NB; ++n)
+        mma16816(lacc[n], kOnes2, kOnes2, kOnes2, kOnes2, pb[h][n][0],
+                 pb[h][n][1]);
     }
   }
   cp_async_wait<0>();  // nothing may land after the slots are reused
 
   // ---- merge the 4 warps' partial results in shared memory ----------------
-#pragma unroll
-  for (int n = 0; n < NB; ++n)
-#pragma unroll
-    for (int c = 0; c < 2; ++c) {
-      float l = l_run[n][c];
-      l += __shfl_xor_sync(0xFFFFFFFFu, l, 4);
-      l += __shfl_xor_sync(0xFFFFFFFFu, l, 8);
-      l += __shfl_xor_sync(0xFFFFFFFFu, l, 16);
-      l_run[n][c] = l;
-    }
   __syncthreads();  // every warp is done with its copy slots
-  float* sO = reinterpret_cast<float*>(smem);        // [warp][16][kD]
-  float* sM = sO + kWarps * 16 * kD;                 // [warp][16]
+  float* sO = reinterpret_cast<float*>(smem);        // [warp][16][kMergeRow]
+  float* sM = sO + kWarps * 16 * kMergeRow;          // [warp][16]
   float* sL = sM + kWarps * 16;                      // [warp][16]
 #pragma unroll
   for (int n = 0; n < NB; ++n)
 #pragma unroll
     for (int c = 0; c < 2; ++c) {
       const int hh = 8 * n + 2 * t + c;
-      float* row = sO + (warp * 16 + hh) * kD + 16 * g;
+      float* row = sO + (warp * 16 + hh) * kMergeRow;
 #pragma unroll
       for (int mb = 0; mb < 8; ++mb)
-        *reinterpret_cast<float2*>(row + 2 * mb) =
+        *reinterpret_cast<float2*>(row + merge_col(16 * g + 2 * mb)) =
             make_float2(o[mb][n][c], o[mb][n][2 + c]);
       if (g == 0) {
         sM[warp * 16 + hh] =
             m_run[n][c] == -INFINITY ? kNoLogit : m_run[n][c];
-        sL[warp * 16 + hh] = l_run[n][c];
+        sL[warp * 16 + hh] = lacc[n][c];
       }
     }
   __syncthreads();
   const int d = tid;  // one head dim per thread
+  const int dcol = merge_col(d);
   const float v_scale = __ldg(p.v_scale);
   for (int hh = 0; hh < p.G; ++hh) {
     float M = sM[hh];
@@ -735,7 +732,7 @@ paged_attention_mma_kernel(const AttnParams p) {
     for (int w = 0; w < kWarps; ++w) {
       const float f = ex2(sM[w * 16 + hh] - M);
       den += sL[w * 16 + hh] * f;
-      acc += sO[(w * 16 + hh) * kD + d] * f;
+      acc += sO[(w * 16 + hh) * kMergeRow + dcol] * f;
     }
     if (nparts == 1) {
       const float y = den > 0.f ? acc * (1.0f / den) * v_scale : 0.f;

@@ -1207,26 +1207,56 @@ paged_attention_pipe_kernel(const AttnParams p) {
 // ---------------------------------------------------------------------------
 // Merge of the partitions of contexts longer than one partition
 // ---------------------------------------------------------------------------
+// 16 rows (sequence, query head) per CTA of 256 threads, a half-warp per
+// row and 8 head dims per lane, so that one wave of CTAs covers a whole
+// decode batch.  The context length is read before the wait for the
+// attention kernel, which writes none of it; every thread waits before it
+// may leave.  Per dim, the sums run over the partitions in order.
+constexpr int kMergeThreads = 256;
+constexpr int kMergeRows = kMergeThreads / 16;
+
 template <bool kF16>
-__global__ void __launch_bounds__(kD)
+__global__ void __launch_bounds__(kMergeThreads)
 attention_merge_kernel(const AttnParams p) {
+  const int sub = threadIdx.x & 15;  // dims 8 sub .. 8 sub + 7
+  const int64_t row =
+      static_cast<int64_t>(blockIdx.x) * kMergeRows + (threadIdx.x >> 4);
+  const bool live = row < static_cast<int64_t>(p.num_seqs) * p.Hq;
+  const int b = live ? static_cast<int>(row / p.Hq) : 0;
+  const int h = live ? static_cast<int>(row - static_cast<int64_t>(b) * p.Hq)
+                     : 0;
+  int L = live ? __ldg(p.lens + b) : 0;
   pdl_prologue();
-  const int h = blockIdx.x, b = blockIdx.y, d = threadIdx.x;
-  int L = __ldg(p.lens + b);
   L = L < 0 ? 0 : (L > p.len_cap ? p.len_cap : L);
   const int nparts = (L + p.part - 1) / p.part;
-  if (nparts <= 1) return;
-  const int64_t row0 = (static_cast<int64_t>(b) * p.Hq + h) * p.max_parts;
+  if (!live || nparts <= 1) return;
+  const int64_t row0 = row * p.max_parts;
   float M = -INFINITY;
+#pragma unroll 4
   for (int i = 0; i < nparts; ++i) M = fmaxf(M, p.max_logits[row0 + i]);
-  float den = 0.f, acc = 0.f;
+  float den = 0.f, acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll 2
   for (int i = 0; i < nparts; ++i) {
     const float w = p.exp_sums[row0 + i] * ex2(p.max_logits[row0 + i] - M);
     den += w;
-    acc += w * p.tmp_out[(row0 + i) * kD + d];
+    const float4* src =
+        reinterpret_cast<const float4*>(p.tmp_out + (row0 + i) * kD + 8 * sub);
+    const float4 x = src[0], y = src[1];
+    acc[0] += w * x.x; acc[1] += w * x.y; acc[2] += w * x.z; acc[3] += w * x.w;
+    acc[4] += w * y.x; acc[5] += w * y.y; acc[6] += w * y.z; acc[7] += w * y.w;
   }
-  const float y = den > 0.f ? acc * (1.0f / den) * __ldg(p.v_scale) : 0.f;
-  p.out[b * p.out_stride0 + h * kD + d] = float_to_out<kF16>(y);
+  const float f = den > 0.f ? 1.0f / den : 0.f;
+  const float vs = __ldg(p.v_scale);
+  uint32_t packed[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const float y0 = den > 0.f ? acc[2 * k] * f * vs : 0.f;
+    const float y1 = den > 0.f ? acc[2 * k + 1] * f * vs : 0.f;
+    packed[k] = static_cast<uint32_t>(float_to_out<kF16>(y0)) |
+                (static_cast<uint32_t>(float_to_out<kF16>(y1)) << 16);
+  }
+  *reinterpret_cast<uint4*>(p.out + b * p.out_stride0 + h * kD + 8 * sub) =
+      make_uint4(packed[0], packed[1], packed[2], packed[3]);
 }
 
 template <int NG, bool kF16>
@@ -1255,8 +1285,7 @@ cudaError_t launch_pipe(const AttnParams& p, cudaStream_t stream) {
   err = launch_kernel(kernel, dim3(grid), kPipeThreads, kPipeSmem, stream,
                       p.pdl, p);
   if (err != cudaSuccess || p.max_parts <= 1) return err;
-  return launch_kernel(attention_merge_kernel<kF16>, dim3(p.Hq, p.num_seqs),
-                       kD, 0, stream, true, p);
+  return launch_attention_merge(p, stream);
 }
 
 template <int NG, bool kF16>
@@ -1282,17 +1311,18 @@ cudaError_t launch_ng(const AttnParams& p, cudaStream_t stream) {
   const dim3 grid(p.max_parts, p.Hkv, p.num_seqs);
   err = launch_kernel(kernel, grid, kThreads, kSmemBytes, stream, p.pdl, p);
   if (err != cudaSuccess || p.max_parts <= 1) return err;
-  return launch_kernel(attention_merge_kernel<kF16>, dim3(p.Hq, p.num_seqs),
-                       kD, 0, stream, true, p);
+  return launch_attention_merge(p, stream);
 }
 
 }  // namespace
 
 cudaError_t launch_attention_merge(const AttnParams& p, cudaStream_t stream) {
-  return p.f16 ? launch_kernel(attention_merge_kernel<true>,
-                               dim3(p.Hq, p.num_seqs), kD, 0, stream, true, p)
-               : launch_kernel(attention_merge_kernel<false>,
-                               dim3(p.Hq, p.num_seqs), kD, 0, stream, true, p);
+  const int64_t rows = static_cast<int64_t>(p.num_seqs) * p.Hq;
+  const dim3 grid(static_cast<unsigned>((rows + kMergeRows - 1) / kMergeRows));
+  return p.f16 ? launch_kernel(attention_merge_kernel<true>, grid,
+                               kMergeThreads, 0, stream, true, p)
+               : launch_kernel(attention_merge_kernel<false>, grid,
+                               kMergeThreads, 0, stream, true, p);
 }
 
 cudaError_t launch_paged_attention_nvfp4(const AttnParams& p,
