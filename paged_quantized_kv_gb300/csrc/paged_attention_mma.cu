@@ -75,12 +75,22 @@ constexpr int kDepth = KVQ_ATTN_MMA_DEPTH;  // steps in flight per warp
 #ifndef KVQ_ATTN_MMA_PART
 #define KVQ_ATTN_MMA_PART 1024
 #endif
-// One step's private slots of one warp, lane-contiguous per piece:
+// One step's slots of one warp.  On contiguous pages the step's 32
+// tokens arrive in the pages' own order (whichever lane copies a chunk,
+// its bytes keep their place), as 16-byte copies:
+//   K data  4 x 512 B: tokens 16h + 8r + 0..7 (j = 2h + r), 64 B each;
+//           lane (g, t) reads bytes 16t .. 16t+15 of token g
+//   V data  4 x 512 B: tokens 16h + 8q + 0..7, 16-byte chunk k of the
+//           piece at chunk k ^ (bit 3 of k, moved to bit 2), so that the
+//           reads of token 2t (+1), bytes 8g .. 8g+7, meet no bank conflict
+//   scales  512 B: per half h, 128 B of K scale rows (8 B per token) then
+//           the 128 B of the half's V scales as the page holds them
+//           (4-token bands of 32 B)
+// Elsewhere every lane copies its own fragments into private,
+// lane-contiguous slots:
 //   K data  4 x 16 B (tokens g + 8j, bytes 16t .. 16t+15)
 //   V data  8 x  8 B (tokens 16h + {2t, 2t+1, 2t+8, 2t+9}, bytes 8g .. 8g+7)
-//   K scale 4 x  8 B (the 8-byte scale row holding groups 2t, 2t+1), or
-//           4 x  4 B on contiguous pages with linear K scales (the word
-//           holding bytes 2t, 2t+1)
+//   K scale 4 x  8 B (the 8-byte scale row holding groups 2t, 2t+1)
 //   V scale 4 x  4 B (the word holding group g of a token pair)
 // followed, after every warp's slots, by the query fragments of the CTA:
 // [n-block][i][lane] x 16 B = lane (g, t)'s dims 32t + 8i .. + 7 of query
@@ -97,11 +107,13 @@ __host__ __device__ constexpr int merge_col(int d) {
 constexpr int kKdOff = 0;
 constexpr int kVdOff = kKdOff + 4 * 16 * 32;
 constexpr int kKsOff = kVdOff + 8 * 8 * 32;
-template <bool kNarrowKs>
+__host__ __device__ constexpr int vchunk(int k) {
+  return k ^ (((k >> 3) & 1) << 2);
+}
+template <bool kContig>
 struct Slots {
-  static constexpr int kKsBytes = kNarrowKs ? 4 : 8;
-  static constexpr int kVsOff = kKsOff + 4 * kKsBytes * 32;
-  static constexpr int kStage = kVsOff + 4 * 4 * 32;
+  static constexpr int kVsOff = kKsOff + 4 * 8 * 32;  // not contiguous
+  static constexpr int kStage = kContig ? kKsOff + 512 : kVsOff + 4 * 4 * 32;
   static constexpr int kWarp = kDepth * kStage;
   static constexpr int kQOff = kWarps * kWarp;
   template <int NB>
@@ -133,19 +145,6 @@ __device__ __forceinline__ void cp_async(uint32_t dst, const void* src,
   else
     asm volatile("cp.async.ca.shared.global [%0], [%1], %2, %3;" ::"r"(dst),
                  "l"(src), "n"(kBytes), "r"(n)
-                 : "memory");
-}
-
-// cp.async of `kBytes` that are all inside the source.
-template <int kBytes>
-__device__ __forceinline__ void cp_async_full(uint32_t dst, const void* src) {
-  if constexpr (kBytes == 16)
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst),
-                 "l"(src)
-                 : "memory");
-  else
-    asm volatile("cp.async.ca.shared.global [%0], [%1], %2;" ::"r"(dst),
-                 "l"(src), "n"(kBytes)
                  : "memory");
 }
 
@@ -297,7 +296,7 @@ template <int NG, bool kF16, bool kContig>
 __global__ void __launch_bounds__(kThreads, NG == 8 ? 4 : 2)
 paged_attention_mma_kernel(const AttnParams p) {
   constexpr int NB = NG / 8;  // n-blocks of 8 query heads
-  using SL = Slots<kContig>;  // contiguous pages have linear K scales
+  using SL = Slots<kContig>;
   extern __shared__ __align__(16) uint8_t smem[];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, t = lane & 3;
@@ -398,11 +397,14 @@ paged_attention_mma_kernel(const AttnParams p) {
     return tok < w1 && ((bmask >> ((idx - e0) & 31)) & 1u) != 0u;
   };
 
-  // lane-constant byte offsets inside 16 contiguous tokens (kContig)
-  const int kd_off = g * 64 + 16 * t;  // + 512 for token g + 8
-  const int ks_off = g * 8 + (t >> 1) * 4;  // linear: + 64 for g + 8
-  const int vd_off = (2 * t) * 64 + 8 * g;  // + 64 for 2t+1, + 512 for 8q
-  const int vs_off = ((2 * t) & ~3) * 8 + (g >> 1) * 8 + (g & 1) * 4;
+  // contiguous pages: where this lane's copy lands in a V piece, and where
+  // its fragments are read from (V data of token 2t + e of a piece; K
+  // scale word of token g; V scale word of tokens 2t, 2t+1)
+  const int v_dst = vchunk(lane) * 16;
+  const int v_rd0 = vchunk(8 * t + (g >> 1)) * 16 + (g & 1) * 8;
+  const int v_rd1 = vchunk(8 * t + 4 + (g >> 1)) * 16 + (g & 1) * 8;
+  const int ks_rd = g * 8 + (t >> 1) * 4;
+  const int vs_rd = 128 + 32 * (t >> 1) + 4 * g;
 
   // Issue the copies of step i (tokens w0 + 32i ..) into its slots and
   // commit them as one group (an empty group past the last step).
@@ -410,66 +412,42 @@ paged_attention_mma_kernel(const AttnParams p) {
     if (i >= nsteps) {
       // nothing to copy
     } else if constexpr (kContig) {
+      // whole 16-token halves: a block with a valid id is copied as it is
+      // (tokens past the range are left out of the softmax and their V
+      // scales zeroed when read), a bad one zero-filled from memory that
+      // surely exists (the query)
       const uint32_t st = wbase + (i % kDepth) * SL::kStage;
+      const uint8_t* qz = reinterpret_cast<const uint8_t*>(p.q);
+      int64_t rel[2], srel[2];
+      bool bok[2];
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         const int T = w0 + kStep * i + 16 * h;
         const int idx = p.b_shift >= 0 ? (T >> p.b_shift) : T / p.B;
         const int32_t blk = __shfl_sync(0xFFFFFFFFu, bt_lane, (idx - e0) & 31);
-        const bool bok = blk >= 0 && blk < p.num_blocks;
-        if (T < w1 && !bok && t == 0 && g == 0 && p.dev_error != nullptr)
+        bok[h] = blk >= 0 && blk < p.num_blocks;
+        if (T < w1 && !bok[h] && lane == 0 && p.dev_error != nullptr)
           atomicOr(p.dev_error, KVQ_DEVERR_BLOCK);
-        const int64_t rel = static_cast<int64_t>(blk) * p.page_stride +
-                            kh * p.dhs + static_cast<int64_t>(T - idx * p.B) * 64;
-        const int64_t srel = static_cast<int64_t>(blk) * p.page_stride +
-                             p.scale_off + kh * p.shs +
-                             static_cast<int64_t>(T - idx * p.B) * 8;
-        // a bad block's copies are zero-filled from memory that surely
-        // exists (the query); in-range tokens past the context still lie
-        // inside their (valid) block
-        const uint8_t* qz = reinterpret_cast<const uint8_t*>(p.q);
-        const uint8_t* kd = bok ? kside + rel + kd_off : qz;
-        const uint8_t* ks = bok ? kside + srel + ks_off : qz;
-        const uint8_t* vd = bok ? vside + rel + vd_off : qz;
-        const uint8_t* vs = bok ? vside + srel + vs_off : qz;
-        if (bok && T + 16 <= w1) {  // all 16 tokens usable: no zero fill
-          const uint32_t d16 = st + lane * 16, d8 = st + lane * 8;
-          const uint32_t d4 = st + lane * 4;
+        const int64_t base = static_cast<int64_t>(blk) * p.page_stride;
+        rel[h] = base + kh * p.dhs + static_cast<int64_t>(T - idx * p.B) * 64;
+        srel[h] = base + p.scale_off + kh * p.shs +
+                  static_cast<int64_t>(T - idx * p.B) * 8;
 #pragma unroll
-          for (int r = 0; r < 2; ++r) {
-            cp_async_full<16>(d16 + kKdOff + (2 * h + r) * 512, kd + 512 * r);
-            cp_async_full<4>(d4 + kKsOff + (2 * h + r) * 128, ks + 64 * r);
-          }
-#pragma unroll
-          for (int q = 0; q < 2; ++q) {
-            cp_async_full<8>(d8 + kVdOff + (4 * h + 2 * q) * 256, vd + 512 * q);
-            cp_async_full<8>(d8 + kVdOff + (4 * h + 2 * q + 1) * 256,
-                             vd + 512 * q + 64);
-            cp_async_full<4>(d4 + SL::kVsOff + (2 * h + q) * 128, vs + 64 * q);
-          }
-          continue;
-        }
-        const int64_t dk = bok ? 1 : 0;  // lane offsets only inside a block
-#pragma unroll
-        for (int r = 0; r < 2; ++r) {  // K: tokens T + g + 8r
-          const bool ok = bok && T + g + 8 * r < w1;
-          const int j = 2 * h + r;
-          cp_async<16>(st + kKdOff + j * 512 + lane * 16, kd + dk * 512 * r,
-                       ok);
-          cp_async<4>(st + kKsOff + j * 128 + lane * 4, ks + dk * 64 * r, ok);
-        }
-#pragma unroll
-        for (int q = 0; q < 2; ++q) {  // V: tokens T + 8q + 2t (+1)
-          const int tok = T + 8 * q + 2 * t;
-          const int piece = 4 * h + 2 * q;
-          cp_async<8>(st + kVdOff + piece * 256 + lane * 8,
-                      vd + dk * 512 * q, bok && tok < w1);
-          cp_async<8>(st + kVdOff + (piece + 1) * 256 + lane * 8,
-                      vd + dk * (512 * q + 64), bok && tok + 1 < w1);
-          cp_async<4>(st + SL::kVsOff + (2 * h + q) * 128 + lane * 4,
-                      vs + dk * 64 * q, bok && tok < w1);
+        for (int r = 0; r < 2; ++r) {
+          const int64_t o = rel[h] + 512 * r + 16 * lane;
+          cp_async<16>(st + kKdOff + (2 * h + r) * 512 + lane * 16,
+                       bok[h] ? kside + o : qz, bok[h]);
+          cp_async<16>(st + kVdOff + (2 * h + r) * 512 + v_dst,
+                       bok[h] ? vside + o : qz, bok[h]);
         }
       }
+      // the step's scales: lanes 16h .. 16h+15 take half h, the first 8 of
+      // them its K scale rows, the other 8 its V scale bands
+      const int sh = lane >> 4;
+      const bool sok = sh ? bok[1] : bok[0];
+      const int64_t so = (sh ? srel[1] : srel[0]) + 16 * (lane & 7);
+      const uint8_t* sside = (lane & 8) ? vside : kside;
+      cp_async<16>(st + kKsOff + lane * 16, sok ? sside + so : qz, sok);
     } else {
       const uint32_t st = wbase + (i % kDepth) * SL::kStage;
       const int T0 = w0 + kStep * i;
@@ -561,7 +539,7 @@ paged_attention_mma_kernel(const AttnParams p) {
         kd[r] = lds128(st + kKdOff + j * 512 + lane * 16);
         uint32_t pair;
         if constexpr (kContig) {
-          pair = prmt(lds32(st + kKsOff + j * 128 + lane * 4), 0u, ksel);
+          pair = prmt(lds32(st + kKsOff + 256 * h + 64 * r + ks_rd), 0u, ksel);
         } else {
           const uint2 ks = lds64(st + kKsOff + j * 256 + lane * 8);
           pair = prmt(ks.x, ks.y, ksel);
@@ -650,10 +628,17 @@ paged_attention_mma_kernel(const AttnParams p) {
       uint32_t sfp[2];    // [pair q]: {sf(2t+8q), sf(2t+8q+1)} as f16x2
 #pragma unroll
       for (int q = 0; q < 2; ++q) {
-        vd[q][0] = lds64(st + kVdOff + (4 * h + 2 * q) * 256 + lane * 8);
-        vd[q][1] = lds64(st + kVdOff + (4 * h + 2 * q + 1) * 256 + lane * 8);
-        const uint32_t w =
-            lds32(st + SL::kVsOff + (2 * h + q) * 128 + lane * 4);
+        uint32_t w;
+        if constexpr (kContig) {
+          const uint32_t piece = st + kVdOff + (2 * h + q) * 512;
+          vd[q][0] = lds64(piece + v_rd0);
+          vd[q][1] = lds64(piece + v_rd1);
+          w = lds32(st + kKsOff + 256 * h + 64 * q + vs_rd);
+        } else {
+          vd[q][0] = lds64(st + kVdOff + (4 * h + 2 * q) * 256 + lane * 8);
+          vd[q][1] = lds64(st + kVdOff + (4 * h + 2 * q + 1) * 256 + lane * 8);
+          w = lds32(st + SL::kVsOff + (2 * h + q) * 128 + lane * 4);
+        }
         // a token past the range may share the word: zero its scale (its
         // data are zero already), so no stray NaN code meets a zero weight
         const int tok = T0 + 16 * h + 8 * q + 2 * t;
