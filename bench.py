@@ -476,7 +476,7 @@ def run_ours(args):
                     "Llama-3.1-70B-shaped attention: 200 sequences, 64 "
                     "query / 8 KV heads, head_size 128, block_size 16, "
                     "contexts 512 + U[0, 2048]; partition_size 512 (the "
-                    "default warp-level-MMA kernel covers up to 1024 tokens "
+                    "default warp-level-MMA kernel covers up to 1280 tokens "
                     "per CTA, then the partition merge); not part of the "
                     "step",
             "ms": round(attn_ms, 5),

@@ -18,17 +18,19 @@
 // per SM with its operands already in registers and needs no handshake.
 //
 // Design, per CTA of 4 warps = one (stretch of context, KV head, sequence):
-// a stretch is KVQ_ATTN_MMA_PART (1024) tokens on contiguous pages (HND,
+// a stretch is KVQ_ATTN_MMA_PART (1280) tokens on contiguous pages (HND,
 // block_size % 16 == 0, linear K scales), else the caller's partition
 // (<= 512); its tokens are split evenly over the warps, which walk them in
 // steps of 32 tokens:
-//   * Loads: every thread copies, with cp.async (zero-filled for tokens past
-//     the context or with a bad block id), exactly the bytes its own MMA
-//     fragments need into a private shared-memory slot, kDepth steps ahead;
-//     the warp waits with cp.async.wait_group only.  Block ids of the warp's
-//     range are loaded once (one per lane) and shuffled; on contiguous pages
-//     one block id and lane-constant offsets serve 16 tokens.  The query
-//     fragments are staged in shared memory once per CTA.
+//   * Loads: cp.async into the warp's own shared-memory slots, kDepth steps
+//     ahead; the warp waits with cp.async.wait_group only.  Block ids of the
+//     warp's range are loaded once (one per lane) and shuffled.  On
+//     contiguous pages one block id serves 16 tokens and the pages' bytes
+//     keep their order (16-byte copies, a step's scales in one copy per
+//     lane; a bad block id zero-filled); elsewhere every thread copies
+//     exactly the bytes its own MMA fragments need, zero-filled for tokens
+//     past the context or with a bad block id.  The query fragments are
+//     staged in shared memory once per CTA.
 //   * Logits S^T[16 tokens x 8 heads] = K' Q'^T per n-block of 8 query
 //     heads: A = K' (rows = tokens), B = Q'^T (k = head dims).  The head
 //     dims are permuted (the same way for K and Q): in k-step s, lane
@@ -73,7 +75,7 @@ constexpr int kDepth = KVQ_ATTN_MMA_DEPTH;  // steps in flight per warp
 // Tokens per CTA on contiguous pages (a multiple of 4 x 32; at most
 // 4 x 32 blocks of 16 tokens).
 #ifndef KVQ_ATTN_MMA_PART
-#define KVQ_ATTN_MMA_PART 1024
+#define KVQ_ATTN_MMA_PART 1280
 #endif
 // One step's slots of one warp.  On contiguous pages the step's 32
 // tokens arrive in the pages' own order (whichever lane copies a chunk,
