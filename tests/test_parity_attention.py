@@ -23,6 +23,8 @@ store -> attention, the Llama-3.1-70B-shaped decode batch (sampled rows),
 clamped contexts and invalid block ids (flags), and bitwise determinism --
 for all three kernels (the default warp-level-MMA one,
 KVQ_F_ATTN_PIPELINED and KVQ_F_ATTN_TCGEN05)."""
+import dataclasses
+
 import numpy as np
 import pytest
 import torch
@@ -275,10 +277,43 @@ def test_clamped_context_and_flags(orc, kernel):
 
 
 @pytest.mark.parametrize("kernel", KERNELS, ids=KIDS)
+def test_bad_blocks_inside_contexts(orc, kernel):
+    """Out-of-range block ids (negative and past the cache) in the middle of
+    contexts: flagged, and their B tokens left out.  The attention of one
+    query token does not depend on the order of the context's tokens, so
+    the reference is the oracle over the block table with those entries
+    removed and each context shortened by one block (a partial last block
+    stays last)."""
+    B = 16
+    wl = W.make_attention("midbad", 96, [64, 40, 100, 1300], num_q_heads=8,
+                          num_kv_heads=2, head_size=128, block_size=B)
+    drop = {0: 1, 2: 2, 3: 40}           # sequence -> block index made bad
+    wl.block_table[0, 1] = -1
+    wl.block_table[2, 2] = wl.num_blocks + 7
+    wl.block_table[3, 40] = wl.num_blocks
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    got = gpu_attention(wl, dev_error=err, kernel=kernel)
+    assert int(err.item()) & kvq.KVQ_DEVERR_BLOCK
+    bt = np.zeros_like(wl.block_table)
+    lens = wl.context_lens.copy()
+    for b in range(wl.num_seqs):
+        row = list(wl.block_table[b])
+        if b in drop:
+            del row[drop[b]]
+            row.append(0)
+            lens[b] -= B
+        bt[b] = row
+    ref_wl = dataclasses.replace(wl, block_table=bt, context_lens=lens)
+    ref, mag = oracle_attention(orc, ref_wl)
+    assert_close(got, ref, mag, _vmax(ref_wl, lens), "bad blocks inside")
+
+
+@pytest.mark.parametrize("kernel", KERNELS, ids=KIDS)
 def test_long_contexts_many_partitions(orc, kernel):
     """Contexts of several thousand tokens (up to 17 partitions of 512; the
-    default kernel's CTAs cover 1024 tokens each) with a max_context_len
-    above the longest context, so the scratch has more rows than used."""
+    default kernel's CTAs cover 1280 tokens each on these pages) with a
+    max_context_len above the longest context, so the scratch has more rows
+    than used."""
     wl = W.make_attention("long", 95, [4097, 8191, 3000, 1, 1024, 2048],
                           num_q_heads=16, num_kv_heads=2, head_size=128,
                           block_size=16)
