@@ -325,10 +325,11 @@ kvq_status kvq_store_indexer_k(const void* k, int64_t k_stride0,
  * Arithmetic (the tolerance of any comparison follows from it): the query
  * is rounded to fp16, e2m1 * sf is exact in fp16, q . (e2m1 * sf) and
  * P . V' accumulate in fp32 on the tensor cores, P = exp2 of the scaled
- * logits minus a maximum over the stretch of context being accumulated
- * (never below the logits it is applied to) is rounded to fp16 and the
+ * logits minus a reference value of the stretch of context being
+ * accumulated (a logit maximum; the default kernel moves it only when a
+ * logit exceeds it by more than 8, so P < 2^8) is rounded to fp16 and the
  * denominator sums the rounded values; stretches merge in fp32 (rescaled
- * by exp2 of the difference of their maxima); out is rounded once.
+ * by exp2 of the difference of their references); out is rounded once.
  *
  * query          bf16 / fp16 (dtype) [num_seqs, num_q_heads, 128], rows
  *                query_stride0 elements apart (multiple of 8), 16-byte

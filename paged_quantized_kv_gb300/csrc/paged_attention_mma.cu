@@ -40,9 +40,11 @@
 //     (cvt.rn.f16x2.e4m3x2, one packed multiply): e2m1 * sf has at most 6
 //     significant bits and lies in [2^-10, 2688], so the operand is exact.
 //   * Online softmax over the warp's steps (exp2 of the scaled logits minus
-//     the running max, rounded to fp16; the denominator sums the rounded
-//     weights, by an MMA of an all-ones A with the weights; the
-//     accumulators are rescaled when the max grows).  The fp16
+//     a running reference, rounded to fp16; the denominator sums the
+//     rounded weights, by an MMA of an all-ones A with the weights; the
+//     reference moves, and the accumulators are rescaled, only when a
+//     step's maximum exceeds it by more than 8, so weights stay below
+//     2^8 and most steps skip the rescale).  The fp16
 //     weights P^T (tokens x heads, in the logits' accumulator layout) are
 //     transposed into the B fragment of the second product with
 //     movmatrix.
@@ -121,8 +123,12 @@ struct Slots {
   template <int NB>
   static constexpr int smem() { return kQOff + NB * 4 * 32 * 16; }
   // the merge buffers reuse the copy slots
-  static_assert(kQOff >= kWarps * 16 * kMergeRow * 4 + 2 * kWarps * 16 * 4,
+  static_assert(kQOff >= (kWarps * 16 * kMergeRow + 2 * kWarps * 16 +
+                          16 * kWarps + 32) * 4,
                 "");
+  static_assert((kWarps * 16 * kMergeRow + 2 * kWarps * 16) % 4 == 0 &&
+                    kWarps == 4,
+                "merge factors: one 16-byte row per head");
 };
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -290,6 +296,10 @@ __device__ __forceinline__ uint16_t float_to_out(float f) {
 // empty.
 constexpr float kNoLogit = -3.0e38f;
 constexpr uint32_t kOnes2 = 0x3C003C00u;  // f16x2 {1, 1}
+// A step's logits may exceed the running reference by up to this much (log2
+// units) before the accumulators are rescaled: weights stay below 2^8, far
+// inside fp16, and their rounding is still relative (2^-11).
+constexpr float kLazy = 8.0f;
 
 // kContig: HND pages with block_size % 16 == 0, so each 16 tokens of a
 // step lie in one block and their rows (and scale rows) are contiguous: one
@@ -331,9 +341,11 @@ paged_attention_mma_kernel(const AttnParams p) {
   // block ids of the warp's range (at most 32 blocks), one per lane
   const int e0 = p.b_shift >= 0 ? (w0 >> p.b_shift) : w0 / p.B;
   int32_t bt_lane = -1;
+  bool lane_in = false;  // block e0 + lane holds tokens of the warp's range
   if (nsteps > 0) {
     const int e1 = p.b_shift >= 0 ? ((w1 - 1) >> p.b_shift) : (w1 - 1) / p.B;
-    if (e0 + lane <= e1)
+    lane_in = e0 + lane <= e1;
+    if (lane_in)
       bt_lane = __ldg(p.block_table + b * p.bt_stride + e0 + lane);
   }
 
@@ -373,10 +385,7 @@ paged_attention_mma_kernel(const AttnParams p) {
     const int idx = p.b_shift >= 0 ? (tok >> p.b_shift) : tok / p.B;
     const int32_t blk = __shfl_sync(0xFFFFFFFFu, bt_lane, (idx - e0) & 31);
     off = tok - idx * p.B;
-    const bool in = tok < w1;
-    const bool ok = in && blk >= 0 && blk < p.num_blocks;
-    if (in && !ok && p.dev_error != nullptr)
-      atomicOr(p.dev_error, KVQ_DEVERR_BLOCK);
+    const bool ok = tok < w1 && blk >= 0 && blk < p.num_blocks;
     const uint8_t* page = side + static_cast<int64_t>(blk) * p.page_stride;
     data = page + kh * p.dhs + static_cast<int64_t>(off) * p.dts;
     sc = page + p.scale_off + kh * p.shs;
@@ -388,9 +397,14 @@ paged_attention_mma_kernel(const AttnParams p) {
     return ok;
   };
 
-  // bit e: the warp's block e0 + e has a valid id
+  // bit e: the warp's block e0 + e has a valid id.  Every block of the
+  // warp's range holds some of its tokens, so a bad id among them is
+  // flagged here, once (its tokens are left out below).
   const uint32_t bmask =
       __ballot_sync(0xFFFFFFFFu, bt_lane >= 0 && bt_lane < p.num_blocks);
+  const uint32_t rmask = __ballot_sync(0xFFFFFFFFu, lane_in);
+  if (lane == 0 && p.dev_error != nullptr && (rmask & ~bmask) != 0u)
+    atomicOr(p.dev_error, KVQ_DEVERR_BLOCK);
 
   // Whether token `tok` takes part (inside the range, valid block id);
   // every lane must call it.
@@ -428,8 +442,6 @@ paged_attention_mma_kernel(const AttnParams p) {
         const int idx = p.b_shift >= 0 ? (T >> p.b_shift) : T / p.B;
         const int32_t blk = __shfl_sync(0xFFFFFFFFu, bt_lane, (idx - e0) & 31);
         bok[h] = blk >= 0 && blk < p.num_blocks;
-        if (T < w1 && !bok[h] && lane == 0 && p.dev_error != nullptr)
-          atomicOr(p.dev_error, KVQ_DEVERR_BLOCK);
         const int64_t base = static_cast<int64_t>(blk) * p.page_stride;
         rel[h] = base + kh * p.dhs + static_cast<int64_t>(T - idx * p.B) * 64;
         srel[h] = base + p.scale_off + kh * p.shs +
@@ -493,11 +505,13 @@ paged_attention_mma_kernel(const AttnParams p) {
   // lacc[n][c]: running denominator of head 8n + 2t + c, already summed
   // over the warp's tokens by the tensor cores (c2, c3 repeat it and are
   // not read)
-  float m_run[NB][2], lacc[NB][4];
+  // m_neg: -m_run, or 0 while m_run is -inf (no usable token yet)
+  float m_run[NB][2], m_neg[NB][2], bmax[NB][2], lacc[NB][4];
   float o[8][NB][4];
 #pragma unroll
   for (int n = 0; n < NB; ++n) {
     m_run[n][0] = m_run[n][1] = -INFINITY;
+    m_neg[n][0] = m_neg[n][1] = 0.f;
     lacc[n][0] = lacc[n][1] = lacc[n][2] = lacc[n][3] = 0.f;
 #pragma unroll
     for (int mb = 0; mb < 8; ++mb)
@@ -580,48 +594,64 @@ paged_attention_mma_kernel(const AttnParams p) {
     }
 
     // ---- online softmax over the 32 tokens --------------------------------
-    uint32_t pb[2][NB][2];  // B fragments of P^T: [half][n][tokens 2t | 2t+8]
+    // The weights are exp2 of the scaled logits minus a reference m_run that
+    // moves only when a step's maximum exceeds it by more than kLazy (then
+    // every accumulator of the warp is rescaled at once); in between the
+    // weights stay below 2^kLazy.
+    float v[NB][2][4];
+    bool grow = false;
 #pragma unroll
     for (int n = 0; n < NB; ++n) {
-      float v[2][4];
 #pragma unroll
       for (int h = 0; h < 2; ++h)
 #pragma unroll
         for (int r = 0; r < 4; ++r) {
           const bool ok = (kvalid >> (2 * h + (r >> 1))) & 1u;
-          v[h][r] = ok ? sacc[h][n][r] * c2 : -INFINITY;
+          v[n][h][r] = ok ? sacc[h][n][r] * c2 : -INFINITY;
         }
 #pragma unroll
       for (int c = 0; c < 2; ++c) {  // head 8n + 2t + c
-        float bm = fmaxf(fmaxf(v[0][c], v[0][2 + c]),
-                         fmaxf(v[1][c], v[1][2 + c]));
+        float bm = fmaxf(fmaxf(v[n][0][c], v[n][0][2 + c]),
+                         fmaxf(v[n][1][c], v[n][1][2 + c]));
         bm = fmaxf(bm, __shfl_xor_sync(0xFFFFFFFFu, bm, 4));
         bm = fmaxf(bm, __shfl_xor_sync(0xFFFFFFFFu, bm, 8));
         bm = fmaxf(bm, __shfl_xor_sync(0xFFFFFFFFu, bm, 16));
-        const float mnew = fmaxf(m_run[n][c], bm);
-        const bool none = mnew == -INFINITY;  // no usable token yet
-        const float alpha = none ? 1.f : ex2(m_run[n][c] - mnew);
-        m_run[n][c] = mnew;
-        lacc[n][c] *= alpha;
-#pragma unroll
-        for (int mb = 0; mb < 8; ++mb) {
-          o[mb][n][c] *= alpha;
-          o[mb][n][2 + c] *= alpha;
-        }
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          v[h][c] = none ? 0.f : ex2(v[h][c] - mnew);
-          v[h][2 + c] = none ? 0.f : ex2(v[h][2 + c] - mnew);
-        }
-      }
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const uint32_t pl = pack_f16x2(v[h][0], v[h][1]);  // token g
-        const uint32_t ph = pack_f16x2(v[h][2], v[h][3]);  // token g + 8
-        pb[h][n][0] = transpose8x8(pl);
-        pb[h][n][1] = transpose8x8(ph);
+        bmax[n][c] = bm;
+        grow |= bm > m_run[n][c] + kLazy;  // false while both are -inf
       }
     }
+    if (__any_sync(0xFFFFFFFFu, grow)) {  // rare after the first step
+#pragma unroll
+      for (int n = 0; n < NB; ++n)
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          const float mnew = fmaxf(m_run[n][c], bmax[n][c]);
+          if (mnew > m_run[n][c]) {
+            const float alpha = ex2(m_run[n][c] - mnew);  // 0 from -inf
+            m_run[n][c] = mnew;
+            m_neg[n][c] = -mnew;
+            lacc[n][c] *= alpha;
+#pragma unroll
+            for (int mb = 0; mb < 8; ++mb) {
+              o[mb][n][c] *= alpha;
+              o[mb][n][2 + c] *= alpha;
+            }
+          }
+        }
+    }
+    uint32_t pb[2][NB][2];  // B fragments of P^T: [half][n][tokens 2t | 2t+8]
+#pragma unroll
+    for (int n = 0; n < NB; ++n)
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        // an unusable token's -inf gives 0 (m_neg is finite)
+        const uint32_t pl = pack_f16x2(ex2(v[n][h][0] + m_neg[n][0]),
+                                       ex2(v[n][h][1] + m_neg[n][1]));
+        const uint32_t ph = pack_f16x2(ex2(v[n][h][2] + m_neg[n][0]),
+                                       ex2(v[n][h][3] + m_neg[n][1]));
+        pb[h][n][0] = transpose8x8(pl);  // token g
+        pb[h][n][1] = transpose8x8(ph);  // token g + 8
+      }
 
     // ---- O^T[16 dims x 8 heads] += V'^T P^T per 16-token half --------------
 #pragma unroll
@@ -707,20 +737,38 @@ paged_attention_mma_kernel(const AttnParams p) {
       }
     }
   __syncthreads();
+  // once per head: M, the warps' factors exp2(m_w - M) and the denominator
+  float* sF = sL + kWarps * 16;  // [16][kWarps] factors (16-byte rows)
+  float* sD = sF + 16 * kWarps;  // [16] denominators
+  float* sX = sD + 16;           // [16] M
+  if (tid < p.G) {
+    const int hh = tid;
+    float M = sM[hh];
+#pragma unroll
+    for (int w = 1; w < kWarps; ++w) M = fmaxf(M, sM[w * 16 + hh]);
+    float den = 0.f;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+      const float f = ex2(sM[w * 16 + hh] - M);
+      sF[hh * kWarps + w] = f;
+      den += sL[w * 16 + hh] * f;
+    }
+    sD[hh] = den;
+    sX[hh] = M;
+  }
+  __syncthreads();
   const int d = tid;  // one head dim per thread
   const int dcol = merge_col(d);
   const float v_scale = __ldg(p.v_scale);
   for (int hh = 0; hh < p.G; ++hh) {
-    float M = sM[hh];
-#pragma unroll
-    for (int w = 1; w < kWarps; ++w) M = fmaxf(M, sM[w * 16 + hh]);
-    float den = 0.f, acc = 0.f;
-#pragma unroll
-    for (int w = 0; w < kWarps; ++w) {
-      const float f = ex2(sM[w * 16 + hh] - M);
-      den += sL[w * 16 + hh] * f;
-      acc += sO[(w * 16 + hh) * kMergeRow + dcol] * f;
-    }
+    const float4 f = *reinterpret_cast<const float4*>(sF + hh * kWarps);
+    const float* col = sO + hh * kMergeRow + dcol;
+    float acc = 0.f;
+    acc += col[0] * f.x;
+    acc += col[16 * kMergeRow] * f.y;
+    acc += col[32 * kMergeRow] * f.z;
+    acc += col[48 * kMergeRow] * f.w;
+    const float den = sD[hh];
     if (nparts == 1) {
       const float y = den > 0.f ? acc * (1.0f / den) * v_scale : 0.f;
       p.out[b * p.out_stride0 + (kh * p.G + hh) * kD + d] =
@@ -731,7 +779,7 @@ paged_attention_mma_kernel(const AttnParams p) {
           part;
       p.tmp_out[r * kD + d] = den > 0.f ? acc * (1.0f / den) : 0.f;
       if (d == 0) {
-        p.max_logits[r] = M;
+        p.max_logits[r] = sX[hh];
         p.exp_sums[r] = den;
       }
     }
