@@ -417,6 +417,14 @@ paged_attention_mma_kernel(const AttnParams p) {
   // its fragments are read from (V data of token 2t + e of a piece; K
   // scale word of token g; V scale word of tokens 2t, 2t+1)
   const int v_dst = vchunk(lane) * 16;
+  // contiguous pages: lane e's block e0 + e as the K-side base of this KV
+  // head (block 0 stands in for a bad id, whose half is zero-filled from
+  // the query instead), V data at + vdelta, the K scale rows at + sdelta
+  const uint8_t* const kb_lane =
+      kside + static_cast<int64_t>((bmask >> lane) & 1u ? bt_lane : 0) *
+                  p.page_stride + kh * p.dhs;
+  const int64_t vdelta = vside - kside;
+  const int64_t sdelta = p.scale_off + kh * p.shs - kh * p.dhs;
   const int v_rd0 = vchunk(8 * t + (g >> 1)) * 16 + (g & 1) * 8;
   const int v_rd1 = vchunk(8 * t + 4 + (g >> 1)) * 16 + (g & 1) * 8;
   const int ks_rd = g * 8 + (t >> 1) * 4;
@@ -434,34 +442,47 @@ paged_attention_mma_kernel(const AttnParams p) {
       // surely exists (the query)
       const uint32_t st = wbase + (i % kDepth) * SL::kStage;
       const uint8_t* qz = reinterpret_cast<const uint8_t*>(p.q);
-      int64_t rel[2], srel[2];
+      const uint8_t* sb[2];
       bool bok[2];
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         const int T = w0 + kStep * i + 16 * h;
         const int idx = p.b_shift >= 0 ? (T >> p.b_shift) : T / p.B;
-        const int32_t blk = __shfl_sync(0xFFFFFFFFu, bt_lane, (idx - e0) & 31);
-        bok[h] = blk >= 0 && blk < p.num_blocks;
-        const int64_t base = static_cast<int64_t>(blk) * p.page_stride;
-        rel[h] = base + kh * p.dhs + static_cast<int64_t>(T - idx * p.B) * 64;
-        srel[h] = base + p.scale_off + kh * p.shs +
-                  static_cast<int64_t>(T - idx * p.B) * 8;
-#pragma unroll
-        for (int r = 0; r < 2; ++r) {
-          const int64_t o = rel[h] + 512 * r + 16 * lane;
-          cp_async<16>(st + kKdOff + (2 * h + r) * 512 + lane * 16,
-                       bok[h] ? kside + o : qz, bok[h]);
-          cp_async<16>(st + kVdOff + (2 * h + r) * 512 + v_dst,
-                       bok[h] ? vside + o : qz, bok[h]);
+        const int e = (idx - e0) & 31;
+        const uint64_t kl = reinterpret_cast<uint64_t>(kb_lane);
+        const uint32_t lo =
+            __shfl_sync(0xFFFFFFFFu, static_cast<uint32_t>(kl), e);
+        const uint32_t hi =
+            __shfl_sync(0xFFFFFFFFu, static_cast<uint32_t>(kl >> 32), e);
+        const uint8_t* kb = reinterpret_cast<const uint8_t*>(
+            (static_cast<uint64_t>(hi) << 32) | lo);
+        // one block holds the whole half: the branch is warp-uniform
+        bok[h] = (bmask >> e) & 1u;
+        const int toff = (T - idx * p.B) * 64;
+        sb[h] = kb + sdelta + (toff >> 3);
+        const uint32_t kd = st + kKdOff + 2 * h * 512 + lane * 16;
+        const uint32_t vd = st + kVdOff + 2 * h * 512 + v_dst;
+        if (bok[h]) {
+          const uint8_t* ka = kb + toff + 16 * lane;
+          const uint8_t* va = ka + vdelta;
+          cp_async<16>(kd, ka, true);
+          cp_async<16>(kd + 512, ka + 512, true);
+          cp_async<16>(vd, va, true);
+          cp_async<16>(vd + 512, va + 512, true);
+        } else {
+          cp_async<16>(kd, qz, false);
+          cp_async<16>(kd + 512, qz, false);
+          cp_async<16>(vd, qz, false);
+          cp_async<16>(vd + 512, qz, false);
         }
       }
       // the step's scales: lanes 16h .. 16h+15 take half h, the first 8 of
       // them its K scale rows, the other 8 its V scale bands
       const int sh = lane >> 4;
       const bool sok = sh ? bok[1] : bok[0];
-      const int64_t so = (sh ? srel[1] : srel[0]) + 16 * (lane & 7);
-      const uint8_t* sside = (lane & 8) ? vside : kside;
-      cp_async<16>(st + kKsOff + lane * 16, sok ? sside + so : qz, sok);
+      const uint8_t* so = (sh ? sb[1] : sb[0]) + 16 * (lane & 7) +
+                          ((lane & 8) ? vdelta : 0);
+      cp_async<16>(st + kKsOff + lane * 16, sok ? so : qz, sok);
     } else {
       const uint32_t st = wbase + (i % kDepth) * SL::kStage;
       const int T0 = w0 + kStep * i;
