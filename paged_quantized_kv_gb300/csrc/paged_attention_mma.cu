@@ -566,6 +566,19 @@ paged_attention_mma_kernel(const AttnParams p) {
     // registers live at a time
     float sacc[2][NB][4];
     uint32_t kvalid = 0;  // bit j: K token T0 + g + 8j is usable
+    if constexpr (kContig) {
+      // each 16-token half lies in one block
+      const int i0 = p.b_shift >= 0 ? (T0 >> p.b_shift) : T0 / p.B;
+      const int i1 =
+          p.b_shift >= 0 ? ((T0 + 16) >> p.b_shift) : (T0 + 16) / p.B;
+      const uint32_t v0 = (bmask >> ((i0 - e0) & 31)) & 1u;
+      const uint32_t v1 = (bmask >> ((i1 - e0) & 31)) & 1u;
+      const int rem = w1 - T0 - g;  // token T0 + g + 8j usable: 8j < rem
+      kvalid = (v0 & static_cast<uint32_t>(rem > 0)) |
+               ((v0 & static_cast<uint32_t>(rem > 8)) << 1) |
+               ((v1 & static_cast<uint32_t>(rem > 16)) << 2) |
+               ((v1 & static_cast<uint32_t>(rem > 24)) << 3);
+    }
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       uint4 kd[2];
@@ -581,7 +594,9 @@ paged_attention_mma_kernel(const AttnParams p) {
           const uint2 ks = lds64(st + kKsOff + j * 256 + lane * 8);
           pair = prmt(ks.x, ks.y, ksel);
         }
-        kvalid |= static_cast<uint32_t>(usable(T0 + g + 8 * j)) << j;
+        if constexpr (!kContig)
+          kvalid |=
+              static_cast<uint32_t>(usable(T0 + g + 8 * j)) << j;
         const uint32_t sfp = e4m3x2_f16x2(pair);
         sfw[r][0] = prmt(sfp, sfp, 0x1010u);
         sfw[r][1] = prmt(sfp, sfp, 0x3232u);
@@ -674,6 +689,8 @@ paged_attention_mma_kernel(const AttnParams p) {
         pb[h][n][1] = transpose8x8(ph);  // token g + 8
       }
 
+    const int vleft = w1 - T0 - 2 * t;  // tokens of the range from 2t on
+
     // ---- O^T[16 dims x 8 heads] += V'^T P^T per 16-token half --------------
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
@@ -693,11 +710,11 @@ paged_attention_mma_kernel(const AttnParams p) {
           w = lds32(st + SL::kVsOff + (2 * h + q) * 128 + lane * 4);
         }
         // a token past the range may share the word: zero its scale (its
-        // data are zero already), so no stray NaN code meets a zero weight
-        const int tok = T0 + 16 * h + 8 * q + 2 * t;
+        // data are zero already), so no stray NaN code meets a zero weight;
+        // left = tokens of the range from this pair's first one on
+        const int left = vleft - 16 * h - 8 * q;
         uint32_t pair = prmt(w, 0u, vsel);
-        if (tok + 1 >= w1) pair &= 0x00FFu;
-        if (tok >= w1) pair = 0u;
+        if (left < 2) pair &= left == 1 ? 0x00FFu : 0u;
         sfp[q] = e4m3x2_f16x2(pair);
       }
 #pragma unroll
