@@ -646,22 +646,25 @@ paged_attention_mma_kernel(const AttnParams p) {
           v[n][h][r] = ok ? sacc[h][n][r] * c2 : -INFINITY;
         }
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {  // head 8n + 2t + c
-        float bm = fmaxf(fmaxf(v[n][0][c], v[n][0][2 + c]),
-                         fmaxf(v[n][1][c], v[n][1][2 + c]));
-        bm = fmaxf(bm, __shfl_xor_sync(0xFFFFFFFFu, bm, 4));
-        bm = fmaxf(bm, __shfl_xor_sync(0xFFFFFFFFu, bm, 8));
-        bm = fmaxf(bm, __shfl_xor_sync(0xFFFFFFFFu, bm, 16));
+      for (int c = 0; c < 2; ++c) {  // head 8n + 2t + c: this lane's tokens
+        const float bm = fmaxf(fmaxf(v[n][0][c], v[n][0][2 + c]),
+                               fmaxf(v[n][1][c], v[n][1][2 + c]));
         bmax[n][c] = bm;
         grow |= bm > m_run[n][c] + kLazy;  // false while both are -inf
       }
     }
+    // the step's maximum over all its tokens exceeds the reference by more
+    // than kLazy exactly when some lane's does; only then is it formed
     if (__any_sync(0xFFFFFFFFu, grow)) {  // rare after the first step
 #pragma unroll
       for (int n = 0; n < NB; ++n)
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
-          const float mnew = fmaxf(m_run[n][c], bmax[n][c]);
+          float bm = bmax[n][c];
+          bm = fmaxf(bm, __shfl_xor_sync(0xFFFFFFFFu, bm, 4));
+          bm = fmaxf(bm, __shfl_xor_sync(0xFFFFFFFFu, bm, 8));
+          bm = fmaxf(bm, __shfl_xor_sync(0xFFFFFFFFu, bm, 16));
+          const float mnew = fmaxf(m_run[n][c], bm);
           if (mnew > m_run[n][c]) {
             const float alpha = ex2(m_run[n][c] - mnew);  // 0 from -inf
             m_run[n][c] = mnew;
