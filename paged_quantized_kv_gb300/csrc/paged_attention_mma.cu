@@ -194,28 +194,52 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b,
   return d;
 }
 
-// Two e4m3 codes (low byte first) -> f16x2 (exact).
-__device__ __forceinline__ uint32_t e4m3x2_f16x2(uint32_t pair) {
-  uint32_t h;
-  const uint16_t in = static_cast<uint16_t>(pair & 0xFFFFu);
-  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"(in));
-  return h;
+// Four bytes of e2m1 pairs (element 2k in the low nibble of byte k) times
+// half kHalf of the f16x2 scale pair `sfp` (both lanes of the multiply take
+// that half) -> four f16x2 words, element 2k in the low half.  Exact: the
+// products have at most 6 significant bits.
+template <int kHalf>
+__device__ __forceinline__ void dequant_word(uint32_t w, uint32_t sfp,
+                                                uint32_t (&o)[4]) {
+  if constexpr (kHalf == 0)
+    asm("{ .reg .b8 q0, q1, q2, q3;\n"
+        "  .reg .b32 h0, h1, h2, h3, sb;\n"
+        "  .reg .b16 s0, s1;\n"
+        "  mov.b32 {s0, s1}, %5;\n"
+        "  mov.b32 sb, {s0, s0};\n"
+        "  mov.b32 {q0, q1, q2, q3}, %4;\n"
+        "  cvt.rn.f16x2.e2m1x2 h0, q0;  cvt.rn.f16x2.e2m1x2 h1, q1;\n"
+        "  cvt.rn.f16x2.e2m1x2 h2, q2;  cvt.rn.f16x2.e2m1x2 h3, q3;\n"
+        "  mul.rn.f16x2 %0, h0, sb;  mul.rn.f16x2 %1, h1, sb;\n"
+        "  mul.rn.f16x2 %2, h2, sb;  mul.rn.f16x2 %3, h3, sb; }"
+        : "=r"(o[0]), "=r"(o[1]), "=r"(o[2]), "=r"(o[3])
+        : "r"(w), "r"(sfp));
+  else
+    asm("{ .reg .b8 q0, q1, q2, q3;\n"
+        "  .reg .b32 h0, h1, h2, h3, sb;\n"
+        "  .reg .b16 s0, s1;\n"
+        "  mov.b32 {s0, s1}, %5;\n"
+        "  mov.b32 sb, {s1, s1};\n"
+        "  mov.b32 {q0, q1, q2, q3}, %4;\n"
+        "  cvt.rn.f16x2.e2m1x2 h0, q0;  cvt.rn.f16x2.e2m1x2 h1, q1;\n"
+        "  cvt.rn.f16x2.e2m1x2 h2, q2;  cvt.rn.f16x2.e2m1x2 h3, q3;\n"
+        "  mul.rn.f16x2 %0, h0, sb;  mul.rn.f16x2 %1, h1, sb;\n"
+        "  mul.rn.f16x2 %2, h2, sb;  mul.rn.f16x2 %3, h3, sb; }"
+        : "=r"(o[0]), "=r"(o[1]), "=r"(o[2]), "=r"(o[3])
+        : "r"(w), "r"(sfp));
 }
 
-// Four bytes of e2m1 pairs (element 2k in the low nibble of byte k) times
-// the f16x2 scale `sf2` -> four f16x2 words, element 2k in the low half.
-// Exact: the products have at most 6 significant bits.
-__device__ __forceinline__ void dequant_word(uint32_t w, uint32_t sf2,
-                                             uint32_t (&o)[4]) {
-  asm("{ .reg .b8 q0, q1, q2, q3;\n"
-      "  .reg .b32 h0, h1, h2, h3;\n"
-      "  mov.b32 {q0, q1, q2, q3}, %4;\n"
-      "  cvt.rn.f16x2.e2m1x2 h0, q0;  cvt.rn.f16x2.e2m1x2 h1, q1;\n"
-      "  cvt.rn.f16x2.e2m1x2 h2, q2;  cvt.rn.f16x2.e2m1x2 h3, q3;\n"
-      "  mul.rn.f16x2 %0, h0, %5;  mul.rn.f16x2 %1, h1, %5;\n"
-      "  mul.rn.f16x2 %2, h2, %5;  mul.rn.f16x2 %3, h3, %5; }"
-      : "=r"(o[0]), "=r"(o[1]), "=r"(o[2]), "=r"(o[3])
-      : "r"(w), "r"(sf2));
+__device__ __forceinline__ uint16_t lds16(uint32_t a) {
+  uint16_t v;
+  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(a));
+  return v;
+}
+
+// Two e4m3 codes (low byte first) -> f16x2 (exact).
+__device__ __forceinline__ uint32_t e4m3x2_f16x2(uint16_t pair) {
+  uint32_t h;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"(pair));
+  return h;
 }
 
 // Four bytes of e2m1 pairs -> four f16x2 words (exact), byte k -> o[k],
@@ -427,8 +451,10 @@ paged_attention_mma_kernel(const AttnParams p) {
   const int64_t sdelta = p.scale_off + kh * p.shs - kh * p.dhs;
   const int v_rd0 = vchunk(8 * t + (g >> 1)) * 16 + (g & 1) * 8;
   const int v_rd1 = vchunk(8 * t + 4 + (g >> 1)) * 16 + (g & 1) * 8;
-  const int ks_rd = g * 8 + (t >> 1) * 4;
-  const int vs_rd = 128 + 32 * (t >> 1) + 4 * g;
+  // contiguous pages: this lane's scale pairs (K: groups 2t, 2t+1 of token
+  // g's row; V: tokens 2t, 2t+1 of group g in their 4-token band)
+  const int ks_rd16 = g * 8 + 2 * t;
+  const int vs_rd16 = 128 + 32 * (t >> 1) + 4 * g + 2 * (t & 1);
 
   // Issue the copies of step i (tokens w0 + 32i ..) into its slots and
   // commit them as one group (an empty group past the last step).
@@ -539,15 +565,14 @@ paged_attention_mma_kernel(const AttnParams p) {
       o[mb][n][0] = o[mb][n][1] = o[mb][n][2] = o[mb][n][3] = 0.f;
   }
   const float c2 = p.scale * __ldg(p.k_scale) * kLog2e;
-  // byte selectors: K scales of groups 2t, 2t+1 (linear: bytes 2t, 2t+1 of
-  // the row; swizzled: bytes off%4 and 4 + off%4 of the band row, off%4 =
-  // g%4 because steps start at multiples of 32 and B % 4 == 0); V scales of
-  // a token pair: bytes 2t%4, 2t%4 + 1 of the word
+  // byte selectors (pages that are not contiguous): K scales of groups 2t,
+  // 2t+1 (linear: bytes 2t, 2t+1 of the row; swizzled: bytes off%4 and
+  // 4 + off%4 of the band row, off%4 = g%4 because steps start at multiples
+  // of 32 and B % 4 == 0); V scales of a token pair: bytes 2t%4, 2t%4 + 1
+  // of the word
   const uint32_t ksel =
-      kContig ? static_cast<uint32_t>(((2 * t) & 3) | ((((2 * t) & 3) + 1) << 4))
-      : p.swizzle_k
-          ? static_cast<uint32_t>((g & 3) | ((4 + (g & 3)) << 4))
-          : static_cast<uint32_t>((2 * t) | ((2 * t + 1) << 4));
+      p.swizzle_k ? static_cast<uint32_t>((g & 3) | ((4 + (g & 3)) << 4))
+                  : static_cast<uint32_t>((2 * t) | ((2 * t + 1) << 4));
   const uint32_t vsel =
       static_cast<uint32_t>(((2 * t) & 3) | ((((2 * t) & 3) + 1) << 4));
 
@@ -582,24 +607,22 @@ paged_attention_mma_kernel(const AttnParams p) {
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       uint4 kd[2];
-      uint32_t sfw[2][2];  // [row][groups 2t | 2t+1] scale as f16x2
+      uint32_t sfw[2];  // [row]: groups 2t | 2t+1 scales as f16x2
 #pragma unroll
       for (int r = 0; r < 2; ++r) {
         const int j = 2 * h + r;
         kd[r] = lds128(st + kKdOff + j * 512 + lane * 16);
-        uint32_t pair;
+        uint16_t pair;
         if constexpr (kContig) {
-          pair = prmt(lds32(st + kKsOff + 256 * h + 64 * r + ks_rd), 0u, ksel);
+          pair = lds16(st + kKsOff + 256 * h + 64 * r + ks_rd16);
         } else {
           const uint2 ks = lds64(st + kKsOff + j * 256 + lane * 8);
-          pair = prmt(ks.x, ks.y, ksel);
+          pair = static_cast<uint16_t>(prmt(ks.x, ks.y, ksel));
         }
         if constexpr (!kContig)
           kvalid |=
               static_cast<uint32_t>(usable(T0 + g + 8 * j)) << j;
-        const uint32_t sfp = e4m3x2_f16x2(pair);
-        sfw[r][0] = prmt(sfp, sfp, 0x1010u);
-        sfw[r][1] = prmt(sfp, sfp, 0x3232u);
+        sfw[r] = e4m3x2_f16x2(pair);
       }
       // two accumulators (even / odd k-steps) halve the dependent chain
       float e2[NB][4];
@@ -614,8 +637,13 @@ paged_attention_mma_kernel(const AttnParams p) {
                             : wd == 2 ? kd[0].z : kd[0].w;
         const uint32_t w1r = wd == 0 ? kd[1].x : wd == 1 ? kd[1].y
                              : wd == 2 ? kd[1].z : kd[1].w;
-        dequant_word(w0, sfw[0][wd >> 1], x0);
-        dequant_word(w1r, sfw[1][wd >> 1], x1);
+        if (wd < 2) {
+          dequant_word<0>(w0, sfw[0], x0);
+          dequant_word<0>(w1r, sfw[1], x1);
+        } else {
+          dequant_word<1>(w0, sfw[0], x0);
+          dequant_word<1>(w1r, sfw[1], x1);
+        }
 #pragma unroll
         for (int n = 0; n < NB; ++n) {
           const uint4 q4 = lds128(qbase + (n * 128 + wd * 32 + lane) * 16);
@@ -701,23 +729,24 @@ paged_attention_mma_kernel(const AttnParams p) {
       uint32_t sfp[2];    // [pair q]: {sf(2t+8q), sf(2t+8q+1)} as f16x2
 #pragma unroll
       for (int q = 0; q < 2; ++q) {
-        uint32_t w;
+        uint16_t pair;
         if constexpr (kContig) {
           const uint32_t piece = st + kVdOff + (2 * h + q) * 512;
           vd[q][0] = lds64(piece + v_rd0);
           vd[q][1] = lds64(piece + v_rd1);
-          w = lds32(st + kKsOff + 256 * h + 64 * q + vs_rd);
+          pair = lds16(st + kKsOff + 256 * h + 64 * q + vs_rd16);
         } else {
           vd[q][0] = lds64(st + kVdOff + (4 * h + 2 * q) * 256 + lane * 8);
           vd[q][1] = lds64(st + kVdOff + (4 * h + 2 * q + 1) * 256 + lane * 8);
-          w = lds32(st + SL::kVsOff + (2 * h + q) * 128 + lane * 4);
+          pair = static_cast<uint16_t>(
+              prmt(lds32(st + SL::kVsOff + (2 * h + q) * 128 + lane * 4), 0u,
+                   vsel));
         }
         // a token past the range may share the word: zero its scale (its
         // data are zero already), so no stray NaN code meets a zero weight;
         // left = tokens of the range from this pair's first one on
         const int left = vleft - 16 * h - 8 * q;
-        uint32_t pair = prmt(w, 0u, vsel);
-        if (left < 2) pair &= left == 1 ? 0x00FFu : 0u;
+        if (left < 2) pair &= left == 1 ? 0x00FF : 0;
         sfp[q] = e4m3x2_f16x2(pair);
       }
 #pragma unroll
