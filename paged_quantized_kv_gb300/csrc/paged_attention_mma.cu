@@ -124,7 +124,7 @@ struct Slots {
   static constexpr int smem() { return kQOff + NB * 4 * 32 * 16; }
   // the merge buffers reuse the copy slots
   static_assert(kQOff >= (kWarps * 16 * kMergeRow + 2 * kWarps * 16 +
-                          16 * kWarps + 32) * 4,
+                          16 * kWarps + 48) * 4,
                 "");
   static_assert((kWarps * 16 * kMergeRow + 2 * kWarps * 16) % 4 == 0 &&
                     kWarps == 4,
@@ -345,7 +345,9 @@ paged_attention_mma_kernel(const AttnParams p) {
       atomicOr(p.dev_error, KVQ_DEVERR_SEQ);
     L = L < 0 ? 0 : p.len_cap;
   }
-  const int p0 = part * p.part;
+  // stretch length: fixed on contiguous pages (the host sets p.part to it)
+  const int S = kContig ? KVQ_ATTN_MMA_PART : p.part;
+  const int p0 = part * S;
   if (p0 >= L) {
     if (part == 0) {  // empty context: the output is zero
       for (int i = tid; i < p.G * kD; i += kThreads)
@@ -353,9 +355,9 @@ paged_attention_mma_kernel(const AttnParams p) {
     }
     return;
   }
-  const int nparts = (L + p.part - 1) / p.part;
+  const int nparts = (L + S - 1) / S;
   // the partition's tokens split evenly over the warps, in whole steps
-  const int ntok = min(p.part, L - p0);
+  const int ntok = min(S, L - p0);
   const int quarter =
       (ntok + kWarps * kStep - 1) / (kWarps * kStep) * kStep;
   const int w0 = p0 + warp * quarter;
@@ -807,10 +809,12 @@ paged_attention_mma_kernel(const AttnParams p) {
       }
     }
   __syncthreads();
-  // once per head: M, the warps' factors exp2(m_w - M) and the denominator
+  // once per head: M, the warps' factors exp2(m_w - M), the denominator and
+  // its reciprocal
   float* sF = sL + kWarps * 16;  // [16][kWarps] factors (16-byte rows)
   float* sD = sF + 16 * kWarps;  // [16] denominators
   float* sX = sD + 16;           // [16] M
+  float* sI = sX + 16;           // [16] 1 / denominator
   if (tid < p.G) {
     const int hh = tid;
     float M = sM[hh];
@@ -824,6 +828,7 @@ paged_attention_mma_kernel(const AttnParams p) {
       den += sL[w * 16 + hh] * f;
     }
     sD[hh] = den;
+    sI[hh] = den > 0.f ? 1.0f / den : 0.f;
     sX[hh] = M;
   }
   __syncthreads();
@@ -838,16 +843,16 @@ paged_attention_mma_kernel(const AttnParams p) {
     acc += col[16 * kMergeRow] * f.y;
     acc += col[32 * kMergeRow] * f.z;
     acc += col[48 * kMergeRow] * f.w;
-    const float den = sD[hh];
+    const float den = sD[hh], inv = sI[hh];
     if (nparts == 1) {
-      const float y = den > 0.f ? acc * (1.0f / den) * v_scale : 0.f;
+      const float y = den > 0.f ? acc * inv * v_scale : 0.f;
       p.out[b * p.out_stride0 + (kh * p.G + hh) * kD + d] =
           float_to_out<kF16>(y);
     } else {
       const int64_t r =
           (static_cast<int64_t>(b) * p.Hq + kh * p.G + hh) * p.max_parts +
           part;
-      p.tmp_out[r * kD + d] = den > 0.f ? acc * (1.0f / den) : 0.f;
+      p.tmp_out[r * kD + d] = den > 0.f ? acc * inv : 0.f;
       if (d == 0) {
         p.max_logits[r] = sX[hh];
         p.exp_sums[r] = den;
@@ -863,7 +868,8 @@ cudaError_t launch_mma(const AttnParams& caller, cudaStream_t stream) {
   // warp ranges; the scratch rows keep the caller's max_parts stride and
   // need fewer entries).  A warp range must span at most 32 blocks.
   AttnParams p = caller;
-  if (kContig && p.part < KVQ_ATTN_MMA_PART) p.part = KVQ_ATTN_MMA_PART;
+  // (the caller's partitions are at most 512 tokens)
+  if (kContig) p.part = KVQ_ATTN_MMA_PART;
   const int parts =
       static_cast<int>((static_cast<int64_t>(p.len_cap) + p.part - 1) / p.part);
   static bool configured[64] = {false};  // per instantiation and device
