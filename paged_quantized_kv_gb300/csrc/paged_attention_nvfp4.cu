@@ -1214,6 +1214,8 @@ paged_attention_pipe_kernel(const AttnParams p) {
 // may leave.  Per dim, the sums run over the partitions in order.
 constexpr int kMergeThreads = 256;
 constexpr int kMergeRows = kMergeThreads / 16;
+// Rows of at most this many partitions issue all their loads at once.
+constexpr int kMergeFew = 4;
 
 template <bool kF16>
 __global__ void __launch_bounds__(kMergeThreads)
@@ -1232,18 +1234,43 @@ attention_merge_kernel(const AttnParams p) {
   if (!live || nparts <= 1) return;
   const int64_t row0 = row * p.max_parts;
   float M = -INFINITY;
-#pragma unroll 4
-  for (int i = 0; i < nparts; ++i) M = fmaxf(M, p.max_logits[row0 + i]);
   float den = 0.f, acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll 2
-  for (int i = 0; i < nparts; ++i) {
-    const float w = p.exp_sums[row0 + i] * ex2(p.max_logits[row0 + i] - M);
+  auto add = [&](float w, const float4& x, const float4& y) {
     den += w;
-    const float4* src =
-        reinterpret_cast<const float4*>(p.tmp_out + (row0 + i) * kD + 8 * sub);
-    const float4 x = src[0], y = src[1];
     acc[0] += w * x.x; acc[1] += w * x.y; acc[2] += w * x.z; acc[3] += w * x.w;
     acc[4] += w * y.x; acc[5] += w * y.y; acc[6] += w * y.z; acc[7] += w * y.w;
+  };
+  if (nparts <= kMergeFew) {
+    // every load of the row in one round trip, then the same sums in order
+    float ml[kMergeFew], es[kMergeFew];
+    float4 xs[kMergeFew], ys[kMergeFew];
+#pragma unroll
+    for (int i = 0; i < kMergeFew; ++i) {
+      if (i < nparts) {
+        ml[i] = p.max_logits[row0 + i];
+        es[i] = p.exp_sums[row0 + i];
+        const float4* src = reinterpret_cast<const float4*>(
+            p.tmp_out + (row0 + i) * kD + 8 * sub);
+        xs[i] = src[0];
+        ys[i] = src[1];
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < kMergeFew; ++i)
+      if (i < nparts) M = fmaxf(M, ml[i]);
+#pragma unroll
+    for (int i = 0; i < kMergeFew; ++i)
+      if (i < nparts) add(es[i] * ex2(ml[i] - M), xs[i], ys[i]);
+  } else {
+#pragma unroll 4
+    for (int i = 0; i < nparts; ++i) M = fmaxf(M, p.max_logits[row0 + i]);
+#pragma unroll 2
+    for (int i = 0; i < nparts; ++i) {
+      const float4* src = reinterpret_cast<const float4*>(
+          p.tmp_out + (row0 + i) * kD + 8 * sub);
+      add(p.exp_sums[row0 + i] * ex2(p.max_logits[row0 + i] - M), src[0],
+          src[1]);
+    }
   }
   const float f = den > 0.f ? 1.0f / den : 0.f;
   const float vs = __ldg(p.v_scale);
