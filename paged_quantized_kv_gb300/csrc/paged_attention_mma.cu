@@ -375,6 +375,14 @@ paged_attention_mma_kernel(const AttnParams p) {
       bt_lane = __ldg(p.block_table + b * p.bt_stride + e0 + lane);
   }
 
+  // Logit scale in log2 units, made positive so that the maximum of the
+  // unscaled logits gives the maximum of the scaled ones: a negative scale
+  // negates the staged query (exact), a zero one zeroes it (every logit 0).
+  float c2 = p.scale * __ldg(p.k_scale) * kLog2e;
+  const uint32_t qflip = c2 < 0.f ? 0x80008000u : 0u;
+  const bool qzero = c2 == 0.f;
+  c2 = qzero ? 1.f : fabsf(c2);
+
   // query fragments into shared memory, once per CTA: entry (n, i, lane)
   // = lane (g, t)'s dims 32t + 8i .. + 7 of head 8n + g, as fp16
   const uint32_t qbase = smem_u32(smem) + SL::kQOff;
@@ -392,6 +400,8 @@ paged_attention_mma_kernel(const AttnParams p) {
         v.z = bf16x2_f16x2(v.z);
         v.w = bf16x2_f16x2(v.w);
       }
+      v.x ^= qflip; v.y ^= qflip; v.z ^= qflip; v.w ^= qflip;
+      if (qzero) v = make_uint4(0u, 0u, 0u, 0u);
     }
     asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(
                      qbase + e * 16),
@@ -566,7 +576,6 @@ paged_attention_mma_kernel(const AttnParams p) {
     for (int mb = 0; mb < 8; ++mb)
       o[mb][n][0] = o[mb][n][1] = o[mb][n][2] = o[mb][n][3] = 0.f;
   }
-  const float c2 = p.scale * __ldg(p.k_scale) * kLog2e;
   // byte selectors (pages that are not contiguous): K scales of groups 2t,
   // 2t+1 (linear: bytes 2t, 2t+1 of the row; swizzled: bytes off%4 and
   // 4 + off%4 of the band row, off%4 = g%4 because steps start at multiples
@@ -663,7 +672,8 @@ paged_attention_mma_kernel(const AttnParams p) {
     // The weights are exp2 of the scaled logits minus a reference m_run that
     // moves only when a step's maximum exceeds it by more than kLazy (then
     // every accumulator of the warp is rescaled at once); in between the
-    // weights stay below 2^kLazy.
+    // weights stay below 2^kLazy.  v holds the unscaled logits; c2 > 0 is
+    // applied to their maxima and inside each weight's exponent (one FMA).
     float v[NB][2][4];
     bool grow = false;
 #pragma unroll
@@ -673,14 +683,14 @@ paged_attention_mma_kernel(const AttnParams p) {
 #pragma unroll
         for (int r = 0; r < 4; ++r) {
           const bool ok = (kvalid >> (2 * h + (r >> 1))) & 1u;
-          v[n][h][r] = ok ? sacc[h][n][r] * c2 : -INFINITY;
+          v[n][h][r] = ok ? sacc[h][n][r] : -INFINITY;
         }
 #pragma unroll
       for (int c = 0; c < 2; ++c) {  // head 8n + 2t + c: this lane's tokens
         const float bm = fmaxf(fmaxf(v[n][0][c], v[n][0][2 + c]),
                                fmaxf(v[n][1][c], v[n][1][2 + c]));
-        bmax[n][c] = bm;
-        grow |= bm > m_run[n][c] + kLazy;  // false while both are -inf
+        bmax[n][c] = bm * c2;
+        grow |= bmax[n][c] > m_run[n][c] + kLazy;  // false while both -inf
       }
     }
     // the step's maximum over all its tokens exceeds the reference by more
@@ -714,10 +724,11 @@ paged_attention_mma_kernel(const AttnParams p) {
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         // an unusable token's -inf gives 0 (m_neg is finite)
-        const uint32_t pl = pack_f16x2(ex2(v[n][h][0] + m_neg[n][0]),
-                                       ex2(v[n][h][1] + m_neg[n][1]));
-        const uint32_t ph = pack_f16x2(ex2(v[n][h][2] + m_neg[n][0]),
-                                       ex2(v[n][h][3] + m_neg[n][1]));
+        auto wgt = [&](int r) {
+          return ex2(fmaf(v[n][h][r], c2, m_neg[n][r & 1]));
+        };
+        const uint32_t pl = pack_f16x2(wgt(0), wgt(1));
+        const uint32_t ph = pack_f16x2(wgt(2), wgt(3));
         pb[h][n][0] = transpose8x8(pl);  // token g
         pb[h][n][1] = transpose8x8(ph);  // token g + 8
       }

@@ -171,6 +171,20 @@ def test_one_hot_logits(orc, kernel):
     _check(orc, wl, kernel=kernel)
 
 
+@pytest.mark.parametrize("kernel", KERNELS, ids=KIDS)
+@pytest.mark.parametrize("scale", [-0.088, 0.0, -50.0])
+@pytest.mark.parametrize("Hq", [16, 32])
+def test_negative_and_zero_scale(orc, Hq, scale, kernel):
+    """A negative softmax scale (the largest weights go to the smallest dot
+    products; -50 makes them one-hot) and a zero one (every logit 0: each
+    output is the mean of its context's values), over contexts of several
+    stretches and partitions, with 8 and 16 query heads per KV head."""
+    wl = W.make_attention(f"scale{scale}_{Hq}", 61, [300, 1500, 40, 2600],
+                          num_q_heads=Hq, num_kv_heads=2, head_size=128,
+                          block_size=16, scale=scale)
+    _check(orc, wl, kernel=kernel)
+
+
 def test_store_then_attention(orc):
     """Pages written by the GPU store from bf16 K/V (scales as a checkpoint
     would give), read by the attention, against the oracle on the same
