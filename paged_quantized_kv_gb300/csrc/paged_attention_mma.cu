@@ -200,7 +200,7 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b,
 // products have at most 6 significant bits.
 template <int kHalf>
 __device__ __forceinline__ void dequant_word(uint32_t w, uint32_t sfp,
-                                                uint32_t (&o)[4]) {
+                                             uint32_t (&o)[4]) {
   if constexpr (kHalf == 0)
     asm("{ .reg .b8 q0, q1, q2, q3;\n"
         "  .reg .b32 h0, h1, h2, h3, sb;\n"
