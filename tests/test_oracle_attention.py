@@ -8,8 +8,10 @@ KV head h / (Hq / Hkv).  Pinned, independently of the oracle's own loops, by
 * torch's scaled_dot_product_attention in float64 (an independent library
   routine) on the K/V rows the load oracle dequantises -- exact in bf16
   when k_scale and v_scale are powers of two -- with the KV heads repeated
-  per query group (HND, NHD, swizzled K scales, fp16 queries);
-* closed forms: a zero query averages the value rows; a one-token context
+  per query group (HND, NHD, swizzled K scales, fp16 queries, negative
+  and zero softmax scales);
+* closed forms: a zero query, or a zero softmax scale, averages the value
+  rows; a one-token context
   returns that token's value row; an empty context returns zeros;
 * invariances: k_scale * c with scale / c (c a power of two) changes
   nothing, v_scale * 2 doubles the output, moving pages to other blocks
@@ -93,6 +95,8 @@ def check_sdpa_agreement(o):
         dict(seed=3, lens=[50, 64], Hq=16, Hkv=2, D=64, B=32,
              flags=oracle.F_SWIZZLE_K_SCALE),
         dict(seed=4, lens=[21, 9], dtype=W.DTYPE_F16),
+        dict(seed=5, lens=[30, 12], scale=-0.2),    # negative softmax scale
+        dict(seed=6, lens=[25, 3], scale=0.0),      # zero: uniform weights
     ]
     for case in cases:
         for layout in LAYOUTS:
@@ -118,6 +122,16 @@ def check_sdpa_agreement(o):
 def check_zero_query_is_mean(o):
     wl = _wl(11, [7, 30, 3])
     wl.query[:] = 0
+    out, _ = _attend(o, wl)
+    G = wl.num_q_heads // wl.num_kv_heads
+    for b, (k, v) in enumerate(_dequant(o, wl)):
+        mean = v.mean(axis=0)                       # [Hkv, D]
+        assert np.allclose(out[b], np.repeat(mean, G, axis=0), rtol=0,
+                           atol=1e-13 * (1 + np.abs(mean).max()))
+
+
+def check_zero_scale_is_mean(o):
+    wl = _wl(17, [9, 40, 2], scale=0.0)
     out, _ = _attend(o, wl)
     G = wl.num_q_heads // wl.num_kv_heads
     for b, (k, v) in enumerate(_dequant(o, wl)):
@@ -196,6 +210,7 @@ def check_mag(o):
 
 
 CHECKS = [check_sdpa_agreement, check_zero_query_is_mean,
+          check_zero_scale_is_mean,
           check_single_token_and_empty, check_scale_invariances,
           check_page_relocation, check_one_hot_limit, check_mag]
 
