@@ -11,8 +11,8 @@ KV head h / (Hq / Hkv).  Pinned, independently of the oracle's own loops, by
   per query group (HND, NHD, swizzled K scales, fp16 queries, negative
   and zero softmax scales);
 * closed forms: a zero query, or a zero softmax scale, averages the value
-  rows; a one-token context
-  returns that token's value row; an empty context returns zeros;
+  rows; a one-token context returns that token's value row; an empty
+  context returns zeros;
 * invariances: k_scale * c with scale / c (c a power of two) changes
   nothing, v_scale * 2 doubles the output, moving pages to other blocks
   changes nothing;
