@@ -5,8 +5,11 @@ One step = the long-context mix: an NVFP4 paged store of 131072 tokens
 followed by an indexer-K gather of 256 sequences x 512 tokens (block_size
 64, head_dim 128, 8192-block cache).  Inputs are seeded synthetic arrays
 copied to HBM before timing; steps run back to back with inputs larger than
-L2 (the store streams 689 MB per step; the gather rotates over 4 buffer
-sets).  The JSON line also carries single-launch times after an L2 flush.
+L2 (the store streams 689 MB per step; the gather rotates over 8 buffer
+sets).  The JSON line also carries, per kernel, the median and spread of
+repeated back-to-back spans, and for every named configuration (tiny,
+decode store, prefill store, prefill gather, long mix) single launches on a
+clean L2 and back-to-back spans, beside the oracle timed on the host cores.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -202,6 +205,150 @@ class ClockSampler:
 QUEUE_S_PER_CALL = 40e-6  # GPU sleep per queued call (host enqueue time)
 GATHER_SETS = 8  # gather buffer sets rotated so no launch finds its data in
 # L2 (8 x 35 MB > the 129 MB L2, even in the gather-only loop)
+SPANS = 11  # timed spans per kernel leg, after one untimed warm-up span
+COLD_REPS = 100  # single launches per cold (clean-L2) median
+
+
+class Timer:
+    """CUDA-event timing on one stream.
+
+    ``span_ms``: mean GPU time per call of `count` back-to-back calls
+    between two events.  The calls are queued behind a GPU sleep long enough
+    for the host to enqueue all of them (the binding spends ~10 us of host
+    time per call, more than a short kernel's GPU time, and would otherwise
+    pace the GPU); the sleep runs before the first event.
+
+    ``stats``: one untimed span (the first calls on freshly allocated
+    buffers measure up to 15 % slower), then SPANS timed spans of `calls`
+    calls each; median, min and max of the per-call times.
+
+    ``cold``: single launches, each after the L2 is emptied of anything the
+    call uses and left clean (a 256 MiB write, then a 256 MiB read, so the
+    write's dirty lines are written back before the launch), an event on
+    each side of the launch; the median of `reps`."""
+
+    def __init__(self, dev, stream):
+        import torch
+        self.torch = torch
+        self.dev = dev
+        self.stream = stream
+        self._flush_w = None
+        self._flush_r = None
+
+    def span_ms(self, fn, count):
+        torch = self.torch
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        torch.cuda._sleep(int(2e9 * max(0.005, count * QUEUE_S_PER_CALL)))
+        e0.record(self.stream)
+        for i in range(count):
+            fn(i)
+        e1.record(self.stream)
+        torch.cuda.synchronize(self.dev)
+        return e0.elapsed_time(e1) / count
+
+    def stats(self, fn, calls, spans=SPANS):
+        self.span_ms(fn, calls)  # warm-up span
+        ms = sorted(self.span_ms(fn, calls) for _ in range(spans))
+        return {"ms": round(statistics.median(ms), 5),
+                "ms_min": round(ms[0], 5), "ms_max": round(ms[-1], 5),
+                "spans": spans, "calls_per_span": calls}
+
+    def clean_l2(self, i):
+        torch = self.torch
+        if self._flush_w is None:
+            self._flush_w = torch.empty(FLUSH_BYTES // 8, dtype=torch.int64,
+                                        device=self.dev)
+            self._flush_r = torch.zeros(FLUSH_BYTES // 8, dtype=torch.int64,
+                                        device=self.dev)
+        self._flush_w.fill_(i)
+        self._flush_r.max()
+
+    def cold(self, fn, reps=COLD_REPS):
+        torch = self.torch
+        ms = []
+        for i in range(reps + 2):
+            self.clean_l2(i)
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(self.stream)
+            fn(i)
+            e1.record(self.stream)
+            torch.cuda.synchronize(self.dev)
+            if i >= 2:
+                ms.append(e0.elapsed_time(e1))
+        ms.sort()
+        return {"us": round(statistics.median(ms) * 1e3, 2),
+                "us_min": round(ms[0] * 1e3, 2),
+                "us_max": round(ms[-1] * 1e3, 2), "launches": reps}
+
+    def free(self):
+        self._flush_w = self._flush_r = None
+
+
+def gbs(byts, ms):
+    return round(byts / (ms / 1e3) / 1e9, 1)
+
+
+def leg(st, byts, peak, tokens=None, tokens_key="tokens_per_s"):
+    """A per-kernel record: the median time with its spread, GB/s and
+    fraction of the HBM peak of the median."""
+    out = dict(st)
+    out["GB_s"] = gbs(byts, st["ms"])
+    out["frac_of_peak"] = round(byts / (st["ms"] / 1e3) / 1e9 / peak, 4)
+    if tokens is not None:
+        out[tokens_key] = round(tokens / (st["ms"] / 1e3), 1)
+    out["algorithmic_bytes"] = int(byts)
+    return out
+
+
+def store_tensors(st, kvq, dev, fill=0xAA, sets=1):
+    """Device copies of a store workload: `sets` copies of the K/V source
+    (and of the cache, each pre-filled with `fill`) at different addresses,
+    the slots and the scales."""
+    import torch
+    T, H, D = st.num_tokens, st.num_heads, st.head_size
+    out = []
+    slots = torch.from_numpy(st.slot_mapping).to(dev)
+    ks = torch.tensor([float(st.k_scale)], dtype=torch.float32, device=dev)
+    vs = torch.tensor([float(st.v_scale)], dtype=torch.float32, device=dev)
+    for _ in range(sets):
+        src = torch.from_numpy(st.src.view(np.int16)).to(dev).view(
+            torch.bfloat16)
+        key = src.as_strided((T, H, D), (st.key_stride0, D, 1),
+                             st.key_offset)
+        value = src.as_strided((T, H, D), (st.value_stride0, D, 1),
+                               st.value_offset)
+        kv, kc, vc = kvq.alloc_nvfp4_cache(st.num_blocks, st.block_size, H,
+                                           D, device=dev, fill=fill)
+        out.append(dict(key=key, value=value, kv=kv, kc=kc, vc=vc,
+                        slots=slots, ks=ks, vs=vs))
+    return out
+
+
+def gather_tensors(ga, dev, sets=1):
+    import torch
+    n = ga.total_tokens
+    return [dict(cache=torch.from_numpy(ga.cache).to(dev).view(
+                     ga.num_blocks, -1),
+                 bt=torch.from_numpy(ga.block_table).to(dev),
+                 cu=torch.from_numpy(ga.cu_seq_lens).to(dev),
+                 k=torch.empty((n, ga.head_dim), dtype=torch.uint8,
+                               device=dev),
+                 s=torch.empty((n, 4), dtype=torch.uint8, device=dev))
+            for _ in range(sets)]
+
+
+def run_store(kvq, t, flags, dev_err, sh):
+    kvq.kvq_store_nvfp4(t["key"], t["value"], t["kc"], t["vc"], t["slots"],
+                        t["ks"], t["vs"], flags=flags, dev_error=dev_err,
+                        stream=sh)
+
+
+def run_gather(kvq, g, block_size, flags, dev_err, sh):
+    kvq.kvq_gather_indexer_k(g["cache"], g["k"], g["s"], g["bt"], g["cu"],
+                             block_size=block_size, flags=flags,
+                             dev_error=dev_err, stream=sh)
 
 
 def run_ours(args):
@@ -217,65 +364,34 @@ def run_ours(args):
     import __graft_entry__
     __graft_entry__.build()
     from paged_quantized_kv_gb300 import kvq
+    from paged_quantized_kv_gb300 import workloads as wlmod
 
     st, ga = make_workload(rank)
     T, H, D = st.num_tokens, st.num_heads, st.head_size
 
     # ---- device-resident inputs and outputs -------------------------------
-    src = torch.from_numpy(st.src.view(np.int16)).to(dev).view(torch.bfloat16)
-    key = src.as_strided((T, H, D), (st.key_stride0, D, 1), st.key_offset)
-    value = src.as_strided((T, H, D), (st.value_stride0, D, 1),
-                           st.value_offset)
-    slots = torch.from_numpy(st.slot_mapping).to(dev)
-    ks = torch.tensor([float(st.k_scale)], dtype=torch.float32, device=dev)
-    vs = torch.tensor([float(st.v_scale)], dtype=torch.float32, device=dev)
-    kv, kc, vc = kvq.alloc_nvfp4_cache(st.num_blocks, st.block_size, H, D,
-                                       device=dev, fill=0xAA)
+    (s4,) = store_tensors(st, kvq, dev)
     n = ga.total_tokens
-    gsets = []
-    for _ in range(GATHER_SETS):  # same bytes at different addresses
-        gsets.append(dict(
-            cache=torch.from_numpy(ga.cache).to(dev).view(ga.num_blocks, -1),
-            bt=torch.from_numpy(ga.block_table).to(dev),
-            cu=torch.from_numpy(ga.cu_seq_lens).to(dev),
-            k=torch.empty((n, ga.head_dim), dtype=torch.uint8, device=dev),
-            s=torch.empty((n, 4), dtype=torch.uint8, device=dev)))
+    gsets = gather_tensors(ga, dev, GATHER_SETS)  # same bytes, other addresses
     dev_err = torch.zeros(1, dtype=torch.int32, device=dev)
     stream = torch.cuda.current_stream(dev)
     sh = stream.cuda_stream
+    tm = Timer(dev, stream)
+    EARLY = kvq.KVQ_F_PDL_EARLY_READ
+    PDL = kvq.KVQ_F_PDL
 
     def store(flags):
-        kvq.kvq_store_nvfp4(key, value, kc, vc, slots, ks, vs, flags=flags,
-                            dev_error=dev_err, stream=sh)
+        run_store(kvq, s4, flags, dev_err, sh)
 
     def gather(i, flags):
-        g = gsets[i % GATHER_SETS]
-        kvq.kvq_gather_indexer_k(g["cache"], g["k"], g["s"], g["bt"], g["cu"],
-                                 block_size=ga.block_size, flags=flags,
-                                 dev_error=dev_err, stream=sh)
+        run_gather(kvq, gsets[i % GATHER_SETS], ga.block_size, flags,
+                   dev_err, sh)
 
     def step(i, flags):
-        store(kvq.KVQ_F_PDL_EARLY_READ if flags else 0)
-        gather(i, kvq.KVQ_F_PDL_EARLY_READ if flags else 0)
-
-    def span_ms(fn, count):
-        """Mean GPU time per call of `count` back-to-back calls between two
-        events.  The calls are queued behind a GPU sleep long enough for the
-        host to enqueue all of them: the binding spends ~10 us of host time
-        per call, more than a short kernel's GPU time, and would otherwise
-        pace the GPU.  The sleep runs before the first event."""
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        torch.cuda._sleep(int(2e9 * max(0.005, count * QUEUE_S_PER_CALL)))
-        e0.record(stream)
-        for i in range(count):
-            fn(i)
-        e1.record(stream)
-        torch.cuda.synchronize(dev)
-        return e0.elapsed_time(e1) / count
+        store(EARLY if flags else 0)
+        gather(i, EARLY if flags else 0)
 
     W = max(args.warmup, 3)
-    PDL = kvq.KVQ_F_PDL
     for i in range(W):
         step(i, PDL)
         step(i, 0)
@@ -290,45 +406,50 @@ def run_ours(args):
         torch.distributed.barrier()
     torch.cuda.synchronize(dev)
     t0 = time.perf_counter()
-    step_ms = span_ms(lambda i: step(i, PDL), K)
+    step_ms = tm.span_ms(lambda i: step(i, PDL), K)
     if world > 1:
         torch.distributed.barrier()
     wall = time.perf_counter() - t0
-    # per-kernel averages: each kernel alone, back to back (inputs larger
-    # than L2: the store streams 689 MB per call; the gather rotates over
-    # GATHER_SETS buffer sets)
-    store_ms = span_ms(lambda i: store(kvq.KVQ_F_PDL_EARLY_READ), K)
-    store_pdl_ms = span_ms(lambda i: store(PDL), K)
-    gather_ms = span_ms(lambda i: gather(i, kvq.KVQ_F_PDL_EARLY_READ), K)
-    gather_meta_ms = span_ms(lambda i: gather(i, kvq.KVQ_F_PDL_EARLY_META), K)
-    plain = {"step_ms": span_ms(lambda i: step(i, 0), K),
-             "store_ms": span_ms(lambda i: store(0), K),
-             "gather_ms": span_ms(lambda i: gather(i, 0), K)}
+    # the same K-step span repeated, for its spread
+    step_rep = sorted(tm.span_ms(lambda i: step(i, PDL), K) for _ in range(5))
+    peak, peak_kind = measured_hbm_peak()
+    st_bytes = st.algorithmic_bytes()
+    ga_bytes = ga.algorithmic_bytes()
+
+    # ---- per-kernel legs: SPANS spans each, median and spread -------------
+    # (inputs larger than L2: the store streams 689 MB per call; the gather
+    # rotates over GATHER_SETS buffer sets)
+    store_st = tm.stats(lambda i: store(EARLY), 20)
+    store_pdl = tm.stats(lambda i: store(PDL), 20)
+    gather_st = tm.stats(lambda i: gather(i, EARLY), 200)
+    gather_meta = tm.stats(lambda i: gather(i, kvq.KVQ_F_PDL_EARLY_META), 200)
+    plain = {"step": tm.stats(lambda i: step(i, 0), 20),
+             "store": tm.stats(lambda i: store(0), 20),
+             "gather": tm.stats(lambda i: gather(i, 0), 200)}
     # the store's other input type and cache layout, same shape
-    key16 = key.to(torch.float16)
-    value16 = value.to(torch.float16)
+    key16 = s4["key"].to(torch.float16)
+    value16 = s4["value"].to(torch.float16)
     kv_n, kc_n, vc_n = kvq.alloc_nvfp4_cache(
         st.num_blocks, st.block_size, H, D, layout=kvq.KVQ_LAYOUT_NHD,
         device=dev, fill=0xAA)
-    variants_ms = {
-        "store_fp16_hnd": span_ms(lambda i: kvq.kvq_store_nvfp4(
-            key16, value16, kc, vc, slots, ks, vs, flags=PDL,
-            dev_error=dev_err, stream=sh), K),
-        "store_bf16_nhd": span_ms(lambda i: kvq.kvq_store_nvfp4(
-            key, value, kc_n, vc_n, slots, ks, vs, flags=PDL,
-            dev_error=dev_err, stream=sh), K),
+    variants = {
+        "store_fp16_hnd": tm.stats(lambda i: kvq.kvq_store_nvfp4(
+            key16, value16, s4["kc"], s4["vc"], s4["slots"], s4["ks"],
+            s4["vs"], flags=PDL, dev_error=dev_err, stream=sh), 20),
+        "store_bf16_nhd": tm.stats(lambda i: kvq.kvq_store_nvfp4(
+            s4["key"], s4["value"], kc_n, vc_n, s4["slots"], s4["ks"],
+            s4["vs"], flags=PDL, dev_error=dev_err, stream=sh), 20),
     }
     del key16, value16, kv_n, kc_n, vc_n
     # the read side: the long-context pages read back to bf16 rows
-    from paged_quantized_kv_gb300 import workloads as wlmod
     lbt, lcu = wlmod.sequences_of_store(st, 512)
     lbt_d = torch.from_numpy(lbt).to(dev)
     lcu_d = torch.from_numpy(lcu).to(dev)
     k_out = torch.empty((T, H, D), dtype=torch.bfloat16, device=dev)
     v_out = torch.empty((T, H, D), dtype=torch.bfloat16, device=dev)
-    load_ms = span_ms(lambda i: kvq.kvq_load_nvfp4(
-        kc, vc, lbt_d, lcu_d, ks, vs, k_out, v_out,
-        flags=kvq.KVQ_F_PDL_EARLY_META, dev_error=dev_err, stream=sh), K)
+    load_st = tm.stats(lambda i: kvq.kvq_load_nvfp4(
+        s4["kc"], s4["vc"], lbt_d, lcu_d, s4["ks"], s4["vs"], k_out, v_out,
+        flags=kvq.KVQ_F_PDL_EARLY_META, dev_error=dev_err, stream=sh), 20)
     load_bytes = wlmod.load_algorithmic_bytes(st, lbt, lcu)
     del k_out, v_out
     # the indexer cache's write side on the gather's shape (K rows rotated
@@ -340,12 +461,12 @@ def run_ours(args):
     islots = torch.from_numpy(iw.slot_mapping).to(dev)
     icache = torch.empty((iw.num_blocks, iw.block_size, iw.head_dim + 4),
                          dtype=torch.uint8, device=dev)
-    istore_ms = span_ms(lambda i: kvq.kvq_store_indexer_k(
-        ik[i % GATHER_SETS], icache, islots, flags=kvq.KVQ_F_PDL_EARLY_READ,
-        dev_error=dev_err, stream=sh), K)
-    istore_pdl_ms = span_ms(lambda i: kvq.kvq_store_indexer_k(
+    istore_st = tm.stats(lambda i: kvq.kvq_store_indexer_k(
+        ik[i % GATHER_SETS], icache, islots, flags=EARLY, dev_error=dev_err,
+        stream=sh), 200)
+    istore_pdl = tm.stats(lambda i: kvq.kvq_store_indexer_k(
         ik[i % GATHER_SETS], icache, islots, flags=PDL, dev_error=dev_err,
-        stream=sh), K)
+        stream=sh), 200)
     istore_bytes = iw.algorithmic_bytes()
     del ik, icache
     # decode attention over NVFP4 pages: one step of Llama-3.1-70B-shaped
@@ -353,12 +474,8 @@ def run_ours(args):
     # 359 MB of pages per call, larger than L2)
     aw = wlmod.attention_workload(rank_seed(5, rank))
     attn = attention_inputs(aw, kvq, dev)
-    attn_ms = span_ms(lambda i: run_attention(attn, kvq, PDL, dev_err, sh),
-                      K)
-    attn_pipe_ms = span_ms(lambda i: run_attention(
-        attn, kvq, PDL | kvq.KVQ_F_ATTN_PIPELINED, dev_err, sh), K)
-    attn_tc_ms = span_ms(lambda i: run_attention(
-        attn, kvq, PDL | kvq.KVQ_F_ATTN_TCGEN05, dev_err, sh), K)
+    attn_st = tm.stats(lambda i: run_attention(attn, kvq, PDL, dev_err, sh),
+                       25)
     attn_bytes = aw.algorithmic_bytes()
     attn_ctx = int(aw.context_lens.astype(np.int64).sum())
     del attn
@@ -373,17 +490,18 @@ def run_ours(args):
     torch.cuda.synchronize(dev)
     clocks = sampler.stop()
     assert int(dev_err.item()) == 0, "device error flag raised"
-    region_ms = step_ms * K
-    cold = single_launch_cold(lambda: store(0), lambda: gather(0, 0), dev)
 
-    st_bytes = st.algorithmic_bytes()
-    ga_bytes = ga.algorithmic_bytes()
+    # ---- each named configuration on its own ------------------------------
+    configs = config_legs(args, kvq, wlmod, tm, dev, dev_err, sh, peak, rank,
+                          long_step=dict(store=lambda i: store(0),
+                                         gather=lambda i: gather(i, 0)))
+    tm.free()
+    assert int(dev_err.item()) == 0, "device error flag raised"
+
     step_s = max_over_ranks(step_ms / 1e3, world, dev)
     total_bytes = sum_over_ranks(float(st_bytes + ga_bytes), world, dev)
     total_tokens = sum_over_ranks(float(T + n), world, dev)
-    peak, peak_kind = measured_hbm_peak()
-    store_gbs = st_bytes / (store_ms / 1e3) / 1e9
-    gather_gbs = ga_bytes / (gather_ms / 1e3) / 1e9
+    store_gbs = st_bytes / (store_st["ms"] / 1e3) / 1e9
     traffic = profiled_traffic("store_nvfp4_long.md", "store_nvfp4.cu")
 
     e2e = run_e2e(args, st, ga, dev, kvq)
@@ -424,80 +542,53 @@ def run_ours(args):
                       "between two CUDA events, all K queued behind a GPU "
                       "sleep before the first event (so the binding's host "
                       "time per call does not pace the GPU); ms_per_step = "
-                      "span / K, max over ranks.  Per-kernel times: K "
-                      "launches of that kernel alone, back to back, same "
-                      "flags, queued the same way",
+                      "span / K, max over ranks.  Per-kernel legs: one "
+                      f"untimed span, then {SPANS} spans of back-to-back "
+                      "calls of that kernel alone, queued the same way; "
+                      "ms = the median span's time per call, with the min "
+                      "and max",
         },
+        "ms_per_step_spans": {
+            "ms": round(statistics.median(step_rep), 5),
+            "ms_min": round(step_rep[0], 5), "ms_max": round(step_rep[-1], 5),
+            "spans": len(step_rep), "calls_per_span": K},
         "tokens_per_s": round(total_tokens / step_s, 1),
         "kernels": {
-            "store_nvfp4": {
-                "ms": round(store_ms, 5),
-                "pdl_only_ms": round(store_pdl_ms, 5),
-                "GB_s": round(store_gbs, 1),
-                "frac_of_peak": round(store_gbs / peak, 4),
-                "tokens_per_s": round(T / (store_ms / 1e3), 1),
-                "algorithmic_bytes": st_bytes},
-            "gather_indexer_k": {
-                "ms": round(gather_ms, 5),
-                "GB_s": round(gather_gbs, 1),
-                "frac_of_peak": round(gather_gbs / peak, 4),
-                "tokens_per_s": round(n / (gather_ms / 1e3), 1),
-                "algorithmic_bytes": ga_bytes,
-                "early_meta_only_ms": round(gather_meta_ms, 5)},
+            "store_nvfp4": dict(
+                leg(store_st, st_bytes, peak, T),
+                pdl_only=leg(store_pdl, st_bytes, peak)),
+            "gather_indexer_k": dict(
+                leg(gather_st, ga_bytes, peak, n),
+                early_meta_only=leg(gather_meta, ga_bytes, peak)),
         },
-        "without_pdl": {k: round(v, 5) for k, v in plain.items()},
-        "load_nvfp4": {
-            "note": "read side: the long-context pages read back to bf16 "
-                    "rows through the block table (not part of the step)",
-            "ms": round(load_ms, 5),
-            "GB_s": round(load_bytes / load_ms / 1e6, 1),
-            "frac_of_peak": round(load_bytes / load_ms / 1e6 / peak, 4),
-            "tokens_per_s": round(T / (load_ms / 1e3), 1),
-            "algorithmic_bytes": load_bytes},
-        "store_variants": {
-            k: {"ms": round(v, 5),
-                "GB_s": round(st_bytes / v / 1e6, 1),
-                "frac_of_peak": round(st_bytes / v / 1e6 / peak, 4)}
-            for k, v in variants_ms.items()},
-        "store_indexer_k": {
-            "note": "write side of the indexer cache on the gather's shape "
-                    "(131072 tokens, head_dim 128, block_size 64), not part "
-                    "of the step; back to back with KVQ_F_PDL_EARLY_READ "
-                    "(K rotated over the buffer sets, the kernel before "
-                    "writes only the cache)",
-            "ms": round(istore_ms, 5),
-            "pdl_only_ms": round(istore_pdl_ms, 5),
-            "GB_s": round(istore_bytes / istore_ms / 1e6, 1),
-            "frac_of_peak": round(istore_bytes / istore_ms / 1e6 / peak, 4),
-            "tokens_per_s": round(iw.num_tokens / (istore_ms / 1e3), 1),
-            "algorithmic_bytes": istore_bytes},
-        "paged_attention_nvfp4": {
-            "note": "decode attention over the NVFP4 pages, one step of "
-                    "Llama-3.1-70B-shaped attention: 200 sequences, 64 "
-                    "query / 8 KV heads, head_size 128, block_size 16, "
-                    "contexts 512 + U[0, 2048]; partition_size 512 (the "
-                    "default warp-level-MMA kernel covers up to 1280 tokens "
-                    "per CTA, then the partition merge); not part of the "
-                    "step",
-            "ms": round(attn_ms, 5),
-            "GB_s": round(attn_bytes / attn_ms / 1e6, 1),
-            "frac_of_peak": round(attn_bytes / attn_ms / 1e6 / peak, 4),
-            "decode_tokens_per_s": round(aw.num_seqs / (attn_ms / 1e3), 1),
-            "context_tokens_per_s": round(attn_ctx / (attn_ms / 1e3), 1),
-            "algorithmic_bytes": attn_bytes,
-            "pipelined_kernel_ms": round(attn_pipe_ms, 5),
-            "pipelined_kernel_frac_of_peak": round(
-                attn_bytes / attn_pipe_ms / 1e6 / peak, 4),
-            "tcgen05_kernel_ms": round(attn_tc_ms, 5),
-            "tcgen05_kernel_frac_of_peak": round(
-                attn_bytes / attn_tc_ms / 1e6 / peak, 4)},
-        "single_launch_after_l2_write_flush": {
-            "note": "each kernel alone after writing a 256 MiB buffer "
-                    "(L2 left dirty), events around the launch; includes "
-                    "the ~4 us event/launch floor an empty kernel shows",
-            "store_ms": cold[0], "gather_ms": cold[1],
-            "store_GB_s": round(st_bytes / cold[0] / 1e6, 1),
-            "gather_GB_s": round(ga_bytes / cold[1] / 1e6, 1)},
+        "without_pdl": {k: leg(v, st_bytes + ga_bytes if k == "step" else
+                               st_bytes if k == "store" else ga_bytes, peak)
+                        for k, v in plain.items()},
+        "load_nvfp4": dict(
+            leg(load_st, load_bytes, peak, T),
+            note="read side: the long-context pages read back to bf16 "
+                 "rows through the block table (not part of the step)"),
+        "store_variants": {k: leg(v, st_bytes, peak)
+                           for k, v in variants.items()},
+        "store_indexer_k": dict(
+            leg(istore_st, istore_bytes, peak, iw.num_tokens),
+            pdl_only=leg(istore_pdl, istore_bytes, peak),
+            note="write side of the indexer cache on the gather's shape "
+                 "(131072 tokens, head_dim 128, block_size 64), not part "
+                 "of the step; back to back with KVQ_F_PDL_EARLY_READ (K "
+                 "rotated over the buffer sets, the kernel before writes "
+                 "only the cache)"),
+        "paged_attention_nvfp4": dict(
+            leg(attn_st, attn_bytes, peak, aw.num_seqs,
+                "decode_tokens_per_s"),
+            context_tokens_per_s=round(attn_ctx / (attn_st["ms"] / 1e3), 1),
+            note="decode attention over the NVFP4 pages, one step of "
+                 "Llama-3.1-70B-shaped attention: 200 sequences, 64 query / "
+                 "8 KV heads, head_size 128, block_size 16, contexts 512 + "
+                 "U[0, 2048]; partition_size 512 (the kernel covers up to "
+                 "1280 tokens per CTA on contiguous pages, then the "
+                 "partition merge); not part of the step"),
+        "configs": configs,
         "roofline": {
             "bound": "hbm",
             "kernel": "store_nvfp4",
@@ -513,19 +604,167 @@ def run_ours(args):
         "e2e": e2e,
         "gpu_launches": 2 * K,
         "gpu_launches_note": "in the timed step region (store + gather per "
-                             "step); the per-kernel loops after it launch "
-                             "their own",
+                             "step); the legs after it launch their own",
         "clocks": clocks,
     }
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(st, ga, args.cpu_sample_tokens)
         line["paged_attention_nvfp4"]["cpu_oracle"] = cpu_attention_baseline(
             aw)
+        cpu_config_legs(configs, rank)
     if world > 1:
         torch.distributed.barrier()
         torch.distributed.destroy_process_group()
     if rank == 0:
         print(json.dumps(line), flush=True)
+
+
+def config_legs(args, kvq, wlmod, tm, dev, dev_err, sh, peak, rank,
+                long_step):
+    """Every named configuration timed alone: single launches after a clean
+    L2 flush (median of COLD_REPS) and back-to-back spans (median of SPANS),
+    beside the floor of an empty launch measured the same way."""
+    import torch
+    EARLY = kvq.KVQ_F_PDL_EARLY_READ
+    out = {}
+    floor = tm.cold(lambda i: torch.cuda._sleep(0))
+    floor_b2b = tm.stats(lambda i: torch.cuda._sleep(0), 200)
+    out["empty_launch_floor"] = {
+        "cold_single_launch": floor,
+        "back_to_back_us": round(floor_b2b["ms"] * 1e3, 3),
+        "note": "a zero-length kernel timed the same two ways: what any "
+                "single launch measured with events costs at least"}
+
+    def store_cfg(idx, name, sets, calls, note):
+        st = wlmod.store_workload(idx, seed=rank_seed(idx, rank))
+        ts = store_tensors(st, kvq, dev, sets=sets)
+        byts = st.algorithmic_bytes()
+        cold = tm.cold(lambda i: run_store(kvq, ts[i % sets], 0, dev_err, sh))
+        b2b = tm.stats(lambda i: run_store(kvq, ts[i % sets], EARLY, dev_err,
+                                           sh), calls)
+        rec = {"kernel": "store_nvfp4", "tokens": st.num_tokens,
+               "stored_tokens": st.stored_tokens,
+               "algorithmic_bytes": int(byts),
+               "cold_single_launch": dict(
+                   cold, GB_s=gbs(byts, cold["us"] / 1e3),
+                   frac_of_peak=round(byts / cold["us"] / 1e3 / peak, 4)),
+               "back_to_back": leg(b2b, byts, peak, st.stored_tokens),
+               "note": note}
+        out[name] = rec
+        del ts
+        return st
+
+    def gather_cfg(idx, name, sets, calls, note):
+        ga = wlmod.gather_workload(idx, seed=rank_seed(idx, rank))
+        gs = gather_tensors(ga, dev, sets)
+        byts = ga.algorithmic_bytes()
+        cold = tm.cold(lambda i: run_gather(kvq, gs[i % sets], ga.block_size,
+                                            0, dev_err, sh))
+        b2b = tm.stats(lambda i: run_gather(kvq, gs[i % sets], ga.block_size,
+                                            EARLY, dev_err, sh), calls)
+        out[name] = {"kernel": "gather_indexer_k", "seqs": ga.num_seqs,
+                     "tokens": ga.total_tokens,
+                     "algorithmic_bytes": int(byts),
+                     "cold_single_launch": dict(
+                         cold, GB_s=gbs(byts, cold["us"] / 1e3),
+                         frac_of_peak=round(byts / cold["us"] / 1e3 / peak,
+                                            4)),
+                     "back_to_back": leg(b2b, byts, peak, ga.total_tokens),
+                     "note": note}
+        del gs
+        return ga
+
+    store_cfg(0, "0_tiny_store", 1, 200,
+              "24 tokens (3 skipped), 2 heads, head_size 64: launch-bound; "
+              "back to back the inputs stay in L2")
+    gather_cfg(0, "0_tiny_gather", 1, 200,
+               "sequences of 5 and 37 tokens: launch-bound; back to back "
+               "the inputs stay in L2")
+    store_cfg(1, "1_decode_store", 1, 200,
+              "256 single-token requests, 8 KV heads, head_size 128, "
+              "random slots over a 65536-block cache: launch-bound (1.35 "
+              "MB); back to back the 1 MB of K/V and the written lines stay "
+              "in L2 (warm), the cold single launch reads from HBM")
+    store_cfg(2, "2_prefill_store", 3, 40,
+              "16 requests x 1024 tokens, 8 KV heads, head_size 128, rows "
+              "2x strided; back to back over 3 input/cache sets (201 MB of "
+              "K/V, none L2-resident at launch)")
+    gather_cfg(3, "3_prefill_gather", GATHER_SETS, 200,
+               "16 sequences of U[1000, 8192] tokens, block_size 64, "
+               "head_dim 128; back to back over 8 buffer sets (8 x 30 MB)")
+    # the long-context mix's two kernels, cold
+    st4, ga4 = make_workload(rank)
+    for key, fn, byts in (("4_long_store", long_step["store"],
+                           st4.algorithmic_bytes()),
+                          ("4_long_gather", long_step["gather"],
+                           ga4.algorithmic_bytes())):
+        cold = tm.cold(fn)
+        out[key] = {"algorithmic_bytes": int(byts),
+                    "cold_single_launch": dict(
+                        cold, GB_s=gbs(byts, cold["us"] / 1e3),
+                        frac_of_peak=round(byts / cold["us"] / 1e3 / peak,
+                                           4)),
+                    "back_to_back": "kernels.store_nvfp4 / "
+                                    "kernels.gather_indexer_k"}
+    return out
+
+
+def cpu_config_legs(configs, rank):
+    """The oracle on each named configuration's full inputs, one thread and
+    every host core (store split by tokens, gather by sequences)."""
+    import oracle
+    from paged_quantized_kv_gb300 import workloads as wlmod
+    o = oracle.get()
+    threads = max(1, os.cpu_count() or 1)
+    for name, idx, kind in (("0_tiny_store", 0, "store"),
+                            ("0_tiny_gather", 0, "gather"),
+                            ("1_decode_store", 1, "store"),
+                            ("2_prefill_store", 2, "store"),
+                            ("3_prefill_gather", 3, "gather")):
+        rec = configs.get(name)
+        if rec is None:
+            continue
+        if kind == "store":
+            st = wlmod.store_workload(idx, seed=rank_seed(idx, rank))
+            ga = oracle_empty_gather(wlmod.gather_workload(0))
+        else:
+            ga = wlmod.gather_workload(idx, seed=rank_seed(idx, rank))
+            st = oracle_empty_store(wlmod.store_workload(0))
+        res = {"kind": "oracle"}
+        for label, nt in (("one_thread", 1), ("all_cores", threads)):
+            cache = np.full(st.cache_bytes, 0xAA, dtype=np.uint8)
+            k = np.empty(max(ga.total_tokens, 1) * ga.head_dim, np.uint8)
+            s = np.empty(max(ga.total_tokens, 1) * 4, np.uint8)
+            t = time.perf_counter()
+            oracle_step_threaded(o, st, ga, cache, k, s, nt)
+            dt = time.perf_counter() - t
+            res[label] = {"seconds": round(dt, 5), "cores": nt,
+                          "GB_s": round(rec["algorithmic_bytes"] / dt / 1e9,
+                                        4)}
+            del cache
+        rec["cpu_oracle"] = res
+
+
+def oracle_empty_store(st):
+    """A store workload with no tokens (the other half of a one-kernel
+    oracle leg)."""
+    from paged_quantized_kv_gb300 import workloads as W
+    return W.StoreWorkload(
+        name="none", num_tokens=0, num_heads=st.num_heads,
+        head_size=st.head_size, block_size=st.block_size, num_blocks=1,
+        src=st.src, key_offset=0, key_stride0=st.key_stride0, value_offset=0,
+        value_stride0=st.value_stride0,
+        slot_mapping=np.zeros(0, np.int64), k_scale=st.k_scale,
+        v_scale=st.v_scale)
+
+
+def oracle_empty_gather(ga):
+    from paged_quantized_kv_gb300 import workloads as W
+    return W.GatherWorkload(
+        name="none", block_size=ga.block_size, head_dim=ga.head_dim,
+        num_blocks=ga.num_blocks, cache=ga.cache,
+        block_table=ga.block_table[:0], cu_seq_lens=np.zeros(1, np.int32),
+        block_stride=ga.block_stride)
 
 
 def attention_inputs(aw, kvq, dev):
@@ -554,28 +793,6 @@ def run_attention(a, kvq, flags, dev_err, stream):
         a["q"], a["kc"], a["vc"], a["bt"], a["lens"], a["ks"], a["vs"],
         a["scale"], a["out"], a["mcl"], 512, es, ml, tmp, flags=flags,
         dev_error=dev_err, stream=stream)
-
-
-def single_launch_cold(store, gather, dev, reps=20):
-    """Median single-launch times (ms) after a 256 MiB write flush."""
-    import torch
-    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
-    out = []
-    for fn in (store, gather):
-        ms = []
-        for i in range(reps + 2):
-            flush.fill_(i & 0xFF)
-            e0 = torch.cuda.Event(enable_timing=True)
-            e1 = torch.cuda.Event(enable_timing=True)
-            e0.record()
-            fn()
-            e1.record()
-            torch.cuda.synchronize(dev)
-            if i >= 2:
-                ms.append(e0.elapsed_time(e1))
-        out.append(round(statistics.median(ms), 5))
-    del flush
-    return out
 
 
 def run_e2e(args, st, ga, dev, kvq):

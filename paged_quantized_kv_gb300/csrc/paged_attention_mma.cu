@@ -48,9 +48,16 @@
 //     weights P^T (tokens x heads, in the logits' accumulator layout) are
 //     transposed into the B fragment of the second product with
 //     movmatrix.
-//   * O^T[16 dims x 8 heads] += V'^T P^T per m-block of 16 head dims, the
-//     dims permuted so that lane (g, t) reads the 8 contiguous bytes
-//     8g .. 8g+7 (group g) of each of its 4 tokens.
+//   * O^T += V'^T P^T per 8-token block, with the contraction index running
+//     over (token, e) pairs so that a V byte (dims 2p, 2p+1 of a token) is
+//     one A register as it stands: the same A meets a B holding each
+//     token's weight at e = 0 (this product sums the even dims) and one
+//     holding it at e = 1 (the odd dims).  Lane (g, t) reads the 8
+//     contiguous bytes 8g .. 8g+7 (group g) of tokens 2t and 2t+1 of each
+//     block; the rows of m-block mb are bytes 2mb and 2mb+1 of the group.
+//   * A step none of whose tokens is left out (all in the warp's range,
+//     every block id valid -- every step but a partial last one) runs a
+//     form with no per-token test at all.
 //   * The 4 warps' (max, sum, O) merge in shared memory; a stretch of a
 //     longer context is written to the caller's scratch (rows max_parts
 //     apart, as for the caller's partitions: a stretch covers at least one
@@ -59,6 +66,8 @@
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdint.h>
+
+#include <type_traits>
 
 #include "kvq_internal.h"
 #include "kvq.h"
@@ -242,21 +251,20 @@ __device__ __forceinline__ uint32_t e4m3x2_f16x2(uint16_t pair) {
   return h;
 }
 
-// Four bytes of e2m1 pairs -> four f16x2 words (exact), byte k -> o[k],
-// the even element in the low half.
-__device__ __forceinline__ void e2m1_word(uint32_t w, uint32_t (&o)[4]) {
-  asm("{ .reg .b8 q0, q1, q2, q3;\n"
-      "  mov.b32 {q0, q1, q2, q3}, %4;\n"
-      "  cvt.rn.f16x2.e2m1x2 %0, q0;  cvt.rn.f16x2.e2m1x2 %1, q1;\n"
-      "  cvt.rn.f16x2.e2m1x2 %2, q2;  cvt.rn.f16x2.e2m1x2 %3, q3; }"
-      : "=r"(o[0]), "=r"(o[1]), "=r"(o[2]), "=r"(o[3])
-      : "r"(w));
-}
-
-__device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
-  uint32_t d;
-  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
-  return d;
+// A pair of fp16 weights {P_lo, P_hi} -> the B registers of the even-dim
+// product ({P_lo, 0}, {P_hi, 0}) and of the odd-dim one ({0, P_lo},
+// {0, P_hi}): packed multiplies by {1, 0} / {0, 1} (exact; the weights are
+// finite and non-negative).
+__device__ __forceinline__ void split_weights(uint32_t w, uint32_t (&b)[4]) {
+  asm("{ .reg .b16 l, h;\n"
+      "  .reg .b32 ll, hh;\n"
+      "  mov.b32 {l, h}, %4;\n"
+      "  mov.b32 ll, {l, l};\n"
+      "  mov.b32 hh, {h, h};\n"
+      "  mul.rn.f16x2 %0, ll, %5;  mul.rn.f16x2 %1, hh, %5;\n"
+      "  mul.rn.f16x2 %2, ll, %6;  mul.rn.f16x2 %3, hh, %6; }"
+      : "=r"(b[0]), "=r"(b[1]), "=r"(b[2]), "=r"(b[3])
+      : "r"(w), "r"(0x00003C00u), "r"(0x3C000000u));
 }
 
 __device__ __forceinline__ float ex2(float x) {
@@ -558,23 +566,29 @@ paged_attention_mma_kernel(const AttnParams p) {
     cp_async_commit();
   };
 
-  // running softmax state of heads 8n + 2t + c, and O^T fragments: o[mb][n]
-  // = rows dims 16g + 2mb (c0, c1) and 16g + 2mb + 1 (c2, c3), columns heads
-  // 8n + 2t, 8n + 2t + 1
+  // running softmax state of heads 8n + 2t + c, and O^T fragments:
+  // o[mb][e][n] = rows dims 16g + 4mb + e (c0, c1) and 16g + 4mb + 2 + e
+  // (c2, c3), columns heads 8n + 2t, 8n + 2t + 1
   // lacc[n][c]: running denominator of head 8n + 2t + c, already summed
   // over the warp's tokens by the tensor cores (c2, c3 repeat it and are
   // not read)
   // m_neg: -m_run, or 0 while m_run is -inf (no usable token yet)
-  float m_run[NB][2], m_neg[NB][2], bmax[NB][2], lacc[NB][4];
-  float o[8][NB][4];
+  // m_thr: (m_run + kLazy) / c2, the unscaled logit above which a step
+  // moves the reference
+  float m_run[NB][2], m_neg[NB][2], m_thr[NB][2], lacc[NB][4];
+  float o[4][2][NB][4];
 #pragma unroll
   for (int n = 0; n < NB; ++n) {
     m_run[n][0] = m_run[n][1] = -INFINITY;
+    m_thr[n][0] = m_thr[n][1] = -INFINITY;
     m_neg[n][0] = m_neg[n][1] = 0.f;
     lacc[n][0] = lacc[n][1] = lacc[n][2] = lacc[n][3] = 0.f;
 #pragma unroll
-    for (int mb = 0; mb < 8; ++mb)
-      o[mb][n][0] = o[mb][n][1] = o[mb][n][2] = o[mb][n][3] = 0.f;
+    for (int mb = 0; mb < 4; ++mb)
+#pragma unroll
+      for (int e = 0; e < 2; ++e)
+        o[mb][e][n][0] = o[mb][e][n][1] = o[mb][e][n][2] =
+            o[mb][e][n][3] = 0.f;
   }
   // byte selectors (pages that are not contiguous): K scales of groups 2t,
   // 2t+1 (linear: bytes 2t, 2t+1 of the row; swizzled: bytes off%4 and
@@ -587,10 +601,12 @@ paged_attention_mma_kernel(const AttnParams p) {
   const uint32_t vsel =
       static_cast<uint32_t>(((2 * t) & 3) | ((((2 * t) & 3) + 1) << 4));
 
-#pragma unroll
-  for (int i = 0; i < kDepth - 1; ++i) issue(i);
-
-  for (int i = 0; i < nsteps; ++i) {
+  // One step of 32 tokens.  kMasked: some token of the step is past the
+  // warp's range or in a block with a bad id (its logit becomes -inf and,
+  // past the range, its V scales are zeroed); otherwise no per-token test
+  // is made at all.
+  auto step = [&](int i, auto masked_tag) {
+    constexpr bool kMasked = decltype(masked_tag)::value;
     issue(i + kDepth - 1);
     cp_async_wait<kDepth - 1>();
     const uint32_t st = wbase + (i % kDepth) * SL::kStage;
@@ -601,8 +617,8 @@ paged_attention_mma_kernel(const AttnParams p) {
     // load), the two tokens' e2m1 words dequantised, two MMAs -- few
     // registers live at a time
     float sacc[2][NB][4];
-    uint32_t kvalid = 0;  // bit j: K token T0 + g + 8j is usable
-    if constexpr (kContig) {
+    uint32_t kvalid = 0xFu;  // bit j: K token T0 + g + 8j is usable
+    if constexpr (kMasked && kContig) {
       // each 16-token half lies in one block
       const int i0 = p.b_shift >= 0 ? (T0 >> p.b_shift) : T0 / p.B;
       const int i1 =
@@ -630,9 +646,10 @@ paged_attention_mma_kernel(const AttnParams p) {
           const uint2 ks = lds64(st + kKsOff + j * 256 + lane * 8);
           pair = static_cast<uint16_t>(prmt(ks.x, ks.y, ksel));
         }
-        if constexpr (!kContig)
-          kvalid |=
-              static_cast<uint32_t>(usable(T0 + g + 8 * j)) << j;
+        if constexpr (kMasked && !kContig) {
+          if (r == 0 && h == 0) kvalid = 0u;
+          kvalid |= static_cast<uint32_t>(usable(T0 + g + 8 * j)) << j;
+        }
         sfw[r] = e4m3x2_f16x2(pair);
       }
       // two accumulators (even / odd k-steps) halve the dependent chain
@@ -644,15 +661,15 @@ paged_attention_mma_kernel(const AttnParams p) {
 #pragma unroll
       for (int wd = 0; wd < 4; ++wd) {  // word wd: k-steps 2wd, 2wd+1
         uint32_t x0[4], x1[4];
-        const uint32_t w0 = wd == 0 ? kd[0].x : wd == 1 ? kd[0].y
-                            : wd == 2 ? kd[0].z : kd[0].w;
+        const uint32_t w0r = wd == 0 ? kd[0].x : wd == 1 ? kd[0].y
+                             : wd == 2 ? kd[0].z : kd[0].w;
         const uint32_t w1r = wd == 0 ? kd[1].x : wd == 1 ? kd[1].y
                              : wd == 2 ? kd[1].z : kd[1].w;
         if (wd < 2) {
-          dequant_word<0>(w0, sfw[0], x0);
+          dequant_word<0>(w0r, sfw[0], x0);
           dequant_word<0>(w1r, sfw[1], x1);
         } else {
-          dequant_word<1>(w0, sfw[0], x0);
+          dequant_word<1>(w0r, sfw[0], x0);
           dequant_word<1>(w1r, sfw[1], x1);
         }
 #pragma unroll
@@ -675,6 +692,7 @@ paged_attention_mma_kernel(const AttnParams p) {
     // weights stay below 2^kLazy.  v holds the unscaled logits; c2 > 0 is
     // applied to their maxima and inside each weight's exponent (one FMA).
     float v[NB][2][4];
+    float bmu[NB][2];  // this lane's maximum unscaled logit of head 8n+2t+c
     bool grow = false;
 #pragma unroll
     for (int n = 0; n < NB; ++n) {
@@ -682,15 +700,18 @@ paged_attention_mma_kernel(const AttnParams p) {
       for (int h = 0; h < 2; ++h)
 #pragma unroll
         for (int r = 0; r < 4; ++r) {
-          const bool ok = (kvalid >> (2 * h + (r >> 1))) & 1u;
-          v[n][h][r] = ok ? sacc[h][n][r] : -INFINITY;
+          if constexpr (kMasked) {
+            const bool ok = (kvalid >> (2 * h + (r >> 1))) & 1u;
+            v[n][h][r] = ok ? sacc[h][n][r] : -INFINITY;
+          } else {
+            v[n][h][r] = sacc[h][n][r];
+          }
         }
 #pragma unroll
       for (int c = 0; c < 2; ++c) {  // head 8n + 2t + c: this lane's tokens
-        const float bm = fmaxf(fmaxf(v[n][0][c], v[n][0][2 + c]),
-                               fmaxf(v[n][1][c], v[n][1][2 + c]));
-        bmax[n][c] = bm * c2;
-        grow |= bmax[n][c] > m_run[n][c] + kLazy;  // false while both -inf
+        bmu[n][c] = fmaxf(fmaxf(v[n][0][c], v[n][0][2 + c]),
+                          fmaxf(v[n][1][c], v[n][1][2 + c]));
+        grow |= bmu[n][c] > m_thr[n][c];  // false while both -inf
       }
     }
     // the step's maximum over all its tokens exceeds the reference by more
@@ -700,7 +721,7 @@ paged_attention_mma_kernel(const AttnParams p) {
       for (int n = 0; n < NB; ++n)
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
-          float bm = bmax[n][c];
+          float bm = bmu[n][c] * c2;
           bm = fmaxf(bm, __shfl_xor_sync(0xFFFFFFFFu, bm, 4));
           bm = fmaxf(bm, __shfl_xor_sync(0xFFFFFFFFu, bm, 8));
           bm = fmaxf(bm, __shfl_xor_sync(0xFFFFFFFFu, bm, 16));
@@ -709,12 +730,15 @@ paged_attention_mma_kernel(const AttnParams p) {
             const float alpha = ex2(m_run[n][c] - mnew);  // 0 from -inf
             m_run[n][c] = mnew;
             m_neg[n][c] = -mnew;
+            m_thr[n][c] = (mnew + kLazy) / c2;
             lacc[n][c] *= alpha;
 #pragma unroll
-            for (int mb = 0; mb < 8; ++mb) {
-              o[mb][n][c] *= alpha;
-              o[mb][n][2 + c] *= alpha;
-            }
+            for (int mb = 0; mb < 4; ++mb)
+#pragma unroll
+              for (int e = 0; e < 2; ++e) {
+                o[mb][e][n][c] *= alpha;
+                o[mb][e][n][2 + c] *= alpha;
+              }
           }
         }
     }
@@ -729,63 +753,66 @@ paged_attention_mma_kernel(const AttnParams p) {
         };
         const uint32_t pl = pack_f16x2(wgt(0), wgt(1));
         const uint32_t ph = pack_f16x2(wgt(2), wgt(3));
-        pb[h][n][0] = transpose8x8(pl);  // token g
-        pb[h][n][1] = transpose8x8(ph);  // token g + 8
+        pb[h][n][0] = transpose8x8(pl);  // tokens 16h + 2t, 16h + 2t + 1
+        pb[h][n][1] = transpose8x8(ph);  // tokens 16h + 8 + 2t, + 1
       }
 
-    const int vleft = w1 - T0 - 2 * t;  // tokens of the range from 2t on
-
-    // ---- O^T[16 dims x 8 heads] += V'^T P^T per 16-token half --------------
+    // ---- O^T += V'^T P^T per 8-token block -------------------------------
+    // The contraction index of a block runs over (token, e) pairs: A holds
+    // the block's V bytes as they are -- one byte = dims 2p, 2p+1 of a token
+    // = one f16x2 register after conversion, no nibble shuffling -- with
+    // rows = dim pairs p, and two products share it: one whose B is the
+    // token's weight at e = 0 and 0 at e = 1 (it sums the even dims of each
+    // pair), one the other way round (the odd dims).  Lane (g, t): columns
+    // 2t, 2t+1 = token 2t of the block, 2t+8, 2t+9 = token 2t+1; rows g and
+    // g+8 of m-block mb = bytes 2mb and 2mb+1 of the token's group g.
+    int vleft = 0;
+    if constexpr (kMasked) vleft = w1 - T0 - 2 * t;
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
-      uint2 vd[2][2];     // [pair q][token 2t+8q+e]
-      uint32_t sfp[2];    // [pair q]: {sf(2t+8q), sf(2t+8q+1)} as f16x2
 #pragma unroll
       for (int q = 0; q < 2; ++q) {
+        uint2 vd0, vd1;  // group g's bytes of tokens 2t and 2t+1
         uint16_t pair;
         if constexpr (kContig) {
           const uint32_t piece = st + kVdOff + (2 * h + q) * 512;
-          vd[q][0] = lds64(piece + v_rd0);
-          vd[q][1] = lds64(piece + v_rd1);
+          vd0 = lds64(piece + v_rd0);
+          vd1 = lds64(piece + v_rd1);
           pair = lds16(st + kKsOff + 256 * h + 64 * q + vs_rd16);
         } else {
-          vd[q][0] = lds64(st + kVdOff + (4 * h + 2 * q) * 256 + lane * 8);
-          vd[q][1] = lds64(st + kVdOff + (4 * h + 2 * q + 1) * 256 + lane * 8);
+          vd0 = lds64(st + kVdOff + (4 * h + 2 * q) * 256 + lane * 8);
+          vd1 = lds64(st + kVdOff + (4 * h + 2 * q + 1) * 256 + lane * 8);
           pair = static_cast<uint16_t>(
               prmt(lds32(st + SL::kVsOff + (2 * h + q) * 128 + lane * 4), 0u,
                    vsel));
         }
-        // a token past the range may share the word: zero its scale (its
-        // data are zero already), so no stray NaN code meets a zero weight;
-        // left = tokens of the range from this pair's first one on
-        const int left = vleft - 16 * h - 8 * q;
-        if (left < 2) pair &= left == 1 ? 0x00FF : 0;
-        sfp[q] = e4m3x2_f16x2(pair);
-      }
-#pragma unroll
-      for (int wi = 0; wi < 2; ++wi) {  // bytes 0..3, then 4..7: m-blocks
-        // interleave the two tokens of a pair nibble by nibble: byte k of
-        // ev holds dim 16g + 8wi + 2k of token 2t+8q (low nibble) and of
-        // token 2t+8q+1 (high nibble); od the odd dims.  One conversion then
-        // gives the A-fragment pair of the two tokens.
-        uint32_t ev[2][4], od[2][4];
-#pragma unroll
-        for (int q = 0; q < 2; ++q) {
-          const uint32_t wa = wi == 0 ? vd[q][0].x : vd[q][0].y;
-          const uint32_t wb = wi == 0 ? vd[q][1].x : vd[q][1].y;
-          e2m1_word((wa & 0x0F0F0F0Fu) | ((wb << 4) & 0xF0F0F0F0u), ev[q]);
-          e2m1_word(((wa >> 4) & 0x0F0F0F0Fu) | (wb & 0xF0F0F0F0u), od[q]);
+        if constexpr (kMasked) {
+          // a token past the range may share the word: zero its scale (its
+          // data may hold anything), so no stray NaN meets a zero weight;
+          // left = tokens of the range from this pair's first one on
+          const int left = vleft - 16 * h - 8 * q;
+          if (left < 2) pair &= left == 1 ? 0x00FF : 0;
         }
+        const uint32_t sfp = e4m3x2_f16x2(pair);  // {sf(2t), sf(2t+1)}
+        uint32_t bw[NB][4];  // even: {P(2t), 0}, {P(2t+1), 0}; odd: swapped
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const int mb = 4 * wi + k;
-          const uint32_t a0 = hmul2(ev[0][k], sfp[0]);
-          const uint32_t a1 = hmul2(od[0][k], sfp[0]);
-          const uint32_t a2 = hmul2(ev[1][k], sfp[1]);
-          const uint32_t a3 = hmul2(od[1][k], sfp[1]);
+        for (int n = 0; n < NB; ++n) split_weights(pb[h][n][q], bw[n]);
 #pragma unroll
-          for (int n = 0; n < NB; ++n)
-            mma16816(o[mb][n], a0, a1, a2, a3, pb[h][n][0], pb[h][n][1]);
+        for (int wi = 0; wi < 2; ++wi) {  // bytes 0..3, then 4..7
+          uint32_t x0[4], x1[4];
+          dequant_word<0>(wi == 0 ? vd0.x : vd0.y, sfp, x0);
+          dequant_word<1>(wi == 0 ? vd1.x : vd1.y, sfp, x1);
+#pragma unroll
+          for (int k = 0; k < 2; ++k) {
+            const int mb = 2 * wi + k;
+#pragma unroll
+            for (int n = 0; n < NB; ++n) {
+              mma16816(o[mb][0][n], x0[2 * k], x0[2 * k + 1], x1[2 * k],
+                       x1[2 * k + 1], bw[n][0], bw[n][1]);
+              mma16816(o[mb][1][n], x0[2 * k], x0[2 * k + 1], x1[2 * k],
+                       x1[2 * k + 1], bw[n][2], bw[n][3]);
+            }
+          }
         }
       }
       // the denominators: an all-ones A times P^T sums the half's 16
@@ -795,7 +822,17 @@ paged_attention_mma_kernel(const AttnParams p) {
         mma16816(lacc[n], kOnes2, kOnes2, kOnes2, kOnes2, pb[h][n][0],
                  pb[h][n][1]);
     }
-  }
+  };
+
+#pragma unroll
+  for (int i = 0; i < kDepth - 1; ++i) issue(i);
+  // the steps with no token to leave out come first; the warp's last
+  // (partial) step, and every step when a block of its range has a bad id,
+  // take the masked form
+  const int nfast = (rmask & ~bmask) != 0u ? 0 : (w1 - w0) / kStep;
+  int i = 0;
+  for (; i < nfast; ++i) step(i, std::false_type{});
+  for (; i < nsteps; ++i) step(i, std::true_type{});
   cp_async_wait<0>();  // nothing may land after the slots are reused
 
   // ---- merge the 4 warps' partial results in shared memory ----------------
@@ -810,9 +847,12 @@ paged_attention_mma_kernel(const AttnParams p) {
       const int hh = 8 * n + 2 * t + c;
       float* row = sO + (warp * 16 + hh) * kMergeRow;
 #pragma unroll
-      for (int mb = 0; mb < 8; ++mb)
-        *reinterpret_cast<float2*>(row + merge_col(16 * g + 2 * mb)) =
-            make_float2(o[mb][n][c], o[mb][n][2 + c]);
+      for (int mb = 0; mb < 4; ++mb) {
+        *reinterpret_cast<float2*>(row + merge_col(16 * g + 4 * mb)) =
+            make_float2(o[mb][0][n][c], o[mb][1][n][c]);
+        *reinterpret_cast<float2*>(row + merge_col(16 * g + 4 * mb + 2)) =
+            make_float2(o[mb][0][n][2 + c], o[mb][1][n][2 + c]);
+      }
       if (g == 0) {
         sM[warp * 16 + hh] =
             m_run[n][c] == -INFINITY ? kNoLogit : m_run[n][c];
