@@ -104,18 +104,8 @@ enum {
      first reads while that kernel finishes and waits for it only before its
      first write (its outputs and dev_error are still written strictly after
      it). */
-  KVQ_F_PDL_EARLY_READ = 1u << 4,
-  /* kvq_paged_attention_nvfp4 only: run the persistent, warp-specialised
-     tcgen05 kernel (one CTA per SM, K' in tensor memory, a dedicated MMA
-     warp) instead of the default one.  Same result contract; the default
-     measured faster on the decode workloads. */
-  KVQ_F_ATTN_PIPELINED = 1u << 3,
-  /* kvq_paged_attention_nvfp4 only: run the tcgen05 kernel with one CTA
-     per (partition, KV head, sequence) (operands staged in shared memory,
-     accumulators in tensor memory) instead of the default one (warp-level
-     MMAs on register fragments).  Same result contract; not together with
-     KVQ_F_ATTN_PIPELINED. */
-  KVQ_F_ATTN_TCGEN05 = 1u << 5
+  KVQ_F_PDL_EARLY_READ = 1u << 4
+  /* (bits 3 and 5 are not used) */
 };
 
 /* Bits OR-ed into *dev_error by the kernels. */
@@ -352,8 +342,7 @@ kvq_status kvq_store_indexer_k(const void* k, int64_t k_stride0,
  *                be initialised; their contents afterwards are unspecified.
  * out            dtype [num_seqs, num_q_heads, 128], rows out_stride0
  *                elements apart (multiple of 8), 16-byte aligned.
- * flags          KVQ_F_SWIZZLE_K_SCALE, KVQ_F_PDL, and at most one of
- *                KVQ_F_ATTN_PIPELINED and KVQ_F_ATTN_TCGEN05, or 0.
+ * flags          KVQ_F_SWIZZLE_K_SCALE, KVQ_F_PDL, or 0.
  * dev_error      nullable (KVQ_DEVERR_BLOCK: the token is left out;
  *                KVQ_DEVERR_SEQ; KVQ_DEVERR_TIMEOUT: nothing of that
  *                (sequence, KV head, partition) is written).
@@ -387,10 +376,11 @@ kvq_status kvq_paged_attention_nvfp4(
  * GPU that loads the library holds until the process exits.
  *
  * Arguments, result and errors: as kvq_paged_attention_nvfp4 without
- * exp_sums, max_logits and tmp_out.  A call that needs more than the array
- * holds -- num_seqs * num_q_heads * ceil(max_context_len / partition_size)
- * * (head_size + 2) * 4 bytes, when that ceiling is above 1 -- returns
- * KVQ_ERR_SCRATCH and launches nothing.
+ * exp_sums, max_logits and tmp_out (its argument checks run first, so a
+ * call it would reject gets the same code).  A call that needs more than
+ * the array holds -- num_seqs * num_q_heads * ceil(max_context_len /
+ * partition_size) * (head_size + 2) * 4 bytes, when that ceiling is above
+ * 1 -- returns KVQ_ERR_SCRATCH and launches nothing.
  *
  * The first call on a device looks up the array's device address (with that
  * device current) and keeps it; make that first call outside any stream

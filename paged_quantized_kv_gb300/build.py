@@ -19,8 +19,8 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libkvq.so")
 
 SOURCES = ["kvq_api.cu", "store_nvfp4.cu", "gather_indexer_k.cu",
-           "load_nvfp4.cu", "store_indexer_k.cu", "paged_attention_nvfp4.cu",
-           "attention_noalloc.cu", "paged_attention_mma.cu"]
+           "load_nvfp4.cu", "store_indexer_k.cu", "attention_noalloc.cu",
+           "paged_attention_mma.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC",
               "-Xcompiler", "-Wall", f"-I{INCLUDE}", f"-I{CSRC}"]

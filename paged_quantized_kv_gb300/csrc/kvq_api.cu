@@ -43,6 +43,63 @@ int ilog2_exact(int64_t v) {  // log2(v) if v is a power of two, else -1
 }
 
 }  // namespace
+
+// Every check kvq_paged_attention_nvfp4 makes except those of its three
+// scratch pointers, in the same order; KVQ_OK when they all pass.
+kvq_status attention_check(
+    const void* query, int64_t query_stride0, int32_t dtype, int32_t num_seqs,
+    int32_t num_q_heads, int32_t num_kv_heads, int32_t head_size,
+    const uint8_t* key_cache, const uint8_t* value_cache, int64_t page_stride,
+    int32_t block_size, int64_t num_blocks, int32_t layout,
+    const int32_t* block_table, int64_t block_table_stride,
+    int32_t max_blocks_per_seq, const int32_t* context_lens,
+    int32_t max_context_len, const float* k_scale, const float* v_scale,
+    float scale, int32_t partition_size, const void* out, int64_t out_stride0,
+    uint32_t flags) {
+  if (dtype != KVQ_DTYPE_BF16 && dtype != KVQ_DTYPE_FP16) return KVQ_ERR_DTYPE;
+  if (layout != KVQ_LAYOUT_HND && layout != KVQ_LAYOUT_NHD)
+    return KVQ_ERR_LAYOUT;
+  if ((flags & ~static_cast<uint32_t>(KVQ_F_SWIZZLE_K_SCALE | KVQ_F_PDL)) !=
+      0u)
+    return KVQ_ERR_ARG;
+  if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 ||
+      head_size <= 0 || block_size <= 0 || num_blocks < 0 ||
+      max_blocks_per_seq < 0 || block_table_stride < max_blocks_per_seq ||
+      max_context_len < 0)
+    return KVQ_ERR_SHAPE;
+  if (head_size != 128 || block_size % 4 != 0) return KVQ_ERR_SHAPE;
+  if (num_q_heads % num_kv_heads != 0 || num_q_heads / num_kv_heads > 16)
+    return KVQ_ERR_SHAPE;
+  if (partition_size <= 0 || partition_size % 128 != 0 ||
+      partition_size > 512)
+    return KVQ_ERR_SHAPE;
+  if (!(scale == scale) || scale == INFINITY || scale == -INFINITY)
+    return KVQ_ERR_ARG;
+  const int64_t H = num_kv_heads, D = head_size, B = block_size;
+  const int64_t S = D / 16;
+  if (page_stride < H * B * (D / 2 + S)) return KVQ_ERR_SHAPE;
+  if (query_stride0 < num_q_heads * D || out_stride0 < num_q_heads * D)
+    return KVQ_ERR_SHAPE;
+  const int64_t max_parts =
+      (static_cast<int64_t>(max_context_len) + partition_size - 1) /
+      partition_size;
+  if (num_seqs > 65535 || num_kv_heads > 65535 || max_parts > (1 << 20) ||
+      static_cast<int64_t>(num_seqs) * num_kv_heads * max_parts >= INT32_MAX)
+    return KVQ_ERR_SHAPE;
+  if (num_seqs == 0) return KVQ_OK;
+  if (query == nullptr || key_cache == nullptr || value_cache == nullptr ||
+      block_table == nullptr || context_lens == nullptr ||
+      k_scale == nullptr || v_scale == nullptr || out == nullptr)
+    return KVQ_ERR_NULL;
+  if (!aligned(query, 16) || query_stride0 % 8 != 0 || !aligned(out, 16) ||
+      out_stride0 % 8 != 0 || !aligned(key_cache, 16) ||
+      !aligned(value_cache, 16) || page_stride % 16 != 0 ||
+      !aligned(block_table, 4) || !aligned(context_lens, 4) ||
+      !aligned(k_scale, 4) || !aligned(v_scale, 4))
+    return KVQ_ERR_ALIGN;
+  return KVQ_OK;
+}
+
 }  // namespace kvq
 
 extern "C" {
@@ -361,52 +418,21 @@ kvq_status kvq_paged_attention_nvfp4(
     float* tmp_out, void* out, int64_t out_stride0, uint32_t flags,
     int32_t* dev_error, void* stream) {
   using namespace kvq;
-  if (dtype != KVQ_DTYPE_BF16 && dtype != KVQ_DTYPE_FP16) return KVQ_ERR_DTYPE;
-  if (layout != KVQ_LAYOUT_HND && layout != KVQ_LAYOUT_NHD)
-    return KVQ_ERR_LAYOUT;
-  if ((flags & ~static_cast<uint32_t>(KVQ_F_SWIZZLE_K_SCALE | KVQ_F_PDL |
-                                      KVQ_F_ATTN_PIPELINED |
-                                      KVQ_F_ATTN_TCGEN05)) != 0u ||
-      ((flags & KVQ_F_ATTN_PIPELINED) && (flags & KVQ_F_ATTN_TCGEN05)))
-    return KVQ_ERR_ARG;
-  if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 ||
-      head_size <= 0 || block_size <= 0 || num_blocks < 0 ||
-      max_blocks_per_seq < 0 || block_table_stride < max_blocks_per_seq ||
-      max_context_len < 0)
-    return KVQ_ERR_SHAPE;
-  if (head_size != 128 || block_size % 4 != 0) return KVQ_ERR_SHAPE;
-  if (num_q_heads % num_kv_heads != 0 || num_q_heads / num_kv_heads > 16)
-    return KVQ_ERR_SHAPE;
-  if (partition_size <= 0 || partition_size % 128 != 0 ||
-      partition_size > 512)
-    return KVQ_ERR_SHAPE;
-  if (!(scale == scale) || scale == INFINITY || scale == -INFINITY)
-    return KVQ_ERR_ARG;
+  const kvq_status st = attention_check(
+      query, query_stride0, dtype, num_seqs, num_q_heads, num_kv_heads,
+      head_size, key_cache, value_cache, page_stride, block_size, num_blocks,
+      layout, block_table, block_table_stride, max_blocks_per_seq,
+      context_lens, max_context_len, k_scale, v_scale, scale, partition_size,
+      out, out_stride0, flags);
+  if (st != KVQ_OK || num_seqs == 0) return st;
   const int64_t H = num_kv_heads, D = head_size, B = block_size;
   const int64_t S = D / 16;
-  if (page_stride < H * B * (D / 2 + S)) return KVQ_ERR_SHAPE;
-  if (query_stride0 < num_q_heads * D || out_stride0 < num_q_heads * D)
-    return KVQ_ERR_SHAPE;
   const int64_t max_parts =
       (static_cast<int64_t>(max_context_len) + partition_size - 1) /
       partition_size;
-  if (num_seqs > 65535 || num_kv_heads > 65535 || max_parts > (1 << 20) ||
-      static_cast<int64_t>(num_seqs) * num_kv_heads * max_parts >= INT32_MAX)
-    return KVQ_ERR_SHAPE;
-  if (num_seqs == 0) return KVQ_OK;
-  if (query == nullptr || key_cache == nullptr || value_cache == nullptr ||
-      block_table == nullptr || context_lens == nullptr ||
-      k_scale == nullptr || v_scale == nullptr || out == nullptr)
-    return KVQ_ERR_NULL;
   if (max_parts > 1 &&
       (exp_sums == nullptr || max_logits == nullptr || tmp_out == nullptr))
     return KVQ_ERR_NULL;
-  if (!aligned(query, 16) || query_stride0 % 8 != 0 || !aligned(out, 16) ||
-      out_stride0 % 8 != 0 || !aligned(key_cache, 16) ||
-      !aligned(value_cache, 16) || page_stride % 16 != 0 ||
-      !aligned(block_table, 4) || !aligned(context_lens, 4) ||
-      !aligned(k_scale, 4) || !aligned(v_scale, 4))
-    return KVQ_ERR_ALIGN;
   if (max_parts > 1 && (!aligned(exp_sums, 4) || !aligned(max_logits, 4) ||
                         !aligned(tmp_out, 16)))
     return KVQ_ERR_ALIGN;
@@ -456,11 +482,8 @@ kvq_status kvq_paged_attention_nvfp4(
   p.swizzle_k = (flags & KVQ_F_SWIZZLE_K_SCALE) != 0u;
   p.f16 = dtype == KVQ_DTYPE_FP16;
   p.pdl = (flags & KVQ_F_PDL) != 0u;
-  p.kernel = (flags & KVQ_F_ATTN_PIPELINED) != 0u   ? kAttnPipelined
-             : (flags & KVQ_F_ATTN_TCGEN05) != 0u ? kAttnTcgen05
-                                                  : kAttnWarpMma;
   const cudaError_t err =
-      launch_paged_attention_nvfp4(p, static_cast<cudaStream_t>(stream));
+      launch_paged_attention_mma(p, static_cast<cudaStream_t>(stream));
   return err == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
 }
 

@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "kvq.h"
+
 namespace kvq {
 
 // ---------------------------------------------------------------------------
@@ -141,20 +143,25 @@ struct AttnParams {
   bool swizzle_k;          // K scales stored swizzled too
   bool f16;                // query / out are fp16 (else bf16)
   bool pdl;
-  int32_t kernel;          // kAttnWarpMma, kAttnTcgen05 or kAttnPipelined
 };
 
-enum {
-  kAttnWarpMma = 0,    // warp-level MMAs on register fragments (default)
-  kAttnTcgen05 = 1,    // tcgen05 per (partition, KV head, sequence) CTA
-  kAttnPipelined = 2   // tcgen05, persistent and warp-specialised
-};
-
-cudaError_t launch_paged_attention_nvfp4(const AttnParams& p,
-                                         cudaStream_t stream);
 cudaError_t launch_paged_attention_mma(const AttnParams& p,
                                        cudaStream_t stream);
-// The partition merge shared by the attention kernels (PDL launch).
+// The argument checks of kvq_paged_attention_nvfp4 other than those of its
+// scratch pointers (KVQ_OK when they pass); kvq_paged_attention_nvfp4_noalloc
+// runs them before it checks its scratch capacity.
+kvq_status attention_check(
+    const void* query, int64_t query_stride0, int32_t dtype, int32_t num_seqs,
+    int32_t num_q_heads, int32_t num_kv_heads, int32_t head_size,
+    const uint8_t* key_cache, const uint8_t* value_cache, int64_t page_stride,
+    int32_t block_size, int64_t num_blocks, int32_t layout,
+    const int32_t* block_table, int64_t block_table_stride,
+    int32_t max_blocks_per_seq, const int32_t* context_lens,
+    int32_t max_context_len, const float* k_scale, const float* v_scale,
+    float scale, int32_t partition_size, const void* out, int64_t out_stride0,
+    uint32_t flags);
+
+// The partition merge of the attention (PDL launch).
 cudaError_t launch_attention_merge(const AttnParams& p, cudaStream_t stream);
 
 // Streaming-multiprocessor count of the current device (cached per device).

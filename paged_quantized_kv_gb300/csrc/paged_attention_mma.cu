@@ -2,12 +2,18 @@
 // sm_103a, on warp-level tensor-core MMAs (mma.sync m16n8k16, fp16
 // operands, fp32 accumulators) with register fragments.
 //
-// Operation: the same as paged_attention_nvfp4.cu (the paged_attention op of
-// vLLM PR #12348 "[ROCm] Faster Custom Paged Attention kernels", read over
-// the NVFP4 pages of vLLM nvfp4_kv_cache_kernels.cu, commit 7ce4c8e): for
+// Operation: the paged_attention op of vLLM PR #12348 "[ROCm] Faster Custom
+// Paged Attention kernels" (out, exp_sums, max_logits, tmp_out, query,
+// key_cache, value_cache, num_kv_heads, scale, block_tables, context_lens,
+// block_size, max_context_len, k_scale, v_scale, partition_size), read over
+// the NVFP4 pages of vLLM nvfp4_kv_cache_kernels.cu (commit 7ce4c8e): for
 // sequence b and query head h (KV head h / G) over the first
 // context_lens[b] tokens, out = softmax(scale * q . K^) V^ with
-// K^ = e2m1(code) * float(sf) * k_scale (V^ with v_scale).
+// K^ = e2m1(code) * float(sf) * k_scale (V^ with v_scale).  A context
+// longer than one CTA's stretch is split: each stretch writes its max
+// logit, exp-sum and normalised output to the caller's scratch, and a
+// second small kernel (the partition merge, at the end of this file)
+// combines them.
 //
 // Why warp-level MMAs here: a decode step multiplies each 128-token tile by
 // at most 16 query heads, so every MMA is tiny (N = 8 or 16).  Measured on
@@ -16,6 +22,11 @@
 // around tensor memory (commit, mbarrier wake-up ~300 cycles) sit on every
 // tile's critical path; mma.sync.m16n8k16 runs at 2 cycles per instruction
 // per SM with its operands already in registers and needs no handshake.
+// Two tcgen05 designs of this operation (one CTA per partition with the
+// logits held in tensor memory; a persistent warp-specialised one) measured
+// 0.25 and 0.11 of the HBM roofline against this kernel's 0.66 on the
+// Llama-70B-shaped step, and 0.20 / 0.10 against 0.39 with 16 query heads
+// per KV head, so they were retired.
 //
 // Design, per CTA of 4 warps = one (stretch of context, KV head, sequence):
 // a stretch is KVQ_ATTN_MMA_PART (1280) tokens on contiguous pages (HND,
@@ -912,6 +923,88 @@ paged_attention_mma_kernel(const AttnParams p) {
   }
 }
 
+// ---------------------------------------------------------------------------
+// Merge of the partitions of contexts longer than one partition
+// ---------------------------------------------------------------------------
+// 16 rows (sequence, query head) per CTA of 256 threads, a half-warp per
+// row and 8 head dims per lane, so that one wave of CTAs covers a whole
+// decode batch.  The context length is read before the wait for the
+// attention kernel, which writes none of it; every thread waits before it
+// may leave.  Per dim, the sums run over the partitions in order.
+constexpr int kMergeThreads = 256;
+constexpr int kMergeRows = kMergeThreads / 16;
+// Rows of at most this many partitions issue all their loads at once.
+constexpr int kMergeFew = 4;
+
+template <bool kF16>
+__global__ void __launch_bounds__(kMergeThreads)
+attention_merge_kernel(const AttnParams p) {
+  const int sub = threadIdx.x & 15;  // dims 8 sub .. 8 sub + 7
+  const int64_t row =
+      static_cast<int64_t>(blockIdx.x) * kMergeRows + (threadIdx.x >> 4);
+  const bool live = row < static_cast<int64_t>(p.num_seqs) * p.Hq;
+  const int b = live ? static_cast<int>(row / p.Hq) : 0;
+  const int h = live ? static_cast<int>(row - static_cast<int64_t>(b) * p.Hq)
+                     : 0;
+  int L = live ? __ldg(p.lens + b) : 0;
+  pdl_prologue();
+  L = L < 0 ? 0 : (L > p.len_cap ? p.len_cap : L);
+  const int nparts = (L + p.part - 1) / p.part;
+  if (!live || nparts <= 1) return;
+  const int64_t row0 = row * p.max_parts;
+  float M = -INFINITY;
+  float den = 0.f, acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  auto add = [&](float w, const float4& x, const float4& y) {
+    den += w;
+    acc[0] += w * x.x; acc[1] += w * x.y; acc[2] += w * x.z; acc[3] += w * x.w;
+    acc[4] += w * y.x; acc[5] += w * y.y; acc[6] += w * y.z; acc[7] += w * y.w;
+  };
+  if (nparts <= kMergeFew) {
+    // every load of the row in one round trip, then the same sums in order
+    float ml[kMergeFew], es[kMergeFew];
+    float4 xs[kMergeFew], ys[kMergeFew];
+#pragma unroll
+    for (int i = 0; i < kMergeFew; ++i) {
+      if (i < nparts) {
+        ml[i] = p.max_logits[row0 + i];
+        es[i] = p.exp_sums[row0 + i];
+        const float4* src = reinterpret_cast<const float4*>(
+            p.tmp_out + (row0 + i) * kD + 8 * sub);
+        xs[i] = src[0];
+        ys[i] = src[1];
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < kMergeFew; ++i)
+      if (i < nparts) M = fmaxf(M, ml[i]);
+#pragma unroll
+    for (int i = 0; i < kMergeFew; ++i)
+      if (i < nparts) add(es[i] * ex2(ml[i] - M), xs[i], ys[i]);
+  } else {
+#pragma unroll 4
+    for (int i = 0; i < nparts; ++i) M = fmaxf(M, p.max_logits[row0 + i]);
+#pragma unroll 2
+    for (int i = 0; i < nparts; ++i) {
+      const float4* src = reinterpret_cast<const float4*>(
+          p.tmp_out + (row0 + i) * kD + 8 * sub);
+      add(p.exp_sums[row0 + i] * ex2(p.max_logits[row0 + i] - M), src[0],
+          src[1]);
+    }
+  }
+  const float f = den > 0.f ? 1.0f / den : 0.f;
+  const float vs = __ldg(p.v_scale);
+  uint32_t packed[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const float y0 = den > 0.f ? acc[2 * k] * f * vs : 0.f;
+    const float y1 = den > 0.f ? acc[2 * k + 1] * f * vs : 0.f;
+    packed[k] = static_cast<uint32_t>(float_to_out<kF16>(y0)) |
+                (static_cast<uint32_t>(float_to_out<kF16>(y1)) << 16);
+  }
+  *reinterpret_cast<uint4*>(p.out + b * p.out_stride0 + h * kD + 8 * sub) =
+      make_uint4(packed[0], packed[1], packed[2], packed[3]);
+}
+
 template <int NG, bool kF16, bool kContig>
 cudaError_t launch_mma(const AttnParams& caller, cudaStream_t stream) {
   auto kernel = paged_attention_mma_kernel<NG, kF16, kContig>;
@@ -951,6 +1044,15 @@ cudaError_t launch_layout(const AttnParams& p, cudaStream_t stream) {
 }
 
 }  // namespace
+
+cudaError_t launch_attention_merge(const AttnParams& p, cudaStream_t stream) {
+  const int64_t rows = static_cast<int64_t>(p.num_seqs) * p.Hq;
+  const dim3 grid(static_cast<unsigned>((rows + kMergeRows - 1) / kMergeRows));
+  return p.f16 ? launch_kernel(attention_merge_kernel<true>, grid,
+                               kMergeThreads, 0, stream, true, p)
+               : launch_kernel(attention_merge_kernel<false>, grid,
+                               kMergeThreads, 0, stream, true, p);
+}
 
 cudaError_t launch_paged_attention_mma(const AttnParams& p,
                                        cudaStream_t stream) {

@@ -52,9 +52,7 @@ KVQ_DTYPE_FP16 = 1
 KVQ_F_SWIZZLE_K_SCALE = 1
 KVQ_F_PDL = 2
 KVQ_F_PDL_EARLY_META = 4
-KVQ_F_ATTN_PIPELINED = 1 << 3
 KVQ_F_PDL_EARLY_READ = 1 << 4
-KVQ_F_ATTN_TCGEN05 = 1 << 5
 KVQ_DEVERR_SLOT = 1
 KVQ_DEVERR_BLOCK = 2
 KVQ_DEVERR_SEQ = 4

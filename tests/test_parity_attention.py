@@ -20,9 +20,11 @@ tiles, one to five partitions, the partition merge), partition sizes 128 to
 swizzled K scales, block sizes 4 to 384 (12 and 384 not powers of two),
 large logits (one-hot weights), pages written by the GPU store, a PDL chain
 store -> attention, the Llama-3.1-70B-shaped decode batch (sampled rows),
-clamped contexts and invalid block ids (flags), and bitwise determinism --
-for all three kernels (the default warp-level-MMA one,
-KVQ_F_ATTN_PIPELINED and KVQ_F_ATTN_TCGEN05)."""
+clamped contexts and invalid block ids (flags), and bitwise determinism.
+The ranges of the kernel's warps (a quarter of a stretch of up to 1280
+tokens each, walked in steps of 32) end inside a step, at a step boundary
+and one token past it across these lengths, so both the unmasked steps and
+the masked last step run, and a bad block id makes a whole range masked."""
 import dataclasses
 
 import numpy as np
@@ -47,7 +49,7 @@ def _upload(wl):
 
 
 def gpu_attention(wl, partition_size=512, max_context_len=None, flags=None,
-                  dev_error=None, caches=None, kernel=0):
+                  dev_error=None, caches=None):
     kv, kc, vc = _upload(wl) if caches is None else caches
     tdt = torch.float16 if wl.dtype == W.DTYPE_F16 else torch.bfloat16
     q = torch.from_numpy(wl.query.view(np.int16)).cuda().view(tdt)
@@ -61,7 +63,7 @@ def gpu_attention(wl, partition_size=512, max_context_len=None, flags=None,
     kvq.kvq_paged_attention_nvfp4(
         q, kc, vc, bt, lens, ks, vs, float(wl.scale), out, mcl,
         partition_size=partition_size,
-        flags=(wl.flags if flags is None else flags) | kernel,
+        flags=wl.flags if flags is None else flags,
         dev_error=dev_error)
     torch.cuda.synchronize()
     return out.float().cpu().numpy().astype(np.float64)
@@ -116,65 +118,53 @@ LENS = [1, 15, 16, 17, 127, 128, 129, 255, 300, 511, 512, 513, 700, 1025,
         2049, 0]
 
 
-# kernel flags: the default (warp-level MMAs), the persistent pipelined
-# tcgen05 kernel, the per-partition tcgen05 kernel
-KERNELS = [0, kvq.KVQ_F_ATTN_PIPELINED, kvq.KVQ_F_ATTN_TCGEN05]
-KIDS = ["warp_mma", "pipelined", "tcgen05"]
-
-
-@pytest.mark.parametrize("kernel", KERNELS, ids=KIDS)
 @pytest.mark.parametrize("part", [512, 256, 128, 384])
-def test_contexts_and_partitions(orc, part, kernel):
+def test_contexts_and_partitions(orc, part):
     wl = W.make_attention("ctx", 21, LENS, num_q_heads=16, num_kv_heads=2,
                           head_size=128, block_size=16)
-    _check(orc, wl, partition_size=part, kernel=kernel)
+    _check(orc, wl, partition_size=part)
 
 
-@pytest.mark.parametrize("kernel", KERNELS, ids=KIDS)
 @pytest.mark.parametrize("G", [1, 2, 4, 8, 16])
-def test_group_sizes(orc, G, kernel):
+def test_group_sizes(orc, G):
     Hkv = 2
     wl = W.make_attention(f"g{G}", 30 + G, [3, 200, 640, 129],
                           num_q_heads=G * Hkv, num_kv_heads=Hkv,
                           head_size=128, block_size=16)
-    _check(orc, wl, kernel=kernel)
+    _check(orc, wl)
 
 
-@pytest.mark.parametrize("kernel", KERNELS, ids=KIDS)
 @pytest.mark.parametrize("dtype", [W.DTYPE_BF16, W.DTYPE_F16])
 @pytest.mark.parametrize("layout", [W.LAYOUT_HND, W.LAYOUT_NHD])
 @pytest.mark.parametrize("swz", [0, oracle.F_SWIZZLE_K_SCALE])
-def test_layouts_dtypes_swizzle(orc, dtype, layout, swz, kernel):
+def test_layouts_dtypes_swizzle(orc, dtype, layout, swz):
     wl = W.make_attention("lay", 40, [77, 600, 5, 1000], num_q_heads=8,
                           num_kv_heads=4, head_size=128, block_size=16,
                           dtype=dtype, flags=swz)
     if layout == W.LAYOUT_NHD:
         wl = _nhd(wl)
-    _check(orc, wl, kernel=kernel)
+    _check(orc, wl)
 
 
-@pytest.mark.parametrize("kernel", KERNELS, ids=KIDS)
 @pytest.mark.parametrize("B", [4, 8, 12, 32, 64, 128, 256, 384])
-def test_block_sizes(orc, B, kernel):
+def test_block_sizes(orc, B):
     lens = [B - 1, B, B + 1, 4 * B + 3, 900]
     wl = W.make_attention(f"B{B}", 50 + B, [n for n in lens if n <= 2100],
                           num_q_heads=8, num_kv_heads=1, head_size=128,
                           block_size=B)
-    _check(orc, wl, kernel=kernel)
+    _check(orc, wl)
 
 
-@pytest.mark.parametrize("kernel", KERNELS, ids=KIDS)
-def test_one_hot_logits(orc, kernel):
+def test_one_hot_logits(orc):
     wl = W.make_attention("hot", 60, [300, 1200, 40], num_q_heads=8,
                           num_kv_heads=2, head_size=128, block_size=16,
                           scale=50.0)
-    _check(orc, wl, kernel=kernel)
+    _check(orc, wl)
 
 
-@pytest.mark.parametrize("kernel", KERNELS, ids=KIDS)
 @pytest.mark.parametrize("scale", [-0.088, 0.0, -50.0])
 @pytest.mark.parametrize("Hq", [16, 32])
-def test_negative_and_zero_scale(orc, Hq, scale, kernel):
+def test_negative_and_zero_scale(orc, Hq, scale):
     """A negative softmax scale (the largest weights go to the smallest dot
     products; -50 makes them one-hot) and a zero one (every logit 0: each
     output is the mean of its context's values), over contexts of several
@@ -182,7 +172,7 @@ def test_negative_and_zero_scale(orc, Hq, scale, kernel):
     wl = W.make_attention(f"scale{scale}_{Hq}", 61, [300, 1500, 40, 2600],
                           num_q_heads=Hq, num_kv_heads=2, head_size=128,
                           block_size=16, scale=scale)
-    _check(orc, wl, kernel=kernel)
+    _check(orc, wl)
 
 
 def test_store_then_attention(orc):
@@ -227,12 +217,11 @@ def test_store_then_attention(orc):
     assert np.array_equal(outs[0], outs[1])
 
 
-@pytest.mark.parametrize("kernel", KERNELS, ids=KIDS)
-def test_llama70b_decode_batch_sampled(orc, kernel):
+def test_llama70b_decode_batch_sampled(orc):
     """The benchmark's decode step (200 sequences, 64 query / 8 KV heads),
     run in full on the GPU; eight sequences checked against the oracle."""
     wl = W.attention_workload()
-    got = gpu_attention(wl, kernel=kernel)
+    got = gpu_attention(wl)
     rng = np.random.default_rng(72)
     pick = np.sort(rng.choice(wl.num_seqs, size=8, replace=False))
     pick[0] = int(np.argmax(wl.context_lens))       # the longest context
@@ -246,33 +235,19 @@ def test_llama70b_decode_batch_sampled(orc, kernel):
                  "llama70b_decode")
 
 
-@pytest.mark.parametrize("kernel", KERNELS, ids=KIDS)
-def test_deterministic(orc, kernel):
+def test_deterministic(orc):
     wl = W.make_attention("det", 80, [900, 33, 1500], num_q_heads=16,
                           num_kv_heads=2, head_size=128, block_size=16)
-    a = gpu_attention(wl, kernel=kernel)
-    b = gpu_attention(wl, kernel=kernel)
+    a = gpu_attention(wl)
+    b = gpu_attention(wl)
     assert np.array_equal(a, b)
 
 
-def test_kernels_agree(orc):
-    """The three kernels on the same inputs, each within the bound of the
-    oracle."""
-    wl = W.make_attention("agree", 81, [1, 200, 513, 2000, 64], num_q_heads=32,
-                          num_kv_heads=4, head_size=128, block_size=16)
-    ref, mag = oracle_attention(orc, wl)
-    vmax = _vmax(wl, wl.context_lens)
-    for k, name in zip(KERNELS, KIDS):
-        assert_close(gpu_attention(wl, kernel=k), ref, mag, vmax, name)
-
-
-@pytest.mark.parametrize("kernel", KERNELS, ids=KIDS)
-def test_clamped_context_and_flags(orc, kernel):
+def test_clamped_context_and_flags(orc):
     wl = W.make_attention("clamp", 90, [700, 100], num_q_heads=8,
                           num_kv_heads=1, head_size=128, block_size=16)
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
-    got = gpu_attention(wl, max_context_len=600, dev_error=err,
-                        kernel=kernel)
+    got = gpu_attention(wl, max_context_len=600, dev_error=err)
     assert int(err.item()) & kvq.KVQ_DEVERR_SEQ
     ref, mag = oracle_attention(orc, wl, np.array([600, 100], np.int32))
     assert_close(got, ref, mag, _vmax(wl, [600, 100]), "clamped")
@@ -283,15 +258,14 @@ def test_clamped_context_and_flags(orc, kernel):
                            num_kv_heads=1, head_size=128, block_size=16)
     bad.block_table[0, 3] = bad.num_blocks + 5
     err.zero_()
-    got = gpu_attention(bad, dev_error=err, kernel=kernel)
+    got = gpu_attention(bad, dev_error=err)
     assert int(err.item()) & kvq.KVQ_DEVERR_BLOCK
     lens = np.array([48, 40], np.int32)
     ref, mag = oracle_attention(orc, bad, lens)
     assert_close(got, ref, mag, _vmax(bad, lens), "bad block")
 
 
-@pytest.mark.parametrize("kernel", KERNELS, ids=KIDS)
-def test_bad_blocks_inside_contexts(orc, kernel):
+def test_bad_blocks_inside_contexts(orc):
     """Out-of-range block ids (negative and past the cache) in the middle of
     contexts: flagged, and their B tokens left out.  The attention of one
     query token does not depend on the order of the context's tokens, so
@@ -306,7 +280,7 @@ def test_bad_blocks_inside_contexts(orc, kernel):
     wl.block_table[2, 2] = wl.num_blocks + 7
     wl.block_table[3, 40] = wl.num_blocks
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
-    got = gpu_attention(wl, dev_error=err, kernel=kernel)
+    got = gpu_attention(wl, dev_error=err)
     assert int(err.item()) & kvq.KVQ_DEVERR_BLOCK
     bt = np.zeros_like(wl.block_table)
     lens = wl.context_lens.copy()
@@ -322,13 +296,12 @@ def test_bad_blocks_inside_contexts(orc, kernel):
     assert_close(got, ref, mag, _vmax(ref_wl, lens), "bad blocks inside")
 
 
-@pytest.mark.parametrize("kernel", KERNELS, ids=KIDS)
-def test_long_contexts_many_partitions(orc, kernel):
+def test_long_contexts_many_partitions(orc):
     """Contexts of several thousand tokens (up to 17 partitions of 512; the
-    default kernel's CTAs cover 1280 tokens each on these pages) with a
+    kernel's CTAs cover 1280 tokens each on these pages) with a
     max_context_len above the longest context, so the scratch has more rows
     than used."""
     wl = W.make_attention("long", 95, [4097, 8191, 3000, 1, 1024, 2048],
                           num_q_heads=16, num_kv_heads=2, head_size=128,
                           block_size=16)
-    _check(orc, wl, partition_size=512, max_context_len=9000, kernel=kernel)
+    _check(orc, wl, partition_size=512, max_context_len=9000)
