@@ -15,9 +15,11 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "kvq.h"
+#include "kvq_internal.h"
 
 namespace {
 
@@ -26,24 +28,28 @@ namespace {
 static __device__ __align__(256) uint8_t g_attn_scratch[KVQ_NOALLOC_SCRATCH_BYTES];
 
 constexpr int kMaxDevices = 64;
-std::mutex g_mutex;
-void* g_scratch_addr[kMaxDevices] = {};
+std::mutex g_mutex;  // taken only until a device's address is known
+std::atomic<void*> g_scratch_addr[kMaxDevices];
 
 // Device address of the array on the current device; looked up once per
 // device (the first call on a device does it, with that device current).
+// Once known, the address is read without a lock.
 cudaError_t scratch_address(void** out) {
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  std::lock_guard<std::mutex> lock(g_mutex);
-  if (g_scratch_addr[dev] == nullptr) {
-    void* p = nullptr;
-    err = cudaGetSymbolAddress(&p, g_attn_scratch);
-    if (err != cudaSuccess) return err;
-    g_scratch_addr[dev] = p;
+  void* p = g_scratch_addr[dev].load(std::memory_order_acquire);
+  if (p == nullptr) {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    p = g_scratch_addr[dev].load(std::memory_order_relaxed);
+    if (p == nullptr) {
+      err = cudaGetSymbolAddress(&p, g_attn_scratch);
+      if (err != cudaSuccess) return err;
+      g_scratch_addr[dev].store(p, std::memory_order_release);
+    }
   }
-  *out = g_scratch_addr[dev];
+  *out = p;
   return cudaSuccess;
 }
 
@@ -59,32 +65,34 @@ extern "C" kvq_status kvq_paged_attention_nvfp4_noalloc(
     int32_t max_context_len, const float* k_scale, const float* v_scale,
     float scale, int32_t partition_size, void* out, int64_t out_stride0,
     uint32_t flags, int32_t* dev_error, void* stream) {
-  // sizes the existing entry point would reject are passed through to it
-  // unchanged, so that it reports them with its own codes
+  // the plain entry point's own checks first, so that a call it would
+  // reject gets the same code here (whatever the scratch it would need)
+  const kvq_status st = kvq::attention_check(
+      query, query_stride0, dtype, num_seqs, num_q_heads, num_kv_heads,
+      head_size, key_cache, value_cache, page_stride, block_size, num_blocks,
+      layout, block_table, block_table_stride, max_blocks_per_seq,
+      context_lens, max_context_len, k_scale, v_scale, scale, partition_size,
+      out, out_stride0, flags);
+  if (st != KVQ_OK || num_seqs == 0) return st;
   float* exp_sums = nullptr;
   float* max_logits = nullptr;
   float* tmp_out = nullptr;
-  if (num_seqs > 0 && num_q_heads > 0 && head_size > 0 &&
-      partition_size > 0 && max_context_len > 0) {
-    const int64_t parts =
-        (static_cast<int64_t>(max_context_len) + partition_size - 1) /
-        partition_size;
-    if (parts > 1) {
-      // tmp_out [rows, head_size] first (16-byte aligned), then the sums
-      // and maxima [rows] each: (head_size + 2) floats per row
-      const int64_t cap = static_cast<int64_t>(KVQ_NOALLOC_SCRATCH_BYTES) /
-                          ((static_cast<int64_t>(head_size) + 2) * 4);
-      if (num_seqs > cap || num_q_heads > cap || parts > cap ||
-          static_cast<int64_t>(num_seqs) * num_q_heads > cap ||
-          static_cast<int64_t>(num_seqs) * num_q_heads * parts > cap)
-        return KVQ_ERR_SCRATCH;
-      const int64_t rows = static_cast<int64_t>(num_seqs) * num_q_heads * parts;
-      void* base = nullptr;
-      if (scratch_address(&base) != cudaSuccess) return KVQ_ERR_CUDA;
-      tmp_out = static_cast<float*>(base);
-      exp_sums = tmp_out + rows * head_size;
-      max_logits = exp_sums + rows;
-    }
+  const int64_t parts =
+      (static_cast<int64_t>(max_context_len) + partition_size - 1) /
+      partition_size;
+  if (parts > 1) {
+    // tmp_out [rows, head_size] first (16-byte aligned), then the sums and
+    // maxima [rows] each: (head_size + 2) floats per row
+    const int64_t cap = static_cast<int64_t>(KVQ_NOALLOC_SCRATCH_BYTES) /
+                        ((static_cast<int64_t>(head_size) + 2) * 4);
+    const int64_t rows =
+        static_cast<int64_t>(num_seqs) * num_q_heads * parts;
+    if (rows > cap) return KVQ_ERR_SCRATCH;
+    void* base = nullptr;
+    if (scratch_address(&base) != cudaSuccess) return KVQ_ERR_CUDA;
+    tmp_out = static_cast<float*>(base);
+    exp_sums = tmp_out + rows * head_size;
+    max_logits = exp_sums + rows;
   }
   return kvq_paged_attention_nvfp4(
       query, query_stride0, dtype, num_seqs, num_q_heads, num_kv_heads,

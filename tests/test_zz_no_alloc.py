@@ -85,3 +85,103 @@ def test_noalloc_refuses_requests_beyond_its_array():
     assert e.value.status == kvq.KVQ_ERR_SCRATCH
     torch.cuda.synchronize()
     assert not out.any()  # nothing was launched
+
+
+def test_noalloc_single_partition_uses_no_scratch(orc):
+    """Every context within one partition: no scratch is needed, the array
+    is not used, and the result equals the plain entry point's."""
+    wl = W.make_attention("noalloc_one", 104, [512, 1, 300, 0, 129],
+                          num_q_heads=8, num_kv_heads=1, head_size=128,
+                          block_size=16)
+    a = _inputs(wl)
+    want = _plain(wl, a, 512)
+    got = _noalloc(wl, a, 512)
+    ref, mag = oracle_attention(orc, wl)
+    tol = (2.0 ** -8 * np.abs(want) + 2.0 ** -9 * mag
+           + 2.0 ** -24 * _vmax(wl, wl.context_lens)[:, None, None])
+    assert np.isfinite(got).all()
+    assert (np.abs(got - want) <= tol).all()
+
+
+def test_noalloc_at_the_limit_and_one_partition_past_it(orc):
+    """A call whose scratch is exactly the most rows the array holds is
+    accepted (and matches the plain entry point); one more partition is
+    refused.  rows = num_seqs * num_q_heads * partitions of the declared
+    max_context_len, which may be far above the actual contexts."""
+    cap = kvq.KVQ_NOALLOC_SCRATCH_BYTES // ((128 + 2) * 4)
+    nseq, hq, parts = 137, 3, 157  # 137 * 3 * 157 == cap
+    assert nseq * hq * parts == cap
+    rng = np.random.default_rng(105)
+    lens = rng.integers(1, 3001, size=nseq)
+    lens[:3] = [3000, 1281, 2560]  # several stretches per context
+    wl = W.make_attention("noalloc_cap", 105, lens, num_q_heads=hq,
+                          num_kv_heads=1, head_size=128, block_size=16)
+    a = _inputs(wl)
+    a["mcl"] = parts * 512  # declared maximum: 157 partitions of 512
+    want = _plain(wl, a, 512)
+    got = _noalloc(wl, a, 512)
+    ref, mag = oracle_attention(orc, wl)
+    tol = (2.0 ** -8 * np.abs(want) + 2.0 ** -9 * mag
+           + 2.0 ** -24 * _vmax(wl, wl.context_lens)[:, None, None])
+    assert np.isfinite(got).all()
+    assert (np.abs(got - want) <= tol).all()
+    out = torch.zeros_like(a["q"])
+    with pytest.raises(kvq.KvqError) as e:
+        kvq.kvq_paged_attention_nvfp4_noalloc(
+            a["q"], a["kc"], a["vc"], a["bt"], a["lens"], a["ks"], a["vs"],
+            float(wl.scale), out, (parts + 1) * 512, partition_size=512)
+    assert e.value.status == kvq.KVQ_ERR_SCRATCH
+    torch.cuda.synchronize()
+    assert not out.any()
+
+
+def test_noalloc_back_to_back_pdl_calls_share_the_array(orc):
+    """Two calls with KVQ_F_PDL on one stream, different shapes, no
+    synchronisation between them: the second call's kernels wait for the
+    first call's merge before they touch the shared array, so both results
+    match the plain entry point's."""
+    wl1 = W.make_attention("noalloc_p1", 106, [2600, 900, 1700, 5],
+                           num_q_heads=16, num_kv_heads=2, head_size=128,
+                           block_size=16)
+    wl2 = W.make_attention("noalloc_p2", 107, [4000, 2561, 130],
+                           num_q_heads=8, num_kv_heads=1, head_size=128,
+                           block_size=16)
+    a1, a2 = _inputs(wl1), _inputs(wl2)
+    want1 = _plain(wl1, a1, 256)
+    want2 = _plain(wl2, a2, 512)
+    out1 = torch.full_like(a1["q"], float("nan"))
+    out2 = torch.full_like(a2["q"], float("nan"))
+    for wl, a, out, part in ((wl1, a1, out1, 256), (wl2, a2, out2, 512)):
+        kvq.kvq_paged_attention_nvfp4_noalloc(
+            a["q"], a["kc"], a["vc"], a["bt"], a["lens"], a["ks"], a["vs"],
+            float(wl.scale), out, a["mcl"], partition_size=part,
+            flags=kvq.KVQ_F_PDL)
+    torch.cuda.synchronize()
+    for wl, out, want in ((wl1, out1, want1), (wl2, out2, want2)):
+        got = out.float().cpu().numpy().astype(np.float64)
+        ref, mag = oracle_attention(orc, wl)
+        tol = (2.0 ** -8 * np.abs(want) + 2.0 ** -9 * mag
+               + 2.0 ** -24 * _vmax(wl, wl.context_lens)[:, None, None])
+        assert np.isfinite(got).all(), wl.name
+        assert (np.abs(got - want) <= tol).all(), wl.name
+
+
+def test_noalloc_rejects_bad_arguments_with_the_plain_codes():
+    """Arguments the plain entry point rejects get its codes, even when the
+    declared context would also need more scratch than the array holds."""
+    wl = W.make_attention("noalloc_args", 108, [16], num_q_heads=8,
+                          num_kv_heads=1, head_size=128, block_size=16)
+    a = _inputs(wl)
+    out = torch.zeros_like(a["q"])
+    huge = 1 << 22  # partitions far past the array
+    for part, flags, code in ((100, 0, kvq.KVQ_ERR_SHAPE),
+                              (1024, 0, kvq.KVQ_ERR_SHAPE),
+                              (512, 1 << 3, kvq.KVQ_ERR_ARG)):
+        with pytest.raises(kvq.KvqError) as e:
+            kvq.kvq_paged_attention_nvfp4_noalloc(
+                a["q"], a["kc"], a["vc"], a["bt"], a["lens"], a["ks"],
+                a["vs"], float(wl.scale), out, huge, partition_size=part,
+                flags=flags)
+        assert e.value.status == code, (part, flags)
+    torch.cuda.synchronize()
+    assert not out.any()
