@@ -220,6 +220,135 @@ gather_indexer_k_kernel(const GatherParams p) {
     *reinterpret_cast<uint32_t*>(p.k_scale + r * 4) = scale_bits;
 }
 
+// ---------------------------------------------------------------------------
+// Bulk-copy form (build option KVQ_GATHER_BULK=1): one CTA of one warp per
+// (sequence, block of its table).  The block's rows of that sequence -- at
+// most B of them, contiguous in the cache and in k_fp8 -- move with two TMA
+// bulk copies (cache -> shared memory, completion counted on an mbarrier
+// waited on with the bounded poll; shared memory -> k_fp8), and their scale
+// bytes (contiguous in the cache, starting at any 4-byte row of k_scale)
+// with one bulk load and 4-byte stores; taken when the rows and scales of a
+// block fit in 48 KB.  Measured on GB300 against the per-row form above
+// (long-context gather, 34.6 MB): a cold single launch 9.38 against 9.63 us
+// (ncu), back to back with KVQ_F_PDL_EARLY_READ 6.41 against 5.57 us (its
+// 8.4 KB-per-warp CTAs find less room beside the finishing predecessor),
+// equal without PDL -- so the per-row form is the default.
+// ---------------------------------------------------------------------------
+__host__ __device__ constexpr int64_t bulk_scale_bytes(int B) {
+  return (static_cast<int64_t>(B) * 4 + 15) & ~int64_t{15};
+}
+
+template <int kEarly>
+__global__ void __launch_bounds__(32)
+gather_bulk_kernel(const GatherParams p) {
+  extern __shared__ __align__(128) uint8_t s_buf[];  // rows, then scales
+  __shared__ __align__(8) uint64_t s_bar;
+  if constexpr (kEarly == kWaitFirst) pdl_prologue();
+  const int lane = threadIdx.x;
+  const int64_t unit = blockIdx.x;
+  const int b = static_cast<int>(unit / p.max_blocks);
+  const int kb = static_cast<int>(unit - static_cast<int64_t>(b) * p.max_blocks);
+  const int64_t c0 = __ldg(p.cu + b);
+  const int64_t len = static_cast<int64_t>(__ldg(p.cu + b + 1)) - c0;
+  const int64_t pos0 = static_cast<int64_t>(kb) * p.B;
+  const int64_t row0 = c0 + pos0;  // first output row of the unit
+  int err = 0;
+  int n = 0;
+  const uint8_t* src = nullptr;
+  if (c0 < 0) {
+    err = len > 0 ? KVQ_DEVERR_SEQ : 0;
+  } else if (len > pos0) {
+    n = static_cast<int>(len - pos0 < p.B ? len - pos0 : p.B);
+    if (row0 + n > p.total) {  // rows past total_tokens are not written
+      err = KVQ_DEVERR_SEQ;
+      n = row0 >= p.total ? 0 : static_cast<int>(p.total - row0);
+    }
+    const int32_t blk = __ldg(p.block_table + b * p.bt_stride + kb);
+    if (blk < 0 || blk >= p.num_blocks) {
+      err |= KVQ_DEVERR_BLOCK;
+      n = 0;
+    } else {
+      src = p.cache + static_cast<int64_t>(blk) * p.block_stride;
+    }
+  }
+  // positions past the block table's last column, and cu_seq_lens that
+  // does not end at total_tokens, are flagged once
+  if (kb == p.max_blocks - 1 && len > static_cast<int64_t>(p.max_blocks) * p.B)
+    err |= KVQ_DEVERR_SEQ;
+  if (unit == 0 && static_cast<int64_t>(__ldg(p.cu + p.num_seqs)) != p.total)
+    err |= KVQ_DEVERR_SEQ;
+
+  const uint32_t kbytes = static_cast<uint32_t>(n) * p.D;
+  const uint32_t sbytes = static_cast<uint32_t>((n * 4 + 15) & ~15);
+  const uint32_t bar = smem_addr(&s_bar);
+  uint8_t* s_scales = s_buf + static_cast<int64_t>(p.B) * p.D;
+  if (lane == 0) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar)
+                 : "memory");
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncwarp();
+  auto issue_loads = [&]() {
+    if (lane != 0 || n == 0) return;
+    asm volatile(
+        "mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;"
+        ::"r"(bar), "r"(kbytes + sbytes + KVQ_TEST_EXTRA_TX)
+        : "memory");
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1], %2, [%3];" ::"r"(smem_addr(s_buf)),
+        "l"(src), "r"(kbytes),
+        "r"(bar)
+        : "memory");
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1], %2, [%3];" ::"r"(smem_addr(s_scales)),
+        "l"(src + static_cast<int64_t>(p.B) * p.D), "r"(sbytes), "r"(bar)
+        : "memory");
+  };
+  if constexpr (kEarly == kWaitWrites) {
+    issue_loads();  // reads while the predecessor finishes
+    pdl_prologue();
+  } else {
+    if constexpr (kEarly == kWaitMeta) pdl_prologue();
+    issue_loads();
+  }
+  if (lane == 0 && err != 0 && p.dev_error != nullptr)
+    atomicOr(p.dev_error, err);
+  if (n == 0) return;
+  if (!mbar_wait(bar, 0)) {
+    // give a copy that may still be in flight a second term before the
+    // shared memory goes away; write nothing
+    mbar_wait(bar, 0);
+    if (lane == 0 && p.dev_error != nullptr)
+      atomicOr(p.dev_error, KVQ_DEVERR_TIMEOUT);
+    return;
+  }
+  if (lane == 0) {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    asm volatile(
+        "cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(
+            p.k_fp8 + row0 * p.D),
+        "r"(smem_addr(s_buf)), "r"(kbytes)
+        : "memory");
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+  }
+  for (int i = lane; i < n; i += 32)
+    *reinterpret_cast<uint32_t*>(p.k_scale + (row0 + i) * 4) =
+        *reinterpret_cast<const uint32_t*>(s_scales + 4 * i);
+  // the bulk store must have read the shared memory before the CTA ends
+  if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
+template <int kEarly>
+cudaError_t launch_bulk(const GatherParams& p, cudaStream_t stream) {
+  const int64_t units = static_cast<int64_t>(p.num_seqs) * p.max_blocks;
+  const size_t smem = static_cast<size_t>(p.B) * p.D + bulk_scale_bytes(p.B);
+  return launch_kernel(gather_bulk_kernel<kEarly>,
+                       dim3(static_cast<unsigned>(units)), 32, smem, stream,
+                       p.pdl, p);
+}
+
 template <int CPR, int kEarly>
 cudaError_t launch_mode(const GatherParams& p, unsigned grid,
                         cudaStream_t stream) {
@@ -248,8 +377,20 @@ cudaError_t launch_cpr(const GatherParams& p, unsigned grid,
 
 }  // namespace
 
+#ifndef KVQ_GATHER_BULK
+#define KVQ_GATHER_BULK 0
+#endif
+
 cudaError_t launch_gather_indexer_k(const GatherParams& p,
                                     cudaStream_t stream) {
+  if (KVQ_GATHER_BULK && p.max_blocks > 0 &&
+      static_cast<int64_t>(p.B) * p.D + bulk_scale_bytes(p.B) <=
+          static_cast<int64_t>(kMaxMetaSmem) &&
+      static_cast<int64_t>(p.num_seqs) * p.max_blocks < (int64_t{1} << 31)) {
+    if (p.early_read) return launch_bulk<kWaitWrites>(p, stream);
+    if (p.early_meta) return launch_bulk<kWaitMeta>(p, stream);
+    return launch_bulk<kWaitFirst>(p, stream);
+  }
   const int64_t units = (p.total + 31) / 32;
   const unsigned grid = static_cast<unsigned>((units + kWarps - 1) / kWarps);
   return p.D == 128 ? launch_cpr<8>(p, grid, stream)
