@@ -229,10 +229,11 @@ gather_indexer_k_kernel(const GatherParams p) {
 // bytes (contiguous in the cache, starting at any 4-byte row of k_scale)
 // with one bulk load and 4-byte stores; taken when the rows and scales of a
 // block fit in 48 KB.  Measured on GB300 against the per-row form above
-// (long-context gather, 34.6 MB): a cold single launch 9.38 against 9.63 us
-// (ncu), back to back with KVQ_F_PDL_EARLY_READ 6.41 against 5.57 us (its
-// 8.4 KB-per-warp CTAs find less room beside the finishing predecessor),
-// equal without PDL -- so the per-row form is the default.
+// (long-context gather, 34.6 MB): a cold single launch 3-8 % faster (ncu:
+// 8.58 against 9.31 us, 9.38 against 9.63 in another capture), back to back
+// with KVQ_F_PDL_EARLY_READ 15 % slower (6.41 against 5.57 us: its 8.4 KB
+// per-warp CTAs find less room beside the finishing predecessor), equal
+// without PDL -- so the per-row form is the default.
 // ---------------------------------------------------------------------------
 __host__ __device__ constexpr int64_t bulk_scale_bytes(int B) {
   return (static_cast<int64_t>(B) * 4 + 15) & ~int64_t{15};

@@ -2,8 +2,8 @@
 library (KVQ_GATHER_BULK=1: one warp per (sequence, block of its table),
 whose rows move cache -> shared memory -> k_fp8 by TMA bulk copies, the
 scale bytes by one bulk load and 4-byte stores).  The default build keeps
-the per-row 16-byte copy, which is faster back to back; this form is a
-little faster as a cold single launch.  Both must give the same bytes: the
+the per-row 16-byte copy, which is faster back to back with early-read
+PDL; this form is 3-8 % faster as a cold single launch.  Both must give the same bytes: the
 gather parity cases (named workloads, sequence-length boundaries, wide
 tables, flagged rows, early-read PDL) and the sharded-gather cases run here
 again against a library built with the option."""
