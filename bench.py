@@ -502,9 +502,10 @@ def run_ours(args):
     assert int(dev_err.item()) == 0, "device error flag raised"
 
     # ---- each named configuration on its own ------------------------------
-    configs = config_legs(args, kvq, wlmod, tm, dev, dev_err, sh, peak, rank,
-                          long_step=dict(store=lambda i: store(0),
-                                         gather=lambda i: gather(i, 0)))
+    configs = config_legs(kvq, wlmod, tm, dev, dev_err, sh, peak, rank,
+                          long_step=dict(store=(lambda i: store(0), st_bytes),
+                                         gather=(lambda i: gather(i, 0),
+                                                 ga_bytes)))
     tm.free()
     assert int(dev_err.item()) == 0, "device error flag raised"
 
@@ -629,8 +630,7 @@ def run_ours(args):
         print(json.dumps(line), flush=True)
 
 
-def config_legs(args, kvq, wlmod, tm, dev, dev_err, sh, peak, rank,
-                long_step):
+def config_legs(kvq, wlmod, tm, dev, dev_err, sh, peak, rank, long_step):
     """Every named configuration timed alone: single launches after a clean
     L2 flush (COLD_REPS of them) and back-to-back spans (median of SPANS),
     beside the floor of an empty launch measured the same way."""
@@ -662,7 +662,6 @@ def config_legs(args, kvq, wlmod, tm, dev, dev_err, sh, peak, rank,
                "note": note}
         out[name] = rec
         del ts
-        return st
 
     def gather_cfg(idx, name, sets, calls, note):
         ga = wlmod.gather_workload(idx, seed=rank_seed(idx, rank))
@@ -682,7 +681,6 @@ def config_legs(args, kvq, wlmod, tm, dev, dev_err, sh, peak, rank,
                      "back_to_back": leg(b2b, byts, peak, ga.total_tokens),
                      "note": note}
         del gs
-        return ga
 
     store_cfg(0, "0_tiny_store", 1, 200,
               "24 tokens (3 skipped), 2 heads, head_size 64: launch-bound; "
@@ -701,13 +699,11 @@ def config_legs(args, kvq, wlmod, tm, dev, dev_err, sh, peak, rank,
               "K/V, none L2-resident at launch)")
     gather_cfg(3, "3_prefill_gather", GATHER_SETS, 200,
                "16 sequences of U[1000, 8192] tokens, block_size 64, "
-               "head_dim 128; back to back over 8 buffer sets (8 x 30 MB)")
-    # the long-context mix's two kernels, cold
-    st4, ga4 = make_workload(rank)
-    for key, fn, byts in (("4_long_store", long_step["store"],
-                           st4.algorithmic_bytes()),
-                          ("4_long_gather", long_step["gather"],
-                           ga4.algorithmic_bytes())):
+               "head_dim 128; back to back over 8 buffer sets (a 35 MB "
+               "cache and 10 MB of outputs each)")
+    # the long-context mix's two kernels, cold (launch, algorithmic bytes)
+    for key, (fn, byts) in (("4_long_store", long_step["store"]),
+                            ("4_long_gather", long_step["gather"])):
         cold = tm.cold(fn)
         out[key] = {"algorithmic_bytes": int(byts),
                     "cold_single_launch": dict(

@@ -73,9 +73,9 @@ def test_gather_shards_union(orc, index, world):
         torch.cuda.synchronize()
         outs.append((k.cpu().numpy().reshape(-1), s.cpu().numpy().reshape(-1)))
     assert int(err.item()) == 0
+    (k_one, s_one), (k_sh, s_sh) = outs
     wk, ws = run_gather(orc, full)
-    for (k_sh, s_sh), (k_one, s_one) in [(outs[1], outs[0])]:
-        assert_bytes_equal(k_sh, k_one, "k_fp8 shards vs one call")
-        assert_bytes_equal(s_sh, s_one, "k_scale shards vs one call")
-        assert_bytes_equal(k_sh, wk, "k_fp8 shards vs oracle")
-        assert_bytes_equal(s_sh, ws, "k_scale shards vs oracle")
+    assert_bytes_equal(k_sh, k_one, "k_fp8 shards vs one call")
+    assert_bytes_equal(s_sh, s_one, "k_scale shards vs one call")
+    assert_bytes_equal(k_sh, wk, "k_fp8 shards vs oracle")
+    assert_bytes_equal(s_sh, ws, "k_scale shards vs oracle")
