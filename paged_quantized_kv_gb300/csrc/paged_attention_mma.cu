@@ -366,21 +366,36 @@ paged_attention_mma_kernel(const AttnParams p) {
   }
   // stretch length: fixed on contiguous pages (the host sets p.part to it)
   const int S = kContig ? KVQ_ATTN_MMA_PART : p.part;
-  const int p0 = part * S;
-  if (p0 >= L) {
+  const int nparts = (L + S - 1) / S;
+  if (part >= nparts) {
     if (part == 0) {  // empty context: the output is zero
       for (int i = tid; i < p.G * kD; i += kThreads)
         p.out[b * p.out_stride0 + (kh * p.G) * kD + i] = 0;
     }
     return;
   }
-  const int nparts = (L + S - 1) / S;
-  // the partition's tokens split evenly over the warps, in whole steps
-  const int ntok = min(S, L - p0);
+  // This CTA's stretch [p0, p1): on contiguous pages the context is split
+  // evenly over its nparts stretches (boundaries at multiples of 32
+  // tokens, every stretch at least 640 tokens when there are several, at
+  // most S + 31), so that no CTA carries a short remainder with three of
+  // its warps idle; elsewhere the caller's partitions.
+  int p0, p1;
+  if constexpr (kContig) {
+    p0 = static_cast<int>(static_cast<int64_t>(part) * L / nparts) & ~31;
+    p1 = part + 1 == nparts
+             ? L
+             : static_cast<int>(static_cast<int64_t>(part + 1) * L / nparts) &
+                   ~31;
+  } else {
+    p0 = part * S;
+    p1 = min(L, p0 + S);
+  }
+  // the stretch's tokens split evenly over the warps, in whole steps
+  const int ntok = p1 - p0;
   const int quarter =
       (ntok + kWarps * kStep - 1) / (kWarps * kStep) * kStep;
   const int w0 = p0 + warp * quarter;
-  const int w1 = min(w0 + quarter, L);
+  const int w1 = min(w0 + quarter, p1);
   const int nsteps = w1 > w0 ? (w1 - w0 + kStep - 1) / kStep : 0;
 
   // block ids of the warp's range (at most 32 blocks), one per lane
