@@ -596,9 +596,10 @@ def run_ours(args):
             note="decode attention over the NVFP4 pages, one step of "
                  "Llama-3.1-70B-shaped attention: 200 sequences, 64 query / "
                  "8 KV heads, head_size 128, block_size 16, contexts 512 + "
-                 "U[0, 2048]; partition_size 512 (the kernel covers up to "
-                 "1280 tokens per CTA on contiguous pages, then the "
-                 "partition merge); not part of the step"),
+                 "U[0, 2048]; partition_size 512 (on these contiguous "
+                 "pages a context splits evenly into ceil(L / 1280) "
+                 "stretches, one CTA each, then the partition merge); not "
+                 "part of the step"),
         "configs": configs,
         "roofline": {
             "bound": "hbm",

@@ -29,9 +29,11 @@
 // per KV head, so they were retired.
 //
 // Design, per CTA of 4 warps = one (stretch of context, KV head, sequence):
-// a stretch is KVQ_ATTN_MMA_PART (1280) tokens on contiguous pages (HND,
-// block_size % 16 == 0, linear K scales), else the caller's partition
-// (<= 512); its tokens are split evenly over the warps, which walk them in
+// on contiguous pages (HND, block_size % 16 == 0, linear K scales) a
+// context of L tokens is split evenly into ceil(L / KVQ_ATTN_MMA_PART)
+// stretches (KVQ_ATTN_MMA_PART = 1280; boundaries at multiples of 32
+// tokens), elsewhere into the caller's partitions (<= 512 tokens); a
+// stretch's tokens are split evenly over the warps, which walk them in
 // steps of 32 tokens:
 //   * Loads: cp.async into the warp's own shared-memory slots, kDepth steps
 //     ahead; the warp waits with cp.async.wait_group only.  Block ids of the
