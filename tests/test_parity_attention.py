@@ -305,3 +305,41 @@ def test_long_contexts_many_partitions(orc):
                           num_q_heads=16, num_kv_heads=2, head_size=128,
                           block_size=16)
     _check(orc, wl, partition_size=512, max_context_len=9000)
+
+
+def _sweep_cases(n=14, seed=2027):
+    """Seeded random mixes of the attention's shape parameters: query heads
+    per KV head, block size (powers of two and other multiples of 4, so
+    both page paths run), layout, swizzled K scales, query type, partition
+    size, and contexts drawn around the block size, the 32-token step, the
+    partition size and the 1280-token stretch (split evenly when a context
+    needs several)."""
+    rng = np.random.default_rng(seed)
+    cases = []
+    for k in range(n):
+        G = int(rng.choice([1, 2, 4, 8, 16]))
+        Hkv = int(rng.choice([1, 2])) if G < 16 else 1
+        B = int(rng.choice([16, 32, 48, 64, 12, 20]))
+        part = int(rng.choice([128, 256, 384, 512]))
+        anchors = [B, 32, part, 1280, 2560, 3840]
+        lens = []
+        for _ in range(int(rng.integers(2, 6))):
+            a = int(rng.choice(anchors)) * int(rng.integers(1, 3))
+            lens.append(max(0, a + int(rng.integers(-3, 4))))
+        lens.append(int(rng.integers(0, 40)))
+        cases.append(dict(name=f"sweep{k}", G=G, Hkv=Hkv, B=B, part=part,
+                          lens=[min(x, 6000) for x in lens],
+                          layout=int(rng.integers(0, 2)),
+                          swz=int(rng.integers(0, 2)) if k % 3 == 0 else 0,
+                          dtype=int(rng.integers(0, 2))))
+    return cases
+
+
+@pytest.mark.parametrize("c", _sweep_cases(), ids=lambda c: c["name"])
+def test_random_shape_sweep(orc, c):
+    wl = W.make_attention(c["name"], 300 + int(c["name"][5:]), c["lens"],
+                          num_q_heads=c["G"] * c["Hkv"],
+                          num_kv_heads=c["Hkv"], head_size=128,
+                          block_size=c["B"], layout=c["layout"],
+                          flags=c["swz"], dtype=c["dtype"])
+    _check(orc, wl, partition_size=c["part"])
