@@ -30,11 +30,14 @@
 //
 // Design, per CTA of 4 warps = one (stretch of context, KV head, sequence):
 // on contiguous pages (HND, block_size % 16 == 0, linear K scales) a
-// context of L tokens is split evenly into ceil(L / KVQ_ATTN_MMA_PART)
+// context of L tokens is split into n = ceil(L / KVQ_ATTN_MMA_PART)
 // stretches (KVQ_ATTN_MMA_PART = 1280; boundaries at multiples of 32
-// tokens), elsewhere into the caller's partitions (<= 512 tokens); a
-// stretch's tokens are split evenly over the warps, which walk them in
-// steps of 32 tokens:
+// tokens) in the proportions 3 : ... : 3 : 1, elsewhere into the caller's
+// partitions (<= 512 tokens); the CTAs are launched stretch-major (every
+// context's first stretch, then the second ones, ...), so that the CTAs
+// that start last, when the SMs begin to fall idle, are the short last
+// stretches; a stretch's tokens are split evenly over the warps, which walk
+// them in steps of 32 tokens:
 //   * Loads: cp.async into the warp's own shared-memory slots, kDepth steps
 //     ahead; the warp waits with cp.async.wait_group only.  Block ids of the
 //     warp's range are loaded once (one per lane) and shuffled.  On
@@ -101,6 +104,17 @@ constexpr int kDepth = KVQ_ATTN_MMA_DEPTH;  // steps in flight per warp
 #ifndef KVQ_ATTN_MMA_PART
 #define KVQ_ATTN_MMA_PART 1280
 #endif
+// Contiguous pages: the last of a context's n > 1 stretches gets 1 /
+// kLastShare of the share of each of the others.
+#ifndef KVQ_ATTN_MMA_LAST_SHARE
+#define KVQ_ATTN_MMA_LAST_SHARE 4
+#endif
+constexpr int kLastShare = KVQ_ATTN_MMA_LAST_SHARE;
+// the longest stretch (the first of two, 2 kLastShare S / (kLastShare + 1)
+// tokens) leaves each warp at most 512 tokens: 32 blocks of 16
+static_assert(2 * kLastShare * KVQ_ATTN_MMA_PART / (kLastShare + 1) <=
+                  4 * 32 * 16,
+              "stretch too long for a warp's block ids");
 // One step's slots of one warp.  On contiguous pages the step's 32
 // tokens arrive in the pages' own order (whichever lane copies a chunk,
 // its bytes keep their place), as 16-byte copies:
@@ -120,7 +134,8 @@ constexpr int kDepth = KVQ_ATTN_MMA_DEPTH;  // steps in flight per warp
 //   V scale 4 x  4 B (the word holding group g of a token pair)
 // followed, after every warp's slots, by the query fragments of the CTA:
 // [n-block][i][lane] x 16 B = lane (g, t)'s dims 32t + 8i .. + 7 of query
-// head 8n + g as fp16.
+// head 8n + g as fp16, and 16 bytes for v_scale (read at the start, used
+// at the end).
 // The warps' partial outputs at the end, one row of head dims per (warp,
 // head): rows kMergeRow floats apart and dim d at column merge_col(d) (bits
 // 1-2 of d XOR bits 5-6), so that both the fragment-layout float2 stores
@@ -142,8 +157,11 @@ struct Slots {
   static constexpr int kStage = kContig ? kKsOff + 512 : kVsOff + 4 * 4 * 32;
   static constexpr int kWarp = kDepth * kStage;
   static constexpr int kQOff = kWarps * kWarp;
+  __host__ __device__ static constexpr int kVsc(int NB) {
+    return kQOff + NB * 4 * 32 * 16;
+  }
   template <int NB>
-  static constexpr int smem() { return kQOff + NB * 4 * 32 * 16; }
+  static constexpr int smem() { return kVsc(NB) + 16; }
   // the merge buffers reuse the copy slots
   static_assert(kQOff >= (kWarps * 16 * kMergeRow + 2 * kWarps * 16 +
                           16 * kWarps + 48) * 4,
@@ -357,7 +375,11 @@ paged_attention_mma_kernel(const AttnParams p) {
   extern __shared__ __align__(16) uint8_t smem[];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, t = lane & 3;
-  const int part = blockIdx.x, kh = blockIdx.y, b = blockIdx.z;
+  // stretch-major launch order: (stretch, sequence, KV head), KV head
+  // fastest
+  const int kh = static_cast<int>(blockIdx.x % p.Hkv);
+  const int sb = static_cast<int>(blockIdx.x / p.Hkv);
+  const int b = sb % p.num_seqs, part = sb / p.num_seqs;
   pdl_prologue();
 
   int L = __ldg(p.lens + b);
@@ -377,16 +399,21 @@ paged_attention_mma_kernel(const AttnParams p) {
     return;
   }
   // This CTA's stretch [p0, p1): on contiguous pages the context is split
-  // evenly over its nparts stretches (boundaries at multiples of 32
-  // tokens, every stretch at least 640 tokens when there are several, at
-  // most S + 31), so that no CTA carries a short remainder with three of
-  // its warps idle; elsewhere the caller's partitions.
+  // over its nparts stretches in the proportions kLastShare : ... :
+  // kLastShare : 1 (boundary i at kLastShare i L / (kLastShare (nparts-1) +
+  // 1), rounded down to a multiple of 32 tokens; the last stretch of two
+  // holds more than S / (kLastShare + 1) tokens), so that no CTA carries a
+  // remainder of a few tokens with three of its warps idle and the last
+  // stretches, launched last, are short; elsewhere the caller's partitions.
   int p0, p1;
   if constexpr (kContig) {
-    p0 = static_cast<int>(static_cast<int64_t>(part) * L / nparts) & ~31;
+    const int64_t den = static_cast<int64_t>(kLastShare) * (nparts - 1) + 1;
+    p0 = static_cast<int>(static_cast<int64_t>(kLastShare) * part * L / den) &
+         ~31;
     p1 = part + 1 == nparts
              ? L
-             : static_cast<int>(static_cast<int64_t>(part + 1) * L / nparts) &
+             : static_cast<int>(static_cast<int64_t>(kLastShare) *
+                                (part + 1) * L / den) &
                    ~31;
   } else {
     p0 = part * S;
@@ -419,32 +446,23 @@ paged_attention_mma_kernel(const AttnParams p) {
   const bool qzero = c2 == 0.f;
   c2 = qzero ? 1.f : fabsf(c2);
 
-  // query fragments into shared memory, once per CTA: entry (n, i, lane)
-  // = lane (g, t)'s dims 32t + 8i .. + 7 of head 8n + g, as fp16
+  // query fragments, staged in shared memory once per CTA: entry (n, i,
+  // lane) = lane (g, t)'s dims 32t + 8i .. + 7 of head 8n + g, as fp16.
+  // Thread tid stages entries tid + 128n (i = its warp, lane = its lane);
+  // they are loaded here and stored once the first copies are out, so that
+  // their latency overlaps that of the block ids.  v_scale, needed only at
+  // the end, is read now as well.
   const uint32_t qbase = smem_u32(smem) + SL::kQOff;
-  for (int e = tid; e < NB * 128; e += kThreads) {
-    const int n = e >> 7, i = (e >> 5) & 3, ln = e & 31;
-    const int hq = 8 * n + (ln >> 2);
-    uint4 v = make_uint4(0u, 0u, 0u, 0u);
-    if (hq < p.G) {
-      v = __ldg(reinterpret_cast<const uint4*>(
-          p.q + b * p.q_stride0 + (kh * p.G + hq) * kD + 32 * (ln & 3) +
-          8 * i));
-      if constexpr (!kF16) {
-        v.x = bf16x2_f16x2(v.x);
-        v.y = bf16x2_f16x2(v.y);
-        v.z = bf16x2_f16x2(v.z);
-        v.w = bf16x2_f16x2(v.w);
-      }
-      v.x ^= qflip; v.y ^= qflip; v.z ^= qflip; v.w ^= qflip;
-      if (qzero) v = make_uint4(0u, 0u, 0u, 0u);
-    }
-    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(
-                     qbase + e * 16),
-                 "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
-                 : "memory");
+  uint4 qv[NB];
+#pragma unroll
+  for (int n = 0; n < NB; ++n) {
+    qv[n] = make_uint4(0u, 0u, 0u, 0u);
+    if (8 * n + g < p.G)
+      qv[n] = __ldg(reinterpret_cast<const uint4*>(
+          p.q + b * p.q_stride0 + (kh * p.G + 8 * n + g) * kD + 32 * t +
+          8 * warp));
   }
-  __syncthreads();
+  const float v_scale_in = tid == 0 ? __ldg(p.v_scale) : 0.f;
 
   const uint32_t wbase = smem_u32(smem) + warp * SL::kWarp;
   const uint8_t* const kside = p.side[0];
@@ -854,6 +872,27 @@ paged_attention_mma_kernel(const AttnParams p) {
 
 #pragma unroll
   for (int i = 0; i < kDepth - 1; ++i) issue(i);
+#pragma unroll
+  for (int n = 0; n < NB; ++n) {
+    uint4 v = qv[n];
+    if (8 * n + g < p.G) {
+      if constexpr (!kF16) {
+        v.x = bf16x2_f16x2(v.x);
+        v.y = bf16x2_f16x2(v.y);
+        v.z = bf16x2_f16x2(v.z);
+        v.w = bf16x2_f16x2(v.w);
+      }
+      v.x ^= qflip; v.y ^= qflip; v.z ^= qflip; v.w ^= qflip;
+      if (qzero) v = make_uint4(0u, 0u, 0u, 0u);
+    }
+    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(
+                     qbase + (tid + kThreads * n) * 16),
+                 "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                 : "memory");
+  }
+  if (tid == 0)
+    *reinterpret_cast<float*>(smem + SL::kVsc(NB)) = v_scale_in;
+  __syncthreads();  // the query is staged
   // the steps with no token to leave out come first; the warp's last
   // (partial) step, and every step when a block of its range has a bad id,
   // take the masked form
@@ -911,30 +950,64 @@ paged_attention_mma_kernel(const AttnParams p) {
     sX[hh] = M;
   }
   __syncthreads();
-  const int d = tid;  // one head dim per thread
-  const int dcol = merge_col(d);
-  const float v_scale = __ldg(p.v_scale);
-  for (int hh = 0; hh < p.G; ++hh) {
+  // The output, 8 dims of one head per thread: physical columns 4k .. 4k+3
+  // and 64 + 4k .. 67 + 4k of the head's rows (a quarter-warp reads 128
+  // contiguous bytes), which by merge_col hold head dims 4k .. 4k+3 and
+  // 64 + 4(k^1) .. +3, their two pairs swapped when k >= 8.  Per dim the
+  // sum runs over the warps in order.
+  const float v_scale = *reinterpret_cast<const float*>(smem + SL::kVsc(NB));
+#pragma unroll
+  for (int r = 0; r < NB; ++r) {
+    const int u = tid + kThreads * r;
+    const int hh = u >> 4, k = u & 15;
+    if (hh >= p.G) break;
     const float4 f = *reinterpret_cast<const float4*>(sF + hh * kWarps);
-    const float* col = sO + hh * kMergeRow + dcol;
-    float acc = 0.f;
-    acc += col[0] * f.x;
-    acc += col[16 * kMergeRow] * f.y;
-    acc += col[32 * kMergeRow] * f.z;
-    acc += col[48 * kMergeRow] * f.w;
+    const float fw[kWarps] = {f.x, f.y, f.z, f.w};
+    float4 a = make_float4(0.f, 0.f, 0.f, 0.f), c = a;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+      const float* row = sO + (w * 16 + hh) * kMergeRow;
+      const float4 x = *reinterpret_cast<const float4*>(row + 4 * k);
+      const float4 y = *reinterpret_cast<const float4*>(row + 64 + 4 * k);
+      a.x += x.x * fw[w]; a.y += x.y * fw[w];
+      a.z += x.z * fw[w]; a.w += x.w * fw[w];
+      c.x += y.x * fw[w]; c.y += y.y * fw[w];
+      c.z += y.z * fw[w]; c.w += y.w * fw[w];
+    }
+    if (k >= 8) {
+      a = make_float4(a.z, a.w, a.x, a.y);
+      c = make_float4(c.z, c.w, c.x, c.y);
+    }
+    const int da = 4 * k, dc = 64 + 4 * (k ^ 1);
     const float den = sD[hh], inv = sI[hh];
     if (nparts == 1) {
-      const float y = den > 0.f ? acc * inv * v_scale : 0.f;
-      p.out[b * p.out_stride0 + (kh * p.G + hh) * kD + d] =
-          float_to_out<kF16>(y);
+      auto pack = [&](float lo, float hi) -> uint32_t {
+        const float ylo = den > 0.f ? lo * inv * v_scale : 0.f;
+        const float yhi = den > 0.f ? hi * inv * v_scale : 0.f;
+        return static_cast<uint32_t>(float_to_out<kF16>(ylo)) |
+               (static_cast<uint32_t>(float_to_out<kF16>(yhi)) << 16);
+      };
+      uint16_t* orow = p.out + b * p.out_stride0 + (kh * p.G + hh) * kD;
+      *reinterpret_cast<uint2*>(orow + da) =
+          make_uint2(pack(a.x, a.y), pack(a.z, a.w));
+      *reinterpret_cast<uint2*>(orow + dc) =
+          make_uint2(pack(c.x, c.y), pack(c.z, c.w));
     } else {
-      const int64_t r =
+      const int64_t rr =
           (static_cast<int64_t>(b) * p.Hq + kh * p.G + hh) * p.max_parts +
           part;
-      p.tmp_out[r * kD + d] = den > 0.f ? acc * inv : 0.f;
-      if (d == 0) {
-        p.max_logits[r] = sX[hh];
-        p.exp_sums[r] = den;
+      const float s = den > 0.f ? inv : 0.f;
+      const bool live = den > 0.f;
+      float* trow = p.tmp_out + rr * kD;
+      *reinterpret_cast<float4*>(trow + da) =
+          live ? make_float4(a.x * s, a.y * s, a.z * s, a.w * s)
+               : make_float4(0.f, 0.f, 0.f, 0.f);
+      *reinterpret_cast<float4*>(trow + dc) =
+          live ? make_float4(c.x * s, c.y * s, c.z * s, c.w * s)
+               : make_float4(0.f, 0.f, 0.f, 0.f);
+      if (k == 0) {
+        p.max_logits[rr] = sX[hh];
+        p.exp_sums[rr] = den;
       }
     }
   }
@@ -1044,7 +1117,11 @@ cudaError_t launch_mma(const AttnParams& caller, cudaStream_t stream) {
     if (err != cudaSuccess) return err;
     configured[dev & 63] = true;
   }
-  const dim3 grid(parts > 0 ? parts : 1, p.Hkv, p.num_seqs);
+  // one CTA per (stretch, sequence, KV head), stretch-major (the checks
+  // keep the count below 2^31)
+  const int64_t ctas =
+      static_cast<int64_t>(parts > 0 ? parts : 1) * p.num_seqs * p.Hkv;
+  const dim3 grid(static_cast<unsigned>(ctas));
   err = launch_kernel(kernel, grid, kThreads,
                       Slots<kContig>::template smem<NG / 8>(), stream, p.pdl,
                       p);

@@ -21,7 +21,7 @@ swizzled K scales, block sizes 4 to 384 (12 and 384 not powers of two),
 large logits (one-hot weights), pages written by the GPU store, a PDL chain
 store -> attention, the Llama-3.1-70B-shaped decode batch (sampled rows),
 clamped contexts and invalid block ids (flags), and bitwise determinism.
-The ranges of the kernel's warps (a quarter of a stretch of up to 1280
+The ranges of the kernel's warps (a quarter of a stretch of up to 2048
 tokens each, walked in steps of 32) end inside a step, at a step boundary
 and one token past it across these lengths, so both the unmasked steps and
 the masked last step run, and a bad block id makes a whole range masked."""
@@ -297,8 +297,9 @@ def test_bad_blocks_inside_contexts(orc):
 
 
 def test_long_contexts_many_partitions(orc):
-    """Contexts of several thousand tokens (up to 17 partitions of 512; the
-    kernel's CTAs cover 1280 tokens each on these pages) with a
+    """Contexts of several thousand tokens (up to 17 partitions of 512; on
+    these pages the kernel's CTAs cover stretches of up to 2048 tokens, the
+    last of a context a quarter of the others) with a
     max_context_len above the longest context, so the scratch has more rows
     than used."""
     wl = W.make_attention("long", 95, [4097, 8191, 3000, 1, 1024, 2048],
@@ -312,8 +313,8 @@ def _sweep_cases(n=14, seed=2027):
     per KV head, block size (powers of two and other multiples of 4, so
     both page paths run), layout, swizzled K scales, query type, partition
     size, and contexts drawn around the block size, the 32-token step, the
-    partition size and the 1280-token stretch (split evenly when a context
-    needs several)."""
+    partition size and the 1280-token stretch (split 4 : ... : 4 : 1 when a
+    context needs several)."""
     rng = np.random.default_rng(seed)
     cases = []
     for k in range(n):

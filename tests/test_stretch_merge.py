@@ -1,0 +1,122 @@
+"""GPU tests of contexts split over several stretches and merged.
+
+On contiguous pages the attention kernel splits a context of more than one
+stretch (1280 tokens) into CTAs in the proportions 4 : ... : 4 : 1, each
+writing its partial result to the caller's scratch, and the partition-merge
+kernel combines them.  These tests run that path against the oracle over
+contexts of two to ten stretches, with scratch full of random bits, twice in
+a row on the same scratch, in a CUDA graph replayed with a new query each
+time, and with partition sizes 512, 384 and 128 (which set the scratch rows
+per head but not the stretches: the outputs are bitwise equal)."""
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+from paged_quantized_kv_gb300 import kvq
+from paged_quantized_kv_gb300 import workloads as W
+from tests.gpu_helpers import to_dev
+from tests.test_parity_attention import (_upload, _vmax, assert_close,
+                                         oracle_attention)
+
+pytestmark = pytest.mark.gpu
+
+LONG = [1281, 2560, 2561, 3841, 6400, 12800, 700, 1]
+
+
+class Call:
+    """One attention call's device buffers, the scratch filled with random
+    bits."""
+
+    def __init__(self, wl, partition_size=512, seed=0):
+        self.wl, self.part = wl, partition_size
+        self.caches = _upload(wl)
+        self.q = torch.from_numpy(wl.query.view(np.int16)).cuda().view(
+            torch.bfloat16)
+        self.out = torch.full(self.q.shape, float("nan"),
+                              dtype=torch.bfloat16, device="cuda")
+        self.bt, self.lens = to_dev(wl.block_table), to_dev(wl.context_lens)
+        self.ks = torch.tensor([float(wl.k_scale)], device="cuda")
+        self.vs = torch.tensor([float(wl.v_scale)], device="cuda")
+        self.mcl = int(wl.context_lens.max())
+        self.scratch = kvq.attention_scratch(
+            wl.num_seqs, wl.num_q_heads, self.mcl, partition_size,
+            wl.head_size, torch.device("cuda"))
+        g = torch.Generator(device="cuda").manual_seed(seed)
+        for t in self.scratch:
+            t.view(torch.int32).copy_(torch.randint(
+                -2 ** 31, 2 ** 31 - 1, t.shape, dtype=torch.int32,
+                device="cuda", generator=g))
+
+    def __call__(self, flags=kvq.KVQ_F_PDL):
+        _, kc, vc = self.caches
+        es, ml, tmp = self.scratch
+        kvq.kvq_paged_attention_nvfp4(
+            self.q, kc, vc, self.bt, self.lens, self.ks, self.vs,
+            float(self.wl.scale), self.out, self.mcl, self.part, es, ml, tmp,
+            flags=flags)
+
+    def result(self):
+        torch.cuda.synchronize()
+        return self.out.float().cpu().numpy().astype(np.float64)
+
+    def check(self, orc, wl=None, what=""):
+        wl = self.wl if wl is None else wl
+        ref, mag = oracle_attention(orc, wl)
+        return assert_close(self.result(), ref, mag,
+                            _vmax(wl, wl.context_lens), what)
+
+
+@pytest.mark.parametrize("part", [512, 128])
+def test_many_stretches_random_scratch(orc, part):
+    wl = W.make_attention(f"long{part}", 110, LONG, num_q_heads=16,
+                          num_kv_heads=2, head_size=128, block_size=16)
+    c = Call(wl, part, seed=part)
+    c()
+    c.check(orc, what="first call")
+    first = c.result()
+    c.out.fill_(float("nan"))
+    c()
+    c.check(orc, what="second call")
+    assert np.array_equal(first, c.result())
+
+
+def test_graph_replays_with_new_queries(orc):
+    wl = W.make_attention("greplay", 112, [3000, 1281, 77, 2600, 5200],
+                          num_q_heads=16, num_kv_heads=2, head_size=128,
+                          block_size=16)
+    c = Call(wl, 512, seed=7)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        c()  # the first call configures the kernel (outside the capture)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(graph, stream=side):
+            c()
+    rng = np.random.default_rng(113)
+    for rep in range(3):
+        qf = rng.standard_normal(wl.query.shape).astype(np.float32)
+        bits = W.bf16_bits(qf.reshape(-1)).reshape(qf.shape)
+        c.q.copy_(torch.from_numpy(bits.view(np.int16)).cuda().view(
+            torch.bfloat16))
+        c.out.fill_(float("nan"))
+        graph.replay()
+        c.check(orc, dataclasses.replace(wl, query=bits), f"replay {rep}")
+
+
+def test_merge_matches_across_partition_sizes(orc):
+    """The stretches do not depend on the caller's partition size; only the
+    scratch row stride does, so the outputs are bitwise equal."""
+    wl = W.make_attention("pstride", 114, [4000, 1500, 2561], num_q_heads=8,
+                          num_kv_heads=1, head_size=128, block_size=16)
+    outs = []
+    for part in (512, 384, 128):
+        c = Call(wl, part, seed=part + 1)
+        c()
+        outs.append(c.result())
+    c.check(orc, what="partition strides")
+    assert np.array_equal(outs[0], outs[1])
+    assert np.array_equal(outs[0], outs[2])
