@@ -136,11 +136,12 @@ static_assert(2 * kLastShare * KVQ_ATTN_MMA_PART / (kLastShare + 1) <=
 // [n-block][i][lane] x 16 B = lane (g, t)'s dims 32t + 8i .. + 7 of query
 // head 8n + g as fp16, and 16 bytes for v_scale (read at the start, used
 // at the end).
-// The warps' partial outputs at the end, one row of head dims per (warp,
-// head): rows kMergeRow floats apart and dim d at column merge_col(d) (bits
-// 1-2 of d XOR bits 5-6), so that both the fragment-layout float2 stores
-// (lane (g, t) writes dims 16g + 2mb, +1 of head 2t + c) and the readers
-// (one dim per thread) meet no bank conflict.
+// The warps' partial outputs at the end, in each warp's own slots: one row
+// of head dims per head, rows kMergeRow floats apart and dim d at column
+// merge_col(d) (bits 1-2 of d XOR bits 5-6), so that both the
+// fragment-layout float2 stores (lane (g, t) writes dims 16g + 4mb + e and
+// 16g + 4mb + 2 + e of head 2t + c) and the readers (a quarter-warp reads
+// 128 contiguous bytes of a row) meet no bank conflict.
 constexpr int kMergeRow = kD + 4;
 __host__ __device__ constexpr int merge_col(int d) {
   return d ^ (((d >> 5) & 3) << 1);
@@ -162,13 +163,9 @@ struct Slots {
   }
   template <int NB>
   static constexpr int smem() { return kVsc(NB) + 16; }
-  // the merge buffers reuse the copy slots
-  static_assert(kQOff >= (kWarps * 16 * kMergeRow + 2 * kWarps * 16 +
-                          16 * kWarps + 48) * 4,
-                "");
-  static_assert((kWarps * 16 * kMergeRow + 2 * kWarps * 16) % 4 == 0 &&
-                    kWarps == 4,
-                "merge factors: one 16-byte row per head");
+  // a warp's partial result (16 rows of kMergeRow floats, then 16 maxima
+  // and 16 sums) reuses its own copy slots
+  static_assert(kWarp >= (16 * kMergeRow + 32) * 4, "");
 };
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -903,16 +900,15 @@ paged_attention_mma_kernel(const AttnParams p) {
   cp_async_wait<0>();  // nothing may land after the slots are reused
 
   // ---- merge the 4 warps' partial results in shared memory ----------------
-  __syncthreads();  // every warp is done with its copy slots
-  float* sO = reinterpret_cast<float*>(smem);        // [warp][16][kMergeRow]
-  float* sM = sO + kWarps * 16 * kMergeRow;          // [warp][16]
-  float* sL = sM + kWarps * 16;                      // [warp][16]
+  // Each warp writes its own into its copy slots (all its copies have
+  // landed; no other warp uses them), so one barrier suffices.
+  float* const wO = reinterpret_cast<float*>(smem + warp * SL::kWarp);
 #pragma unroll
   for (int n = 0; n < NB; ++n)
 #pragma unroll
     for (int c = 0; c < 2; ++c) {
       const int hh = 8 * n + 2 * t + c;
-      float* row = sO + (warp * 16 + hh) * kMergeRow;
+      float* row = wO + hh * kMergeRow;
 #pragma unroll
       for (int mb = 0; mb < 4; ++mb) {
         *reinterpret_cast<float2*>(row + merge_col(16 * g + 4 * mb)) =
@@ -921,34 +917,11 @@ paged_attention_mma_kernel(const AttnParams p) {
             make_float2(o[mb][0][n][2 + c], o[mb][1][n][2 + c]);
       }
       if (g == 0) {
-        sM[warp * 16 + hh] =
+        wO[16 * kMergeRow + hh] =
             m_run[n][c] == -INFINITY ? kNoLogit : m_run[n][c];
-        sL[warp * 16 + hh] = lacc[n][c];
+        wO[16 * kMergeRow + 16 + hh] = lacc[n][c];
       }
     }
-  __syncthreads();
-  // once per head: M, the warps' factors exp2(m_w - M), the denominator and
-  // its reciprocal
-  float* sF = sL + kWarps * 16;  // [16][kWarps] factors (16-byte rows)
-  float* sD = sF + 16 * kWarps;  // [16] denominators
-  float* sX = sD + 16;           // [16] M
-  float* sI = sX + 16;           // [16] 1 / denominator
-  if (tid < p.G) {
-    const int hh = tid;
-    float M = sM[hh];
-#pragma unroll
-    for (int w = 1; w < kWarps; ++w) M = fmaxf(M, sM[w * 16 + hh]);
-    float den = 0.f;
-#pragma unroll
-    for (int w = 0; w < kWarps; ++w) {
-      const float f = ex2(sM[w * 16 + hh] - M);
-      sF[hh * kWarps + w] = f;
-      den += sL[w * 16 + hh] * f;
-    }
-    sD[hh] = den;
-    sI[hh] = den > 0.f ? 1.0f / den : 0.f;
-    sX[hh] = M;
-  }
   __syncthreads();
   // The output, 8 dims of one head per thread: physical columns 4k .. 4k+3
   // and 64 + 4k .. 67 + 4k of the head's rows (a quarter-warp reads 128
@@ -961,12 +934,29 @@ paged_attention_mma_kernel(const AttnParams p) {
     const int u = tid + kThreads * r;
     const int hh = u >> 4, k = u & 15;
     if (hh >= p.G) break;
-    const float4 f = *reinterpret_cast<const float4*>(sF + hh * kWarps);
-    const float fw[kWarps] = {f.x, f.y, f.z, f.w};
+    // the head's maximum M over the warps, their factors exp2(m_w - M) and
+    // the denominator
+    const float* wbuf[kWarps];
+    float mw[kWarps];
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+      wbuf[w] = reinterpret_cast<const float*>(smem + w * SL::kWarp);
+      mw[w] = wbuf[w][16 * kMergeRow + hh];
+    }
+    float M = mw[0];
+#pragma unroll
+    for (int w = 1; w < kWarps; ++w) M = fmaxf(M, mw[w]);
+    float fw[kWarps], den = 0.f;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+      fw[w] = ex2(mw[w] - M);
+      den += wbuf[w][16 * kMergeRow + 16 + hh] * fw[w];
+    }
+    const float inv = den > 0.f ? 1.0f / den : 0.f;
     float4 a = make_float4(0.f, 0.f, 0.f, 0.f), c = a;
 #pragma unroll
     for (int w = 0; w < kWarps; ++w) {
-      const float* row = sO + (w * 16 + hh) * kMergeRow;
+      const float* row = wbuf[w] + hh * kMergeRow;
       const float4 x = *reinterpret_cast<const float4*>(row + 4 * k);
       const float4 y = *reinterpret_cast<const float4*>(row + 64 + 4 * k);
       a.x += x.x * fw[w]; a.y += x.y * fw[w];
@@ -979,7 +969,6 @@ paged_attention_mma_kernel(const AttnParams p) {
       c = make_float4(c.z, c.w, c.x, c.y);
     }
     const int da = 4 * k, dc = 64 + 4 * (k ^ 1);
-    const float den = sD[hh], inv = sI[hh];
     if (nparts == 1) {
       auto pack = [&](float lo, float hi) -> uint32_t {
         const float ylo = den > 0.f ? lo * inv * v_scale : 0.f;
@@ -1006,7 +995,7 @@ paged_attention_mma_kernel(const AttnParams p) {
           live ? make_float4(c.x * s, c.y * s, c.z * s, c.w * s)
                : make_float4(0.f, 0.f, 0.f, 0.f);
       if (k == 0) {
-        p.max_logits[rr] = sX[hh];
+        p.max_logits[rr] = M;
         p.exp_sums[rr] = den;
       }
     }
