@@ -31,8 +31,8 @@
 // Design, per CTA of 4 warps = one (stretch of context, KV head, sequence):
 // on contiguous pages (HND, block_size % 16 == 0, linear K scales) a
 // context of L tokens is split into n = ceil(L / KVQ_ATTN_MMA_PART)
-// stretches (KVQ_ATTN_MMA_PART = 1280; boundaries at multiples of 32
-// tokens) in the proportions 3 : ... : 3 : 1, elsewhere into the caller's
+// stretches (KVQ_ATTN_MMA_PART = 1792; boundaries at multiples of 32
+// tokens) in the proportions 4 : ... : 4 : 1, elsewhere into the caller's
 // partitions (<= 512 tokens); the CTAs are launched stretch-major (every
 // context's first stretch, then the second ones, ...), so that the CTAs
 // that start last, when the SMs begin to fall idle, are the short last
@@ -40,7 +40,7 @@
 // them in steps of 32 tokens:
 //   * Loads: cp.async into the warp's own shared-memory slots, kDepth steps
 //     ahead; the warp waits with cp.async.wait_group only.  Block ids of the
-//     warp's range are loaded once (one per lane) and shuffled.  On
+//     warp's range are loaded once (one or two per lane) and shuffled.  On
 //     contiguous pages one block id serves 16 tokens and the pages' bytes
 //     keep their order (16-byte copies, a step's scales in one copy per
 //     lane; a bad block id zero-filled); elsewhere every thread copies
@@ -99,10 +99,10 @@ constexpr int kStep = 32;        // tokens per warp step
 #define KVQ_ATTN_MMA_DEPTH 2
 #endif
 constexpr int kDepth = KVQ_ATTN_MMA_DEPTH;  // steps in flight per warp
-// Tokens per CTA on contiguous pages (a multiple of 4 x 32; at most
-// 4 x 32 blocks of 16 tokens).
+// Contiguous pages: a context of up to this many tokens is one stretch;
+// longer ones are split (see kLastShare).
 #ifndef KVQ_ATTN_MMA_PART
-#define KVQ_ATTN_MMA_PART 1280
+#define KVQ_ATTN_MMA_PART 1792
 #endif
 // Contiguous pages: the last of a context's n > 1 stretches gets 1 /
 // kLastShare of the share of each of the others.
@@ -111,9 +111,9 @@ constexpr int kDepth = KVQ_ATTN_MMA_DEPTH;  // steps in flight per warp
 #endif
 constexpr int kLastShare = KVQ_ATTN_MMA_LAST_SHARE;
 // the longest stretch (the first of two, 2 kLastShare S / (kLastShare + 1)
-// tokens) leaves each warp at most 512 tokens: 32 blocks of 16
+// tokens) leaves each warp at most 1024 tokens: 64 blocks of 16
 static_assert(2 * kLastShare * KVQ_ATTN_MMA_PART / (kLastShare + 1) <=
-                  4 * 32 * 16,
+                  4 * 64 * 16,
               "stretch too long for a warp's block ids");
 // One step's slots of one warp.  On contiguous pages the step's 32
 // tokens arrive in the pages' own order (whichever lane copies a chunk,
@@ -424,15 +424,21 @@ paged_attention_mma_kernel(const AttnParams p) {
   const int w1 = min(w0 + quarter, p1);
   const int nsteps = w1 > w0 ? (w1 - w0 + kStep - 1) / kStep : 0;
 
-  // block ids of the warp's range (at most 32 blocks), one per lane
+  // block ids of the warp's range, one or two per lane: blocks e0 + lane
+  // and, on contiguous pages (ranges of up to 64 blocks), e0 + 32 + lane;
+  // elsewhere a range spans at most 32 blocks
   const int e0 = p.b_shift >= 0 ? (w0 >> p.b_shift) : w0 / p.B;
-  int32_t bt_lane = -1;
-  bool lane_in = false;  // block e0 + lane holds tokens of the warp's range
+  int32_t bt_lane = -1, bt_hi = -1;
+  bool lane_in = false, hi_in = false;  // the block holds tokens of the range
   if (nsteps > 0) {
     const int e1 = p.b_shift >= 0 ? ((w1 - 1) >> p.b_shift) : (w1 - 1) / p.B;
+    const int32_t* row = p.block_table + b * p.bt_stride;
     lane_in = e0 + lane <= e1;
-    if (lane_in)
-      bt_lane = __ldg(p.block_table + b * p.bt_stride + e0 + lane);
+    if (lane_in) bt_lane = __ldg(row + e0 + lane);
+    if constexpr (kContig) {
+      hi_in = e0 + 32 + lane <= e1;
+      if (hi_in) bt_hi = __ldg(row + e0 + 32 + lane);
+    }
   }
 
   // Logit scale in log2 units, made positive so that the maximum of the
@@ -489,8 +495,15 @@ paged_attention_mma_kernel(const AttnParams p) {
   // flagged here, once (its tokens are left out below).
   const uint32_t bmask =
       __ballot_sync(0xFFFFFFFFu, bt_lane >= 0 && bt_lane < p.num_blocks);
-  const uint32_t rmask = __ballot_sync(0xFFFFFFFFu, lane_in);
-  if (lane == 0 && p.dev_error != nullptr && (rmask & ~bmask) != 0u)
+  const uint64_t bmask64 =
+      bmask | static_cast<uint64_t>(__ballot_sync(
+                  0xFFFFFFFFu, bt_hi >= 0 && bt_hi < p.num_blocks))
+                  << 32;
+  const uint64_t rmask64 =
+      __ballot_sync(0xFFFFFFFFu, lane_in) |
+      static_cast<uint64_t>(__ballot_sync(0xFFFFFFFFu, hi_in)) << 32;
+  const bool bad_block = (rmask64 & ~bmask64) != 0u;
+  if (lane == 0 && p.dev_error != nullptr && bad_block)
     atomicOr(p.dev_error, KVQ_DEVERR_BLOCK);
 
   // Whether token `tok` takes part (inside the range, valid block id);
@@ -504,11 +517,15 @@ paged_attention_mma_kernel(const AttnParams p) {
   // its fragments are read from (V data of token 2t + e of a piece; K
   // scale word of token g; V scale word of tokens 2t, 2t+1)
   const int v_dst = vchunk(lane) * 16;
-  // contiguous pages: lane e's block e0 + e as the K-side base of this KV
-  // head (block 0 stands in for a bad id, whose half is zero-filled from
-  // the query instead), V data at + vdelta, the K scale rows at + sdelta
+  // contiguous pages: lane e's blocks e0 + e and e0 + 32 + e as the K-side
+  // bases of this KV head (block 0 stands in for a bad id, whose half is
+  // zero-filled from the query instead), V data at + vdelta, the K scale
+  // rows at + sdelta
   const uint8_t* const kb_lane =
       kside + static_cast<int64_t>((bmask >> lane) & 1u ? bt_lane : 0) *
+                  p.page_stride + kh * p.dhs;
+  const uint8_t* const kb_hi =
+      kside + static_cast<int64_t>((bmask64 >> (32 + lane)) & 1u ? bt_hi : 0) *
                   p.page_stride + kh * p.dhs;
   const int64_t vdelta = vside - kside;
   const int64_t sdelta = p.scale_off + kh * p.shs - kh * p.dhs;
@@ -537,16 +554,17 @@ paged_attention_mma_kernel(const AttnParams p) {
       for (int h = 0; h < 2; ++h) {
         const int T = w0 + kStep * i + 16 * h;
         const int idx = p.b_shift >= 0 ? (T >> p.b_shift) : T / p.B;
-        const int e = (idx - e0) & 31;
-        const uint64_t kl = reinterpret_cast<uint64_t>(kb_lane);
+        const int e = idx - e0;  // 0 .. 63, warp-uniform
+        const uint64_t kl =
+            reinterpret_cast<uint64_t>(e < 32 ? kb_lane : kb_hi);
         const uint32_t lo =
-            __shfl_sync(0xFFFFFFFFu, static_cast<uint32_t>(kl), e);
+            __shfl_sync(0xFFFFFFFFu, static_cast<uint32_t>(kl), e & 31);
         const uint32_t hi =
-            __shfl_sync(0xFFFFFFFFu, static_cast<uint32_t>(kl >> 32), e);
+            __shfl_sync(0xFFFFFFFFu, static_cast<uint32_t>(kl >> 32), e & 31);
         const uint8_t* kb = reinterpret_cast<const uint8_t*>(
             (static_cast<uint64_t>(hi) << 32) | lo);
         // one block holds the whole half: the branch is warp-uniform
-        bok[h] = (bmask >> e) & 1u;
+        bok[h] = (bmask64 >> e) & 1u;
         const int toff = (T - idx * p.B) * 64;
         sb[h] = kb + sdelta + (toff >> 3);
         const uint32_t kd = st + kKdOff + 2 * h * 512 + lane * 16;
@@ -666,8 +684,8 @@ paged_attention_mma_kernel(const AttnParams p) {
       const int i0 = p.b_shift >= 0 ? (T0 >> p.b_shift) : T0 / p.B;
       const int i1 =
           p.b_shift >= 0 ? ((T0 + 16) >> p.b_shift) : (T0 + 16) / p.B;
-      const uint32_t v0 = (bmask >> ((i0 - e0) & 31)) & 1u;
-      const uint32_t v1 = (bmask >> ((i1 - e0) & 31)) & 1u;
+      const uint32_t v0 = static_cast<uint32_t>(bmask64 >> (i0 - e0)) & 1u;
+      const uint32_t v1 = static_cast<uint32_t>(bmask64 >> (i1 - e0)) & 1u;
       const int rem = w1 - T0 - g;  // token T0 + g + 8j usable: 8j < rem
       kvalid = (v0 & static_cast<uint32_t>(rem > 0)) |
                ((v0 & static_cast<uint32_t>(rem > 8)) << 1) |
@@ -893,7 +911,7 @@ paged_attention_mma_kernel(const AttnParams p) {
   // the steps with no token to leave out come first; the warp's last
   // (partial) step, and every step when a block of its range has a bad id,
   // take the masked form
-  const int nfast = (rmask & ~bmask) != 0u ? 0 : (w1 - w0) / kStep;
+  const int nfast = bad_block ? 0 : (w1 - w0) / kStep;
   int i = 0;
   for (; i < nfast; ++i) step(i, std::false_type{});
   for (; i < nsteps; ++i) step(i, std::true_type{});

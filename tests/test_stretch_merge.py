@@ -120,3 +120,53 @@ def test_merge_matches_across_partition_sizes(orc):
     c.check(orc, what="partition strides")
     assert np.array_equal(outs[0], outs[1])
     assert np.array_equal(outs[0], outs[2])
+
+
+@pytest.mark.parametrize("B", [16, 32, 48])
+def test_stretch_boundaries(orc, B):
+    """Contexts at the stretch length (1792) and at twice it, one token
+    either side: the first of two stretches then holds up to 2848 tokens,
+    a warp range up to 46 blocks of 16 (the block ids of its second 32
+    blocks come from each lane's second entry)."""
+    wl = W.make_attention(f"edge{B}", 115, [1792, 1793, 3584, 3585, 2000],
+                          num_q_heads=8, num_kv_heads=1, head_size=128,
+                          block_size=B)
+    c = Call(wl, 512, seed=B)
+    c()
+    c.check(orc, what=f"stretch edges B={B}")
+
+
+def test_bad_blocks_in_long_ranges(orc):
+    """Out-of-range block ids among the second 32 blocks of a warp's range
+    (contexts of 3584 and 3000 tokens: warp ranges of 736 and 608 tokens,
+    46 and 38 blocks) and among the first 32 (2100 tokens): flagged, and
+    their 16 tokens left out, as the oracle gives with those blocks removed
+    from the table."""
+    B = 16
+    wl = W.make_attention("longbad", 116, [3584, 3000, 2100],
+                          num_q_heads=8, num_kv_heads=1, head_size=128,
+                          block_size=B)
+    drop = {0: 40, 1: 73, 2: 33}         # sequence -> block made bad
+    wl.block_table[0, 40] = -3
+    wl.block_table[1, 73] = wl.num_blocks
+    wl.block_table[2, 33] = wl.num_blocks + 100
+    c = Call(wl, 512, seed=9)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    _, kc, vc = c.caches
+    es, ml, tmp = c.scratch
+    kvq.kvq_paged_attention_nvfp4(
+        c.q, kc, vc, c.bt, c.lens, c.ks, c.vs, float(wl.scale), c.out,
+        c.mcl, 512, es, ml, tmp, flags=kvq.KVQ_F_PDL, dev_error=err)
+    got = c.result()
+    assert int(err.item()) & kvq.KVQ_DEVERR_BLOCK
+    bt = np.zeros_like(wl.block_table)
+    lens = wl.context_lens.copy()
+    for b in range(wl.num_seqs):
+        row = list(wl.block_table[b])
+        del row[drop[b]]
+        row.append(0)
+        lens[b] -= B
+        bt[b] = row
+    ref_wl = dataclasses.replace(wl, block_table=bt, context_lens=lens)
+    ref, mag = oracle_attention(orc, ref_wl)
+    assert_close(got, ref, mag, _vmax(ref_wl, lens), "bad blocks, long")
