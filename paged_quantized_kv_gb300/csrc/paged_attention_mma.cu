@@ -364,9 +364,13 @@ constexpr float kLazy = 8.0f;
 // kContig: HND pages with block_size % 16 == 0, so each 16 tokens of a
 // step lie in one block and their rows (and scale rows) are contiguous: one
 // block id and lane-constant offsets per 16 tokens.
-template <int NG, bool kF16, bool kContig>
+// kPages: 0 = other pages, 1 = contiguous, 2 = contiguous with
+// block_size 16, where (warp ranges starting at multiples of 32 tokens)
+// half h of a warp's step i is its block 2i + h, whole.
+template <int NG, bool kF16, int kPages>
 __global__ void __launch_bounds__(kThreads, NG == 8 ? 4 : 2)
 paged_attention_mma_kernel(const AttnParams p) {
+  constexpr bool kContig = kPages != 0, kB16 = kPages == 2;
   constexpr int NB = NG / 8;  // n-blocks of 8 query heads
   using SL = Slots<kContig>;
   extern __shared__ __align__(16) uint8_t smem[];
@@ -553,7 +557,8 @@ paged_attention_mma_kernel(const AttnParams p) {
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         const int T = w0 + kStep * i + 16 * h;
-        const int idx = p.b_shift >= 0 ? (T >> p.b_shift) : T / p.B;
+        const int idx = kB16 ? e0 + 2 * i + h
+                        : p.b_shift >= 0 ? (T >> p.b_shift) : T / p.B;
         const int e = idx - e0;  // 0 .. 63, warp-uniform
         const uint64_t kl =
             reinterpret_cast<uint64_t>(e < 32 ? kb_lane : kb_hi);
@@ -565,7 +570,7 @@ paged_attention_mma_kernel(const AttnParams p) {
             (static_cast<uint64_t>(hi) << 32) | lo);
         // one block holds the whole half: the branch is warp-uniform
         bok[h] = (bmask64 >> e) & 1u;
-        const int toff = (T - idx * p.B) * 64;
+        const int toff = kB16 ? 0 : (T - idx * p.B) * 64;
         sb[h] = kb + sdelta + (toff >> 3);
         const uint32_t kd = st + kKdOff + 2 * h * 512 + lane * 16;
         const uint32_t vd = st + kVdOff + 2 * h * 512 + v_dst;
@@ -681,9 +686,11 @@ paged_attention_mma_kernel(const AttnParams p) {
     uint32_t kvalid = 0xFu;  // bit j: K token T0 + g + 8j is usable
     if constexpr (kMasked && kContig) {
       // each 16-token half lies in one block
-      const int i0 = p.b_shift >= 0 ? (T0 >> p.b_shift) : T0 / p.B;
-      const int i1 =
-          p.b_shift >= 0 ? ((T0 + 16) >> p.b_shift) : (T0 + 16) / p.B;
+      const int i0 = kB16 ? e0 + 2 * i
+                     : p.b_shift >= 0 ? (T0 >> p.b_shift) : T0 / p.B;
+      const int i1 = kB16 ? i0 + 1
+                     : p.b_shift >= 0 ? ((T0 + 16) >> p.b_shift)
+                                      : (T0 + 16) / p.B;
       const uint32_t v0 = static_cast<uint32_t>(bmask64 >> (i0 - e0)) & 1u;
       const uint32_t v1 = static_cast<uint32_t>(bmask64 >> (i1 - e0)) & 1u;
       const int rem = w1 - T0 - g;  // token T0 + g + 8j usable: 8j < rem
@@ -1102,9 +1109,10 @@ attention_merge_kernel(const AttnParams p) {
       make_uint4(packed[0], packed[1], packed[2], packed[3]);
 }
 
-template <int NG, bool kF16, bool kContig>
+template <int NG, bool kF16, int kPages>
 cudaError_t launch_mma(const AttnParams& caller, cudaStream_t stream) {
-  auto kernel = paged_attention_mma_kernel<NG, kF16, kContig>;
+  constexpr bool kContig = kPages != 0;
+  auto kernel = paged_attention_mma_kernel<NG, kF16, kPages>;
   // A CTA may cover a longer partition than the caller's (fewer, longer
   // warp ranges; the scratch rows keep the caller's max_parts stride and
   // need fewer entries).  A warp range must span at most 32 blocks.
@@ -1140,8 +1148,9 @@ template <int NG, bool kF16>
 cudaError_t launch_layout(const AttnParams& p, cudaStream_t stream) {
   const bool contig = p.dts == kD / 2 && p.sts == kD / 16 &&
                       p.B % 16 == 0 && !p.swizzle_k;
-  return contig ? launch_mma<NG, kF16, true>(p, stream)
-                : launch_mma<NG, kF16, false>(p, stream);
+  if (!contig) return launch_mma<NG, kF16, 0>(p, stream);
+  return p.B == 16 ? launch_mma<NG, kF16, 2>(p, stream)
+                   : launch_mma<NG, kF16, 1>(p, stream);
 }
 
 }  // namespace
