@@ -542,7 +542,9 @@ paged_attention_mma_kernel(const AttnParams p) {
 
   // Issue the copies of step i (tokens w0 + 32i ..) into its slots and
   // commit them as one group (an empty group past the last step).
-  auto issue = [&](int i) {
+  // kValid: every block id of the warp's range is valid (no test).
+  auto issue = [&](int i, auto valid_tag) {
+    constexpr bool kValid = decltype(valid_tag)::value;
     if (i >= nsteps) {
       // nothing to copy
     } else if constexpr (kContig) {
@@ -569,7 +571,7 @@ paged_attention_mma_kernel(const AttnParams p) {
         const uint8_t* kb = reinterpret_cast<const uint8_t*>(
             (static_cast<uint64_t>(hi) << 32) | lo);
         // one block holds the whole half: the branch is warp-uniform
-        bok[h] = (bmask64 >> e) & 1u;
+        bok[h] = kValid || ((bmask64 >> e) & 1u) != 0u;
         const int toff = kB16 ? 0 : (T - idx * p.B) * 64;
         sb[h] = kb + sdelta + (toff >> 3);
         const uint32_t kd = st + kKdOff + 2 * h * 512 + lane * 16;
@@ -673,7 +675,8 @@ paged_attention_mma_kernel(const AttnParams p) {
   // is made at all.
   auto step = [&](int i, auto masked_tag) {
     constexpr bool kMasked = decltype(masked_tag)::value;
-    issue(i + kDepth - 1);
+    // the unmasked steps run only when no block id of the range is bad
+    issue(i + kDepth - 1, std::integral_constant<bool, !kMasked>{});
     cp_async_wait<kDepth - 1>();
     const uint32_t st = wbase + (i % kDepth) * SL::kStage;
     const int T0 = w0 + kStep * i;
@@ -893,7 +896,7 @@ paged_attention_mma_kernel(const AttnParams p) {
   };
 
 #pragma unroll
-  for (int i = 0; i < kDepth - 1; ++i) issue(i);
+  for (int i = 0; i < kDepth - 1; ++i) issue(i, std::false_type{});
 #pragma unroll
   for (int n = 0; n < NB; ++n) {
     uint4 v = qv[n];
