@@ -368,7 +368,7 @@ constexpr float kLazy = 8.0f;
 // block_size 16, where (warp ranges starting at multiples of 32 tokens)
 // half h of a warp's step i is its block 2i + h, whole.
 template <int NG, bool kF16, int kPages>
-__global__ void __launch_bounds__(kThreads, NG == 8 ? 4 : 2)
+__global__ void __launch_bounds__(kThreads, NG == 8 ? 4 : 3)
 paged_attention_mma_kernel(const AttnParams p) {
   constexpr bool kContig = kPages != 0, kB16 = kPages == 2;
   constexpr int NB = NG / 8;  // n-blocks of 8 query heads
