@@ -597,7 +597,7 @@ def run_ours(args):
                  "Llama-3.1-70B-shaped attention: 200 sequences, 64 query / "
                  "8 KV heads, head_size 128, block_size 16, contexts 512 + "
                  "U[0, 2048]; partition_size 512 (on these contiguous "
-                 "pages a context splits into ceil(L / 1280) stretches in "
+                 "pages a context splits into ceil(L / 1792) stretches in "
                  "the proportions 4 : ... : 4 : 1, one CTA each, launched "
                  "stretch-major, then the partition merge); not part of "
                  "the step"),

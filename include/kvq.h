@@ -316,8 +316,8 @@ kvq_status kvq_store_indexer_k(const void* k, int64_t k_stride0,
  * is rounded to fp16, e2m1 * sf is exact in fp16, q . (e2m1 * sf) and
  * P . V' accumulate in fp32 on the tensor cores, P = exp2 of the scaled
  * logits minus a reference value of the stretch of context being
- * accumulated (a logit maximum; the default kernel moves it only when a
- * logit exceeds it by more than 8, so P < 2^8) is rounded to fp16 and the
+ * accumulated (a logit maximum; the kernel moves it only when a logit
+ * exceeds it by more than 8, so P < 2^8) is rounded to fp16 and the
  * denominator sums the rounded values; stretches merge in fp32 (rescaled
  * by exp2 of the difference of their references); out is rounded once.
  *
@@ -344,8 +344,7 @@ kvq_status kvq_store_indexer_k(const void* k, int64_t k_stride0,
  *                elements apart (multiple of 8), 16-byte aligned.
  * flags          KVQ_F_SWIZZLE_K_SCALE, KVQ_F_PDL, or 0.
  * dev_error      nullable (KVQ_DEVERR_BLOCK: the token is left out;
- *                KVQ_DEVERR_SEQ; KVQ_DEVERR_TIMEOUT: nothing of that
- *                (sequence, KV head, partition) is written).
+ *                KVQ_DEVERR_SEQ).
  * num_seqs == 0 returns KVQ_OK without launching.
  */
 kvq_status kvq_paged_attention_nvfp4(

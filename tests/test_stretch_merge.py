@@ -1,7 +1,7 @@
 """GPU tests of contexts split over several stretches and merged.
 
 On contiguous pages the attention kernel splits a context of more than one
-stretch (1280 tokens) into CTAs in the proportions 4 : ... : 4 : 1, each
+stretch (1792 tokens) into CTAs in the proportions 4 : ... : 4 : 1, each
 writing its partial result to the caller's scratch, and the partition-merge
 kernel combines them.  These tests run that path against the oracle over
 contexts of two to ten stretches, with scratch full of random bits, twice in
