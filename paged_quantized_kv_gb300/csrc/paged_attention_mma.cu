@@ -364,13 +364,17 @@ constexpr float kLazy = 8.0f;
 // kContig: HND pages with block_size % 16 == 0, so each 16 tokens of a
 // step lie in one block and their rows (and scale rows) are contiguous: one
 // block id and lane-constant offsets per 16 tokens.
-// kPages: 0 = other pages, 1 = contiguous, 2 = contiguous with
-// block_size 16, where (warp ranges starting at multiples of 32 tokens)
-// half h of a warp's step i is its block 2i + h, whole.
+// kPages: 0 = other pages; 1, 2 = contiguous (HND); 3, 4 = token rows
+// (NHD, block_size % 16 == 0, linear K scales: a head's 64-byte data rows
+// and 8-byte scale rows H rows apart, copied row by row into the same
+// shared-memory layout); 2 and 4 with block_size 16, where (warp ranges
+// starting at multiples of 32 tokens) half h of a warp's step i is its
+// block 2i + h, whole.
 template <int NG, bool kF16, int kPages>
 __global__ void __launch_bounds__(kThreads, NG == 8 ? 4 : 3)
 paged_attention_mma_kernel(const AttnParams p) {
-  constexpr bool kContig = kPages != 0, kB16 = kPages == 2;
+  constexpr bool kContig = kPages != 0, kB16 = kPages == 2 || kPages == 4;
+  constexpr bool kRows = kPages >= 3;
   constexpr int NB = NG / 8;  // n-blocks of 8 query heads
   using SL = Slots<kContig>;
   extern __shared__ __align__(16) uint8_t smem[];
@@ -533,6 +537,12 @@ paged_attention_mma_kernel(const AttnParams p) {
                   p.page_stride + kh * p.dhs;
   const int64_t vdelta = vside - kside;
   const int64_t sdelta = p.scale_off + kh * p.shs - kh * p.dhs;
+  // contiguous pages: bytes between the data (scale) rows of consecutive
+  // tokens of the head, and this lane's 16 bytes of the first 8 tokens'
+  // data rows (token lane / 4, chunk lane % 4; 16 lane on HND pages)
+  const int64_t dts = kRows ? p.dts : kD / 2;
+  const int64_t sts = kRows ? p.sts : kD / 16;
+  const int64_t lane_doff = (lane >> 2) * dts + (lane & 3) * 16;
   const int v_rd0 = vchunk(8 * t + (g >> 1)) * 16 + (g & 1) * 8;
   const int v_rd1 = vchunk(8 * t + 4 + (g >> 1)) * 16 + (g & 1) * 8;
   // contiguous pages: this lane's scale pairs (K: groups 2t, 2t+1 of token
@@ -572,17 +582,29 @@ paged_attention_mma_kernel(const AttnParams p) {
             (static_cast<uint64_t>(hi) << 32) | lo);
         // one block holds the whole half: the branch is warp-uniform
         bok[h] = kValid || ((bmask64 >> e) & 1u) != 0u;
-        const int toff = kB16 ? 0 : (T - idx * p.B) * 64;
-        sb[h] = kb + sdelta + (toff >> 3);
+        const int tok = kB16 ? 0 : T - idx * p.B;  // the half's first row
         const uint32_t kd = st + kKdOff + 2 * h * 512 + lane * 16;
         const uint32_t vd = st + kVdOff + 2 * h * 512 + v_dst;
+        // this lane's first K copy and the distance to its second (8
+        // tokens on); two forms of the same addresses on HND pages (the
+        // first measured faster with block_size 16, the second with 32)
+        const uint8_t* ka;
+        int64_t k8;
+        if constexpr (kRows || kB16) {
+          sb[h] = kb + sdelta + tok * sts;
+          ka = kb + tok * dts + lane_doff;
+          k8 = 8 * dts;
+        } else {
+          sb[h] = kb + sdelta + tok * (kD / 16);
+          ka = kb + tok * (kD / 2) + 16 * lane;
+          k8 = 512;
+        }
         if (bok[h]) {
-          const uint8_t* ka = kb + toff + 16 * lane;
           const uint8_t* va = ka + vdelta;
           cp_async<16>(kd, ka, true);
-          cp_async<16>(kd + 512, ka + 512, true);
+          cp_async<16>(kd + 512, ka + k8, true);
           cp_async<16>(vd, va, true);
-          cp_async<16>(vd + 512, va + 512, true);
+          cp_async<16>(vd + 512, va + k8, true);
         } else {
           cp_async<16>(kd, qz, false);
           cp_async<16>(kd + 512, qz, false);
@@ -590,13 +612,23 @@ paged_attention_mma_kernel(const AttnParams p) {
           cp_async<16>(vd + 512, qz, false);
         }
       }
-      // the step's scales: lanes 16h .. 16h+15 take half h, the first 8 of
-      // them its K scale rows, the other 8 its V scale bands
+      // the step's scales: lanes 16h .. 16h+15 take half h
       const int sh = lane >> 4;
       const bool sok = sh ? bok[1] : bok[0];
-      const uint8_t* so = (sh ? sb[1] : sb[0]) + 16 * (lane & 7) +
-                          ((lane & 8) ? vdelta : 0);
-      cp_async<16>(st + kKsOff + lane * 16, sok ? so : qz, sok);
+      const uint8_t* const sbh = sh ? sb[1] : sb[0];
+      if constexpr (kRows) {
+        // scale row lane % 16 of the half: the K row of its token and V
+        // row lane % 16 (4-token band lane % 16 / 4), 8 bytes each
+        const uint8_t* so = sbh + (lane & 15) * sts;
+        const uint32_t sd = st + kKsOff + 256 * sh + 8 * (lane & 15);
+        cp_async<8>(sd, sok ? so : qz, sok);
+        cp_async<8>(sd + 128, sok ? so + vdelta : qz, sok);
+      } else {
+        // the first 8 lanes the half's K scale rows, the other 8 its V
+        // scale bands, 16 contiguous bytes each
+        const uint8_t* so = sbh + 16 * (lane & 7) + ((lane & 8) ? vdelta : 0);
+        cp_async<16>(st + kKsOff + lane * 16, sok ? so : qz, sok);
+      }
     } else {
       const uint32_t st = wbase + (i % kDepth) * SL::kStage;
       const int T0 = w0 + kStep * i;
@@ -1151,9 +1183,17 @@ template <int NG, bool kF16>
 cudaError_t launch_layout(const AttnParams& p, cudaStream_t stream) {
   const bool contig = p.dts == kD / 2 && p.sts == kD / 16 &&
                       p.B % 16 == 0 && !p.swizzle_k;
-  if (!contig) return launch_mma<NG, kF16, 0>(p, stream);
-  return p.B == 16 ? launch_mma<NG, kF16, 2>(p, stream)
-                   : launch_mma<NG, kF16, 1>(p, stream);
+  // token rows: NHD pages (a head's rows H rows apart)
+  const bool rows = p.dhs == kD / 2 && p.dts == p.Hkv * (kD / 2) &&
+                    p.shs == kD / 16 && p.sts == p.Hkv * (kD / 16) &&
+                    p.B % 16 == 0 && !p.swizzle_k;
+  if (contig)
+    return p.B == 16 ? launch_mma<NG, kF16, 2>(p, stream)
+                     : launch_mma<NG, kF16, 1>(p, stream);
+  if (rows)
+    return p.B == 16 ? launch_mma<NG, kF16, 4>(p, stream)
+                     : launch_mma<NG, kF16, 3>(p, stream);
+  return launch_mma<NG, kF16, 0>(p, stream);
 }
 
 }  // namespace

@@ -17,6 +17,7 @@ import torch
 from paged_quantized_kv_gb300 import kvq
 from paged_quantized_kv_gb300 import workloads as W
 from tests.gpu_helpers import to_dev
+from tests.test_oracle_attention import _nhd
 from tests.test_parity_attention import (_upload, _vmax, assert_close,
                                          oracle_attention)
 
@@ -122,21 +123,26 @@ def test_merge_matches_across_partition_sizes(orc):
     assert np.array_equal(outs[0], outs[2])
 
 
+@pytest.mark.parametrize("layout", [W.LAYOUT_HND, W.LAYOUT_NHD])
 @pytest.mark.parametrize("B", [16, 32, 48])
-def test_stretch_boundaries(orc, B):
+def test_stretch_boundaries(orc, B, layout):
     """Contexts at the stretch length (1792) and at twice it, one token
     either side: the first of two stretches then holds up to 2848 tokens,
     a warp range up to 46 blocks of 16 (the block ids of its second 32
-    blocks come from each lane's second entry)."""
-    wl = W.make_attention(f"edge{B}", 115, [1792, 1793, 3584, 3585, 2000],
-                          num_q_heads=8, num_kv_heads=1, head_size=128,
-                          block_size=B)
+    blocks come from each lane's second entry); HND pages and NHD ones
+    (with 2 KV heads, so that a head's token rows are 2 rows apart)."""
+    wl = W.make_attention(f"edge{B}_{layout}", 115,
+                          [1792, 1793, 3584, 3585, 2000], num_q_heads=16,
+                          num_kv_heads=2, head_size=128, block_size=B)
+    if layout == W.LAYOUT_NHD:
+        wl = _nhd(wl)
     c = Call(wl, 512, seed=B)
     c()
-    c.check(orc, what=f"stretch edges B={B}")
+    c.check(orc, what=f"stretch edges B={B} layout={layout}")
 
 
-def test_bad_blocks_in_long_ranges(orc):
+@pytest.mark.parametrize("layout", [W.LAYOUT_HND, W.LAYOUT_NHD])
+def test_bad_blocks_in_long_ranges(orc, layout):
     """Out-of-range block ids among the second 32 blocks of a warp's range
     (contexts of 3584 and 3000 tokens: warp ranges of 736 and 608 tokens,
     46 and 38 blocks) and among the first 32 (2100 tokens): flagged, and
@@ -146,6 +152,8 @@ def test_bad_blocks_in_long_ranges(orc):
     wl = W.make_attention("longbad", 116, [3584, 3000, 2100],
                           num_q_heads=8, num_kv_heads=1, head_size=128,
                           block_size=B)
+    if layout == W.LAYOUT_NHD:
+        wl = _nhd(wl)
     drop = {0: 40, 1: 73, 2: 33}         # sequence -> block made bad
     wl.block_table[0, 40] = -3
     wl.block_table[1, 73] = wl.num_blocks
