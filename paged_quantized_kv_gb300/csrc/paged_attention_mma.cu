@@ -365,16 +365,19 @@ constexpr float kLazy = 8.0f;
 // step lie in one block and their rows (and scale rows) are contiguous: one
 // block id and lane-constant offsets per 16 tokens.
 // kPages: 0 = other pages; 1, 2 = contiguous (HND); 3, 4 = token rows
-// (NHD, block_size % 16 == 0, linear K scales: a head's 64-byte data rows
-// and 8-byte scale rows H rows apart, copied row by row into the same
-// shared-memory layout); 2 and 4 with block_size 16, where (warp ranges
-// starting at multiples of 32 tokens) half h of a warp's step i is its
-// block 2i + h, whole.
+// (NHD, block_size % 16 == 0: a head's 64-byte data rows and 8-byte scale
+// rows H rows apart, copied row by row into the same shared-memory
+// layout); 2 and 4 with block_size 16, where (warp ranges starting at
+// multiples of 32 tokens) half h of a warp's step i is its block 2i + h,
+// whole; 5 .. 8 = 1 .. 4 with the K scales swizzled like the V scales
+// (the same bytes copied, read as bands).
 template <int NG, bool kF16, int kPages>
 __global__ void __launch_bounds__(kThreads, NG == 8 ? 4 : 3)
 paged_attention_mma_kernel(const AttnParams p) {
-  constexpr bool kContig = kPages != 0, kB16 = kPages == 2 || kPages == 4;
-  constexpr bool kRows = kPages >= 3;
+  constexpr bool kSwzK = kPages >= 5;
+  constexpr int kForm = kSwzK ? kPages - 4 : kPages;
+  constexpr bool kContig = kForm != 0, kB16 = kForm == 2 || kForm == 4;
+  constexpr bool kRows = kForm >= 3;
   constexpr int NB = NG / 8;  // n-blocks of 8 query heads
   using SL = Slots<kContig>;
   extern __shared__ __align__(16) uint8_t smem[];
@@ -548,6 +551,7 @@ paged_attention_mma_kernel(const AttnParams p) {
   // contiguous pages: this lane's scale pairs (K: groups 2t, 2t+1 of token
   // g's row; V: tokens 2t, 2t+1 of group g in their 4-token band)
   const int ks_rd16 = g * 8 + 2 * t;
+  const int ks_rd64 = (g >> 2) * 32 + 8 * t;  // K scales swizzled
   const int vs_rd16 = 128 + 32 * (t >> 1) + 4 * g + 2 * (t & 1);
 
   // Issue the copies of step i (tokens w0 + 32i ..) into its slots and
@@ -555,6 +559,7 @@ paged_attention_mma_kernel(const AttnParams p) {
   // kValid: every block id of the warp's range is valid (no test).
   auto issue = [&](int i, auto valid_tag) {
     constexpr bool kValid = decltype(valid_tag)::value;
+    static_cast<void>(kValid);  // (only the contiguous forms test it)
     if (i >= nsteps) {
       // nothing to copy
     } else if constexpr (kContig) {
@@ -743,7 +748,12 @@ paged_attention_mma_kernel(const AttnParams p) {
         const int j = 2 * h + r;
         kd[r] = lds128(st + kKdOff + j * 512 + lane * 16);
         uint16_t pair;
-        if constexpr (kContig) {
+        if constexpr (kContig && kSwzK) {
+          // band (2r + g / 4), row t: scales 2t, 2t+1 of token 8r + g at
+          // bytes g % 4 and 4 + g % 4
+          const uint2 ks = lds64(st + kKsOff + 256 * h + 64 * r + ks_rd64);
+          pair = static_cast<uint16_t>(prmt(ks.x, ks.y, ksel));
+        } else if constexpr (kContig) {
           pair = lds16(st + kKsOff + 256 * h + 64 * r + ks_rd16);
         } else {
           const uint2 ks = lds64(st + kKsOff + j * 256 + lane * 8);
@@ -1150,7 +1160,8 @@ cudaError_t launch_mma(const AttnParams& caller, cudaStream_t stream) {
   auto kernel = paged_attention_mma_kernel<NG, kF16, kPages>;
   // A CTA may cover a longer partition than the caller's (fewer, longer
   // warp ranges; the scratch rows keep the caller's max_parts stride and
-  // need fewer entries).  A warp range must span at most 32 blocks.
+  // need fewer entries).  A warp range spans at most 64 blocks on
+  // contiguous pages, 32 elsewhere.
   AttnParams p = caller;
   // (the caller's partitions are at most 512 tokens)
   if (kContig) p.part = KVQ_ATTN_MMA_PART;
@@ -1179,21 +1190,26 @@ cudaError_t launch_mma(const AttnParams& caller, cudaStream_t stream) {
   return launch_attention_merge(p, stream);
 }
 
-template <int NG, bool kF16>
-cudaError_t launch_layout(const AttnParams& p, cudaStream_t stream) {
-  const bool contig = p.dts == kD / 2 && p.sts == kD / 16 &&
-                      p.B % 16 == 0 && !p.swizzle_k;
+template <int NG, bool kF16, int kSwz>
+cudaError_t launch_form(const AttnParams& p, cudaStream_t stream) {
+  const bool contig = p.dts == kD / 2 && p.sts == kD / 16 && p.B % 16 == 0;
   // token rows: NHD pages (a head's rows H rows apart)
   const bool rows = p.dhs == kD / 2 && p.dts == p.Hkv * (kD / 2) &&
                     p.shs == kD / 16 && p.sts == p.Hkv * (kD / 16) &&
-                    p.B % 16 == 0 && !p.swizzle_k;
+                    p.B % 16 == 0;
   if (contig)
-    return p.B == 16 ? launch_mma<NG, kF16, 2>(p, stream)
-                     : launch_mma<NG, kF16, 1>(p, stream);
+    return p.B == 16 ? launch_mma<NG, kF16, 2 + kSwz>(p, stream)
+                     : launch_mma<NG, kF16, 1 + kSwz>(p, stream);
   if (rows)
-    return p.B == 16 ? launch_mma<NG, kF16, 4>(p, stream)
-                     : launch_mma<NG, kF16, 3>(p, stream);
+    return p.B == 16 ? launch_mma<NG, kF16, 4 + kSwz>(p, stream)
+                     : launch_mma<NG, kF16, 3 + kSwz>(p, stream);
   return launch_mma<NG, kF16, 0>(p, stream);
+}
+
+template <int NG, bool kF16>
+cudaError_t launch_layout(const AttnParams& p, cudaStream_t stream) {
+  return p.swizzle_k ? launch_form<NG, kF16, 4>(p, stream)
+                     : launch_form<NG, kF16, 0>(p, stream);
 }
 
 }  // namespace

@@ -56,7 +56,7 @@ class Call:
         kvq.kvq_paged_attention_nvfp4(
             self.q, kc, vc, self.bt, self.lens, self.ks, self.vs,
             float(self.wl.scale), self.out, self.mcl, self.part, es, ml, tmp,
-            flags=flags)
+            flags=flags | self.wl.flags)
 
     def result(self):
         torch.cuda.synchronize()
@@ -123,22 +123,25 @@ def test_merge_matches_across_partition_sizes(orc):
     assert np.array_equal(outs[0], outs[2])
 
 
+@pytest.mark.parametrize("swz", [0, 1])
 @pytest.mark.parametrize("layout", [W.LAYOUT_HND, W.LAYOUT_NHD])
 @pytest.mark.parametrize("B", [16, 32, 48])
-def test_stretch_boundaries(orc, B, layout):
+def test_stretch_boundaries(orc, B, layout, swz):
     """Contexts at the stretch length (1792) and at twice it, one token
     either side: the first of two stretches then holds up to 2848 tokens,
     a warp range up to 46 blocks of 16 (the block ids of its second 32
     blocks come from each lane's second entry); HND pages and NHD ones
-    (with 2 KV heads, so that a head's token rows are 2 rows apart)."""
-    wl = W.make_attention(f"edge{B}_{layout}", 115,
+    (with 2 KV heads, so that a head's token rows are 2 rows apart), K
+    scales linear and swizzled."""
+    wl = W.make_attention(f"edge{B}_{layout}_{swz}", 115,
                           [1792, 1793, 3584, 3585, 2000], num_q_heads=16,
-                          num_kv_heads=2, head_size=128, block_size=B)
+                          num_kv_heads=2, head_size=128, block_size=B,
+                          flags=swz)
     if layout == W.LAYOUT_NHD:
         wl = _nhd(wl)
     c = Call(wl, 512, seed=B)
     c()
-    c.check(orc, what=f"stretch edges B={B} layout={layout}")
+    c.check(orc, what=f"stretch edges B={B} layout={layout} swz={swz}")
 
 
 @pytest.mark.parametrize("layout", [W.LAYOUT_HND, W.LAYOUT_NHD])
