@@ -24,13 +24,15 @@
 // per SM with its operands already in registers and needs no handshake.
 // Two tcgen05 designs of this operation (one CTA per partition with the
 // logits held in tensor memory; a persistent warp-specialised one) measured
-// 0.25 and 0.11 of the HBM roofline against this kernel's 0.66 on the
-// Llama-70B-shaped step, and 0.20 / 0.10 against 0.39 with 16 query heads
-// per KV head, so they were retired.
+// 0.25 and 0.11 of the HBM roofline against this kernel's 0.66 (0.78 now)
+// on the Llama-70B-shaped step, and 0.20 / 0.10 against 0.39 (0.45 now)
+// with 16 query heads per KV head, so they were retired.
 //
 // Design, per CTA of 4 warps = one (stretch of context, KV head, sequence):
-// on contiguous pages (HND, block_size % 16 == 0, linear K scales) a
-// context of L tokens is split into n = ceil(L / KVQ_ATTN_MMA_PART)
+// on contiguous pages (block_size % 16 == 0: HND, whose 16-token halves
+// are contiguous, or NHD, whose token rows are copied row by row; K scales
+// linear or swizzled) a context of L tokens is split into
+// n = ceil(L / KVQ_ATTN_MMA_PART)
 // stretches (KVQ_ATTN_MMA_PART = 1792; boundaries at multiples of 32
 // tokens) in the proportions 4 : ... : 4 : 1, elsewhere into the caller's
 // partitions (<= 512 tokens); the CTAs are launched stretch-major (every
@@ -42,11 +44,11 @@
 //     ahead; the warp waits with cp.async.wait_group only.  Block ids of the
 //     warp's range are loaded once (one or two per lane) and shuffled.  On
 //     contiguous pages one block id serves 16 tokens and the pages' bytes
-//     keep their order (16-byte copies, a step's scales in one copy per
-//     lane; a bad block id zero-filled); elsewhere every thread copies
-//     exactly the bytes its own MMA fragments need, zero-filled for tokens
-//     past the context or with a bad block id.  The query fragments are
-//     staged in shared memory once per CTA.
+//     keep their order (16-byte copies, a step's scales in one or two
+//     copies per lane; a bad block id zero-filled); elsewhere every thread
+//     copies exactly the bytes its own MMA fragments need, zero-filled for
+//     tokens past the context or with a bad block id.  The query fragments
+//     are staged in shared memory once per CTA.
 //   * Logits S^T[16 tokens x 8 heads] = K' Q'^T per n-block of 8 query
 //     heads: A = K' (rows = tokens), B = Q'^T (k = head dims).  The head
 //     dims are permuted (the same way for K and Q): in k-step s, lane
