@@ -21,6 +21,7 @@ scaling, the slowest rank's time counts.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import os
@@ -489,6 +490,12 @@ def run_ours(args):
     attn_bytes = aw.algorithmic_bytes()
     attn_ctx = int(aw.context_lens.astype(np.int64).sum())
     del attn
+    # the same step on NHD pages (the same bytes read in that layout)
+    attn = attention_inputs(
+        dataclasses.replace(aw, layout=wlmod.LAYOUT_NHD), kvq, dev)
+    attn_nhd_st = tm.stats(
+        lambda i: run_attention(attn, kvq, PDL, dev_err, sh), 25)
+    del attn
     # keep the same steps running so the clock sampler sees the load
     t1 = time.perf_counter()
     j = 0
@@ -601,6 +608,12 @@ def run_ours(args):
                  "the proportions 4 : ... : 4 : 1, one CTA each, launched "
                  "stretch-major, then the partition merge); not part of "
                  "the step"),
+        "paged_attention_nvfp4_nhd": dict(
+            leg(attn_nhd_st, attn_bytes, peak, aw.num_seqs,
+                "decode_tokens_per_s"),
+            note="the same attention step on NHD pages (block_size 16: a "
+                 "head's token rows 8 rows apart, copied row by row); not "
+                 "part of the step"),
         "configs": configs,
         "roofline": {
             "bound": "hbm",
@@ -781,7 +794,7 @@ def attention_inputs(aw, kvq, dev):
     import torch
     kv, kc, vc = kvq.alloc_nvfp4_cache(aw.num_blocks, aw.block_size,
                                        aw.num_kv_heads, aw.head_size,
-                                       device=dev)
+                                       aw.layout, device=dev)
     kv.view(-1).copy_(torch.from_numpy(aw.cache))
     q = torch.from_numpy(aw.query.view(np.int16)).to(dev).view(torch.bfloat16)
     mcl = int(aw.context_lens.max())
