@@ -88,12 +88,13 @@ enum {
      PDL-launched kernel to do the same.  Useful when these calls run back
      to back with other kernels on one stream. */
   KVQ_F_PDL = 1u << 1,
-  /* kvq_gather_indexer_k and kvq_load_nvfp4; implies KVQ_F_PDL.  The caller
-     promises that
-     block_table and cu_seq_lens are not written by the kernel that runs
-     just before this call on the stream (they are ready before it starts),
-     so the kernel stages them while that kernel finishes and waits only
-     before it reads the cache or the scales, or writes anything. */
+  /* kvq_gather_indexer_k, kvq_load_nvfp4 and kvq_paged_attention_nvfp4;
+     implies KVQ_F_PDL.  The caller promises that block_table and
+     cu_seq_lens (attention: query, block_table, context_lens, k_scale and
+     v_scale) are not written by the kernel that runs just before this call
+     on the stream (they are ready before it starts), so the kernel stages
+     them while that kernel finishes and waits only before it reads the
+     cache or the scales (attention: the pages), or writes anything. */
   KVQ_F_PDL_EARLY_META = 1u << 2,
   /* kvq_gather_indexer_k (implies KVQ_F_PDL_EARLY_META), kvq_store_nvfp4
      and kvq_store_indexer_k (imply KVQ_F_PDL).  The caller promises that the
@@ -342,7 +343,9 @@ kvq_status kvq_store_indexer_k(const void* k, int64_t k_stride0,
  *                be initialised; their contents afterwards are unspecified.
  * out            dtype [num_seqs, num_q_heads, 128], rows out_stride0
  *                elements apart (multiple of 8), 16-byte aligned.
- * flags          KVQ_F_SWIZZLE_K_SCALE, KVQ_F_PDL, or 0.
+ * flags          KVQ_F_SWIZZLE_K_SCALE, KVQ_F_PDL, KVQ_F_PDL_EARLY_META
+ *                (e.g. after kvq_store_nvfp4, which writes only the pages),
+ *                or 0.
  * dev_error      nullable (KVQ_DEVERR_BLOCK: the token is left out;
  *                KVQ_DEVERR_SEQ).
  * num_seqs == 0 returns KVQ_OK without launching.

@@ -59,8 +59,8 @@ kvq_status attention_check(
   if (dtype != KVQ_DTYPE_BF16 && dtype != KVQ_DTYPE_FP16) return KVQ_ERR_DTYPE;
   if (layout != KVQ_LAYOUT_HND && layout != KVQ_LAYOUT_NHD)
     return KVQ_ERR_LAYOUT;
-  if ((flags & ~static_cast<uint32_t>(KVQ_F_SWIZZLE_K_SCALE | KVQ_F_PDL)) !=
-      0u)
+  if ((flags & ~static_cast<uint32_t>(KVQ_F_SWIZZLE_K_SCALE | KVQ_F_PDL |
+                                     KVQ_F_PDL_EARLY_META)) != 0u)
     return KVQ_ERR_ARG;
   if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 ||
       head_size <= 0 || block_size <= 0 || num_blocks < 0 ||
@@ -481,7 +481,8 @@ kvq_status kvq_paged_attention_nvfp4(
   p.len_cap = static_cast<int32_t>(std::min<int64_t>(cap, INT32_MAX));
   p.swizzle_k = (flags & KVQ_F_SWIZZLE_K_SCALE) != 0u;
   p.f16 = dtype == KVQ_DTYPE_FP16;
-  p.pdl = (flags & KVQ_F_PDL) != 0u;
+  p.early_meta = (flags & KVQ_F_PDL_EARLY_META) != 0u;
+  p.pdl = p.early_meta || (flags & KVQ_F_PDL) != 0u;
   const cudaError_t err =
       launch_paged_attention_mma(p, static_cast<cudaStream_t>(stream));
   return err == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;

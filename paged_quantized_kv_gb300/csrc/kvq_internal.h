@@ -143,6 +143,7 @@ struct AttnParams {
   bool swizzle_k;          // K scales stored swizzled too
   bool f16;                // query / out are fp16 (else bf16)
   bool pdl;
+  bool early_meta;         // lengths, block ids, query read before the wait
 };
 
 cudaError_t launch_paged_attention_mma(const AttnParams& p,

@@ -390,18 +390,30 @@ paged_attention_mma_kernel(const AttnParams p) {
   const int kh = static_cast<int>(blockIdx.x % p.Hkv);
   const int sb = static_cast<int>(blockIdx.x / p.Hkv);
   const int b = sb % p.num_seqs, part = sb / p.num_seqs;
-  pdl_prologue();
+  // PDL: wait for the kernel before here, or -- when the caller promised
+  // that it writes none of the query, block table, context lengths and
+  // scales (KVQ_F_PDL_EARLY_META) -- only before the first read of the
+  // pages and the first write, so that the lengths, block ids and query
+  // load while it finishes
+  const bool early = p.early_meta;
+  if (!early) asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   int L = __ldg(p.lens + b);
-  if (L < 0 || L > p.len_cap) {
-    if (p.dev_error != nullptr && part == 0 && kh == 0 && tid == 0)
+  const bool bad_len = L < 0 || L > p.len_cap;
+  if (bad_len) L = L < 0 ? 0 : p.len_cap;
+  // flags a clamped length (once per sequence); a write, so after the wait
+  auto flag_len = [&]() {
+    if (bad_len && p.dev_error != nullptr && part == 0 && kh == 0 &&
+        tid == 0)
       atomicOr(p.dev_error, KVQ_DEVERR_SEQ);
-    L = L < 0 ? 0 : p.len_cap;
-  }
+  };
   // stretch length: fixed on contiguous pages (the host sets p.part to it)
   const int S = kContig ? KVQ_ATTN_MMA_PART : p.part;
   const int nparts = (L + S - 1) / S;
   if (part >= nparts) {
+    if (early) asm volatile("griddepcontrol.wait;" ::: "memory");
+    flag_len();
     if (part == 0) {  // empty context: the output is zero
       for (int i = tid; i < p.G * kD; i += kThreads)
         p.out[b * p.out_stride0 + (kh * p.G) * kD + i] = 0;
@@ -479,6 +491,8 @@ paged_attention_mma_kernel(const AttnParams p) {
           8 * warp));
   }
   const float v_scale_in = tid == 0 ? __ldg(p.v_scale) : 0.f;
+  if (early) asm volatile("griddepcontrol.wait;" ::: "memory");
+  flag_len();
 
   const uint32_t wbase = smem_u32(smem) + warp * SL::kWarp;
   const uint8_t* const kside = p.side[0];

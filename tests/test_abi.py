@@ -226,7 +226,8 @@ def attn(lib, **kw):
 @pytest.mark.parametrize("kw,code", [
     (dict(dtype=2), kvq.KVQ_ERR_DTYPE),
     (dict(layout=2), kvq.KVQ_ERR_LAYOUT),
-    (dict(flags=4), kvq.KVQ_ERR_ARG),
+    (dict(flags=8), kvq.KVQ_ERR_ARG),
+    (dict(flags=16), kvq.KVQ_ERR_ARG),
     (dict(scale=float("nan")), kvq.KVQ_ERR_ARG),
     (dict(scale=float("inf")), kvq.KVQ_ERR_ARG),
     (dict(head_size=64), kvq.KVQ_ERR_SHAPE),

@@ -179,7 +179,7 @@ def test_store_then_attention(orc):
     """Pages written by the GPU store from bf16 K/V (scales as a checkpoint
     would give), read by the attention, against the oracle on the same
     bytes; also as a PDL chain in which the attention reads what the store
-    just wrote."""
+    just wrote, with and without early metadata reads."""
     swl = W.make_store("sa", 70, num_tokens=3 * 512, num_heads=2,
                        head_size=128, block_size=16, num_blocks=200,
                        slots="runs", request_len=512)
@@ -193,12 +193,15 @@ def test_store_then_attention(orc):
     q_bits = W.bf16_bits(qf.reshape(-1)).reshape(qf.shape)
     q = torch.from_numpy(q_bits.view(np.int16)).cuda().view(torch.bfloat16)
     outs = []
-    for flags in (0, kvq.KVQ_F_PDL):
+    bt_d, lens_d = to_dev(bt), to_dev(lens)
+    for flags in (0, kvq.KVQ_F_PDL, kvq.KVQ_F_PDL_EARLY_META):
         out = torch.empty_like(q)
-        kvq.kvq_store_nvfp4(key, value, kc, vc, slots, ks, vs, flags=flags)
+        kvq.kvq_store_nvfp4(key, value, kc, vc, slots, ks, vs,
+                            flags=flags & kvq.KVQ_F_PDL)
+        # the store writes only the pages: the attention may read its
+        # lengths, block ids and query before it finishes
         kvq.kvq_paged_attention_nvfp4(
-            q, kc, vc, to_dev(bt), to_dev(lens), ks, vs, 0.088, out, 512,
-            flags=flags)
+            q, kc, vc, bt_d, lens_d, ks, vs, 0.088, out, 512, flags=flags)
         torch.cuda.synchronize()
         outs.append(out.float().cpu().numpy().astype(np.float64))
         kv.zero_()
@@ -215,6 +218,7 @@ def test_store_then_attention(orc):
     for got in outs:
         assert_close(got, ref, mag, vmax, "store->attention")
     assert np.array_equal(outs[0], outs[1])
+    assert np.array_equal(outs[0], outs[2])
 
 
 def test_llama70b_decode_batch_sampled(orc):

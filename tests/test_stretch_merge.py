@@ -181,3 +181,27 @@ def test_bad_blocks_in_long_ranges(orc, layout):
     ref_wl = dataclasses.replace(wl, block_table=bt, context_lens=lens)
     ref, mag = oracle_attention(orc, ref_wl)
     assert_close(got, ref, mag, _vmax(ref_wl, lens), "bad blocks, long")
+
+
+def test_early_metadata_back_to_back(orc):
+    """Calls with KVQ_F_PDL_EARLY_META back to back on one stream (each
+    after the previous call's merge kernel, which writes only the output):
+    the lengths, block ids and query are read before the wait, the pages
+    and every write after it; both results equal the plain call's and the
+    oracle's."""
+    wl = W.make_attention("early", 117, [3000, 77, 1800, 2600, 0, 1],
+                          num_q_heads=16, num_kv_heads=2, head_size=128,
+                          block_size=16)
+    c = Call(wl, 512, seed=11)
+    c(flags=0)
+    plain = c.result()
+    outs = []
+    for _ in range(3):
+        c.out.fill_(float("nan"))
+        torch.cuda.synchronize()
+        c(flags=kvq.KVQ_F_PDL_EARLY_META)
+        c(flags=kvq.KVQ_F_PDL_EARLY_META)
+        outs.append(c.result())
+    c.check(orc, what="early metadata")
+    for o in outs:
+        assert np.array_equal(o, plain)
