@@ -76,11 +76,16 @@
 //   * A step none of whose tokens is left out (all in the warp's range,
 //     every block id valid -- every step but a partial last one) runs a
 //     form with no per-token test at all.
-//   * The 4 warps' (max, sum, O) merge in shared memory; a stretch of a
-//     longer context is written to the caller's scratch (rows max_parts
-//     apart, as for the caller's partitions: a stretch covers at least one
-//     partition, so fewer rows are used) and merged by the partition-merge
-//     kernel.
+//   * The 4 warps' (max, sum, O) merge in shared memory (each warp writes
+//     its own into its copy slots, one barrier, every output thread
+//     combines the four for its head); a stretch of a longer context is
+//     written to the caller's scratch (rows max_parts apart, as for the
+//     caller's partitions: a stretch covers at least one partition, so
+//     fewer rows are used) and merged by the partition-merge kernel.
+//   * Start-up: the query loads go out with the block-id loads and are
+//     staged once the first step's copies are issued; with
+//     KVQ_F_PDL_EARLY_META the context length, block ids, query and scales
+//     are read before the PDL wait.
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdint.h>
