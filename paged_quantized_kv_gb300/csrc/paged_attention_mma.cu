@@ -29,9 +29,9 @@
 // with 16 query heads per KV head, so they were retired.
 //
 // Design, per CTA of 4 warps = one (stretch of context, KV head, sequence):
-// on contiguous pages (block_size % 16 == 0: HND, whose 16-token halves
-// are contiguous, or NHD, whose token rows are copied row by row; K scales
-// linear or swizzled) a context of L tokens is split into
+// on contiguous pages (a power-of-two block_size >= 16: HND, whose 16-token
+// halves are contiguous, or NHD, whose token rows are copied row by row; K
+// scales linear or swizzled) a context of L tokens is split into
 // n = ceil(L / KVQ_ATTN_MMA_PART)
 // stretches (KVQ_ATTN_MMA_PART = 1792; boundaries at multiples of 32
 // tokens) in the proportions 4 : ... : 4 : 1, elsewhere into the caller's
@@ -371,10 +371,10 @@ constexpr float kLazy = 8.0f;
 // kContig: HND pages with block_size % 16 == 0, so each 16 tokens of a
 // step lie in one block and their rows (and scale rows) are contiguous: one
 // block id and lane-constant offsets per 16 tokens.
-// kPages: 0 = other pages; 1, 2 = contiguous (HND); 3, 4 = token rows
-// (NHD, block_size % 16 == 0: a head's 64-byte data rows and 8-byte scale
-// rows H rows apart, copied row by row into the same shared-memory
-// layout); 2 and 4 with block_size 16, where (warp ranges starting at
+// kPages: 0 = other pages; 1, 2 = contiguous (HND, a power-of-two
+// block_size >= 16); 3, 4 = token rows (NHD, the same block sizes: a
+// head's 64-byte data rows and 8-byte scale rows H rows apart, copied row
+// by row into the same shared-memory layout); 2 and 4 with block_size 16, where (warp ranges starting at
 // multiples of 32 tokens) half h of a warp's step i is its block 2i + h,
 // whole; 5 .. 8 = 1 .. 4 with the K scales swizzled like the V scales
 // (the same bytes copied, read as bands).
@@ -595,8 +595,8 @@ paged_attention_mma_kernel(const AttnParams p) {
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         const int T = w0 + kStep * i + 16 * h;
-        const int idx = kB16 ? e0 + 2 * i + h
-                        : p.b_shift >= 0 ? (T >> p.b_shift) : T / p.B;
+        // (contiguous pages have a power-of-two block size)
+        const int idx = kB16 ? e0 + 2 * i + h : T >> p.b_shift;
         const int e = idx - e0;  // 0 .. 63, warp-uniform
         const uint64_t kl =
             reinterpret_cast<uint64_t>(e < 32 ? kb_lane : kb_hi);
@@ -608,7 +608,7 @@ paged_attention_mma_kernel(const AttnParams p) {
             (static_cast<uint64_t>(hi) << 32) | lo);
         // one block holds the whole half: the branch is warp-uniform
         bok[h] = kValid || ((bmask64 >> e) & 1u) != 0u;
-        const int tok = kB16 ? 0 : T - idx * p.B;  // the half's first row
+        const int tok = kB16 ? 0 : T & (p.B - 1);  // the half's first row
         const uint32_t kd = st + kKdOff + 2 * h * 512 + lane * 16;
         const uint32_t vd = st + kVdOff + 2 * h * 512 + v_dst;
         // this lane's first K copy and the distance to its second (8
@@ -747,11 +747,8 @@ paged_attention_mma_kernel(const AttnParams p) {
     uint32_t kvalid = 0xFu;  // bit j: K token T0 + g + 8j is usable
     if constexpr (kMasked && kContig) {
       // each 16-token half lies in one block
-      const int i0 = kB16 ? e0 + 2 * i
-                     : p.b_shift >= 0 ? (T0 >> p.b_shift) : T0 / p.B;
-      const int i1 = kB16 ? i0 + 1
-                     : p.b_shift >= 0 ? ((T0 + 16) >> p.b_shift)
-                                      : (T0 + 16) / p.B;
+      const int i0 = kB16 ? e0 + 2 * i : T0 >> p.b_shift;
+      const int i1 = kB16 ? i0 + 1 : (T0 + 16) >> p.b_shift;
       const uint32_t v0 = static_cast<uint32_t>(bmask64 >> (i0 - e0)) & 1u;
       const uint32_t v1 = static_cast<uint32_t>(bmask64 >> (i1 - e0)) & 1u;
       const int rem = w1 - T0 - g;  // token T0 + g + 8j usable: 8j < rem
@@ -1213,11 +1210,13 @@ cudaError_t launch_mma(const AttnParams& caller, cudaStream_t stream) {
 
 template <int NG, bool kF16, int kSwz>
 cudaError_t launch_form(const AttnParams& p, cudaStream_t stream) {
-  const bool contig = p.dts == kD / 2 && p.sts == kD / 16 && p.B % 16 == 0;
+  // block sizes: powers of two from 16 up (block index and offset by
+  // shifts and masks); others take the per-fragment path
+  const bool pow2 = p.B >= 16 && p.b_shift >= 0;
+  const bool contig = p.dts == kD / 2 && p.sts == kD / 16 && pow2;
   // token rows: NHD pages (a head's rows H rows apart)
   const bool rows = p.dhs == kD / 2 && p.dts == p.Hkv * (kD / 2) &&
-                    p.shs == kD / 16 && p.sts == p.Hkv * (kD / 16) &&
-                    p.B % 16 == 0;
+                    p.shs == kD / 16 && p.sts == p.Hkv * (kD / 16) && pow2;
   if (contig)
     return p.B == 16 ? launch_mma<NG, kF16, 2 + kSwz>(p, stream)
                      : launch_mma<NG, kF16, 1 + kSwz>(p, stream);

@@ -132,7 +132,8 @@ def test_stretch_boundaries(orc, B, layout, swz):
     a warp range up to 46 blocks of 16 (the block ids of its second 32
     blocks come from each lane's second entry); HND pages and NHD ones
     (with 2 KV heads, so that a head's token rows are 2 rows apart), K
-    scales linear and swizzled."""
+    scales linear and swizzled; block size 48 takes the per-fragment path
+    with the caller's partitions."""
     wl = W.make_attention(f"edge{B}_{layout}_{swz}", 115,
                           [1792, 1793, 3584, 3585, 2000], num_q_heads=16,
                           num_kv_heads=2, head_size=128, block_size=B,
