@@ -122,6 +122,10 @@ constexpr int kLastShare = KVQ_ATTN_MMA_LAST_SHARE;
 static_assert(2 * kLastShare * KVQ_ATTN_MMA_PART / (kLastShare + 1) <=
                   4 * 64 * 16,
               "stretch too long for a warp's block ids");
+// The stretch length on contiguous pages with block_size 8.
+constexpr int kPartB8 = 1280;
+static_assert(2 * kLastShare * kPartB8 / (kLastShare + 1) <= 4 * 64 * 8,
+              "stretch too long for a warp's block ids");
 // One step's slots of one warp.  On contiguous pages the step's 32
 // tokens arrive in the pages' own order (whichever lane copies a chunk,
 // its bytes keep their place), as 16-byte copies:
@@ -368,21 +372,26 @@ constexpr uint32_t kOnes2 = 0x3C003C00u;  // f16x2 {1, 1}
 // inside fp16, and their rounding is still relative (2^-11).
 constexpr float kLazy = 8.0f;
 
-// kContig: HND pages with block_size % 16 == 0, so each 16 tokens of a
-// step lie in one block and their rows (and scale rows) are contiguous: one
-// block id and lane-constant offsets per 16 tokens.
+// kContig (kPages != 0): pages whose rows a warp copies as whole 8- or
+// 16-token pieces in the pages' own order, one block id and lane-constant
+// offsets per piece.
 // kPages: 0 = other pages; 1, 2 = contiguous (HND, a power-of-two
 // block_size >= 16); 3, 4 = token rows (NHD, the same block sizes: a
 // head's 64-byte data rows and 8-byte scale rows H rows apart, copied row
-// by row into the same shared-memory layout); 2 and 4 with block_size 16, where (warp ranges starting at
-// multiples of 32 tokens) half h of a warp's step i is its block 2i + h,
-// whole; 5 .. 8 = 1 .. 4 with the K scales swizzled like the V scales
-// (the same bytes copied, read as bands).
+// by row into the same shared-memory layout); 2 and 4 with block_size 16,
+// where (warp ranges starting at multiples of 32 tokens) half h of a
+// warp's step i is its block 2i + h, whole; 5 .. 8 = 1 .. 4 with the K
+// scales swizzled like the V scales (the same bytes copied, read as
+// bands); 9, 10 = 1, 3 with block_size 8 (linear K scales): 8-token piece
+// j of step i is block 4i + j, and a stretch is kPartB8 tokens long, so
+// that a warp's range spans at most 64 blocks.
 template <int NG, bool kF16, int kPages>
 __global__ void __launch_bounds__(kThreads, NG == 8 ? 4 : 3)
 paged_attention_mma_kernel(const AttnParams p) {
-  constexpr bool kSwzK = kPages >= 5;
-  constexpr int kForm = kSwzK ? kPages - 4 : kPages;
+  constexpr bool kB8 = kPages >= 9;
+  constexpr bool kSwzK = kPages >= 5 && !kB8;
+  constexpr int kForm = kB8 ? (kPages == 9 ? 1 : 3) : kSwzK ? kPages - 4
+                                                            : kPages;
   constexpr bool kContig = kForm != 0, kB16 = kForm == 2 || kForm == 4;
   constexpr bool kRows = kForm >= 3;
   constexpr int NB = NG / 8;  // n-blocks of 8 query heads
@@ -414,7 +423,7 @@ paged_attention_mma_kernel(const AttnParams p) {
       atomicOr(p.dev_error, KVQ_DEVERR_SEQ);
   };
   // stretch length: fixed on contiguous pages (the host sets p.part to it)
-  const int S = kContig ? KVQ_ATTN_MMA_PART : p.part;
+  const int S = kB8 ? kPartB8 : kContig ? KVQ_ATTN_MMA_PART : p.part;
   const int nparts = (L + S - 1) / S;
   if (part >= nparts) {
     if (early) asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -583,6 +592,58 @@ paged_attention_mma_kernel(const AttnParams p) {
     static_cast<void>(kValid);  // (only the contiguous forms test it)
     if (i >= nsteps) {
       // nothing to copy
+    } else if constexpr (kB8) {
+      // blocks of 8 tokens: piece 2h + u of step i (tokens 16h + 8u ..) is
+      // the warp's block 4i + 2h + u, whole, copied as on block_size 16
+      const uint32_t st = wbase + (i % kDepth) * SL::kStage;
+      const uint8_t* qz = reinterpret_cast<const uint8_t*>(p.q);
+      const uint8_t* sbp[4];
+      bool okp[4];
+#pragma unroll
+      for (int pc = 0; pc < 4; ++pc) {
+        const int e = 4 * i + pc;  // < 64, warp-uniform
+        const uint64_t kl =
+            reinterpret_cast<uint64_t>(e < 32 ? kb_lane : kb_hi);
+        const uint32_t lo =
+            __shfl_sync(0xFFFFFFFFu, static_cast<uint32_t>(kl), e & 31);
+        const uint32_t hi =
+            __shfl_sync(0xFFFFFFFFu, static_cast<uint32_t>(kl >> 32), e & 31);
+        const uint8_t* kb = reinterpret_cast<const uint8_t*>(
+            (static_cast<uint64_t>(hi) << 32) | lo);
+        okp[pc] = kValid || ((bmask64 >> e) & 1u) != 0u;
+        sbp[pc] = kb + sdelta;
+        const uint32_t kd = st + kKdOff + pc * 512 + lane * 16;
+        const uint32_t vd = st + kVdOff + pc * 512 + v_dst;
+        const uint8_t* ka = kb + lane_doff;
+        if (okp[pc]) {
+          cp_async<16>(kd, ka, true);
+          cp_async<16>(vd, ka + vdelta, true);
+        } else {
+          cp_async<16>(kd, qz, false);
+          cp_async<16>(vd, qz, false);
+        }
+      }
+      // the step's scales: lanes 16h .. 16h+15 take half h
+      const int sh = lane >> 4, li = lane & 15;
+      // the piece whose scales this lane copies
+      const int pc = 2 * sh + (kRows ? li >> 3 : (li >> 2) & 1);
+      const bool sok = pc == 0 ? okp[0] : pc == 1 ? okp[1]
+                       : pc == 2 ? okp[2] : okp[3];
+      const uint8_t* const sbs = pc == 0 ? sbp[0] : pc == 1 ? sbp[1]
+                                 : pc == 2 ? sbp[2] : sbp[3];
+      if constexpr (kRows) {
+        // the K row of token li and V row li of the half: row li % 8 of
+        // its block
+        const uint8_t* so = sbs + (li & 7) * sts;
+        const uint32_t sd = st + kKsOff + 256 * sh + 8 * li;
+        cp_async<8>(sd, sok ? so : qz, sok);
+        cp_async<8>(sd + 128, sok ? so + vdelta : qz, sok);
+      } else {
+        // lanes 0-3 / 4-7 the K scale rows of the half's two blocks, 8-11
+        // / 12-15 their V scale bands, 16 contiguous bytes each
+        const uint8_t* so = sbs + 16 * (li & 3) + ((li & 8) ? vdelta : 0);
+        cp_async<16>(st + kKsOff + lane * 16, sok ? so : qz, sok);
+      }
     } else if constexpr (kContig) {
       // whole 16-token halves: a block with a valid id is copied as it is
       // (tokens past the range are left out of the softmax and their V
@@ -745,7 +806,15 @@ paged_attention_mma_kernel(const AttnParams p) {
     // registers live at a time
     float sacc[2][NB][4];
     uint32_t kvalid = 0xFu;  // bit j: K token T0 + g + 8j is usable
-    if constexpr (kMasked && kContig) {
+    if constexpr (kMasked && kB8) {
+      // 8-token piece j of the step is the warp's block 4i + j
+      const uint32_t vb = static_cast<uint32_t>(bmask64 >> (4 * i)) & 0xFu;
+      const int rem = w1 - T0 - g;  // token T0 + g + 8j usable: 8j < rem
+      kvalid = (vb & 1u & static_cast<uint32_t>(rem > 0)) |
+               (((vb >> 1) & 1u & static_cast<uint32_t>(rem > 8)) << 1) |
+               (((vb >> 2) & 1u & static_cast<uint32_t>(rem > 16)) << 2) |
+               (((vb >> 3) & 1u & static_cast<uint32_t>(rem > 24)) << 3);
+    } else if constexpr (kMasked && kContig) {
       // each 16-token half lies in one block
       const int i0 = kB16 ? e0 + 2 * i : T0 >> p.b_shift;
       const int i1 = kB16 ? i0 + 1 : (T0 + 16) >> p.b_shift;
@@ -1182,7 +1251,7 @@ cudaError_t launch_mma(const AttnParams& caller, cudaStream_t stream) {
   // contiguous pages, 32 elsewhere.
   AttnParams p = caller;
   // (the caller's partitions are at most 512 tokens)
-  if (kContig) p.part = KVQ_ATTN_MMA_PART;
+  if (kContig) p.part = kPages >= 9 ? kPartB8 : KVQ_ATTN_MMA_PART;
   const int parts =
       static_cast<int>((static_cast<int64_t>(p.len_cap) + p.part - 1) / p.part);
   static bool configured[64] = {false};  // per instantiation and device
@@ -1223,6 +1292,14 @@ cudaError_t launch_form(const AttnParams& p, cudaStream_t stream) {
   if (rows)
     return p.B == 16 ? launch_mma<NG, kF16, 4 + kSwz>(p, stream)
                      : launch_mma<NG, kF16, 3 + kSwz>(p, stream);
+  // block_size 8 with linear K scales: two blocks per 16-token half
+  if (kSwz == 0 && p.B == 8 && p.dhs == 8 * (kD / 2) && p.dts == kD / 2 &&
+      p.shs == 8 * (kD / 16) && p.sts == kD / 16)
+    return launch_mma<NG, kF16, 9>(p, stream);
+  if (kSwz == 0 && p.B == 8 && p.dhs == kD / 2 &&
+      p.dts == p.Hkv * (kD / 2) && p.shs == kD / 16 &&
+      p.sts == p.Hkv * (kD / 16))
+    return launch_mma<NG, kF16, 10>(p, stream);
   return launch_mma<NG, kF16, 0>(p, stream);
 }
 

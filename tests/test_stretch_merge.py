@@ -125,15 +125,16 @@ def test_merge_matches_across_partition_sizes(orc):
 
 @pytest.mark.parametrize("swz", [0, 1])
 @pytest.mark.parametrize("layout", [W.LAYOUT_HND, W.LAYOUT_NHD])
-@pytest.mark.parametrize("B", [16, 32, 48])
+@pytest.mark.parametrize("B", [16, 32, 48, 8])
 def test_stretch_boundaries(orc, B, layout, swz):
     """Contexts at the stretch length (1792) and at twice it, one token
     either side: the first of two stretches then holds up to 2848 tokens,
     a warp range up to 46 blocks of 16 (the block ids of its second 32
     blocks come from each lane's second entry); HND pages and NHD ones
     (with 2 KV heads, so that a head's token rows are 2 rows apart), K
-    scales linear and swizzled; block size 48 takes the per-fragment path
-    with the caller's partitions."""
+    scales linear and swizzled; block size 8 (linear K scales) splits at
+    1280 tokens, and 48 (and 8 with swizzled K scales) takes the
+    per-fragment path with the caller's partitions."""
     wl = W.make_attention(f"edge{B}_{layout}_{swz}", 115,
                           [1792, 1793, 3584, 3585, 2000], num_q_heads=16,
                           num_kv_heads=2, head_size=128, block_size=B,
@@ -145,23 +146,26 @@ def test_stretch_boundaries(orc, B, layout, swz):
     c.check(orc, what=f"stretch edges B={B} layout={layout} swz={swz}")
 
 
+@pytest.mark.parametrize("B", [16, 8])
 @pytest.mark.parametrize("layout", [W.LAYOUT_HND, W.LAYOUT_NHD])
-def test_bad_blocks_in_long_ranges(orc, layout):
+def test_bad_blocks_in_long_ranges(orc, layout, B):
     """Out-of-range block ids among the second 32 blocks of a warp's range
-    (contexts of 3584 and 3000 tokens: warp ranges of 736 and 608 tokens,
-    46 and 38 blocks) and among the first 32 (2100 tokens): flagged, and
-    their 16 tokens left out, as the oracle gives with those blocks removed
-    from the table."""
-    B = 16
-    wl = W.make_attention("longbad", 116, [3584, 3000, 2100],
+    (block_size 16, contexts of 3584 and 3000 tokens: warp ranges of 736
+    and 608 tokens, 46 and 38 blocks; block_size 8, 3584 and 3000 tokens:
+    52 and 44 blocks) and among the first 32: flagged, and their tokens
+    left out, as the oracle gives with those blocks removed from the
+    table."""
+    wl = W.make_attention(f"longbad{B}", 116, [3584, 3000, 2100],
                           num_q_heads=8, num_kv_heads=1, head_size=128,
                           block_size=B)
     if layout == W.LAYOUT_NHD:
         wl = _nhd(wl)
-    drop = {0: 40, 1: 73, 2: 33}         # sequence -> block made bad
-    wl.block_table[0, 40] = -3
-    wl.block_table[1, 73] = wl.num_blocks
-    wl.block_table[2, 33] = wl.num_blocks + 100
+    # sequence -> block made bad (block_size 8: warp ranges of 52, 44 and
+    # 52 blocks in the first stretches)
+    drop = {0: 40, 1: 73, 2: 33} if B == 16 else {0: 40, 1: 33, 2: 5}
+    wl.block_table[0, drop[0]] = -3
+    wl.block_table[1, drop[1]] = wl.num_blocks
+    wl.block_table[2, drop[2]] = wl.num_blocks + 100
     c = Call(wl, 512, seed=9)
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     _, kc, vc = c.caches
