@@ -408,10 +408,11 @@ paged_attention_mma_kernel(const AttnParams p) {
   // that it writes none of the query, block table, context lengths and
   // scales (KVQ_F_PDL_EARLY_META) -- only before the first read of the
   // pages and the first write, so that the lengths, block ids and query
-  // load while it finishes
+  // load while it finishes.  The next kernel may launch only after the
+  // wait, as everywhere here: a kernel two launches back has then always
+  // finished when another early read starts.
   const bool early = p.early_meta;
-  if (!early) asm volatile("griddepcontrol.wait;" ::: "memory");
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  if (!early) pdl_prologue();
 
   int L = __ldg(p.lens + b);
   const bool bad_len = L < 0 || L > p.len_cap;
@@ -426,7 +427,7 @@ paged_attention_mma_kernel(const AttnParams p) {
   const int S = kB8 ? kPartB8 : kContig ? KVQ_ATTN_MMA_PART : p.part;
   const int nparts = (L + S - 1) / S;
   if (part >= nparts) {
-    if (early) asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (early) pdl_prologue();
     flag_len();
     if (part == 0) {  // empty context: the output is zero
       for (int i = tid; i < p.G * kD; i += kThreads)
@@ -505,7 +506,7 @@ paged_attention_mma_kernel(const AttnParams p) {
           8 * warp));
   }
   const float v_scale_in = tid == 0 ? __ldg(p.v_scale) : 0.f;
-  if (early) asm volatile("griddepcontrol.wait;" ::: "memory");
+  if (early) pdl_prologue();
   flag_len();
 
   const uint32_t wbase = smem_u32(smem) + warp * SL::kWarp;
