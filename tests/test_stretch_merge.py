@@ -210,3 +210,24 @@ def test_early_metadata_back_to_back(orc):
     c.check(orc, what="early metadata")
     for o in outs:
         assert np.array_equal(o, plain)
+
+
+@pytest.mark.parametrize("dtype", [W.DTYPE_BF16, W.DTYPE_F16])
+@pytest.mark.parametrize("G", [8, 16, 3])
+@pytest.mark.parametrize("layout", [W.LAYOUT_HND, W.LAYOUT_NHD])
+def test_block_size_8_forms(orc, layout, G, dtype):
+    """Block size 8 on HND and NHD pages with 3, 8 and 16 query heads per
+    KV head and both query types, contexts from one token to several
+    1280-token stretches (ragged last steps and pieces)."""
+    wl = W.make_attention(f"b8_{layout}_{G}_{dtype}", 118,
+                          [1, 7, 8, 9, 33, 300, 1281, 2600, 4001],
+                          num_q_heads=2 * G, num_kv_heads=2, head_size=128,
+                          block_size=8, dtype=dtype)
+    if layout == W.LAYOUT_NHD:
+        wl = _nhd(wl)
+    tdt = torch.float16 if dtype == W.DTYPE_F16 else torch.bfloat16
+    c = Call(wl, 512, seed=G)
+    c.q = torch.from_numpy(wl.query.view(np.int16)).cuda().view(tdt)
+    c.out = torch.full(c.q.shape, float("nan"), dtype=tdt, device="cuda")
+    c()
+    c.check(orc, what=f"block_size 8 layout={layout} G={G} dtype={dtype}")
