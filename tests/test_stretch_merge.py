@@ -218,9 +218,11 @@ def test_early_metadata_back_to_back(orc):
 def test_block_size_8_forms(orc, layout, G, dtype):
     """Block size 8 on HND and NHD pages with 3, 8 and 16 query heads per
     KV head and both query types, contexts from one token to several
-    1280-token stretches (ragged last steps and pieces)."""
+    1280-token stretches, at the stretch length and twice it (ragged last
+    steps and pieces)."""
     wl = W.make_attention(f"b8_{layout}_{G}_{dtype}", 118,
-                          [1, 7, 8, 9, 33, 300, 1281, 2600, 4001],
+                          [1, 7, 8, 9, 33, 300, 1280, 1281, 2560, 2561,
+                           4001],
                           num_q_heads=2 * G, num_kv_heads=2, head_size=128,
                           block_size=8, dtype=dtype)
     if layout == W.LAYOUT_NHD:
