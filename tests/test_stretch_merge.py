@@ -46,6 +46,8 @@ class Call:
             wl.head_size, torch.device("cuda"))
         g = torch.Generator(device="cuda").manual_seed(seed)
         for t in self.scratch:
+            if t is None:  # every context within one partition: no scratch
+                continue
             t.view(torch.int32).copy_(torch.randint(
                 -2 ** 31, 2 ** 31 - 1, t.shape, dtype=torch.int32,
                 device="cuda", generator=g))
@@ -233,3 +235,45 @@ def test_block_size_8_forms(orc, layout, G, dtype):
     c.out = torch.full(c.q.shape, float("nan"), dtype=tdt, device="cuda")
     c()
     c.check(orc, what=f"block_size 8 layout={layout} G={G} dtype={dtype}")
+
+
+def _form_cases(n=20, seed=4049):
+    """Seeded mixes aimed at the contiguous-page forms: block sizes 8 and
+    powers of two from 16 to 128, HND and NHD pages, linear and swizzled K
+    scales, 1 to 16 query heads per KV head, both query types, partition
+    sizes 128 to 512, and contexts drawn around the block size, the step,
+    the stretch lengths (1280 for block size 8, 1792 otherwise) and twice
+    them."""
+    rng = np.random.default_rng(seed)
+    cases = []
+    for k in range(n):
+        B = int(rng.choice([8, 16, 32, 64, 128]))
+        S = 1280 if B == 8 else 1792
+        G = int(rng.choice([1, 2, 4, 6, 8, 12, 16]))
+        anchors = [B, 32, S, 2 * S, 3 * S]
+        lens = [max(0, int(rng.choice(anchors)) + int(rng.integers(-3, 4)))
+                for _ in range(int(rng.integers(2, 5)))]
+        lens.append(int(rng.integers(0, 40)))
+        cases.append(dict(name=f"form{k}", B=B, G=G, lens=lens,
+                          layout=int(rng.integers(0, 2)),
+                          swz=int(rng.integers(0, 2)),
+                          dtype=int(rng.integers(0, 2)),
+                          part=int(rng.choice([128, 256, 384, 512]))))
+    return cases
+
+
+@pytest.mark.parametrize("c", _form_cases(), ids=lambda c: c["name"])
+def test_random_form_sweep(orc, c):
+    wl = W.make_attention(c["name"], 500 + int(c["name"][4:]), c["lens"],
+                          num_q_heads=c["G"] * 2, num_kv_heads=2,
+                          head_size=128, block_size=c["B"],
+                          flags=c["swz"], dtype=c["dtype"])
+    if c["layout"] == W.LAYOUT_NHD:
+        wl = _nhd(wl)
+    tdt = torch.float16 if c["dtype"] == W.DTYPE_F16 else torch.bfloat16
+    call = Call(wl, c["part"], seed=7 + int(c["name"][4:]))
+    call.q = torch.from_numpy(wl.query.view(np.int16)).cuda().view(tdt)
+    call.out = torch.full(call.q.shape, float("nan"), dtype=tdt,
+                          device="cuda")
+    call()
+    call.check(orc, what=str(c))
